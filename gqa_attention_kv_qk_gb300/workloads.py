@@ -1,0 +1,194 @@
+"""Named decode workloads and their seeded synthetic inputs.
+
+This module holds no arithmetic of the method: it names the workloads (shapes,
+dtypes, rotary and masking parameters as plain data) and draws seeded random
+tensors for them. Both the CUDA path's tests and benchmark and the oracle's
+tests take their inputs from here, so the two sides see identical data; each
+side then does its own arithmetic (quantising a vq8 cache included).
+
+Draws are ~N(0, 1) in fp32 from torch's CPU generator, then cast to bf16
+(round to nearest even) where the workload's dtype is bf16. Every tensor, and
+every (sequence, kv head) slice of a cache, has its own generator seeded from
+(workload seed, tensor tag, slice index), so slices can be drawn on their own
+and the result never depends on the order of the draws.
+"""
+from __future__ import annotations
+
+import copy
+
+import numpy as np
+import torch
+
+TILE = 64  # cache capacities are rounded up to a multiple of this many slots
+
+# The five workloads. Method keys follow the oracle / library vocabulary;
+# workload keys: batch, seq_len (int, or (lo, hi) inclusive for ragged lengths),
+# steps, seed, layers (per-layer overrides; one cache per layer).
+CONFIGS: dict[str, dict] = {
+    # Tiny Llama-3.2-1B-like step: fp32 everything, seed 0.
+    "llama32_1b_tiny": dict(
+        batch=1, n_q_heads=32, n_kv_heads=8, head_dim=64, seq_len=256, steps=1, seed=0,
+        kv_dtype="f32", io_dtype="f32", out_dtype="f32",
+        rope_style="interleaved", rope_theta=500000.0, rope_scaling="llama3", factor=32.0,
+        low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
+    # Llama-3.1-8B-like decode: 16 sequences at 8192 cached tokens, 64 steps.
+    "llama31_8b_decode": dict(
+        batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, seq_len=8192, steps=64, seed=1,
+        kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
+        low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
+    # Qwen3-8B-like ragged decode: lengths uniform in [1024, 32768], QK RMSNorm.
+    "qwen3_8b_ragged": dict(
+        batch=32, n_q_heads=32, n_kv_heads=8, head_dim=128, seq_len=(1024, 32768), steps=1,
+        seed=2, kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=1000000.0, rope_scaling="none",
+        qk_norm=True, norm_eps=1e-6, norm_w_range=(0.5, 1.5)),
+    # Gemma-2-9B-like decode: two layers per step (4096-token window, then global),
+    # softcap 50, scale 1/sqrt(256).
+    "gemma2_9b_swa": dict(
+        batch=8, n_q_heads=16, n_kv_heads=8, head_dim=256, seq_len=16384, steps=1, seed=3,
+        kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=10000.0, rope_scaling="none",
+        softcap=50.0, scale=1.0 / 16.0, layers=[dict(window=4096), dict(window=0)]),
+    # gpt-oss-like decode: vq8 cache, per-head sink logits, YaRN factor 32.
+    "gptoss_vq8_sink": dict(
+        batch=64, n_q_heads=64, n_kv_heads=8, head_dim=64, seq_len=4096, steps=1, seed=4,
+        kv_dtype="vq8", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=150000.0, rope_scaling="yarn", factor=32.0,
+        original_max_pos=4096, beta_fast=32.0, beta_slow=1.0, has_sink=True),
+}
+
+_TAGS = {"q": 1, "k_new": 2, "v_new": 3, "k_cache": 4, "v_cache": 5, "q_norm_w": 6,
+         "k_norm_w": 7, "sink": 8, "seq_lens": 9}
+
+
+def config(name: str, **overrides) -> dict:
+    """A copy of a named workload with keys overridden (for smaller test cases)."""
+    cfg = copy.deepcopy(CONFIGS[name])
+    cfg.update(overrides)
+    cfg["name"] = name
+    return cfg
+
+
+def layer_configs(cfg: dict) -> list[dict]:
+    """One config per layer (a workload without 'layers' has one layer)."""
+    layers = cfg.get("layers") or [{}]
+    out = []
+    for i, over in enumerate(layers):
+        c = copy.deepcopy(cfg)
+        c.pop("layers", None)
+        c.update(over)
+        c["layer"] = i
+        out.append(c)
+    return out
+
+
+def _gen(seed: int, tag: str, idx: int = 0, layer: int = 0) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed((seed * 1_000_003 + _TAGS[tag] * 10_007 + layer * 101 + idx) % (2**62))
+    return g
+
+
+def _cast(x: torch.Tensor, dtype: str) -> torch.Tensor:
+    if dtype == "f32":
+        return x
+    if dtype in ("bf16", "vq8"):
+        return x.to(torch.bfloat16)
+    raise ValueError(dtype)
+
+
+def capacity(cfg: dict, extra: int = 0) -> int:
+    """Slots per (sequence, kv head): the longest cached length + extra, rounded up."""
+    sl = cfg["seq_len"]
+    longest = sl[1] if isinstance(sl, (tuple, list)) else sl
+    need = longest + max(extra, 1)
+    return (need + TILE - 1) // TILE * TILE
+
+
+def seq_lens(cfg: dict) -> torch.Tensor:
+    """Cached tokens per sequence before the first step (int32 [B])."""
+    B = cfg["batch"]
+    sl = cfg["seq_len"]
+    if isinstance(sl, (tuple, list)):
+        return torch.randint(int(sl[0]), int(sl[1]) + 1, (B,), generator=_gen(cfg["seed"], "seq_lens"),
+                             dtype=torch.int64).to(torch.int32)
+    return torch.full((B,), int(sl), dtype=torch.int32)
+
+
+def step_inputs(cfg: dict, step: int = 0) -> dict:
+    """q [B][Hq][D], k_new and v_new [B][Hkv][D] in the io dtype, fresh for each step."""
+    B, Hq, Hkv, D = cfg["batch"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    layer = cfg.get("layer", 0)
+    io = cfg.get("io_dtype", "bf16")
+    out = {}
+    for tag, shape in (("q", (B, Hq, D)), ("k_new", (B, Hkv, D)), ("v_new", (B, Hkv, D))):
+        x = torch.randn(shape, generator=_gen(cfg["seed"], tag, step, layer), dtype=torch.float32)
+        out[tag] = _cast(x, io)
+    return out
+
+
+def norm_weights(cfg: dict) -> dict:
+    """QK RMSNorm weights [D] fp32, ~U(lo, hi); None when the workload has no norm."""
+    if not cfg.get("qk_norm"):
+        return {"q_norm_w": None, "k_norm_w": None}
+    lo, hi = cfg.get("norm_w_range", (1.0, 1.0))
+    D = cfg["head_dim"]
+    layer = cfg.get("layer", 0)
+    out = {}
+    for tag in ("q_norm_w", "k_norm_w"):
+        u = torch.rand((D,), generator=_gen(cfg["seed"], tag, 0, layer), dtype=torch.float32)
+        out[tag] = (lo + (hi - lo) * u).to(torch.float32)
+    return out
+
+
+def sinks(cfg: dict):
+    """Per-query-head sink logits [Hq] fp32 ~N(0, 1); None without sinks."""
+    if not cfg.get("has_sink"):
+        return None
+    return torch.randn((cfg["n_q_heads"],), generator=_gen(cfg["seed"], "sink", 0, cfg.get("layer", 0)),
+                       dtype=torch.float32)
+
+
+def cache_slice(cfg: dict, b: int, g: int, n: int, which: str) -> torch.Tensor:
+    """Rows [0, n) of cache slice (b, g): k in the key storage dtype (f32 / bf16);
+    v in f32 / bf16, or as fp32 values for a vq8 cache (each side quantises them)."""
+    D, Hkv = cfg["head_dim"], cfg["n_kv_heads"]
+    idx = b * Hkv + g
+    x = torch.randn((n, D), generator=_gen(cfg["seed"], which, idx, cfg.get("layer", 0)),
+                    dtype=torch.float32)
+    kv = cfg.get("kv_dtype", "bf16")
+    if kv == "f32":
+        return x
+    if which == "k_cache" or kv == "bf16":
+        return x.to(torch.bfloat16)
+    return x  # vq8 values, fp32
+
+
+def cache(cfg: dict, cap: int, lens: torch.Tensor, fill_unused: str = "zero") -> dict:
+    """Host caches [B][Hkv][cap][D] with rows [0, lens[b]) drawn; unused rows are
+    zero or NaN (fill_unused='nan', to prove they are never read into a result).
+    For vq8 'v_values' holds fp32 values; each side quantises them itself."""
+    B, Hkv, D = cfg["batch"], cfg["n_kv_heads"], cfg["head_dim"]
+    kv = cfg.get("kv_dtype", "bf16")
+    kdt = torch.float32 if kv == "f32" else torch.bfloat16
+    vdt = torch.float32 if kv in ("f32", "vq8") else torch.bfloat16
+    fill = float("nan") if fill_unused == "nan" else 0.0
+    k = torch.full((B, Hkv, cap, D), fill, dtype=kdt)
+    v = torch.full((B, Hkv, cap, D), fill, dtype=vdt)
+    for b in range(B):
+        n = int(lens[b])
+        for g in range(Hkv):
+            k[b, g, :n] = cache_slice(cfg, b, g, n, "k_cache")
+            v[b, g, :n] = cache_slice(cfg, b, g, n, "v_cache")
+    key = "v_values" if kv == "vq8" else "v_cache"
+    return {"k_cache": k, key: v}
+
+
+# ---------------------------------------------------------------- numpy views
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """A CPU tensor as the numpy array the oracle takes (bf16 -> uint16 bit patterns)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()

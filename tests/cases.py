@@ -1,0 +1,49 @@
+"""Test cases built from the seeded workload generators.
+
+`host_case` draws one step's inputs and a cache; `oracle_arrays` turns them into
+the storage arrays the oracle takes (a vq8 cache quantised by the oracle's own
+quantiser). Nothing here computes any part of the method.
+"""
+import numpy as np
+import torch
+
+from gqa_attention_kv_qk_gb300 import workloads as W
+
+
+def host_case(cfg: dict, lens=None, cap=None, step: int = 0, fill_unused: str = "zero") -> dict:
+    lens = W.seq_lens(cfg) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
+    cap = cap or W.capacity(cfg, extra=cfg.get("steps", 1))
+    case = dict(cfg=cfg, lens=lens.clone(), cap=cap)
+    case.update(W.cache(cfg, cap, lens, fill_unused=fill_unused))
+    case.update(W.step_inputs(cfg, step))
+    case.update(W.norm_weights(cfg))
+    case["sink"] = W.sinks(cfg)
+    return case
+
+
+def oracle_arrays(case: dict, oracle_mod) -> dict:
+    """Storage arrays for the oracle (copies: the oracle's append mutates them)."""
+    cfg = case["cfg"]
+    a = dict(
+        q=W.bits(case["q"]).copy(), k_new=W.bits(case["k_new"]).copy(),
+        v_new=W.bits(case["v_new"]).copy(),
+        k_cache=W.bits(case["k_cache"]).copy(),
+        seq_lens=case["lens"].numpy().astype(np.int32).copy(),
+        q_norm_w=None if case["q_norm_w"] is None else case["q_norm_w"].numpy().copy(),
+        k_norm_w=None if case["k_norm_w"] is None else case["k_norm_w"].numpy().copy(),
+        sink=None if case["sink"] is None else case["sink"].numpy().copy(),
+    )
+    if cfg.get("kv_dtype") == "vq8":
+        codes, scales = oracle_mod.vq8_quantize(case["v_values"].numpy())
+        a["v_cache"], a["v_scale"] = codes, scales
+    else:
+        a["v_cache"], a["v_scale"] = W.bits(case["v_cache"]).copy(), None
+    return a
+
+
+def run_oracle_step(case: dict, oracle_mod, n_threads=None):
+    a = oracle_arrays(case, oracle_mod)
+    out = oracle_mod.decode_step(case["cfg"], a["q"], a["k_new"], a["v_new"], a["q_norm_w"],
+                                 a["k_norm_w"], a["sink"], a["k_cache"], a["v_cache"],
+                                 a["v_scale"], a["seq_lens"], n_threads=n_threads)
+    return out, a
