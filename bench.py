@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA decode step on GB300: decode-attention HBM GB/s and decode
+steps/sec at 1 GPU (N replicas under torchrun).
+
+Workload (default): the Llama-3.1-8B-like decode, 16 sequences at 8192 cached
+tokens, 32 q / 8 kv heads, head_dim 128, bf16 cache, NeoX RoPE with llama3
+factor 8. One benchmark step = 64 consecutive decode steps from 8192 cached
+tokens (each: RoPE/append, split-K partials, combine), after which the lengths
+return to 8192 (a 64-byte device copy) so every step times the same work. The
+64 decode steps are captured once in a CUDA graph and replayed. The KV cache
+(~545 MB) is larger than L2 (129 MB), so no flush is needed between steps.
+
+value       = algorithmic bytes of all timed steps / device time (CUDA events)
+e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each with
+              the step's q/k/v copied from pinned host memory and out copied back
+roofline    = the split-K partial kernel alone: its algorithmic bytes (visible KV
+              rows) / its mean launch duration, against the measured HBM copy peak
+cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_attention_kv_qk_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attention HBM GB/s (% of GB300 peak) and decode steps/sec at 1 GPU"
+DECODES_PER_STEP = {"llama31_8b_decode": 64}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def _kv_row_bytes(cfg: dict) -> tuple[int, int]:
+    D = cfg["head_dim"]
+    kv = cfg.get("kv_dtype", "bf16")
+    if kv == "f32":
+        return 4 * D, 4 * D
+    if kv == "bf16":
+        return 2 * D, 2 * D
+    return 2 * D, D + 4  # vq8: bf16 key row; int8 value row + fp32 scale
+
+
+def visible(n: int, window: int) -> int:
+    return min(n, window) if window else n
+
+
+def partial_bytes(cfg: dict, lens_after: list[int]) -> int:
+    """Visible K and V rows the split-K partial must read (one read per kv head)."""
+    kb, vb = _kv_row_bytes(cfg)
+    w = cfg.get("window", 0) or 0
+    return sum(visible(n, w) for n in lens_after) * cfg["n_kv_heads"] * (kb + vb)
+
+
+def decode_step_bytes(cfg: dict, lens_before: list[int]) -> int:
+    """One decode step: the partial's KV reads plus the q/k/v reads, the appended
+    rows and the output."""
+    B, Hq, Hkv, D = cfg["batch"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    io = 4 if cfg.get("io_dtype") == "f32" else 2
+    ob = 4 if cfg.get("out_dtype", "f32") == "f32" else 2
+    kb, vb = _kv_row_bytes(cfg)
+    small = B * (Hq + 2 * Hkv) * D * io + B * Hkv * (kb + vb) + B * Hq * D * ob
+    return partial_bytes(cfg, [n + 1 for n in lens_before]) + small
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines: list[str] = []
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        ident = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.cmd = [exe, "-i", ident, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                    "-lms", "50"]
+
+    def __enter__(self):
+        if hasattr(self, "cmd"):
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_sample(cfg: dict, case: dict, budget_s: float, n_threads: int) -> dict:
+    """Time the fp64 CPU oracle on whole decode steps of a prefix of the batch
+    (all heads of each sequence), growing the prefix up to the time budget.
+    Returns bytes processed, seconds, and a description of the sample."""
+    from oracle import oracle as O
+    from tests.cases import oracle_arrays  # the same storage arrays the parity tests use
+
+    a = oracle_arrays(case, O)
+    B = cfg["batch"]
+    lens0 = a["seq_lens"].copy()
+
+    def run(nb: int) -> float:
+        sl = lens0[:nb].copy()
+        t = time.perf_counter()
+        O.decode_step(cfg, a["q"][:nb].copy(), a["k_new"][:nb].copy(), a["v_new"][:nb].copy(), a["q_norm_w"],
+                      a["k_norm_w"], a["sink"], a["k_cache"][:nb], a["v_cache"][:nb],
+                      None if a["v_scale"] is None else a["v_scale"][:nb], sl, n_threads=n_threads)
+        return time.perf_counter() - t
+
+    t1 = run(1)
+    nb = int(max(1, min(B, budget_s / max(t1, 1e-6))))
+    secs = run(nb) if nb > 1 else t1
+    lens = [int(x) for x in lens0[:nb]]
+    sub = dict(cfg, batch=nb)
+    return {"bytes": decode_step_bytes(sub, lens), "seconds": secs,
+            "sample": f"one decode step of {nb} of {B} sequences (all {cfg['n_q_heads']} q heads), "
+                      f"{n_threads} threads"}
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+def build_layers(cfg: dict, cap_extra: int, device: str):
+    from tests.cases import gpu_layer, host_case
+    layers, cases = [], []
+    for lc in W.layer_configs(cfg):
+        case = host_case(lc, cap=W.capacity(lc, extra=cap_extra))
+        layers.append(gpu_layer(case, device))
+        cases.append(case)
+    return layers, cases
+
+
+def run_uaa(args, world, rank, local) -> dict | None:
+    from gqa_attention_kv_qk_gb300 import binding as Bd
+    from gqa_attention_kv_qk_gb300 import build as ext
+    ext.build()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    name = args.workload
+    cfg = W.config(name, seed=W.CONFIGS[name]["seed"] + 1000 * rank)
+    n_dec = DECODES_PER_STEP.get(name, 1)
+    layers, cases = build_layers(cfg, cap_extra=n_dec + 1, device=device)
+    lens0 = [case["lens"].clone() for case in cases]
+    lens0_dev = [l.to(device) for l in lens0]
+    hint = [int(l.max()) + n_dec - 1 for l in lens0]
+    stream = torch.cuda.Stream(device)
+    inputs = [{k: case[k].to(device) for k in ("q", "k_new", "v_new")} for case in cases]
+
+    def reset():
+        for layer, l0 in zip(layers, lens0_dev):
+            layer.seq_lens.copy_(l0, non_blocking=True)
+
+    def one_step():  # one benchmark step: n_dec decode steps of every layer, then lengths reset
+        for _ in range(n_dec):
+            for li, layer in enumerate(layers):
+                inp = inputs[li]
+                layer.step(inp["q"], inp["k_new"], inp["v_new"], stream=stream, max_seq_len=hint[li])
+        reset()
+
+    # bytes of one benchmark step (lengths grow by one per decode step)
+    step_bytes = 0
+    part_bytes = 0
+    for lc, l0 in zip(W.layer_configs(cfg), lens0):
+        base = [int(x) for x in l0]
+        for t in range(n_dec):
+            cur = [x + t for x in base]
+            step_bytes += decode_step_bytes(lc, cur)
+            part_bytes += partial_bytes(lc, [x + 1 for x in cur])
+    launches_per_step = 3 * n_dec * len(layers)
+
+    with torch.cuda.stream(stream):
+        # warm-up, then capture one benchmark step in a graph
+        for _ in range(max(1, args.warmup)):
+            one_step()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            one_step()
+        for _ in range(args.warmup):
+            graph.replay()
+        stream.synchronize()
+
+        # ---- timed region: exactly K benchmark steps
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clocks:
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        dev_s = ev0.elapsed_time(ev1) / 1e3
+        for layer in layers:
+            st = layer.device_status(stream)
+            if st:
+                raise RuntimeError(f"device flags 0x{st:x} after the timed region")
+
+        # ---- the partial kernel alone (events on the launching stream)
+        pe = []
+        reset()
+        for _ in range(n_dec):
+            for li, layer in enumerate(layers):
+                inp = inputs[li]
+                args_ = layer.args(inp["q"], inp["k_new"], inp["v_new"], max_seq_len=hint[li])
+                Bd.uaa_rope_qk_norm_append(layer.desc, args_, layer.ws, stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                Bd.uaa_decode_attn_partial(layer.desc, args_, layer.ws, stream)
+                e1.record(stream)
+                Bd.uaa_decode_attn_combine(layer.desc, args_, layer.ws, stream)
+                pe.append((e0, e1))
+        stream.synchronize()
+        part_s = sum(a.elapsed_time(b) for a, b in pe) / 1e3
+        n_part = len(pe)
+        reset()
+        stream.synchronize()
+
+        # ---- end to end through the public call, host buffers
+        host_in = [{k: v.cpu().pin_memory() for k, v in case_in.items()} for case_in in
+                   [{k: case[k] for k in ("q", "k_new", "v_new")} for case in cases]]
+        host_out = [torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory() for layer in layers]
+        h2d = sum(t.numel() * t.element_size() for hi in host_in for t in hi.values()) * n_dec
+        d2h = sum(t.numel() * t.element_size() for t in host_out) * n_dec
+        dev_in = [{k: torch.empty_like(v, device=device) for k, v in hi.items()} for hi in host_in]
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            for li in range(len(layers)):
+                layers[li].set_lengths(lens0[li])
+            for _ in range(n_dec):
+                for li, layer in enumerate(layers):
+                    for k in ("q", "k_new", "v_new"):
+                        dev_in[li][k].copy_(host_in[li][k], non_blocking=True)
+                    out = layer.step(dev_in[li]["q"], dev_in[li]["k_new"], dev_in[li]["v_new"], stream=stream,
+                                     max_seq_len=hint[li])
+                    host_out[li].copy_(out, non_blocking=True)
+            stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+        barrier(world)
+
+    dev_s = max_over_ranks(dev_s, world)
+    e2e_s = max_over_ranks(e2e_s, world)
+    total_bytes = sum_over_ranks(step_bytes * args.steps, world)
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    value = total_bytes / dev_s / 1e9
+    part_gbs = (part_bytes / n_part) / (part_s / n_part) / 1e9 if n_part else None
+    clk = clocks.summary()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_thr = len(os.sched_getaffinity(0))
+        smp = oracle_sample(W.layer_configs(cfg)[0], cases[0], args.cpu_budget, n_thr)
+        cpu = {"value": smp["bytes"] / smp["seconds"] / 1e9, "unit": "GB/s", "cores": n_thr, "kind": "oracle",
+               "sample": smp["sample"]}
+    decodes = n_dec * args.steps * world
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["kv_dtype"] != "f32" else "f32",
+        "data": "synthetic (seeded N(0,1) cache and inputs)",
+        "decode_steps_per_s": round(decodes / dev_s / world, 2),
+        "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "config": {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"], "n_q_heads": cfg["n_q_heads"],
+                   "n_kv_heads": cfg["n_kv_heads"], "head_dim": cfg["head_dim"], "kv_dtype": cfg["kv_dtype"],
+                   "decode_steps_per_step": n_dec, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (KV cache %.0f MB)" % (part_bytes / n_dec / 1e6),
+                   "timing": "CUDA graph of one benchmark step, replayed K times; CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": round(part_gbs, 2) if part_gbs else None,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(part_gbs / peaks["hbm_gbs"], 4) if part_gbs else None,
+                     "traffic": None, "kernel": "split-K partial", "peak_source": peaks["source"],
+                     "bytes_per_launch": part_bytes // max(1, n_dec * len(layers)),
+                     "mean_launch_us": round(part_s / n_part * 1e6, 2) if n_part else None},
+        "e2e": {"value": round(total_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+
+
+def run_reference(args, world, rank) -> dict | None:
+    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    from tests.cases import host_case
+    name = args.workload
+    cfg = W.config(name)
+    lc = W.layer_configs(cfg)[0]
+    case = host_case(lc, cap=W.capacity(lc, extra=2))
+    n_thr = len(os.sched_getaffinity(0))
+    budget = max(0.5, args.cpu_budget / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(lc, case, budget / 4, n_thr)
+    tot_b = tot_s = 0.0
+    sample = ""
+    for _ in range(args.steps):
+        smp = oracle_sample(lc, case, budget, n_thr)
+        tot_b += smp["bytes"]
+        tot_s += smp["seconds"]
+        sample = smp["sample"]
+    v = tot_b / tot_s / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) cache and inputs)",
+            "config": {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"]},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": n_thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["uaa", "reference"], default="uaa")
+    ap.add_argument("--workload", default="llama31_8b_decode", choices=list(W.CONFIGS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "uaa":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup(args.gpus)
+    res = run_reference(args, world, rank) if args.impl == "reference" else run_uaa(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,546 @@
+// api.cu -- the C ABI of libuaa: descriptor validation (typed refusals that name
+// the fact, the Model support matrix page's "Conformance CLI" convention), the
+// split geometry, workspace layout, TMA descriptors and the kernel launches.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+uaa_status fail(uaa_status st, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+uaa_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(UAA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define UAA_TRY(expr)                          \
+    do {                                       \
+        const uaa_status st_ = (expr);         \
+        if (st_ != UAA_OK) return st_;         \
+    } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// ---------------------------------------------------------------- descriptor checks
+
+uaa_status check_desc(const uaa_attn_desc* d)
+{
+    if (!d) return fail(UAA_ERR_INVALID_ARGUMENT, "desc is NULL");
+    if (d->n_kv_heads <= 0) return fail(UAA_ERR_UNSUPPORTED, "n_kv_heads=%d is not positive", d->n_kv_heads);
+    if (d->n_q_heads <= 0 || d->n_q_heads % d->n_kv_heads != 0)
+        return fail(UAA_ERR_UNSUPPORTED,
+                    "n_q_heads=%d is not a positive multiple of n_kv_heads=%d (integral GQA ratio required)",
+                    d->n_q_heads, d->n_kv_heads);
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+        return fail(UAA_ERR_UNSUPPORTED, "head_dim=%d is not supported (supported: {64, 128, 256})",
+                    d->head_dim);
+    if (!(d->scale >= 0.f) || !isfinite(d->scale))
+        return fail(UAA_ERR_UNSUPPORTED, "scale=%g is not a finite value >= 0", (double)d->scale);
+    const uaa_rope_params& r = d->rope;
+    if (r.style != UAA_ROPE_NEOX && r.style != UAA_ROPE_INTERLEAVED)
+        return fail(UAA_ERR_UNSUPPORTED, "rope.style=%d is not NEOX (0) or INTERLEAVED (1)", r.style);
+    if (!(r.theta > 0.0) || !isfinite(r.theta))
+        return fail(UAA_ERR_UNSUPPORTED, "rope.theta=%g is not a finite value > 0", r.theta);
+    if (r.scaling == UAA_ROPE_SCALING_LLAMA3) {
+        if (!(r.factor >= 1.0) || !(r.low_freq_factor > 0.0) || !(r.high_freq_factor > r.low_freq_factor) ||
+            r.original_max_pos <= 0)
+            return fail(UAA_ERR_UNSUPPORTED,
+                        "llama3 rope scaling needs factor>=1, 0<low_freq_factor<high_freq_factor, "
+                        "original_max_pos>0 (got %g, %g, %g, %d)",
+                        r.factor, r.low_freq_factor, r.high_freq_factor, r.original_max_pos);
+    } else if (r.scaling == UAA_ROPE_SCALING_YARN) {
+        if (!(r.factor > 0.0) || r.original_max_pos <= 0 || !(r.beta_slow > 0.0) || !(r.beta_fast > r.beta_slow))
+            return fail(UAA_ERR_UNSUPPORTED,
+                        "yarn rope scaling needs factor>0, original_max_pos>0, beta_fast>beta_slow>0 "
+                        "(got %g, %d, %g, %g)",
+                        r.factor, r.original_max_pos, r.beta_fast, r.beta_slow);
+    } else if (r.scaling != UAA_ROPE_SCALING_NONE) {
+        return fail(UAA_ERR_UNSUPPORTED, "rope.scaling=%d is not supported (none, llama3, yarn)", r.scaling);
+    }
+    if (d->qk_norm != 0 && d->qk_norm != 1)
+        return fail(UAA_ERR_UNSUPPORTED, "qk_norm=%d is not 0 or 1", d->qk_norm);
+    if (d->qk_norm && (!(d->norm_eps >= 0.f) || !isfinite(d->norm_eps)))
+        return fail(UAA_ERR_UNSUPPORTED, "norm_eps=%g is not a finite value >= 0", (double)d->norm_eps);
+    if (d->window < 0) return fail(UAA_ERR_UNSUPPORTED, "window=%d is negative", d->window);
+    if (!(d->softcap >= 0.f) || !isfinite(d->softcap))
+        return fail(UAA_ERR_UNSUPPORTED, "softcap=%g is not a finite value >= 0", (double)d->softcap);
+    if (d->has_sink != 0 && d->has_sink != 1)
+        return fail(UAA_ERR_UNSUPPORTED, "has_sink=%d is not 0 or 1", d->has_sink);
+    if (d->kv_dtype != UAA_DTYPE_F32 && d->kv_dtype != UAA_DTYPE_BF16 && d->kv_dtype != UAA_DTYPE_VQ8)
+        return fail(UAA_ERR_UNSUPPORTED, "kv_dtype=%d is not F32, BF16 or VQ8", d->kv_dtype);
+    if (d->io_dtype != UAA_DTYPE_F32 && d->io_dtype != UAA_DTYPE_BF16)
+        return fail(UAA_ERR_UNSUPPORTED, "io_dtype=%d is not F32 or BF16", d->io_dtype);
+    if (d->out_dtype != UAA_DTYPE_F32 && d->out_dtype != UAA_DTYPE_BF16)
+        return fail(UAA_ERR_UNSUPPORTED, "out_dtype=%d is not F32 or BF16", d->out_dtype);
+    return UAA_OK;
+}
+
+// ---------------------------------------------------------------- split geometry
+
+struct Plan {
+    int G;
+    int kernel;          // 0 CUDA-core, 1 tensor-core
+    int heads_per_cta;
+    int head_groups;
+    int n_head_tiles;
+    int chunk_tiles;
+    int S;
+    size_t off_status, off_qrot, off_opart, off_lse, total;
+};
+
+int device_sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+// The split count comes from the longest visible range and the SM count: the
+// key tiles of all (sequence, kv head, head group) units are cut into chunks so
+// that about three waves of resident CTAs cover them, at least four tiles a chunk.
+uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, Plan* pl)
+{
+    UAA_TRY(check_desc(d));
+    if (batch < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "batch=%d is negative", batch);
+    if (max_len < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "max_seq_len=%d is negative", max_len);
+    if (n_sm <= 0) return fail(UAA_ERR_INVALID_ARGUMENT, "SM count %d is not positive", n_sm);
+    Plan p{};
+    p.G = d->n_q_heads / d->n_kv_heads;
+    p.kernel = d->kv_dtype == UAA_DTYPE_F32 ? 0 : 1;
+    if (p.kernel == 0) {
+        p.heads_per_cta = 8;
+        p.n_head_tiles = 1;
+    } else if (d->head_dim == 256 || p.G <= 8) {
+        p.heads_per_cta = 8;
+        p.n_head_tiles = 1;
+    } else {
+        p.heads_per_cta = 16;
+        p.n_head_tiles = 2;
+    }
+    p.head_groups = (p.G + p.heads_per_cta - 1) / p.heads_per_cta;
+
+    long long max_keys = (long long)max_len + 1;
+    if (d->window > 0 && d->window < max_keys) max_keys = d->window;
+    const int max_tiles = (int)((max_keys + uaa::kTileKeys - 1) / uaa::kTileKeys) + (d->window > 0 ? 1 : 0);
+    const long long units = (long long)(batch > 0 ? batch : 1) * d->n_kv_heads * p.head_groups;
+    const int per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
+    const long long target = (long long)n_sm * per_sm * 3;
+    long long chunk = (units * max_tiles + target - 1) / target;
+    if (chunk < 4) chunk = 4;
+    if (chunk > max_tiles) chunk = max_tiles;
+    p.S = (int)((max_tiles + chunk - 1) / chunk);
+    p.chunk_tiles = (max_tiles + p.S - 1) / p.S;
+
+    const size_t B = (size_t)(batch > 0 ? batch : 0), Hq = d->n_q_heads, D = d->head_dim;
+    p.off_status = 0;
+    p.off_qrot = 256;
+    p.off_opart = p.off_qrot + align256(B * Hq * D * 4);
+    p.off_lse = p.off_opart + align256(B * Hq * p.S * D * 4);
+    p.total = p.off_lse + align256(B * Hq * p.S * 4);
+    *pl = p;
+    return UAA_OK;
+}
+
+uaa_status check_args(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, bool need_io)
+{
+    if (!a) return fail(UAA_ERR_INVALID_ARGUMENT, "args is NULL");
+    if (!ws || !ws->ptr) return fail(UAA_ERR_INVALID_ARGUMENT, "workspace is NULL");
+    if (!aligned16(ws->ptr)) return fail(UAA_ERR_INVALID_ARGUMENT, "workspace is not 16-byte aligned");
+    if (a->batch < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "batch=%d is negative", a->batch);
+    if (a->max_seq_len < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "max_seq_len=%d is negative", a->max_seq_len);
+    if (a->cache_capacity <= 0 || a->cache_capacity % 4 != 0)
+        return fail(UAA_ERR_INVALID_ARGUMENT, "cache_capacity=%d is not a positive multiple of 4",
+                    a->cache_capacity);
+    if ((long long)a->max_seq_len + 1 > a->cache_capacity)
+        return fail(UAA_ERR_CAPACITY, "max_seq_len=%d + 1 new token does not fit cache_capacity=%d",
+                    a->max_seq_len, a->cache_capacity);
+    if ((long long)a->batch * d->n_kv_heads * a->cache_capacity > 2147483647LL - 2 * uaa::kTileKeys)
+        return fail(UAA_ERR_UNSUPPORTED, "batch*n_kv_heads*cache_capacity=%lld exceeds 2^31 cache rows",
+                    (long long)a->batch * d->n_kv_heads * a->cache_capacity);
+    struct {
+        const void* p;
+        const char* name;
+        bool needed;
+    } ptrs[] = {
+        {a->q, "q", need_io},
+        {a->k_new, "k_new", need_io},
+        {a->v_new, "v_new", need_io},
+        {a->k_cache, "k_cache", true},
+        {a->v_cache, "v_cache", true},
+        {a->seq_lens, "seq_lens", true},
+        {a->out, "out", true},
+        {a->v_scale, "v_scale", d->kv_dtype == UAA_DTYPE_VQ8},
+        {a->q_norm_w, "q_norm_w", need_io && d->qk_norm},
+        {a->k_norm_w, "k_norm_w", need_io && d->qk_norm},
+        {a->sink, "sink", d->has_sink != 0},
+    };
+    for (auto& e : ptrs) {
+        if (e.needed && !e.p && a->batch > 0)  // a batch of 0 reads and writes nothing
+            return fail(d->has_sink && !strcmp(e.name, "sink") ? UAA_ERR_UNSUPPORTED : UAA_ERR_INVALID_ARGUMENT,
+                        "%s is NULL%s", e.name,
+                        !strcmp(e.name, "sink") ? " while has_sink=1" : "");
+        if (e.p && !aligned16(e.p)) return fail(UAA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", e.name);
+    }
+    if (a->q_rot && !aligned16(a->q_rot)) return fail(UAA_ERR_INVALID_ARGUMENT, "q_rot is not 16-byte aligned");
+    return UAA_OK;
+}
+
+uaa_status prepare(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, bool need_io,
+                   Plan* pl)
+{
+    UAA_TRY(check_desc(d));
+    UAA_TRY(check_args(d, a, ws, need_io));
+    const int n_sm = device_sm_count();
+    if (n_sm <= 0) return fail(UAA_ERR_CUDA, "no CUDA device: the SM count query failed");
+    UAA_TRY(make_plan(d, a->batch, a->max_seq_len, n_sm, pl));
+    if (ws->bytes < pl->total)
+        return fail(UAA_ERR_INVALID_ARGUMENT, "workspace has %zu bytes, the step needs %zu", ws->bytes,
+                    pl->total);
+    return UAA_OK;
+}
+
+float softmax_scale(const uaa_attn_desc* d)
+{
+    return d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)d->head_dim);
+}
+
+// Rotary frequencies theta'_p / pi in fp64 and the cos/sin multiplier: plain
+// base^(-2p/D); llama3 wavelength interpolation; YaRN ramp over the pair index
+// between the pairs whose wavelength fits beta_fast / beta_slow times into the
+// original context (huggingface_decoder_completeness.md, P0.2; YaRN as published).
+void rope_table(const uaa_attn_desc* d, double* inv_freq_over_pi, float* mscale)
+{
+    const int D = d->head_dim;
+    const double pi = 3.14159265358979323846;
+    const uaa_rope_params& r = d->rope;
+    double ms = 1.0;
+    double lo = 0.0, hi = 0.0;
+    if (r.scaling == UAA_ROPE_SCALING_YARN) {
+        const double ln_base = log(r.theta);
+        lo = D * log(r.original_max_pos / (2.0 * pi * r.beta_fast)) / (2.0 * ln_base);
+        hi = D * log(r.original_max_pos / (2.0 * pi * r.beta_slow)) / (2.0 * ln_base);
+        ms = r.attn_factor > 0.0 ? r.attn_factor : (r.factor > 1.0 ? 1.0 + 0.1 * log(r.factor) : 1.0);
+    }
+    for (int i = 0; i < D / 2; ++i) {
+        const double f = pow(r.theta, -(2.0 * i) / D);
+        double g = f;
+        if (r.scaling == UAA_ROPE_SCALING_LLAMA3) {
+            const double wl = 2.0 * pi / f;
+            const double wl_keep = r.original_max_pos / r.high_freq_factor;
+            const double wl_div = r.original_max_pos / r.low_freq_factor;
+            if (wl > wl_div) {
+                g = f / r.factor;
+            } else if (wl >= wl_keep) {
+                const double t = (r.original_max_pos / wl - r.low_freq_factor) /
+                                 (r.high_freq_factor - r.low_freq_factor);
+                g = t * f + (1.0 - t) * f / r.factor;
+            }
+        } else if (r.scaling == UAA_ROPE_SCALING_YARN) {
+            double ramp = hi > lo ? (i - lo) / (hi - lo) : (i >= lo ? 1.0 : 0.0);
+            ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
+            g = ramp * (f / r.factor) + (1.0 - ramp) * f;
+        }
+        inv_freq_over_pi[i] = g / pi;
+    }
+    *mscale = (float)ms;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+uaa_status encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, void* ptr, uint64_t inner, uint64_t rows,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw,
+                     const char* what)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(tm, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(UAA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return UAA_OK;
+}
+
+// ---------------------------------------------------------------- the three launches
+
+uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                      cudaStream_t s)
+{
+    if (a->batch == 0) return UAA_OK;
+    uaa::AppendParams p{};
+    p.B = a->batch;
+    p.Hq = d->n_q_heads;
+    p.Hkv = d->n_kv_heads;
+    p.D = d->head_dim;
+    p.cap = a->cache_capacity;
+    p.max_len = a->max_seq_len;
+    p.style = d->rope.style;
+    p.qk_norm = d->qk_norm;
+    p.eps = d->norm_eps;
+    const float scale = softmax_scale(d);
+    p.qscale = d->softcap > 0.f ? scale / d->softcap : scale * uaa::kLog2e;
+    p.io_dtype = d->io_dtype;
+    p.kv_dtype = d->kv_dtype;
+    p.q = a->q;
+    p.k_new = a->k_new;
+    p.v_new = a->v_new;
+    p.q_norm_w = a->q_norm_w;
+    p.k_norm_w = a->k_norm_w;
+    p.k_cache = a->k_cache;
+    p.v_cache = a->v_cache;
+    p.v_scale = a->v_scale;
+    p.seq_lens = a->seq_lens;
+    char* w = static_cast<char*>(ws->ptr);
+    p.q_prime = reinterpret_cast<float*>(w + pl.off_qrot);
+    p.q_rot_out = a->q_rot;
+    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+    rope_table(d, p.inv_freq_over_pi, &p.mscale);
+    const cudaError_t e = uaa::launch_append(p, s);
+    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "append kernel launch");
+}
+
+uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                       cudaStream_t s)
+{
+    if (a->batch == 0) return UAA_OK;
+    uaa::PartialParams p{};
+    p.B = a->batch;
+    p.Hq = d->n_q_heads;
+    p.Hkv = d->n_kv_heads;
+    p.D = d->head_dim;
+    p.G = pl.G;
+    p.heads_per_cta = pl.heads_per_cta;
+    p.head_groups = pl.head_groups;
+    p.cap = a->cache_capacity;
+    p.window = d->window;
+    p.S = pl.S;
+    p.chunk_tiles = pl.chunk_tiles;
+    p.softcap_log2e = d->softcap > 0.f ? d->softcap * uaa::kLog2e : 0.f;
+    char* w = static_cast<char*>(ws->ptr);
+    p.q_prime = reinterpret_cast<const float*>(w + pl.off_qrot);
+    p.k_cache = a->k_cache;
+    p.v_cache = a->v_cache;
+    p.v_scale = a->v_scale;
+    p.seq_lens = a->seq_lens;
+    p.o_part = reinterpret_cast<float*>(w + pl.off_opart);
+    p.lse_part = reinterpret_cast<float*>(w + pl.off_lse);
+    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+    cudaError_t e;
+    if (pl.kernel == 0) {
+        e = uaa::launch_partial_simt(p, s);
+    } else {
+        const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
+        const uint64_t D = d->head_dim;
+        CUtensorMap tk, tv, ts;
+        UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, 64,
+                          CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
+        if (d->kv_dtype == UAA_DTYPE_VQ8) {
+            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, (uint32_t)D, 64,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, "v_cache codes"));
+            UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, a->cache_capacity,
+                              (uint64_t)a->batch * d->n_kv_heads, (uint64_t)a->cache_capacity * 4, 64, 1,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
+        } else {
+            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, 64,
+                              CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
+            ts = tv;  // unused by the bf16 kernel
+        }
+        e = uaa::launch_partial_tc(p, tk, tv, ts, d->kv_dtype, pl.n_head_tiles, s);
+    }
+    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "partial kernel launch");
+}
+
+uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                       cudaStream_t s)
+{
+    if (a->batch == 0) return UAA_OK;
+    uaa::CombineParams p{};
+    p.B = a->batch;
+    p.Hq = d->n_q_heads;
+    p.Hkv = d->n_kv_heads;
+    p.D = d->head_dim;
+    p.G = pl.G;
+    p.window = d->window;
+    p.S = pl.S;
+    p.chunk_tiles = pl.chunk_tiles;
+    p.out_dtype = d->out_dtype;
+    p.sink = d->has_sink ? a->sink : nullptr;
+    p.seq_lens = a->seq_lens;
+    char* w = static_cast<char*>(ws->ptr);
+    p.o_part = reinterpret_cast<const float*>(w + pl.off_opart);
+    p.lse_part = reinterpret_cast<const float*>(w + pl.off_lse);
+    p.out = a->out;
+    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+    const cudaError_t e = uaa::launch_combine(p, s);
+    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "combine kernel launch");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- exported C ABI
+
+extern "C" {
+
+uaa_status uaa_rope_qk_norm_append(const uaa_attn_desc* desc, const uaa_step_args* args, const uaa_workspace* ws,
+                                   cudaStream_t stream)
+{
+    Plan pl{};
+    UAA_TRY(prepare(desc, args, ws, true, &pl));
+    return run_append(desc, args, ws, pl, stream);
+}
+
+uaa_status uaa_decode_attn_partial(const uaa_attn_desc* desc, const uaa_step_args* args, const uaa_workspace* ws,
+                                   cudaStream_t stream)
+{
+    Plan pl{};
+    UAA_TRY(prepare(desc, args, ws, false, &pl));
+    return run_partial(desc, args, ws, pl, stream);
+}
+
+uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_args* args, const uaa_workspace* ws,
+                                   cudaStream_t stream)
+{
+    Plan pl{};
+    UAA_TRY(prepare(desc, args, ws, false, &pl));
+    return run_combine(desc, args, ws, pl, stream);
+}
+
+uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args, const uaa_workspace* ws,
+                           cudaStream_t stream)
+{
+    Plan pl{};
+    UAA_TRY(prepare(desc, args, ws, true, &pl));
+    UAA_TRY(run_append(desc, args, ws, pl, stream));
+    UAA_TRY(run_partial(desc, args, ws, pl, stream));
+    return run_combine(desc, args, ws, pl, stream);
+}
+
+size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm)
+{
+    Plan pl{};
+    if (n_sm <= 0) n_sm = device_sm_count();
+    if (make_plan(desc, batch, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
+    return pl.total;
+}
+
+int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm)
+{
+    Plan pl{};
+    if (n_sm <= 0) n_sm = device_sm_count();
+    if (make_plan(desc, batch, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
+    return pl.S;
+}
+
+uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm,
+                                    uaa_workspace_layout* layout)
+{
+    if (!layout) return fail(UAA_ERR_INVALID_ARGUMENT, "layout is NULL");
+    Plan pl{};
+    if (n_sm <= 0) n_sm = device_sm_count();
+    UAA_TRY(make_plan(desc, batch, max_seq_len, n_sm, &pl));
+    layout->n_splits = pl.S;
+    layout->chunk_keys = pl.chunk_tiles * uaa::kTileKeys;
+    layout->heads_per_cta = pl.heads_per_cta;
+    layout->kernel = pl.kernel;
+    layout->status_offset = pl.off_status;
+    layout->q_rot_offset = pl.off_qrot;
+    layout->o_part_offset = pl.off_opart;
+    layout->lse_part_offset = pl.off_lse;
+    layout->total_bytes = pl.total;
+    return UAA_OK;
+}
+
+uaa_status uaa_vq8_quantize(const void* v, int32_t v_dtype, int64_t n_rows, int32_t head_dim, int8_t* codes,
+                            float* scales, cudaStream_t stream)
+{
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(UAA_ERR_UNSUPPORTED, "head_dim=%d is not supported (supported: {64, 128, 256})", head_dim);
+    if (v_dtype != UAA_DTYPE_F32 && v_dtype != UAA_DTYPE_BF16)
+        return fail(UAA_ERR_UNSUPPORTED, "v_dtype=%d is not F32 or BF16", v_dtype);
+    if (n_rows < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "n_rows=%lld is negative", (long long)n_rows);
+    if (n_rows == 0) return UAA_OK;
+    if (!v || !codes || !scales) return fail(UAA_ERR_INVALID_ARGUMENT, "a vq8_quantize pointer is NULL");
+    if (!aligned16(v) || !aligned16(codes) || !aligned16(scales))
+        return fail(UAA_ERR_INVALID_ARGUMENT, "vq8_quantize pointers must be 16-byte aligned");
+    const cudaError_t e = uaa::launch_vq8_quantize(v, v_dtype, n_rows, head_dim, codes, scales, stream);
+    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "vq8 quantize kernel launch");
+}
+
+uaa_status uaa_device_status(const uaa_workspace* ws, cudaStream_t stream, uint32_t* flags)
+{
+    if (!ws || !ws->ptr || !flags) return fail(UAA_ERR_INVALID_ARGUMENT, "workspace or flags is NULL");
+    uint32_t f = 0;
+    cudaError_t e = cudaMemcpyAsync(&f, ws->ptr, sizeof f, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && f) e = cudaMemsetAsync(ws->ptr, 0, sizeof f, stream);
+    if (e == cudaSuccess && f) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    *flags = f;
+    if (f)
+        return fail(UAA_ERR_DEVICE, "device flags 0x%x:%s%s%s", f, (f & UAA_DEVFLAG_CAPACITY) ? " capacity" : "",
+                    (f & UAA_DEVFLAG_LEN_HINT) ? " max_seq_len-exceeded" : "",
+                    (f & UAA_DEVFLAG_TIMEOUT) ? " wait-timeout" : "");
+    return UAA_OK;
+}
+
+const char* uaa_last_error(void) { return g_err; }
+
+const char* uaa_status_string(uaa_status s)
+{
+    switch (s) {
+    case UAA_OK: return "UAA_OK";
+    case UAA_ERR_INVALID_ARGUMENT: return "UAA_ERR_INVALID_ARGUMENT";
+    case UAA_ERR_UNSUPPORTED: return "UAA_ERR_UNSUPPORTED";
+    case UAA_ERR_CAPACITY: return "UAA_ERR_CAPACITY";
+    case UAA_ERR_CUDA: return "UAA_ERR_CUDA";
+    case UAA_ERR_DEVICE: return "UAA_ERR_DEVICE";
+    }
+    return "UAA_UNKNOWN_STATUS";
+}
+
+int32_t uaa_abi_version(void) { return UAA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// append.cu -- step 1 of the decode step: per-head QK RMSNorm, rotary embedding at
+// the absolute KV index, and the append of the new k / v rows to the cache.
+//
+// One CTA per sequence. The CTA first builds the cos / sin table of the
+// sequence's position (the angle pos * theta'_p is formed and reduced in fp64,
+// then rounded to fp32), then each warp takes whole head rows: q rows go to
+// the workspace pre-multiplied by the partial kernel's logit prescale, k rows
+// and v rows go to slot seq_lens[b] of the cache. vq8 values are quantised in
+// fp32 with IEEE division and round-half-even, the storage rule of the vq8
+// cache (llamay "Models and formats", "The KV cache, in three precisions").
+#include "internal.cuh"
+
+namespace uaa {
+namespace {
+
+constexpr int kAppendWarps = 8;
+
+__device__ __forceinline__ void store_kv(void* cache, int dtype, size_t i, float v)
+{
+    if (dtype == UAA_DTYPE_F32)
+        static_cast<float*>(cache)[i] = v;
+    else
+        static_cast<__nv_bfloat16*>(cache)[i] = __float2bfloat16_rn(v);
+}
+
+// vq8 storage rule on a row of D fp32 values held EPL per lane:
+// s = max|v| / 127, code = rint(v / s), |code| <= 127; s = 0 gives codes 0.
+template <int EPL>
+__device__ __forceinline__ void quantize_row(const float (&x)[EPL], int lane, int8_t* codes,
+                                             float* scale)
+{
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        float c = 0.f;
+        if (s != 0.f) c = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.f), 127.f);
+        codes[lane + 32 * i] = static_cast<int8_t>(static_cast<int>(c));
+    }
+    if (lane == 0) *scale = s;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p)
+{
+    constexpr int EPL = D / 32;  // row elements per lane
+    constexpr int HALF = D / 2;
+    __shared__ float2 cs[HALF];
+    __shared__ float rowbuf[kAppendWarps][D];
+
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = p.seq_lens[b];
+    const bool fits = L >= 0 && L < p.cap;
+    if (threadIdx.x == 0) {
+        if (!fits) atomicOr(p.status, UAA_DEVFLAG_CAPACITY);
+        else if (L > p.max_len) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
+    }
+    const int pos = fits ? L : 0;
+
+    // cos / sin of pos * theta'_p: fp64 product, exact pi-scaled reduction in sincospi.
+    for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
+        double sn, cn;
+        sincospi(static_cast<double>(pos) * p.inv_freq_over_pi[i], &sn, &cn);
+        cs[i] = make_float2(static_cast<float>(cn) * p.mscale, static_cast<float>(sn) * p.mscale);
+    }
+    __syncthreads();
+
+    const int n_rows = p.Hq + 2 * p.Hkv;
+    for (int r = warp; r < n_rows; r += kAppendWarps) {
+        const bool is_q = r < p.Hq;
+        const bool is_k = !is_q && r < p.Hq + p.Hkv;
+        const int head = is_q ? r : (is_k ? r - p.Hq : r - p.Hq - p.Hkv);
+        const size_t in_row = (static_cast<size_t>(b) * (is_q ? p.Hq : p.Hkv) + head) * D;
+        const void* src = is_q ? p.q : (is_k ? p.k_new : p.v_new);
+        float x[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) x[i] = load_elem(src, p.io_dtype, in_row + lane + 32 * i);
+
+        const size_t slot = ((static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos) * D;
+        if (!is_q && !is_k) {  // value row: stored as given (or quantised)
+            if (!fits) continue;
+            if (p.kv_dtype == UAA_DTYPE_VQ8) {
+                quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot,
+                                  p.v_scale + (static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos);
+            } else {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) store_kv(p.v_cache, p.kv_dtype, slot + lane + 32 * i, x[i]);
+            }
+            continue;
+        }
+
+        if (p.qk_norm) {  // RMSNorm over the head row, before the rotation
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) ss += x[i] * x[i];
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + p.eps);
+            const float* w = is_q ? p.q_norm_w : p.k_norm_w;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) x[i] = x[i] * inv * w[lane + 32 * i];
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) rowbuf[warp][lane + 32 * i] = x[i];
+        __syncwarp();
+
+        for (int pp = lane; pp < HALF; pp += 32) {
+            const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
+            const int ib = p.style == UAA_ROPE_NEOX ? pp + HALF : 2 * pp + 1;
+            const float a = rowbuf[warp][ia], bb = rowbuf[warp][ib];
+            const float2 c = cs[pp];
+            const float ya = a * c.x - bb * c.y;
+            const float yb = a * c.y + bb * c.x;
+            if (is_q) {
+                float* qp = p.q_prime + in_row;
+                qp[ia] = ya * p.qscale;
+                qp[ib] = yb * p.qscale;
+                if (p.q_rot_out) {
+                    p.q_rot_out[in_row + ia] = ya;
+                    p.q_rot_out[in_row + ib] = yb;
+                }
+            } else if (fits) {
+                store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
+                         slot + ia, ya);
+                store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
+                         slot + ib, yb);
+            }
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_dtype,
+                                                           int64_t n_rows, int8_t* codes,
+                                                           float* scales)
+{
+    constexpr int EPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         r < n_rows; r += warps) {
+        float x[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) x[i] = load_elem(v, v_dtype, static_cast<size_t>(r) * D + lane + 32 * i);
+        quantize_row<EPL>(x, lane, codes + static_cast<size_t>(r) * D, scales + r);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
+{
+    const dim3 grid(p.B), block(kAppendWarps * 32);
+    switch (p.D) {
+    case 64: append_kernel<64><<<grid, block, 0, s>>>(p); break;
+    case 128: append_kernel<128><<<grid, block, 0, s>>>(p); break;
+    case 256: append_kernel<256><<<grid, block, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
+                                float* scales, cudaStream_t s)
+{
+    const int64_t blocks64 = (n_rows + 7) / 8;
+    const unsigned blocks = static_cast<unsigned>(blocks64 < 65535 * 16 ? blocks64 : 65535 * 16);
+    switch (D) {
+    case 64: vq8_quantize_kernel<64><<<blocks, 256, 0, s>>>(v, v_dtype, n_rows, codes, scales); break;
+    case 128: vq8_quantize_kernel<128><<<blocks, 256, 0, s>>>(v, v_dtype, n_rows, codes, scales); break;
+    case 256: vq8_quantize_kernel<256><<<blocks, 256, 0, s>>>(v, v_dtype, n_rows, codes, scales); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace uaa

@@ -1,0 +1,118 @@
+"""DecodeLayer: one attention layer's KV cache and workspace on a CUDA device.
+
+PyTorch allocates the device memory and supplies the stream; every step of the
+method runs in libuaa through the C ABI (binding.py). This is the call a user
+makes: build the layer, load or grow its cache, then `step(q, k_new, v_new)`.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _require_cuda(device):
+    if not torch.cuda.is_available():
+        raise RuntimeError("DecodeLayer needs a CUDA device; libuaa has no CPU implementation")
+    return torch.device(device)
+
+
+class DecodeLayer:
+    def __init__(self, cfg: dict, batch: int, capacity: int, device="cuda"):
+        self.cfg = dict(cfg)
+        self.device = _require_cuda(device)
+        self.batch = int(batch)
+        self.capacity = int(capacity)
+        self.desc = B.make_desc(cfg)
+        Hq, Hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+        kv = cfg.get("kv_dtype", "bf16")
+        dev = self.device
+        kdt = torch.float32 if kv == "f32" else torch.bfloat16
+        self.k_cache = torch.zeros((batch, Hkv, capacity, D), dtype=kdt, device=dev)
+        if kv == "vq8":
+            self.v_cache = torch.zeros((batch, Hkv, capacity, D), dtype=torch.int8, device=dev)
+            self.v_scale = torch.zeros((batch, Hkv, capacity), dtype=torch.float32, device=dev)
+        else:
+            self.v_cache = torch.zeros((batch, Hkv, capacity, D), dtype=kdt, device=dev)
+            self.v_scale = None
+        self.seq_lens = torch.zeros((batch,), dtype=torch.int32, device=dev)
+        self.max_len_hint = 0
+        self.out = torch.empty((batch, Hq, D), dtype=_TORCH_DTYPE[cfg.get("out_dtype", "f32")], device=dev)
+        self.q_norm_w = self.k_norm_w = self.sink = None
+        # workspace sized for the longest allowed sequence; zeroed once (status word)
+        nbytes = B.uaa_workspace_size(self.desc, batch, capacity - 1, 0)
+        if nbytes == 0:
+            raise B.UaaError(B.UAA_ERR_UNSUPPORTED, B.last_error())
+        self.ws_tensor = torch.zeros((nbytes,), dtype=torch.uint8, device=dev)
+        self.ws = B.UaaWorkspace(self.ws_tensor.data_ptr(), nbytes)
+
+    # ------------------------------------------------------------ state
+    def set_params(self, q_norm_w=None, k_norm_w=None, sink=None):
+        to = lambda t: None if t is None else t.to(device=self.device, dtype=torch.float32).contiguous()
+        self.q_norm_w, self.k_norm_w, self.sink = to(q_norm_w), to(k_norm_w), to(sink)
+
+    def load_cache(self, k_cache, v, lens):
+        """Copy host caches in. For a vq8 layer `v` holds fp32 values, quantised on
+        the device by uaa_vq8_quantize (the append's own rule)."""
+        self.k_cache.copy_(k_cache)
+        if self.v_scale is not None:
+            vals = v.to(device=self.device, dtype=torch.float32).contiguous()
+            D = self.cfg["head_dim"]
+            B.uaa_vq8_quantize(vals.data_ptr(), B.DTYPE["f32"], vals.numel() // D, D, self.v_cache.data_ptr(),
+                               self.v_scale.data_ptr(), torch.cuda.current_stream(self.device))
+        else:
+            self.v_cache.copy_(v)
+        lens = torch.as_tensor(lens, dtype=torch.int32)
+        self.seq_lens.copy_(lens)
+        self.max_len_hint = int(lens.max()) if lens.numel() else 0
+
+    def set_lengths(self, lens):
+        lens = torch.as_tensor(lens, dtype=torch.int32)
+        self.seq_lens.copy_(lens)
+        self.max_len_hint = int(lens.max()) if lens.numel() else 0
+
+    # ------------------------------------------------------------ calls
+    def args(self, q, k_new, v_new, max_seq_len=None, q_rot=None) -> B.UaaStepArgs:
+        a = B.UaaStepArgs()
+        a.batch = self.batch
+        a.q, a.k_new, a.v_new = B.ptr(q), B.ptr(k_new), B.ptr(v_new)
+        a.q_norm_w, a.k_norm_w, a.sink = B.ptr(self.q_norm_w), B.ptr(self.k_norm_w), B.ptr(self.sink)
+        a.k_cache, a.v_cache, a.v_scale = B.ptr(self.k_cache), B.ptr(self.v_cache), B.ptr(self.v_scale)
+        a.cache_capacity = self.capacity
+        a.seq_lens = B.ptr(self.seq_lens)
+        a.max_seq_len = self.max_len_hint if max_seq_len is None else int(max_seq_len)
+        a.out = B.ptr(self.out)
+        a.q_rot = B.ptr(q_rot)
+        return a
+
+    def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True):
+        """One decode step (append, split-K partials, combine) on `stream`."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        B.uaa_decode_attn(self.desc, self.args(q, k_new, v_new, max_seq_len), self.ws, s)
+        if advance_hint and max_seq_len is None:
+            self.max_len_hint += 1
+        return self.out
+
+    def append(self, q, k_new, v_new, stream=None, q_rot=None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        B.uaa_rope_qk_norm_append(self.desc, self.args(q, k_new, v_new, q_rot=q_rot), self.ws, s)
+
+    def partial(self, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        B.uaa_decode_attn_partial(self.desc, self.args(None, None, None), self.ws, s)
+
+    def combine(self, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        B.uaa_decode_attn_combine(self.desc, self.args(None, None, None), self.ws, s)
+        self.max_len_hint += 1
+        return self.out
+
+    def layout(self, max_seq_len=None) -> B.UaaWorkspaceLayout:
+        return B.uaa_get_workspace_layout(self.desc, self.batch,
+                                          self.max_len_hint if max_seq_len is None else max_seq_len, 0)
+
+    def device_status(self, stream=None) -> int:
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        return B.uaa_device_status(self.ws, s)

@@ -1,0 +1,216 @@
+/*
+ * uaa.h -- C ABI of the GB300 (sm_103a) grouped-query-attention decode step.
+ *
+ * One decode step of one attention layer, for a batch of sequences that each
+ * hold a KV cache:
+ *
+ *   1. uaa_rope_qk_norm_append: optional per-head RMSNorm of the new q and k
+ *      rows, rotary position embedding at the sequence's absolute KV index, and
+ *      the append of k and v at slot seq_lens[b] (seq_lens[b] then grows by 1).
+ *   2. uaa_decode_attn_partial: split-K flash decoding; each CTA attends one
+ *      key range of one (sequence, kv head, head group) and writes a partial
+ *      (normalised output row and log-sum-exp) to the workspace.
+ *   3. uaa_decode_attn_combine: log-sum-exp merge of the partials, the sink
+ *      logit added to the denominator, the output written.
+ *   uaa_decode_attn runs 1-3 on one stream.
+ *
+ * Where the method is defined (page title, then section):
+ *   - integral GQA ratio, head_dim set, 1/sqrt(head_dim) scale, the split-K
+ *     decode and KV-producer paths (prior art):
+ *       Model support matrix, "Structural fact requirements", "Kernel path
+ *       capabilities"; the typed-refusal convention: "Conformance CLI";
+ *   - RoPE scaling (llama3, YaRN), QK-norm before RoPE, RMSNorm, positions at
+ *     the absolute KV index, sliding window, attention-logit softcap:
+ *       huggingface_decoder_completeness.md, P0.2, P1.1, P1.2, P1.3, P1.4;
+ *   - NeoX vs interleaved pairing and the llama3 parameters:
+ *       FreeToken PR #722 "serve Llama and Mistral llama-arch GGUF", "Changes";
+ *       llamay "Models and formats", "Architectures";
+ *   - per-head attention sink in the softmax denominator, YaRN for gpt-oss:
+ *       llamay "Models and formats", "Architectures" (gpt-oss row);
+ *   - the vq8 cache (int8 values, per-token per-head fp32 scale, keys exact):
+ *       llamay "Models and formats", "The KV cache, in three precisions".
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte
+ *     aligned, row-major and dense. The library never allocates device memory,
+ *     never synchronises (except uaa_device_status) and launches only on the
+ *     given stream.
+ *   - Layouts: q [B][Hq][D]; k_new, v_new [B][Hkv][D] (io_dtype);
+ *     k_cache [B][Hkv][cap][D] (fp32, or bf16 for BF16 and VQ8 caches);
+ *     v_cache [B][Hkv][cap][D] (fp32, bf16, or int8 codes for VQ8);
+ *     v_scale [B][Hkv][cap] fp32 (VQ8 only); seq_lens [B] int32;
+ *     out [B][Hq][D] (out_dtype). Query head h reads kv head h / (Hq / Hkv).
+ *   - Facts outside the supported ranges are refused with a status and a
+ *     message naming the fact (uaa_last_error), never approximated.
+ *   - A step's entry points must receive the same descriptor and arguments;
+ *     partial and combine run after the append of the same step (they read
+ *     seq_lens after its increment).
+ */
+#ifndef UAA_H
+#define UAA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define UAA_ABI_VERSION 1
+
+typedef enum {
+    UAA_OK = 0,
+    UAA_ERR_INVALID_ARGUMENT = 1, /* null or misaligned pointer, workspace too small */
+    UAA_ERR_UNSUPPORTED = 2,      /* a fact outside the supported range */
+    UAA_ERR_CAPACITY = 3,         /* max_seq_len + 1 does not fit the cache */
+    UAA_ERR_CUDA = 4,             /* a CUDA call failed; the message names it */
+    UAA_ERR_DEVICE = 5            /* uaa_device_status found a device-side flag */
+} uaa_status;
+
+typedef enum { UAA_ROPE_NEOX = 0, UAA_ROPE_INTERLEAVED = 1 } uaa_rope_style;
+typedef enum {
+    UAA_ROPE_SCALING_NONE = 0,
+    UAA_ROPE_SCALING_LLAMA3 = 1,
+    UAA_ROPE_SCALING_YARN = 2
+} uaa_rope_scaling;
+typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2 } uaa_dtype;
+
+/* Device-side status flags (sticky, in the workspace; read by uaa_device_status). */
+#define UAA_DEVFLAG_CAPACITY 0x1u   /* seq_lens[b] >= cache_capacity: that sequence was not appended */
+#define UAA_DEVFLAG_LEN_HINT 0x2u   /* seq_lens[b] > max_seq_len: too few splits, out rows are NaN */
+#define UAA_DEVFLAG_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up; outputs are invalid */
+
+/* Rotary embedding. Pair p of a head row is (p, p + D/2) for NEOX and (2p, 2p+1)
+ * for INTERLEAVED; theta_p = theta^(-2p/D), rotated by angle pos * theta'_p.
+ * LLAMA3: Llama-3.1 wavelength interpolation (factor, low_freq_factor,
+ *   high_freq_factor, original_max_pos).
+ * YARN: ramp over the pair index between the pairs whose wavelength fits
+ *   beta_fast and beta_slow times into original_max_pos (not rounded); theta'
+ *   blends theta / factor and theta; cos and sin are multiplied by attn_factor
+ *   (<= 0 selects 0.1 ln(factor) + 1). */
+typedef struct {
+    int32_t style;            /* uaa_rope_style */
+    double theta;             /* base, > 0 */
+    int32_t scaling;          /* uaa_rope_scaling */
+    double factor;
+    double low_freq_factor;
+    double high_freq_factor;
+    int32_t original_max_pos;
+    double beta_fast;
+    double beta_slow;
+    double attn_factor;
+} uaa_rope_params;
+
+typedef struct {
+    int32_t n_q_heads;        /* Hq, a positive multiple of n_kv_heads */
+    int32_t n_kv_heads;       /* Hkv > 0 */
+    int32_t head_dim;         /* D in {64, 128, 256} */
+    float scale;              /* softmax scale; 0 selects 1/sqrt(D) */
+    uaa_rope_params rope;
+    int32_t qk_norm;          /* 1: RMSNorm of each q and k head row before RoPE */
+    float norm_eps;           /* RMSNorm epsilon, >= 0 */
+    int32_t window;           /* 0: none; W > 0: keys j with pos - W < j <= pos */
+    float softcap;            /* 0: none; c > 0: s -> c tanh(s / c), after the scale */
+    int32_t has_sink;         /* 1: sink[h] joins the softmax denominator of head h */
+    int32_t kv_dtype;         /* UAA_DTYPE_F32, _BF16 or _VQ8 */
+    int32_t io_dtype;         /* q, k_new, v_new: UAA_DTYPE_F32 or _BF16 */
+    int32_t out_dtype;        /* out: UAA_DTYPE_F32 or _BF16 */
+} uaa_attn_desc;
+
+typedef struct {
+    int32_t batch;            /* B >= 0 (0 is a no-op) */
+    const void* q;            /* [B][Hq][D] io_dtype */
+    const void* k_new;        /* [B][Hkv][D] io_dtype */
+    const void* v_new;        /* [B][Hkv][D] io_dtype */
+    const float* q_norm_w;    /* [D], required when qk_norm */
+    const float* k_norm_w;    /* [D], required when qk_norm */
+    const float* sink;        /* [Hq], required when has_sink */
+    void* k_cache;            /* [B][Hkv][cap][D] */
+    void* v_cache;            /* [B][Hkv][cap][D] */
+    float* v_scale;           /* [B][Hkv][cap], VQ8 only */
+    int32_t cache_capacity;   /* cap: slots per (sequence, kv head), a multiple of 4 */
+    int32_t* seq_lens;        /* [B]: tokens cached before the step; the append adds 1 */
+    int32_t max_seq_len;      /* host bound on seq_lens[b] before the step; sizes the splits */
+    void* out;                /* [B][Hq][D] out_dtype */
+    float* q_rot;             /* optional [B][Hq][D] fp32: the normed, rotated q rows */
+} uaa_step_args;
+
+/* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed
+ * once after allocation. It holds the rotated q rows, the split partials and the
+ * device status word; it must not be shared by steps that run concurrently. */
+typedef struct {
+    void* ptr;
+    size_t bytes;
+} uaa_workspace;
+
+/* Where each array lives in the workspace, and the split geometry. */
+typedef struct {
+    int32_t n_splits;         /* S: partial slots per (sequence, query head) */
+    int32_t chunk_keys;       /* keys per split (a multiple of 64); split s of a sequence
+                                 covers 64-key tiles [t0 + s c, t0 + (s+1) c), t0 = lo / 64 */
+    int32_t heads_per_cta;    /* query heads one partial CTA handles */
+    int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
+    size_t status_offset;     /* uint32 device flags */
+    size_t q_rot_offset;      /* fp32 [B][Hq][D]: rotated q times the kernel's logit prescale */
+    size_t o_part_offset;     /* fp32 [B][Hq][S][D]: normalised partial outputs */
+    size_t lse_part_offset;   /* fp32 [B][Hq][S]: partial log2-sum-exp of the final logits */
+    size_t total_bytes;
+} uaa_workspace_layout;
+
+/* Step 1 (append). Writes the k/v rows at slot seq_lens[b], increments seq_lens,
+ * and stores the rotated q rows in the workspace (and in args->q_rot if set). */
+uaa_status uaa_rope_qk_norm_append(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                   const uaa_workspace* ws, cudaStream_t stream);
+
+/* Step 2 (split-K partials) over the visible keys of every sequence. */
+uaa_status uaa_decode_attn_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                   const uaa_workspace* ws, cudaStream_t stream);
+
+/* Step 3 (log-sum-exp combine + sink) into args->out. */
+uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                   const uaa_workspace* ws, cudaStream_t stream);
+
+/* Steps 1-3 on one stream: the whole decode step of one layer. */
+uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
+                           const uaa_workspace* ws, cudaStream_t stream);
+
+/* Workspace bytes for a step of `batch` sequences whose lengths before the step
+ * are at most max_seq_len. n_sm <= 0 queries the current device's SM count; the
+ * launches always use the current device's count. Returns 0 on a refused desc. */
+size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len,
+                          int32_t n_sm);
+
+/* Number of split slots S per (sequence, query head); 0 on a refused desc. */
+int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len,
+                       int32_t n_sm);
+
+/* The workspace layout and split geometry (host only; n_sm as above). */
+uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch,
+                                    int32_t max_seq_len, int32_t n_sm,
+                                    uaa_workspace_layout* layout);
+
+/* Quantise n_rows rows of head_dim values (fp32 or bf16, v_dtype) to the vq8
+ * storage: codes = rint(v / s) with s = max|v| / 127 in fp32 (the append's rule).
+ * Used to fill a vq8 cache from existing values. */
+uaa_status uaa_vq8_quantize(const void* v, int32_t v_dtype, int64_t n_rows, int32_t head_dim,
+                            int8_t* codes, float* scales, cudaStream_t stream);
+
+/* Waits for the stream, reads the device flags (UAA_DEVFLAG_*) of the workspace
+ * into *flags, clears them, and returns UAA_ERR_DEVICE if any was set. */
+uaa_status uaa_device_status(const uaa_workspace* ws, cudaStream_t stream, uint32_t* flags);
+
+/* The message of the last refused or failed call on this thread. */
+const char* uaa_last_error(void);
+
+/* A fixed name for a status code. */
+const char* uaa_status_string(uaa_status status);
+
+/* UAA_ABI_VERSION of the built library. */
+int32_t uaa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

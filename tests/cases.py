@@ -47,3 +47,16 @@ def run_oracle_step(case: dict, oracle_mod, n_threads=None):
                                  a["k_norm_w"], a["sink"], a["k_cache"], a["v_cache"],
                                  a["v_scale"], a["seq_lens"], n_threads=n_threads)
     return out, a
+
+
+# ---------------------------------------------------------------- GPU side
+
+def gpu_layer(case: dict, device="cuda"):
+    """A DecodeLayer holding the case's cache (a vq8 cache is quantised on the device)."""
+    from gqa_attention_kv_qk_gb300.layer import DecodeLayer
+    cfg = case["cfg"]
+    layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device)
+    v = case["v_values"] if cfg.get("kv_dtype") == "vq8" else case["v_cache"]
+    layer.load_cache(case["k_cache"], v, case["lens"])
+    layer.set_params(case["q_norm_w"], case["k_norm_w"], case["sink"])
+    return layer

@@ -1,0 +1,179 @@
+"""Host-side tests of the C ABI: the library loads and exports every entry point
+include/uaa.h declares, descriptors outside the supported ranges are refused with
+a message naming the fact, and the split geometry is consistent. No call here
+reaches a GPU: every refusal returns before the first CUDA call, and the geometry
+queries take an explicit SM count."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gqa_attention_kv_qk_gb300 import binding as B
+from gqa_attention_kv_qk_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "uaa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gqa_attention_kv_qk_gb300 import build
+    build.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(uaa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_entry_point_is_exported(L):
+    names = declared_functions()
+    assert "uaa_decode_attn" in names and len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
+    bound = {s[0] for s in B._SIGS}
+    assert bound == set(names), "binding and header disagree"
+    assert B.uaa_abi_version() == 1
+
+
+def good_desc(**kw):
+    cfg = W.config("llama31_8b_decode")
+    cfg.update(kw)
+    return B.make_desc(cfg)
+
+
+def fake_args(**kw):
+    a = B.UaaStepArgs()
+    a.batch = 2
+    for f in ("q", "k_new", "v_new", "k_cache", "v_cache", "seq_lens", "out", "v_scale", "q_norm_w",
+              "k_norm_w", "sink"):
+        setattr(a, f, 0x10000)  # aligned, never dereferenced: every case fails before any launch
+    a.cache_capacity = 128
+    a.max_seq_len = 64
+    a.q_rot = None
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+WS = B.UaaWorkspace(0x20000, 1 << 30)
+
+
+@pytest.mark.parametrize("kw,status,fact", [
+    (dict(head_dim=96), B.UAA_ERR_UNSUPPORTED, "head_dim=96"),
+    (dict(head_dim=32), B.UAA_ERR_UNSUPPORTED, "head_dim=32"),
+    (dict(n_q_heads=30), B.UAA_ERR_UNSUPPORTED, "n_q_heads=30"),
+    (dict(n_kv_heads=0), B.UAA_ERR_UNSUPPORTED, "n_kv_heads=0"),
+    (dict(window=-1), B.UAA_ERR_UNSUPPORTED, "window=-1"),
+    (dict(softcap=-2.0), B.UAA_ERR_UNSUPPORTED, "softcap=-2"),
+    (dict(rope_theta=0.0), B.UAA_ERR_UNSUPPORTED, "rope.theta=0"),
+    (dict(rope_scaling="llama3", factor=0.5), B.UAA_ERR_UNSUPPORTED, "llama3"),
+    (dict(rope_scaling="yarn", beta_fast=1.0, beta_slow=32.0), B.UAA_ERR_UNSUPPORTED, "yarn"),
+])
+def test_descriptor_refusals_name_the_fact(L, kw, status, fact):
+    st = B.uaa_decode_attn(good_desc(**kw), fake_args(), WS, None, check=False)
+    assert st == status
+    assert fact in B.last_error()
+
+
+def test_enum_refusals(L):
+    d = good_desc()
+    d.kv_dtype = 7
+    assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert "kv_dtype=7" in B.last_error()
+    d = good_desc()
+    d.rope.scaling = 9
+    assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert "rope.scaling=9" in B.last_error()
+    d = good_desc()
+    d.rope.style = 3
+    assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,status,fact", [
+    (dict(q=None), B.UAA_ERR_INVALID_ARGUMENT, "q is NULL"),
+    (dict(k_cache=0x10001), B.UAA_ERR_INVALID_ARGUMENT, "k_cache is not 16-byte aligned"),
+    (dict(seq_lens=None), B.UAA_ERR_INVALID_ARGUMENT, "seq_lens is NULL"),
+    (dict(max_seq_len=128), B.UAA_ERR_CAPACITY, "does not fit cache_capacity=128"),
+    (dict(cache_capacity=130), B.UAA_ERR_INVALID_ARGUMENT, "cache_capacity=130"),
+    (dict(batch=-1), B.UAA_ERR_INVALID_ARGUMENT, "batch=-1"),
+])
+def test_argument_refusals(L, kw, status, fact):
+    st = B.uaa_decode_attn(good_desc(), fake_args(**kw), WS, None, check=False)
+    assert st == status
+    assert fact in B.last_error()
+
+
+def test_sink_flag_without_pointer_is_refused(L):
+    st = B.uaa_decode_attn(good_desc(has_sink=True), fake_args(sink=None), WS, None, check=False)
+    assert st == B.UAA_ERR_UNSUPPORTED and "sink is NULL while has_sink=1" in B.last_error()
+    st = B.uaa_decode_attn(good_desc(qk_norm=True), fake_args(q_norm_w=None), WS, None, check=False)
+    assert st == B.UAA_ERR_INVALID_ARGUMENT and "q_norm_w" in B.last_error()
+
+
+def test_vq8_quantize_refusals(L):
+    assert B.uaa_vq8_quantize(0x10000, 0, 4, 96, 0x10000, 0x10000, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert B.uaa_vq8_quantize(0x10000, 2, 4, 64, 0x10000, 0x10000, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert B.uaa_vq8_quantize(0x10001, 0, 4, 64, 0x10000, 0x10000, None, check=False) == B.UAA_ERR_INVALID_ARGUMENT
+    assert B.uaa_vq8_quantize(0, 0, 0, 64, 0, 0, None, check=False) == B.UAA_OK  # nothing to do
+
+
+@pytest.mark.parametrize("name", list(W.CONFIGS))
+def test_split_geometry_covers_every_visible_key(L, name):
+    for layer in W.layer_configs(W.config(name)):
+        d = B.make_desc(layer)
+        batch = layer["batch"]
+        longest = W.capacity(layer, extra=layer.get("steps", 1)) - 1
+        for n_sm in (1, 20, 152):
+            lay = B.uaa_get_workspace_layout(d, batch, longest, n_sm)
+            S, ck = lay.n_splits, lay.chunk_keys
+            assert S >= 1 and ck % 64 == 0 and ck > 0
+            visible = min(longest + 1, layer.get("window") or longest + 1)
+            tiles = -(-visible // 64) + (1 if layer.get("window") else 0)
+            assert S * (ck // 64) >= tiles, "splits must cover the visible tiles"
+            assert (S - 1) * (ck // 64) < tiles, "no split slot is always empty"
+            assert lay.kernel == (0 if layer["kv_dtype"] == "f32" else 1)
+            Hq, D = layer["n_q_heads"], layer["head_dim"]
+            assert lay.o_part_offset >= lay.q_rot_offset + batch * Hq * D * 4
+            assert lay.lse_part_offset >= lay.o_part_offset + batch * Hq * S * D * 4
+            assert lay.total_bytes >= lay.lse_part_offset + batch * Hq * S * 4
+            assert B.uaa_workspace_size(d, batch, longest, n_sm) == lay.total_bytes
+            assert B.uaa_num_splits(d, batch, longest, n_sm) == S
+            for off in (lay.q_rot_offset, lay.o_part_offset, lay.lse_part_offset):
+                assert off % 256 == 0
+
+
+def test_geometry_query_refuses_bad_desc(L):
+    assert B.uaa_workspace_size(good_desc(head_dim=48), 4, 100, 152) == 0
+    assert B.uaa_num_splits(good_desc(n_q_heads=9), 4, 100, 152) == 0
+    assert "n_q_heads=9" in B.last_error()
+
+
+def test_status_strings(L):
+    for s, name in ((0, "UAA_OK"), (1, "UAA_ERR_INVALID_ARGUMENT"), (2, "UAA_ERR_UNSUPPORTED"),
+                    (3, "UAA_ERR_CAPACITY"), (4, "UAA_ERR_CUDA"), (5, "UAA_ERR_DEVICE")):
+        assert B.status_string(s) == name
+
+
+def test_struct_sizes_match_the_header(L, tmp_path):
+    """Compile a probe against include/uaa.h and compare sizeof/offsetof with ctypes."""
+    import subprocess
+    src = tmp_path / "probe.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "uaa.h"\n'
+        'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(uaa_attn_desc), sizeof(uaa_step_args),'
+        ' sizeof(uaa_workspace), sizeof(uaa_workspace_layout), offsetof(uaa_attn_desc, out_dtype),'
+        ' offsetof(uaa_step_args, q_rot), offsetof(uaa_workspace_layout, total_bytes)); return 0;}\n')
+    exe = tmp_path / "probe"
+    r = subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src),
+                        "-o", str(exe)], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("no C compiler / CUDA headers for the probe: " + r.stderr[:200])
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    want = [ctypes.sizeof(B.UaaAttnDesc), ctypes.sizeof(B.UaaStepArgs), ctypes.sizeof(B.UaaWorkspace),
+            ctypes.sizeof(B.UaaWorkspaceLayout), B.UaaAttnDesc.out_dtype.offset, B.UaaStepArgs.q_rot.offset,
+            B.UaaWorkspaceLayout.total_bytes.offset]
+    assert got == want

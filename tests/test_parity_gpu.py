@@ -1,0 +1,300 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+The bar: cache-append slots, positions (seq_lens) and vq8 codes/scales bit-exact;
+appended key rows within one bf16 ulp (the GPU rotates in fp32, the oracle in
+fp64, both round to nearest even); outputs max|d| <= 2e-3 and mean|d| <= 2e-4
+against the fp64 oracle (fp32 outputs).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gqa_attention_kv_qk_gb300 import binding as B
+from gqa_attention_kv_qk_gb300 import workloads as W
+from tests.cases import gpu_layer, host_case, oracle_arrays
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN = 2e-3, 2e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gqa_attention_kv_qk_gb300 import build
+    build.build()
+
+
+def f64(a):
+    if isinstance(a, torch.Tensor):
+        return a.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def bf16_bits_to_f64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def assert_out_close(got, want, what="out", tol_max=TOL_MAX, tol_mean=TOL_MEAN):
+    d = np.abs(f64(got) - want)
+    assert np.all(np.isfinite(f64(got))), f"{what}: non-finite values"
+    assert d.max() <= tol_max and d.mean() <= tol_mean, f"{what}: max {d.max():.3g} mean {d.mean():.3g}"
+    return d.max(), d.mean()
+
+
+def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero", check_qrot=True,
+                    max_seq_len=None):
+    """Run `steps` chained decode steps on both sides and compare everything the
+    step writes. Returns the worst (max, mean) output error."""
+    case = host_case(cfg, lens=lens, cap=cap, fill_unused=fill_unused)
+    a = oracle_arrays(case, oracle_mod)
+    layer = gpu_layer(case)
+    kv = cfg.get("kv_dtype", "bf16")
+    if kv == "vq8":  # both quantisers on the same fp32 values
+        assert np.array_equal(layer.v_cache.cpu().numpy(), a["v_cache"])
+        assert np.array_equal(layer.v_scale.cpu().numpy().view(np.uint32), a["v_scale"].view(np.uint32))
+    B_, Hq, D = cfg["batch"], cfg["n_q_heads"], cfg["head_dim"]
+    worst = (0.0, 0.0)
+    for step in range(steps):
+        inp = W.step_inputs(cfg, step)
+        pre = a["seq_lens"].copy()
+        q_rot = torch.empty((B_, Hq, D), dtype=torch.float32, device="cuda")
+        dev = {k: v.cuda() for k, v in inp.items()}
+        layer.append(dev["q"], dev["k_new"], dev["v_new"], q_rot=q_rot)
+        layer.partial()
+        out = layer.combine().clone()
+        torch.cuda.synchronize()
+        qr = oracle_mod.append(cfg, W.bits(inp["q"]).copy(), W.bits(inp["k_new"]).copy(),
+                               W.bits(inp["v_new"]).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
+                               a["v_cache"], a["v_scale"], a["seq_lens"])
+        want = oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"])
+        # positions / slots: bit-exact
+        assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
+        assert layer.device_status() == 0
+        if check_qrot:
+            assert np.allclose(q_rot.cpu().numpy(), qr, rtol=2e-5, atol=2e-5)
+        # the appended rows
+        for b in range(B_):
+            slot = int(pre[b])
+            kg = f64(layer.k_cache[b, :, slot].float())
+            if kv == "f32":
+                ko = a["k_cache"][b, :, slot].astype(np.float64)
+                assert np.allclose(kg, ko, rtol=1e-5, atol=1e-6)
+                assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
+            else:
+                ko = bf16_bits_to_f64(a["k_cache"][b, :, slot])
+                assert np.all(np.abs(kg - ko) <= np.abs(ko) * 2.0 ** -7 + 1e-30), "k row beyond one bf16 ulp"
+                if kv == "bf16":
+                    vg = layer.v_cache[b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
+                    assert np.array_equal(vg, a["v_cache"][b, :, slot])
+                else:
+                    assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
+                    assert np.array_equal(layer.v_scale[b, :, slot].cpu().numpy().view(np.uint32),
+                                          a["v_scale"][b, :, slot].view(np.uint32))
+        mx, mean = assert_out_close(out, want, f"step {step}")
+        worst = (max(worst[0], mx), max(worst[1], mean))
+    return worst
+
+
+# ------------------------------------------------------------------ the five workloads, small
+
+SMALL = {
+    "llama32_1b_tiny": dict(lens=[256]),
+    "llama31_8b_decode": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
+    "qwen3_8b_ragged": dict(overrides=dict(batch=5, seq_len=(1, 2100)), lens=[1, 64, 129, 2000, 777]),
+    "gemma2_9b_swa": dict(overrides=dict(batch=2, seq_len=5000), lens=[3000, 4999]),
+    "gptoss_vq8_sink": dict(overrides=dict(batch=3, seq_len=4096), lens=[100, 1000, 4095]),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_workload_parity_small(oracle_mod, name):
+    spec = SMALL[name]
+    cfg = W.config(name, **spec.get("overrides", {}))
+    for layer_cfg in W.layer_configs(cfg):
+        run_and_compare(oracle_mod, layer_cfg, spec["lens"], steps=cfg.get("steps", 1))
+
+
+# ------------------------------------------------------------------ edge cases
+
+EDGE = [
+    # (id, workload, overrides, lens)
+    ("first-token", "llama31_8b_decode", dict(batch=3, seq_len=200), [0, 0, 63]),
+    ("tile-boundaries", "llama31_8b_decode", dict(batch=4, seq_len=300), [63, 64, 127, 255]),
+    ("last-slot", "llama31_8b_decode", dict(batch=2, seq_len=255), [255, 10]),
+    ("window-1", "gemma2_9b_swa", dict(batch=2, seq_len=500, layers=[dict(window=1)]), [499, 3]),
+    ("window-ragged", "gemma2_9b_swa", dict(batch=3, seq_len=1000, layers=[dict(window=100)]), [999, 150, 40]),
+    ("window-wider", "gemma2_9b_swa", dict(batch=2, seq_len=300, layers=[dict(window=4096)]), [299, 17]),
+    ("softcap-strong", "gemma2_9b_swa", dict(batch=2, seq_len=600, softcap=1.0, layers=None), [599, 200]),
+    ("mha-g1", "llama31_8b_decode", dict(batch=2, n_q_heads=8, n_kv_heads=8, seq_len=300), [299, 77]),
+    ("g16", "llama31_8b_decode", dict(batch=2, n_q_heads=32, n_kv_heads=2, seq_len=300), [299, 77]),
+    ("g32-two-groups", "llama31_8b_decode", dict(batch=2, n_q_heads=32, n_kv_heads=1, seq_len=300), [299, 77]),
+    ("d64-bf16", "gptoss_vq8_sink", dict(batch=2, kv_dtype="bf16", seq_len=500), [499, 64]),
+    ("d128-vq8", "llama31_8b_decode", dict(batch=2, kv_dtype="vq8", seq_len=500), [499, 64]),
+    ("d256-vq8-sink", "gemma2_9b_swa", dict(batch=2, kv_dtype="vq8", has_sink=True, seq_len=500, layers=None),
+     [499, 64]),
+    ("d64-g16-vq8", "gptoss_vq8_sink", dict(batch=2, n_q_heads=32, n_kv_heads=2, seq_len=300), [299, 5]),
+    ("f32-io-bf16-cache", "llama31_8b_decode", dict(batch=2, io_dtype="f32", seq_len=300), [299, 5]),
+    ("bf16-io-f32-cache", "llama32_1b_tiny", dict(batch=2, io_dtype="bf16", seq_len=300), [299, 5]),
+    ("f32-d256-window", "gemma2_9b_swa", dict(batch=2, kv_dtype="f32", io_dtype="f32", seq_len=300,
+                                            layers=[dict(window=50)]), [299, 5]),
+    ("yarn-qknorm-interleaved", "gptoss_vq8_sink", dict(batch=2, qk_norm=True, norm_w_range=(0.5, 1.5),
+                                                       rope_style="interleaved", seq_len=300), [299, 5]),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_cases(oracle_mod, spec):
+    _, name, over, lens = spec
+    cfg = W.config(name, **over)
+    for layer_cfg in W.layer_configs(cfg):
+        run_and_compare(oracle_mod, layer_cfg, lens)
+
+
+def test_unused_slots_hold_nan(oracle_mod):
+    """Slots beyond each sequence hold NaN; masking must keep them out of every result."""
+    for name, over, lens in (("llama31_8b_decode", dict(batch=3, seq_len=400), [10, 200, 399]),
+                             ("gptoss_vq8_sink", dict(batch=2, seq_len=400), [33, 380]),
+                             ("gemma2_9b_swa", dict(batch=2, seq_len=400, layers=[dict(window=70)]), [399, 90])):
+        cfg = W.layer_configs(W.config(name, **over))[0]
+        run_and_compare(oracle_mod, cfg, lens, fill_unused="nan")
+
+
+def test_bf16_output(oracle_mod):
+    cfg = W.config("llama31_8b_decode", batch=2, seq_len=300, out_dtype="bf16")
+    case = host_case(cfg, lens=[299, 40])
+    a = oracle_arrays(case, oracle_mod)
+    layer = gpu_layer(case)
+    out = layer.step(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda()).float().cpu().numpy()
+    want = oracle_mod.decode_step(cfg, a["q"], a["k_new"], a["v_new"], None, None, None, a["k_cache"],
+                                  a["v_cache"], None, a["seq_lens"])
+    assert np.all(np.abs(out - want) <= TOL_MAX + np.abs(want) * 2.0 ** -8)
+
+
+def test_batch_zero_is_a_no_op():
+    cfg = W.config("llama31_8b_decode", batch=1, seq_len=10)
+    from gqa_attention_kv_qk_gb300.layer import DecodeLayer
+    layer = DecodeLayer(cfg, 1, 64)
+    args = layer.args(None, None, None)
+    args.batch = 0
+    assert B.uaa_decode_attn(layer.desc, args, layer.ws, torch.cuda.current_stream(), check=False) == B.UAA_OK
+
+
+# ------------------------------------------------------------------ device-side checks
+
+def test_capacity_flag_and_no_write(oracle_mod):
+    cfg = W.config("llama31_8b_decode", batch=2, seq_len=60)
+    case = host_case(cfg, lens=[60, 10], cap=64)
+    layer = gpu_layer(case)
+    layer.set_lengths([64, 10])  # sequence 0 is full
+    before = layer.k_cache.clone()
+    args = layer.args(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda(), max_seq_len=62)
+    B.uaa_decode_attn(layer.desc, args, layer.ws, torch.cuda.current_stream())
+    flags = layer.device_status()
+    assert flags & B.UAA_DEVFLAG_CAPACITY
+    assert layer.seq_lens.cpu().tolist() == [64, 11]
+    assert torch.equal(layer.k_cache[0], before[0])
+    assert layer.device_status() == 0  # cleared by the read
+
+
+def test_length_hint_violation_is_flagged():
+    cfg = W.config("llama31_8b_decode", batch=2, seq_len=3000)
+    case = host_case(cfg, lens=[2999, 5])
+    layer = gpu_layer(case)
+    args = layer.args(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda(), max_seq_len=5)
+    B.uaa_decode_attn(layer.desc, args, layer.ws, torch.cuda.current_stream())
+    flags = layer.device_status()
+    assert flags & B.UAA_DEVFLAG_LEN_HINT
+    out = layer.out.cpu()
+    assert torch.isnan(out[0]).all() and torch.isfinite(out[1]).all()
+
+
+# ------------------------------------------------------------------ split partials
+
+@pytest.mark.parametrize("name,over,lens", [
+    ("llama31_8b_decode", dict(batch=2, seq_len=3000), [2999, 700]),
+    ("gptoss_vq8_sink", dict(batch=2, seq_len=3000), [2999, 130]),
+    ("gemma2_9b_swa", dict(batch=2, seq_len=3000, layers=[dict(window=1000)]), [2999, 1500]),
+    ("llama32_1b_tiny", dict(batch=1, seq_len=700), [699]),
+])
+def test_partials_match_oracle_ranges(oracle_mod, name, over, lens):
+    """Each split's partial (normalised row, log-sum-exp) equals the oracle's
+    softmax restricted to the split's key range."""
+    cfg = W.layer_configs(W.config(name, **over))[0]
+    case = host_case(cfg, lens=lens)
+    a = oracle_arrays(case, oracle_mod)
+    layer = gpu_layer(case)
+    lay = layer.layout()
+    dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
+    layer.append(dev["q"], dev["k_new"], dev["v_new"])
+    layer.partial()
+    torch.cuda.synchronize()
+    qr = oracle_mod.append(cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"], a["k_cache"],
+                           a["v_cache"], a["v_scale"], a["seq_lens"])
+    Bn, Hq, D, Hkv = cfg["batch"], cfg["n_q_heads"], cfg["head_dim"], cfg["n_kv_heads"]
+    S, ck = lay.n_splits, lay.chunk_keys
+    ws = layer.ws_tensor
+    o_part = ws[lay.o_part_offset: lay.o_part_offset + Bn * Hq * S * D * 4].view(torch.float32)
+    o_part = o_part.view(Bn, Hq, S, D).cpu().numpy()
+    lse = ws[lay.lse_part_offset: lay.lse_part_offset + Bn * Hq * S * 4].view(torch.float32)
+    lse = lse.view(Bn, Hq, S).cpu().numpy()
+    G = Hq // Hkv
+    checked = 0
+    for b in range(Bn):
+        n = int(a["seq_lens"][b])
+        W_ = cfg.get("window", 0) or 0
+        lo = max(0, n - W_) if W_ else 0
+        t0 = lo // 64
+        for s in range(S):
+            j0, j1 = max(lo, (t0 * 64) + s * ck), min(n, t0 * 64 + (s + 1) * ck)
+            if j1 <= j0:
+                continue
+            for h in range(0, Hq, max(1, Hq // 8)):
+                g = h // G
+                kr = a["k_cache"][b, g]
+                vr = a["v_cache"][b, g]
+                sr = None if a["v_scale"] is None else a["v_scale"][b, g]
+                o, l_nat = oracle_mod.attend_range(cfg, qr[b, h], kr, vr, sr, j0, j1)
+                assert np.max(np.abs(o_part[b, h, s] - o)) <= TOL_MAX
+                assert abs(lse[b, h, s] * math.log(2.0) - l_nat) <= 2e-3 * max(1.0, abs(l_nat))
+                checked += 1
+    assert checked > 0
+
+
+# ------------------------------------------------------------------ full size, sampled
+
+FULL = ["llama32_1b_tiny", "llama31_8b_decode", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(oracle_mod, name):
+    """The workloads at their full sizes, in the launch configuration the benchmark
+    times (one fused uaa_decode_attn call per layer); outputs checked on sampled
+    (sequence, head) rows, cache writes and lengths checked everywhere."""
+    cfg = W.config(name)
+    rng = np.random.default_rng(123)
+    for layer_cfg in W.layer_configs(cfg):
+        case = host_case(layer_cfg)
+        layer = gpu_layer(case)
+        layer.step(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda())
+        out = layer.out.cpu().numpy()
+        a = oracle_arrays(case, oracle_mod)
+        qr = oracle_mod.append(layer_cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"],
+                               a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"])
+        assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
+        assert layer.device_status() == 0
+        Bn, Hq = layer_cfg["batch"], layer_cfg["n_q_heads"]
+        units = sorted({(int(rng.integers(Bn)), int(rng.integers(Hq))) for _ in range(24)} | {(0, 0), (Bn - 1, Hq - 1)})
+        want = oracle_mod.attend(layer_cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"],
+                                 a["seq_lens"], units=units)
+        got = np.stack([out[b, h] for b, h in units])
+        assert_out_close(got, want, name)
+        if layer_cfg["kv_dtype"] == "vq8":
+            pre = case["lens"].numpy()
+            for b in range(Bn):
+                assert np.array_equal(layer.v_cache[b, :, pre[b]].cpu().numpy(), a["v_cache"][b, :, pre[b]])
