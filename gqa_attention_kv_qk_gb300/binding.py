@@ -93,6 +93,7 @@ _SIGS = [
     ("uaa_last_error", ctypes.c_char_p, []),
     ("uaa_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("uaa_abi_version", ctypes.c_int32, []),
+    ("uaa_decode_attn_static", ctypes.c_int, [_P(UaaAttnDesc), _P(UaaStepArgs), ctypes.c_void_p]),
 ]
 
 
@@ -195,6 +196,15 @@ def uaa_device_status(ws, stream=None) -> int:
 
 def uaa_abi_version() -> int:
     return int(lib().uaa_abi_version())
+
+
+UAA_STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def uaa_decode_attn_static(desc, args, stream=None, check=True) -> int:
+    """uaa_decode_attn for callers that cannot allocate device memory: the scratch
+    is the library's built-in UAA_STATIC_SCRATCH_BYTES array (see include/uaa.h)."""
+    return _check(lib().uaa_decode_attn_static(ctypes.byref(desc), ctypes.byref(args), _stream(stream)), check)
 
 
 # ---------------------------------------------------------------- marshalling helpers

@@ -544,3 +544,61 @@ const char* uaa_status_string(uaa_status s)
 int32_t uaa_abi_version(void) { return UAA_ABI_VERSION; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- built-in scratch
+// For callers that cannot allocate device memory: the workspace of
+// uaa_decode_attn_static is this array. In host code the name is only a
+// host-side stand-in, so the device address is looked up once per device
+// (cudaGetSymbolAddress, device current) and handed to the kernels.
+static __device__ __align__(256) unsigned char g_static_scratch[UAA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[64] = {};
+
+uaa_status static_scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(UAA_ERR_UNSUPPORTED, "device index %d is above 63", dev);
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+        g_static_scratch_addr[dev] = p;
+    }
+    *out = g_static_scratch_addr[dev];
+    return UAA_OK;
+}
+
+}  // namespace
+
+extern "C" uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                             cudaStream_t stream)
+{
+    UAA_TRY(check_desc(desc));
+    if (!args) return fail(UAA_ERR_INVALID_ARGUMENT, "args is NULL");
+    const int n_sm = device_sm_count();
+    if (n_sm <= 0) return fail(UAA_ERR_CUDA, "no CUDA device: the SM count query failed");
+    Plan pl{};
+    UAA_TRY(make_plan(desc, args->batch, args->max_seq_len, n_sm, &pl));
+    if (pl.total > (size_t)UAA_STATIC_SCRATCH_BYTES)
+        return fail(UAA_ERR_INVALID_ARGUMENT,
+                    "this step needs %zu bytes of scratch; the built-in scratch of uaa_decode_attn_static "
+                    "holds %zu bytes (pass a workspace to uaa_decode_attn instead)",
+                    pl.total, (size_t)UAA_STATIC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    UAA_TRY(static_scratch_address(&scratch));
+    const uaa_workspace ws{scratch, (size_t)UAA_STATIC_SCRATCH_BYTES};
+    UAA_TRY(check_args(desc, args, &ws, true));
+    if (args->batch == 0) return UAA_OK;
+    // the status word is the only scratch that must start at zero
+    const cudaError_t e = cudaMemsetAsync(static_cast<char*>(scratch) + pl.off_status, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch status word");
+    UAA_TRY(run_append(desc, args, &ws, pl, stream));
+    UAA_TRY(run_partial(desc, args, &ws, pl, stream));
+    return run_combine(desc, args, &ws, pl, stream);
+}

@@ -210,6 +210,35 @@ const char* uaa_status_string(uaa_status status);
 /* UAA_ABI_VERSION of the built library. */
 int32_t uaa_abi_version(void);
 
+/* Bytes of the library's built-in scratch array (see uaa_decode_attn_static). */
+#define UAA_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* uaa_decode_attn without a caller workspace. The pages have no counterpart of
+ * this entry point: it exists for callers that cannot allocate device memory
+ * themselves -- for example a plugin whose host framework owns every device
+ * allocation and forbids direct cudaMalloc, or a latency-bound serving loop that
+ * must never block on the allocator's implicit device synchronisation.
+ *
+ * The split partials, rotated q rows and status word then live in one
+ * file-scope __device__ array of UAA_STATIC_SCRATCH_BYTES (8 MiB) that every
+ * GPU which loads the library holds until the process exits. The caller still
+ * passes every input and output in args; this call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *   - A step whose workspace would exceed UAA_STATIC_SCRATCH_BYTES (see
+ *     uaa_workspace_size) is refused with UAA_ERR_INVALID_ARGUMENT and a message
+ *     giving both sizes; nothing is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *     first call on a device before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents. Each call clears the status word it starts from; device-side
+ *     flags are therefore not reported (a step that breaks max_seq_len still
+ *     writes NaN rows). Calls whose kernels overlap on the GPU (two streams, or
+ *     two threads) race on the array: serialise them.
+ * Results equal uaa_decode_attn's for the same desc and args. */
+uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                  cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
