@@ -48,6 +48,27 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the partial kernel from the committed ncu summary
+    (profiles/partial_tc_<workload>.md), or None when there is none or when the
+    kernel's sources changed since the counters were taken."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", f"partial_tc_{workload}.md")
+    if not os.path.exists(prof):
+        return None
+    text = open(prof).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m_h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
+    if not (m_t and m_h):
+        return None
+    csrc = os.path.join(ROOT, "gqa_attention_kv_qk_gb300", "csrc")
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("partial_tc.cu", "ptx.cuh", "internal.cuh"))
+    if hashlib.sha256(blob).hexdigest()[:16] != m_h.group(1):
+        return None
+    return int(m_t.group(1))
+
+
 # ---------------------------------------------------------------- algorithmic bytes
 
 def _kv_row_bytes(cfg: dict) -> tuple[int, int]:
@@ -368,7 +389,8 @@ def run_uaa(args, world, rank, local) -> dict | None:
         "roofline": {"bound": "hbm", "achieved": round(part_gbs, 2) if part_gbs else None,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(part_gbs / peaks["hbm_gbs"], 4) if part_gbs else None,
-                     "traffic": None, "kernel": "split-K partial", "peak_source": peaks["source"],
+                     "traffic": measured_traffic(name), "kernel": "split-K partial",
+                     "peak_source": peaks["source"],
                      "bytes_per_launch": part_bytes // max(1, n_dec * len(layers)),
                      "mean_launch_us": round(part_s / n_part * 1e6, 2) if n_part else None},
         "e2e": {"value": round(total_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

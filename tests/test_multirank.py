@@ -1,0 +1,69 @@
+"""The N > 1 host logic of bench.py on CPU: two gloo ranks over 127.0.0.1.
+
+The decode path shards by batch with no exchange (replicas), so the only
+cross-rank steps are the barrier, the max of the timed regions and the sum of
+the bytes; rank 0 alone prints, and the reference arm does its work on rank 0
+only while the other ranks exit cleanly.
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank: int, world: int, port: int, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch.distributed as dist
+
+    import bench
+    w, r, local = bench.dist_setup(world)
+    assert (w, r, local) == (world, rank, rank)
+    bench.barrier(w)
+    mx = bench.max_over_ranks(float(rank + 1) * 1.5, w)
+    sm = bench.sum_over_ranks(float(10 * (rank + 1)), w)
+
+    class A:  # reference-arm arguments: rank != 0 must return without work
+        steps, warmup, workload, cpu_budget = 1, 0, "llama32_1b_tiny", 0.1
+    ref = bench.run_reference(A, w, r) if r != 0 else "skipped"
+    q.put((rank, mx, sm, ref))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_and_only_rank0_works():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    codes = [p.exitcode for p in procs]
+    assert codes == [0, 0], codes
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert got[0][1] == pytest.approx(3.0) and got[1][1] == pytest.approx(3.0)   # max over ranks
+    assert got[0][2] == pytest.approx(30.0) and got[1][2] == pytest.approx(30.0)  # sum over ranks
+    assert got[1][3] is None                                                     # rank 1 did no work
+
+
+def test_byte_accounting_counts_visible_keys_once_per_kv_head():
+    import bench
+    cfg = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=64, kv_dtype="bf16", io_dtype="bf16",
+               out_dtype="f32", window=0)
+    assert bench.partial_bytes(cfg, [10, 20]) == (10 + 20) * 2 * (128 + 128)
+    cfg_w = dict(cfg, window=15)
+    assert bench.partial_bytes(cfg_w, [10, 20]) == (10 + 15) * 2 * 256
+    cfg_q = dict(cfg, kv_dtype="vq8")
+    assert bench.partial_bytes(cfg_q, [5]) == 5 * 2 * (128 + 64 + 4)
+    small = 2 * (8 + 4) * 64 * 2 + 2 * 2 * 256 + 2 * 8 * 64 * 4
+    assert bench.decode_step_bytes(cfg, [9, 19]) == bench.partial_bytes(cfg, [10, 20]) + small
