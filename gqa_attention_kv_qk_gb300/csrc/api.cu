@@ -150,8 +150,12 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     long long chunk = (units * max_tiles + target - 1) / target;
     if (chunk < 4) chunk = 4;
     if (chunk > max_tiles) chunk = max_tiles;
+    // the tensor-core kernel reads stages of `mg` tiles: splits hold a multiple of mg
+    const int mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim) / uaa::kTileKeys : 1;
     p.S = (int)((max_tiles + chunk - 1) / chunk);
     p.chunk_tiles = (max_tiles + p.S - 1) / p.S;
+    p.chunk_tiles = (p.chunk_tiles + mg - 1) / mg * mg;
+    p.S = (max_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
 
     const size_t B = (size_t)(batch > 0 ? batch : 0), Hq = d->n_q_heads, D = d->head_dim;
     p.off_status = 0;
@@ -374,17 +378,21 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     } else {
         const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
         const uint64_t D = d->head_dim;
+        const uint32_t tk_rows = (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim);  // box height
         CUtensorMap tk, tv, ts;
-        UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, 64,
+        UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
         if (d->kv_dtype == UAA_DTYPE_VQ8) {
-            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, (uint32_t)D, 64,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, "v_cache codes"));
+            // codes: boxes of 64 rows x min(D, 128) bytes, swizzled like the bf16 boxes so
+            // the kernel's ldmatrix reads on them are free of bank conflicts
+            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, D > 128 ? 128u : (uint32_t)D,
+                              tk_rows, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                              "v_cache codes"));
             UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, a->cache_capacity,
-                              (uint64_t)a->batch * d->n_kv_heads, (uint64_t)a->cache_capacity * 4, 64, 1,
+                              (uint64_t)a->batch * d->n_kv_heads, (uint64_t)a->cache_capacity * 4, tk_rows, 1,
                               CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
         } else {
-            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, 64,
+            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, tk_rows,
                               CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
             ts = tv;  // unused by the bf16 kernel
         }

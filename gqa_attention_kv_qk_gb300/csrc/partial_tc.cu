@@ -1,30 +1,40 @@
 // partial_tc.cu -- split-K decode partial for bf16 and vq8 caches: TMA tile
-// loads into a shared-memory ring, bf16 tensor-core contractions.
+// loads into a shared-memory ring, tensor-core contractions.
 //
 // Work unit: one CTA per (split, kv head x head group, sequence). Every query
 // head of the kv head's group (up to 8 * NHT per CTA) is served from the same
 // K/V tiles, so each tile leaves HBM once per CTA.
 //
 // Warp roles (160 threads):
-//   warp 4 (producer): one lane streams the split's 64-key tiles with 2-D TMA
-//     loads (cp.async.bulk.tensor) into a ring of kStages stages; K and bf16 V
-//     boxes are 64 rows x 128 bytes with the 128-byte swizzle, vq8 codes are
-//     one 64 x D-byte box, vq8 scales one 64-float box. Full / empty mbarriers
-//     hand stages back and forth.
-//   warps 0-3 (consumers): warp w owns keys 16w .. 16w+15 of every tile.
+//   warp 4 (producer): one lane streams the split's keys, TK = 64 MG per stage,
+//     with 2-D TMA loads (cp.async.bulk.tensor) into a ring of kStages stages.
+//     Key and bf16 value boxes are TK rows x 128 bytes with the 128-byte swizzle;
+//     vq8 code boxes are TK rows x min(D, 128) bytes with the 64- or 128-byte
+//     swizzle; vq8 scales are one TK-float box. Full / empty mbarriers pass
+//     stages between the producer and the consumers.
+//   warps 0-3 (consumers): warp w owns keys 16 MG w .. 16 MG (w+1) - 1 of every
+//     stage, as MG groups of 16 keys that share one softmax round (MG = 2 for
+//     head_dim 64, else 1).
 //     S^T (16 keys x 8 heads) = K_tile (16 x D) . Q'^T (D x 8) with mma.m16n8k16
-//     (keys on M, heads on N, no padding of M). The fp32 q' rows are split into
+//     (keys on M, heads on N: no padding of M). The fp32 q' rows are split into
 //     bf16 hi + lo parts, two MMAs each, so the logits keep ~16 significant bits.
-//     Online softmax (log2 domain) runs on the fp32 accumulators; P is split
-//     into bf16 hi + lo, transposed in registers with movmatrix into the B
-//     operand of O^T (D x 8) += V^T (D x 16 keys) . P^T (16 keys x 8 heads),
-//     V^T fragments come from ldmatrix.trans. vq8 codes are widened to bf16
-//     (exact) in a per-warp staging area; the per-key scale is folded into P.
+//     Online softmax (log2 domain) runs on the fp32 accumulators. P is split into
+//     hi + lo parts and moved with movmatrix into the B operand of
+//     O^T (D x 8) += V^T (D x 16 keys) . P^T (16 keys x 8 heads).
+//       bf16 values: V^T fragments come from ldmatrix.trans on the bf16 tile.
+//       vq8 values: ldmatrix.trans runs on the int8 tile itself (a b16 element
+//       is then a pair of adjacent codes), one byte permute and one fp16
+//       subtract per pair widen the codes exactly, and the PV product runs in
+//       fp16. The per-key scale is folded into P; to keep P * scale inside
+//       [0, 1] it is divided by the warp's running maximum scale r, and O is
+//       kept in units of r (a new maximum rescales O as a new logit maximum does).
 //   At the end the four warp states are merged through shared memory and the
 //   CTA writes one normalised partial row and its log2-sum-exp per head.
 //
 // Every wait is bounded (kWaitLimitCycles); a wait that gives up sets
 // UAA_DEVFLAG_TIMEOUT and the CTA unwinds without further waits.
+#include <cuda_fp16.h>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -33,38 +43,50 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kBoxBytes = kTileKeys * 128;  // 64 rows x 128 bytes
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// MG: 16-key groups each consumer warp takes per stage (2 for head_dim 64, where a
+// key costs few bytes and the per-stage softmax work is shared by 32 keys).
+template <int D>
+struct KeyGroups {
+    static constexpr int kMG = D == 64 ? 2 : 1;
+};
+
 template <int D, bool VQ8>
 struct Shape {
-    static constexpr int kBoxes = D / 64;                   // 128-byte column boxes of a bf16 row
-    static constexpr int kKBytes = kTileKeys * D * 2;
-    static constexpr int kVBytes = VQ8 ? kTileKeys * D : kTileKeys * D * 2;
-    static constexpr int kSBytes = VQ8 ? kTileKeys * 4 : 0;
+    static constexpr int kMG = KeyGroups<D>::kMG;
+    static constexpr int kTK = kTileKeys * kMG;             // keys per stage
+    static constexpr int kBoxBytes = kTK * 128;             // kTK rows x 128 bytes
+    static constexpr int kKBoxes = D / 64;                  // 128-byte column boxes of a bf16 row
+    static constexpr int kVBoxes = VQ8 ? (D > 128 ? D / 128 : 1) : D / 64;
+    static constexpr int kKBytes = kTK * D * 2;
+    static constexpr int kVBytes = VQ8 ? kTK * D : kTK * D * 2;
+    static constexpr int kSBytes = VQ8 ? kTK * 4 : 0;
     static constexpr int kStageBytes = round_up(kKBytes + kVBytes + kSBytes, 1024);
     static constexpr int kTxBytes = kKBytes + kVBytes + kSBytes;
-    static constexpr int kStagingWarpBytes = VQ8 ? 16 * D * 2 : 0;  // bf16 copy of 16 rows
-    static constexpr int kStagingBytes = kConsumerWarps * kStagingWarpBytes;
-    static constexpr int kBudget = (D == 256 ? 196608 : 98304) - kStagingBytes;
+    static constexpr int kBudget = D == 256 ? 196608 : 112640;
     static constexpr int kStagesRaw = kBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kStagingBytes + 16 * kStages;
+    static constexpr int kSmemBytes = 1024 + kRingBytes + 16 * kStages;
 };
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in a ring tile: boxes of
-// 64 rows x 128 bytes, chunk index XOR (row mod 8) inside each 128-byte row.
+// Byte offset of 16-byte chunk `chunk` of row `row` in a bf16 stage: boxes of
+// TK rows x 128 bytes, chunk index XOR (row mod 8) inside each 128-byte row.
+template <int TK>
 __device__ __forceinline__ uint32_t tile_off(int row, int chunk)
 {
-    return static_cast<uint32_t>((chunk >> 3) * kBoxBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    return static_cast<uint32_t>((chunk >> 3) * (TK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// Same swizzle for a warp's 16-row staging copy.
-__device__ __forceinline__ uint32_t staging_off(int row, int chunk)
+// The same for an int8 code stage of D-byte rows: D = 64 uses the 64-byte swizzle
+// (chunk XOR ((row / 2) mod 4)), D = 128 and 256 the 128-byte one per 128-byte box.
+template <int D, int TK>
+__device__ __forceinline__ uint32_t code_off(int row, int chunk)
 {
-    return static_cast<uint32_t>((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    if (D == 64) return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+    return static_cast<uint32_t>((chunk >> 3) * (TK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
@@ -81,19 +103,34 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
     lo = pack_bf16(x0 - h0, x1 - h1);
 }
 
-// Four int8 codes -> two bf16x2 words, exactly: byte c + 128 is placed in the
-// mantissa of 2^23 (fp32), 2^23 + 128 is subtracted, and the upper halves of
-// the two fp32 results (integers of magnitude <= 128) are the bf16 values.
-__device__ __forceinline__ void widen_codes(uint32_t w, uint32_t& p01, uint32_t& p23)
+// The same split into fp16 hi + lo parts (values in [0, 1]).
+__device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint32_t& lo)
 {
-    const uint32_t u = w ^ 0x80808080u;
-    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
-    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
-    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
-    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
-    p01 = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-    p23 = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+    __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
 }
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b)
+{
+    __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// A register from ldmatrix.trans on int8 rows holds codes (key k, value d),
+// (k, d+1), (k+1, d), (k+1, d+1) in bytes 0-3. Returns the fp16 pairs
+// [(k, d), (k+1, d)] and [(k, d+1), (k+1, d+1)], exactly: byte c + 128 goes into
+// the mantissa of 1024 (fp16 0x6400) and 1152 (0x6480) is subtracted.
+__device__ __forceinline__ void widen_code_pairs(uint32_t r, uint32_t& d_even, uint32_t& d_odd)
+{
+    const uint32_t u = r ^ 0x80808080u;
+    d_even = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
+    d_odd = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
+}
+
+__device__ __forceinline__ bool key_ok(int k, int lo, int hi) { return k >= lo && k < hi; }
 
 template <int D, bool VQ8, int NHT>
 __global__ void __launch_bounds__(kThreads, (D == 256 ? 1 : 2))
@@ -101,14 +138,15 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_s, const PartialParams p)
 {
     using SH = Shape<D, VQ8>;
-    constexpr int KS = D / 16;     // k-steps of QK, m-tiles of PV
-    constexpr int HC = 8 * NHT;    // head columns of the CTA
+    constexpr int MG = SH::kMG;     // 16-key groups per warp per stage
+    constexpr int TK = SH::kTK;     // keys per stage
+    constexpr int KS = D / 16;      // k-steps of QK, m-tiles of PV
+    constexpr int HC = 8 * NHT;     // head columns of the CTA
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const uint32_t staging = base + SH::kRingBytes;
-    const uint32_t bar_full = staging + SH::kStagingBytes;
+    const uint32_t bar_full = base + SH::kRingBytes;
     const uint32_t bar_empty = bar_full + 8 * SH::kStages;
 
     const int sigma = blockIdx.x;
@@ -126,6 +164,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int tb = t0 + sigma * p.chunk_tiles;
     if (hi <= lo || tb >= t1) return;  // uniform over the CTA: this split has no keys
     const int n_tiles = min(tb + p.chunk_tiles, t1) - tb;
+    const int n_stages = (n_tiles + MG - 1) / MG;  // the host keeps chunk_tiles a multiple of MG
     const int h0 = kvh * p.G + hg * HC;
     const int nh = min(HC, p.G - hg * HC);
 
@@ -147,7 +186,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int head_row = b * p.Hkv + kvh;
             const int row0 = head_row * p.cap;
             bool ok = true;
-            for (int i = 0; i < n_tiles && ok; ++i) {
+            for (int i = 0; i < n_stages && ok; ++i) {
                 const int s = i % SH::kStages;
                 if (i >= SH::kStages &&
                     !ptx::mbar_wait(bar_empty + 8 * s, ((i / SH::kStages) & 1) ^ 1, kWaitLimitCycles)) {
@@ -158,22 +197,24 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint32_t st = base + s * SH::kStageBytes;
                 const uint32_t bar = bar_full + 8 * s;
                 ptx::mbar_arrive_expect_tx(bar, SH::kTxBytes);
-                const int key = (tb + i) * kTileKeys;
+                const int key = (tb + MG * i) * kTileKeys;
                 const int y = row0 + key;
 #pragma unroll
-                for (int c = 0; c < SH::kBoxes; ++c) ptx::tma_load_2d(st + c * kBoxBytes, &tm_k, c * 64, y, bar);
+                for (int c = 0; c < SH::kKBoxes; ++c) ptx::tma_load_2d(st + c * SH::kBoxBytes, &tm_k, c * 64, y, bar);
                 if (VQ8) {
-                    ptx::tma_load_2d(st + SH::kKBytes, &tm_v, 0, y, bar);
+#pragma unroll
+                    for (int c = 0; c < SH::kVBoxes; ++c)
+                        ptx::tma_load_2d(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 128, y, bar);
                     ptx::tma_load_2d(st + SH::kKBytes + SH::kVBytes, &tm_s, key, head_row, bar);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < SH::kBoxes; ++c)
-                        ptx::tma_load_2d(st + SH::kKBytes + c * kBoxBytes, &tm_v, c * 64, y, bar);
+                    for (int c = 0; c < SH::kVBoxes; ++c)
+                        ptx::tma_load_2d(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 64, y, bar);
                 }
             }
             // Copies in flight land before the CTA may exit (bounded).
-            const int first = n_tiles > SH::kStages ? n_tiles - SH::kStages : 0;
-            for (int i = first; i < n_tiles && ok; ++i)
+            const int first = n_stages > SH::kStages ? n_stages - SH::kStages : 0;
+            for (int i = first; i < n_stages && ok; ++i)
                 ok = ptx::mbar_wait(bar_full + 8 * (i % SH::kStages), (i / SH::kStages) & 1, kWaitLimitCycles);
         }
         return;
@@ -206,65 +247,93 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
         for (int mi = 0; mi < KS; ++mi) o[nt][mi][0] = o[nt][mi][1] = o[nt][mi][2] = o[nt][mi][3] = 0.f;
     }
+    float r_scale = 0.f;  // vq8: the warp's running maximum value scale (O is kept in units of it)
 
-    const int key_w = 16 * warp;
+    const int key_w = 16 * MG * warp;  // this warp's first key in a stage
     const float cap2 = p.softcap_log2e;
-    const uint32_t my_staging = staging + warp * SH::kStagingWarpBytes;
     // ldmatrix lane roles: matrix q = lane / 8, row r = lane % 8 of that matrix.
     const int lq = lane >> 3, lr = lane & 7;
     bool failed = false;
 
-    for (int i = 0; i < n_tiles; ++i) {
+    for (int i = 0; i < n_stages; ++i) {
         const int s = i % SH::kStages;
         if (!failed && !ptx::mbar_wait(bar_full + 8 * s, (i / SH::kStages) & 1, kWaitLimitCycles)) {
             failed = true;
             if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
         }
-        const int key0 = (tb + i) * kTileKeys + key_w;  // absolute slot of this warp's first key
-        if (!failed && key0 < hi && key0 + 16 > lo) {
-            const bool whole = key0 >= lo && key0 + 16 <= hi;
+        const int kbase = (tb + MG * i) * kTileKeys + key_w;  // absolute slot of this warp's first key
+        if (!failed && kbase < hi && kbase + 16 * MG > lo) {
+            const bool whole = kbase >= lo && kbase + 16 * MG <= hi;
             const uint32_t st = base + s * SH::kStageBytes;
 
-            // S^T = K . Q'^T (keys x heads)
-            float sacc[NHT][4];
+            // S^T = K . Q'^T (keys x heads), one accumulator per 16-key group
+            float sacc[MG][NHT][4];
 #pragma unroll
-            for (int nt = 0; nt < NHT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+            for (int mg = 0; mg < MG; ++mg)
+#pragma unroll
+                for (int nt = 0; nt < NHT; ++nt) sacc[mg][nt][0] = sacc[mg][nt][1] = sacc[mg][nt][2] = sacc[mg][nt][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-                uint32_t a[4];
-                ptx::ldsm_x4(a, st + tile_off(key_w + lr + 8 * (lq & 1), 2 * kk + (lq >> 1)));
 #pragma unroll
-                for (int nt = 0; nt < NHT; ++nt) {
-                    ptx::mma_bf16(sacc[nt], a, qhi[nt][kk][0], qhi[nt][kk][1]);
-                    ptx::mma_bf16(sacc[nt], a, qlo[nt][kk][0], qlo[nt][kk][1]);
+                for (int mg = 0; mg < MG; ++mg) {
+                    uint32_t a[4];
+                    ptx::ldsm_x4(a, st + tile_off<TK>(key_w + 16 * mg + lr + 8 * (lq & 1), 2 * kk + (lq >> 1)));
+#pragma unroll
+                    for (int nt = 0; nt < NHT; ++nt) {
+                        ptx::mma_bf16(sacc[mg][nt], a, qhi[nt][kk][0], qhi[nt][kk][1]);
+                        ptx::mma_bf16(sacc[mg][nt], a, qlo[nt][kk][0], qlo[nt][kk][1]);
+                    }
                 }
             }
 
-            // online softmax; this thread holds keys g, g+8 and heads 2t, 2t+1
-            bool vg = true, vg8 = true;
-            if (!whole) {
-                vg = key0 + g >= lo && key0 + g < hi;
-                vg8 = key0 + g + 8 >= lo && key0 + g + 8 < hi;
+            // this thread holds keys 16 mg + g and 16 mg + g + 8, heads 2t and 2t + 1
+            bool vg[MG], vg8[MG];
+#pragma unroll
+            for (int mg = 0; mg < MG; ++mg) {
+                vg[mg] = whole || key_ok(kbase + 16 * mg + g, lo, hi);
+                vg8[mg] = whole || key_ok(kbase + 16 * mg + g + 8, lo, hi);
             }
-            float sc_g = 1.f, sc_g8 = 1.f;
-            if (VQ8) {
-                const float* scl = reinterpret_cast<const float*>(base_ptr + s * SH::kStageBytes + SH::kKBytes + SH::kVBytes);
-                sc_g = scl[key_w + g];
-                sc_g8 = scl[key_w + g + 8];
+            float w_g[MG], w_g8[MG], r_ratio = 1.f;
+            if (VQ8) {  // per-key scale relative to the running maximum; masked keys get 0
+                const float* scl = reinterpret_cast<const float*>(base_ptr + s * SH::kStageBytes + SH::kKBytes +
+                                                                  SH::kVBytes);
+                float smax = 0.f;
+#pragma unroll
+                for (int mg = 0; mg < MG; ++mg) {
+                    w_g[mg] = vg[mg] ? scl[key_w + 16 * mg + g] : 0.f;
+                    w_g8[mg] = vg8[mg] ? scl[key_w + 16 * mg + g + 8] : 0.f;
+                    smax = fmaxf(smax, fmaxf(w_g[mg], w_g8[mg]));
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
+                const float r_new = fmaxf(r_scale, smax);
+                const float inv = r_new > 0.f ? ptx::rcp(r_new) : 0.f;
+                r_ratio = r_new > 0.f ? r_scale * inv : 1.f;
+#pragma unroll
+                for (int mg = 0; mg < MG; ++mg) {
+                    w_g[mg] *= inv;
+                    w_g8[mg] *= inv;
+                }
+                r_scale = r_new;
             }
-            uint32_t bph[NHT][2], bpl[NHT][2];
+
+            float x[MG][NHT][4], f[NHT][2];
+            bool rescale = false;
 #pragma unroll
             for (int nt = 0; nt < NHT; ++nt) {
-                float x0 = sacc[nt][0], x1 = sacc[nt][1], x2 = sacc[nt][2], x3 = sacc[nt][3];
-                if (cap2 > 0.f) {
-                    x0 = tanhf(x0) * cap2;
-                    x1 = tanhf(x1) * cap2;
-                    x2 = tanhf(x2) * cap2;
-                    x3 = tanhf(x3) * cap2;
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int mg = 0; mg < MG; ++mg) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float v = sacc[mg][nt][e];
+                        if (cap2 > 0.f) v = tanhf(v) * cap2;
+                        if (!((e < 2) ? vg[mg] : vg8[mg])) v = -INFINITY;
+                        x[mg][nt][e] = v;
+                    }
+                    mx0 = fmaxf(mx0, fmaxf(x[mg][nt][0], x[mg][nt][2]));
+                    mx1 = fmaxf(mx1, fmaxf(x[mg][nt][1], x[mg][nt][3]));
                 }
-                if (!vg) x0 = x1 = -INFINITY;
-                if (!vg8) x2 = x3 = -INFINITY;
-                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -273,87 +342,103 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
                 const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
                 const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float al0 = exp2f(m[nt][0] - mu0), al1 = exp2f(m[nt][1] - mu1);
-                float p0 = exp2f(x0 - mu0), p1 = exp2f(x1 - mu1);
-                float p2 = exp2f(x2 - mu0), p3 = exp2f(x3 - mu1);
-                l[nt][0] = l[nt][0] * al0 + p0 + p2;
-                l[nt][1] = l[nt][1] * al1 + p1 + p3;
+                const float al0 = ptx::ex2(m[nt][0] - mu0), al1 = ptx::ex2(m[nt][1] - mu1);
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int mg = 0; mg < MG; ++mg) {
+                    x[mg][nt][0] = ptx::ex2(x[mg][nt][0] - mu0);
+                    x[mg][nt][1] = ptx::ex2(x[mg][nt][1] - mu1);
+                    x[mg][nt][2] = ptx::ex2(x[mg][nt][2] - mu0);
+                    x[mg][nt][3] = ptx::ex2(x[mg][nt][3] - mu1);
+                    ls0 += x[mg][nt][0] + x[mg][nt][2];
+                    ls1 += x[mg][nt][1] + x[mg][nt][3];
+                }
+                l[nt][0] = l[nt][0] * al0 + ls0;
+                l[nt][1] = l[nt][1] * al1 + ls1;
                 m[nt][0] = mn0;
                 m[nt][1] = mn1;
+                f[nt][0] = al0 * r_ratio;
+                f[nt][1] = al1 * r_ratio;
+                rescale |= f[nt][0] != 1.f || f[nt][1] != 1.f;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int mi = 0; mi < KS; ++mi) {
-                    o[nt][mi][0] *= al0;
-                    o[nt][mi][1] *= al1;
-                    o[nt][mi][2] *= al0;
-                    o[nt][mi][3] *= al1;
-                }
-                if (VQ8) {  // fold the per-key scale into P; masked keys may hold any bits
-                    p0 = vg ? p0 * sc_g : 0.f;
-                    p1 = vg ? p1 * sc_g : 0.f;
-                    p2 = vg8 ? p2 * sc_g8 : 0.f;
-                    p3 = vg8 ? p3 * sc_g8 : 0.f;
-                }
-                uint32_t h01, l01, h23, l23;
-                split_bf16(p0, p1, h01, l01);  // key g, heads 2t, 2t+1
-                split_bf16(p2, p3, h23, l23);  // key g+8
-                bph[nt][0] = ptx::movmatrix_trans(h01);
-                bph[nt][1] = ptx::movmatrix_trans(h23);
-                bpl[nt][0] = ptx::movmatrix_trans(l01);
-                bpl[nt][1] = ptx::movmatrix_trans(l23);
+                for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+                    for (int mi = 0; mi < KS; ++mi) {
+                        o[nt][mi][0] *= f[nt][0];
+                        o[nt][mi][1] *= f[nt][1];
+                        o[nt][mi][2] *= f[nt][0];
+                        o[nt][mi][3] *= f[nt][1];
+                    }
             }
 
-            if (VQ8) {
-                // widen this warp's 16 rows of codes into the bf16 staging copy
-                const int r = lane >> 1, half = lane & 1;
-                const uint8_t* src = base_ptr + s * SH::kStageBytes + SH::kKBytes +
-                                     static_cast<size_t>(key_w + r) * D + half * (D / 2);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * c);
-                    uint4 lo4, hi4;
-                    widen_codes(w.x, lo4.x, lo4.y);
-                    widen_codes(w.y, lo4.z, lo4.w);
-                    widen_codes(w.z, hi4.x, hi4.y);
-                    widen_codes(w.w, hi4.z, hi4.w);
-                    const int oc = half * (D / 16) + 2 * c;
-                    uint8_t* stg = base_ptr + (my_staging - base);
-                    *reinterpret_cast<uint4*>(stg + staging_off(r, oc)) = lo4;
-                    *reinterpret_cast<uint4*>(stg + staging_off(r, oc + 1)) = hi4;
-                }
-                __syncwarp();
-            }
-
-            // key-validity masks for V^T fragments: registers 0,1 hold keys 2t, 2t+1;
-            // registers 2,3 hold keys 2t+8, 2t+9 (lower half = lower key)
-            uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
-            if (!VQ8 && !whole) {
-                const int k = key0 + 2 * t;
-                m01 = ((k >= lo && k < hi) ? 0x0000ffffu : 0u) | ((k + 1 >= lo && k + 1 < hi) ? 0xffff0000u : 0u);
-                m89 = ((k + 8 >= lo && k + 8 < hi) ? 0x0000ffffu : 0u) |
-                      ((k + 9 >= lo && k + 9 < hi) ? 0xffff0000u : 0u);
-            }
-
-            // O^T += V^T . P^T
-#pragma unroll
-            for (int mi = 0; mi < KS; ++mi) {
-                uint32_t a[4];
-                const int row = lr + 8 * (lq >> 1);
-                const int chunk = 2 * mi + (lq & 1);
-                if (VQ8)
-                    ptx::ldsm_x4_trans(a, my_staging + staging_off(row, chunk));
-                else
-                    ptx::ldsm_x4_trans(a, st + SH::kKBytes + tile_off(key_w + row, chunk));
-                a[0] &= m01;
-                a[1] &= m01;
-                a[2] &= m89;
-                a[3] &= m89;
+            for (int mg = 0; mg < MG; ++mg) {
+                uint32_t bph[NHT][2], bpl[NHT][2];
 #pragma unroll
                 for (int nt = 0; nt < NHT; ++nt) {
-                    ptx::mma_bf16(o[nt][mi], a, bph[nt][0], bph[nt][1]);
-                    ptx::mma_bf16(o[nt][mi], a, bpl[nt][0], bpl[nt][1]);
+                    uint32_t h01, l01, h23, l23;
+                    if (VQ8) {
+                        split_f16(x[mg][nt][0] * w_g[mg], x[mg][nt][1] * w_g[mg], h01, l01);     // key g
+                        split_f16(x[mg][nt][2] * w_g8[mg], x[mg][nt][3] * w_g8[mg], h23, l23);   // key g+8
+                    } else {
+                        split_bf16(x[mg][nt][0], x[mg][nt][1], h01, l01);
+                        split_bf16(x[mg][nt][2], x[mg][nt][3], h23, l23);
+                    }
+                    bph[nt][0] = ptx::movmatrix_trans(h01);
+                    bph[nt][1] = ptx::movmatrix_trans(h23);
+                    bpl[nt][0] = ptx::movmatrix_trans(l01);
+                    bpl[nt][1] = ptx::movmatrix_trans(l23);
+                }
+                const int krow = key_w + 16 * mg;  // this group's first row in the stage
+                if (VQ8) {
+                    // O^T += V^T . P^T straight from the int8 stage: one ldmatrix.x4.trans covers
+                    // 16 keys x 32 values = m-tiles 2j (values 32j .. 32j+15) and 2j+1; in m-tile
+                    // mi row g holds value 16 mi + 2g and row g + 8 holds 16 mi + 2g + 1.
+                    const uint32_t vst = st + SH::kKBytes;
+#pragma unroll
+                    for (int j = 0; j < D / 32; ++j) {
+                        uint32_t r[4];
+                        ptx::ldsm_x4_trans(r, vst + code_off<D, TK>(krow + lr + 8 * (lq >> 1), 2 * j + (lq & 1)));
+                        uint32_t a[4], c[4];
+                        widen_code_pairs(r[0], a[0], a[1]);  // keys 2t, 2t+1; values 32j + 2g, +1
+                        widen_code_pairs(r[2], a[2], a[3]);  // keys 2t+8, 2t+9
+                        widen_code_pairs(r[1], c[0], c[1]);  // values 32j + 16 + 2g, +1
+                        widen_code_pairs(r[3], c[2], c[3]);
+#pragma unroll
+                        for (int nt = 0; nt < NHT; ++nt) {
+                            ptx::mma_f16(o[nt][2 * j], a, bph[nt][0], bph[nt][1]);
+                            ptx::mma_f16(o[nt][2 * j], a, bpl[nt][0], bpl[nt][1]);
+                            ptx::mma_f16(o[nt][2 * j + 1], c, bph[nt][0], bph[nt][1]);
+                            ptx::mma_f16(o[nt][2 * j + 1], c, bpl[nt][0], bpl[nt][1]);
+                        }
+                    }
+                } else {
+                    // key-validity masks for V^T fragments: registers 0,1 hold keys 2t, 2t+1;
+                    // registers 2,3 hold keys 2t+8, 2t+9 (lower half = lower key)
+                    uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+                    if (!whole) {
+                        const int k = kbase + 16 * mg + 2 * t;
+                        m01 = (key_ok(k, lo, hi) ? 0x0000ffffu : 0u) | (key_ok(k + 1, lo, hi) ? 0xffff0000u : 0u);
+                        m89 = (key_ok(k + 8, lo, hi) ? 0x0000ffffu : 0u) | (key_ok(k + 9, lo, hi) ? 0xffff0000u : 0u);
+                    }
+#pragma unroll
+                    for (int mi = 0; mi < KS; ++mi) {
+                        uint32_t a[4];
+                        ptx::ldsm_x4_trans(a, st + SH::kKBytes + tile_off<TK>(krow + lr + 8 * (lq >> 1), 2 * mi + (lq & 1)));
+                        a[0] &= m01;
+                        a[1] &= m01;
+                        a[2] &= m89;
+                        a[3] &= m89;
+#pragma unroll
+                        for (int nt = 0; nt < NHT; ++nt) {
+                            ptx::mma_bf16(o[nt][mi], a, bph[nt][0], bph[nt][1]);
+                            ptx::mma_bf16(o[nt][mi], a, bpl[nt][0], bpl[nt][1]);
+                        }
+                    }
                 }
             }
-            if (VQ8) __syncwarp();
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
@@ -381,6 +466,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 red_l[warp * HC + nt * 8 + 2 * t + j] = l[nt][j];
             }
     }
+    const float o_unit = VQ8 ? r_scale : 1.f;
 #pragma unroll
     for (int nt = 0; nt < NHT; ++nt)
 #pragma unroll
@@ -388,8 +474,8 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int hc = nt * 8 + 2 * t + (k & 1);
-                const int d = 16 * mi + g + 8 * (k >> 1);
-                red_o[(warp * HC + hc) * OS + d] = o[nt][mi][k];
+                const int d = VQ8 ? 16 * mi + 2 * g + (k >> 1) : 16 * mi + g + 8 * (k >> 1);
+                red_o[(warp * HC + hc) * OS + d] = o[nt][mi][k] * o_unit;
             }
     ptx::named_barrier_sync(1, kConsumerWarps * 32);
 
@@ -403,9 +489,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const float mw = red_m[w * HC + hc];
-                const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                L += red_l[w * HC + hc] * f;
-                acc += red_o[(w * HC + hc) * OS + d] * f;
+                const float fw = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                L += red_l[w * HC + hc] * fw;
+                acc += red_o[(w * HC + hc) * OS + d] * fw;
             }
         }
         const size_t row = (static_cast<size_t>(b) * p.Hq + h0 + hc) * p.S + sigma;
@@ -424,10 +510,10 @@ cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUte
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 31 && !(configured_device_mask & (1 << dev))) {
+    if (dev >= 31 || !(configured_device_mask & (1 << dev))) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmemBytes);
         if (e != cudaSuccess) return e;
-        configured_device_mask |= 1 << dev;
+        if (dev < 31) configured_device_mask |= 1 << dev;
     }
     const dim3 grid(p.S, p.Hkv * p.head_groups, p.B);
     kern<<<grid, kThreads, SH::kSmemBytes, s>>>(tk, tv, ts, p);
@@ -435,6 +521,8 @@ cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUte
 }
 
 }  // namespace
+
+int partial_tc_keys_per_stage(int D) { return D == 64 ? KeyGroups<64>::kMG * kTileKeys : kTileKeys; }
 
 size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles)
 {
