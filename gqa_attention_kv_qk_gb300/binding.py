@@ -59,10 +59,13 @@ class UaaWorkspace(ctypes.Structure):
 
 
 class UaaWorkspaceLayout(ctypes.Structure):
-    _fields_ = [("n_splits", ctypes.c_int32), ("chunk_keys", ctypes.c_int32),
+    _fields_ = [("n_ctas", ctypes.c_int32), ("stage_keys", ctypes.c_int32),
                 ("heads_per_cta", ctypes.c_int32), ("kernel", ctypes.c_int32),
+                ("n_slices", ctypes.c_int32), ("slice_batch", ctypes.c_int32),
                 ("status_offset", ctypes.c_size_t), ("q_rot_offset", ctypes.c_size_t),
-                ("o_part_offset", ctypes.c_size_t), ("lse_part_offset", ctypes.c_size_t),
+                ("prefix_offset", ctypes.c_size_t), ("rec_lse_offset", ctypes.c_size_t),
+                ("rec_o_offset", ctypes.c_size_t), ("prefix_stride", ctypes.c_size_t),
+                ("rec_lse_stride", ctypes.c_size_t), ("rec_o_stride", ctypes.c_size_t),
                 ("total_bytes", ctypes.c_size_t)]
 
 

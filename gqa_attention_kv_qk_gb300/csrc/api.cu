@@ -97,12 +97,15 @@ uaa_status check_desc(const uaa_attn_desc* d)
 struct Plan {
     int G;
     int kernel;          // 0 CUDA-core, 1 tensor-core
-    int heads_per_cta;
-    int head_groups;
-    int n_head_tiles;
-    int chunk_tiles;
-    int S;
-    size_t off_status, off_qrot, off_opart, off_lse, total;
+    int heads_per_cta;   // query heads of one unit
+    int head_groups;     // units per kv head
+    int n_head_tiles;    // 8-head column tiles of the tensor-core kernel
+    int mg;              // 64-key tiles per ring stage
+    int n_ctas;          // P: persistent CTAs of the partial kernel
+    int slice;           // sequences per partial launch
+    int n_slices;
+    size_t off_status, off_qrot, off_prefix, off_rec_lse, off_rec_o, total;
+    size_t prefix_stride, rec_lse_stride, rec_o_stride;  // bytes per slice
 };
 
 int device_sm_count()
@@ -117,9 +120,12 @@ int device_sm_count()
     return n;
 }
 
-// The split count comes from the longest visible range and the SM count: the
-// key tiles of all (sequence, kv head, head group) units are cut into chunks so
-// that about three waves of resident CTAs cover them, at least four tiles a chunk.
+// Geometry of a step. The partial kernels are persistent: P = SMs x resident CTAs
+// (4 for the CUDA-core kernel, 2 for the tensor-core kernel, 1 at head_dim 256),
+// each attending one contiguous range of all units' key stages (the stream-K
+// partition in internal.cuh), so the split needs no length bound. Batches above
+// kMaxSliceBatch sequences are cut into slices (one partial + combine launch each)
+// because a CTA keeps the slice's stage prefix in shared memory.
 uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, Plan* pl)
 {
     UAA_TRY(check_desc(d));
@@ -129,10 +135,7 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     Plan p{};
     p.G = d->n_q_heads / d->n_kv_heads;
     p.kernel = d->kv_dtype == UAA_DTYPE_F32 ? 0 : 1;
-    if (p.kernel == 0) {
-        p.heads_per_cta = 8;
-        p.n_head_tiles = 1;
-    } else if (d->head_dim == 256 || p.G <= 8) {
+    if (p.kernel == 0 || d->head_dim == 256 || p.G <= 8) {
         p.heads_per_cta = 8;
         p.n_head_tiles = 1;
     } else {
@@ -140,29 +143,23 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
         p.n_head_tiles = 2;
     }
     p.head_groups = (p.G + p.heads_per_cta - 1) / p.heads_per_cta;
-
-    long long max_keys = (long long)max_len + 1;
-    if (d->window > 0 && d->window < max_keys) max_keys = d->window;
-    const int max_tiles = (int)((max_keys + uaa::kTileKeys - 1) / uaa::kTileKeys) + (d->window > 0 ? 1 : 0);
-    const long long units = (long long)(batch > 0 ? batch : 1) * d->n_kv_heads * p.head_groups;
+    p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim) / uaa::kTileKeys : 1;
     const int per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
-    const long long target = (long long)n_sm * per_sm * 3;
-    long long chunk = (units * max_tiles + target - 1) / target;
-    if (chunk < 4) chunk = 4;
-    if (chunk > max_tiles) chunk = max_tiles;
-    // the tensor-core kernel reads stages of `mg` tiles: splits hold a multiple of mg
-    const int mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim) / uaa::kTileKeys : 1;
-    p.S = (int)((max_tiles + chunk - 1) / chunk);
-    p.chunk_tiles = (max_tiles + p.S - 1) / p.S;
-    p.chunk_tiles = (p.chunk_tiles + mg - 1) / mg * mg;
-    p.S = (max_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+    p.n_ctas = n_sm * per_sm;
+    p.slice = batch < uaa::kMaxSliceBatch ? (batch > 0 ? batch : 1) : uaa::kMaxSliceBatch;
+    p.n_slices = batch > 0 ? (batch + p.slice - 1) / p.slice : 0;
 
     const size_t B = (size_t)(batch > 0 ? batch : 0), Hq = d->n_q_heads, D = d->head_dim;
+    const size_t HC = (size_t)p.heads_per_cta, P = (size_t)p.n_ctas;
+    p.prefix_stride = align256(((size_t)p.slice + 1) * 4);
+    p.rec_lse_stride = align256(2 * P * HC * 4);
+    p.rec_o_stride = align256(2 * P * HC * D * 4);
     p.off_status = 0;
     p.off_qrot = 256;
-    p.off_opart = p.off_qrot + align256(B * Hq * D * 4);
-    p.off_lse = p.off_opart + align256(B * Hq * p.S * D * 4);
-    p.total = p.off_lse + align256(B * Hq * p.S * 4);
+    p.off_prefix = p.off_qrot + align256(B * Hq * D * 4);
+    p.off_rec_lse = p.off_prefix + p.n_slices * p.prefix_stride;
+    p.off_rec_o = p.off_rec_lse + p.n_slices * p.rec_lse_stride;
+    p.total = p.off_rec_o + p.n_slices * p.rec_o_stride;
     *pl = p;
     return UAA_OK;
 }
@@ -350,40 +347,17 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
                        cudaStream_t s)
 {
     if (a->batch == 0) return UAA_OK;
-    uaa::PartialParams p{};
-    p.B = a->batch;
-    p.Hq = d->n_q_heads;
-    p.Hkv = d->n_kv_heads;
-    p.D = d->head_dim;
-    p.G = pl.G;
-    p.heads_per_cta = pl.heads_per_cta;
-    p.head_groups = pl.head_groups;
-    p.cap = a->cache_capacity;
-    p.window = d->window;
-    p.S = pl.S;
-    p.chunk_tiles = pl.chunk_tiles;
-    p.softcap_log2e = d->softcap > 0.f ? d->softcap * uaa::kLog2e : 0.f;
     char* w = static_cast<char*>(ws->ptr);
-    p.q_prime = reinterpret_cast<const float*>(w + pl.off_qrot);
-    p.k_cache = a->k_cache;
-    p.v_cache = a->v_cache;
-    p.v_scale = a->v_scale;
-    p.seq_lens = a->seq_lens;
-    p.o_part = reinterpret_cast<float*>(w + pl.off_opart);
-    p.lse_part = reinterpret_cast<float*>(w + pl.off_lse);
-    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
-    cudaError_t e;
-    if (pl.kernel == 0) {
-        e = uaa::launch_partial_simt(p, s);
-    } else {
+    const size_t D = d->head_dim, Hq = d->n_q_heads;
+    const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
+    CUtensorMap tk, tv, ts;
+    if (pl.kernel == 1) {
         const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
-        const uint64_t D = d->head_dim;
         const uint32_t tk_rows = (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim);  // box height
-        CUtensorMap tk, tv, ts;
         UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
         if (d->kv_dtype == UAA_DTYPE_VQ8) {
-            // codes: boxes of 64 rows x min(D, 128) bytes, swizzled like the bf16 boxes so
+            // codes: boxes of tk_rows x min(D, 128) bytes, swizzled like the bf16 boxes so
             // the kernel's ldmatrix reads on them are free of bank conflicts
             UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, D > 128 ? 128u : (uint32_t)D,
                               tk_rows, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -396,34 +370,76 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
                               CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
             ts = tv;  // unused by the bf16 kernel
         }
-        e = uaa::launch_partial_tc(p, tk, tv, ts, d->kv_dtype, pl.n_head_tiles, s);
     }
-    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "partial kernel launch");
+    for (int sl = 0; sl < pl.n_slices; ++sl) {
+        const int b0 = sl * pl.slice;
+        const int nb = a->batch - b0 < pl.slice ? a->batch - b0 : pl.slice;
+        uaa::PartialParams p{};
+        p.B = nb;
+        p.Hq = d->n_q_heads;
+        p.Hkv = d->n_kv_heads;
+        p.D = d->head_dim;
+        p.G = pl.G;
+        p.b_off = b0;
+        p.heads_per_cta = pl.heads_per_cta;
+        p.head_groups = pl.head_groups;
+        p.cap = a->cache_capacity;
+        p.window = d->window;
+        p.mg = pl.mg;
+        p.softcap_log2e = d->softcap > 0.f ? d->softcap * uaa::kLog2e : 0.f;
+        p.q_prime = reinterpret_cast<const float*>(w + pl.off_qrot) + (size_t)b0 * Hq * D;
+        p.k_cache = a->k_cache;
+        p.v_cache = a->v_cache;
+        p.v_scale = a->v_scale;
+        p.seq_lens = a->seq_lens + b0;
+        p.prefix = reinterpret_cast<int*>(w + pl.off_prefix + sl * pl.prefix_stride);
+        p.rec_lse = reinterpret_cast<float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
+        p.rec_o = reinterpret_cast<float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
+        p.sink = d->has_sink ? a->sink : nullptr;
+        p.out = static_cast<char*>(a->out) + (size_t)b0 * Hq * D * out_elem;
+        p.out_dtype = d->out_dtype;
+        p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+        const cudaError_t e = pl.kernel == 0
+                                  ? uaa::launch_partial_simt(p, pl.n_ctas, s)
+                                  : uaa::launch_partial_tc(p, tk, tv, ts, d->kv_dtype, pl.n_head_tiles, pl.n_ctas, s);
+        if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
+    }
+    return UAA_OK;
 }
 
 uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
                        cudaStream_t s)
 {
     if (a->batch == 0) return UAA_OK;
-    uaa::CombineParams p{};
-    p.B = a->batch;
-    p.Hq = d->n_q_heads;
-    p.Hkv = d->n_kv_heads;
-    p.D = d->head_dim;
-    p.G = pl.G;
-    p.window = d->window;
-    p.S = pl.S;
-    p.chunk_tiles = pl.chunk_tiles;
-    p.out_dtype = d->out_dtype;
-    p.sink = d->has_sink ? a->sink : nullptr;
-    p.seq_lens = a->seq_lens;
     char* w = static_cast<char*>(ws->ptr);
-    p.o_part = reinterpret_cast<const float*>(w + pl.off_opart);
-    p.lse_part = reinterpret_cast<const float*>(w + pl.off_lse);
-    p.out = a->out;
-    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
-    const cudaError_t e = uaa::launch_combine(p, s);
-    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "combine kernel launch");
+    const size_t D = d->head_dim, Hq = d->n_q_heads;
+    const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
+    for (int sl = 0; sl < pl.n_slices; ++sl) {
+        const int b0 = sl * pl.slice;
+        const int nb = a->batch - b0 < pl.slice ? a->batch - b0 : pl.slice;
+        uaa::CombineParams p{};
+        p.B = nb;
+        p.Hq = d->n_q_heads;
+        p.Hkv = d->n_kv_heads;
+        p.D = d->head_dim;
+        p.G = pl.G;
+        p.heads_per_cta = pl.heads_per_cta;
+        p.head_groups = pl.head_groups;
+        p.window = d->window;
+        p.mg = pl.mg;
+        p.P = pl.n_ctas;
+        p.out_dtype = d->out_dtype;
+        p.sink = d->has_sink ? a->sink : nullptr;
+        p.seq_lens = a->seq_lens + b0;
+        p.prefix = reinterpret_cast<const int*>(w + pl.off_prefix + sl * pl.prefix_stride);
+        p.rec_lse = reinterpret_cast<const float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
+        p.rec_o = reinterpret_cast<const float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
+        p.out = static_cast<char*>(a->out) + (size_t)b0 * Hq * D * out_elem;
+        p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+        const cudaError_t e = uaa::launch_combine(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    }
+    return UAA_OK;
 }
 
 }  // namespace
@@ -479,7 +495,7 @@ int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq
     Plan pl{};
     if (n_sm <= 0) n_sm = device_sm_count();
     if (make_plan(desc, batch, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
-    return pl.S;
+    return pl.n_ctas;
 }
 
 uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm,
@@ -489,14 +505,20 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, in
     Plan pl{};
     if (n_sm <= 0) n_sm = device_sm_count();
     UAA_TRY(make_plan(desc, batch, max_seq_len, n_sm, &pl));
-    layout->n_splits = pl.S;
-    layout->chunk_keys = pl.chunk_tiles * uaa::kTileKeys;
+    layout->n_ctas = pl.n_ctas;
+    layout->stage_keys = pl.mg * uaa::kTileKeys;
     layout->heads_per_cta = pl.heads_per_cta;
     layout->kernel = pl.kernel;
+    layout->n_slices = pl.n_slices;
+    layout->slice_batch = pl.slice;
     layout->status_offset = pl.off_status;
     layout->q_rot_offset = pl.off_qrot;
-    layout->o_part_offset = pl.off_opart;
-    layout->lse_part_offset = pl.off_lse;
+    layout->prefix_offset = pl.off_prefix;
+    layout->rec_lse_offset = pl.off_rec_lse;
+    layout->rec_o_offset = pl.off_rec_o;
+    layout->prefix_stride = pl.prefix_stride;
+    layout->rec_lse_stride = pl.rec_lse_stride;
+    layout->rec_o_stride = pl.rec_o_stride;
     layout->total_bytes = pl.total;
     return UAA_OK;
 }

@@ -1,9 +1,11 @@
 // append.cu -- step 1 of the decode step: per-head QK RMSNorm, rotary embedding at
 // the absolute KV index, and the append of the new k / v rows to the cache.
 //
-// One CTA per sequence. The CTA first builds the cos / sin table of the
-// sequence's position (the angle pos * theta'_p is formed and reduced in fp64,
-// then rounded to fp32), then each warp takes whole head rows: q rows go to
+// One CTA of 16 warps per sequence. The CTA first builds the cos / sin table of
+// the sequence's position (the angle pos * theta'_p is formed and reduced in
+// fp64, then rounded to fp32), while each warp loads its first head row; then
+// each warp takes whole rows (loading the next while it processes the current
+// one): q rows go to
 // the workspace pre-multiplied by the partial kernel's logit prescale, k rows
 // and v rows go to slot seq_lens[b] of the cache. vq8 values are quantised in
 // fp32 with IEEE division and round-half-even, the storage rule of the vq8
@@ -13,7 +15,7 @@
 namespace uaa {
 namespace {
 
-constexpr int kAppendWarps = 8;
+constexpr int kAppendWarps = 16;
 
 __device__ __forceinline__ void store_kv(void* cache, int dtype, size_t i, float v)
 {
@@ -43,6 +45,18 @@ __device__ __forceinline__ void quantize_row(const float (&x)[EPL], int lane, in
     if (lane == 0) *scale = s;
 }
 
+// Row r of sequence b: the q rows (r < Hq), then the k rows, then the v rows.
+__device__ __forceinline__ const void* row_source(const AppendParams& p, int b, int r, size_t& at)
+{
+    if (r < p.Hq) {
+        at = (static_cast<size_t>(b) * p.Hq + r) * p.D;
+        return p.q;
+    }
+    const int kv = r < p.Hq + p.Hkv ? r - p.Hq : r - p.Hq - p.Hkv;
+    at = (static_cast<size_t>(b) * p.Hkv + kv) * p.D;
+    return r < p.Hq + p.Hkv ? p.k_new : p.v_new;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p)
 {
@@ -51,8 +65,21 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     __shared__ float2 cs[HALF];
     __shared__ float rowbuf[kAppendWarps][D];
 
+    grid_dependency_wait();  // the step's inputs and the previous step's reads are complete
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // each warp takes rows warp, warp + W, ...; the next row is loaded while the
+    // current one is processed (the first load goes out before the length's)
+    const int n_rows = p.Hq + 2 * p.Hkv;
+    float x[EPL], nxt[EPL];
+    if (warp < n_rows) {
+        size_t at;
+        const void* src = row_source(p, b, warp, at);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) nxt[i] = load_elem(src, p.io_dtype, at + lane + 32 * i);
+    }
+
     const int L = p.seq_lens[b];
     const bool fits = L >= 0 && L < p.cap;
     if (threadIdx.x == 0) {
@@ -61,24 +88,30 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     }
     const int pos = fits ? L : 0;
 
-    // cos / sin of pos * theta'_p: fp64 product, exact pi-scaled reduction in sincospi.
+    // cos / sin of pos * theta'_p: the angle in units of pi, t = pos * theta'_p / pi,
+    // is formed in fp64 and reduced exactly to t - 2 rint(t / 2) in [-1, 1]; the
+    // reduced value is rounded to fp32 for sincospif (error ~ 2^-24 pi rad).
     for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-        double sn, cn;
-        sincospi(static_cast<double>(pos) * p.inv_freq_over_pi[i], &sn, &cn);
-        cs[i] = make_float2(static_cast<float>(cn) * p.mscale, static_cast<float>(sn) * p.mscale);
+        const double t = static_cast<double>(pos) * p.inv_freq_over_pi[i];
+        const double r = fma(-2.0, rint(0.5 * t), t);
+        float sn, cn;
+        sincospif(static_cast<float>(r), &sn, &cn);
+        cs[i] = make_float2(cn * p.mscale, sn * p.mscale);
     }
-    __syncthreads();
-
-    const int n_rows = p.Hq + 2 * p.Hkv;
+    __syncthreads();  // the cos / sin table is complete
     for (int r = warp; r < n_rows; r += kAppendWarps) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) x[i] = nxt[i];
+        if (r + kAppendWarps < n_rows) {
+            size_t at;
+            const void* src = row_source(p, b, r + kAppendWarps, at);
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) nxt[i] = load_elem(src, p.io_dtype, at + lane + 32 * i);
+        }
         const bool is_q = r < p.Hq;
         const bool is_k = !is_q && r < p.Hq + p.Hkv;
         const int head = is_q ? r : (is_k ? r - p.Hq : r - p.Hq - p.Hkv);
         const size_t in_row = (static_cast<size_t>(b) * (is_q ? p.Hq : p.Hkv) + head) * D;
-        const void* src = is_q ? p.q : (is_k ? p.k_new : p.v_new);
-        float x[EPL];
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) x[i] = load_elem(src, p.io_dtype, in_row + lane + 32 * i);
 
         const size_t slot = ((static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos) * D;
         if (!is_q && !is_k) {  // value row: stored as given (or quantised)
@@ -158,12 +191,11 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
     const dim3 grid(p.B), block(kAppendWarps * 32);
     switch (p.D) {
-    case 64: append_kernel<64><<<grid, block, 0, s>>>(p); break;
-    case 128: append_kernel<128><<<grid, block, 0, s>>>(p); break;
-    case 256: append_kernel<256><<<grid, block, 0, s>>>(p); break;
+    case 64: return launch_dependent(append_kernel<64>, grid, block, 0, s, p);
+    case 128: return launch_dependent(append_kernel<128>, grid, block, 0, s, p);
+    case 256: return launch_dependent(append_kernel<256>, grid, block, 0, s, p);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,

@@ -1,55 +1,107 @@
-// combine.cu -- step 3 of the decode step: log-sum-exp merge of the split-K
-// partials and the per-head sink logit.
+// combine.cu -- step 3 of the decode step: log-sum-exp merge of the records of
+// units that the stream-K partition cut between CTAs, with the per-head sink.
 //
-// One thread per output element (b, h, d). With partial rows o_s (normalised)
-// and their log2-sum-exp e_s (of the final logits, in log2 units), and the sink
-// logit z_h of the head (llamay "Models and formats", "Architectures": a
-// per-head sink in the softmax denominator):
-//   M   = max(max_s e_s, z_h log2 e)
-//   out = sum_s o_s 2^(e_s - M) / (sum_s 2^(e_s - M) + 2^(z_h log2 e - M))
+// One CTA per unit (sequence, kv head, head group). A unit that lies inside one
+// CTA's range was written by the partial kernel already and is skipped. For a
+// cut unit with records (o_c normalised, e_c the log2-sum-exp of the final
+// logits) from its owner CTAs, and the sink logit z_h of each head (llamay
+// "Models and formats", "Architectures": a per-head sink in the softmax
+// denominator):
+//   M   = max(max_c e_c, z_h log2 e)
+//   out = sum_c o_c 2^(e_c - M) / (sum_c 2^(e_c - M) + 2^(z_h log2 e - M))
 // which is the full softmax over every visible key with the sink's mass in the
-// denominator only. A sequence with no visible key and no sink gets zeros.
+// denominator only. A sequence with no visible key gets zeros.
+//
+// With P = min(CTAs, stages) every CTA range is non-empty, so the owners of a cut
+// unit's stages are exactly the CTAs cA .. cB. The record weights are formed per
+// head from one parallel round of loads; every thread then loads all records'
+// rows for four output elements before it adds any of them.
 #include "internal.cuh"
 
 namespace uaa {
 namespace {
 
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p)
+constexpr int kCombineThreads = 128;
+constexpr int kMaxHeads = 16;    // heads of one unit
+constexpr int kRecBatch = 4;     // records loaded together per output element
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
-    const size_t total = static_cast<size_t>(p.B) * p.Hq * p.D;
-    for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int d = static_cast<int>(idx % p.D);
-        const int h = static_cast<int>((idx / p.D) % p.Hq);
-        const int b = static_cast<int>(idx / (static_cast<size_t>(p.D) * p.Hq));
-        int lo, hi;
-        key_range(p.seq_lens[b], p.window, lo, hi);
-        const int ns = splits_needed(lo, hi, p.chunk_tiles);
-        float result;
-        if (ns > p.S) {  // the max_seq_len bound was broken: not enough split slots
-            if (d == 0 && h == 0) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
-            result = __int_as_float(0x7fc00000);
-        } else {
-            const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.S;
-            const float z = p.sink ? p.sink[h] * kLog2e : -INFINITY;
-            float M = z;
-            for (int s = 0; s < ns; ++s) M = fmaxf(M, p.lse_part[row + s]);
-            float num = 0.f, den = 0.f;
-            if (M != -INFINITY) {
-                den = p.sink ? exp2f(z - M) : 0.f;
-                for (int s = 0; s < ns; ++s) {
-                    const float e = p.lse_part[row + s];
-                    const float w = e == -INFINITY ? 0.f : exp2f(e - M);
-                    num = fmaf(w, p.o_part[(row + s) * p.D + d], num);
-                    den += w;
-                }
+    extern __shared__ float wts[];  // [R][nh]: record log2-sum-exp, then weights
+    grid_dependency_wait();         // the partial kernel's records are complete
+
+    const int units = p.Hkv * p.head_groups;
+    const int b = blockIdx.x / units, u = blockIdx.x - b * units;
+    const int kvh = u / p.head_groups, hg = u - kvh * p.head_groups;
+    const int HC = p.heads_per_cta;
+    const int h0 = kvh * p.G + hg * HC;
+    const int nh = min(HC, p.G - hg * HC);
+    const int D = p.D;
+    const int stg = (p.prefix[b + 1] - p.prefix[b]) / units;
+    const int tid = threadIdx.x;
+    const size_t out0 = (static_cast<size_t>(b) * p.Hq + h0) * D;
+    if (stg == 0) {  // nothing visible: zeros
+        for (int idx = tid; idx < nh * D; idx += kCombineThreads) store_out(p.out, p.out_dtype, out0 + idx, 0.f);
+        return;
+    }
+    const long long T = p.prefix[p.B];
+    const int P = T < p.P ? static_cast<int>(T) : p.P;
+    const long long A = p.prefix[b] + static_cast<long long>(u) * stg;
+    const int cA = cta_of(A, T, P), cB = cta_of(A + stg - 1, T, P);
+    if (cA == cB) return;  // a whole unit: the partial kernel wrote it
+    const bool first_is_slot0 = range_start(cA, T, P) == A;
+    const int R = cB - cA + 1;  // the unit's records: owners cA .. cB
+
+    for (int i = tid; i < R * nh; i += kCombineThreads)
+        wts[i] = p.rec_lse[static_cast<size_t>(record_of(cA + i / nh, cA, first_is_slot0)) * HC + (i % nh)];
+    __syncthreads();
+    for (int hc = tid; hc < nh; hc += kCombineThreads) {
+        const float z = p.sink ? p.sink[h0 + hc] * kLog2e : -INFINITY;
+        float M = z;
+        for (int r = 0; r < R; ++r) M = fmaxf(M, wts[r * nh + hc]);
+        float den = 0.f;
+        if (M != -INFINITY) {
+            den = p.sink ? exp2f(z - M) : 0.f;
+            for (int r = 0; r < R; ++r) {
+                const float e = wts[r * nh + hc];
+                const float w = e == -INFINITY ? 0.f : exp2f(e - M);
+                wts[r * nh + hc] = w;
+                den += w;
             }
-            result = den > 0.f ? num / den : 0.f;
         }
-        if (p.out_dtype == UAA_DTYPE_F32)
-            static_cast<float*>(p.out)[idx] = result;
-        else
-            static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(result);
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        for (int r = 0; r < R; ++r) wts[r * nh + hc] = M == -INFINITY ? 0.f : wts[r * nh + hc] * inv;
+    }
+    __syncthreads();
+    for (int base = tid; base < nh * D; base += 4 * kCombineThreads) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r0 = 0; r0 < R; r0 += kRecBatch) {
+            float v[kRecBatch][4];
+#pragma unroll
+            for (int r = 0; r < kRecBatch; ++r)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int idx = base + k * kCombineThreads;
+                    v[r][k] = 0.f;
+                    if (r0 + r < R && idx < nh * D) {
+                        const int hc = idx / D, d = idx - hc * D;
+                        const int rec = record_of(cA + r0 + r, cA, first_is_slot0);
+                        v[r][k] = p.rec_o[(static_cast<size_t>(rec) * HC + hc) * D + d];
+                    }
+                }
+#pragma unroll
+            for (int r = 0; r < kRecBatch; ++r)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int idx = base + k * kCombineThreads;
+                    if (r0 + r < R && idx < nh * D) acc[k] = fmaf(wts[(r0 + r) * nh + idx / D], v[r][k], acc[k]);
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int idx = base + k * kCombineThreads;
+            if (idx < nh * D) store_out(p.out, p.out_dtype, out0 + idx, acc[k]);
+        }
     }
 }
 
@@ -57,12 +109,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p)
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s)
 {
-    const size_t total = static_cast<size_t>(p.B) * p.Hq * p.D;
-    if (total == 0) return cudaSuccess;
-    size_t blocks = (total + 255) / 256;
-    if (blocks > 65535u * 8u) blocks = 65535u * 8u;
-    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    const long long blocks = static_cast<long long>(p.B) * p.Hkv * p.head_groups;
+    if (blocks == 0) return cudaSuccess;
+    // weights for up to every CTA's record of a unit (a unit never has more records than CTAs)
+    const size_t smem = static_cast<size_t>(p.P) * (p.heads_per_cta < kMaxHeads ? p.heads_per_cta : kMaxHeads) * 4;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_dependent(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads), smem, s, p);
 }
 
 }  // namespace uaa

@@ -42,32 +42,54 @@ struct AppendParams {
     double inv_freq_over_pi[kMaxHeadDim / 2];  // theta'_p / pi, fp64
 };
 
+// The partial kernels are persistent and share one stream-K partition. Work is
+// the list of ring stages (MG 64-key tiles each) of every unit = (sequence b,
+// kv head, head group), units ordered by b then kv head then head group; a
+// sequence with visible tiles [t0, t1) has ceil((t1 - t0) / MG) stages per
+// unit. With T stages in total and P = min(launched CTAs, T), CTA c < P owns
+// stages [floor(c T / P), floor((c + 1) T / P)) (never empty), cut at unit
+// boundaries into segments; CTAs c >= P have nothing to do. A segment that is a whole
+// unit writes the unit's output rows; any other segment writes one record
+// (normalised rows + log2-sum-exp) in slot 0 (the CTA's first segment) or 1
+// (its last), and the combine kernel merges the records of such units.
+//
+// Record index (2 c + slot) of the piece of a cut unit that CTA c owns: the
+// piece in the first owner cA is that CTA's first segment (slot 0) only if the
+// unit starts where cA's range starts; every later owner's piece starts its
+// range (slot 0).
 struct PartialParams {
     int B, Hq, Hkv, D, G;
-    int heads_per_cta;      // query heads per CTA
+    int b_off;              // first sequence of this launch (batches are cut into slices)
+    int heads_per_cta;      // query heads per unit (8 * NHT for the tensor-core kernel)
     int head_groups;        // ceil(G / heads_per_cta)
     int cap, window;
-    int S, chunk_tiles;
+    int mg;                 // 64-key tiles per stage
     float softcap_log2e;    // 0: no softcap; else softcap * log2(e)
-    const float* q_prime;
-    const void* k_cache;
+    const float* q_prime;   // [B][Hq][D] (slice-relative: already offset by b_off)
+    const void* k_cache;    // whole caches (rows indexed with b_off + b)
     const void* v_cache;
     const float* v_scale;
-    const int* seq_lens;
-    float* o_part;          // [B][Hq][S][D]
-    float* lse_part;        // [B][Hq][S]
+    const int* seq_lens;    // slice-relative
+    int* prefix;            // [B + 1] stage prefix over sequences, written for the combine
+    float* rec_o;           // [2P][heads_per_cta][D]
+    float* rec_lse;         // [2P][heads_per_cta]
+    const float* sink;      // [Hq] or null
+    void* out;              // [B][Hq][D] slice-relative
+    int out_dtype;
     unsigned* status;
 };
 
 struct CombineParams {
     int B, Hq, Hkv, D, G;
-    int window, S, chunk_tiles;
+    int heads_per_cta, head_groups;
+    int window, mg, P;
     int out_dtype;
     const float* sink;      // [Hq] or null
-    const int* seq_lens;
-    const float* o_part;
-    const float* lse_part;
-    void* out;
+    const int* seq_lens;    // slice-relative
+    const int* prefix;      // [B + 1]
+    const float* rec_o;
+    const float* rec_lse;
+    void* out;              // slice-relative
     unsigned* status;
 };
 
@@ -75,21 +97,58 @@ struct CombineParams {
 // Each returns the launch error (cudaGetLastError) of its kernel.
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
-cudaError_t launch_partial_simt(const PartialParams& p, cudaStream_t s);
+cudaError_t launch_partial_simt(const PartialParams& p, int n_ctas, cudaStream_t s);
 cudaError_t launch_partial_tc(const PartialParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_s, int kv_dtype,
-                              int n_head_tiles, cudaStream_t s);
+                              int n_head_tiles, int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
                                 float* scales, cudaStream_t s);
 
 // Dynamic shared memory the tensor-core partial kernel needs.
 size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles);
-// Keys per ring stage of the tensor-core partial kernel (the TMA box height); its
-// splits hold a multiple of keys_per_stage / 64 tiles.
+// Keys per ring stage of the tensor-core partial kernel (the TMA box height).
 int partial_tc_keys_per_stage(int D);
+// Largest batch slice one partial launch takes (its stage prefix lives in shared memory).
+constexpr int kMaxSliceBatch = 1024;
+
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous kernel on the stream finishes; every kernel launched this way runs
+// `griddepcontrol.wait` (grid_dependency_wait) before it reads anything an
+// earlier launch wrote, so only its launch and set-up overlap.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 // ---------------------------------------------------------------- device helpers
+
+// Waits until the previous grid on the stream has completed and its memory is
+// visible (a no-op for a kernel launched without programmatic dependence).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void store_out(void* out, int dtype, size_t i, float v)
+{
+    if (dtype == UAA_DTYPE_F32)
+        static_cast<float*>(out)[i] = v;
+    else
+        static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+}
 
 // Visible keys of a sequence holding n keys after the append: [lo, n) with a
 // window W keeping the last W of them (positions j > pos - W, pos = n - 1).
@@ -99,12 +158,118 @@ __host__ __device__ inline void key_range(int n, int window, int& lo, int& hi)
     lo = (window > 0 && n > window) ? n - window : 0;
 }
 
-// Splits covering tiles [lo / 64, ceil(hi / 64)) in chunks of chunk_tiles tiles.
-__host__ __device__ inline int splits_needed(int lo, int hi, int chunk_tiles)
+// Ring stages (mg tiles of 64 keys each) covering tiles [lo / 64, ceil(hi / 64)).
+__host__ __device__ inline int stages_of(int lo, int hi, int mg)
 {
     if (hi <= lo) return 0;
     const int t0 = lo / kTileKeys, t1 = (hi + kTileKeys - 1) / kTileKeys;
-    return (t1 - t0 + chunk_tiles - 1) / chunk_tiles;
+    return (t1 - t0 + mg - 1) / mg;
+}
+
+__host__ __device__ inline int record_of(int c, int cA, bool first_is_slot0)
+{
+    return 2 * c + ((c == cA && !first_is_slot0) ? 1 : 0);
+}
+
+// Stream-K partition of T stages over P CTAs.
+__host__ __device__ inline long long range_start(int c, long long T, int P)
+{
+    return static_cast<long long>(c) * T / P;
+}
+
+// The CTA whose range holds stage x, 0 <= x < T (P <= T): the largest c with
+// floor(c T / P) <= x, i.e. ceil((x + 1) P / T) - 1.
+__host__ __device__ inline int cta_of(long long x, long long T, int P)
+{
+    return static_cast<int>(((x + 1) * P + T - 1) / T) - 1;
+}
+
+// Visible keys [lo, hi) of sequence b, clamped to the cache (a longer length is
+// flagged by the caller).
+__device__ __forceinline__ void visible_keys(int n, int window, int cap, int& lo, int& hi)
+{
+    key_range(n, window, lo, hi);
+    if (hi > cap) hi = cap;
+}
+
+// Block-wide prefix[0..B] of units * stages per sequence into shared memory
+// (warp 0 scans, every thread returns after the barrier). Writes the prefix to
+// `global_copy` too when it is not null.
+__device__ inline void build_stage_prefix(const int* seq_lens, int B, int window, int cap, int mg, int units,
+                                          int* prefix, int* global_copy, unsigned* status)
+{
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        if (lane == 0) {
+            prefix[0] = 0;
+            if (global_copy) global_copy[0] = 0;
+        }
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int v = 0;
+            if (b < B) {
+                const int n = seq_lens[b];
+                if (n > cap && status) atomicOr(status, UAA_DEVFLAG_CAPACITY);
+                int lo, hi;
+                visible_keys(n, window, cap, lo, hi);
+                v = units * stages_of(lo, hi, mg);
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (b < B) {
+                prefix[b + 1] = carry + v;
+                if (global_copy) global_copy[b + 1] = carry + v;
+            }
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+}
+
+// Largest b with prefix[b] <= x (prefix non-decreasing, prefix[0] = 0 <= x < prefix[B]).
+__device__ __forceinline__ int find_sequence(const int* prefix, int B, long long x)
+{
+    int lo = 0, hi = B;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// One segment of a CTA's stage range.
+struct Segment {
+    int b;          // slice-relative sequence
+    int kvh, hg;    // kv head and head group of the unit
+    int st0;        // first stage within the unit
+    int n_st;       // stages in the segment
+    int stages;     // stages of the whole unit
+    int lo, hi;     // visible keys of the sequence
+    bool whole;     // the segment is the whole unit
+};
+
+__device__ __forceinline__ Segment segment_at(const int* prefix, const int* seq_lens, int B, int window, int cap,
+                                              int head_groups, int units, long long pos, long long end)
+{
+    Segment sg;
+    sg.b = find_sequence(prefix, B, pos);
+    const int per_seq = prefix[sg.b + 1] - prefix[sg.b];
+    sg.stages = per_seq / units;
+    const int local = static_cast<int>(pos - prefix[sg.b]);
+    const int u = local / sg.stages;
+    sg.st0 = local - u * sg.stages;
+    const long long left = end - pos;
+    sg.n_st = left < sg.stages - sg.st0 ? static_cast<int>(left) : sg.stages - sg.st0;
+    sg.kvh = u / head_groups;
+    sg.hg = u - sg.kvh * head_groups;
+    visible_keys(seq_lens[sg.b], window, cap, sg.lo, sg.hi);
+    sg.whole = sg.st0 == 0 && sg.n_st == sg.stages;
+    return sg;
 }
 
 __device__ __forceinline__ float warp_sum(float v)

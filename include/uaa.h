@@ -7,13 +7,16 @@
  *   1. uaa_rope_qk_norm_append: optional per-head RMSNorm of the new q and k
  *      rows, rotary position embedding at the sequence's absolute KV index, and
  *      the append of k and v at slot seq_lens[b] (seq_lens[b] then grows by 1).
- *   2. uaa_decode_attn_partial: split-K flash decoding; each CTA attends one
- *      key range of one (sequence, kv head, head group) and writes a partial
- *      (normalised output row and log-sum-exp) to the workspace.
- *   3. uaa_decode_attn_combine: log-sum-exp merge of the partials, the sink
- *      logit added to the denominator, the output written.
+ *   2. uaa_decode_attn_partial: split-K flash decoding. A persistent grid of P
+ *      CTAs splits the key stages of all units (sequence, kv head, head group)
+ *      into P equal contiguous ranges (a stream-K partition). A unit that lies
+ *      inside one CTA's range is finished there and its output rows written;
+ *      every other unit leaves one record (normalised output rows and
+ *      log-sum-exp) per CTA it touches in the workspace.
+ *   3. uaa_decode_attn_combine: log-sum-exp merge of those records, the sink
+ *      logit added to the denominator, the remaining output rows written.
  *   uaa_decode_attn runs 1-3 on one stream.
- *
+
  * Where the method is defined (page title, then section):
  *   - integral GQA ratio, head_dim set, 1/sqrt(head_dim) scale, the split-K
  *     decode and KV-producer paths (prior art):
@@ -58,7 +61,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 1
+#define UAA_ABI_VERSION 2
 
 typedef enum {
     UAA_OK = 0,
@@ -79,7 +82,7 @@ typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2 } uaa_dt
 
 /* Device-side status flags (sticky, in the workspace; read by uaa_device_status). */
 #define UAA_DEVFLAG_CAPACITY 0x1u   /* seq_lens[b] >= cache_capacity: that sequence was not appended */
-#define UAA_DEVFLAG_LEN_HINT 0x2u   /* seq_lens[b] > max_seq_len: too few splits, out rows are NaN */
+#define UAA_DEVFLAG_LEN_HINT 0x2u   /* seq_lens[b] > max_seq_len at the append (results stay exact) */
 #define UAA_DEVFLAG_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up; outputs are invalid */
 
 /* Rotary embedding. Pair p of a head row is (p, p + D/2) for NEOX and (2p, 2p+1)
@@ -132,7 +135,7 @@ typedef struct {
     float* v_scale;           /* [B][Hkv][cap], VQ8 only */
     int32_t cache_capacity;   /* cap: slots per (sequence, kv head), a multiple of 4 */
     int32_t* seq_lens;        /* [B]: tokens cached before the step; the append adds 1 */
-    int32_t max_seq_len;      /* host bound on seq_lens[b] before the step; sizes the splits */
+    int32_t max_seq_len;      /* host bound on seq_lens[b] before the step (+1 must fit cap) */
     void* out;                /* [B][Hq][D] out_dtype */
     float* q_rot;             /* optional [B][Hq][D] fp32: the normed, rotated q rows */
 } uaa_step_args;
@@ -147,15 +150,22 @@ typedef struct {
 
 /* Where each array lives in the workspace, and the split geometry. */
 typedef struct {
-    int32_t n_splits;         /* S: partial slots per (sequence, query head) */
-    int32_t chunk_keys;       /* keys per split (a multiple of 64); split s of a sequence
-                                 covers 64-key tiles [t0 + s c, t0 + (s+1) c), t0 = lo / 64 */
-    int32_t heads_per_cta;    /* query heads one partial CTA handles */
+    int32_t n_ctas;           /* P: persistent CTAs of the partial step (stream-K ranges) */
+    int32_t stage_keys;       /* keys per ring stage: 64, or 128 at head_dim 64 (bf16/vq8) */
+    int32_t heads_per_cta;    /* query heads of one unit (sequence, kv head, head group) */
     int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
+    int32_t n_slices;         /* partial + combine launches (batch slices) */
+    int32_t slice_batch;      /* sequences per slice (the last may hold fewer) */
     size_t status_offset;     /* uint32 device flags */
     size_t q_rot_offset;      /* fp32 [B][Hq][D]: rotated q times the kernel's logit prescale */
-    size_t o_part_offset;     /* fp32 [B][Hq][S][D]: normalised partial outputs */
-    size_t lse_part_offset;   /* fp32 [B][Hq][S]: partial log2-sum-exp of the final logits */
+    size_t prefix_offset;     /* int32 [n_slices][slice_batch + 1]: units x stages, prefix over
+                                 the slice's sequences */
+    size_t rec_lse_offset;    /* fp32 [n_slices][2P][heads_per_cta]: record log2-sum-exp */
+    size_t rec_o_offset;      /* fp32 [n_slices][2P][heads_per_cta][D]: normalised record rows;
+                                 record 2c + 0 is CTA c's first segment, 2c + 1 its last */
+    size_t prefix_stride;     /* bytes between slices of each of the three arrays above */
+    size_t rec_lse_stride;
+    size_t rec_o_stride;
     size_t total_bytes;
 } uaa_workspace_layout;
 
@@ -164,11 +174,12 @@ typedef struct {
 uaa_status uaa_rope_qk_norm_append(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
-/* Step 2 (split-K partials) over the visible keys of every sequence. */
+/* Step 2 (split-K partials) over the visible keys of every sequence; writes the
+ * output rows of units finished inside one CTA and records for the others. */
 uaa_status uaa_decode_attn_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
-/* Step 3 (log-sum-exp combine + sink) into args->out. */
+/* Step 3 (log-sum-exp combine + sink) of the recorded units into args->out. */
 uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
@@ -182,7 +193,8 @@ uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
 size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len,
                           int32_t n_sm);
 
-/* Number of split slots S per (sequence, query head); 0 on a refused desc. */
+/* Number of CTAs P the split-K step runs (each attends one contiguous range of
+ * the key stages of all units); 0 on a refused desc. */
 int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len,
                        int32_t n_sm);
 

@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 1
+    assert B.uaa_abi_version() == 2
 
 
 def good_desc(**kw):
@@ -122,28 +122,36 @@ def test_vq8_quantize_refusals(L):
 
 
 @pytest.mark.parametrize("name", list(W.CONFIGS))
-def test_split_geometry_covers_every_visible_key(L, name):
+def test_workspace_layout_is_consistent(L, name):
     for layer in W.layer_configs(W.config(name)):
         d = B.make_desc(layer)
         batch = layer["batch"]
         longest = W.capacity(layer, extra=layer.get("steps", 1)) - 1
         for n_sm in (1, 20, 152):
             lay = B.uaa_get_workspace_layout(d, batch, longest, n_sm)
-            S, ck = lay.n_splits, lay.chunk_keys
-            assert S >= 1 and ck % 64 == 0 and ck > 0
-            visible = min(longest + 1, layer.get("window") or longest + 1)
-            tiles = -(-visible // 64) + (1 if layer.get("window") else 0)
-            assert S * (ck // 64) >= tiles, "splits must cover the visible tiles"
-            assert (S - 1) * (ck // 64) < tiles, "no split slot is always empty"
-            assert lay.kernel == (0 if layer["kv_dtype"] == "f32" else 1)
-            Hq, D = layer["n_q_heads"], layer["head_dim"]
-            assert lay.o_part_offset >= lay.q_rot_offset + batch * Hq * D * 4
-            assert lay.lse_part_offset >= lay.o_part_offset + batch * Hq * S * D * 4
-            assert lay.total_bytes >= lay.lse_part_offset + batch * Hq * S * 4
+            kernel = 0 if layer["kv_dtype"] == "f32" else 1
+            per_sm = 4 if kernel == 0 else (1 if layer["head_dim"] == 256 else 2)
+            assert lay.kernel == kernel and lay.n_ctas == n_sm * per_sm
+            assert lay.stage_keys == (128 if kernel == 1 and layer["head_dim"] == 64 else 64)
+            assert lay.n_slices == -(-batch // lay.slice_batch) and lay.slice_batch <= 1024
+            Hq, D, HC, P = layer["n_q_heads"], layer["head_dim"], lay.heads_per_cta, lay.n_ctas
+            assert lay.prefix_offset >= lay.q_rot_offset + batch * Hq * D * 4
+            assert lay.prefix_stride >= (lay.slice_batch + 1) * 4
+            assert lay.rec_lse_offset >= lay.prefix_offset + lay.n_slices * lay.prefix_stride
+            assert lay.rec_lse_stride >= 2 * P * HC * 4
+            assert lay.rec_o_offset >= lay.rec_lse_offset + lay.n_slices * lay.rec_lse_stride
+            assert lay.rec_o_stride >= 2 * P * HC * D * 4
+            assert lay.total_bytes >= lay.rec_o_offset + lay.n_slices * lay.rec_o_stride
             assert B.uaa_workspace_size(d, batch, longest, n_sm) == lay.total_bytes
-            assert B.uaa_num_splits(d, batch, longest, n_sm) == S
-            for off in (lay.q_rot_offset, lay.o_part_offset, lay.lse_part_offset):
+            assert B.uaa_num_splits(d, batch, longest, n_sm) == P
+            for off in (lay.q_rot_offset, lay.prefix_offset, lay.rec_lse_offset, lay.rec_o_offset):
                 assert off % 256 == 0
+
+
+def test_large_batches_are_sliced(L):
+    d = B.make_desc(W.config("llama31_8b_decode"))
+    lay = B.uaa_get_workspace_layout(d, 2500, 100, 152)
+    assert (lay.slice_batch, lay.n_slices) == (1024, 3)
 
 
 def test_geometry_query_refuses_bad_desc(L):

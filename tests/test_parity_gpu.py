@@ -201,68 +201,103 @@ def test_capacity_flag_and_no_write(oracle_mod):
     assert layer.device_status() == 0  # cleared by the read
 
 
-def test_length_hint_violation_is_flagged():
+def test_length_hint_violation_is_flagged_and_results_stay_exact(oracle_mod):
+    """max_seq_len only bounds the cache check; a longer sequence is flagged at the
+    append, and the stream-K split still covers every key."""
     cfg = W.config("llama31_8b_decode", batch=2, seq_len=3000)
     case = host_case(cfg, lens=[2999, 5])
+    a = oracle_arrays(case, oracle_mod)
     layer = gpu_layer(case)
     args = layer.args(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda(), max_seq_len=5)
     B.uaa_decode_attn(layer.desc, args, layer.ws, torch.cuda.current_stream())
     flags = layer.device_status()
     assert flags & B.UAA_DEVFLAG_LEN_HINT
-    out = layer.out.cpu()
-    assert torch.isnan(out[0]).all() and torch.isfinite(out[1]).all()
+    want = oracle_mod.decode_step(cfg, a["q"], a["k_new"], a["v_new"], None, None, None, a["k_cache"],
+                                  a["v_cache"], None, a["seq_lens"])
+    assert_out_close(layer.out.cpu(), want)
 
 
 # ------------------------------------------------------------------ split partials
 
+def stream_k_segments(prefix, n_ctas, units, head_groups):
+    """The documented stream-K partition: with P = min(CTAs, T), CTA c owns stages
+    [c T / P, (c+1) T / P) of the concatenated unit stages, cut at unit boundaries."""
+    import bisect
+    T = int(prefix[-1])
+    n_ctas = min(n_ctas, T)  # CTAs beyond the stage count have nothing to do
+    for c in range(n_ctas):
+        s, e = c * T // n_ctas, (c + 1) * T // n_ctas
+        pos = s
+        while pos < e:
+            b = bisect.bisect_right(prefix, pos) - 1
+            stg = (int(prefix[b + 1]) - int(prefix[b])) // units
+            local = pos - int(prefix[b])
+            u, st0 = divmod(local, stg)
+            n = min(e - pos, stg - st0)
+            kvh, hg = divmod(u, head_groups)
+            yield dict(cta=c, slot=0 if pos == s else 1, b=b, kvh=kvh, hg=hg, st0=st0, n=n,
+                       whole=(st0 == 0 and n == stg))
+            pos += n
+
+
 @pytest.mark.parametrize("name,over,lens", [
-    ("llama31_8b_decode", dict(batch=2, seq_len=3000), [2999, 700]),
+    ("llama31_8b_decode", dict(batch=3, seq_len=3000), [2999, 700, 1]),
     ("gptoss_vq8_sink", dict(batch=2, seq_len=3000), [2999, 130]),
     ("gemma2_9b_swa", dict(batch=2, seq_len=3000, layers=[dict(window=1000)]), [2999, 1500]),
     ("llama32_1b_tiny", dict(batch=1, seq_len=700), [699]),
+    ("llama31_8b_decode", dict(batch=2, n_q_heads=32, n_kv_heads=2, seq_len=900), [899, 64]),
 ])
-def test_partials_match_oracle_ranges(oracle_mod, name, over, lens):
-    """Each split's partial (normalised row, log-sum-exp) equals the oracle's
-    softmax restricted to the split's key range."""
+def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens):
+    """After the append and the partial step: each record equals the oracle's
+    softmax restricted to its segment's keys, and each unit finished inside one
+    CTA has its output rows (sink included) equal to the full attention."""
     cfg = W.layer_configs(W.config(name, **over))[0]
     case = host_case(cfg, lens=lens)
     a = oracle_arrays(case, oracle_mod)
     layer = gpu_layer(case)
     lay = layer.layout()
     dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
+    layer.out.fill_(float("nan"))
     layer.append(dev["q"], dev["k_new"], dev["v_new"])
     layer.partial()
     torch.cuda.synchronize()
     qr = oracle_mod.append(cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"], a["k_cache"],
                            a["v_cache"], a["v_scale"], a["seq_lens"])
+    full = oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"])
     Bn, Hq, D, Hkv = cfg["batch"], cfg["n_q_heads"], cfg["head_dim"], cfg["n_kv_heads"]
-    S, ck = lay.n_splits, lay.chunk_keys
-    ws = layer.ws_tensor
-    o_part = ws[lay.o_part_offset: lay.o_part_offset + Bn * Hq * S * D * 4].view(torch.float32)
-    o_part = o_part.view(Bn, Hq, S, D).cpu().numpy()
-    lse = ws[lay.lse_part_offset: lay.lse_part_offset + Bn * Hq * S * 4].view(torch.float32)
-    lse = lse.view(Bn, Hq, S).cpu().numpy()
     G = Hq // Hkv
-    checked = 0
-    for b in range(Bn):
+    HC, P, mg = lay.heads_per_cta, lay.n_ctas, lay.stage_keys // 64
+    hgroups = -(-G // HC)
+    ws = layer.ws_tensor
+    assert lay.n_slices == 1
+    prefix = ws[lay.prefix_offset: lay.prefix_offset + (Bn + 1) * 4].view(torch.int32).cpu().numpy()
+    rec_lse = ws[lay.rec_lse_offset: lay.rec_lse_offset + 2 * P * HC * 4].view(torch.float32).view(2 * P, HC)
+    rec_o = ws[lay.rec_o_offset: lay.rec_o_offset + 2 * P * HC * D * 4].view(torch.float32).view(2 * P, HC, D)
+    rec_lse, rec_o = rec_lse.cpu().numpy(), rec_o.cpu().numpy()
+    out = layer.out.cpu().numpy()
+    W_ = cfg.get("window", 0) or 0
+    n_whole = n_rec = 0
+    for sg in stream_k_segments(prefix, P, Hkv * hgroups, hgroups):
+        b = sg["b"]
         n = int(a["seq_lens"][b])
-        W_ = cfg.get("window", 0) or 0
         lo = max(0, n - W_) if W_ else 0
         t0 = lo // 64
-        for s in range(S):
-            j0, j1 = max(lo, (t0 * 64) + s * ck), min(n, t0 * 64 + (s + 1) * ck)
-            if j1 <= j0:
-                continue
-            for h in range(0, Hq, max(1, Hq // 8)):
-                g = h // G
-                kr = a["k_cache"][b, g]
-                vr = a["v_cache"][b, g]
+        j0 = max(lo, (t0 + mg * sg["st0"]) * 64)
+        j1 = min(n, (t0 + mg * (sg["st0"] + sg["n"])) * 64)
+        heads = [sg["kvh"] * G + sg["hg"] * HC + hc for hc in range(HC) if sg["hg"] * HC + hc < G]
+        for hc, h in enumerate(heads):
+            if sg["whole"]:
+                assert np.max(np.abs(out[b, h] - full[b, h])) <= TOL_MAX
+                n_whole += 1
+            else:
+                g = sg["kvh"]
                 sr = None if a["v_scale"] is None else a["v_scale"][b, g]
-                o, l_nat = oracle_mod.attend_range(cfg, qr[b, h], kr, vr, sr, j0, j1)
-                assert np.max(np.abs(o_part[b, h, s] - o)) <= TOL_MAX
-                assert abs(lse[b, h, s] * math.log(2.0) - l_nat) <= 2e-3 * max(1.0, abs(l_nat))
-                checked += 1
-    assert checked > 0
+                o, l_nat = oracle_mod.attend_range(cfg, qr[b, h], a["k_cache"][b, g], a["v_cache"][b, g], sr, j0, j1)
+                r = 2 * sg["cta"] + sg["slot"]
+                assert np.max(np.abs(rec_o[r, hc] - o)) <= TOL_MAX
+                assert abs(rec_lse[r, hc] * math.log(2.0) - l_nat) <= 2e-3 * max(1.0, abs(l_nat))
+                n_rec += 1
+    assert n_rec > 0  # every case here has units cut between CTAs
 
 
 # ------------------------------------------------------------------ full size, sampled
