@@ -5,7 +5,7 @@ steps/sec at 1 GPU (N replicas under torchrun).
 Workload (default): the Llama-3.1-8B-like decode, 16 sequences at 8192 cached
 tokens, 32 q / 8 kv heads, head_dim 128, bf16 cache, NeoX RoPE with llama3
 factor 8. One benchmark step = 64 consecutive decode steps from 8192 cached
-tokens (each: RoPE/append, split-K partials, combine), after which the lengths
+tokens (each: RoPE/append + split-K partials in one kernel, combine), after which the lengths
 return to 8192 (a 64-byte device copy) so every step times the same work. The
 64 decode steps are captured once in a CUDA graph and replayed. The KV cache
 (~545 MB) is larger than L2 (129 MB), so no flush is needed between steps.
@@ -13,7 +13,8 @@ return to 8192 (a 64-byte device copy) so every step times the same work. The
 value       = algorithmic bytes of all timed steps / device time (CUDA events)
 e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each with
               the step's q/k/v copied from pinned host memory and out copied back
-roofline    = the split-K partial kernel alone: its algorithmic bytes (visible KV
+roofline    = the split-K partial kernel alone (for bf16 / vq8 caches the kernel
+              that also performs the append): its algorithmic bytes (visible KV
               rows) / its mean launch duration, against the measured HBM copy peak
 cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample
 """
@@ -282,7 +283,10 @@ def run_uaa(args, world, rank, local) -> dict | None:
             cur = [x + t for x in base]
             step_bytes += decode_step_bytes(lc, cur)
             part_bytes += partial_bytes(lc, [x + 1 for x in cur])
-    launches_per_step = 3 * n_dec * len(layers)
+    # kernels of one decode step of a layer: the fused append+partial and the
+    # combine (bf16 / vq8 caches), or append, partial and combine (fp32 caches)
+    fused = [layer.layout().kernel == 1 for layer in layers]
+    launches_per_step = n_dec * sum(2 if f else 3 for f in fused)
 
     with torch.cuda.stream(stream):
         # warm-up, then capture one benchmark step in a graph
@@ -314,20 +318,29 @@ def run_uaa(args, world, rank, local) -> dict | None:
             if st:
                 raise RuntimeError(f"device flags 0x{st:x} after the timed region")
 
-        # ---- the partial kernel alone (events on the launching stream)
+        # ---- the partial kernel alone (events on the launching stream): the fused
+        # append+partial kernel of the step for bf16 / vq8 caches, the partial
+        # kernel after its separate append for fp32 caches
         pe = []
-        reset()
-        for _ in range(n_dec):
-            for li, layer in enumerate(layers):
-                inp = inputs[li]
-                args_ = layer.args(inp["q"], inp["k_new"], inp["v_new"], max_seq_len=hint[li])
-                Bd.uaa_rope_qk_norm_append(layer.desc, args_, layer.ws, stream)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                Bd.uaa_decode_attn_partial(layer.desc, args_, layer.ws, stream)
-                e1.record(stream)
-                Bd.uaa_decode_attn_combine(layer.desc, args_, layer.ws, stream)
-                pe.append((e0, e1))
+        rounds = -(-20 // n_dec)  # at least 20 launches per layer
+        for _ in range(rounds):
+            reset()
+            for _ in range(n_dec):
+                for li, layer in enumerate(layers):
+                    inp = inputs[li]
+                    args_ = layer.args(inp["q"], inp["k_new"], inp["v_new"], max_seq_len=hint[li])
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    if fused[li]:
+                        e0.record(stream)
+                        Bd.uaa_decode_attn_append_partial(layer.desc, args_, layer.ws, stream)
+                        e1.record(stream)
+                    else:
+                        Bd.uaa_rope_qk_norm_append(layer.desc, args_, layer.ws, stream)
+                        e0.record(stream)
+                        Bd.uaa_decode_attn_partial(layer.desc, args_, layer.ws, stream)
+                        e1.record(stream)
+                    Bd.uaa_decode_attn_combine(layer.desc, args_, layer.ws, stream)
+                    pe.append((e0, e1))
         stream.synchronize()
         part_s = sum(a.elapsed_time(b) for a, b in pe) / 1e3
         n_part = len(pe)
@@ -365,7 +378,8 @@ def run_uaa(args, world, rank, local) -> dict | None:
         return None
     peaks = measured_peaks()
     value = total_bytes / dev_s / 1e9
-    part_gbs = (part_bytes / n_part) / (part_s / n_part) / 1e9 if n_part else None
+    # part_bytes covers one round (n_dec launches per layer); the timing covers all rounds
+    part_gbs = (part_bytes / (n_dec * len(layers))) / (part_s / n_part) / 1e9 if n_part else None
     clk = clocks.summary()
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -389,7 +403,8 @@ def run_uaa(args, world, rank, local) -> dict | None:
         "roofline": {"bound": "hbm", "achieved": round(part_gbs, 2) if part_gbs else None,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(part_gbs / peaks["hbm_gbs"], 4) if part_gbs else None,
-                     "traffic": measured_traffic(name), "kernel": "split-K partial",
+                     "traffic": measured_traffic(name),
+                     "kernel": "fused append + split-K partial" if all(fused) else "split-K partial",
                      "peak_source": peaks["source"],
                      "bytes_per_launch": part_bytes // max(1, n_dec * len(layers)),
                      "mean_launch_us": round(part_s / n_part * 1e6, 2) if n_part else None},

@@ -84,6 +84,8 @@ _SIGS = [
     ("uaa_rope_qk_norm_append", ctypes.c_int, [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
     ("uaa_decode_attn_partial", ctypes.c_int, [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
     ("uaa_decode_attn_combine", ctypes.c_int, [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
+    ("uaa_decode_attn_append_partial", ctypes.c_int,
+     [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
     ("uaa_decode_attn", ctypes.c_int, [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
     ("uaa_workspace_size", ctypes.c_size_t, [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("uaa_num_splits", ctypes.c_int32, [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
@@ -159,6 +161,11 @@ def uaa_decode_attn_partial(desc, args, ws, stream=None, check=True) -> int:
 def uaa_decode_attn_combine(desc, args, ws, stream=None, check=True) -> int:
     return _check(lib().uaa_decode_attn_combine(ctypes.byref(desc), ctypes.byref(args), ctypes.byref(ws),
                                                 _stream(stream)), check)
+
+
+def uaa_decode_attn_append_partial(desc, args, ws, stream=None, check=True) -> int:
+    return _check(lib().uaa_decode_attn_append_partial(ctypes.byref(desc), ctypes.byref(args), ctypes.byref(ws),
+                                                       _stream(stream)), check)
 
 
 def uaa_decode_attn(desc, args, ws, stream=None, check=True) -> int:

@@ -227,6 +227,14 @@ float softmax_scale(const uaa_attn_desc* d)
     return d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)d->head_dim);
 }
 
+// The prescale of the rotated q rows: logits come out in the log2 domain
+// (scale log2 e), or as s / c when a softcap c applies tanh to them first.
+float qscale(const uaa_attn_desc* d)
+{
+    const float scale = softmax_scale(d);
+    return d->softcap > 0.f ? scale / d->softcap : scale * uaa::kLog2e;
+}
+
 // Rotary frequencies theta'_p / pi in fp64 and the cos/sin multiplier: plain
 // base^(-2p/D); llama3 wavelength interpolation; YaRN ramp over the pair index
 // between the pairs whose wavelength fits beta_fast / beta_slow times into the
@@ -321,8 +329,7 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.style = d->rope.style;
     p.qk_norm = d->qk_norm;
     p.eps = d->norm_eps;
-    const float scale = softmax_scale(d);
-    p.qscale = d->softcap > 0.f ? scale / d->softcap : scale * uaa::kLog2e;
+    p.qscale = qscale(d);
     p.io_dtype = d->io_dtype;
     p.kv_dtype = d->kv_dtype;
     p.q = a->q;
@@ -343,8 +350,9 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     return e == cudaSuccess ? UAA_OK : cuda_fail(e, "append kernel launch");
 }
 
+// fused: the tensor-core kernel also performs the append (steps 1 and 2 in one launch).
 uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
-                       cudaStream_t s)
+                       cudaStream_t s, bool fused = false)
 {
     if (a->batch == 0) return UAA_OK;
     char* w = static_cast<char*>(ws->ptr);
@@ -399,6 +407,26 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.out = static_cast<char*>(a->out) + (size_t)b0 * Hq * D * out_elem;
         p.out_dtype = d->out_dtype;
         p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+        if (fused) {
+            const size_t io_elem = d->io_dtype == UAA_DTYPE_F32 ? 4 : 2;
+            const size_t Hkv = d->n_kv_heads;
+            p.fused = 1;
+            p.max_len = a->max_seq_len;
+            p.arrivals = reinterpret_cast<unsigned*>(w + pl.off_status) + 1;
+            p.q = static_cast<const char*>(a->q) + (size_t)b0 * Hq * D * io_elem;
+            p.k_new = static_cast<const char*>(a->k_new) + (size_t)b0 * Hkv * D * io_elem;
+            p.v_new = static_cast<const char*>(a->v_new) + (size_t)b0 * Hkv * D * io_elem;
+            p.io_dtype = d->io_dtype;
+            p.kv_dtype = d->kv_dtype;
+            p.style = d->rope.style;
+            p.qk_norm = d->qk_norm;
+            p.eps = d->norm_eps;
+            p.qscale = qscale(d);
+            p.q_norm_w = a->q_norm_w;
+            p.k_norm_w = a->k_norm_w;
+            p.q_rot_out = a->q_rot ? a->q_rot + (size_t)b0 * Hq * D : nullptr;
+            rope_table(d, p.inv_freq_over_pi, &p.mscale);
+        }
         const cudaError_t e = pl.kernel == 0
                                   ? uaa::launch_partial_simt(p, pl.n_ctas, s)
                                   : uaa::launch_partial_tc(p, tk, tv, ts, d->kv_dtype, pl.n_head_tiles, pl.n_ctas, s);
@@ -442,6 +470,16 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     return UAA_OK;
 }
 
+// Steps 1 and 2: one fused launch for the tensor-core kernel, append then
+// partial for the fp32 kernel.
+uaa_status run_append_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws,
+                              const Plan& pl, cudaStream_t s)
+{
+    if (pl.kernel == 1) return run_partial(d, a, ws, pl, s, true);
+    UAA_TRY(run_append(d, a, ws, pl, s));
+    return run_partial(d, a, ws, pl, s);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- exported C ABI
@@ -472,13 +510,20 @@ uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_arg
     return run_combine(desc, args, ws, pl, stream);
 }
 
+uaa_status uaa_decode_attn_append_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                          const uaa_workspace* ws, cudaStream_t stream)
+{
+    Plan pl{};
+    UAA_TRY(prepare(desc, args, ws, true, &pl));
+    return run_append_partial(desc, args, ws, pl, stream);
+}
+
 uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args, const uaa_workspace* ws,
                            cudaStream_t stream)
 {
     Plan pl{};
     UAA_TRY(prepare(desc, args, ws, true, &pl));
-    UAA_TRY(run_append(desc, args, ws, pl, stream));
-    UAA_TRY(run_partial(desc, args, ws, pl, stream));
+    UAA_TRY(run_append_partial(desc, args, ws, pl, stream));
     return run_combine(desc, args, ws, pl, stream);
 }
 
@@ -628,7 +673,6 @@ extern "C" uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const ua
     // the status word is the only scratch that must start at zero
     const cudaError_t e = cudaMemsetAsync(static_cast<char*>(scratch) + pl.off_status, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch status word");
-    UAA_TRY(run_append(desc, args, &ws, pl, stream));
-    UAA_TRY(run_partial(desc, args, &ws, pl, stream));
+    UAA_TRY(run_append_partial(desc, args, &ws, pl, stream));
     return run_combine(desc, args, &ws, pl, stream);
 }

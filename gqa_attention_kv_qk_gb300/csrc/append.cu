@@ -2,14 +2,13 @@
 // the absolute KV index, and the append of the new k / v rows to the cache.
 //
 // One CTA of 16 warps per sequence. The CTA first builds the cos / sin table of
-// the sequence's position (the angle pos * theta'_p is formed and reduced in
-// fp64, then rounded to fp32), while each warp loads its first head row; then
-// each warp takes whole rows (loading the next while it processes the current
-// one): q rows go to
-// the workspace pre-multiplied by the partial kernel's logit prescale, k rows
-// and v rows go to slot seq_lens[b] of the cache. vq8 values are quantised in
-// fp32 with IEEE division and round-half-even, the storage rule of the vq8
-// cache (llamay "Models and formats", "The KV cache, in three precisions").
+// the sequence's position (rope_cos_sin) while each warp loads its first head
+// row; then each warp takes whole rows, loading the next while it processes the
+// current one: q rows go to the workspace pre-multiplied by the partial
+// kernel's logit prescale, k rows and v rows go to slot seq_lens[b] of the
+// cache. vq8 values are quantised in fp32 with IEEE division and
+// round-half-even, the storage rule of the vq8 cache (llamay "Models and
+// formats", "The KV cache, in three precisions").
 #include "internal.cuh"
 
 namespace uaa {
@@ -25,8 +24,7 @@ __device__ __forceinline__ void store_kv(void* cache, int dtype, size_t i, float
         static_cast<__nv_bfloat16*>(cache)[i] = __float2bfloat16_rn(v);
 }
 
-// vq8 storage rule on a row of D fp32 values held EPL per lane:
-// s = max|v| / 127, code = rint(v / s), |code| <= 127; s = 0 gives codes 0.
+// vq8 storage of a row of D fp32 values held EPL per lane (vq8_scale, vq8_code).
 template <int EPL>
 __device__ __forceinline__ void quantize_row(const float (&x)[EPL], int lane, int8_t* codes,
                                              float* scale)
@@ -34,14 +32,9 @@ __device__ __forceinline__ void quantize_row(const float (&x)[EPL], int lane, in
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
+    const float s = vq8_scale(warp_max(amax));
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        float c = 0.f;
-        if (s != 0.f) c = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.f), 127.f);
-        codes[lane + 32 * i] = static_cast<int8_t>(static_cast<int>(c));
-    }
+    for (int i = 0; i < EPL; ++i) codes[lane + 32 * i] = vq8_code(x[i], s);
     if (lane == 0) *scale = s;
 }
 
@@ -57,7 +50,7 @@ __device__ __forceinline__ const void* row_source(const AppendParams& p, int b, 
     return r < p.Hq + p.Hkv ? p.k_new : p.v_new;
 }
 
-template <int D>
+template <int D, typename T>  // T: the io element type (float or __nv_bfloat16)
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p)
 {
     constexpr int EPL = D / 32;  // row elements per lane
@@ -77,7 +70,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
         size_t at;
         const void* src = row_source(p, b, warp, at);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) nxt[i] = load_elem(src, p.io_dtype, at + lane + 32 * i);
+        for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
     }
 
     const int L = p.seq_lens[b];
@@ -88,16 +81,9 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     }
     const int pos = fits ? L : 0;
 
-    // cos / sin of pos * theta'_p: the angle in units of pi, t = pos * theta'_p / pi,
-    // is formed in fp64 and reduced exactly to t - 2 rint(t / 2) in [-1, 1]; the
-    // reduced value is rounded to fp32 for sincospif (error ~ 2^-24 pi rad).
-    for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-        const double t = static_cast<double>(pos) * p.inv_freq_over_pi[i];
-        const double r = fma(-2.0, rint(0.5 * t), t);
-        float sn, cn;
-        sincospif(static_cast<float>(r), &sn, &cn);
-        cs[i] = make_float2(cn * p.mscale, sn * p.mscale);
-    }
+#pragma unroll
+    for (int i0 = 0; i0 < HALF; i0 += 32)  // warp w takes pairs 32 w .. 32 w + 31
+        if (warp == i0 / 32) cs[i0 + lane] = rope_cos_sin(pos, param_at_lane(p.inv_freq_over_pi + i0, lane), p.mscale);
     __syncthreads();  // the cos / sin table is complete
     for (int r = warp; r < n_rows; r += kAppendWarps) {
 #pragma unroll
@@ -106,7 +92,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
             size_t at;
             const void* src = row_source(p, b, r + kAppendWarps, at);
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) nxt[i] = load_elem(src, p.io_dtype, at + lane + 32 * i);
+            for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
         }
         const bool is_q = r < p.Hq;
         const bool is_k = !is_q && r < p.Hq + p.Hkv;
@@ -131,7 +117,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
 #pragma unroll
             for (int i = 0; i < EPL; ++i) ss += x[i] * x[i];
             ss = warp_sum(ss);
-            const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + p.eps);
+            const float inv = rms_inv(ss, D, p.eps);
             const float* w = is_q ? p.q_norm_w : p.k_norm_w;
 #pragma unroll
             for (int i = 0; i < EPL; ++i) x[i] = x[i] * inv * w[lane + 32 * i];
@@ -143,10 +129,8 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
         for (int pp = lane; pp < HALF; pp += 32) {
             const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
             const int ib = p.style == UAA_ROPE_NEOX ? pp + HALF : 2 * pp + 1;
-            const float a = rowbuf[warp][ia], bb = rowbuf[warp][ib];
-            const float2 c = cs[pp];
-            const float ya = a * c.x - bb * c.y;
-            const float yb = a * c.y + bb * c.x;
+            float ya = rowbuf[warp][ia], yb = rowbuf[warp][ib];
+            rope_rotate(ya, yb, cs[pp]);
             if (is_q) {
                 float* qp = p.q_prime + in_row;
                 qp[ia] = ya * p.qscale;
@@ -190,10 +174,17 @@ __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
     const dim3 grid(p.B), block(kAppendWarps * 32);
+    const bool f32 = p.io_dtype == UAA_DTYPE_F32;
     switch (p.D) {
-    case 64: return launch_dependent(append_kernel<64>, grid, block, 0, s, p);
-    case 128: return launch_dependent(append_kernel<128>, grid, block, 0, s, p);
-    case 256: return launch_dependent(append_kernel<256>, grid, block, 0, s, p);
+    case 64:
+        return f32 ? launch_dependent(append_kernel<64, float>, grid, block, 0, s, p)
+                   : launch_dependent(append_kernel<64, __nv_bfloat16>, grid, block, 0, s, p);
+    case 128:
+        return f32 ? launch_dependent(append_kernel<128, float>, grid, block, 0, s, p)
+                   : launch_dependent(append_kernel<128, __nv_bfloat16>, grid, block, 0, s, p);
+    case 256:
+        return f32 ? launch_dependent(append_kernel<256, float>, grid, block, 0, s, p)
+                   : launch_dependent(append_kernel<256, __nv_bfloat16>, grid, block, 0, s, p);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -66,10 +66,10 @@ struct PartialParams {
     int mg;                 // 64-key tiles per stage
     float softcap_log2e;    // 0: no softcap; else softcap * log2(e)
     const float* q_prime;   // [B][Hq][D] (slice-relative: already offset by b_off)
-    const void* k_cache;    // whole caches (rows indexed with b_off + b)
-    const void* v_cache;
-    const float* v_scale;
-    const int* seq_lens;    // slice-relative
+    void* k_cache;          // whole caches (rows indexed with b_off + b)
+    void* v_cache;
+    float* v_scale;
+    int* seq_lens;          // slice-relative (advanced by the fused kernel only)
     int* prefix;            // [B + 1] stage prefix over sequences, written for the combine
     float* rec_o;           // [2P][heads_per_cta][D]
     float* rec_lse;         // [2P][heads_per_cta]
@@ -77,6 +77,22 @@ struct PartialParams {
     void* out;              // [B][Hq][D] slice-relative
     int out_dtype;
     unsigned* status;
+    // Fused append (steps 1 and 2 in one kernel): seq_lens hold the lengths
+    // before the step; a sequence with room (0 <= L < cap) gets its new token at
+    // slot L, attends keys up to and including it, and leaves with L + 1.
+    int fused;
+    int max_len;
+    unsigned* arrivals;     // grid arrival counter (zero between launches)
+    const void* q;          // [B][Hq][D] io_dtype, slice-relative
+    const void* k_new;      // [B][Hkv][D] io_dtype, slice-relative
+    const void* v_new;
+    int io_dtype, kv_dtype;
+    int style, qk_norm;
+    float eps, qscale, mscale;
+    const float* q_norm_w;
+    const float* k_norm_w;
+    float* q_rot_out;       // optional [B][Hq][D], slice-relative
+    double inv_freq_over_pi[kMaxHeadDim / 2];
 };
 
 struct CombineParams {
@@ -192,11 +208,20 @@ __device__ __forceinline__ void visible_keys(int n, int window, int cap, int& lo
     if (hi > cap) hi = cap;
 }
 
-// Block-wide prefix[0..B] of units * stages per sequence into shared memory
-// (warp 0 scans, every thread returns after the barrier). Writes the prefix to
-// `global_copy` too when it is not null.
+// Keys that the partial kernel attends for a sequence holding L keys: with the
+// fused append the new token (slot L) is included when it fits the cache.
+__device__ __forceinline__ void sequence_keys(int L, int window, int cap, bool fused, int& lo, int& hi)
+{
+    visible_keys(fused && L >= 0 && L < cap ? L + 1 : L, window, cap, lo, hi);
+}
+
+// Block-wide prefix[0..B] of units * stages per sequence into shared memory, and
+// the lengths themselves into lens[0..B) (warp 0 scans, every thread returns
+// after the barrier; nothing reads seq_lens afterwards). Writes the prefix to
+// `global_copy` too when it is not null; flags go to `status` when it is not null.
 __device__ inline void build_stage_prefix(const int* seq_lens, int B, int window, int cap, int mg, int units,
-                                          int* prefix, int* global_copy, unsigned* status)
+                                          int* prefix, int* lens, int* global_copy, unsigned* status,
+                                          bool fused = false, int max_len = 0)
 {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
@@ -210,9 +235,11 @@ __device__ inline void build_stage_prefix(const int* seq_lens, int B, int window
             int v = 0;
             if (b < B) {
                 const int n = seq_lens[b];
-                if (n > cap && status) atomicOr(status, UAA_DEVFLAG_CAPACITY);
+                lens[b] = n;
+                if (status && (fused ? (n < 0 || n >= cap) : n > cap)) atomicOr(status, UAA_DEVFLAG_CAPACITY);
+                if (status && fused && n >= 0 && n < cap && n > max_len) atomicOr(status, UAA_DEVFLAG_LEN_HINT);
                 int lo, hi;
-                visible_keys(n, window, cap, lo, hi);
+                sequence_keys(n, window, cap, fused, lo, hi);
                 v = units * stages_of(lo, hi, mg);
             }
 #pragma unroll
@@ -253,8 +280,9 @@ struct Segment {
     bool whole;     // the segment is the whole unit
 };
 
-__device__ __forceinline__ Segment segment_at(const int* prefix, const int* seq_lens, int B, int window, int cap,
-                                              int head_groups, int units, long long pos, long long end)
+__device__ __forceinline__ Segment segment_at(const int* prefix, const int* lens, int B, int window, int cap,
+                                              int head_groups, int units, long long pos, long long end,
+                                              bool fused = false)
 {
     Segment sg;
     sg.b = find_sequence(prefix, B, pos);
@@ -267,7 +295,7 @@ __device__ __forceinline__ Segment segment_at(const int* prefix, const int* seq_
     sg.n_st = left < sg.stages - sg.st0 ? static_cast<int>(left) : sg.stages - sg.st0;
     sg.kvh = u / head_groups;
     sg.hg = u - sg.kvh * head_groups;
-    visible_keys(seq_lens[sg.b], window, cap, sg.lo, sg.hi);
+    sequence_keys(lens[sg.b], window, cap, fused, sg.lo, sg.hi);
     sg.whole = sg.st0 == 0 && sg.n_st == sg.stages;
     return sg;
 }
@@ -290,6 +318,79 @@ __device__ __forceinline__ float load_elem(const void* base, int dtype, size_t i
 {
     if (dtype == UAA_DTYPE_F32) return static_cast<const float*>(base)[i];
     return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+}
+
+// Element i of a row of T (float or __nv_bfloat16) as fp32. Loops over row
+// elements take T as a template parameter: a per-element branch on a run-time
+// dtype keeps the loads of a loop from issuing back to back.
+template <typename T>
+__device__ __forceinline__ float load_as_float(const void* base, size_t i)
+{
+    if constexpr (sizeof(T) == 4)
+        return static_cast<const float*>(base)[i];
+    else
+        return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+}
+
+// Elements i and i + 1 (i even).
+__device__ __forceinline__ float2 load_pair(const void* base, int dtype, size_t i)
+{
+    if (dtype == UAA_DTYPE_F32) return *reinterpret_cast<const float2*>(static_cast<const float*>(base) + i);
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(base) + i));
+}
+
+// ---------------------------------------------------------------- append arithmetic
+// One definition each, used by the separate append kernel and by the fused one.
+
+// cos and sin of pos * theta'_p, times mscale. The angle in units of pi,
+// t = pos * theta'_p / pi, is formed in fp64 and reduced exactly to
+// t - 2 rint(t / 2) in [-1, 1]; the reduced value is rounded to fp32 for
+// sincospif (error ~ 2^-24 pi rad at any position).
+__device__ __forceinline__ float2 rope_cos_sin(int pos, double inv_freq_over_pi, float mscale)
+{
+    const double t = static_cast<double>(pos) * inv_freq_over_pi;
+    const double r = fma(-2.0, rint(0.5 * t), t);
+    float sn, cn;
+    sincospif(static_cast<float>(r), &sn, &cn);
+    return make_float2(cn * mscale, sn * mscale);
+}
+
+// Entry `lane` of 32 consecutive kernel-parameter values (table32 a fixed
+// offset into the kernel's parameters). Each read has a fixed offset: a
+// per-lane index into kernel parameters would serialise the lanes' reads on the
+// constant cache.
+__device__ __forceinline__ double param_at_lane(const double* table32, int lane)
+{
+    double v = 0.0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v = lane == i ? table32[i] : v;
+    return v;
+}
+
+// Rotation of pair (a, b) by the angle whose (cos, sin) is cs.
+__device__ __forceinline__ void rope_rotate(float& a, float& b, float2 cs)
+{
+    const float ya = a * cs.x - b * cs.y;
+    const float yb = a * cs.y + b * cs.x;
+    a = ya;
+    b = yb;
+}
+
+// RMSNorm factor 1 / sqrt(mean(x^2) + eps) from the row's sum of squares.
+__device__ __forceinline__ float rms_inv(float sum_sq, int D, float eps)
+{
+    return 1.0f / sqrtf(sum_sq / static_cast<float>(D) + eps);
+}
+
+// vq8 storage rule of a row with max|v| = amax: s = amax / 127 (IEEE division),
+// code = rint(v / s) with ties to even, |code| <= 127; s = 0 gives codes 0.
+__device__ __forceinline__ float vq8_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+
+__device__ __forceinline__ int8_t vq8_code(float v, float s)
+{
+    if (s == 0.f) return 0;
+    const float c = fminf(fmaxf(rintf(__fdiv_rn(v, s)), -127.f), 127.f);
+    return static_cast<int8_t>(static_cast<int>(c));
 }
 
 }  // namespace uaa

@@ -27,19 +27,20 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
     __shared__ float red_l[kSimtWarps][kSimtHeads];
     __shared__ float red_o[kSimtWarps][kSimtHeads][D];
     __shared__ int prefix[kMaxSliceBatch + 1];
+    __shared__ int lens[kMaxSliceBatch];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.Hkv * p.head_groups;
     grid_dependency_wait();  // the append's lengths, q rows and cache rows are complete
-    build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, 1, units, prefix, blockIdx.x == 0 ? p.prefix : nullptr,
-                       p.status);
+    build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, 1, units, prefix, lens,
+                       blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr);
     const long long T = prefix[p.B];
     const int P = T < gridDim.x ? static_cast<int>(T) : static_cast<int>(gridDim.x);  // every range non-empty
     const long long s_c = static_cast<int>(blockIdx.x) < P ? range_start(blockIdx.x, T, P) : 0;
     const long long e_c = static_cast<int>(blockIdx.x) < P ? range_start(blockIdx.x + 1, T, P) : 0;
 
     for (long long pos = s_c; pos < e_c;) {
-        const Segment sg = segment_at(prefix, p.seq_lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
+        const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
         const int h0 = sg.kvh * p.G + sg.hg * kSimtHeads;
         const int nh = min(kSimtHeads, p.G - sg.hg * kSimtHeads);
         const int t0 = sg.lo / kTileKeys;

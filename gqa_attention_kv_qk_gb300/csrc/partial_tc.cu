@@ -7,7 +7,19 @@
 // kv head, head group); every query head of the unit's group (up to 8 * NHT) is
 // served from the same K/V stage, so each key row leaves HBM once.
 //
-// Warp roles (160 threads):
+// With PartialParams.fused the same kernel also performs the append of the
+// step (steps 1 and 2 in one launch); otherwise it reads the q' rows that the
+// separate append left in the workspace.
+//
+// Warp roles (192 threads):
+//   warp 5 (prep): walks the same segments one ahead of the consumers and
+//     writes each segment's q' rows, as bf16 hi + lo fragments, into a shared
+//     slot: fused, it normalises, rotates and prescales the unit's q rows
+//     itself (lane j takes rotation pairs j + 32 i, both pairings lane-local)
+//     and, for the segment that ends a unit, forms the new key row (RMSNorm,
+//     rotation, bf16) and value row (bf16, or vq8 codes + scale) into one of
+//     two staging slots and, once per kv head, into the cache; the last CTA to
+//     have read the lengths advances seq_lens.
 //   warp 4 (producer): one lane walks the CTA's segments and streams their
 //     stages, TK = 64 MG keys each, with 2-D TMA loads (cp.async.bulk.tensor)
 //     into a ring of kStages stages, straight across segment boundaries. Key and
@@ -31,6 +43,9 @@
 //       fp16. The per-key scale is folded into P; to keep P * scale inside
 //       [0, 1] it is divided by the warp's running maximum scale r, and O is
 //       kept in units of r (a new maximum rescales O as a new logit maximum does).
+//     The warp that owns the new key's row copies the staged rows over that
+//     row of the unit's last stage after it lands (the tile load brought
+//     whatever the slot held before the step).
 //   At the end of a segment the four warp states are merged through the
 //   shared memory of the segment's last stage (held back from the producer
 //   until the merge is done). A whole unit writes its output rows, with the
@@ -47,7 +62,9 @@ namespace uaa {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;  // warp 4
+constexpr int kPrepWarp = kConsumerWarps + 1;  // warp 5
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -58,10 +75,15 @@ struct KeyGroups {
     static constexpr int kMG = D == 64 ? 2 : 1;
 };
 
-template <int D, bool VQ8>
+// Shared memory, from a 1024-byte aligned base: the ring of kStages stages |
+// full / empty barriers per stage | q-full, q-empty, q-first barriers | stage prefix |
+// lengths | q' fragment slot | two new-row staging slots. The ring takes what the
+// per-CTA budget leaves (two CTAs per SM below head_dim 256).
+template <int D, bool VQ8, int NHT>
 struct Shape {
     static constexpr int kMG = KeyGroups<D>::kMG;
     static constexpr int kTK = kTileKeys * kMG;             // keys per stage
+    static constexpr int kHC = 8 * NHT;                     // query heads of a unit
     static constexpr int kBoxBytes = kTK * 128;             // kTK rows x 128 bytes
     static constexpr int kKBoxes = D / 64;                  // 128-byte column boxes of a bf16 row
     static constexpr int kVBoxes = VQ8 ? (D > 128 ? D / 128 : 1) : D / 64;
@@ -70,12 +92,22 @@ struct Shape {
     static constexpr int kSBytes = VQ8 ? kTK * 4 : 0;
     static constexpr int kStageBytes = round_up(kKBytes + kVBytes + kSBytes, 1024);
     static constexpr int kTxBytes = kKBytes + kVBytes + kSBytes;
-    static constexpr int kBudget = D == 256 ? 196608 : 104448;
-    static constexpr int kStagesRaw = kBudget / kStageBytes;
-    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
-    static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kPrefixBytes = round_up((kMaxSliceBatch + 1) * 4, 16);
-    static constexpr int kSmemBytes = 1024 + kRingBytes + 16 * kStages + kPrefixBytes;
+    static constexpr int kLensBytes = kMaxSliceBatch * 4;
+    // q' of one head: D / 2 dim pairs as (bf16x2 hi, bf16x2 lo), rows padded by 32
+    // bytes so the 8 rows a warp reads at once fall in distinct banks
+    static constexpr int kFragRow = D * 4 + 32;
+    static constexpr int kFragBytes = kHC * kFragRow;
+    // a new key row (bf16) and value row (bf16, or int8 codes + fp32 scale)
+    static constexpr int kNewRowBytes = round_up(2 * D + (VQ8 ? D + 4 : 2 * D), 16);
+    static constexpr int kFixedBytes = 1024 + 32 + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes;
+    static constexpr int kCtaBudget = D == 256 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
+    static constexpr int kStagesRaw = (kCtaBudget - kFixedBytes) / (kStageBytes + 16);
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static_assert(kStages >= 2, "a ring of at least two stages");
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kFixedBytes + kRingBytes + 16 * kStages;
+    static_assert(kSmemBytes <= kCtaBudget, "shared memory budget of one CTA");
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a bf16 stage: boxes of
@@ -138,12 +170,259 @@ __device__ __forceinline__ void widen_code_pairs(uint32_t r, uint32_t& d_even, u
 
 __device__ __forceinline__ bool key_ok(int k, int lo, int hi) { return k >= lo && k < hi; }
 
+// bf16 hi + lo parts of x into element e of a q' fragment row.
+__device__ __forceinline__ void store_frag(uint8_t* row, int e, float x)
+{
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+    *reinterpret_cast<__nv_bfloat16*>(row + (e >> 1) * 8 + (e & 1) * 2) = h;
+    *reinterpret_cast<__nv_bfloat16*>(row + (e >> 1) * 8 + 4 + (e & 1) * 2) = l;
+}
+
+// Prep warp, fused append: q' rows of the unit's heads h0 .. h0 + nh - 1 of
+// sequence b (RMSNorm, rotation, logit prescale) into the fragment slot; lane
+// takes rotation pairs lane + 32 j with (cos, sin) csr[j], recomputed for
+// position pos (after the rows' loads are issued) when new_seq. Rows of missing
+// heads are zero.
+template <int D, int HC, typename T>
+__device__ __forceinline__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool write_rot,
+                                             bool new_seq, int pos, const double (&freq)[D / 64],
+                                             float2 (&csr)[D / 64], uint8_t* frag, int row_bytes, int lane)
+{
+    constexpr int NP = D / 64;
+#pragma unroll 1
+    for (int hc0 = 0; hc0 < HC; hc0 += 8) {
+        float xa[8][NP], xb[8][NP];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // all eight rows' loads first
+            const size_t qoff = (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int pp = lane + 32 * j;
+                const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
+                const int ib = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
+                xa[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + ia) : 0.f;
+                xb[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + ib) : 0.f;
+            }
+        }
+        if (new_seq && hc0 == 0) {  // the rows' loads are in flight: (cos, sin) of this sequence's position
+#pragma unroll
+            for (int j = 0; j < NP; ++j) csr[j] = rope_cos_sin(pos, freq[j], p.mscale);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint8_t* row = frag + (hc0 + i) * row_bytes;
+            const bool hv = hc0 + i < nh;
+            if (p.qk_norm && hv) {
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < NP; ++j) ss += xa[i][j] * xa[i][j] + xb[i][j] * xb[i][j];
+                const float inv = rms_inv(warp_sum(ss), D, p.eps);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const int pp = lane + 32 * j;
+                    const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
+                    const int ib = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
+                    xa[i][j] = xa[i][j] * inv * p.q_norm_w[ia];
+                    xb[i][j] = xb[i][j] * inv * p.q_norm_w[ib];
+                }
+            }
+            const size_t qoff = (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int pp = lane + 32 * j;
+                const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
+                const int ib = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
+                float ya = xa[i][j], yb = xb[i][j];
+                if (hv) rope_rotate(ya, yb, csr[j]);
+                if (write_rot && hv) {
+                    p.q_rot_out[qoff + ia] = ya;
+                    p.q_rot_out[qoff + ib] = yb;
+                }
+                store_frag(row, ia, ya * p.qscale);
+                store_frag(row, ib, yb * p.qscale);
+            }
+        }
+    }
+}
+
+// Prep warp, separate append: the workspace's q' rows (already rotated and
+// prescaled, fp32) into the fragment slot, eight rows' loads at a time.
+template <int D, int HC>
+__device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int h0, int nh, uint8_t* frag,
+                                              int row_bytes, int lane)
+{
+#pragma unroll 1
+    for (int hc0 = 0; hc0 < HC; hc0 += 8) {
+        float2 x[8][D / 64];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float* qrow = p.q_prime + (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j)
+                x[i][j] = hc0 + i < nh ? *reinterpret_cast<const float2*>(qrow + 2 * lane + 64 * j)
+                                       : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) {
+                uint32_t h, l;
+                split_bf16(x[i][j].x, x[i][j].y, h, l);
+                *reinterpret_cast<uint2*>(frag + (hc0 + i) * row_bytes + (lane + 32 * j) * 8) = make_uint2(h, l);
+            }
+    }
+}
+
+// Fused append, one warp per CTA at kernel start (while warp 0 reads the
+// lengths, before any tile load): brings this CTA's share of the step's q,
+// k_new and v_new rows (128-byte lines c, c + P, c + 2P, ...) into L2 with the
+// evict-last policy, so that the prep warp's reads of them find them there (the
+// key stream, loaded evict-first, does not push them out).
+__device__ __forceinline__ void prefetch_step_inputs(const PartialParams& p, int D, int lane)
+{
+    const size_t esz = p.io_dtype == UAA_DTYPE_F32 ? 4 : 2;
+    const size_t q_lines = (static_cast<size_t>(p.B) * p.Hq * D * esz + 127) / 128;
+    const size_t kv_lines = (static_cast<size_t>(p.B) * p.Hkv * D * esz + 127) / 128;
+    const size_t total = q_lines + 2 * kv_lines;
+    for (size_t l = blockIdx.x + static_cast<size_t>(gridDim.x) * lane; l < total; l += 32 * gridDim.x) {
+        const char* a = l < q_lines ? static_cast<const char*>(p.q) + 128 * l
+                        : l < q_lines + kv_lines ? static_cast<const char*>(p.k_new) + 128 * (l - q_lines)
+                                                 : static_cast<const char*>(p.v_new) + 128 * (l - q_lines - kv_lines);
+        ptx::prefetch_l2_keep(a);
+    }
+}
+
+// Starts bringing the new k and v rows of (b, kvh) into L2 (their loads follow
+// the q rows' processing).
+template <int D>
+__device__ __forceinline__ void prefetch_new_rows(const PartialParams& p, int b, int kvh, int lane)
+{
+    const int bytes = D * (p.io_dtype == UAA_DTYPE_F32 ? 4 : 2);
+    const size_t off = (static_cast<size_t>(b) * p.Hkv + kvh) * bytes;
+    if (lane < 2 * bytes / 128) {
+        const int row = lane >= bytes / 128 ? 1 : 0;
+        const char* src = static_cast<const char*>(row ? p.v_new : p.k_new) + off + 128 * (lane - row * (bytes / 128));
+        ptx::prefetch_l2_keep(src);
+    }
+}
+
+// Prep warp, fused append: the new key row (RMSNorm, rotation, bf16) and value
+// row (bf16, or vq8 codes and scale) of (b, kvh) into a staging slot (key at 0,
+// value at 2 D, vq8 scale at 3 D), and into the cache at slot L when `store`.
+template <int D, bool VQ8, typename T>
+__device__ __forceinline__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L,
+                                              const float2 (&csr)[D / 64], uint8_t* staging, bool store, int lane)
+{
+    constexpr int NP = D / 64;   // rotation pairs per lane
+    constexpr int EPL = D / 32;  // values per lane
+    const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D;
+    const size_t slot = (static_cast<size_t>(p.b_off + b) * p.Hkv + kvh) * p.cap + L;
+    float ka[NP], kb[NP], v[EPL];
+    int ia[NP], ib[NP];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        const int pp = lane + 32 * j;
+        ia[j] = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
+        ib[j] = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
+        ka[j] = load_as_float<T>(p.k_new, src + ia[j]);
+        kb[j] = load_as_float<T>(p.k_new, src + ib[j]);
+        ss += ka[j] * ka[j] + kb[j] * kb[j];
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) v[i] = load_as_float<T>(p.v_new, src + lane + 32 * i);
+    if (p.qk_norm) {
+        const float inv = rms_inv(warp_sum(ss), D, p.eps);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            ka[j] = ka[j] * inv * p.k_norm_w[ia[j]];
+            kb[j] = kb[j] * inv * p.k_norm_w[ib[j]];
+        }
+    }
+    __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(staging);
+    __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.k_cache) + slot * D;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        rope_rotate(ka[j], kb[j], csr[j]);
+        const __nv_bfloat16 ha = __float2bfloat16_rn(ka[j]), hb = __float2bfloat16_rn(kb[j]);
+        ks[ia[j]] = ha;
+        ks[ib[j]] = hb;
+        if (store) {
+            kc[ia[j]] = ha;
+            kc[ib[j]] = hb;
+        }
+    }
+    if (VQ8) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float sc = vq8_scale(warp_max(amax));
+        int8_t* vs = reinterpret_cast<int8_t*>(staging + 2 * D);
+        int8_t* vc = static_cast<int8_t*>(p.v_cache) + slot * D;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int8_t code = vq8_code(v[i], sc);
+            vs[lane + 32 * i] = code;
+            if (store) vc[lane + 32 * i] = code;
+        }
+        if (lane == 0) {
+            *reinterpret_cast<float*>(staging + 3 * D) = sc;
+            if (store) p.v_scale[slot] = sc;
+        }
+    } else {
+        __nv_bfloat16* vs = reinterpret_cast<__nv_bfloat16*>(staging + 2 * D);
+        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(p.v_cache) + slot * D;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
+            vs[lane + 32 * i] = h;
+            if (store) vc[lane + 32 * i] = h;
+        }
+    }
+}
+
+// Fused append, one thread per CTA, after the CTA's lengths are in shared
+// memory: counts the CTA in; the last CTA of the grid to do so (every other CTA
+// has read seq_lens by then) advances each length whose token fitted. The
+// counter wraps to zero on the last arrival, ready for the next launch.
+__device__ __noinline__ void count_in_and_advance(const PartialParams& p, const int* lens)
+{
+    __threadfence();
+    if (atomicInc(p.arrivals, gridDim.x - 1) != gridDim.x - 1) return;
+    __threadfence();
+    for (int b = 0; b < p.B; ++b)
+        if (lens[b] >= 0 && lens[b] < p.cap) p.seq_lens[b] = lens[b] + 1;
+}
+
+// Owner warp of the new key: the staged rows over row r of the loaded stage.
+template <int D, bool VQ8, int TK>
+__device__ __forceinline__ void patch_stage_row(const uint8_t* staging, uint8_t* stage, int r, int k_bytes,
+                                                int v_bytes, int lane)
+{
+    for (int c = lane; c < D / 8; c += 32)
+        *reinterpret_cast<uint4*>(stage + tile_off<TK>(r, c)) = *reinterpret_cast<const uint4*>(staging + 16 * c);
+    if (VQ8) {
+        for (int c = lane; c < D / 16; c += 32)
+            *reinterpret_cast<uint4*>(stage + k_bytes + code_off<D, TK>(r, c)) =
+                *reinterpret_cast<const uint4*>(staging + 2 * D + 16 * c);
+        if (lane == 0)
+            *reinterpret_cast<float*>(stage + k_bytes + v_bytes + 4 * r) =
+                *reinterpret_cast<const float*>(staging + 3 * D);
+    } else {
+        for (int c = lane; c < D / 8; c += 32)
+            *reinterpret_cast<uint4*>(stage + k_bytes + tile_off<TK>(r, c)) =
+                *reinterpret_cast<const uint4*>(staging + 2 * D + 16 * c);
+    }
+    __syncwarp();
+}
+
 template <int D, bool VQ8, int NHT>
 __global__ void __launch_bounds__(kThreads, (D == 256 ? 1 : 2))
 partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_s, const PartialParams p)
 {
-    using SH = Shape<D, VQ8>;
+    using SH = Shape<D, VQ8, NHT>;
     constexpr int MG = SH::kMG;     // 16-key groups per warp per stage
     constexpr int TK = SH::kTK;     // keys per stage
     constexpr int KS = D / 16;      // k-steps of QK, m-tiles of PV
@@ -158,7 +437,13 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t bar_full = base + SH::kRingBytes;
     const uint32_t bar_empty = bar_full + 8 * SH::kStages;
-    int* prefix = reinterpret_cast<int*>(base_ptr + SH::kRingBytes + 16 * SH::kStages);
+    const uint32_t bar_qfull = bar_empty + 8 * SH::kStages;  // prep warp -> consumers: a segment's q' is ready
+    const uint32_t bar_qempty = bar_qfull + 8;               // consumers -> prep warp: the q' slot is free
+    const uint32_t bar_qfirst = bar_qfull + 16;              // prep warp -> producer: the first q' is ready
+    int* prefix = reinterpret_cast<int*>(base_ptr + SH::kRingBytes + 16 * SH::kStages + 32);
+    int* lens = prefix + SH::kPrefixBytes / 4;
+    uint8_t* frag = reinterpret_cast<uint8_t*>(lens) + SH::kLensBytes;
+    uint8_t* staging = frag + SH::kFragBytes;  // two slots of kNewRowBytes, by segment parity
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.Hkv * p.head_groups;
@@ -167,32 +452,58 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             ptx::mbar_init(bar_full + 8 * s, 1);
             ptx::mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
+        ptx::mbar_init(bar_qfull, 1);
+        ptx::mbar_init(bar_qempty, kConsumerWarps);
+        ptx::mbar_init(bar_qfirst, 1);  // completes once
         ptx::fence_barrier_init();
-    } else if (threadIdx.x == 32 * kConsumerWarps) {
+    } else if (threadIdx.x == 32 * kProducerWarp) {
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
         if (VQ8) ptx::prefetch_tensormap(&tm_s);
     }
-    grid_dependency_wait();  // the append's lengths, q rows and cache rows are complete
-    build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, MG, units, prefix, blockIdx.x == 0 ? p.prefix : nullptr,
-                       p.status);  // ends with __syncthreads
+    grid_dependency_wait();  // the step's inputs (and a separate append's rows) are complete
+    if (p.fused && warp == kPrepWarp) prefetch_step_inputs(p, D, lane);  // while warp 0 reads seq_lens
+    build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, MG, units, prefix, lens,
+                       blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr, p.fused != 0,
+                       p.max_len);  // ends with __syncthreads; seq_lens is not read again
     const long long T = prefix[p.B];
     const int P = T < gridDim.x ? static_cast<int>(T) : static_cast<int>(gridDim.x);  // every range non-empty
-    if (static_cast<int>(blockIdx.x) >= P) return;  // uniform over the CTA: no stages
+    // Fused append: every CTA counts in once its lengths are read (an active CTA's
+    // producer does so after its first ring fill, off the consumers' path); the
+    // last to count in advances seq_lens once its own work is issued.
+    if (static_cast<int>(blockIdx.x) >= P) {  // uniform over the CTA: no stages
+        if (threadIdx.x == 0 && p.fused) count_in_and_advance(p, lens);
+        return;
+    }
     const long long s_c = range_start(blockIdx.x, T, P), e_c = range_start(blockIdx.x + 1, T, P);
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             bool ok = true;
-            int it = 0;  // stages issued
+            bool counted = false;  // fused: this CTA has counted in
+            int it = 0;            // stages issued
+            const uint64_t stream_policy = ptx::l2_evict_first_policy();  // keys and values are read once
             for (long long pos = s_c; pos < e_c && ok;) {
-                const Segment sg = segment_at(prefix, p.seq_lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
+                const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c,
+                                              p.fused != 0);
                 const int head_row = (p.b_off + sg.b) * p.Hkv + sg.kvh;
                 const int row0 = head_row * p.cap;
                 const int t0 = sg.lo / kTileKeys;
                 for (int k = 0; k < sg.n_st; ++k, ++it) {
                     const int s = it % SH::kStages;
+                    if (p.fused && it == 1 && !ptx::mbar_wait(bar_qfirst, 0, kWaitLimitCycles)) {
+                        // The first stage is on its way; the rest of the ring waits for the first
+                        // q' rows, whose reads would otherwise queue behind the whole ring fill
+                        // (~5 us) while the consumers need both.
+                        atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    if (p.fused && !counted && it == SH::kStages) {  // the ring is full: wait time
+                        count_in_and_advance(p, lens);
+                        counted = true;
+                    }
                     if (it >= SH::kStages &&
                         !ptx::mbar_wait(bar_empty + 8 * s, ((it / SH::kStages) & 1) ^ 1, kWaitLimitCycles)) {
                         atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
@@ -206,24 +517,80 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     const int y = row0 + key;
 #pragma unroll
                     for (int c = 0; c < SH::kKBoxes; ++c)
-                        ptx::tma_load_2d(st + c * SH::kBoxBytes, &tm_k, c * 64, y, bar);
+                        ptx::tma_load_2d_hint(st + c * SH::kBoxBytes, &tm_k, c * 64, y, bar, stream_policy);
                     if (VQ8) {
 #pragma unroll
                         for (int c = 0; c < SH::kVBoxes; ++c)
-                            ptx::tma_load_2d(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 128, y, bar);
-                        ptx::tma_load_2d(st + SH::kKBytes + SH::kVBytes, &tm_s, key, head_row, bar);
+                            ptx::tma_load_2d_hint(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 128, y, bar,
+                                                  stream_policy);
+                        ptx::tma_load_2d_hint(st + SH::kKBytes + SH::kVBytes, &tm_s, key, head_row, bar,
+                                              stream_policy);
                     } else {
 #pragma unroll
                         for (int c = 0; c < SH::kVBoxes; ++c)
-                            ptx::tma_load_2d(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 64, y, bar);
+                            ptx::tma_load_2d_hint(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 64, y, bar,
+                                                  stream_policy);
                     }
                 }
                 pos += sg.n_st;
             }
+            if (p.fused && !counted) count_in_and_advance(p, lens);
             // Copies in flight land before the CTA may exit (bounded).
             const int first = it > SH::kStages ? it - SH::kStages : 0;
             for (int i = first; i < it && ok; ++i)
                 ok = ptx::mbar_wait(bar_full + 8 * (i % SH::kStages), (i / SH::kStages) & 1, kWaitLimitCycles);
+        }
+        return;
+    }
+
+    if (warp == kPrepWarp) {
+        // ------------------------------------------------------------ prep
+        // One segment ahead of the consumers: segment i's q' fragments (and, when
+        // the segment ends its unit and the new token fits, the new k / v rows in
+        // staging slot i mod 2) are written once the consumers have taken segment
+        // i - 1's fragments (which also means segment i - 2 is finished).
+        float2 csr[D / 64];
+        double freq[D / 64];  // theta'_p / pi of this lane's rotation pairs lane + 32 j
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) freq[j] = p.fused ? param_at_lane(p.inv_freq_over_pi + 32 * j, lane) : 0.0;
+        int cs_b = -1;  // the sequence csr belongs to
+        int seg = 0;
+        for (long long pos = s_c; pos < e_c; ++seg) {
+            const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c,
+                                          p.fused != 0);
+            if (seg > 0 && !ptx::mbar_wait(bar_qempty, (seg - 1) & 1, kWaitLimitCycles)) {
+                if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                break;
+            }
+            const int h0 = sg.kvh * p.G + sg.hg * HC;
+            const int nh = min(HC, p.G - sg.hg * HC);
+            if (p.fused) {
+                const int L = lens[sg.b];
+                const bool fits = L >= 0 && L < p.cap;
+                const bool ends = fits && sg.st0 + sg.n_st == sg.stages;
+                if (ends) prefetch_new_rows<D>(p, sg.b, sg.kvh, lane);
+                const bool rot = p.q_rot_out != nullptr && sg.st0 == 0;
+                uint8_t* st_row = staging + (seg & 1) * SH::kNewRowBytes;
+                if (p.io_dtype == UAA_DTYPE_F32) {
+                    prep_fused_q<D, HC, float>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq, csr, frag,
+                                               SH::kFragRow, lane);
+                    if (ends) prep_new_rows<D, VQ8, float>(p, sg.b, sg.kvh, L, csr, st_row, sg.hg == 0, lane);
+                } else {
+                    prep_fused_q<D, HC, __nv_bfloat16>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq, csr,
+                                                       frag, SH::kFragRow, lane);
+                    if (ends)
+                        prep_new_rows<D, VQ8, __nv_bfloat16>(p, sg.b, sg.kvh, L, csr, st_row, sg.hg == 0, lane);
+                }
+                cs_b = sg.b;
+            } else {
+                prep_loaded_q<D, HC>(p, sg.b, h0, nh, frag, SH::kFragRow, lane);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(bar_qfull);
+                if (seg == 0) ptx::mbar_arrive(bar_qfirst);
+            }
+            pos += sg.n_st;
         }
         return;
     }
@@ -235,31 +602,47 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // ldmatrix lane roles: matrix q = lane / 8, row r = lane % 8 of that matrix.
     const int lq = lane >> 3, lr = lane & 7;
     bool failed = false;
-    int it = 0;  // stages consumed
+    int it = 0;   // stages consumed
+    int seg = 0;  // segments consumed
 
-    for (long long pos = s_c; pos < e_c;) {
-        const Segment sg = segment_at(prefix, p.seq_lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
+    for (long long pos = s_c; pos < e_c; ++seg) {
+        const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c,
+                                      p.fused != 0);
         const int lo = sg.lo, hi = sg.hi;
         const int t0 = lo / kTileKeys;
         const int h0 = sg.kvh * p.G + sg.hg * HC;
         const int nh = min(HC, p.G - sg.hg * HC);
 
+        // fused append: the new key (slot L) is row new_r of the unit's last stage,
+        // which consumer warp new_w owns; -1 when this segment does not end the unit
+        const int L = lens[sg.b];
+        const bool fits = p.fused && L >= 0 && L < p.cap;
+        const int new_r =
+            fits && sg.st0 + sg.n_st == sg.stages ? L - (t0 + MG * (sg.stages - 1)) * kTileKeys : -1;
+        const int new_w = new_r >= 0 ? new_r / (16 * MG) : -1;
+
+        // this segment's q' fragments from the prep warp: head nt * 8 + g, dims
+        // 16 kk + 2t (+1) and 16 kk + 2t + 8 (+9), as (hi, lo) bf16 pairs
+        if (!failed && !ptx::mbar_wait(bar_qfull, seg & 1, kWaitLimitCycles)) {
+            failed = true;
+            if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+        }
         uint32_t qhi[NHT][KS][2], qlo[NHT][KS][2];
 #pragma unroll
         for (int nt = 0; nt < NHT; ++nt) {
-            const int head = nt * 8 + g;
-            const float* qrow = p.q_prime + (static_cast<size_t>(sg.b) * p.Hq + h0 + head) * D;
+            const uint8_t* row = frag + (nt * 8 + g) * SH::kFragRow;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-                float2 x01 = make_float2(0.f, 0.f), x89 = make_float2(0.f, 0.f);
-                if (head < nh) {
-                    x01 = *reinterpret_cast<const float2*>(qrow + 16 * kk + 2 * t);
-                    x89 = *reinterpret_cast<const float2*>(qrow + 16 * kk + 2 * t + 8);
-                }
-                split_bf16(x01.x, x01.y, qhi[nt][kk][0], qlo[nt][kk][0]);
-                split_bf16(x89.x, x89.y, qhi[nt][kk][1], qlo[nt][kk][1]);
+                const uint2 a = *reinterpret_cast<const uint2*>(row + (8 * kk + t) * 8);
+                const uint2 c = *reinterpret_cast<const uint2*>(row + (8 * kk + t + 4) * 8);
+                qhi[nt][kk][0] = a.x;
+                qlo[nt][kk][0] = a.y;
+                qhi[nt][kk][1] = c.x;
+                qlo[nt][kk][1] = c.y;
             }
         }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_qempty);  // the slot may be refilled
 
         float m[NHT][2], l[NHT][2], o[NHT][KS][4];
 #pragma unroll
@@ -278,6 +661,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             }
             const int kbase = (t0 + MG * (sg.st0 + k)) * kTileKeys + key_w;  // this warp's first key
+            if (!failed && warp == new_w && k + 1 == sg.n_st)  // the new key's row, over what the load brought
+                patch_stage_row<D, VQ8, TK>(staging + (seg & 1) * SH::kNewRowBytes, base_ptr + s * SH::kStageBytes,
+                                            new_r, SH::kKBytes, SH::kVBytes, lane);
             if (!failed && kbase < hi && kbase + 16 * MG > lo) {
                 const bool whole = kbase >= lo && kbase + 16 * MG <= hi;
                 const uint32_t st = base + s * SH::kStageBytes;
@@ -547,7 +933,7 @@ template <int D, bool VQ8, int NHT>
 cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& ts, int n_ctas, cudaStream_t s)
 {
-    using SH = Shape<D, VQ8>;
+    using SH = Shape<D, VQ8, NHT>;
     auto kern = partial_tc_kernel<D, VQ8, NHT>;
     static int configured_device_mask = 0;  // bit per device that has the smem attribute set
     int dev = 0;
@@ -567,12 +953,18 @@ int partial_tc_keys_per_stage(int D) { return D == 64 ? KeyGroups<64>::kMG * kTi
 
 size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles)
 {
-    (void)n_head_tiles;
     const bool vq8 = kv_dtype == UAA_DTYPE_VQ8;
+    if (n_head_tiles == 2) {
+        switch (D) {
+        case 64: return vq8 ? Shape<64, true, 2>::kSmemBytes : Shape<64, false, 2>::kSmemBytes;
+        case 128: return vq8 ? Shape<128, true, 2>::kSmemBytes : Shape<128, false, 2>::kSmemBytes;
+        default: return 0;
+        }
+    }
     switch (D) {
-    case 64: return vq8 ? Shape<64, true>::kSmemBytes : Shape<64, false>::kSmemBytes;
-    case 128: return vq8 ? Shape<128, true>::kSmemBytes : Shape<128, false>::kSmemBytes;
-    case 256: return vq8 ? Shape<256, true>::kSmemBytes : Shape<256, false>::kSmemBytes;
+    case 64: return vq8 ? Shape<64, true, 1>::kSmemBytes : Shape<64, false, 1>::kSmemBytes;
+    case 128: return vq8 ? Shape<128, true, 1>::kSmemBytes : Shape<128, false, 1>::kSmemBytes;
+    case 256: return vq8 ? Shape<256, true, 1>::kSmemBytes : Shape<256, false, 1>::kSmemBytes;
     default: return 0;
     }
 }

@@ -87,10 +87,10 @@ class DecodeLayer:
         a.q_rot = B.ptr(q_rot)
         return a
 
-    def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True):
+    def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True, q_rot=None):
         """One decode step (append, split-K partials, combine) on `stream`."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
-        B.uaa_decode_attn(self.desc, self.args(q, k_new, v_new, max_seq_len), self.ws, s)
+        B.uaa_decode_attn(self.desc, self.args(q, k_new, v_new, max_seq_len, q_rot=q_rot), self.ws, s)
         if advance_hint and max_seq_len is None:
             self.max_len_hint += 1
         return self.out
@@ -98,6 +98,11 @@ class DecodeLayer:
     def append(self, q, k_new, v_new, stream=None, q_rot=None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         B.uaa_rope_qk_norm_append(self.desc, self.args(q, k_new, v_new, q_rot=q_rot), self.ws, s)
+
+    def append_partial(self, q, k_new, v_new, stream=None, q_rot=None):
+        """Steps 1 and 2 (one fused kernel for bf16 / vq8 caches); follow with combine()."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        B.uaa_decode_attn_append_partial(self.desc, self.args(q, k_new, v_new, q_rot=q_rot), self.ws, s)
 
     def partial(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)

@@ -15,7 +15,9 @@
  *      log-sum-exp) per CTA it touches in the workspace.
  *   3. uaa_decode_attn_combine: log-sum-exp merge of those records, the sink
  *      logit added to the denominator, the remaining output rows written.
- *   uaa_decode_attn runs 1-3 on one stream.
+ *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16 and vq8 caches in one
+ *   kernel that forms q', k and v of the new token itself and attends the new
+ *   key from shared memory); uaa_decode_attn runs 1-3 on one stream.
 
  * Where the method is defined (page title, then section):
  *   - integral GQA ratio, head_dim set, 1/sqrt(head_dim) scale, the split-K
@@ -47,7 +49,8 @@
  *     message naming the fact (uaa_last_error), never approximated.
  *   - A step's entry points must receive the same descriptor and arguments;
  *     partial and combine run after the append of the same step (they read
- *     seq_lens after its increment).
+ *     seq_lens after its increment). The combine may follow either the
+ *     separate append + partial or uaa_decode_attn_append_partial.
  */
 #ifndef UAA_H
 #define UAA_H
@@ -61,7 +64,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 2
+#define UAA_ABI_VERSION 3
 
 typedef enum {
     UAA_OK = 0,
@@ -141,8 +144,10 @@ typedef struct {
 } uaa_step_args;
 
 /* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed
- * once after allocation. It holds the rotated q rows, the split partials and the
- * device status word; it must not be shared by steps that run concurrently. */
+ * once after allocation. It holds the rotated q rows, the split partials, the
+ * device status word and (the next uint32) the arrival counter of the fused
+ * kernel, which every completed launch leaves at zero; it must not be shared by
+ * steps that run concurrently. After UAA_DEVFLAG_TIMEOUT zero it again. */
 typedef struct {
     void* ptr;
     size_t bytes;
@@ -183,7 +188,20 @@ uaa_status uaa_decode_attn_partial(const uaa_attn_desc* desc, const uaa_step_arg
 uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
-/* Steps 1-3 on one stream: the whole decode step of one layer. */
+/* Steps 1 and 2 on one stream. For bf16 and vq8 caches this is one kernel: each
+ * unit normalises and rotates its q rows in registers (the workspace's q rows
+ * are not written), the warp that owns slot seq_lens[b] of a unit's last key
+ * stage forms the new k and v rows and writes them over that slot of the
+ * loaded stage (and, once per kv head, into the cache), and the last CTA to
+ * have read the lengths advances seq_lens. Results, cache rows and seq_lens are
+ * those of uaa_rope_qk_norm_append followed by uaa_decode_attn_partial, up to
+ * fp32 rounding order (appended key rows within one bf16 ulp). For fp32 caches
+ * it is those two launches. Follow it with uaa_decode_attn_combine. */
+uaa_status uaa_decode_attn_append_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
+                                          const uaa_workspace* ws, cudaStream_t stream);
+
+/* Steps 1-3 on one stream: the whole decode step of one layer
+ * (uaa_decode_attn_append_partial, then uaa_decode_attn_combine). */
 uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
                            const uaa_workspace* ws, cudaStream_t stream);
 
@@ -244,10 +262,11 @@ int32_t uaa_abi_version(void);
  *     first call on a device before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents. Each call clears the status word it starts from; device-side
- *     flags are therefore not reported (a step that breaks max_seq_len still
- *     writes NaN rows). Calls whose kernels overlap on the GPU (two streams, or
- *     two threads) race on the array: serialise them.
- * Results equal uaa_decode_attn's for the same desc and args. */
+ *     flags are therefore not reported (a sequence without a free slot is
+ *     silently not appended). Calls whose kernels overlap on the GPU (two
+ *     streams, or two threads) race on the array: serialise them.
+ * It runs the same kernels as uaa_decode_attn: results equal uaa_decode_attn's
+ * for the same desc and args. */
 uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const uaa_step_args* args,
                                   cudaStream_t stream);
 

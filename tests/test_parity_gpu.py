@@ -2,9 +2,11 @@
 same seeded inputs.
 
 The bar: cache-append slots, positions (seq_lens) and vq8 codes/scales bit-exact;
-appended key rows within one bf16 ulp (the GPU rotates in fp32, the oracle in
-fp64, both round to nearest even); outputs max|d| <= 2e-3 and mean|d| <= 2e-4
-against the fp64 oracle (fp32 outputs).
+appended key rows within one bf16 ulp plus 2^-18 of the row's largest entry (the
+GPU rotates in fp32, the oracle in fp64, both round to nearest even; where the
+rotation cancels, the fp32 error of a few ulps of the row's entries can move the
+small result across a bf16 rounding boundary); outputs max|d| <= 2e-3 and
+mean|d| <= 2e-4 against the fp64 oracle (fp32 outputs).
 """
 import math
 
@@ -46,10 +48,15 @@ def assert_out_close(got, want, what="out", tol_max=TOL_MAX, tol_mean=TOL_MEAN):
     return d.max(), d.mean()
 
 
+ENTRIES = ("split", "fused")
+
+
 def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero", check_qrot=True,
-                    max_seq_len=None):
+                    max_seq_len=None, entry="split"):
     """Run `steps` chained decode steps on both sides and compare everything the
-    step writes. Returns the worst (max, mean) output error."""
+    step writes. entry "split" runs the three step entry points one by one,
+    "fused" the whole-step call (one append+partial kernel for bf16 / vq8
+    caches, then the combine). Returns the worst (max, mean) output error."""
     case = host_case(cfg, lens=lens, cap=cap, fill_unused=fill_unused)
     a = oracle_arrays(case, oracle_mod)
     layer = gpu_layer(case)
@@ -64,10 +71,15 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         pre = a["seq_lens"].copy()
         q_rot = torch.empty((B_, Hq, D), dtype=torch.float32, device="cuda")
         dev = {k: v.cuda() for k, v in inp.items()}
-        layer.append(dev["q"], dev["k_new"], dev["v_new"], q_rot=q_rot)
-        layer.partial()
-        out = layer.combine().clone()
+        if entry == "split":
+            layer.append(dev["q"], dev["k_new"], dev["v_new"], q_rot=q_rot)
+            layer.partial()
+            out = layer.combine().clone()
+        else:
+            out = layer.step(dev["q"], dev["k_new"], dev["v_new"], q_rot=q_rot).clone()
         torch.cuda.synchronize()
+        # the fused kernel's arrival counter is back at zero after every launch
+        assert int(layer.ws_tensor[4:8].view(torch.int32).item()) == 0
         qr = oracle_mod.append(cfg, W.bits(inp["q"]).copy(), W.bits(inp["k_new"]).copy(),
                                W.bits(inp["v_new"]).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
                                a["v_cache"], a["v_scale"], a["seq_lens"])
@@ -87,7 +99,11 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
                 assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
             else:
                 ko = bf16_bits_to_f64(a["k_cache"][b, :, slot])
-                assert np.all(np.abs(kg - ko) <= np.abs(ko) * 2.0 ** -7 + 1e-30), "k row beyond one bf16 ulp"
+                # one bf16 ulp, plus the fp32 rotation's absolute error where the
+                # rotation cancels (|a cos - b sin| far below the row's entries)
+                row_max = np.abs(ko).max(axis=-1, keepdims=True)
+                assert np.all(np.abs(kg - ko) <= np.abs(ko) * 2.0 ** -7 + row_max * 2.0 ** -18), \
+                    "k row beyond one bf16 ulp + the fp32 rotation error"
                 if kv == "bf16":
                     vg = layer.v_cache[b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
                     assert np.array_equal(vg, a["v_cache"][b, :, slot])
@@ -111,12 +127,13 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("name", list(SMALL))
-def test_workload_parity_small(oracle_mod, name):
+def test_workload_parity_small(oracle_mod, name, entry):
     spec = SMALL[name]
     cfg = W.config(name, **spec.get("overrides", {}))
     for layer_cfg in W.layer_configs(cfg):
-        run_and_compare(oracle_mod, layer_cfg, spec["lens"], steps=cfg.get("steps", 1))
+        run_and_compare(oracle_mod, layer_cfg, spec["lens"], steps=cfg.get("steps", 1), entry=entry)
 
 
 # ------------------------------------------------------------------ edge cases
@@ -147,21 +164,37 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("spec", EDGE, ids=[e[0] for e in EDGE])
-def test_edge_cases(oracle_mod, spec):
+def test_edge_cases(oracle_mod, spec, entry):
     _, name, over, lens = spec
     cfg = W.config(name, **over)
     for layer_cfg in W.layer_configs(cfg):
-        run_and_compare(oracle_mod, layer_cfg, lens)
+        run_and_compare(oracle_mod, layer_cfg, lens, entry=entry)
 
 
-def test_unused_slots_hold_nan(oracle_mod):
-    """Slots beyond each sequence hold NaN; masking must keep them out of every result."""
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_unused_slots_hold_nan(oracle_mod, entry):
+    """Slots beyond each sequence hold NaN; masking must keep them out of every
+    result, and the fused kernel must replace the loaded NaN row of the new slot."""
     for name, over, lens in (("llama31_8b_decode", dict(batch=3, seq_len=400), [10, 200, 399]),
                              ("gptoss_vq8_sink", dict(batch=2, seq_len=400), [33, 380]),
-                             ("gemma2_9b_swa", dict(batch=2, seq_len=400, layers=[dict(window=70)]), [399, 90])):
+                             ("gemma2_9b_swa", dict(batch=2, seq_len=400, layers=[dict(window=70)]), [399, 90]),
+                             ("qwen3_8b_ragged", dict(batch=3, seq_len=(1, 400)), [0, 127, 128])):
         cfg = W.layer_configs(W.config(name, **over))[0]
-        run_and_compare(oracle_mod, cfg, lens, fill_unused="nan")
+        run_and_compare(oracle_mod, cfg, lens, fill_unused="nan", steps=2, entry=entry)
+
+
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_batch_slices(oracle_mod, entry):
+    """More sequences than one launch takes: the step runs as several slices
+    (each with its own stage prefix and records), lengths advance in every slice."""
+    cfg = W.config("qwen3_8b_ragged", batch=1100, n_q_heads=8, n_kv_heads=2, seq_len=(1, 130))
+    lay_batch = B.uaa_get_workspace_layout(B.make_desc(cfg), 1100, 130, 152)
+    assert lay_batch.n_slices == 2
+    rng = np.random.default_rng(5)
+    run_and_compare(oracle_mod, cfg, [int(x) for x in rng.integers(0, 130, size=1100)], cap=256, entry=entry,
+                    check_qrot=True)
 
 
 def test_bf16_output(oracle_mod):
@@ -240,6 +273,7 @@ def stream_k_segments(prefix, n_ctas, units, head_groups):
             pos += n
 
 
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("name,over,lens", [
     ("llama31_8b_decode", dict(batch=3, seq_len=3000), [2999, 700, 1]),
     ("gptoss_vq8_sink", dict(batch=2, seq_len=3000), [2999, 130]),
@@ -247,10 +281,11 @@ def stream_k_segments(prefix, n_ctas, units, head_groups):
     ("llama32_1b_tiny", dict(batch=1, seq_len=700), [699]),
     ("llama31_8b_decode", dict(batch=2, n_q_heads=32, n_kv_heads=2, seq_len=900), [899, 64]),
 ])
-def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens):
-    """After the append and the partial step: each record equals the oracle's
-    softmax restricted to its segment's keys, and each unit finished inside one
-    CTA has its output rows (sink included) equal to the full attention."""
+def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry):
+    """After the append and the partial step (separate, or the fused
+    append+partial call): each record equals the oracle's softmax restricted to
+    its segment's keys, and each unit finished inside one CTA has its output rows
+    (sink included) equal to the full attention."""
     cfg = W.layer_configs(W.config(name, **over))[0]
     case = host_case(cfg, lens=lens)
     a = oracle_arrays(case, oracle_mod)
@@ -258,8 +293,11 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens):
     lay = layer.layout()
     dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
     layer.out.fill_(float("nan"))
-    layer.append(dev["q"], dev["k_new"], dev["v_new"])
-    layer.partial()
+    if entry == "split":
+        layer.append(dev["q"], dev["k_new"], dev["v_new"])
+        layer.partial()
+    else:
+        layer.append_partial(dev["q"], dev["k_new"], dev["v_new"])
     torch.cuda.synchronize()
     qr = oracle_mod.append(cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"], a["k_cache"],
                            a["v_cache"], a["v_scale"], a["seq_lens"])
