@@ -76,7 +76,7 @@ struct KeyGroups {
 };
 
 // Shared memory, from a 1024-byte aligned base: the ring of kStages stages |
-// full / empty barriers per stage | q-full, q-empty, q-first barriers | stage prefix |
+// full / empty barriers per stage | q-full, q-empty barriers | stage prefix |
 // lengths | q' fragment slot | two new-row staging slots. The ring takes what the
 // per-CTA budget leaves (two CTAs per SM below head_dim 256).
 template <int D, bool VQ8, int NHT>
@@ -100,7 +100,7 @@ struct Shape {
     static constexpr int kFragBytes = kHC * kFragRow;
     // a new key row (bf16) and value row (bf16, or int8 codes + fp32 scale)
     static constexpr int kNewRowBytes = round_up(2 * D + (VQ8 ? D + 4 : 2 * D), 16);
-    static constexpr int kFixedBytes = 1024 + 32 + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes;
+    static constexpr int kFixedBytes = 1024 + 16 + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes;
     static constexpr int kCtaBudget = D == 256 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
     static constexpr int kStagesRaw = (kCtaBudget - kFixedBytes) / (kStageBytes + 16);
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
@@ -274,25 +274,6 @@ __device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int
     }
 }
 
-// Fused append, one warp per CTA at kernel start (while warp 0 reads the
-// lengths, before any tile load): brings this CTA's share of the step's q,
-// k_new and v_new rows (128-byte lines c, c + P, c + 2P, ...) into L2 with the
-// evict-last policy, so that the prep warp's reads of them find them there (the
-// key stream, loaded evict-first, does not push them out).
-__device__ __forceinline__ void prefetch_step_inputs(const PartialParams& p, int D, int lane)
-{
-    const size_t esz = p.io_dtype == UAA_DTYPE_F32 ? 4 : 2;
-    const size_t q_lines = (static_cast<size_t>(p.B) * p.Hq * D * esz + 127) / 128;
-    const size_t kv_lines = (static_cast<size_t>(p.B) * p.Hkv * D * esz + 127) / 128;
-    const size_t total = q_lines + 2 * kv_lines;
-    for (size_t l = blockIdx.x + static_cast<size_t>(gridDim.x) * lane; l < total; l += 32 * gridDim.x) {
-        const char* a = l < q_lines ? static_cast<const char*>(p.q) + 128 * l
-                        : l < q_lines + kv_lines ? static_cast<const char*>(p.k_new) + 128 * (l - q_lines)
-                                                 : static_cast<const char*>(p.v_new) + 128 * (l - q_lines - kv_lines);
-        ptx::prefetch_l2_keep(a);
-    }
-}
-
 // Starts bringing the new k and v rows of (b, kvh) into L2 (their loads follow
 // the q rows' processing).
 template <int D>
@@ -439,8 +420,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t bar_empty = bar_full + 8 * SH::kStages;
     const uint32_t bar_qfull = bar_empty + 8 * SH::kStages;  // prep warp -> consumers: a segment's q' is ready
     const uint32_t bar_qempty = bar_qfull + 8;               // consumers -> prep warp: the q' slot is free
-    const uint32_t bar_qfirst = bar_qfull + 16;              // prep warp -> producer: the first q' is ready
-    int* prefix = reinterpret_cast<int*>(base_ptr + SH::kRingBytes + 16 * SH::kStages + 32);
+    int* prefix = reinterpret_cast<int*>(base_ptr + SH::kRingBytes + 16 * SH::kStages + 16);
     int* lens = prefix + SH::kPrefixBytes / 4;
     uint8_t* frag = reinterpret_cast<uint8_t*>(lens) + SH::kLensBytes;
     uint8_t* staging = frag + SH::kFragBytes;  // two slots of kNewRowBytes, by segment parity
@@ -454,7 +434,6 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         ptx::mbar_init(bar_qfull, 1);
         ptx::mbar_init(bar_qempty, kConsumerWarps);
-        ptx::mbar_init(bar_qfirst, 1);  // completes once
         ptx::fence_barrier_init();
     } else if (threadIdx.x == 32 * kProducerWarp) {
         ptx::prefetch_tensormap(&tm_k);
@@ -462,7 +441,6 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (VQ8) ptx::prefetch_tensormap(&tm_s);
     }
     grid_dependency_wait();  // the step's inputs (and a separate append's rows) are complete
-    if (p.fused && warp == kPrepWarp) prefetch_step_inputs(p, D, lane);  // while warp 0 reads seq_lens
     build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, MG, units, prefix, lens,
                        blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr, p.fused != 0,
                        p.max_len);  // ends with __syncthreads; seq_lens is not read again
@@ -492,14 +470,6 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int t0 = sg.lo / kTileKeys;
                 for (int k = 0; k < sg.n_st; ++k, ++it) {
                     const int s = it % SH::kStages;
-                    if (p.fused && it == 1 && !ptx::mbar_wait(bar_qfirst, 0, kWaitLimitCycles)) {
-                        // The first stage is on its way; the rest of the ring waits for the first
-                        // q' rows, whose reads would otherwise queue behind the whole ring fill
-                        // (~5 us) while the consumers need both.
-                        atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
                     if (p.fused && !counted && it == SH::kStages) {  // the ring is full: wait time
                         count_in_and_advance(p, lens);
                         counted = true;
@@ -586,10 +556,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 prep_loaded_q<D, HC>(p, sg.b, h0, nh, frag, SH::kFragRow, lane);
             }
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bar_qfull);
-                if (seg == 0) ptx::mbar_arrive(bar_qfirst);
-            }
+            if (lane == 0) ptx::mbar_arrive(bar_qfull);
             pos += sg.n_st;
         }
         return;
