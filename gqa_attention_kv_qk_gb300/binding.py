@@ -66,7 +66,8 @@ class UaaWorkspaceLayout(ctypes.Structure):
                 ("prefix_offset", ctypes.c_size_t), ("rec_lse_offset", ctypes.c_size_t),
                 ("rec_o_offset", ctypes.c_size_t), ("prefix_stride", ctypes.c_size_t),
                 ("rec_lse_stride", ctypes.c_size_t), ("rec_o_stride", ctypes.c_size_t),
-                ("total_bytes", ctypes.c_size_t)]
+                ("ranges_offset", ctypes.c_size_t), ("ranges_stride", ctypes.c_size_t),
+                ("balance_offset", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
 
 
 class UaaError(RuntimeError):

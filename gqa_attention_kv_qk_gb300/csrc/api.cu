@@ -104,8 +104,9 @@ struct Plan {
     int n_ctas;          // P: persistent CTAs of the partial kernel
     int slice;           // sequences per partial launch
     int n_slices;
-    size_t off_status, off_qrot, off_prefix, off_rec_lse, off_rec_o, total;
-    size_t prefix_stride, rec_lse_stride, rec_o_stride;  // bytes per slice
+    int per_sm;          // resident CTAs per SM
+    size_t off_status, off_qrot, off_prefix, off_rec_lse, off_rec_o, off_ranges, off_balance, total;
+    size_t prefix_stride, rec_lse_stride, rec_o_stride, ranges_stride;  // bytes per slice
 };
 
 int device_sm_count()
@@ -118,6 +119,28 @@ int device_sm_count()
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
     if (dev < 64) cache[dev] = n;
     return n;
+}
+
+// Range-balance state of the tensor-core kernel (BalanceState), at a fixed
+// offset after the status word so that it survives changes of batch: header |
+// claim[P] (uint64) | rate[P] | weight[P] | cumw[P + 1], each part 256-byte
+// aligned.
+size_t balance_bytes(int P)
+{
+    return 256 + align256((size_t)P * 8) + 2 * align256((size_t)P * 4) + align256(((size_t)P + 1) * 4);
+}
+
+uaa::BalanceState balance_of(void* ws, const Plan& pl)
+{
+    char* b = static_cast<char*>(ws) + pl.off_balance;
+    const size_t P = (size_t)pl.n_ctas;
+    uaa::BalanceState r;
+    r.header = reinterpret_cast<unsigned*>(b);
+    r.claim = reinterpret_cast<unsigned long long*>(b + 256);
+    r.rate = reinterpret_cast<float*>(b + 256 + align256(P * 8));
+    r.weight = reinterpret_cast<float*>(b + 256 + align256(P * 8) + align256(P * 4));
+    r.cumw = reinterpret_cast<unsigned*>(b + 256 + align256(P * 8) + 2 * align256(P * 4));
+    return r;
 }
 
 // Geometry of a step. The partial kernels are persistent: P = SMs x resident CTAs
@@ -144,8 +167,8 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     }
     p.head_groups = (p.G + p.heads_per_cta - 1) / p.heads_per_cta;
     p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim) / uaa::kTileKeys : 1;
-    const int per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
-    p.n_ctas = n_sm * per_sm;
+    p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
+    p.n_ctas = n_sm * p.per_sm;
     p.slice = batch < uaa::kMaxSliceBatch ? (batch > 0 ? batch : 1) : uaa::kMaxSliceBatch;
     p.n_slices = batch > 0 ? (batch + p.slice - 1) / p.slice : 0;
 
@@ -154,12 +177,15 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     p.prefix_stride = align256(((size_t)p.slice + 1) * 4);
     p.rec_lse_stride = align256(2 * P * HC * 4);
     p.rec_o_stride = align256(2 * P * HC * D * 4);
+    p.ranges_stride = align256((P + 1) * 8);
     p.off_status = 0;
-    p.off_qrot = 256;
+    p.off_balance = 256;
+    p.off_qrot = p.off_balance + balance_bytes(p.n_ctas);
     p.off_prefix = p.off_qrot + align256(B * Hq * D * 4);
     p.off_rec_lse = p.off_prefix + p.n_slices * p.prefix_stride;
     p.off_rec_o = p.off_rec_lse + p.n_slices * p.rec_lse_stride;
-    p.total = p.off_rec_o + p.n_slices * p.rec_o_stride;
+    p.off_ranges = p.off_rec_o + p.n_slices * p.rec_o_stride;
+    p.total = p.off_ranges + p.n_slices * p.ranges_stride;
     *pl = p;
     return UAA_OK;
 }
@@ -401,6 +427,12 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.v_scale = a->v_scale;
         p.seq_lens = a->seq_lens + b0;
         p.prefix = reinterpret_cast<int*>(w + pl.off_prefix + sl * pl.prefix_stride);
+        p.ranges = reinterpret_cast<long long*>(w + pl.off_ranges + sl * pl.ranges_stride);
+        if (pl.kernel == 1) {
+            p.bal = balance_of(w, pl);
+            p.slice = sl;
+            p.per_sm = pl.per_sm;
+        }
         p.rec_lse = reinterpret_cast<float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
         p.rec_o = reinterpret_cast<float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
         p.sink = d->has_sink ? a->sink : nullptr;
@@ -460,6 +492,8 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.sink = d->has_sink ? a->sink : nullptr;
         p.seq_lens = a->seq_lens + b0;
         p.prefix = reinterpret_cast<const int*>(w + pl.off_prefix + sl * pl.prefix_stride);
+        p.ranges = reinterpret_cast<const long long*>(w + pl.off_ranges + sl * pl.ranges_stride);
+        if (pl.kernel == 1) p.bal = balance_of(w, pl);
         p.rec_lse = reinterpret_cast<const float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
         p.rec_o = reinterpret_cast<const float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
         p.out = static_cast<char*>(a->out) + (size_t)b0 * Hq * D * out_elem;
@@ -564,6 +598,9 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, in
     layout->prefix_stride = pl.prefix_stride;
     layout->rec_lse_stride = pl.rec_lse_stride;
     layout->rec_o_stride = pl.rec_o_stride;
+    layout->ranges_offset = pl.off_ranges;
+    layout->ranges_stride = pl.ranges_stride;
+    layout->balance_offset = pl.off_balance;
     layout->total_bytes = pl.total;
     return UAA_OK;
 }

@@ -12,8 +12,9 @@
 // which is the full softmax over every visible key with the sink's mass in the
 // denominator only. A sequence with no visible key gets zeros.
 //
-// With P = min(CTAs, stages) every CTA range is non-empty, so the owners of a cut
-// unit's stages are exactly the CTAs cA .. cB. The record weights are formed per
+// The partial kernel leaves the table of its P' = min(CTAs, stages) range starts;
+// every range is non-empty, so the owners of a cut unit's stages are exactly
+// the ranges cA .. cB (found by binary search in the table). The record weights are formed per
 // head from one parallel round of loads; every thread then loads all records'
 // rows for four output elements before it adds any of them.
 #include "internal.cuh"
@@ -27,8 +28,12 @@ constexpr int kRecBatch = 4;     // records loaded together per output element
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
-    extern __shared__ float wts[];  // [R][nh]: record log2-sum-exp, then weights
-    grid_dependency_wait();         // the partial kernel's records are complete
+    extern __shared__ long long starts[];  // [P' + 1] range starts, then [R][nh] weights (floats)
+    grid_dependency_wait();                // the partial kernel's records are complete
+    if (blockIdx.x == gridDim.x - 1) {     // the extra CTA: the partial kernel's range balance
+        if (p.bal.header && threadIdx.x < 32) rebalance(p.bal, p.P, threadIdx.x);
+        return;
+    }
 
     const int units = p.Hkv * p.head_groups;
     const int b = blockIdx.x / units, u = blockIdx.x - b * units;
@@ -47,10 +52,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const long long T = p.prefix[p.B];
     const int P = T < p.P ? static_cast<int>(T) : p.P;
     const long long A = p.prefix[b] + static_cast<long long>(u) * stg;
-    const int cA = cta_of(A, T, P), cB = cta_of(A + stg - 1, T, P);
+    for (int i = tid; i <= P; i += kCombineThreads) starts[i] = p.ranges[i];
+    __syncthreads();
+    const int cA = range_of(starts, P, A), cB = range_of(starts, P, A + stg - 1);
     if (cA == cB) return;  // a whole unit: the partial kernel wrote it
-    const bool first_is_slot0 = range_start(cA, T, P) == A;
+    const bool first_is_slot0 = starts[cA] == A;
     const int R = cB - cA + 1;  // the unit's records: owners cA .. cB
+    float* wts = reinterpret_cast<float*>(starts + P + 1);
 
     for (int i = tid; i < R * nh; i += kCombineThreads)
         wts[i] = p.rec_lse[static_cast<size_t>(record_of(cA + i / nh, cA, first_is_slot0)) * HC + (i % nh)];
@@ -109,10 +117,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s)
 {
-    const long long blocks = static_cast<long long>(p.B) * p.Hkv * p.head_groups;
-    if (blocks == 0) return cudaSuccess;
-    // weights for up to every CTA's record of a unit (a unit never has more records than CTAs)
-    const size_t smem = static_cast<size_t>(p.P) * (p.heads_per_cta < kMaxHeads ? p.heads_per_cta : kMaxHeads) * 4;
+    // one CTA per unit, and one that rebalances the partial kernel's ranges
+    const long long blocks = static_cast<long long>(p.B) * p.Hkv * p.head_groups + 1;
+    if (blocks == 1) return cudaSuccess;
+    // the range starts, then weights for up to every range's record of a unit
+    const size_t smem = static_cast<size_t>(p.P + 1) * 8 +
+                        static_cast<size_t>(p.P) * (p.heads_per_cta < kMaxHeads ? p.heads_per_cta : kMaxHeads) * 4;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));

@@ -42,21 +42,50 @@ struct AppendParams {
     double inv_freq_over_pi[kMaxHeadDim / 2];  // theta'_p / pi, fp64
 };
 
+// Range-balance state of the tensor-core partial kernel, at a fixed workspace
+// offset: header[0] = kBalanceMagic and header[1] = P once the combine has
+// written the tables for P slots, header[2] = launch generation (advanced by
+// every combine); claim[v] = tag of the launch holding slot v, tag =
+// (generation + 1) << 20 | slice (unique per partial launch, so slots are
+// never reset); rate[v] = stages per ns of slot v in the last launch (0: none);
+// weight[v] = moving average of the rates; cumw[0 .. P] = cumulative integer
+// weights (cumw[P] = 0: none yet).
+struct BalanceState {
+    unsigned* header;
+    unsigned long long* claim;
+    float* rate;
+    float* weight;
+    unsigned* cumw;
+};
+constexpr unsigned kBalanceMagic = 0x42414c31u;
+
 // The partial kernels are persistent and share one stream-K partition. Work is
 // the list of ring stages (MG 64-key tiles each) of every unit = (sequence b,
 // kv head, head group), units ordered by b then kv head then head group; a
 // sequence with visible tiles [t0, t1) has ceil((t1 - t0) / MG) stages per
-// unit. With T stages in total and P = min(launched CTAs, T), CTA c < P owns
-// stages [floor(c T / P), floor((c + 1) T / P)) (never empty), cut at unit
-// boundaries into segments; CTAs c >= P have nothing to do. A segment that is a whole
-// unit writes the unit's output rows; any other segment writes one record
-// (normalised rows + log2-sum-exp) in slot 0 (the CTA's first segment) or 1
-// (its last), and the combine kernel merges the records of such units.
+// unit. With T stages in total and P' = min(launched CTAs, T) ranges, range
+// v < P' is stages [start[v], start[v + 1]) (never empty), cut at unit
+// boundaries into segments. Uniform ranges: start[v] = floor(v T / P'). The
+// tensor-core kernel weights the ranges by each CTA slot's measured speed (see
+// Balance below) when T >= the launched CTAs. The kernel that ran writes the
+// table start[0 .. P'] to the workspace for the combine. A segment that is a
+// whole unit writes the unit's output rows; any other segment writes one
+// record (normalised rows + log2-sum-exp) in slot 0 (the range's first
+// segment) or 1 (its last), and the combine kernel merges the records of such
+// units.
 //
-// Record index (2 c + slot) of the piece of a cut unit that CTA c owns: the
-// piece in the first owner cA is that CTA's first segment (slot 0) only if the
-// unit starts where cA's range starts; every later owner's piece starts its
-// range (slot 0).
+// Record index (2 v + slot) of the piece of a cut unit in range v: the piece in
+// the first owner vA is that range's first segment (slot 0) only if the unit
+// starts where vA starts; every later owner's piece starts its range (slot 0).
+//
+// Balance (tensor-core kernel): CTAs run at different speeds on different SMs
+// (some groups of SMs stream 7-10 % slower), so equal ranges leave the fast
+// CTAs idle at the end. Each CTA claims a range slot tied to its SM (slot
+// per_sm * smid + k, k-th CTA on the SM; any free slot if taken), takes the
+// range that the slot weights give it, and records its stages per ns. The
+// combine that follows blends the rates into the weights (moving average),
+// writes the cumulative integer weights for the next launch and frees the
+// slots, so a partial launch must be followed by its combine.
 struct PartialParams {
     int B, Hq, Hkv, D, G;
     int b_off;              // first sequence of this launch (batches are cut into slices)
@@ -71,6 +100,11 @@ struct PartialParams {
     float* v_scale;
     int* seq_lens;          // slice-relative (advanced by the fused kernel only)
     int* prefix;            // [B + 1] stage prefix over sequences, written for the combine
+    long long* ranges;      // [P' + 1] range starts, written for the combine
+    // balance state (tensor-core kernel; null: uniform ranges)
+    BalanceState bal;
+    int slice;              // index of this launch's batch slice (part of the claim tag)
+    int per_sm;             // CTAs per SM of the launch
     float* rec_o;           // [2P][heads_per_cta][D]
     float* rec_lse;         // [2P][heads_per_cta]
     const float* sink;      // [Hq] or null
@@ -103,6 +137,8 @@ struct CombineParams {
     const float* sink;      // [Hq] or null
     const int* seq_lens;    // slice-relative
     const int* prefix;      // [B + 1]
+    const long long* ranges;  // [P' + 1] range starts of the partial launch
+    BalanceState bal;       // of the tensor-core partial kernel (null pointers otherwise)
     const float* rec_o;
     const float* rec_lse;
     void* out;              // slice-relative
@@ -391,6 +427,135 @@ __device__ __forceinline__ int8_t vq8_code(float v, float s)
     if (s == 0.f) return 0;
     const float c = fminf(fmaxf(rintf(__fdiv_rn(v, s)), -127.f), 127.f);
     return static_cast<int8_t>(static_cast<int>(c));
+}
+
+// ---------------------------------------------------------------- range slots
+
+__device__ __forceinline__ unsigned long long global_time_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One thread of a tensor-core CTA (while warp 0 scans the lengths): claims a
+// range slot v with this launch's tag and returns it with the slot's
+// cumulative weights cumw[v], cumw[v + 1] and the total (0 when the tables are
+// not for this P). Returns -1 only if every slot carries this launch's tag (a
+// partial launch repeated without its combine).
+__device__ inline int claim_slot(const PartialParams& p, unsigned& w0, unsigned& w1, unsigned& wP)
+{
+    const int P = static_cast<int>(gridDim.x);
+    const BalanceState& b = p.bal;
+    const bool tables = __ldcg(b.header) == kBalanceMagic && __ldcg(b.header + 1) == static_cast<unsigned>(P);
+    const unsigned long long tag =
+        (static_cast<unsigned long long>(__ldcg(b.header + 2)) + 1ull) << 20 | static_cast<unsigned>(p.slice);
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const int v0 = static_cast<int>((static_cast<unsigned long long>(smid) * p.per_sm) % P);
+    wP = tables ? __ldcg(b.cumw + P) : 0u;
+    for (int k = 0; k < P; ++k) {
+        const int v = v0 + k < P ? v0 + k : v0 + k - P;
+        const unsigned long long old = __ldcg(b.claim + v);
+        if (old != tag && atomicCAS(b.claim + v, old, tag) == old) {
+            w0 = wP ? __ldcg(b.cumw + v) : 0u;
+            w1 = wP ? __ldcg(b.cumw + v + 1) : 0u;
+            return v;
+        }
+    }
+    w0 = w1 = 0;
+    return -1;
+}
+
+// The range [s, e) of slot v when the launch holds T stages (empty: no work),
+// writing start[v] (and start[P'] = T from the last range) for the combine.
+// Weighted when every slot has a weight (wP > 0) and T >= P: one stage each,
+// the other T - P shared in proportion to the weights; otherwise uniform over
+// P' = min(P, T).
+__device__ inline void slot_range(const PartialParams& p, int v, unsigned w0, unsigned w1, unsigned wP, long long T,
+                                  long long& s, long long& e)
+{
+    const int P = static_cast<int>(gridDim.x);
+    const int Pp = T < P ? static_cast<int>(T) : P;
+    s = e = 0;
+    if (v < 0 || v >= Pp) return;
+    if (T >= P && wP > 0) {
+        const long long extra = T - P;
+        s = v + extra * w0 / wP;
+        e = v + 1 + extra * w1 / wP;
+    } else {
+        s = range_start(v, T, Pp);
+        e = range_start(v + 1, T, Pp);
+    }
+    p.ranges[v] = s;
+    if (v == Pp - 1) p.ranges[Pp] = T;
+}
+
+// Warp 0 of one CTA of the combine, after a partial launch of P CTAs: blends
+// the slot rates into the weights (moving average; tables written for another
+// P start over), writes the cumulative integer weights (each >= 1) for the next
+// launch and advances the generation; while any slot has no weight yet the
+// next launch uses uniform ranges (cumw[P] = 0).
+__device__ inline void rebalance(const BalanceState& b, int P, int lane)
+{
+    constexpr int kPerLane = 16;  // slots per lane per pass, loaded together
+    const bool fresh = !(__ldcg(b.header) == kBalanceMagic && __ldcg(b.header + 1) == static_cast<unsigned>(P));
+    float mx = 0.f;
+    bool all = true;
+    for (int v0 = 0; v0 < P; v0 += 32 * kPerLane) {
+        float r[kPerLane], w[kPerLane];
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int v = v0 + lane + 32 * i;
+            r[i] = v < P ? __ldcg(b.rate + v) : 0.f;
+            w[i] = v < P && !fresh ? __ldcg(b.weight + v) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int v = v0 + lane + 32 * i;
+            if (v >= P) continue;
+            const bool ok = r[i] > 0.f && r[i] < 1e30f;  // a rate this launch measured
+            const float nw = ok ? (w[i] > 0.f ? 0.75f * w[i] + 0.25f * r[i] : r[i]) : w[i];
+            b.weight[v] = nw;
+            b.rate[v] = 0.f;
+            mx = fmaxf(mx, nw);
+            all = all && nw > 0.f;
+        }
+    }
+    mx = warp_max(mx);
+    all = __all_sync(0xffffffffu, all) && mx > 0.f;
+    unsigned carry = 0;
+    if (lane == 0) b.cumw[0] = 0u;
+    for (int v0 = 0; v0 < P; v0 += 32) {
+        const int v = v0 + lane;
+        unsigned x = 0;
+        if (v < P && all) x = max(1u, static_cast<unsigned>(65536.f * fminf(b.weight[v] / mx, 1.f)));
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (v < P) b.cumw[v + 1] = all ? carry + x : 0u;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) {
+        b.header[0] = kBalanceMagic;
+        b.header[1] = static_cast<unsigned>(P);
+        b.header[2] = __ldcg(b.header + 2) + 1u;
+    }
+}
+
+// The range holding stage x: the largest v < n with start[v] <= x (start
+// ascending, start[0] = 0 <= x).
+__device__ __forceinline__ int range_of(const long long* start, int n, long long x)
+{
+    int lo = 0, hi = n;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
 }
 
 }  // namespace uaa

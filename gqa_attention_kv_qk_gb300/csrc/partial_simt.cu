@@ -2,8 +2,10 @@
 //
 // Persistent over the stream-K partition of internal.cuh (stages of one 64-key
 // tile, units of up to 8 query heads). Four warps; the unit's query rows sit in
-// registers, D/32 values per lane. Warps take the segment's keys round-robin;
-// per key the lanes hold D/32 elements of the key and value rows, the per-head
+// registers, D/32 values per lane. Warps take blocks of 16/(D/32) consecutive keys
+// round-robin and load a block's rows before using any (a key at a time would
+// pay one memory round trip per key); per key the lanes hold D/32 elements of
+// the key and value rows, the per-head
 // dot products are reduced across the warp, and each warp keeps an online
 // softmax (running max, sum, output row) per head in the log2 domain. The four
 // warp states are merged in shared memory: a whole unit writes its output rows
@@ -23,6 +25,7 @@ template <int D>
 __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const PartialParams p)
 {
     constexpr int EPL = D / 32;
+    constexpr int KB = 16 / EPL;  // keys per load block: 32 row registers per lane
     __shared__ float red_m[kSimtWarps][kSimtHeads];
     __shared__ float red_l[kSimtWarps][kSimtHeads];
     __shared__ float red_o[kSimtWarps][kSimtHeads][D];
@@ -38,6 +41,10 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
     const int P = T < gridDim.x ? static_cast<int>(T) : static_cast<int>(gridDim.x);  // every range non-empty
     const long long s_c = static_cast<int>(blockIdx.x) < P ? range_start(blockIdx.x, T, P) : 0;
     const long long e_c = static_cast<int>(blockIdx.x) < P ? range_start(blockIdx.x + 1, T, P) : 0;
+    if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < P) {  // uniform ranges: slot = CTA index
+        p.ranges[blockIdx.x] = s_c;
+        if (static_cast<int>(blockIdx.x) == P - 1) p.ranges[P] = T;
+    }
 
     for (long long pos = s_c; pos < e_c;) {
         const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
@@ -66,28 +73,37 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
         const size_t rows0 = (static_cast<size_t>(p.b_off + sg.b) * p.Hkv + sg.kvh) * p.cap;
         const float* K = static_cast<const float*>(p.k_cache) + rows0 * D;
         const float* V = static_cast<const float*>(p.v_cache) + rows0 * D;
-        for (int j = j_beg + warp; j < j_end; j += kSimtWarps) {
-            float kx[EPL], vx[EPL];
+        // warp w takes blocks of KB consecutive keys round-robin; a block's rows are
+        // all loaded before the first is used (one memory round trip per block)
+        for (int jb = j_beg + warp * KB; jb < j_end; jb += kSimtWarps * KB) {
+            float kx[KB][EPL], vx[KB][EPL];
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                kx[i] = K[static_cast<size_t>(j) * D + lane + 32 * i];
-                vx[i] = V[static_cast<size_t>(j) * D + lane + 32 * i];
-            }
+            for (int u = 0; u < KB; ++u)
 #pragma unroll
-            for (int h = 0; h < kSimtHeads; ++h) {
-                if (h >= nh) break;
-                float dot = 0.f;
+                for (int i = 0; i < EPL; ++i) {
+                    const bool ok = jb + u < j_end;
+                    kx[u][i] = ok ? K[static_cast<size_t>(jb + u) * D + lane + 32 * i] : 0.f;
+                    vx[u][i] = ok ? V[static_cast<size_t>(jb + u) * D + lane + 32 * i] : 0.f;
+                }
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) dot = fmaf(q[h][i], kx[i], dot);
-                dot = warp_sum(dot);
-                const float sc = p.softcap_log2e > 0.f ? tanhf(dot) * p.softcap_log2e : dot;
-                const float mn = fmaxf(m[h], sc);
-                const float alpha = exp2f(m[h] - mn);
-                const float pj = exp2f(sc - mn);
-                l[h] = l[h] * alpha + pj;
+            for (int u = 0; u < KB; ++u) {
+                if (jb + u >= j_end) break;
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) o[h][i] = fmaf(pj, vx[i], o[h][i] * alpha);
-                m[h] = mn;
+                for (int h = 0; h < kSimtHeads; ++h) {
+                    if (h >= nh) break;
+                    float dot = 0.f;
+#pragma unroll
+                    for (int i = 0; i < EPL; ++i) dot = fmaf(q[h][i], kx[u][i], dot);
+                    dot = warp_sum(dot);
+                    const float sc = p.softcap_log2e > 0.f ? tanhf(dot) * p.softcap_log2e : dot;
+                    const float mn = fmaxf(m[h], sc);
+                    const float alpha = exp2f(m[h] - mn);
+                    const float pj = exp2f(sc - mn);
+                    l[h] = l[h] * alpha + pj;
+#pragma unroll
+                    for (int i = 0; i < EPL; ++i) o[h][i] = fmaf(pj, vx[u][i], o[h][i] * alpha);
+                    m[h] = mn;
+                }
             }
         }
 

@@ -76,7 +76,7 @@ struct KeyGroups {
 };
 
 // Shared memory, from a 1024-byte aligned base: the ring of kStages stages |
-// full / empty barriers per stage | q-full, q-empty barriers | stage prefix |
+// full / empty barriers per stage | q-full, q-empty barriers and the range | stage prefix |
 // lengths | q' fragment slot | two new-row staging slots. The ring takes what the
 // per-CTA budget leaves (two CTAs per SM below head_dim 256).
 template <int D, bool VQ8, int NHT>
@@ -100,7 +100,9 @@ struct Shape {
     static constexpr int kFragBytes = kHC * kFragRow;
     // a new key row (bf16) and value row (bf16, or int8 codes + fp32 scale)
     static constexpr int kNewRowBytes = round_up(2 * D + (VQ8 ? D + 4 : 2 * D), 16);
-    static constexpr int kFixedBytes = 1024 + 16 + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes;
+    // q-full and q-empty barriers, then the CTA's range slot, its weights, start, end
+    static constexpr int kCtlBytes = 48;
+    static constexpr int kFixedBytes = 1024 + kCtlBytes + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes;
     static constexpr int kCtaBudget = D == 256 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
     static constexpr int kStagesRaw = (kCtaBudget - kFixedBytes) / (kStageBytes + 16);
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
@@ -420,7 +422,8 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t bar_empty = bar_full + 8 * SH::kStages;
     const uint32_t bar_qfull = bar_empty + 8 * SH::kStages;  // prep warp -> consumers: a segment's q' is ready
     const uint32_t bar_qempty = bar_qfull + 8;               // consumers -> prep warp: the q' slot is free
-    int* prefix = reinterpret_cast<int*>(base_ptr + SH::kRingBytes + 16 * SH::kStages + 16);
+    uint8_t* ctl = base_ptr + SH::kRingBytes + 16 * SH::kStages;  // barriers 0, 8; slot 16; weights 20-28; range 32, 40
+    int* prefix = reinterpret_cast<int*>(ctl + SH::kCtlBytes);
     int* lens = prefix + SH::kPrefixBytes / 4;
     uint8_t* frag = reinterpret_cast<uint8_t*>(lens) + SH::kLensBytes;
     uint8_t* staging = frag + SH::kFragBytes;  // two slots of kNewRowBytes, by segment parity
@@ -441,19 +444,39 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (VQ8) ptx::prefetch_tensormap(&tm_s);
     }
     grid_dependency_wait();  // the step's inputs (and a separate append's rows) are complete
+    if (threadIdx.x == 32 * kPrepWarp) {  // the range slot, while warp 0 scans the lengths
+        unsigned w0, w1, wP;
+        const int v = claim_slot(p, w0, w1, wP);
+        if (v < 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);  // slots left claimed by an unfinished launch
+        *reinterpret_cast<int*>(ctl + 16) = v;
+        *reinterpret_cast<unsigned*>(ctl + 20) = w0;
+        *reinterpret_cast<unsigned*>(ctl + 24) = w1;
+        *reinterpret_cast<unsigned*>(ctl + 28) = wP;
+    }
     build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, MG, units, prefix, lens,
                        blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr, p.fused != 0,
                        p.max_len);  // ends with __syncthreads; seq_lens is not read again
-    const long long T = prefix[p.B];
-    const int P = T < gridDim.x ? static_cast<int>(T) : static_cast<int>(gridDim.x);  // every range non-empty
+    unsigned long long t_begin = 0;
+    if (threadIdx.x == 0) {
+        long long rs, re;
+        slot_range(p, *reinterpret_cast<const int*>(ctl + 16), *reinterpret_cast<const unsigned*>(ctl + 20),
+                   *reinterpret_cast<const unsigned*>(ctl + 24), *reinterpret_cast<const unsigned*>(ctl + 28),
+                   prefix[p.B], rs, re);
+        *reinterpret_cast<long long*>(ctl + 32) = rs;
+        *reinterpret_cast<long long*>(ctl + 40) = re;
+        t_begin = global_time_ns();
+    }
+    __syncthreads();
+    const int slot = *reinterpret_cast<const int*>(ctl + 16);
+    const long long s_c = *reinterpret_cast<const long long*>(ctl + 32);
+    const long long e_c = *reinterpret_cast<const long long*>(ctl + 40);
     // Fused append: every CTA counts in once its lengths are read (an active CTA's
     // producer does so after its first ring fill, off the consumers' path); the
     // last to count in advances seq_lens once its own work is issued.
-    if (static_cast<int>(blockIdx.x) >= P) {  // uniform over the CTA: no stages
+    if (e_c <= s_c) {  // uniform over the CTA: no stages
         if (threadIdx.x == 0 && p.fused) count_in_and_advance(p, lens);
         return;
     }
-    const long long s_c = range_start(blockIdx.x, T, P), e_c = range_start(blockIdx.x + 1, T, P);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -831,7 +854,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         float* red_l = red_m + kConsumerWarps * HC;
         float* red_o = red_l + kConsumerWarps * HC;
         const float o_unit = VQ8 ? r_scale : 1.f;
-        const size_t rec = 2 * static_cast<size_t>(blockIdx.x) + (pos == s_c ? 0 : 1);
+        const size_t rec = 2 * static_cast<size_t>(slot) + (pos == s_c ? 0 : 1);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += RC) {
             ptx::named_barrier_sync(1, kConsumerWarps * 32);  // stage (or previous round) no longer read
@@ -893,6 +916,10 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s_last);
         pos += sg.n_st;
+    }
+    if (threadIdx.x == 0) {  // this slot's speed, for the combine's rebalance
+        const unsigned long long dt = global_time_ns() - t_begin;
+        p.bal.rate[slot] = static_cast<float>(e_c - s_c) / static_cast<float>(dt > 0 ? dt : 1);
     }
 }
 

@@ -9,10 +9,13 @@
  *      the append of k and v at slot seq_lens[b] (seq_lens[b] then grows by 1).
  *   2. uaa_decode_attn_partial: split-K flash decoding. A persistent grid of P
  *      CTAs splits the key stages of all units (sequence, kv head, head group)
- *      into P equal contiguous ranges (a stream-K partition). A unit that lies
- *      inside one CTA's range is finished there and its output rows written;
- *      every other unit leaves one record (normalised output rows and
- *      log-sum-exp) per CTA it touches in the workspace.
+ *      into P contiguous ranges (a stream-K partition). The tensor-core kernel
+ *      sizes the ranges by the speed each CTA slot measured in the previous
+ *      launches on the same workspace (the SMs of a GB300 do not all stream
+ *      equally fast), so results may differ in rounding from launch to launch.
+ *      A unit that lies inside one range is finished there and its output rows
+ *      written; every other unit leaves one record (normalised output rows and
+ *      log-sum-exp) per range it touches in the workspace.
  *   3. uaa_decode_attn_combine: log-sum-exp merge of those records, the sink
  *      logit added to the denominator, the remaining output rows written.
  *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16 and vq8 caches in one
@@ -64,7 +67,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 3
+#define UAA_ABI_VERSION 4
 
 typedef enum {
     UAA_OK = 0,
@@ -86,7 +89,9 @@ typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2 } uaa_dt
 /* Device-side status flags (sticky, in the workspace; read by uaa_device_status). */
 #define UAA_DEVFLAG_CAPACITY 0x1u   /* seq_lens[b] >= cache_capacity: that sequence was not appended */
 #define UAA_DEVFLAG_LEN_HINT 0x2u   /* seq_lens[b] > max_seq_len at the append (results stay exact) */
-#define UAA_DEVFLAG_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up; outputs are invalid */
+#define UAA_DEVFLAG_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up, or the workspace's
+                                       scheduling state was left by such a launch; outputs are
+                                       invalid until the workspace is zeroed again */
 
 /* Rotary embedding. Pair p of a head row is (p, p + D/2) for NEOX and (2p, 2p+1)
  * for INTERLEAVED; theta_p = theta^(-2p/D), rotated by angle pos * theta'_p.
@@ -145,9 +150,11 @@ typedef struct {
 
 /* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed
  * once after allocation. It holds the rotated q rows, the split partials, the
- * device status word and (the next uint32) the arrival counter of the fused
- * kernel, which every completed launch leaves at zero; it must not be shared by
- * steps that run concurrently. After UAA_DEVFLAG_TIMEOUT zero it again. */
+ * device status word, the arrival counter of the fused kernel and the range
+ * balance state (counters that every completed launch leaves at zero, and the
+ * measured slot speeds that carry over to the next launch); it must not be
+ * shared by steps that run concurrently. After UAA_DEVFLAG_TIMEOUT zero it
+ * again. */
 typedef struct {
     void* ptr;
     size_t bytes;
@@ -171,6 +178,11 @@ typedef struct {
     size_t prefix_stride;     /* bytes between slices of each of the three arrays above */
     size_t rec_lse_stride;
     size_t rec_o_stride;
+    size_t ranges_offset;     /* int64 [n_slices][P' + 1]: start stage of each range of the
+                                 last partial launch of the slice (P' = min(P, stages)) */
+    size_t ranges_stride;
+    size_t balance_offset;    /* range-balance state of the tensor-core kernel (opaque), right
+                                 after the status word so that it survives a change of batch */
     size_t total_bytes;
 } uaa_workspace_layout;
 

@@ -78,8 +78,13 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         else:
             out = layer.step(dev["q"], dev["k_new"], dev["v_new"], q_rot=q_rot).clone()
         torch.cuda.synchronize()
-        # the fused kernel's arrival counter is back at zero after every launch
+        # the fused kernel's arrival counter is back at zero after every launch, and
+        # the combine has written the range-balance tables for this grid
         assert int(layer.ws_tensor[4:8].view(torch.int32).item()) == 0
+        lay = layer.layout()
+        if lay.kernel == 1:
+            hdr = layer.ws_tensor[lay.balance_offset: lay.balance_offset + 12].view(torch.int32).cpu().tolist()
+            assert hdr[0] == 0x42414c31 and hdr[1] == lay.n_ctas and hdr[2] >= 1
         qr = oracle_mod.append(cfg, W.bits(inp["q"]).copy(), W.bits(inp["k_new"]).copy(),
                                W.bits(inp["v_new"]).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
                                a["v_cache"], a["v_scale"], a["seq_lens"])
@@ -185,6 +190,36 @@ def test_unused_slots_hold_nan(oracle_mod, entry):
         run_and_compare(oracle_mod, cfg, lens, fill_unused="nan", steps=2, entry=entry)
 
 
+def test_ranges_follow_measured_speed():
+    """The tensor-core kernel sizes its ranges by the speeds measured in earlier
+    launches on the same workspace: after a few launches the range table differs
+    from the uniform split, still covers every stage once, and the slot weights
+    are positive."""
+    cfg = W.config("llama31_8b_decode", batch=4, seq_len=4000)
+    case = host_case(cfg)
+    layer = gpu_layer(case)
+    dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
+    lens0 = layer.seq_lens.clone()
+    for _ in range(4):
+        layer.seq_lens.copy_(lens0)
+        layer.step(dev["q"], dev["k_new"], dev["v_new"], advance_hint=False)
+    torch.cuda.synchronize()
+    lay = layer.layout()
+    ws = layer.ws_tensor
+    T = int(ws[lay.prefix_offset: lay.prefix_offset + (cfg["batch"] + 1) * 4].view(torch.int32)[-1].item())
+    P = lay.n_ctas
+    assert T >= P
+    starts = ws[lay.ranges_offset: lay.ranges_offset + (P + 1) * 8].view(torch.int64).cpu().numpy()
+    assert starts[0] == 0 and starts[-1] == T and np.all(np.diff(starts) >= 1)
+    uniform = np.array([c * T // P for c in range(P + 1)])
+    assert not np.array_equal(starts, uniform)
+    al = lambda x: -(-x // 256) * 256
+    w0 = lay.balance_offset + 256 + al(8 * P) + al(4 * P)
+    weight = ws[w0: w0 + 4 * P].view(torch.float32)
+    assert bool(torch.all(weight > 0))
+    assert layer.device_status() == 0
+
+
 @pytest.mark.parametrize("entry", ENTRIES)
 def test_batch_slices(oracle_mod, entry):
     """More sequences than one launch takes: the step runs as several slices
@@ -252,14 +287,15 @@ def test_length_hint_violation_is_flagged_and_results_stay_exact(oracle_mod):
 
 # ------------------------------------------------------------------ split partials
 
-def stream_k_segments(prefix, n_ctas, units, head_groups):
-    """The documented stream-K partition: with P = min(CTAs, T), CTA c owns stages
-    [c T / P, (c+1) T / P) of the concatenated unit stages, cut at unit boundaries."""
+def stream_k_segments(prefix, starts, units, head_groups):
+    """The documented stream-K partition: range c holds stages [starts[c],
+    starts[c+1]) of the concatenated unit stages (the table the partial kernel
+    leaves in the workspace), cut at unit boundaries."""
     import bisect
     T = int(prefix[-1])
-    n_ctas = min(n_ctas, T)  # CTAs beyond the stage count have nothing to do
-    for c in range(n_ctas):
-        s, e = c * T // n_ctas, (c + 1) * T // n_ctas
+    assert starts[0] == 0 and starts[-1] == T and np.all(np.diff(starts) > 0)
+    for c in range(len(starts) - 1):
+        s, e = int(starts[c]), int(starts[c + 1])
         pos = s
         while pos < e:
             b = bisect.bisect_right(prefix, pos) - 1
@@ -292,12 +328,18 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry
     layer = gpu_layer(case)
     lay = layer.layout()
     dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
-    layer.out.fill_(float("nan"))
-    if entry == "split":
-        layer.append(dev["q"], dev["k_new"], dev["v_new"])
-        layer.partial()
-    else:
-        layer.append_partial(dev["q"], dev["k_new"], dev["v_new"])
+    lens0 = layer.seq_lens.clone()
+    stream = torch.cuda.current_stream()
+    for rep in range(3):  # from the second launch on, the tensor-core kernel's ranges are weighted
+        if rep:  # the combine frees the range slots of the previous partial launch
+            B.uaa_decode_attn_combine(layer.desc, layer.args(None, None, None), layer.ws, stream)
+        layer.seq_lens.copy_(lens0)
+        layer.out.fill_(float("nan"))
+        if entry == "split":
+            layer.append(dev["q"], dev["k_new"], dev["v_new"])
+            layer.partial()
+        else:
+            layer.append_partial(dev["q"], dev["k_new"], dev["v_new"])
     torch.cuda.synchronize()
     qr = oracle_mod.append(cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"], a["k_cache"],
                            a["v_cache"], a["v_scale"], a["seq_lens"])
@@ -309,13 +351,15 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry
     ws = layer.ws_tensor
     assert lay.n_slices == 1
     prefix = ws[lay.prefix_offset: lay.prefix_offset + (Bn + 1) * 4].view(torch.int32).cpu().numpy()
+    n_ranges = min(P, int(prefix[-1]))
+    starts = ws[lay.ranges_offset: lay.ranges_offset + (n_ranges + 1) * 8].view(torch.int64).cpu().numpy()
     rec_lse = ws[lay.rec_lse_offset: lay.rec_lse_offset + 2 * P * HC * 4].view(torch.float32).view(2 * P, HC)
     rec_o = ws[lay.rec_o_offset: lay.rec_o_offset + 2 * P * HC * D * 4].view(torch.float32).view(2 * P, HC, D)
     rec_lse, rec_o = rec_lse.cpu().numpy(), rec_o.cpu().numpy()
     out = layer.out.cpu().numpy()
     W_ = cfg.get("window", 0) or 0
     n_whole = n_rec = 0
-    for sg in stream_k_segments(prefix, P, Hkv * hgroups, hgroups):
+    for sg in stream_k_segments(prefix, starts, Hkv * hgroups, hgroups):
         b = sg["b"]
         n = int(a["seq_lens"][b])
         lo = max(0, n - W_) if W_ else 0
