@@ -77,7 +77,7 @@ struct KeyGroups {
 
 // Shared memory, from a 1024-byte aligned base: the ring of kStages stages |
 // full / empty barriers per stage | q-full, q-empty barriers and the range | stage prefix |
-// lengths | q' fragment slot | two new-row staging slots. The ring takes what the
+// lengths | q' fragment slot | two new-row staging slots | rotation tables. The ring takes what the
 // per-CTA budget leaves (two CTAs per SM below head_dim 256).
 template <int D, bool VQ8, int NHT>
 struct Shape {
@@ -100,9 +100,12 @@ struct Shape {
     static constexpr int kFragBytes = kHC * kFragRow;
     // a new key row (bf16) and value row (bf16, or int8 codes + fp32 scale)
     static constexpr int kNewRowBytes = round_up(2 * D + (VQ8 ? D + 4 : 2 * D), 16);
-    // q-full and q-empty barriers, then the CTA's range slot, its weights, start, end
-    static constexpr int kCtlBytes = 48;
-    static constexpr int kFixedBytes = 1024 + kCtlBytes + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes;
+    // q-full and q-empty barriers, then the CTA's range slot, its weights, start, end, go flag
+    static constexpr int kCtlBytes = 64;
+    // fused append: theta'_p / pi (fp64) and the (cos, sin) of the current sequence, D / 2 each
+    static constexpr int kTabBytes = 8 * D;
+    static constexpr int kFixedBytes =
+        1024 + kCtlBytes + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes + kTabBytes;
     static constexpr int kCtaBudget = D == 256 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
     static constexpr int kStagesRaw = (kCtaBudget - kFixedBytes) / (kStageBytes + 16);
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
@@ -172,6 +175,17 @@ __device__ __forceinline__ void widen_code_pairs(uint32_t r, uint32_t& d_even, u
 
 __device__ __forceinline__ bool key_ok(int k, int lo, int hi) { return k >= lo && k < hi; }
 
+// Once per CTA the prep warp, having issued the reads of its first q rows, lets
+// the producer fill the rest of its ring (flag at `go`; the producer issues the
+// first stage, then waits for it). Reads issued after the whole first ring
+// fill wait behind it in HBM (~30 MB requested at once, 5-8 us); behind one
+// stage per CTA they land in ~1.5 us. A flag rather than a barrier: bar.sync
+// would wait for the reads to land.
+__device__ __forceinline__ void release_producer(uint32_t go, int lane)
+{
+    if (lane == 0) ptx::flag_set(go, 1u);  // no __syncwarp: it too would wait for the reads
+}
+
 // bf16 hi + lo parts of x into element e of a q' fragment row.
 __device__ __forceinline__ void store_frag(uint8_t* row, int e, float x)
 {
@@ -183,15 +197,20 @@ __device__ __forceinline__ void store_frag(uint8_t* row, int e, float x)
 
 // Prep warp, fused append: q' rows of the unit's heads h0 .. h0 + nh - 1 of
 // sequence b (RMSNorm, rotation, logit prescale) into the fragment slot; lane
-// takes rotation pairs lane + 32 j with (cos, sin) csr[j], recomputed for
-// position pos (after the rows' loads are issued) when new_seq. Rows of missing
-// heads are zero.
+// takes rotation pairs lane + 32 j. When new_seq, (cos, sin) of position pos
+// for pair i go to cs[i] first (from theta'_i / pi in freq[i]), while the rows'
+// reads are in flight. Rows of missing heads are zero.
+// The reads of eight rows go out together; their values are parked in the
+// fragment rows (element e as fp32 at byte 4 e, the bytes its hi / lo pair
+// takes later) and each head is then finished in a rolled loop: at a launch's
+// start this code runs cold, and an unrolled body cost microseconds of
+// instruction fetch.
 template <int D, int HC, typename T>
-__device__ __forceinline__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool write_rot,
-                                             bool new_seq, int pos, const double (&freq)[D / 64],
-                                             float2 (&csr)[D / 64], uint8_t* frag, int row_bytes, int lane)
+__device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool write_rot, bool new_seq, int pos,
+                             const double* freq, float2* cs, uint8_t* frag, int row_bytes, uint32_t go, int lane)
 {
     constexpr int NP = D / 64;
+    const bool neox = p.style == UAA_ROPE_NEOX;
 #pragma unroll 1
     for (int hc0 = 0; hc0 < HC; hc0 += 8) {
         float xa[8][NP], xb[8][NP];
@@ -201,48 +220,63 @@ __device__ __forceinline__ void prep_fused_q(const PartialParams& p, int b, int 
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 const int pp = lane + 32 * j;
-                const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
-                const int ib = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
-                xa[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + ia) : 0.f;
-                xb[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + ib) : 0.f;
+                xa[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + (neox ? pp : 2 * pp)) : 0.f;
+                xb[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + (neox ? pp + D / 2 : 2 * pp + 1)) : 0.f;
             }
         }
+        if (go && hc0 == 0) release_producer(go, lane);  // the first loads are issued: the key stream may start
         if (new_seq && hc0 == 0) {  // the rows' loads are in flight: (cos, sin) of this sequence's position
-#pragma unroll
-            for (int j = 0; j < NP; ++j) csr[j] = rope_cos_sin(pos, freq[j], p.mscale);
+#pragma unroll 1
+            for (int j = 0; j < NP; ++j) cs[lane + 32 * j] = rope_cos_sin(pos, freq[lane + 32 * j], p.mscale);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+            float* raw = reinterpret_cast<float*>(frag + (hc0 + i) * row_bytes);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int pp = lane + 32 * j;
+                raw[neox ? pp : 2 * pp] = xa[i][j];
+                raw[neox ? pp + D / 2 : 2 * pp + 1] = xb[i][j];
+            }
+        }
+        __syncwarp();
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
             uint8_t* row = frag + (hc0 + i) * row_bytes;
+            const float* raw = reinterpret_cast<const float*>(row);
             const bool hv = hc0 + i < nh;
+            float ya[NP], yb[NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int pp = lane + 32 * j;
+                ya[j] = raw[neox ? pp : 2 * pp];
+                yb[j] = raw[neox ? pp + D / 2 : 2 * pp + 1];
+            }
+            __syncwarp();  // every lane has its values before any writes fragments over them
             if (p.qk_norm && hv) {
                 float ss = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP; ++j) ss += xa[i][j] * xa[i][j] + xb[i][j] * xb[i][j];
+                for (int j = 0; j < NP; ++j) ss += ya[j] * ya[j] + yb[j] * yb[j];
                 const float inv = rms_inv(warp_sum(ss), D, p.eps);
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
                     const int pp = lane + 32 * j;
-                    const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
-                    const int ib = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
-                    xa[i][j] = xa[i][j] * inv * p.q_norm_w[ia];
-                    xb[i][j] = xb[i][j] * inv * p.q_norm_w[ib];
+                    ya[j] = ya[j] * inv * p.q_norm_w[neox ? pp : 2 * pp];
+                    yb[j] = yb[j] * inv * p.q_norm_w[neox ? pp + D / 2 : 2 * pp + 1];
                 }
             }
             const size_t qoff = (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 const int pp = lane + 32 * j;
-                const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
-                const int ib = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
-                float ya = xa[i][j], yb = xb[i][j];
-                if (hv) rope_rotate(ya, yb, csr[j]);
+                const int ia = neox ? pp : 2 * pp, ib = neox ? pp + D / 2 : 2 * pp + 1;
+                if (hv) rope_rotate(ya[j], yb[j], cs[pp]);
                 if (write_rot && hv) {
-                    p.q_rot_out[qoff + ia] = ya;
-                    p.q_rot_out[qoff + ib] = yb;
+                    p.q_rot_out[qoff + ia] = ya[j];
+                    p.q_rot_out[qoff + ib] = yb[j];
                 }
-                store_frag(row, ia, ya * p.qscale);
-                store_frag(row, ib, yb * p.qscale);
+                store_frag(row, ia, ya[j] * p.qscale);
+                store_frag(row, ib, yb[j] * p.qscale);
             }
         }
     }
@@ -252,7 +286,7 @@ __device__ __forceinline__ void prep_fused_q(const PartialParams& p, int b, int 
 // prescaled, fp32) into the fragment slot, eight rows' loads at a time.
 template <int D, int HC>
 __device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int h0, int nh, uint8_t* frag,
-                                              int row_bytes, int lane)
+                                              int row_bytes, uint32_t go, int lane)
 {
 #pragma unroll 1
     for (int hc0 = 0; hc0 < HC; hc0 += 8) {
@@ -265,6 +299,7 @@ __device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int
                 x[i][j] = hc0 + i < nh ? *reinterpret_cast<const float2*>(qrow + 2 * lane + 64 * j)
                                        : make_float2(0.f, 0.f);
         }
+        if (go && hc0 == 0) release_producer(go, lane);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -294,8 +329,8 @@ __device__ __forceinline__ void prefetch_new_rows(const PartialParams& p, int b,
 // row (bf16, or vq8 codes and scale) of (b, kvh) into a staging slot (key at 0,
 // value at 2 D, vq8 scale at 3 D), and into the cache at slot L when `store`.
 template <int D, bool VQ8, typename T>
-__device__ __forceinline__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L,
-                                              const float2 (&csr)[D / 64], uint8_t* staging, bool store, int lane)
+__device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, const float2* cs, uint8_t* staging,
+                              bool store, int lane)
 {
     constexpr int NP = D / 64;   // rotation pairs per lane
     constexpr int EPL = D / 32;  // values per lane
@@ -327,7 +362,7 @@ __device__ __forceinline__ void prep_new_rows(const PartialParams& p, int b, int
     __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.k_cache) + slot * D;
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
-        rope_rotate(ka[j], kb[j], csr[j]);
+        rope_rotate(ka[j], kb[j], cs[lane + 32 * j]);
         const __nv_bfloat16 ha = __float2bfloat16_rn(ka[j]), hb = __float2bfloat16_rn(kb[j]);
         ks[ia[j]] = ha;
         ks[ib[j]] = hb;
@@ -422,11 +457,15 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t bar_empty = bar_full + 8 * SH::kStages;
     const uint32_t bar_qfull = bar_empty + 8 * SH::kStages;  // prep warp -> consumers: a segment's q' is ready
     const uint32_t bar_qempty = bar_qfull + 8;               // consumers -> prep warp: the q' slot is free
-    uint8_t* ctl = base_ptr + SH::kRingBytes + 16 * SH::kStages;  // barriers 0, 8; slot 16; weights 20-28; range 32, 40
+    // control block: barriers at 0 and 8; slot 16; weights 20-28; range start 32, end 40; go flag 48
+    uint8_t* ctl = base_ptr + SH::kRingBytes + 16 * SH::kStages;
+    const uint32_t go = ptx::smem_u32(ctl + 48);  // release_producer's flag (never 0 as an address)
     int* prefix = reinterpret_cast<int*>(ctl + SH::kCtlBytes);
     int* lens = prefix + SH::kPrefixBytes / 4;
     uint8_t* frag = reinterpret_cast<uint8_t*>(lens) + SH::kLensBytes;
     uint8_t* staging = frag + SH::kFragBytes;  // two slots of kNewRowBytes, by segment parity
+    double* freq_s = reinterpret_cast<double*>(staging + 2 * SH::kNewRowBytes);  // [D / 2] theta'_p / pi
+    float2* cs_s = reinterpret_cast<float2*>(freq_s + D / 2);                    // [D / 2] (cos, sin)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.Hkv * p.head_groups;
@@ -437,6 +476,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         ptx::mbar_init(bar_qfull, 1);
         ptx::mbar_init(bar_qempty, kConsumerWarps);
+        ptx::flag_set(go, 0u);
         ptx::fence_barrier_init();
     } else if (threadIdx.x == 32 * kProducerWarp) {
         ptx::prefetch_tensormap(&tm_k);
@@ -444,6 +484,8 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (VQ8) ptx::prefetch_tensormap(&tm_s);
     }
     grid_dependency_wait();  // the step's inputs (and a separate append's rows) are complete
+    if (p.fused && threadIdx.x >= 32 && threadIdx.x < 32 + D / 2)  // the rotation table, while warp 0 scans
+        freq_s[threadIdx.x - 32] = p.inv_freq_over_pi[threadIdx.x - 32];
     if (threadIdx.x == 32 * kPrepWarp) {  // the range slot, while warp 0 scans the lengths
         unsigned w0, w1, wP;
         const int v = claim_slot(p, w0, w1, wP);
@@ -493,6 +535,13 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int t0 = sg.lo / kTileKeys;
                 for (int k = 0; k < sg.n_st; ++k, ++it) {
                     const int s = it % SH::kStages;
+                    if (it == 1 && !ptx::flag_wait(go, kWaitLimitCycles)) {
+                        // the first stage is on its way; the rest of the ring follows the prep
+                        // warp's first q reads (release_producer)
+                        atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
                     if (p.fused && !counted && it == SH::kStages) {  // the ring is full: wait time
                         count_in_and_advance(p, lens);
                         counted = true;
@@ -542,11 +591,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // the segment ends its unit and the new token fits, the new k / v rows in
         // staging slot i mod 2) are written once the consumers have taken segment
         // i - 1's fragments (which also means segment i - 2 is finished).
-        float2 csr[D / 64];
-        double freq[D / 64];  // theta'_p / pi of this lane's rotation pairs lane + 32 j
-#pragma unroll
-        for (int j = 0; j < D / 64; ++j) freq[j] = p.fused ? param_at_lane(p.inv_freq_over_pi + 32 * j, lane) : 0.0;
-        int cs_b = -1;  // the sequence csr belongs to
+        int cs_b = -1;  // the sequence whose (cos, sin) are in cs_s
         int seg = 0;
         for (long long pos = s_c; pos < e_c; ++seg) {
             const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c,
@@ -565,18 +610,18 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const bool rot = p.q_rot_out != nullptr && sg.st0 == 0;
                 uint8_t* st_row = staging + (seg & 1) * SH::kNewRowBytes;
                 if (p.io_dtype == UAA_DTYPE_F32) {
-                    prep_fused_q<D, HC, float>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq, csr, frag,
-                                               SH::kFragRow, lane);
-                    if (ends) prep_new_rows<D, VQ8, float>(p, sg.b, sg.kvh, L, csr, st_row, sg.hg == 0, lane);
+                    prep_fused_q<D, HC, float>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s, frag,
+                                               SH::kFragRow, seg == 0 ? go : 0u, lane);
+                    if (ends) prep_new_rows<D, VQ8, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
                 } else {
-                    prep_fused_q<D, HC, __nv_bfloat16>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq, csr,
-                                                       frag, SH::kFragRow, lane);
+                    prep_fused_q<D, HC, __nv_bfloat16>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s,
+                                                       frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
                     if (ends)
-                        prep_new_rows<D, VQ8, __nv_bfloat16>(p, sg.b, sg.kvh, L, csr, st_row, sg.hg == 0, lane);
+                        prep_new_rows<D, VQ8, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
                 }
                 cs_b = sg.b;
             } else {
-                prep_loaded_q<D, HC>(p, sg.b, h0, nh, frag, SH::kFragRow, lane);
+                prep_loaded_q<D, HC>(p, sg.b, h0, nh, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_qfull);

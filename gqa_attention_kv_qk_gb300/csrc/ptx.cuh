@@ -184,6 +184,32 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Shared-memory flag without memory ordering: the store does not wait for the
+// thread's earlier loads (bar.sync and a release arrive would), the load is not
+// cached in registers.
+__device__ __forceinline__ void flag_set(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t flag_get(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Waits until the flag is non-zero; gives up after `limit` cycles (returns false).
+__device__ __forceinline__ bool flag_wait(uint32_t addr, long long limit)
+{
+    const long long t0 = clock64();
+    while (flag_get(addr) == 0u) {
+        if (clock64() - t0 > limit) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned),
 // completed by cp_async_wait_all in the issuing thread.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)
