@@ -166,7 +166,7 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
         p.n_head_tiles = 2;
     }
     p.head_groups = (p.G + p.heads_per_cta - 1) / p.heads_per_cta;
-    p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim) / uaa::kTileKeys : 1;
+    p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype) / uaa::kTileKeys : 1;
     p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
     p.n_ctas = n_sm * p.per_sm;
     p.slice = batch < uaa::kMaxSliceBatch ? (batch > 0 ? batch : 1) : uaa::kMaxSliceBatch;
@@ -387,7 +387,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     CUtensorMap tk, tv, ts;
     if (pl.kernel == 1) {
         const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
-        const uint32_t tk_rows = (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim);  // box height
+        const uint32_t tk_rows = (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype);  // box height
         UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
         if (d->kv_dtype == UAA_DTYPE_VQ8) {

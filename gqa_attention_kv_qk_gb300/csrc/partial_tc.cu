@@ -29,7 +29,7 @@
 //     stages between the producer and the consumers.
 //   warps 0-3 (consumers): warp w owns keys 16 MG w .. 16 MG (w+1) - 1 of every
 //     stage, as MG groups of 16 keys that share one softmax round (MG = 2 for
-//     head_dim 64, else 1).
+//     bf16 and 4 for vq8 at head_dim 64, else 1).
 //     S^T (16 keys x 8 heads) = K (16 x D) . Q'^T (D x 8) with mma.m16n8k16
 //     (keys on M, heads on N: no padding of M). The fp32 q' rows are split into
 //     bf16 hi + lo parts, two MMAs each, so the logits keep ~16 significant bits.
@@ -68,11 +68,13 @@ constexpr int kThreads = (kConsumerWarps + 2) * 32;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// MG: 16-key groups each consumer warp takes per stage (2 for head_dim 64, where a
-// key costs few bytes and the per-stage softmax work is shared by 32 keys).
-template <int D>
+// MG: 16-key groups each consumer warp takes per stage: at head_dim 64 a key
+// costs few bytes and the per-stage softmax work is shared by 16 MG keys (2 for
+// bf16; 4 for vq8, whose consumers are the slowest per byte: one 256-key stage
+// gives each warp four independent QK chains).
+template <int D, bool VQ8>
 struct KeyGroups {
-    static constexpr int kMG = D == 64 ? 2 : 1;
+    static constexpr int kMG = D == 64 ? (VQ8 ? 4 : 2) : 1;
 };
 
 // Shared memory, from a 1024-byte aligned base: the ring of kStages stages |
@@ -81,7 +83,7 @@ struct KeyGroups {
 // per-CTA budget leaves (two CTAs per SM below head_dim 256).
 template <int D, bool VQ8, int NHT>
 struct Shape {
-    static constexpr int kMG = KeyGroups<D>::kMG;
+    static constexpr int kMG = KeyGroups<D, VQ8>::kMG;
     static constexpr int kTK = kTileKeys * kMG;             // keys per stage
     static constexpr int kHC = 8 * NHT;                     // query heads of a unit
     static constexpr int kBoxBytes = kTK * 128;             // kTK rows x 128 bytes
@@ -988,7 +990,11 @@ cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUte
 
 }  // namespace
 
-int partial_tc_keys_per_stage(int D) { return D == 64 ? KeyGroups<64>::kMG * kTileKeys : kTileKeys; }
+int partial_tc_keys_per_stage(int D, int kv_dtype)
+{
+    if (D != 64) return kTileKeys;
+    return (kv_dtype == UAA_DTYPE_VQ8 ? KeyGroups<64, true>::kMG : KeyGroups<64, false>::kMG) * kTileKeys;
+}
 
 size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles)
 {

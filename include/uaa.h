@@ -163,7 +163,7 @@ typedef struct {
 /* Where each array lives in the workspace, and the split geometry. */
 typedef struct {
     int32_t n_ctas;           /* P: persistent CTAs of the partial step (stream-K ranges) */
-    int32_t stage_keys;       /* keys per ring stage: 64, or 128 at head_dim 64 (bf16/vq8) */
+    int32_t stage_keys;       /* keys per ring stage: 64; at head_dim 64 128 (bf16), 256 (vq8) */
     int32_t heads_per_cta;    /* query heads of one unit (sequence, kv head, head group) */
     int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
     int32_t n_slices;         /* partial + combine launches (batch slices) */

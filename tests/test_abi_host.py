@@ -132,7 +132,8 @@ def test_workspace_layout_is_consistent(L, name):
             kernel = 0 if layer["kv_dtype"] == "f32" else 1
             per_sm = 4 if kernel == 0 else (1 if layer["head_dim"] == 256 else 2)
             assert lay.kernel == kernel and lay.n_ctas == n_sm * per_sm
-            assert lay.stage_keys == (128 if kernel == 1 and layer["head_dim"] == 64 else 64)
+            d64 = kernel == 1 and layer["head_dim"] == 64
+            assert lay.stage_keys == ((256 if layer["kv_dtype"] == "vq8" else 128) if d64 else 64)
             assert lay.n_slices == -(-batch // lay.slice_batch) and lay.slice_batch <= 1024
             Hq, D, HC, P = layer["n_q_heads"], layer["head_dim"], lay.heads_per_cta, lay.n_ctas
             assert lay.prefix_offset >= lay.q_rot_offset + batch * Hq * D * 4
