@@ -13,6 +13,7 @@ return to 8192 (a 64-byte device copy) so every step times the same work. The
 value       = algorithmic bytes of all timed steps / device time (CUDA events)
 e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each with
               the step's q/k/v copied from pinned host memory and out copied back
+              (double-buffered, copies on a second stream overlapping the kernels)
 roofline    = the split-K partial kernel alone (for bf16 / vq8 caches the kernel
               that also performs the append): its algorithmic bytes (visible KV
               rows) / its mean launch duration, against the measured HBM copy peak
@@ -348,26 +349,56 @@ def run_uaa(args, world, rank, local) -> dict | None:
         stream.synchronize()
 
         # ---- end to end through the public call, host buffers
+        # Every decode step copies its own q / k / v from pinned host memory and
+        # reads its own output back, inside the timed region. Inputs and outputs are
+        # double-buffered per layer and the copies run on a second stream, so the
+        # next call's input copy and the last call's read-back overlap the current
+        # call's kernels, as in a serving loop.
         host_in = [{k: v.cpu().pin_memory() for k, v in case_in.items()} for case_in in
                    [{k: case[k] for k in ("q", "k_new", "v_new")} for case in cases]]
-        host_out = [torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory() for layer in layers]
+        host_out = [[torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory() for _ in range(2)]
+                    for layer in layers]
         h2d = sum(t.numel() * t.element_size() for hi in host_in for t in hi.values()) * n_dec
-        d2h = sum(t.numel() * t.element_size() for t in host_out) * n_dec
-        dev_in = [{k: torch.empty_like(v, device=device) for k, v in hi.items()} for hi in host_in]
+        d2h = sum(ho[0].numel() * ho[0].element_size() for ho in host_out) * n_dec
+        dev_in = [[{k: torch.empty_like(v, device=device) for k, v in hi.items()} for _ in range(2)] for hi in host_in]
+        dev_out = [[torch.empty_like(layer.out) for _ in range(2)] for layer in layers]
+        copy = torch.cuda.Stream(device)
+        ev = [[{n: torch.cuda.Event() for n in ("in", "done", "read")} for _ in range(2)] for _ in layers]
+        # every call of the timed region: (benchmark step, decode step, layer); buffer
+        # slot = the call's index among its layer's calls, mod 2
+        calls = [(k, t, li) for k in range(args.steps) for t in range(n_dec) for li in range(len(layers))]
+        slot = [(k * n_dec + t) % 2 for k, t, _ in calls]
+
+        def copy_in(c):  # input copy of call c into its buffer, once the buffer's last user ran
+            li, b = calls[c][2], slot[c]
+            copy.wait_event(ev[li][b]["done"])
+            with torch.cuda.stream(copy):
+                for k in ("q", "k_new", "v_new"):
+                    dev_in[li][b][k].copy_(host_in[li][k], non_blocking=True)
+            ev[li][b]["in"].record(copy)
+
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            for li in range(len(layers)):
-                layers[li].set_lengths(lens0[li])
-            for _ in range(n_dec):
-                for li, layer in enumerate(layers):
-                    for k in ("q", "k_new", "v_new"):
-                        dev_in[li][k].copy_(host_in[li][k], non_blocking=True)
-                    out = layer.step(dev_in[li]["q"], dev_in[li]["k_new"], dev_in[li]["v_new"], stream=stream,
-                                     max_seq_len=hint[li])
-                    host_out[li].copy_(out, non_blocking=True)
-            stream.synchronize()
+        copy_in(0)
+        for c, (k, t, li) in enumerate(calls):
+            if t == 0 and li == 0:
+                reset()  # lengths back to the start of the benchmark step (device copy, in stream order)
+            if c + 1 < len(calls):
+                copy_in(c + 1)
+            b = slot[c]
+            e = ev[li][b]
+            stream.wait_event(e["in"])
+            stream.wait_event(e["read"])  # the buffer's previous output has been read back
+            d = dev_in[li][b]
+            layers[li].step(d["q"], d["k_new"], d["v_new"], stream=stream, max_seq_len=hint[li], out=dev_out[li][b])
+            e["done"].record(stream)
+            copy.wait_event(e["done"])
+            with torch.cuda.stream(copy):
+                host_out[li][b].copy_(dev_out[li][b], non_blocking=True)
+            e["read"].record(copy)
+        stream.synchronize()
+        copy.synchronize()
         e2e_s = time.perf_counter() - t0
         barrier(world)
 

@@ -74,7 +74,7 @@ class DecodeLayer:
         self.max_len_hint = int(lens.max()) if lens.numel() else 0
 
     # ------------------------------------------------------------ calls
-    def args(self, q, k_new, v_new, max_seq_len=None, q_rot=None) -> B.UaaStepArgs:
+    def args(self, q, k_new, v_new, max_seq_len=None, q_rot=None, out=None) -> B.UaaStepArgs:
         a = B.UaaStepArgs()
         a.batch = self.batch
         a.q, a.k_new, a.v_new = B.ptr(q), B.ptr(k_new), B.ptr(v_new)
@@ -83,17 +83,20 @@ class DecodeLayer:
         a.cache_capacity = self.capacity
         a.seq_lens = B.ptr(self.seq_lens)
         a.max_seq_len = self.max_len_hint if max_seq_len is None else int(max_seq_len)
-        a.out = B.ptr(self.out)
+        a.out = B.ptr(self.out if out is None else out)
         a.q_rot = B.ptr(q_rot)
         return a
 
-    def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True, q_rot=None):
-        """One decode step (append, split-K partials, combine) on `stream`."""
+    def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True, q_rot=None, out=None):
+        """One decode step (append, split-K partials, combine) on `stream`; the output
+        rows go to `out` (a [B][Hq][D] tensor of the layer's output dtype) if given."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
-        B.uaa_decode_attn(self.desc, self.args(q, k_new, v_new, max_seq_len, q_rot=q_rot), self.ws, s)
+        if out is not None:
+            assert out.shape == self.out.shape and out.dtype == self.out.dtype and out.is_contiguous()
+        B.uaa_decode_attn(self.desc, self.args(q, k_new, v_new, max_seq_len, q_rot=q_rot, out=out), self.ws, s)
         if advance_hint and max_seq_len is None:
             self.max_len_hint += 1
-        return self.out
+        return self.out if out is None else out
 
     def append(self, q, k_new, v_new, stream=None, q_rot=None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
