@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 {
     extern __shared__ long long starts[];  // [P' + 1] range starts, then [R][nh] weights (floats)
     grid_dependency_wait();                // the partial kernel's records are complete
+    allow_dependent_launch();
     if (blockIdx.x == gridDim.x - 1) {     // the extra CTA: the partial kernel's range balance
         if (p.bal.header && threadIdx.x < 32) rebalance(p.bal, p.P, threadIdx.x);
         return;

@@ -194,6 +194,16 @@ __device__ __forceinline__ void grid_dependency_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Lets the next kernel on the stream (launched with launch_dependent) be
+// scheduled before this one completes: its CTAs take SMs as this grid's tail
+// frees them and do their set-up; its grid_dependency_wait still waits for this
+// grid to complete. Only the combine uses it: triggered from the partial kernel
+// it cost 3 % (combine CTAs parked on SMs the partial kernel's tail still used).
+__device__ __forceinline__ void allow_dependent_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void store_out(void* out, int dtype, size_t i, float v)
 {
     if (dtype == UAA_DTYPE_F32)
