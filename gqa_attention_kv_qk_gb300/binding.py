@@ -67,6 +67,7 @@ class UaaWorkspaceLayout(ctypes.Structure):
                 ("rec_o_offset", ctypes.c_size_t), ("prefix_stride", ctypes.c_size_t),
                 ("rec_lse_stride", ctypes.c_size_t), ("rec_o_stride", ctypes.c_size_t),
                 ("ranges_offset", ctypes.c_size_t), ("ranges_stride", ctypes.c_size_t),
+                ("owners_offset", ctypes.c_size_t), ("owners_stride", ctypes.c_size_t),
                 ("balance_offset", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
 
 

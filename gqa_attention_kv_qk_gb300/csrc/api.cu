@@ -105,8 +105,8 @@ struct Plan {
     int slice;           // sequences per partial launch
     int n_slices;
     int per_sm;          // resident CTAs per SM
-    size_t off_status, off_qrot, off_prefix, off_rec_lse, off_rec_o, off_ranges, off_balance, total;
-    size_t prefix_stride, rec_lse_stride, rec_o_stride, ranges_stride;  // bytes per slice
+    size_t off_status, off_qrot, off_prefix, off_rec_lse, off_rec_o, off_ranges, off_owners, off_balance, total;
+    size_t prefix_stride, rec_lse_stride, rec_o_stride, ranges_stride, owners_stride;  // bytes per slice
 };
 
 int device_sm_count()
@@ -178,6 +178,7 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     p.rec_lse_stride = align256(2 * P * HC * 4);
     p.rec_o_stride = align256(2 * P * HC * D * 4);
     p.ranges_stride = align256((P + 1) * 8);
+    p.owners_stride = align256((size_t)p.slice * d->n_kv_heads * p.head_groups * 8);
     p.off_status = 0;
     p.off_balance = 256;
     p.off_qrot = p.off_balance + balance_bytes(p.n_ctas);
@@ -185,7 +186,8 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     p.off_rec_lse = p.off_prefix + p.n_slices * p.prefix_stride;
     p.off_rec_o = p.off_rec_lse + p.n_slices * p.rec_lse_stride;
     p.off_ranges = p.off_rec_o + p.n_slices * p.rec_o_stride;
-    p.total = p.off_ranges + p.n_slices * p.ranges_stride;
+    p.off_owners = p.off_ranges + p.n_slices * p.ranges_stride;
+    p.total = p.off_owners + p.n_slices * p.owners_stride;
     *pl = p;
     return UAA_OK;
 }
@@ -428,6 +430,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.seq_lens = a->seq_lens + b0;
         p.prefix = reinterpret_cast<int*>(w + pl.off_prefix + sl * pl.prefix_stride);
         p.ranges = reinterpret_cast<long long*>(w + pl.off_ranges + sl * pl.ranges_stride);
+        p.owners = reinterpret_cast<unsigned*>(w + pl.off_owners + sl * pl.owners_stride);
         if (pl.kernel == 1) {
             p.bal = balance_of(w, pl);
             p.slice = sl;
@@ -493,6 +496,7 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.seq_lens = a->seq_lens + b0;
         p.prefix = reinterpret_cast<const int*>(w + pl.off_prefix + sl * pl.prefix_stride);
         p.ranges = reinterpret_cast<const long long*>(w + pl.off_ranges + sl * pl.ranges_stride);
+        p.owners = reinterpret_cast<unsigned*>(w + pl.off_owners + sl * pl.owners_stride);
         if (pl.kernel == 1) p.bal = balance_of(w, pl);
         p.rec_lse = reinterpret_cast<const float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
         p.rec_o = reinterpret_cast<const float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
@@ -600,6 +604,8 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, in
     layout->rec_o_stride = pl.rec_o_stride;
     layout->ranges_offset = pl.off_ranges;
     layout->ranges_stride = pl.ranges_stride;
+    layout->owners_offset = pl.off_owners;
+    layout->owners_stride = pl.owners_stride;
     layout->balance_offset = pl.off_balance;
     layout->total_bytes = pl.total;
     return UAA_OK;

@@ -12,9 +12,9 @@
 // which is the full softmax over every visible key with the sink's mass in the
 // denominator only. A sequence with no visible key gets zeros.
 //
-// The partial kernel leaves the table of its P' = min(CTAs, stages) range starts;
-// every range is non-empty, so the owners of a cut unit's stages are exactly
-// the ranges cA .. cB (found by binary search in the table). The record weights are formed per
+// Every range is non-empty, so the owners of a cut unit's stages are exactly the
+// ranges cA .. cB, which the partial kernel leaves per unit (UnitOwners in
+// internal.cuh). The record weights are formed per
 // head from one parallel round of loads; every thread then loads all records'
 // rows for four output elements before it adds any of them.
 #include "internal.cuh"
@@ -28,8 +28,8 @@ constexpr int kRecBatch = 4;     // records loaded together per output element
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
-    extern __shared__ long long starts[];  // [P' + 1] range starts, then [R][nh] weights (floats)
-    grid_dependency_wait();                // the partial kernel's records are complete
+    extern __shared__ float wts[];  // [R][nh]: record log2-sum-exp, then weights
+    grid_dependency_wait();         // the partial kernel's records are complete
     allow_dependent_launch();
     if (blockIdx.x == gridDim.x - 1) {     // the extra CTA: the partial kernel's range balance
         if (p.bal.header && threadIdx.x < 32) rebalance(p.bal, p.P, threadIdx.x);
@@ -43,23 +43,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int h0 = kvh * p.G + hg * HC;
     const int nh = min(HC, p.G - hg * HC);
     const int D = p.D;
-    const int stg = (p.prefix[b + 1] - p.prefix[b]) / units;
     const int tid = threadIdx.x;
     const size_t out0 = (static_cast<size_t>(b) * p.Hq + h0) * D;
-    if (stg == 0) {  // nothing visible: zeros
+    // the unit's first and last owner, left by the partial kernel (cleared for the next launch)
+    unsigned* own = p.owners + 2 * static_cast<size_t>(blockIdx.x);
+    const unsigned first = own[0], last = own[1];
+    __syncthreads();  // every thread has read the pair
+    if (tid == 0) {
+        own[0] = 0u;
+        own[1] = 0u;
+    }
+    if (first == 0u || last == 0u) {  // no visible key: zeros
         for (int idx = tid; idx < nh * D; idx += kCombineThreads) store_out(p.out, p.out_dtype, out0 + idx, 0.f);
         return;
     }
-    const long long T = p.prefix[p.B];
-    const int P = T < p.P ? static_cast<int>(T) : p.P;
-    const long long A = p.prefix[b] + static_cast<long long>(u) * stg;
-    for (int i = tid; i <= P; i += kCombineThreads) starts[i] = p.ranges[i];
-    __syncthreads();
-    const int cA = range_of(starts, P, A), cB = range_of(starts, P, A + stg - 1);
+    const int cA = static_cast<int>(first & 0x7fffffffu) - 1, cB = static_cast<int>(last) - 1;
     if (cA == cB) return;  // a whole unit: the partial kernel wrote it
-    const bool first_is_slot0 = starts[cA] == A;
+    const bool first_is_slot0 = (first & 0x80000000u) != 0u;
     const int R = cB - cA + 1;  // the unit's records: owners cA .. cB
-    float* wts = reinterpret_cast<float*>(starts + P + 1);
 
     for (int i = tid; i < R * nh; i += kCombineThreads)
         wts[i] = p.rec_lse[static_cast<size_t>(record_of(cA + i / nh, cA, first_is_slot0)) * HC + (i % nh)];
@@ -121,9 +122,8 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s)
     // one CTA per unit, and one that rebalances the partial kernel's ranges
     const long long blocks = static_cast<long long>(p.B) * p.Hkv * p.head_groups + 1;
     if (blocks == 1) return cudaSuccess;
-    // the range starts, then weights for up to every range's record of a unit
-    const size_t smem = static_cast<size_t>(p.P + 1) * 8 +
-                        static_cast<size_t>(p.P) * (p.heads_per_cta < kMaxHeads ? p.heads_per_cta : kMaxHeads) * 4;
+    // weights for up to every range's record of a unit
+    const size_t smem = static_cast<size_t>(p.P) * (p.heads_per_cta < kMaxHeads ? p.heads_per_cta : kMaxHeads) * 4;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));

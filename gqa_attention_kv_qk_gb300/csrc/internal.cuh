@@ -78,6 +78,12 @@ constexpr unsigned kBalanceMagic = 0x42414c31u;
 // the first owner vA is that range's first segment (slot 0) only if the unit
 // starts where vA starts; every later owner's piece starts its range (slot 0).
 //
+// Unit owners: the partial kernel writes, for each unit it touches, owners[2 u]
+// = (vA + 1) | 2^31 if the first piece is vA's first segment, from the range
+// holding the unit's first stage, and owners[2 u + 1] = vB + 1 from the range
+// holding its last stage; the combine reads the pair (0: no stages) and clears
+// it, so it needs neither the range table nor the stage prefix.
+//
 // Balance (tensor-core kernel): CTAs run at different speeds on different SMs
 // (some groups of SMs stream 7-10 % slower), so equal ranges leave the fast
 // CTAs idle at the end. Each CTA claims a range slot tied to its SM (slot
@@ -101,6 +107,7 @@ struct PartialParams {
     int* seq_lens;          // slice-relative (advanced by the fused kernel only)
     int* prefix;            // [B + 1] stage prefix over sequences, written for the combine
     long long* ranges;      // [P' + 1] range starts, written for the combine
+    unsigned* owners;       // [B][units][2] first / last owner of each unit (UnitOwners), for the combine
     // balance state (tensor-core kernel; null: uniform ranges)
     BalanceState bal;
     int slice;              // index of this launch's batch slice (part of the claim tag)
@@ -138,6 +145,7 @@ struct CombineParams {
     const int* seq_lens;    // slice-relative
     const int* prefix;      // [B + 1]
     const long long* ranges;  // [P' + 1] range starts of the partial launch
+    unsigned* owners;       // [B][units][2] written by the partial launch, cleared here
     BalanceState bal;       // of the tensor-core partial kernel (null pointers otherwise)
     const float* rec_o;
     const float* rec_lse;

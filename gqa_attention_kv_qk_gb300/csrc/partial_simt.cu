@@ -50,6 +50,11 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
         const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
         const int h0 = sg.kvh * p.G + sg.hg * kSimtHeads;
         const int nh = min(kSimtHeads, p.G - sg.hg * kSimtHeads);
+        if (threadIdx.x == 0) {  // this range's part in the unit's owners, for the combine
+            unsigned* own = p.owners + 2 * (static_cast<size_t>(sg.b) * units + sg.kvh * p.head_groups + sg.hg);
+            if (sg.st0 == 0) own[0] = (blockIdx.x + 1u) | (pos == s_c ? 0x80000000u : 0u);
+            if (sg.st0 + sg.n_st == sg.stages) own[1] = blockIdx.x + 1u;
+        }
         const int t0 = sg.lo / kTileKeys;
         const int j_beg = max(sg.lo, (t0 + sg.st0) * kTileKeys);
         const int j_end = min(sg.hi, (t0 + sg.st0 + sg.n_st) * kTileKeys);

@@ -604,6 +604,11 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
             const int h0 = sg.kvh * p.G + sg.hg * HC;
             const int nh = min(HC, p.G - sg.hg * HC);
+            if (lane == 0) {  // this range's part in the unit's owners, for the combine
+                unsigned* own = p.owners + 2 * (static_cast<size_t>(sg.b) * units + sg.kvh * p.head_groups + sg.hg);
+                if (sg.st0 == 0) own[0] = (static_cast<unsigned>(slot) + 1u) | (pos == s_c ? 0x80000000u : 0u);
+                if (sg.st0 + sg.n_st == sg.stages) own[1] = static_cast<unsigned>(slot) + 1u;
+            }
             if (p.fused) {
                 const int L = lens[sg.b];
                 const bool fits = L >= 0 && L < p.cap;

@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 4
+#define UAA_ABI_VERSION 5
 
 typedef enum {
     UAA_OK = 0,
@@ -181,6 +181,9 @@ typedef struct {
     size_t ranges_offset;     /* int64 [n_slices][P' + 1]: start stage of each range of the
                                  last partial launch of the slice (P' = min(P, stages)) */
     size_t ranges_stride;
+    size_t owners_offset;     /* uint32 [n_slices][slice_batch][units][2]: first / last range
+                                 owning each unit's stages (the combine reads and clears them) */
+    size_t owners_stride;
     size_t balance_offset;    /* range-balance state of the tensor-core kernel (opaque), right
                                  after the status word so that it survives a change of batch */
     size_t total_bytes;

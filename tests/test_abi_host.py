@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 4
+    assert B.uaa_abi_version() == 5
 
 
 def good_desc(**kw):
@@ -146,11 +146,14 @@ def test_workspace_layout_is_consistent(L, name):
             assert lay.q_rot_offset >= lay.balance_offset + 256 + 8 * P + 4 * (3 * P + 1)
             assert lay.ranges_offset >= lay.rec_o_offset + lay.n_slices * lay.rec_o_stride
             assert lay.ranges_stride >= (P + 1) * 8
-            assert lay.total_bytes >= lay.ranges_offset + lay.n_slices * lay.ranges_stride
+            assert lay.owners_offset >= lay.ranges_offset + lay.n_slices * lay.ranges_stride
+            units = layer["n_kv_heads"] * -(-(Hq // layer["n_kv_heads"]) // HC)
+            assert lay.owners_stride >= lay.slice_batch * units * 8
+            assert lay.total_bytes >= lay.owners_offset + lay.n_slices * lay.owners_stride
             assert B.uaa_workspace_size(d, batch, longest, n_sm) == lay.total_bytes
             assert B.uaa_num_splits(d, batch, longest, n_sm) == P
             for off in (lay.q_rot_offset, lay.prefix_offset, lay.rec_lse_offset, lay.rec_o_offset,
-                        lay.ranges_offset, lay.balance_offset):
+                        lay.ranges_offset, lay.owners_offset, lay.balance_offset):
                 assert off % 256 == 0
 
 
