@@ -465,14 +465,22 @@ __device__ inline int claim_slot(const PartialParams& p, unsigned& w0, unsigned&
 {
     const int P = static_cast<int>(gridDim.x);
     const BalanceState& b = p.bal;
-    const bool tables = __ldcg(b.header) == kBalanceMagic && __ldcg(b.header + 1) == static_cast<unsigned>(P);
-    const unsigned long long tag =
-        (static_cast<unsigned long long>(__ldcg(b.header + 2)) + 1ull) << 20 | static_cast<unsigned>(p.slice);
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     const int v0 = static_cast<int>((static_cast<unsigned long long>(smid) * p.per_sm) % P);
-    wP = tables ? __ldcg(b.cumw + P) : 0u;
-    for (int k = 0; k < P; ++k) {
+    // one round of independent reads: the header, the first-choice slot and its weights
+    const unsigned magic = __ldcg(b.header), hp = __ldcg(b.header + 1), gen = __ldcg(b.header + 2);
+    const unsigned c0 = __ldcg(b.cumw + v0), c1 = __ldcg(b.cumw + v0 + 1), cP = __ldcg(b.cumw + P);
+    const unsigned long long seen = __ldcg(b.claim + v0);
+    const bool tables = magic == kBalanceMagic && hp == static_cast<unsigned>(P);
+    const unsigned long long tag = (static_cast<unsigned long long>(gen) + 1ull) << 20 | static_cast<unsigned>(p.slice);
+    wP = tables ? cP : 0u;
+    if (seen != tag && atomicCAS(b.claim + v0, seen, tag) == seen) {
+        w0 = wP ? c0 : 0u;
+        w1 = wP ? c1 : 0u;
+        return v0;
+    }
+    for (int k = 1; k < P; ++k) {  // the first choice was taken: the next free slot
         const int v = v0 + k < P ? v0 + k : v0 + k - P;
         const unsigned long long old = __ldcg(b.claim + v);
         if (old != tag && atomicCAS(b.claim + v, old, tag) == old) {

@@ -459,9 +459,11 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t bar_empty = bar_full + 8 * SH::kStages;
     const uint32_t bar_qfull = bar_empty + 8 * SH::kStages;  // prep warp -> consumers: a segment's q' is ready
     const uint32_t bar_qempty = bar_qfull + 8;               // consumers -> prep warp: the q' slot is free
-    // control block: barriers at 0 and 8; slot 16; weights 20-28; range start 32, end 40; go flag 48
+    // control block: barriers at 0 and 8; slot 16; weights 20-28; range start 32, end 40; go flag 48;
+    // staging-ready flags 56, 60
     uint8_t* ctl = base_ptr + SH::kRingBytes + 16 * SH::kStages;
     const uint32_t go = ptx::smem_u32(ctl + 48);  // release_producer's flag (never 0 as an address)
+    const uint32_t rows_ready = ptx::smem_u32(ctl + 56);  // [2]: segment + 1 whose new rows staging slot i holds
     int* prefix = reinterpret_cast<int*>(ctl + SH::kCtlBytes);
     int* lens = prefix + SH::kPrefixBytes / 4;
     uint8_t* frag = reinterpret_cast<uint8_t*>(lens) + SH::kLensBytes;
@@ -479,6 +481,8 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         ptx::mbar_init(bar_qfull, 1);
         ptx::mbar_init(bar_qempty, kConsumerWarps);
         ptx::flag_set(go, 0u);
+        ptx::flag_set(rows_ready, 0u);
+        ptx::flag_set(rows_ready + 4, 0u);
         ptx::fence_barrier_init();
     } else if (threadIdx.x == 32 * kProducerWarp) {
         ptx::prefetch_tensormap(&tm_k);
@@ -616,17 +620,30 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (ends) prefetch_new_rows<D>(p, sg.b, sg.kvh, lane);
                 const bool rot = p.q_rot_out != nullptr && sg.st0 == 0;
                 uint8_t* st_row = staging + (seg & 1) * SH::kNewRowBytes;
-                if (p.io_dtype == UAA_DTYPE_F32) {
+                if (p.io_dtype == UAA_DTYPE_F32)
                     prep_fused_q<D, HC, float>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s, frag,
                                                SH::kFragRow, seg == 0 ? go : 0u, lane);
-                    if (ends) prep_new_rows<D, VQ8, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
-                } else {
+                else
                     prep_fused_q<D, HC, __nv_bfloat16>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s,
                                                        frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
-                    if (ends)
-                        prep_new_rows<D, VQ8, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
-                }
                 cs_b = sg.b;
+                // the q' fragments go to the consumers first; the new rows are needed only at
+                // the segment's last stage (rows_ready)
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_qfull);
+                if (ends) {
+                    if (p.io_dtype == UAA_DTYPE_F32)
+                        prep_new_rows<D, VQ8, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
+                    else
+                        prep_new_rows<D, VQ8, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence_block();
+                        ptx::flag_set(rows_ready + 4 * (seg & 1), static_cast<unsigned>(seg) + 1u);
+                    }
+                }
+                pos += sg.n_st;
+                continue;
             } else {
                 prep_loaded_q<D, HC>(p, sg.b, h0, nh, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
             }
@@ -703,9 +720,20 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             }
             const int kbase = (t0 + MG * (sg.st0 + k)) * kTileKeys + key_w;  // this warp's first key
-            if (!failed && warp == new_w && k + 1 == sg.n_st)  // the new key's row, over what the load brought
-                patch_stage_row<D, VQ8, TK>(staging + (seg & 1) * SH::kNewRowBytes, base_ptr + s * SH::kStageBytes,
-                                            new_r, SH::kKBytes, SH::kVBytes, lane);
+            if (!failed && warp == new_w && k + 1 == sg.n_st) {  // the new key's row, over what the load brought
+                bool ready = true;
+                if (lane == 0) {
+                    ready = ptx::flag_wait_eq(rows_ready + 4 * (seg & 1), static_cast<unsigned>(seg) + 1u,
+                                              kWaitLimitCycles);
+                    if (!ready) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                    __threadfence_block();
+                }
+                if (__shfl_sync(0xffffffffu, ready, 0))
+                    patch_stage_row<D, VQ8, TK>(staging + (seg & 1) * SH::kNewRowBytes,
+                                                base_ptr + s * SH::kStageBytes, new_r, SH::kKBytes, SH::kVBytes, lane);
+                else
+                    failed = true;
+            }
             if (!failed && kbase < hi && kbase + 16 * MG > lo) {
                 const bool whole = kbase >= lo && kbase + 16 * MG <= hi;
                 const uint32_t st = base + s * SH::kStageBytes;

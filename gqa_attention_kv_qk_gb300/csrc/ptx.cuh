@@ -210,6 +210,17 @@ __device__ __forceinline__ bool flag_wait(uint32_t addr, long long limit)
     return true;
 }
 
+// Waits until the flag holds `value`; gives up after `limit` cycles (returns false).
+__device__ __forceinline__ bool flag_wait_eq(uint32_t addr, uint32_t value, long long limit)
+{
+    const long long t0 = clock64();
+    while (flag_get(addr) != value) {
+        if (clock64() - t0 > limit) return false;
+        __nanosleep(32);
+    }
+    return true;
+}
+
 // 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned),
 // completed by cp_async_wait_all in the issuing thread.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)
