@@ -75,6 +75,18 @@ class DecodeLayer:
 
     # ------------------------------------------------------------ calls
     def args(self, q, k_new, v_new, max_seq_len=None, q_rot=None, out=None) -> B.UaaStepArgs:
+        """The step's argument struct (a copy of one built once per distinct set of pointers)."""
+        msl = self.max_len_hint if max_seq_len is None else int(max_seq_len)
+        key = (B.ptr(q), B.ptr(k_new), B.ptr(v_new), msl, B.ptr(q_rot), B.ptr(self.out if out is None else out))
+        cache = self.__dict__.setdefault("_args_cache", {})
+        a = cache.get(key)
+        if a is None:
+            if len(cache) > 64:
+                cache.clear()
+            a = cache[key] = self._build_args(q, k_new, v_new, msl, q_rot, out)
+        return B.UaaStepArgs.from_buffer_copy(a)  # a copy: callers may change fields
+
+    def _build_args(self, q, k_new, v_new, max_seq_len, q_rot, out) -> B.UaaStepArgs:
         a = B.UaaStepArgs()
         a.batch = self.batch
         a.q, a.k_new, a.v_new = B.ptr(q), B.ptr(k_new), B.ptr(v_new)
@@ -82,7 +94,7 @@ class DecodeLayer:
         a.k_cache, a.v_cache, a.v_scale = B.ptr(self.k_cache), B.ptr(self.v_cache), B.ptr(self.v_scale)
         a.cache_capacity = self.capacity
         a.seq_lens = B.ptr(self.seq_lens)
-        a.max_seq_len = self.max_len_hint if max_seq_len is None else int(max_seq_len)
+        a.max_seq_len = max_seq_len
         a.out = B.ptr(self.out if out is None else out)
         a.q_rot = B.ptr(q_rot)
         return a
