@@ -21,7 +21,7 @@ import torch
 
 TILE = 64  # cache capacities are rounded up to a multiple of this many slots
 
-# The five workloads. Method keys follow the oracle / library vocabulary;
+# The workloads. Method keys follow the oracle / library vocabulary;
 # workload keys: batch, seq_len (int, or (lo, hi) inclusive for ragged lengths),
 # steps, seed, layers (per-layer overrides; one cache per layer).
 CONFIGS: dict[str, dict] = {
@@ -56,6 +56,17 @@ CONFIGS: dict[str, dict] = {
         kv_dtype="vq8", io_dtype="bf16", out_dtype="f32",
         rope_style="neox", rope_theta=150000.0, rope_scaling="yarn", factor=32.0,
         original_max_pos=4096, beta_fast=32.0, beta_slow=1.0, has_sink=True),
+    # Gemma-3-12B-like decode: QK RMSNorm whose weights are stored as deltas from
+    # one (applied as 1 + w), scale 1/sqrt(256), no softcap; one layer of each
+    # kind per step (the model runs five local layers per global one): a local
+    # layer with a 1024-token window and base 10^4, a global one with base 10^6
+    # and linear scaling 8.
+    "gemma3_12b_local_global": dict(
+        batch=8, n_q_heads=16, n_kv_heads=8, head_dim=256, seq_len=(1024, 16384), steps=1, seed=5,
+        kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=1000000.0, rope_scaling="linear", factor=8.0,
+        qk_norm=True, norm_offset=True, norm_eps=1e-6, norm_w_range=(-0.5, 0.5), scale=1.0 / 16.0,
+        layers=[dict(window=1024, rope_theta=10000.0, rope_scaling="none", factor=1.0), dict(window=0)]),
 }
 
 _TAGS = {"q": 1, "k_new": 2, "v_new": 3, "k_cache": 4, "v_cache": 5, "q_norm_w": 6,

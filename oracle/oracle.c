@@ -55,8 +55,9 @@ uint16_t oracle_bf16_from_double(double x)
 /* ------------------------------------------------------------------ RoPE */
 
 /*
- * Inverse frequencies theta_p = base^(-2p/D), p = 0 .. D/2-1, then the scaling
- * rule (huggingface_decoder_completeness.md, P0.2 "RoPE scaling"):
+ * Inverse frequencies theta_p = base^(-2p/D), p = 0 .. D/2-1, over the D rotated
+ * dims of a head (its rotary_dim, else head_dim), then the scaling rule
+ * (huggingface_decoder_completeness.md, P0.2 "RoPE scaling"):
  *
  * llama3 (Llama-3.1 frequency interpolation; its four parameters factor, low 1,
  * high 4, original 8192 are the ones FreeToken PR #722 "Changes" recovers):
@@ -75,12 +76,23 @@ uint16_t oracle_bf16_from_double(double x)
  *   ramp_p = clamp((p - lo) / (hi - lo), 0, 1),
  *   theta'_p = theta_p / factor * ramp_p + theta_p * (1 - ramp_p),
  *   cos and sin are multiplied by attn_factor (default 0.1 ln(factor) + 1).
+ *
+ * linear: theta_p / factor.
  */
+/* Rotated dims of a head: rotary_dim, or the whole head (decoder page, P1.5:
+ * rotary_dim = head_dim * partial_rotary_factor; the frequencies follow the
+ * rotated dims). */
+static int rotary_dims(const oracle_desc* d)
+{
+    return d->rotary_dim > 0 ? d->rotary_dim : d->head_dim;
+}
+
 void oracle_rope_inv_freq(const oracle_desc* d, double* inv_freq, double* mscale)
 {
-    const int D = d->head_dim, half = D / 2;
+    const int D = rotary_dims(d), half = D / 2;
     const double base = d->rope_theta;
     *mscale = 1.0;
+    for (int p = 0; p < d->head_dim / 2; ++p) inv_freq[p] = 0.0;
     for (int p = 0; p < half; ++p)
         inv_freq[p] = pow(base, -2.0 * (double)p / (double)D);
 
@@ -116,17 +128,23 @@ void oracle_rope_inv_freq(const oracle_desc* d, double* inv_freq, double* mscale
             *mscale = d->attn_factor;
         else
             *mscale = d->factor > 1.0 ? 0.1 * log(d->factor) + 1.0 : 1.0;
+    } else if (d->rope_scaling == ORACLE_SCALING_LINEAR) {
+        /* linear: every frequency divided by factor, i.e. positions divided by
+         * it (support-matrix page, "Structural fact requirements": the gemma3
+         * lane's global layers) */
+        for (int p = 0; p < half; ++p) inv_freq[p] /= d->factor;
     }
 }
 
-/* RMSNorm over one head row (decoder page, P1.1 with offset 0, and P1.2: over
- * the last axis of each q and k head). */
-void oracle_rms_norm(const double* x, const float* w, int n, double eps, double* y)
+/* RMSNorm over one head row (decoder page, P1.1: offset 0, or 1 where the
+ * weight is stored as a delta, x * rsqrt * (1 + w); P1.2: over the last axis of
+ * each q and k head). */
+void oracle_rms_norm(const double* x, const float* w, int n, double eps, double w_offset, double* y)
 {
     double ss = 0.0;
     for (int i = 0; i < n; ++i) ss += x[i] * x[i];
     const double inv = 1.0 / sqrt(ss / (double)n + eps);
-    for (int i = 0; i < n; ++i) y[i] = x[i] * inv * (double)w[i];
+    for (int i = 0; i < n; ++i) y[i] = x[i] * inv * ((double)w[i] + w_offset);
 }
 
 /* Pair p is (p, p + D/2) for NeoX halves (the qwen convention), (2p, 2p+1) for
@@ -135,7 +153,8 @@ void oracle_rms_norm(const double* x, const float* w, int n, double eps, double*
 void oracle_rope_rotate(const oracle_desc* d, const double* inv_freq, double mscale,
                         long pos, const double* x, double* y)
 {
-    const int D = d->head_dim, half = D / 2;
+    const int D = rotary_dims(d), half = D / 2;
+    for (int i = D; i < d->head_dim; ++i) y[i] = x[i];  /* not rotated */
     for (int p = 0; p < half; ++p) {
         const int ia = d->rope_style == ORACLE_ROPE_NEOX ? p : 2 * p;
         const int ib = d->rope_style == ORACLE_ROPE_NEOX ? p + half : 2 * p + 1;
@@ -210,7 +229,7 @@ static void norm_and_rotate(const oracle_desc* d, const double* inv_freq, double
 {
     const int D = d->head_dim;
     if (d->qk_norm) {
-        oracle_rms_norm(x, norm_w, D, d->norm_eps, tmp);
+        oracle_rms_norm(x, norm_w, D, d->norm_eps, d->norm_offset ? 1.0 : 0.0, tmp);
         memcpy(x, tmp, sizeof(double) * (size_t)D);
     }
     oracle_rope_rotate(d, inv_freq, mscale, pos, x, tmp);

@@ -8,11 +8,13 @@
  * What one decode step computes, and where each part is defined:
  *   1. optional per-head RMSNorm of the new q and k rows, before rotation
  *      (huggingface_decoder_completeness.md, P1.2 "Qwen3 QK-norm"; RMSNorm
- *      itself: same page, P1.1);
+ *      itself, with Gemma's (1 + w) weight offset: same page, P1.1);
  *   2. rotary position embedding of q and k at the absolute KV index, NeoX
- *      halves or interleaved pairs, plain theta, Llama-3.1 "llama3" scaling or
- *      YaRN (same page, P0.2 and P1.3; llamay "Models and formats",
- *      "Architectures"; FreeToken PR #722, "Changes"; YaRN: Peng et al., 2023);
+ *      halves or interleaved pairs, plain theta, Llama-3.1 "llama3" scaling,
+ *      YaRN or linear scaling, over the whole head or its first rotary_dim
+ *      dims (same page, P0.2, P1.3 and P1.5; llamay "Models and formats",
+ *      "Architectures"; FreeToken PR #722, "Changes"; YaRN: Peng et al., 2023;
+ *      linear: Model support matrix, "Structural fact requirements");
  *   3. append of k and v at slot seq_len, the cache being fp32, bf16 or "vq8"
  *      (int8 values with one fp32 scale per token and head, keys exact)
  *      (llamay "Models and formats", "The KV cache, in three precisions");
@@ -39,7 +41,7 @@ extern "C" {
 #endif
 
 enum { ORACLE_ROPE_NEOX = 0, ORACLE_ROPE_INTERLEAVED = 1 };
-enum { ORACLE_SCALING_NONE = 0, ORACLE_SCALING_LLAMA3 = 1, ORACLE_SCALING_YARN = 2 };
+enum { ORACLE_SCALING_NONE = 0, ORACLE_SCALING_LLAMA3 = 1, ORACLE_SCALING_YARN = 2, ORACLE_SCALING_LINEAR = 3 };
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_VQ8 = 2 };
 
 typedef struct {
@@ -64,19 +66,24 @@ typedef struct {
     int has_sink;            /* 1: one sink logit per query head in the denominator */
     int kv_dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_VQ8 */
     int io_dtype;            /* ORACLE_F32 / ORACLE_BF16 for q, k_new, v_new */
+    int rotary_dim;          /* rotated dims of a head (even, <= head_dim); 0: head_dim */
+    int norm_offset;         /* 1: the RMSNorm weight is applied as (1 + w) */
 } oracle_desc;
 
 /* bf16 <-> fp64. The rounding is round-to-nearest, ties to even, overflow to inf. */
 double oracle_bf16_to_double(uint16_t h);
 uint16_t oracle_bf16_from_double(double x);
 
-/* Rotary inverse frequencies after scaling ([head_dim/2]) and the cos/sin multiplier. */
+/* Rotary inverse frequencies after scaling ([head_dim/2]; pairs at or beyond
+ * rotary_dim/2 are not rotated and get 0) and the cos/sin multiplier. */
 void oracle_rope_inv_freq(const oracle_desc* d, double* inv_freq, double* mscale);
 
-/* y = x * w / sqrt(mean(x^2) + eps) over one row of length n. */
-void oracle_rms_norm(const double* x, const float* w, int n, double eps, double* y);
+/* y = x * (w + w_offset) / sqrt(mean(x^2) + eps) over one row of length n
+ * (w_offset 0, or 1 for a weight stored as a delta from one). */
+void oracle_rms_norm(const double* x, const float* w, int n, double eps, double w_offset, double* y);
 
-/* Rotate one head row x (length head_dim) to absolute position pos. */
+/* Rotate one head row x (length head_dim) to absolute position pos; dims at or
+ * beyond rotary_dim are copied unchanged. */
 void oracle_rope_rotate(const oracle_desc* d, const double* inv_freq, double mscale,
                         long pos, const double* x, double* y);
 

@@ -8,6 +8,7 @@ A step description is a plain dict with the keys
   n_q_heads n_kv_heads head_dim scale rope_style rope_theta rope_scaling factor
   low_freq_factor high_freq_factor original_max_pos beta_fast beta_slow
   attn_factor qk_norm norm_eps window softcap has_sink kv_dtype io_dtype
+  rotary_dim norm_offset
 (missing keys take the neutral value: no scaling, no norm, no window, ...).
 """
 import ctypes
@@ -18,7 +19,7 @@ import numpy as np
 from . import build as _build
 
 _STYLE = {"neox": 0, "interleaved": 1}
-_SCALING = {"none": 0, "llama3": 1, "yarn": 2}
+_SCALING = {"none": 0, "llama3": 1, "yarn": 2, "linear": 3}
 _DTYPE = {"f32": 0, "bf16": 1, "vq8": 2}
 
 
@@ -34,6 +35,7 @@ class OracleDesc(ctypes.Structure):
         ("qk_norm", ctypes.c_int), ("norm_eps", ctypes.c_double),
         ("window", ctypes.c_int), ("softcap", ctypes.c_double), ("has_sink", ctypes.c_int),
         ("kv_dtype", ctypes.c_int), ("io_dtype", ctypes.c_int),
+        ("rotary_dim", ctypes.c_int), ("norm_offset", ctypes.c_int),
     ]
 
 
@@ -60,6 +62,8 @@ def make_desc(cfg: dict) -> OracleDesc:
     d.has_sink = int(bool(cfg.get("has_sink", False)))
     d.kv_dtype = _DTYPE[cfg.get("kv_dtype", "bf16")]
     d.io_dtype = _DTYPE[cfg.get("io_dtype", "bf16")]
+    d.rotary_dim = int(cfg.get("rotary_dim", 0) or 0)
+    d.norm_offset = int(bool(cfg.get("norm_offset", False)))
     return d
 
 
@@ -78,7 +82,7 @@ def lib():
         L.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         L.oracle_bf16_from_double.restype = ctypes.c_uint16
         L.oracle_rope_inv_freq.argtypes = [P(OracleDesc), dp, dp]
-        L.oracle_rms_norm.argtypes = [dp, fp, ctypes.c_int, ctypes.c_double, dp]
+        L.oracle_rms_norm.argtypes = [dp, fp, ctypes.c_int, ctypes.c_double, ctypes.c_double, dp]
         L.oracle_rope_rotate.argtypes = [P(OracleDesc), dp, ctypes.c_double, ctypes.c_long, dp, dp]
         L.oracle_vq8_quantize_row.argtypes = [fp, ctypes.c_int, P(ctypes.c_int8), fp]
         L.oracle_append.argtypes = [P(OracleDesc), ctypes.c_int, vp, vp, vp, fp, fp, vp, vp, fp,
@@ -140,12 +144,12 @@ def rope_inv_freq(cfg: dict):
     return out, ms.value
 
 
-def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float, w_offset: float = 0.0) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     w = np.ascontiguousarray(w, dtype=np.float32)
     y = np.zeros_like(x)
     lib().oracle_rms_norm(_ptr(x, ctypes.c_double), _ptr(w, ctypes.c_float), x.size, eps,
-                          _ptr(y, ctypes.c_double))
+                          float(w_offset), _ptr(y, ctypes.c_double))
     return y
 
 

@@ -23,10 +23,14 @@ def pair_indices(D: int, style: str):
     return 2 * p, 2 * p + 1
 
 
-def rotation_matrix(D: int, style: str, inv_freq: np.ndarray, mscale: float, pos: int) -> np.ndarray:
-    R = np.zeros((D, D), dtype=np.float64)
-    ia, ib = pair_indices(D, style)
-    ang = pos * inv_freq
+def rotation_matrix(D: int, style: str, inv_freq: np.ndarray, mscale: float, pos: int,
+                    rotary_dim: int = 0) -> np.ndarray:
+    """Block diagonal: the rotation of the first rotary_dim dims (all of them when
+    0), and the identity on the rest."""
+    rd = rotary_dim or D
+    R = np.eye(D, dtype=np.float64)
+    ia, ib = pair_indices(rd, style)
+    ang = pos * np.asarray(inv_freq)[: rd // 2]
     c, s = np.cos(ang) * mscale, np.sin(ang) * mscale
     R[ia, ia] = c
     R[ia, ib] = -s
@@ -35,8 +39,8 @@ def rotation_matrix(D: int, style: str, inv_freq: np.ndarray, mscale: float, pos
     return R
 
 
-def rmsnorm_rows(X: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
-    return X / np.sqrt(np.mean(X * X, axis=-1, keepdims=True) + eps) * w.astype(np.float64)
+def rmsnorm_rows(X: np.ndarray, w: np.ndarray, eps: float, w_offset: float = 0.0) -> np.ndarray:
+    return X / np.sqrt(np.mean(X * X, axis=-1, keepdims=True) + eps) * (w.astype(np.float64) + w_offset)
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
@@ -61,8 +65,10 @@ def decode_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, v_scale, seq_lens,
     Hkv = k_new.shape[1]
     G = Hq // Hkv
     style = cfg.get("rope_style", "neox")
+    rd = cfg.get("rotary_dim", 0) or D
+    off = 1.0 if cfg.get("norm_offset") else 0.0
     if inv_freq is None:
-        inv_freq = plain_inv_freq(D, cfg.get("rope_theta", 10000.0))
+        inv_freq = plain_inv_freq(rd, cfg.get("rope_theta", 10000.0))
     scale = cfg.get("scale", 0.0) or 1.0 / np.sqrt(D)
     kv = cfg.get("kv_dtype", "bf16")
     W = cfg.get("window", 0) or 0
@@ -70,11 +76,11 @@ def decode_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, v_scale, seq_lens,
     out = np.zeros((B, Hq, D))
     for b in range(B):
         pos = int(seq_lens[b])
-        R = rotation_matrix(D, style, inv_freq, mscale, pos)
+        R = rotation_matrix(D, style, inv_freq, mscale, pos, rd)
         qb, kb = q[b].astype(np.float64), k_new[b].astype(np.float64)
         if cfg.get("qk_norm"):
-            qb = rmsnorm_rows(qb, q_norm_w, cfg.get("norm_eps", 1e-6))
-            kb = rmsnorm_rows(kb, k_norm_w, cfg.get("norm_eps", 1e-6))
+            qb = rmsnorm_rows(qb, q_norm_w, cfg.get("norm_eps", 1e-6), off)
+            kb = rmsnorm_rows(kb, k_norm_w, cfg.get("norm_eps", 1e-6), off)
         qr = qb @ R.T
         kr = kb @ R.T
         if kv == "bf16":

@@ -230,6 +230,84 @@ def test_rmsnorm_one_row_and_invariants(oracle_mod):
         assert np.allclose(yc, np.sign(c) / math.sqrt(1 + 1e-6 / c ** 2), rtol=1e-14)
 
 
+def test_rmsnorm_weight_offset(oracle_mod):
+    """Decoder page P1.1: a weight stored as a delta from one applies as (1 + w);
+    a zero delta is the unit-weight norm, and the offset adds x / rms(x)."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(256)
+    w = rng.uniform(-0.5, 0.5, 256).astype(np.float32)
+    y = oracle_mod.rms_norm(x, w, 1e-6, 1.0)
+    r = np.sqrt(np.mean(x * x) + 1e-6)
+    assert np.allclose(y, x / r * (1.0 + w.astype(np.float64)), rtol=1e-14)
+    zeros, ones = np.zeros(256, dtype=np.float32), np.ones(256, dtype=np.float32)
+    assert np.array_equal(oracle_mod.rms_norm(x, zeros, 1e-6, 1.0), oracle_mod.rms_norm(x, ones, 1e-6, 0.0))
+    assert np.allclose(y - oracle_mod.rms_norm(x, w, 1e-6, 0.0), x / r, rtol=1e-12, atol=1e-15)
+
+
+# ------------------------------------------------------------------ partial rotary, linear scaling
+
+@pytest.mark.parametrize("style,D,R", [("neox", 64, 32), ("neox", 128, 96), ("interleaved", 64, 16),
+                                       ("neox", 256, 64)])
+def test_partial_rotary_rotates_the_first_dims_only(oracle_mod, style, D, R):
+    """Decoder page P1.5: rotary_dim = head_dim * partial_rotary_factor dims
+    rotate, with the frequencies of an R-wide head; the other dims pass as they
+    are. Checked against complex multiplication and against the full rotation of
+    an R-wide head on the first R dims."""
+    base = 10000.0
+    cfg = rope_cfg(rope_style=style, head_dim=D, rotary_dim=R, rope_theta=base)
+    inv, ms = oracle_mod.rope_inv_freq(cfg)
+    theta = base ** (-np.arange(R // 2) * 2.0 / R)
+    assert np.allclose(inv[: R // 2], theta, rtol=1e-15) and not inv[R // 2:].any() and ms == 1.0
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(D)
+    ia, ib = BF.pair_indices(R, style)
+    head_r = rope_cfg(rope_style=style, head_dim=R, rope_theta=base)
+    for pos in (0, 5, 3001):
+        y = oracle_mod.rope_rotate(cfg, x, pos)
+        assert np.array_equal(y[R:], x[R:])
+        z = (x[ia] + 1j * x[ib]) * np.exp(1j * pos * theta)
+        assert np.allclose(y[ia], z.real, atol=1e-12) and np.allclose(y[ib], z.imag, atol=1e-12)
+        assert np.array_equal(y[:R], oracle_mod.rope_rotate(head_r, x[:R].copy(), pos))
+
+
+def test_full_rotary_dim_is_the_default(oracle_mod):
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal(128)
+    for style in ("neox", "interleaved"):
+        a = rope_cfg(rope_style=style, head_dim=128, rope_scaling="yarn", factor=32.0, original_max_pos=4096)
+        for pos in (1, 70000):
+            assert np.array_equal(oracle_mod.rope_rotate(a, x, pos),
+                                  oracle_mod.rope_rotate(dict(a, rotary_dim=128), x, pos))
+
+
+def test_yarn_factor_leaves_pass_through_dims_alone(oracle_mod):
+    """The attention factor scales the rotated pairs only (each keeps length
+    mscale times its own); dims beyond rotary_dim are copied."""
+    cfg = rope_cfg(head_dim=64, rotary_dim=32, rope_scaling="yarn", factor=32.0, original_max_pos=4096,
+                   rope_theta=150000.0)
+    inv, ms = oracle_mod.rope_inv_freq(cfg)
+    assert ms == pytest.approx(0.1 * math.log(32.0) + 1.0, rel=1e-15)
+    x = np.random.default_rng(10).standard_normal(64)
+    y = oracle_mod.rope_rotate(cfg, x, 999)
+    ia, ib = BF.pair_indices(32, "neox")
+    assert np.allclose(np.hypot(y[ia], y[ib]), ms * np.hypot(x[ia], x[ib]), rtol=1e-13)
+    assert np.array_equal(y[32:], x[32:])
+
+
+@pytest.mark.parametrize("factor", [8.0, 4.0])
+def test_linear_scaling_divides_positions(oracle_mod, factor):
+    """Support matrix, gemma3 lane: linear scaling of the global layers. Every
+    frequency is divided by the factor, so position f t rotates as position t
+    does without scaling (bit for bit: a power-of-two factor scales exactly)."""
+    cfg = rope_cfg(head_dim=128, rope_theta=1000000.0, rope_scaling="linear", factor=factor)
+    inv, ms = oracle_mod.rope_inv_freq(cfg)
+    assert np.array_equal(inv, unscaled(oracle_mod, cfg) / factor) and ms == 1.0
+    plain = dict(cfg, rope_scaling="none")
+    x = np.random.default_rng(11).standard_normal(128)
+    for t in (1, 100, 4096):
+        assert np.array_equal(oracle_mod.rope_rotate(cfg, x, int(factor) * t), oracle_mod.rope_rotate(plain, x, t))
+
+
 # ------------------------------------------------------------------ vq8
 
 def test_vq8_codes_bit_exact_vs_numpy_fp32(oracle_mod):
@@ -374,6 +452,12 @@ GRID = [
     dict(name="llama32_1b_tiny", n_q_heads=8, n_kv_heads=2, head_dim=64),
     dict(name="llama31_8b_decode", n_q_heads=4, n_kv_heads=2, head_dim=128, rope_scaling="none",
          kv_dtype="f32", io_dtype="f32", softcap=2.0, window=13, has_sink=True),
+    dict(name="qwen3_8b_ragged", n_q_heads=8, n_kv_heads=2, head_dim=128, rotary_dim=96, norm_offset=True),
+    dict(name="llama32_1b_tiny", n_q_heads=8, n_kv_heads=2, head_dim=64, rotary_dim=16),
+    dict(name="gptoss_vq8_sink", n_q_heads=8, n_kv_heads=2, head_dim=64, rotary_dim=32),
+    dict(name="gemma3_12b_local_global", n_q_heads=4, n_kv_heads=2, head_dim=64, layers=None),
+    dict(name="gemma3_12b_local_global", n_q_heads=4, n_kv_heads=2, head_dim=64,
+         layers=[dict(window=9, rope_theta=10000.0, rope_scaling="none")]),
 ]
 
 
@@ -432,7 +516,8 @@ def _err(a, b):
 
 
 @pytest.mark.parametrize("mistake", ["drop_sink", "ignore_window", "wrong_pairing", "skip_norm",
-                                     "no_softcap", "plain_rope_not_llama3"])
+                                     "no_softcap", "plain_rope_not_llama3", "no_norm_offset",
+                                     "full_rotary_not_partial", "no_linear_scaling", "global_theta_on_local"])
 def test_planted_mistakes_break_the_tolerance(oracle_mod, mistake):
     """llamay 'The bound, and why it is the one it is': a bound has teeth only if a
     degraded variant fails it. Each planted mistake must exceed the parity bar on
@@ -450,6 +535,15 @@ def test_planted_mistakes_break_the_tolerance(oracle_mod, mistake):
                                             layers=None), "softcap", 0.0, [150, 199], 4),
         "plain_rope_not_llama3": ("llama31_8b_decode", dict(n_q_heads=8, n_kv_heads=2),
                                   "rope_scaling", "none", [8000, 8100], 1),
+        "no_norm_offset": ("gemma3_12b_local_global", dict(n_q_heads=8, n_kv_heads=2, layers=None),
+                           "norm_offset", False, [150, 199], 1),
+        "full_rotary_not_partial": ("qwen3_8b_ragged", dict(n_q_heads=8, n_kv_heads=2, rotary_dim=96),
+                                    "rotary_dim", 0, [150, 199], 1),
+        "no_linear_scaling": ("gemma3_12b_local_global", dict(n_q_heads=8, n_kv_heads=2, layers=None),
+                              "rope_scaling", "none", [150, 199], 1),
+        "global_theta_on_local": ("gemma3_12b_local_global", dict(n_q_heads=8, n_kv_heads=2,
+                                  layers=[dict(window=1024, rope_theta=10000.0, rope_scaling="none")]),
+                                  "rope_theta", 1000000.0, [150, 199], 1),
     }[mistake]
     cfg = W.layer_configs(W.config(name, batch=2, seq_len=(0, max(lens) + 1), steps=1, **over))[0]
     case = host_case(cfg, lens=lens)
