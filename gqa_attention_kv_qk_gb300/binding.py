@@ -23,7 +23,7 @@ UAA_DEVFLAG_LEN_HINT = 0x2
 UAA_DEVFLAG_TIMEOUT = 0x4
 
 ROPE_STYLE = {"neox": 0, "interleaved": 1}
-ROPE_SCALING = {"none": 0, "llama3": 1, "yarn": 2}
+ROPE_SCALING = {"none": 0, "llama3": 1, "yarn": 2, "linear": 3}
 DTYPE = {"f32": 0, "bf16": 1, "vq8": 2}
 
 
@@ -41,7 +41,8 @@ class UaaAttnDesc(ctypes.Structure):
                 ("qk_norm", ctypes.c_int32), ("norm_eps", ctypes.c_float), ("window", ctypes.c_int32),
                 ("softcap", ctypes.c_float), ("has_sink", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
+                ("norm_offset", ctypes.c_int32)]
 
 
 class UaaStepArgs(ctypes.Structure):
@@ -247,6 +248,8 @@ def make_desc(cfg: dict) -> UaaAttnDesc:
     d.kv_dtype = DTYPE[cfg.get("kv_dtype", "bf16")]
     d.io_dtype = DTYPE[cfg.get("io_dtype", "bf16")]
     d.out_dtype = DTYPE[cfg.get("out_dtype", "f32")]
+    d.rotary_dim = int(cfg.get("rotary_dim", 0) or 0)
+    d.norm_offset = int(bool(cfg.get("norm_offset", False)))
     return d
 
 

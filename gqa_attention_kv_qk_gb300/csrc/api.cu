@@ -71,9 +71,18 @@ uaa_status check_desc(const uaa_attn_desc* d)
                         "yarn rope scaling needs factor>0, original_max_pos>0, beta_fast>beta_slow>0 "
                         "(got %g, %d, %g, %g)",
                         r.factor, r.original_max_pos, r.beta_fast, r.beta_slow);
+    } else if (r.scaling == UAA_ROPE_SCALING_LINEAR) {
+        if (!(r.factor > 0.0) || !isfinite(r.factor))
+            return fail(UAA_ERR_UNSUPPORTED, "linear rope scaling needs a finite factor>0 (got %g)", r.factor);
     } else if (r.scaling != UAA_ROPE_SCALING_NONE) {
-        return fail(UAA_ERR_UNSUPPORTED, "rope.scaling=%d is not supported (none, llama3, yarn)", r.scaling);
+        return fail(UAA_ERR_UNSUPPORTED, "rope.scaling=%d is not supported (none, llama3, yarn, linear)",
+                    r.scaling);
     }
+    if (d->rotary_dim != 0 && (d->rotary_dim < 2 || d->rotary_dim > d->head_dim || d->rotary_dim % 2 != 0))
+        return fail(UAA_ERR_UNSUPPORTED, "rotary_dim=%d is not 0 or an even value in [2, head_dim=%d]",
+                    d->rotary_dim, d->head_dim);
+    if (d->norm_offset != 0 && d->norm_offset != 1)
+        return fail(UAA_ERR_UNSUPPORTED, "norm_offset=%d is not 0 or 1", d->norm_offset);
     if (d->qk_norm != 0 && d->qk_norm != 1)
         return fail(UAA_ERR_UNSUPPORTED, "qk_norm=%d is not 0 or 1", d->qk_norm);
     if (d->qk_norm && (!(d->norm_eps >= 0.f) || !isfinite(d->norm_eps)))
@@ -264,12 +273,17 @@ float qscale(const uaa_attn_desc* d)
 }
 
 // Rotary frequencies theta'_p / pi in fp64 and the cos/sin multiplier: plain
-// base^(-2p/D); llama3 wavelength interpolation; YaRN ramp over the pair index
-// between the pairs whose wavelength fits beta_fast / beta_slow times into the
-// original context (huggingface_decoder_completeness.md, P0.2; YaRN as published).
+// base^(-2p/R) over the R rotated dims; llama3 wavelength interpolation; YaRN
+// ramp over the pair index between the pairs whose wavelength fits beta_fast /
+// beta_slow times into the original context; linear division by the factor
+// (huggingface_decoder_completeness.md, P0.2 and P1.5; YaRN as published).
+// Entries of pairs beyond R/2 stay 0 (those pairs are not rotated).
+int rotary_dims(const uaa_attn_desc* d) { return d->rotary_dim > 0 ? d->rotary_dim : d->head_dim; }
+
 void rope_table(const uaa_attn_desc* d, double* inv_freq_over_pi, float* mscale)
 {
-    const int D = d->head_dim;
+    const int D = rotary_dims(d);
+    for (int i = 0; i < d->head_dim / 2; ++i) inv_freq_over_pi[i] = 0.0;
     const double pi = 3.14159265358979323846;
     const uaa_rope_params& r = d->rope;
     double ms = 1.0;
@@ -298,6 +312,8 @@ void rope_table(const uaa_attn_desc* d, double* inv_freq_over_pi, float* mscale)
             double ramp = hi > lo ? (i - lo) / (hi - lo) : (i >= lo ? 1.0 : 0.0);
             ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
             g = ramp * (f / r.factor) + (1.0 - ramp) * f;
+        } else if (r.scaling == UAA_ROPE_SCALING_LINEAR) {
+            g = f / r.factor;
         }
         inv_freq_over_pi[i] = g / pi;
     }
@@ -355,8 +371,10 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.cap = a->cache_capacity;
     p.max_len = a->max_seq_len;
     p.style = d->rope.style;
+    p.half_rot = rotary_dims(d) / 2;
     p.qk_norm = d->qk_norm;
     p.eps = d->norm_eps;
+    p.norm_offset = d->norm_offset ? 1.f : 0.f;
     p.qscale = qscale(d);
     p.io_dtype = d->io_dtype;
     p.kv_dtype = d->kv_dtype;
@@ -454,8 +472,10 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
             p.io_dtype = d->io_dtype;
             p.kv_dtype = d->kv_dtype;
             p.style = d->rope.style;
+            p.half_rot = rotary_dims(d) / 2;
             p.qk_norm = d->qk_norm;
             p.eps = d->norm_eps;
+            p.norm_offset = d->norm_offset ? 1.f : 0.f;
             p.qscale = qscale(d);
             p.q_norm_w = a->q_norm_w;
             p.k_norm_w = a->k_norm_w;

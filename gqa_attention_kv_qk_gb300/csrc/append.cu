@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
 
 #pragma unroll
     for (int i0 = 0; i0 < HALF; i0 += 32)  // warp w takes pairs 32 w .. 32 w + 31
-        if (warp == i0 / 32) cs[i0 + lane] = rope_cos_sin(pos, param_at_lane(p.inv_freq_over_pi + i0, lane), p.mscale);
+        if (warp == i0 / 32)
+            cs[i0 + lane] = rope_pair_cos_sin(i0 + lane, p.half_rot, pos, param_at_lane(p.inv_freq_over_pi + i0, lane),
+                                              p.mscale);
     __syncthreads();  // the cos / sin table is complete
     for (int r = warp; r < n_rows; r += kAppendWarps) {
 #pragma unroll
@@ -120,15 +122,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
             const float inv = rms_inv(ss, D, p.eps);
             const float* w = is_q ? p.q_norm_w : p.k_norm_w;
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) x[i] = x[i] * inv * w[lane + 32 * i];
+            for (int i = 0; i < EPL; ++i) x[i] = x[i] * inv * (w[lane + 32 * i] + p.norm_offset);
         }
 #pragma unroll
         for (int i = 0; i < EPL; ++i) rowbuf[warp][lane + 32 * i] = x[i];
         __syncwarp();
 
         for (int pp = lane; pp < HALF; pp += 32) {
-            const int ia = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
-            const int ib = p.style == UAA_ROPE_NEOX ? pp + HALF : 2 * pp + 1;
+            const int2 e = rope_pair(pp, p.half_rot, D, p.style == UAA_ROPE_NEOX);
+            const int ia = e.x, ib = e.y;
             float ya = rowbuf[warp][ia], yb = rowbuf[warp][ib];
             rope_rotate(ya, yb, cs[pp]);
             if (is_q) {

@@ -22,8 +22,10 @@ struct AppendParams {
     int B, Hq, Hkv, D;
     int cap, max_len;
     int style;              // UAA_ROPE_NEOX / _INTERLEAVED
+    int half_rot;           // rotated pairs per head row (rotary_dim / 2)
     int qk_norm;
     float eps;
+    float norm_offset;      // added to each RMSNorm weight (0, or 1 for Gemma's stored delta)
     float qscale;           // q_prime = rotated q * qscale (the partial kernel's logit prescale)
     float mscale;           // cos / sin multiplier (YaRN attention factor, else 1)
     int io_dtype, kv_dtype;
@@ -129,7 +131,9 @@ struct PartialParams {
     const void* v_new;
     int io_dtype, kv_dtype;
     int style, qk_norm;
+    int half_rot;           // rotated pairs per head row (rotary_dim / 2)
     float eps, qscale, mscale;
+    float norm_offset;      // added to each RMSNorm weight
     const float* q_norm_w;
     const float* k_norm_w;
     float* q_rot_out;       // optional [B][Hq][D], slice-relative
@@ -419,6 +423,26 @@ __device__ __forceinline__ double param_at_lane(const double* table32, int lane)
 #pragma unroll
     for (int i = 0; i < 32; ++i) v = lane == i ? table32[i] : v;
     return v;
+}
+
+// (cos, sin) of rotation pair pp of a head whose first half_rot pairs rotate:
+// the angle pos * theta'_pp, or (1, 0) for a pair that passes unchanged (the
+// dims beyond rotary_dim, which no attention factor scales).
+__device__ __forceinline__ float2 rope_pair_cos_sin(int pp, int half_rot, int pos, double inv_freq_over_pi,
+                                                    float mscale)
+{
+    return pp < half_rot ? rope_cos_sin(pos, inv_freq_over_pi, mscale) : make_float2(1.f, 0.f);
+}
+
+// Row elements (a, b) of rotation pair pp, 0 <= pp < D/2, in a head of D dims
+// whose first 2 half_rot dims rotate. Interleaved: (2pp, 2pp+1) throughout.
+// NeoX: (pp, pp + half_rot) for a rotated pair; the pass-through dims
+// 2 half_rot .. D-1 are paired as (pp + half_rot, pp + D/2) so that every
+// element belongs to exactly one pair (with half_rot = D/2: (pp, pp + D/2)).
+__device__ __forceinline__ int2 rope_pair(int pp, int half_rot, int D, bool neox)
+{
+    if (!neox) return make_int2(2 * pp, 2 * pp + 1);
+    return pp < half_rot ? make_int2(pp, pp + half_rot) : make_int2(pp + half_rot, pp + D / 2);
 }
 
 // Rotation of pair (a, b) by the angle whose (cos, sin) is cs.

@@ -212,7 +212,13 @@ __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool
                              const double* freq, float2* cs, uint8_t* frag, int row_bytes, uint32_t go, int lane)
 {
     constexpr int NP = D / 64;
-    const bool neox = p.style == UAA_ROPE_NEOX;
+    int ia[NP], ib[NP];  // the row elements of this lane's pairs
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        const int2 e = rope_pair(lane + 32 * j, p.half_rot, D, p.style == UAA_ROPE_NEOX);
+        ia[j] = e.x;
+        ib[j] = e.y;
+    }
 #pragma unroll 1
     for (int hc0 = 0; hc0 < HC; hc0 += 8) {
         float xa[8][NP], xb[8][NP];
@@ -221,24 +227,23 @@ __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool
             const size_t qoff = (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                const int pp = lane + 32 * j;
-                xa[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + (neox ? pp : 2 * pp)) : 0.f;
-                xb[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + (neox ? pp + D / 2 : 2 * pp + 1)) : 0.f;
+                xa[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + ia[j]) : 0.f;
+                xb[i][j] = hc0 + i < nh ? load_as_float<T>(p.q, qoff + ib[j]) : 0.f;
             }
         }
         if (go && hc0 == 0) release_producer(go, lane);  // the first loads are issued: the key stream may start
         if (new_seq && hc0 == 0) {  // the rows' loads are in flight: (cos, sin) of this sequence's position
 #pragma unroll 1
-            for (int j = 0; j < NP; ++j) cs[lane + 32 * j] = rope_cos_sin(pos, freq[lane + 32 * j], p.mscale);
+            for (int j = 0; j < NP; ++j)
+                cs[lane + 32 * j] = rope_pair_cos_sin(lane + 32 * j, p.half_rot, pos, freq[lane + 32 * j], p.mscale);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float* raw = reinterpret_cast<float*>(frag + (hc0 + i) * row_bytes);
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                const int pp = lane + 32 * j;
-                raw[neox ? pp : 2 * pp] = xa[i][j];
-                raw[neox ? pp + D / 2 : 2 * pp + 1] = xb[i][j];
+                raw[ia[j]] = xa[i][j];
+                raw[ib[j]] = xb[i][j];
             }
         }
         __syncwarp();
@@ -250,9 +255,8 @@ __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool
             float ya[NP], yb[NP];
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                const int pp = lane + 32 * j;
-                ya[j] = raw[neox ? pp : 2 * pp];
-                yb[j] = raw[neox ? pp + D / 2 : 2 * pp + 1];
+                ya[j] = raw[ia[j]];
+                yb[j] = raw[ib[j]];
             }
             __syncwarp();  // every lane has its values before any writes fragments over them
             if (p.qk_norm && hv) {
@@ -262,23 +266,20 @@ __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool
                 const float inv = rms_inv(warp_sum(ss), D, p.eps);
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
-                    const int pp = lane + 32 * j;
-                    ya[j] = ya[j] * inv * p.q_norm_w[neox ? pp : 2 * pp];
-                    yb[j] = yb[j] * inv * p.q_norm_w[neox ? pp + D / 2 : 2 * pp + 1];
+                    ya[j] = ya[j] * inv * (p.q_norm_w[ia[j]] + p.norm_offset);
+                    yb[j] = yb[j] * inv * (p.q_norm_w[ib[j]] + p.norm_offset);
                 }
             }
             const size_t qoff = (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                const int pp = lane + 32 * j;
-                const int ia = neox ? pp : 2 * pp, ib = neox ? pp + D / 2 : 2 * pp + 1;
-                if (hv) rope_rotate(ya[j], yb[j], cs[pp]);
+                if (hv) rope_rotate(ya[j], yb[j], cs[lane + 32 * j]);
                 if (write_rot && hv) {
-                    p.q_rot_out[qoff + ia] = ya[j];
-                    p.q_rot_out[qoff + ib] = yb[j];
+                    p.q_rot_out[qoff + ia[j]] = ya[j];
+                    p.q_rot_out[qoff + ib[j]] = yb[j];
                 }
-                store_frag(row, ia, ya[j] * p.qscale);
-                store_frag(row, ib, yb[j] * p.qscale);
+                store_frag(row, ia[j], ya[j] * p.qscale);
+                store_frag(row, ib[j], yb[j] * p.qscale);
             }
         }
     }
@@ -343,9 +344,9 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
-        const int pp = lane + 32 * j;
-        ia[j] = p.style == UAA_ROPE_NEOX ? pp : 2 * pp;
-        ib[j] = p.style == UAA_ROPE_NEOX ? pp + D / 2 : 2 * pp + 1;
+        const int2 e = rope_pair(lane + 32 * j, p.half_rot, D, p.style == UAA_ROPE_NEOX);
+        ia[j] = e.x;
+        ib[j] = e.y;
         ka[j] = load_as_float<T>(p.k_new, src + ia[j]);
         kb[j] = load_as_float<T>(p.k_new, src + ib[j]);
         ss += ka[j] * ka[j] + kb[j] * kb[j];
@@ -356,8 +357,8 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
         const float inv = rms_inv(warp_sum(ss), D, p.eps);
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
-            ka[j] = ka[j] * inv * p.k_norm_w[ia[j]];
-            kb[j] = kb[j] * inv * p.k_norm_w[ib[j]];
+            ka[j] = ka[j] * inv * (p.k_norm_w[ia[j]] + p.norm_offset);
+            kb[j] = kb[j] * inv * (p.k_norm_w[ib[j]] + p.norm_offset);
         }
     }
     __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(staging);

@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 5
+#define UAA_ABI_VERSION 6
 
 typedef enum {
     UAA_OK = 0,
@@ -82,7 +82,8 @@ typedef enum { UAA_ROPE_NEOX = 0, UAA_ROPE_INTERLEAVED = 1 } uaa_rope_style;
 typedef enum {
     UAA_ROPE_SCALING_NONE = 0,
     UAA_ROPE_SCALING_LLAMA3 = 1,
-    UAA_ROPE_SCALING_YARN = 2
+    UAA_ROPE_SCALING_YARN = 2,
+    UAA_ROPE_SCALING_LINEAR = 3
 } uaa_rope_scaling;
 typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2 } uaa_dtype;
 
@@ -93,14 +94,24 @@ typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2 } uaa_dt
                                        scheduling state was left by such a launch; outputs are
                                        invalid until the workspace is zeroed again */
 
-/* Rotary embedding. Pair p of a head row is (p, p + D/2) for NEOX and (2p, 2p+1)
- * for INTERLEAVED; theta_p = theta^(-2p/D), rotated by angle pos * theta'_p.
+/* Rotary embedding of the first R = rotary_dim dims of each head row (R = D when
+ * the descriptor's rotary_dim is 0; the other D - R dims pass unchanged: the
+ * partial rotary of the decoder-completeness page, P1.5). Pair p < R/2 is
+ * (p, p + R/2) for NEOX and (2p, 2p+1) for INTERLEAVED; theta_p = theta^(-2p/R),
+ * rotated by angle pos * theta'_p.
  * LLAMA3: Llama-3.1 wavelength interpolation (factor, low_freq_factor,
  *   high_freq_factor, original_max_pos).
+ * LINEAR: theta'_p = theta_p / factor (positions divided by factor; the global
+ *   layers of the gemma3 lane, support-matrix page, "Structural fact
+ *   requirements").
  * YARN: ramp over the pair index between the pairs whose wavelength fits
  *   beta_fast and beta_slow times into original_max_pos (not rounded); theta'
  *   blends theta / factor and theta; cos and sin are multiplied by attn_factor
- *   (<= 0 selects 0.1 ln(factor) + 1). */
+ *   (<= 0 selects 0.1 ln(factor) + 1).
+ * The descriptor is per layer: a model whose layers differ in rotary base,
+ *   scaling or window (Gemma 3's local layers with a sliding window and a
+ *   second base, its global layers with linear scaling: llamay "Architectures")
+ *   passes each layer its own. */
 typedef struct {
     int32_t style;            /* uaa_rope_style */
     double theta;             /* base, > 0 */
@@ -128,6 +139,9 @@ typedef struct {
     int32_t kv_dtype;         /* UAA_DTYPE_F32, _BF16 or _VQ8 */
     int32_t io_dtype;         /* q, k_new, v_new: UAA_DTYPE_F32 or _BF16 */
     int32_t out_dtype;        /* out: UAA_DTYPE_F32 or _BF16 */
+    int32_t rotary_dim;       /* rotated dims per head: 0 (all D), or even, 2 <= R <= D */
+    int32_t norm_offset;      /* 1: the QK RMSNorm weight applies as (1 + w) (Gemma's
+                                 stored delta, decoder-completeness page P1.1); else 0 */
 } uaa_attn_desc;
 
 typedef struct {

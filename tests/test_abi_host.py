@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 5
+    assert B.uaa_abi_version() == 6
 
 
 def good_desc(**kw):
@@ -72,6 +72,10 @@ WS = B.UaaWorkspace(0x20000, 1 << 30)
     (dict(rope_theta=0.0), B.UAA_ERR_UNSUPPORTED, "rope.theta=0"),
     (dict(rope_scaling="llama3", factor=0.5), B.UAA_ERR_UNSUPPORTED, "llama3"),
     (dict(rope_scaling="yarn", beta_fast=1.0, beta_slow=32.0), B.UAA_ERR_UNSUPPORTED, "yarn"),
+    (dict(rope_scaling="linear", factor=0.0), B.UAA_ERR_UNSUPPORTED, "linear"),
+    (dict(rotary_dim=31), B.UAA_ERR_UNSUPPORTED, "rotary_dim=31"),
+    (dict(rotary_dim=130), B.UAA_ERR_UNSUPPORTED, "rotary_dim=130"),
+    (dict(rotary_dim=-2), B.UAA_ERR_UNSUPPORTED, "rotary_dim=-2"),
 ])
 def test_descriptor_refusals_name_the_fact(L, kw, status, fact):
     st = B.uaa_decode_attn(good_desc(**kw), fake_args(), WS, None, check=False)
@@ -84,6 +88,10 @@ def test_enum_refusals(L):
     d.kv_dtype = 7
     assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
     assert "kv_dtype=7" in B.last_error()
+    d = good_desc()
+    d.norm_offset = 2
+    assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert "norm_offset=2" in B.last_error()
     d = good_desc()
     d.rope.scaling = 9
     assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
@@ -181,8 +189,9 @@ def test_struct_sizes_match_the_header(L, tmp_path):
     src = tmp_path / "probe.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "uaa.h"\n'
-        'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(uaa_attn_desc), sizeof(uaa_step_args),'
+        'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(uaa_attn_desc), sizeof(uaa_step_args),'
         ' sizeof(uaa_workspace), sizeof(uaa_workspace_layout), offsetof(uaa_attn_desc, out_dtype),'
+        ' offsetof(uaa_attn_desc, norm_offset),'
         ' offsetof(uaa_step_args, q_rot), offsetof(uaa_workspace_layout, total_bytes)); return 0;}\n')
     exe = tmp_path / "probe"
     r = subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src),
@@ -191,6 +200,7 @@ def test_struct_sizes_match_the_header(L, tmp_path):
         pytest.skip("no C compiler / CUDA headers for the probe: " + r.stderr[:200])
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     want = [ctypes.sizeof(B.UaaAttnDesc), ctypes.sizeof(B.UaaStepArgs), ctypes.sizeof(B.UaaWorkspace),
-            ctypes.sizeof(B.UaaWorkspaceLayout), B.UaaAttnDesc.out_dtype.offset, B.UaaStepArgs.q_rot.offset,
+            ctypes.sizeof(B.UaaWorkspaceLayout), B.UaaAttnDesc.out_dtype.offset, B.UaaAttnDesc.norm_offset.offset,
+            B.UaaStepArgs.q_rot.offset,
             B.UaaWorkspaceLayout.total_bytes.offset]
     assert got == want

@@ -121,7 +121,7 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
     return worst
 
 
-# ------------------------------------------------------------------ the five workloads, small
+# ------------------------------------------------------------------ the workloads, small
 
 SMALL = {
     "llama32_1b_tiny": dict(lens=[256]),
@@ -129,6 +129,7 @@ SMALL = {
     "qwen3_8b_ragged": dict(overrides=dict(batch=5, seq_len=(1, 2100)), lens=[1, 64, 129, 2000, 777]),
     "gemma2_9b_swa": dict(overrides=dict(batch=2, seq_len=5000), lens=[3000, 4999]),
     "gptoss_vq8_sink": dict(overrides=dict(batch=3, seq_len=4096), lens=[100, 1000, 4095]),
+    "gemma3_12b_local_global": dict(overrides=dict(batch=3, seq_len=(1, 3000)), lens=[2999, 1023, 5]),
 }
 
 
@@ -166,6 +167,18 @@ EDGE = [
                                             layers=[dict(window=50)]), [299, 5]),
     ("yarn-qknorm-interleaved", "gptoss_vq8_sink", dict(batch=2, qk_norm=True, norm_w_range=(0.5, 1.5),
                                                        rope_style="interleaved", seq_len=300), [299, 5]),
+    # partial rotary (rotary_dim < head_dim), the (1 + w) norm weight, linear scaling
+    ("rotary96-of-128-qknorm", "qwen3_8b_ragged", dict(batch=2, seq_len=300, rotary_dim=96), [299, 5]),
+    ("rotary16-of-64-interleaved", "llama32_1b_tiny", dict(batch=2, seq_len=300, rotary_dim=16,
+                                                           io_dtype="bf16", kv_dtype="bf16"), [299, 5]),
+    ("rotary32-of-64-yarn-vq8", "gptoss_vq8_sink", dict(batch=2, seq_len=300, rotary_dim=32), [299, 5]),
+    ("f32-rotary48-norm-offset", "llama32_1b_tiny", dict(batch=2, seq_len=300, rotary_dim=48, qk_norm=True,
+                                                         norm_offset=True, norm_w_range=(-0.5, 0.5)), [299, 5]),
+    ("d256-rotary64-linear", "gemma3_12b_local_global", dict(batch=2, seq_len=600, rotary_dim=64, layers=None),
+     [599, 10]),
+    ("d64-vq8-norm-offset-local", "gemma3_12b_local_global",
+     dict(batch=2, seq_len=600, head_dim=64, kv_dtype="vq8", layers=[dict(window=100, rope_theta=10000.0,
+                                                                          rope_scaling="none")]), [599, 40]),
 ]
 
 
@@ -384,7 +397,8 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry
 
 # ------------------------------------------------------------------ full size, sampled
 
-FULL = ["llama32_1b_tiny", "llama31_8b_decode", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink"]
+FULL = ["llama32_1b_tiny", "llama31_8b_decode", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink",
+        "gemma3_12b_local_global"]
 
 
 @pytest.mark.slow
