@@ -162,13 +162,14 @@ def sinks(cfg: dict):
 
 def cache_slice(cfg: dict, b: int, g: int, n: int, which: str) -> torch.Tensor:
     """Rows [0, n) of cache slice (b, g): k in the key storage dtype (f32 / bf16);
-    v in f32 / bf16, or as fp32 values for a vq8 cache (each side quantises them)."""
+    v in f32 / bf16, or as fp32 values for a vq8 cache (each side quantises them);
+    a q8 cache has both k and v as fp32 values."""
     D, Hkv = cfg["head_dim"], cfg["n_kv_heads"]
     idx = b * Hkv + g
     x = torch.randn((n, D), generator=_gen(cfg["seed"], which, idx, cfg.get("layer", 0)),
                     dtype=torch.float32)
     kv = cfg.get("kv_dtype", "bf16")
-    if kv == "f32":
+    if kv in ("f32", "q8"):
         return x
     if which == "k_cache" or kv == "bf16":
         return x.to(torch.bfloat16)
@@ -178,11 +179,12 @@ def cache_slice(cfg: dict, b: int, g: int, n: int, which: str) -> torch.Tensor:
 def cache(cfg: dict, cap: int, lens: torch.Tensor, fill_unused: str = "zero") -> dict:
     """Host caches [B][Hkv][cap][D] with rows [0, lens[b]) drawn; unused rows are
     zero or NaN (fill_unused='nan', to prove they are never read into a result).
-    For vq8 'v_values' holds fp32 values; each side quantises them itself."""
+    For vq8 'v_values' holds fp32 values, for q8 'k_values' too; each side
+    quantises them itself."""
     B, Hkv, D = cfg["batch"], cfg["n_kv_heads"], cfg["head_dim"]
     kv = cfg.get("kv_dtype", "bf16")
-    kdt = torch.float32 if kv == "f32" else torch.bfloat16
-    vdt = torch.float32 if kv in ("f32", "vq8") else torch.bfloat16
+    kdt = torch.float32 if kv in ("f32", "q8") else torch.bfloat16
+    vdt = torch.float32 if kv in ("f32", "vq8", "q8") else torch.bfloat16
     fill = float("nan") if fill_unused == "nan" else 0.0
     k = torch.full((B, Hkv, cap, D), fill, dtype=kdt)
     v = torch.full((B, Hkv, cap, D), fill, dtype=vdt)
@@ -191,8 +193,9 @@ def cache(cfg: dict, cap: int, lens: torch.Tensor, fill_unused: str = "zero") ->
         for g in range(Hkv):
             k[b, g, :n] = cache_slice(cfg, b, g, n, "k_cache")
             v[b, g, :n] = cache_slice(cfg, b, g, n, "v_cache")
-    key = "v_values" if kv == "vq8" else "v_cache"
-    return {"k_cache": k, key: v}
+    kkey = "k_values" if kv == "q8" else "k_cache"
+    vkey = "v_values" if kv in ("vq8", "q8") else "v_cache"
+    return {kkey: k, vkey: v}
 
 
 # ---------------------------------------------------------------- numpy views

@@ -201,10 +201,13 @@ static double load_io(const void* base, int dtype, size_t i)
                                : oracle_bf16_to_double(((const uint16_t*)base)[i]);
 }
 
-static double load_key(const void* rows, int kv_dtype, size_t i)
+/* Key j, element dd: stored as given (f32, bf16), or code times the row's scale (q8). */
+static double load_key(const void* rows, const float* scale_rows, int kv_dtype, size_t j, int D, int dd)
 {
-    return kv_dtype == ORACLE_F32 ? (double)((const float*)rows)[i]
-                                  : oracle_bf16_to_double(((const uint16_t*)rows)[i]);
+    const size_t i = j * (size_t)D + (size_t)dd;
+    if (kv_dtype == ORACLE_F32) return (double)((const float*)rows)[i];
+    if (kv_dtype == ORACLE_Q8) return (double)((const int8_t*)rows)[i] * (double)scale_rows[j];
+    return oracle_bf16_to_double(((const uint16_t*)rows)[i]);
 }
 
 static double load_value(const void* rows, const float* scale_rows, int kv_dtype, size_t j,
@@ -238,7 +241,7 @@ static void norm_and_rotate(const oracle_desc* d, const double* inv_freq, double
 
 int oracle_append(const oracle_desc* d, int B, const void* q, const void* k_new,
                   const void* v_new, const float* q_norm_w, const float* k_norm_w,
-                  void* k_cache, void* v_cache, float* v_scale, int cap,
+                  void* k_cache, void* v_cache, float* v_scale, float* k_scale, int cap,
                   int32_t* seq_lens, double* q_rot)
 {
     const int D = d->head_dim, Hq = d->n_q_heads, Hkv = d->n_kv_heads;
@@ -259,7 +262,14 @@ int oracle_append(const oracle_desc* d, int B, const void* q, const void* k_new,
             const size_t slot = (((size_t)b * Hkv + g) * (size_t)cap + (size_t)pos) * (size_t)D;
             for (int i = 0; i < D; ++i) x[i] = load_io(k_new, d->io_dtype, in + (size_t)i);
             norm_and_rotate(d, inv_freq, mscale, pos, k_norm_w, x, tmp);
-            for (int i = 0; i < D; ++i) {
+            if (d->kv_dtype == ORACLE_Q8) {
+                /* q8: the rotated key rounded to fp32, then the vq8 rule (llamay "The
+                 * KV cache, in three precisions": q8 quantises keys and values) */
+                for (int i = 0; i < D; ++i) vrow[i] = (float)x[i];
+                oracle_vq8_quantize_row(vrow, D, (int8_t*)k_cache + slot,
+                                        &k_scale[((size_t)b * Hkv + g) * (size_t)cap + (size_t)pos]);
+            }
+            for (int i = 0; i < D && d->kv_dtype != ORACLE_Q8; ++i) {
                 if (d->kv_dtype == ORACLE_F32)
                     ((float*)k_cache)[slot + (size_t)i] = (float)x[i];
                 else
@@ -306,7 +316,7 @@ int oracle_append(const oracle_desc* d, int B, const void* q, const void* k_new,
  */
 void oracle_attend_range(const oracle_desc* d, const double* q_row,
                          const void* k_rows, const void* v_rows, const float* scale_rows,
-                         long j_lo, long j_hi, int has_sink, double sink,
+                         const float* k_scale_rows, long j_lo, long j_hi, int has_sink, double sink,
                          double* o, double* lse)
 {
     const int D = d->head_dim;
@@ -318,7 +328,7 @@ void oracle_attend_range(const oracle_desc* d, const double* q_row,
         const long j = j_lo + t;
         double dot = 0.0;
         for (int i = 0; i < D; ++i)
-            dot += q_row[i] * load_key(k_rows, d->kv_dtype, (size_t)j * (size_t)D + (size_t)i);
+            dot += q_row[i] * load_key(k_rows, k_scale_rows, d->kv_dtype, (size_t)j, D, i);
         double st = scale * dot;
         if (d->softcap > 0.0) st = d->softcap * tanh(st / d->softcap);
         s[t] = st;
@@ -348,6 +358,7 @@ typedef struct {
     const void* k_cache;
     const void* v_cache;
     const float* v_scale;
+    const float* k_scale;
     int cap;
     const int32_t* seq_lens;
     const int32_t* units;
@@ -372,17 +383,19 @@ static void attend_unit(const attend_job* job, int u)
     if (d->window > 0 && n - d->window > 0) lo = n - d->window;
     const size_t head = (size_t)b * Hkv + (size_t)g;
     const size_t row0 = head * (size_t)job->cap * (size_t)D;
-    const void* k_rows = d->kv_dtype == ORACLE_F32
-                             ? (const void*)((const float*)job->k_cache + row0)
-                             : (const void*)((const uint16_t*)job->k_cache + row0);
+    const void* k_rows = d->kv_dtype == ORACLE_F32  ? (const void*)((const float*)job->k_cache + row0)
+                         : d->kv_dtype == ORACLE_Q8 ? (const void*)((const int8_t*)job->k_cache + row0)
+                                                    : (const void*)((const uint16_t*)job->k_cache + row0);
     const void* v_rows;
     if (d->kv_dtype == ORACLE_F32) v_rows = (const float*)job->v_cache + row0;
     else if (d->kv_dtype == ORACLE_BF16) v_rows = (const uint16_t*)job->v_cache + row0;
     else v_rows = (const int8_t*)job->v_cache + row0;
-    const float* scale_rows = d->kv_dtype == ORACLE_VQ8 ? job->v_scale + head * (size_t)job->cap : NULL;
+    const int int8_values = d->kv_dtype == ORACLE_VQ8 || d->kv_dtype == ORACLE_Q8;
+    const float* scale_rows = int8_values ? job->v_scale + head * (size_t)job->cap : NULL;
+    const float* k_scale_rows = d->kv_dtype == ORACLE_Q8 ? job->k_scale + head * (size_t)job->cap : NULL;
     double lse;
     oracle_attend_range(d, job->q_rot + ((size_t)b * Hq + (size_t)h) * (size_t)D, k_rows, v_rows,
-                        scale_rows, lo, n, d->has_sink, d->has_sink ? (double)job->sink[h] : 0.0,
+                        scale_rows, k_scale_rows, lo, n, d->has_sink, d->has_sink ? (double)job->sink[h] : 0.0,
                         job->out + (size_t)u * (size_t)D, &lse);
 }
 
@@ -395,7 +408,7 @@ static void* attend_worker(void* arg)
 
 void oracle_attend(const oracle_desc* d, int B, const double* q_rot, const float* sink,
                    const void* k_cache, const void* v_cache, const float* v_scale,
-                   int cap, const int32_t* seq_lens, const int32_t* units, int n_units,
+                   const float* k_scale, int cap, const int32_t* seq_lens, const int32_t* units, int n_units,
                    double* out, int n_threads)
 {
     if (!units) n_units = B * d->n_q_heads;
@@ -404,7 +417,7 @@ void oracle_attend(const oracle_desc* d, int B, const double* q_rot, const float
     attend_job* jobs = (attend_job*)malloc(sizeof(attend_job) * (size_t)n_threads);
     pthread_t* tids = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
     for (int t = 0; t < n_threads; ++t) {
-        attend_job j = {d, B, q_rot, sink, k_cache, v_cache, v_scale, cap, seq_lens,
+        attend_job j = {d, B, q_rot, sink, k_cache, v_cache, v_scale, k_scale, cap, seq_lens,
                         units, n_units, out, t, n_threads};
         jobs[t] = j;
     }
@@ -418,14 +431,14 @@ void oracle_attend(const oracle_desc* d, int B, const double* q_rot, const float
 int oracle_decode_step(const oracle_desc* d, int B, const void* q, const void* k_new,
                        const void* v_new, const float* q_norm_w, const float* k_norm_w,
                        const float* sink, void* k_cache, void* v_cache, float* v_scale,
-                       int cap, int32_t* seq_lens, double* out, int n_threads)
+                       float* k_scale, int cap, int32_t* seq_lens, double* out, int n_threads)
 {
     double* q_rot = (double*)malloc(sizeof(double) * (size_t)B * (size_t)d->n_q_heads *
                                     (size_t)d->head_dim + 1);
     int rc = oracle_append(d, B, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, v_scale,
-                           cap, seq_lens, q_rot);
+                           k_scale, cap, seq_lens, q_rot);
     if (rc == 0)
-        oracle_attend(d, B, q_rot, sink, k_cache, v_cache, v_scale, cap, seq_lens, NULL, 0, out,
+        oracle_attend(d, B, q_rot, sink, k_cache, v_cache, v_scale, k_scale, cap, seq_lens, NULL, 0, out,
                       n_threads);
     free(q_rot);
     return rc;

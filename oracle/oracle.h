@@ -15,8 +15,9 @@
  *      dims (same page, P0.2, P1.3 and P1.5; llamay "Models and formats",
  *      "Architectures"; FreeToken PR #722, "Changes"; YaRN: Peng et al., 2023;
  *      linear: Model support matrix, "Structural fact requirements");
- *   3. append of k and v at slot seq_len, the cache being fp32, bf16 or "vq8"
- *      (int8 values with one fp32 scale per token and head, keys exact)
+ *   3. append of k and v at slot seq_len, the cache being fp32, bf16, "vq8"
+ *      (int8 values with one fp32 scale per token and head, keys exact) or
+ *      "q8" (keys too: int8 codes of the rotated key with their own scale)
  *      (llamay "Models and formats", "The KV cache, in three precisions");
  *   4. attention of each query head over its kv head's cache (integral GQA
  *      ratio, Model support matrix, "Structural fact requirements"), with an
@@ -26,9 +27,11 @@
  *
  * Layouts (all row-major, caller-owned):
  *   q        [B][Hq][D]    k_new, v_new [B][Hkv][D]      (io_dtype: f32 or bf16)
- *   k_cache  [B][Hkv][cap][D]  (kv_dtype f32 -> float, bf16/vq8 -> uint16 bf16 bits)
- *   v_cache  [B][Hkv][cap][D]  (f32 -> float, bf16 -> uint16, vq8 -> int8 codes)
- *   v_scale  [B][Hkv][cap]     (vq8 only, fp32)
+ *   k_cache  [B][Hkv][cap][D]  (kv_dtype f32 -> float, bf16/vq8 -> uint16 bf16 bits,
+ *                               q8 -> int8 codes)
+ *   v_cache  [B][Hkv][cap][D]  (f32 -> float, bf16 -> uint16, vq8/q8 -> int8 codes)
+ *   v_scale  [B][Hkv][cap]     (vq8 and q8, fp32)
+ *   k_scale  [B][Hkv][cap]     (q8 only, fp32)
  *   seq_lens [B] int32: tokens cached before the step; incremented by the append.
  */
 #ifndef GQA_ORACLE_H
@@ -42,7 +45,7 @@ extern "C" {
 
 enum { ORACLE_ROPE_NEOX = 0, ORACLE_ROPE_INTERLEAVED = 1 };
 enum { ORACLE_SCALING_NONE = 0, ORACLE_SCALING_LLAMA3 = 1, ORACLE_SCALING_YARN = 2, ORACLE_SCALING_LINEAR = 3 };
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_VQ8 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_VQ8 = 2, ORACLE_Q8 = 3 };
 
 typedef struct {
     int n_q_heads;
@@ -64,7 +67,7 @@ typedef struct {
     int window;              /* 0: none; W: the last W positions are visible */
     double softcap;          /* 0: none; c: s -> c tanh(s / c) */
     int has_sink;            /* 1: one sink logit per query head in the denominator */
-    int kv_dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_VQ8 */
+    int kv_dtype;            /* ORACLE_F32 / ORACLE_BF16 / ORACLE_VQ8 / ORACLE_Q8 */
     int io_dtype;            /* ORACLE_F32 / ORACLE_BF16 for q, k_new, v_new */
     int rotary_dim;          /* rotated dims of a head (even, <= head_dim); 0: head_dim */
     int norm_offset;         /* 1: the RMSNorm weight is applied as (1 + w) */
@@ -87,7 +90,8 @@ void oracle_rms_norm(const double* x, const float* w, int n, double eps, double 
 void oracle_rope_rotate(const oracle_desc* d, const double* inv_freq, double mscale,
                         long pos, const double* x, double* y);
 
-/* vq8 storage rule, in fp32 arithmetic: s = max|v| / 127, code = rint(v / s). */
+/* vq8 storage rule, in fp32 arithmetic: s = max|v| / 127, code = rint(v / s).
+ * q8 stores the rotated key row (rounded to fp32) by the same rule. */
 void oracle_vq8_quantize_row(const float* v, int n, int8_t* codes, float* scale);
 
 /* Append step for every sequence. Returns 0, or -1 (nothing written) when some
@@ -95,30 +99,31 @@ void oracle_vq8_quantize_row(const float* v, int n, int8_t* codes, float* scale)
  * in fp64, [B][Hq][D]. */
 int oracle_append(const oracle_desc* d, int B, const void* q, const void* k_new,
                   const void* v_new, const float* q_norm_w, const float* k_norm_w,
-                  void* k_cache, void* v_cache, float* v_scale, int cap,
+                  void* k_cache, void* v_cache, float* v_scale, float* k_scale, int cap,
                   int32_t* seq_lens, double* q_rot);
 
 /* Softmax attention of one query row over keys [j_lo, j_hi) of one kv head.
- * k_rows / v_rows / scale_rows point at slot 0 of that head's cache rows.
+ * k_rows / v_rows / scale_rows (values) / k_scale_rows (q8 keys) point at slot 0
+ * of that head's cache rows.
  * sink: the head's sink logit (included in the denominator) when has_sink.
  * o receives the output row, *lse the natural log of the denominator. */
 void oracle_attend_range(const oracle_desc* d, const double* q_row,
                          const void* k_rows, const void* v_rows, const float* scale_rows,
-                         long j_lo, long j_hi, int has_sink, double sink,
+                         const float* k_scale_rows, long j_lo, long j_hi, int has_sink, double sink,
                          double* o, double* lse);
 
 /* Attention for (b, h) units after the append. units: n_units pairs (b, h),
  * or NULL for every (b, h) in order. out: [n_units][D] (or [B][Hq][D]). */
 void oracle_attend(const oracle_desc* d, int B, const double* q_rot, const float* sink,
                    const void* k_cache, const void* v_cache, const float* v_scale,
-                   int cap, const int32_t* seq_lens, const int32_t* units, int n_units,
+                   const float* k_scale, int cap, const int32_t* seq_lens, const int32_t* units, int n_units,
                    double* out, int n_threads);
 
 /* append + attend for the whole batch. Returns the append's status. */
 int oracle_decode_step(const oracle_desc* d, int B, const void* q, const void* k_new,
                        const void* v_new, const float* q_norm_w, const float* k_norm_w,
                        const float* sink, void* k_cache, void* v_cache, float* v_scale,
-                       int cap, int32_t* seq_lens, double* out, int n_threads);
+                       float* k_scale, int cap, int32_t* seq_lens, double* out, int n_threads);
 
 #ifdef __cplusplus
 }

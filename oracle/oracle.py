@@ -2,7 +2,7 @@
 
 Test infrastructure: only the tests, the smoke check and the benchmark's
 CPU-baseline / reference legs import this module. Arrays are numpy; bf16 data
-travels as uint16 bit patterns, vq8 codes as int8.
+travels as uint16 bit patterns, vq8 / q8 codes as int8.
 
 A step description is a plain dict with the keys
   n_q_heads n_kv_heads head_dim scale rope_style rope_theta rope_scaling factor
@@ -20,7 +20,7 @@ from . import build as _build
 
 _STYLE = {"neox": 0, "interleaved": 1}
 _SCALING = {"none": 0, "llama3": 1, "yarn": 2, "linear": 3}
-_DTYPE = {"f32": 0, "bf16": 1, "vq8": 2}
+_DTYPE = {"f32": 0, "bf16": 1, "vq8": 2, "q8": 3}
 
 
 class OracleDesc(ctypes.Structure):
@@ -85,15 +85,15 @@ def lib():
         L.oracle_rms_norm.argtypes = [dp, fp, ctypes.c_int, ctypes.c_double, ctypes.c_double, dp]
         L.oracle_rope_rotate.argtypes = [P(OracleDesc), dp, ctypes.c_double, ctypes.c_long, dp, dp]
         L.oracle_vq8_quantize_row.argtypes = [fp, ctypes.c_int, P(ctypes.c_int8), fp]
-        L.oracle_append.argtypes = [P(OracleDesc), ctypes.c_int, vp, vp, vp, fp, fp, vp, vp, fp,
+        L.oracle_append.argtypes = [P(OracleDesc), ctypes.c_int, vp, vp, vp, fp, fp, vp, vp, fp, fp,
                                     ctypes.c_int, ip, dp]
         L.oracle_append.restype = ctypes.c_int
-        L.oracle_attend_range.argtypes = [P(OracleDesc), dp, vp, vp, fp, ctypes.c_long,
+        L.oracle_attend_range.argtypes = [P(OracleDesc), dp, vp, vp, fp, fp, ctypes.c_long,
                                           ctypes.c_long, ctypes.c_int, ctypes.c_double, dp, dp]
-        L.oracle_attend.argtypes = [P(OracleDesc), ctypes.c_int, dp, fp, vp, vp, fp, ctypes.c_int,
+        L.oracle_attend.argtypes = [P(OracleDesc), ctypes.c_int, dp, fp, vp, vp, fp, fp, ctypes.c_int,
                                     ip, ip, ctypes.c_int, dp, ctypes.c_int]
         L.oracle_decode_step.argtypes = [P(OracleDesc), ctypes.c_int, vp, vp, vp, fp, fp, fp, vp,
-                                         vp, fp, ctypes.c_int, ip, dp, ctypes.c_int]
+                                         vp, fp, fp, ctypes.c_int, ip, dp, ctypes.c_int]
         L.oracle_decode_step.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -185,8 +185,8 @@ def vq8_quantize(v: np.ndarray):
 # ---------------------------------------------------------------- the step
 
 def append(cfg: dict, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, v_scale,
-           seq_lens) -> np.ndarray:
-    """Append in place (caches and seq_lens mutate). Returns q_rot fp64 [B][Hq][D]."""
+           seq_lens, k_scale=None) -> np.ndarray:
+    """Append in place (caches, scales and seq_lens mutate). Returns q_rot fp64 [B][Hq][D]."""
     d = make_desc(cfg)
     io = cfg.get("io_dtype", "bf16")
     q, k_new, v_new = (_io_array(a, io) for a in (q, k_new, v_new))
@@ -201,6 +201,7 @@ def append(cfg: dict, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, v_s
     rc = lib().oracle_append(ctypes.byref(d), B, _ptr(q), _ptr(k_new), _ptr(v_new),
                              _ptr(w_q, ctypes.c_float), _ptr(w_k, ctypes.c_float),
                              _ptr(k_cache), _ptr(v_cache), _ptr(v_scale, ctypes.c_float),
+                             _ptr(k_scale, ctypes.c_float),
                              cap, _ptr(seq_lens, ctypes.c_int32), _ptr(q_rot, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle append refused: a sequence is at capacity")
@@ -208,7 +209,7 @@ def append(cfg: dict, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, v_s
 
 
 def attend(cfg: dict, q_rot, sink, k_cache, v_cache, v_scale, seq_lens, units=None,
-           n_threads=None) -> np.ndarray:
+           n_threads=None, k_scale=None) -> np.ndarray:
     """Attention after the append. units: None (all, -> [B][Hq][D]) or list of (b, h)."""
     d = make_desc(cfg)
     q_rot = np.ascontiguousarray(q_rot, dtype=np.float64)
@@ -226,13 +227,14 @@ def attend(cfg: dict, q_rot, sink, k_cache, v_cache, v_scale, seq_lens, units=No
         out = np.zeros((n_units, d.head_dim), dtype=np.float64)
     lib().oracle_attend(ctypes.byref(d), B, _ptr(q_rot, ctypes.c_double),
                         _ptr(sink_a, ctypes.c_float), _ptr(k_cache), _ptr(v_cache),
-                        _ptr(v_scale, ctypes.c_float), cap, _ptr(seq_lens, ctypes.c_int32),
+                        _ptr(v_scale, ctypes.c_float), _ptr(k_scale, ctypes.c_float), cap,
+                        _ptr(seq_lens, ctypes.c_int32),
                         _ptr(u_arr, ctypes.c_int32), n_units, _ptr(out, ctypes.c_double),
                         int(n_threads or default_threads()))
     return out
 
 
-def attend_range(cfg: dict, q_row, k_rows, v_rows, scale_rows, j_lo, j_hi, sink=None):
+def attend_range(cfg: dict, q_row, k_rows, v_rows, scale_rows, j_lo, j_hi, sink=None, k_scale_rows=None):
     """One query row over keys [j_lo, j_hi) of one kv head's rows. -> (o, natural lse)."""
     d = make_desc(cfg)
     q_row = np.ascontiguousarray(q_row, dtype=np.float64)
@@ -243,6 +245,8 @@ def attend_range(cfg: dict, q_row, k_rows, v_rows, scale_rows, j_lo, j_hi, sink=
                               _ptr(np.ascontiguousarray(v_rows)),
                               _ptr(None if scale_rows is None else np.ascontiguousarray(scale_rows),
                                    ctypes.c_float),
+                              _ptr(None if k_scale_rows is None else np.ascontiguousarray(k_scale_rows),
+                                   ctypes.c_float),
                               int(j_lo), int(j_hi), int(sink is not None),
                               float(sink if sink is not None else 0.0), _ptr(o, ctypes.c_double),
                               ctypes.byref(lse))
@@ -250,7 +254,7 @@ def attend_range(cfg: dict, q_row, k_rows, v_rows, scale_rows, j_lo, j_hi, sink=
 
 
 def decode_step(cfg: dict, q, k_new, v_new, q_norm_w, k_norm_w, sink, k_cache, v_cache,
-                v_scale, seq_lens, n_threads=None) -> np.ndarray:
+                v_scale, seq_lens, n_threads=None, k_scale=None) -> np.ndarray:
     """append + attend over the whole batch; caches and seq_lens mutate in place."""
-    q_rot = append(cfg, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, v_scale, seq_lens)
-    return attend(cfg, q_rot, sink, k_cache, v_cache, v_scale, seq_lens, None, n_threads)
+    q_rot = append(cfg, q, k_new, v_new, q_norm_w, k_norm_w, k_cache, v_cache, v_scale, seq_lens, k_scale)
+    return attend(cfg, q_rot, sink, k_cache, v_cache, v_scale, seq_lens, None, n_threads, k_scale)

@@ -58,7 +58,7 @@ def vq8_numpy(v: np.ndarray):
 
 
 def decode_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, v_scale, seq_lens,
-                q_norm_w=None, k_norm_w=None, sink=None, inv_freq=None, mscale=1.0):
+                q_norm_w=None, k_norm_w=None, sink=None, inv_freq=None, mscale=1.0, k_scale=None):
     """All arrays fp64 (values, codes as float, scales as float). Caches mutate.
     Returns out [B][Hq][D]."""
     B, Hq, D = q.shape
@@ -89,6 +89,13 @@ def decode_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, v_scale, seq_lens,
         elif kv == "f32":
             kr = kr.astype(np.float32).astype(np.float64)
             vb = v_new[b].astype(np.float32).astype(np.float64)
+        elif kv == "q8":
+            kcodes, ks = vq8_numpy(kr.astype(np.float32))
+            k_scale[b, :, pos] = ks
+            kr = kcodes.astype(np.float64)
+            codes, s = vq8_numpy(v_new[b].astype(np.float32))
+            v_scale[b, :, pos] = s
+            vb = codes.astype(np.float64)
         else:
             kr = bf16_round(kr)
             codes, s = vq8_numpy(v_new[b].astype(np.float32))
@@ -101,8 +108,10 @@ def decode_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, v_scale, seq_lens,
         lo = max(0, n - W) if W > 0 else 0
         K = np.repeat(k_cache[b, :, lo:n], G, axis=0)          # [Hq][n'][D]
         V = np.repeat(v_cache[b, :, lo:n], G, axis=0)
-        if kv == "vq8":
+        if kv in ("vq8", "q8"):
             V = V * np.repeat(v_scale[b, :, lo:n], G, axis=0)[..., None]
+        if kv == "q8":
+            K = K * np.repeat(k_scale[b, :, lo:n], G, axis=0)[..., None]
         S = scale * np.einsum("hd,hjd->hj", qr, K)
         if cap_ > 0:
             S = cap_ * np.tanh(S / cap_)

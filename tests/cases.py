@@ -1,8 +1,8 @@
 """Test cases built from the seeded workload generators.
 
 `host_case` draws one step's inputs and a cache; `oracle_arrays` turns them into
-the storage arrays the oracle takes (a vq8 cache quantised by the oracle's own
-quantiser). Nothing here computes any part of the method.
+the storage arrays the oracle takes (a vq8 or q8 cache quantised by the oracle's
+own quantiser). Nothing here computes any part of the method.
 """
 import numpy as np
 import torch
@@ -27,13 +27,17 @@ def oracle_arrays(case: dict, oracle_mod) -> dict:
     a = dict(
         q=W.bits(case["q"]).copy(), k_new=W.bits(case["k_new"]).copy(),
         v_new=W.bits(case["v_new"]).copy(),
-        k_cache=W.bits(case["k_cache"]).copy(),
         seq_lens=case["lens"].numpy().astype(np.int32).copy(),
         q_norm_w=None if case["q_norm_w"] is None else case["q_norm_w"].numpy().copy(),
         k_norm_w=None if case["k_norm_w"] is None else case["k_norm_w"].numpy().copy(),
         sink=None if case["sink"] is None else case["sink"].numpy().copy(),
     )
-    if cfg.get("kv_dtype") == "vq8":
+    kv = cfg.get("kv_dtype")
+    if kv == "q8":
+        a["k_cache"], a["k_scale"] = oracle_mod.vq8_quantize(case["k_values"].numpy())
+    else:
+        a["k_cache"], a["k_scale"] = W.bits(case["k_cache"]).copy(), None
+    if kv in ("vq8", "q8"):
         codes, scales = oracle_mod.vq8_quantize(case["v_values"].numpy())
         a["v_cache"], a["v_scale"] = codes, scales
     else:
@@ -45,18 +49,19 @@ def run_oracle_step(case: dict, oracle_mod, n_threads=None):
     a = oracle_arrays(case, oracle_mod)
     out = oracle_mod.decode_step(case["cfg"], a["q"], a["k_new"], a["v_new"], a["q_norm_w"],
                                  a["k_norm_w"], a["sink"], a["k_cache"], a["v_cache"],
-                                 a["v_scale"], a["seq_lens"], n_threads=n_threads)
+                                 a["v_scale"], a["seq_lens"], n_threads=n_threads, k_scale=a["k_scale"])
     return out, a
 
 
 # ---------------------------------------------------------------- GPU side
 
 def gpu_layer(case: dict, device="cuda"):
-    """A DecodeLayer holding the case's cache (a vq8 cache is quantised on the device)."""
+    """A DecodeLayer holding the case's cache (a vq8 / q8 cache is quantised on the device)."""
     from gqa_attention_kv_qk_gb300.layer import DecodeLayer
     cfg = case["cfg"]
     layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device)
-    v = case["v_values"] if cfg.get("kv_dtype") == "vq8" else case["v_cache"]
-    layer.load_cache(case["k_cache"], v, case["lens"])
+    k = case["k_values"] if cfg.get("kv_dtype") == "q8" else case["k_cache"]
+    v = case["v_values"] if cfg.get("kv_dtype") in ("vq8", "q8") else case["v_cache"]
+    layer.load_cache(k, v, case["lens"])
     layer.set_params(case["q_norm_w"], case["k_norm_w"], case["sink"])
     return layer

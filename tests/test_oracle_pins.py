@@ -441,6 +441,30 @@ def test_split_merge_equals_full_softmax(oracle_mod):
         assert M + math.log(sum(wts)) == pytest.approx(lse_full, rel=1e-13)
 
 
+def test_q8_on_representable_rows_is_the_exact_cache(oracle_mod):
+    """llamay "The KV cache, in three precisions": q8 stores keys and values as
+    int8 codes with a scale per row. Rows that are integers times 2^-6 with a
+    largest magnitude of 127 quantise exactly, so attention over a q8 cache of
+    them equals attention over the same rows kept in fp32, bit for bit."""
+    rng = np.random.default_rng(12)
+    D, n = 64, 90
+    ck = rng.integers(-127, 128, (n, D)); ck[:, 0] = 127
+    cv = rng.integers(-127, 128, (n, D)); cv[:, 5] = -127
+    k = (ck * 2.0 ** -6).astype(np.float32)
+    v = (cv * 2.0 ** -6).astype(np.float32)
+    kq, ks = oracle_mod.vq8_quantize(k)
+    vq, vs = oracle_mod.vq8_quantize(v)
+    assert np.array_equal(kq, ck.astype(np.int8)) and np.all(ks == np.float32(2.0 ** -6))
+    q = rng.standard_normal(D)
+    for extra in (dict(), dict(softcap=2.0), dict(window=0, has_sink=True)):
+        c8 = rope_cfg(head_dim=D, kv_dtype="q8", **extra)
+        c32 = rope_cfg(head_dim=D, kv_dtype="f32", **extra)
+        sink = 0.3 if extra.get("has_sink") else None
+        o8, l8 = oracle_mod.attend_range(c8, q, kq, vq, vs, 3, n, sink=sink, k_scale_rows=ks)
+        o32, l32 = oracle_mod.attend_range(c32, q, k, v, None, 3, n, sink=sink)
+        assert np.array_equal(o8, o32) and l8 == l32
+
+
 # ------------------------------------------------------------------ brute force
 
 GRID = [
@@ -456,6 +480,10 @@ GRID = [
     dict(name="llama32_1b_tiny", n_q_heads=8, n_kv_heads=2, head_dim=64, rotary_dim=16),
     dict(name="gptoss_vq8_sink", n_q_heads=8, n_kv_heads=2, head_dim=64, rotary_dim=32),
     dict(name="gemma3_12b_local_global", n_q_heads=4, n_kv_heads=2, head_dim=64, layers=None),
+    dict(name="llama31_8b_decode", n_q_heads=8, n_kv_heads=2, head_dim=128, kv_dtype="q8"),
+    dict(name="gptoss_vq8_sink", n_q_heads=8, n_kv_heads=2, head_dim=64, kv_dtype="q8", window=11),
+    dict(name="qwen3_8b_ragged", n_q_heads=4, n_kv_heads=4, head_dim=64, kv_dtype="q8", io_dtype="f32",
+         softcap=3.0),
     dict(name="gemma3_12b_local_global", n_q_heads=4, n_kv_heads=2, head_dim=64,
          layers=[dict(window=9, rope_theta=10000.0, rope_scaling="none")]),
 ]
@@ -471,10 +499,14 @@ def test_whole_step_matches_bruteforce(oracle_mod, spec):
     out, a = run_oracle_step(case, oracle_mod)
     # brute force on fp64 copies of the same stored inputs
     f64 = lambda t: t.to(torch.float64).numpy().copy()
-    B, Hkv, cap, D = case["k_cache"].shape
-    kc, vc = f64(case["k_cache"]), None
-    vs = None
-    if cfg["kv_dtype"] == "vq8":
+    kv = cfg["kv_dtype"]
+    vs = ks = None
+    if kv == "q8":
+        codes, s = BF.vq8_numpy(case["k_values"].numpy())
+        kc, ks = codes.astype(np.float64), s.astype(np.float64)
+    else:
+        kc = f64(case["k_cache"])
+    if kv in ("vq8", "q8"):
         codes, s = BF.vq8_numpy(case["v_values"].numpy())
         vc, vs = codes.astype(np.float64), s.astype(np.float64)
     else:
@@ -486,11 +518,15 @@ def test_whole_step_matches_bruteforce(oracle_mod, spec):
     ref = BF.decode_step(cfg, f64(case["q"]), f64(case["k_new"]), f64(case["v_new"]), kc, vc, vs,
                          lens, None if case["q_norm_w"] is None else case["q_norm_w"].numpy(),
                          None if case["k_norm_w"] is None else case["k_norm_w"].numpy(),
-                         None if case["sink"] is None else case["sink"].numpy(), inv, ms)
+                         None if case["sink"] is None else case["sink"].numpy(), inv, ms, ks)
     assert np.array_equal(lens, a["seq_lens"])
     assert np.allclose(out, ref, rtol=1e-9, atol=1e-11)
-    if cfg["kv_dtype"] == "vq8":
+    if kv in ("vq8", "q8"):
         assert np.array_equal(a["v_cache"], vc.astype(np.int8))
+        assert np.array_equal(a["v_scale"], vs.astype(np.float32))
+    if kv == "q8":  # the appended keys' codes and scales: the vq8 rule on the rotated key
+        assert np.array_equal(a["k_cache"], kc.astype(np.int8))
+        assert np.array_equal(a["k_scale"], ks.astype(np.float32))
 
 
 def test_interleaved_step_equals_permuted_neox_step(oracle_mod):
