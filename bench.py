@@ -14,7 +14,7 @@ value       = algorithmic bytes of all timed steps / device time (CUDA events)
 e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each with
               the step's q/k/v copied from pinned host memory and out copied back
               (double-buffered, copies on a second stream overlapping the kernels)
-roofline    = the split-K partial kernel alone (for bf16 / vq8 caches the kernel
+roofline    = the split-K partial kernel alone (for bf16 / vq8 / q8 caches the kernel
               that also performs the append): its algorithmic bytes (visible KV
               rows) / its mean launch duration, against the measured HBM copy peak
 cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample
@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 from gqa_attention_kv_qk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (% of GB300 peak) and decode steps/sec at 1 GPU"
-DECODES_PER_STEP = {"llama31_8b_decode": 64}
+DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64}
 
 
 def measured_peaks() -> dict:
@@ -80,6 +80,8 @@ def _kv_row_bytes(cfg: dict) -> tuple[int, int]:
         return 4 * D, 4 * D
     if kv == "bf16":
         return 2 * D, 2 * D
+    if kv == "q8":
+        return D + 4, D + 4  # int8 key and value rows, each with its fp32 scale
     return 2 * D, D + 4  # vq8: bf16 key row; int8 value row + fp32 scale
 
 
@@ -223,7 +225,8 @@ def oracle_sample(cfg: dict, case: dict, budget_s: float, n_threads: int) -> dic
         t = time.perf_counter()
         O.decode_step(cfg, a["q"][:nb].copy(), a["k_new"][:nb].copy(), a["v_new"][:nb].copy(), a["q_norm_w"],
                       a["k_norm_w"], a["sink"], a["k_cache"][:nb], a["v_cache"][:nb],
-                      None if a["v_scale"] is None else a["v_scale"][:nb], sl, n_threads=n_threads)
+                      None if a["v_scale"] is None else a["v_scale"][:nb], sl, n_threads=n_threads,
+                      k_scale=None if a["k_scale"] is None else a["k_scale"][:nb])
         return time.perf_counter() - t
 
     t1 = run(1)
@@ -440,7 +443,7 @@ def run_uaa(args, world, rank, local) -> dict | None:
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["kv_dtype"] != "f32" else "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"f32": "f32", "q8": "f16"}.get(cfg["kv_dtype"], "bf16"),
         "data": "synthetic (seeded N(0,1) cache and inputs)",
         "decode_steps_per_s": round(decodes / dev_s / world, 2),
         "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),

@@ -24,7 +24,7 @@ UAA_DEVFLAG_TIMEOUT = 0x4
 
 ROPE_STYLE = {"neox": 0, "interleaved": 1}
 ROPE_SCALING = {"none": 0, "llama3": 1, "yarn": 2, "linear": 3}
-DTYPE = {"f32": 0, "bf16": 1, "vq8": 2}
+DTYPE = {"f32": 0, "bf16": 1, "vq8": 2, "q8": 3}
 
 
 class UaaRopeParams(ctypes.Structure):
@@ -52,7 +52,7 @@ class UaaStepArgs(ctypes.Structure):
                 ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("cache_capacity", ctypes.c_int32),
                 ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
-                ("out", ctypes.c_void_p), ("q_rot", ctypes.c_void_p)]
+                ("out", ctypes.c_void_p), ("q_rot", ctypes.c_void_p), ("k_scale", ctypes.c_void_p)]
 
 
 class UaaWorkspace(ctypes.Structure):

@@ -92,8 +92,9 @@ uaa_status check_desc(const uaa_attn_desc* d)
         return fail(UAA_ERR_UNSUPPORTED, "softcap=%g is not a finite value >= 0", (double)d->softcap);
     if (d->has_sink != 0 && d->has_sink != 1)
         return fail(UAA_ERR_UNSUPPORTED, "has_sink=%d is not 0 or 1", d->has_sink);
-    if (d->kv_dtype != UAA_DTYPE_F32 && d->kv_dtype != UAA_DTYPE_BF16 && d->kv_dtype != UAA_DTYPE_VQ8)
-        return fail(UAA_ERR_UNSUPPORTED, "kv_dtype=%d is not F32, BF16 or VQ8", d->kv_dtype);
+    if (d->kv_dtype != UAA_DTYPE_F32 && d->kv_dtype != UAA_DTYPE_BF16 && d->kv_dtype != UAA_DTYPE_VQ8 &&
+        d->kv_dtype != UAA_DTYPE_Q8)
+        return fail(UAA_ERR_UNSUPPORTED, "kv_dtype=%d is not F32, BF16, VQ8 or Q8", d->kv_dtype);
     if (d->io_dtype != UAA_DTYPE_F32 && d->io_dtype != UAA_DTYPE_BF16)
         return fail(UAA_ERR_UNSUPPORTED, "io_dtype=%d is not F32 or BF16", d->io_dtype);
     if (d->out_dtype != UAA_DTYPE_F32 && d->out_dtype != UAA_DTYPE_BF16)
@@ -229,7 +230,8 @@ uaa_status check_args(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
         {a->v_cache, "v_cache", true},
         {a->seq_lens, "seq_lens", true},
         {a->out, "out", true},
-        {a->v_scale, "v_scale", d->kv_dtype == UAA_DTYPE_VQ8},
+        {a->v_scale, "v_scale", d->kv_dtype == UAA_DTYPE_VQ8 || d->kv_dtype == UAA_DTYPE_Q8},
+        {a->k_scale, "k_scale", d->kv_dtype == UAA_DTYPE_Q8},
         {a->q_norm_w, "q_norm_w", need_io && d->qk_norm},
         {a->k_norm_w, "k_norm_w", need_io && d->qk_norm},
         {a->sink, "sink", d->has_sink != 0},
@@ -386,6 +388,7 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.k_cache = a->k_cache;
     p.v_cache = a->v_cache;
     p.v_scale = a->v_scale;
+    p.k_scale = a->k_scale;
     p.seq_lens = a->seq_lens;
     char* w = static_cast<char*>(ws->ptr);
     p.q_prime = reinterpret_cast<float*>(w + pl.off_qrot);
@@ -404,26 +407,36 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     char* w = static_cast<char*>(ws->ptr);
     const size_t D = d->head_dim, Hq = d->n_q_heads;
     const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
-    CUtensorMap tk, tv, ts;
+    CUtensorMap tk, tv, ts, tks;
     if (pl.kernel == 1) {
         const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
         const uint32_t tk_rows = (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype);  // box height
-        UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
-                          CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
-        if (d->kv_dtype == UAA_DTYPE_VQ8) {
-            // codes: boxes of tk_rows x min(D, 128) bytes, swizzled like the bf16 boxes so
-            // the kernel's ldmatrix reads on them are free of bank conflicts
-            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, D > 128 ? 128u : (uint32_t)D,
-                              tk_rows, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+        const uint64_t heads = (uint64_t)a->batch * d->n_kv_heads;
+        // int8 codes: boxes of tk_rows x min(D, 128) bytes, swizzled like the bf16 boxes so
+        // the kernel's ldmatrix reads on them are free of bank conflicts; scales: one
+        // tk_rows-float box per stage
+        const uint32_t code_box = D > 128 ? 128u : (uint32_t)D;
+        const CUtensorMapSwizzle code_sw = D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+        if (d->kv_dtype == UAA_DTYPE_Q8) {
+            UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->k_cache, D, rows, D, code_box, tk_rows, code_sw,
+                              "k_cache codes"));
+            UAA_TRY(encode_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->k_scale, a->cache_capacity, heads,
+                              (uint64_t)a->cache_capacity * 4, tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "k_scale"));
+        } else {
+            UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
+                              CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
+        }
+        if (d->kv_dtype == UAA_DTYPE_VQ8 || d->kv_dtype == UAA_DTYPE_Q8) {
+            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, code_box, tk_rows, code_sw,
                               "v_cache codes"));
-            UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, a->cache_capacity,
-                              (uint64_t)a->batch * d->n_kv_heads, (uint64_t)a->cache_capacity * 4, tk_rows, 1,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
+            UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, a->cache_capacity, heads,
+                              (uint64_t)a->cache_capacity * 4, tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
         } else {
             UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, tk_rows,
                               CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
             ts = tv;  // unused by the bf16 kernel
         }
+        if (d->kv_dtype != UAA_DTYPE_Q8) tks = ts;  // unused without key codes
     }
     for (int sl = 0; sl < pl.n_slices; ++sl) {
         const int b0 = sl * pl.slice;
@@ -445,6 +458,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.k_cache = a->k_cache;
         p.v_cache = a->v_cache;
         p.v_scale = a->v_scale;
+        p.k_scale = a->k_scale;
         p.seq_lens = a->seq_lens + b0;
         p.prefix = reinterpret_cast<int*>(w + pl.off_prefix + sl * pl.prefix_stride);
         p.ranges = reinterpret_cast<long long*>(w + pl.off_ranges + sl * pl.ranges_stride);
@@ -484,7 +498,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         }
         const cudaError_t e = pl.kernel == 0
                                   ? uaa::launch_partial_simt(p, pl.n_ctas, s)
-                                  : uaa::launch_partial_tc(p, tk, tv, ts, d->kv_dtype, pl.n_head_tiles, pl.n_ctas, s);
+                                  : uaa::launch_partial_tc(p, tk, tv, ts, tks, d->kv_dtype, pl.n_head_tiles, pl.n_ctas, s);
         if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
     }
     return UAA_OK;

@@ -6,9 +6,9 @@
 // row; then each warp takes whole rows, loading the next while it processes the
 // current one: q rows go to the workspace pre-multiplied by the partial
 // kernel's logit prescale, k rows and v rows go to slot seq_lens[b] of the
-// cache. vq8 values are quantised in fp32 with IEEE division and
-// round-half-even, the storage rule of the vq8 cache (llamay "Models and
-// formats", "The KV cache, in three precisions").
+// cache. vq8 values (and q8 keys, after the rotation) are quantised in fp32
+// with IEEE division and round-half-even, the storage rule of the vq8 cache
+// (llamay "Models and formats", "The KV cache, in three precisions").
 #include "internal.cuh"
 
 namespace uaa {
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
         const size_t slot = ((static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos) * D;
         if (!is_q && !is_k) {  // value row: stored as given (or quantised)
             if (!fits) continue;
-            if (p.kv_dtype == UAA_DTYPE_VQ8) {
+            if (p.kv_dtype == UAA_DTYPE_VQ8 || p.kv_dtype == UAA_DTYPE_Q8) {
                 quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot,
                                   p.v_scale + (static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos);
             } else {
@@ -141,6 +141,9 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                     p.q_rot_out[in_row + ia] = ya;
                     p.q_rot_out[in_row + ib] = yb;
                 }
+            } else if (fits && p.kv_dtype == UAA_DTYPE_Q8) {  // the whole rotated row first: its scale
+                rowbuf[warp][ia] = ya;                          // needs max |k| (pairs are disjoint)
+                rowbuf[warp][ib] = yb;
             } else if (fits) {
                 store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
                          slot + ia, ya);
@@ -149,6 +152,14 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
             }
         }
         __syncwarp();
+        if (is_k && fits && p.kv_dtype == UAA_DTYPE_Q8) {  // q8 key: codes and scale of the rotated row
+            float y[EPL];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) y[i] = rowbuf[warp][lane + 32 * i];
+            quantize_row<EPL>(y, lane, static_cast<int8_t*>(p.k_cache) + slot,
+                              p.k_scale + (static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos);
+            __syncwarp();  // the row is read before the next one overwrites it
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + 1;

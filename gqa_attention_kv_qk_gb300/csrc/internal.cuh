@@ -37,6 +37,7 @@ struct AppendParams {
     void* k_cache;
     void* v_cache;
     float* v_scale;
+    float* k_scale;         // q8 caches: the key rows' scales
     int* seq_lens;
     float* q_prime;         // workspace [B][Hq][D]
     float* q_rot_out;       // optional [B][Hq][D]
@@ -106,6 +107,7 @@ struct PartialParams {
     void* k_cache;          // whole caches (rows indexed with b_off + b)
     void* v_cache;
     float* v_scale;
+    float* k_scale;         // q8 caches: the key rows' scales
     int* seq_lens;          // slice-relative (advanced by the fused kernel only)
     int* prefix;            // [B + 1] stage prefix over sequences, written for the combine
     long long* ranges;      // [P' + 1] range starts, written for the combine
@@ -163,8 +165,8 @@ struct CombineParams {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_partial_simt(const PartialParams& p, int n_ctas, cudaStream_t s);
 cudaError_t launch_partial_tc(const PartialParams& p, const CUtensorMap& tm_k,
-                              const CUtensorMap& tm_v, const CUtensorMap& tm_s, int kv_dtype,
-                              int n_head_tiles, int n_ctas, cudaStream_t s);
+                              const CUtensorMap& tm_v, const CUtensorMap& tm_s, const CUtensorMap& tm_ks,
+                              int kv_dtype, int n_head_tiles, int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
                                 float* scales, cudaStream_t s);

@@ -1,4 +1,4 @@
-// partial_tc.cu -- split-K decode partial for bf16 and vq8 caches: a persistent,
+// partial_tc.cu -- split-K decode partial for bf16, vq8 and q8 caches: a persistent,
 // warp-specialised kernel with TMA tile loads into a shared-memory ring and
 // tensor-core contractions.
 //
@@ -22,10 +22,11 @@
 //     have read the lengths advances seq_lens.
 //   warp 4 (producer): one lane walks the CTA's segments and streams their
 //     stages, TK = 64 MG keys each, with 2-D TMA loads (cp.async.bulk.tensor)
-//     into a ring of kStages stages, straight across segment boundaries. Key and
-//     bf16 value boxes are TK rows x 128 bytes with the 128-byte swizzle; vq8
-//     code boxes are TK rows x min(D, 128) bytes with the 64- or 128-byte
-//     swizzle; vq8 scales are one TK-float box. Full / empty mbarriers pass
+//     into a ring of kStages stages, straight across segment boundaries. bf16
+//     key and value boxes are TK rows x 128 bytes with the 128-byte swizzle;
+//     int8 code boxes (vq8 / q8 values, q8 keys) are TK rows x min(D, 128) bytes
+//     with the 64- or 128-byte swizzle; scales are one TK-float box per row
+//     kind. Full / empty mbarriers pass
 //     stages between the producer and the consumers.
 //   warps 0-3 (consumers): warp w owns keys 16 MG w .. 16 MG (w+1) - 1 of every
 //     stage, as MG groups of 16 keys that share one softmax round (MG = 2 for
@@ -33,6 +34,10 @@
 //     S^T (16 keys x 8 heads) = K (16 x D) . Q'^T (D x 8) with mma.m16n8k16
 //     (keys on M, heads on N: no padding of M). The fp32 q' rows are split into
 //     bf16 hi + lo parts, two MMAs each, so the logits keep ~16 significant bits.
+//       q8 keys: ldmatrix (not transposed) on the int8 stage hands each thread
+//       four consecutive codes of a key row, widened exactly to fp16; the q'
+//       parts are fp16 and laid out in the same dim order, and each key's
+//       logit is multiplied by its scale after the contraction.
 //     Online softmax (log2 domain) runs on the fp32 accumulators. P is split into
 //     hi + lo parts and moved with movmatrix into the B operand of
 //     O^T (D x 8) += V^T (D x 16 keys) . P^T (16 keys x 8 heads).
@@ -68,30 +73,42 @@ constexpr int kThreads = (kConsumerWarps + 2) * 32;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// MG: 16-key groups each consumer warp takes per stage: at head_dim 64 a key
-// costs few bytes and the per-stage softmax work is shared by 16 MG keys (2 for
-// bf16; 4 for vq8, whose consumers are the slowest per byte: one 256-key stage
-// gives each warp four independent QK chains).
-template <int D, bool VQ8>
+// Cache kinds of the kernel's KV template argument: bf16 keys and values; vq8
+// (bf16 keys, int8 value codes + per-key scale); q8 (int8 codes for both).
+constexpr int kKvBf16 = 0, kKvVq8 = 1, kKvQ8 = 2;
+
+// MG: 16-key groups each consumer warp takes per stage: where a key costs few
+// bytes the consumers, not HBM, set the pace, and MG independent QK chains per
+// warp hide their latency. Head_dim 64: 2 for bf16, 4 for vq8 and q8 (one
+// 256-key stage); q8 at head_dims 128 and 256: 2 (a q8 key row is half a bf16
+// one: with one group its consumers measured 15 % slower).
+template <int D, int KV>
 struct KeyGroups {
-    static constexpr int kMG = D == 64 ? (VQ8 ? 4 : 2) : 1;
+    static constexpr int kMG = D == 64 ? (KV != kKvBf16 ? 4 : 2) : (KV == kKvQ8 ? 2 : 1);
 };
 
 // Shared memory, from a 1024-byte aligned base: the ring of kStages stages |
 // full / empty barriers per stage | q-full, q-empty barriers and the range | stage prefix |
 // lengths | q' fragment slot | two new-row staging slots | rotation tables. The ring takes what the
 // per-CTA budget leaves (two CTAs per SM below head_dim 256).
-template <int D, bool VQ8, int NHT>
+template <int D, int KV, int NHT>
 struct Shape {
-    static constexpr int kMG = KeyGroups<D, VQ8>::kMG;
+    static constexpr int kD = D;
+    static constexpr bool kVQ8 = KV != kKvBf16;              // int8 value codes + scales
+    static constexpr bool kKQ8 = KV == kKvQ8;                // int8 key codes + scales
+    static constexpr int kMG = KeyGroups<D, KV>::kMG;
     static constexpr int kTK = kTileKeys * kMG;             // keys per stage
     static constexpr int kHC = 8 * NHT;                     // query heads of a unit
     static constexpr int kBoxBytes = kTK * 128;             // kTK rows x 128 bytes
-    static constexpr int kKBoxes = D / 64;                  // 128-byte column boxes of a bf16 row
-    static constexpr int kVBoxes = VQ8 ? (D > 128 ? D / 128 : 1) : D / 64;
-    static constexpr int kKBytes = kTK * D * 2;
-    static constexpr int kVBytes = VQ8 ? kTK * D : kTK * D * 2;
-    static constexpr int kSBytes = VQ8 ? kTK * 4 : 0;
+    static constexpr int kCodeBoxes = D > 128 ? D / 128 : 1;  // boxes of an int8 code row
+    static constexpr int kKBoxes = kKQ8 ? kCodeBoxes : D / 64;
+    static constexpr int kVBoxes = kVQ8 ? kCodeBoxes : D / 64;
+    static constexpr int kKBytes = kKQ8 ? kTK * D : kTK * D * 2;
+    static constexpr int kVBytes = kVQ8 ? kTK * D : kTK * D * 2;
+    // a stage: keys | values | value scales (int8 values) | key scales (int8 keys)
+    static constexpr int kVScaleOff = kKBytes + kVBytes;
+    static constexpr int kKScaleOff = kVScaleOff + (kVQ8 ? kTK * 4 : 0);
+    static constexpr int kSBytes = (kVQ8 ? kTK * 4 : 0) + (kKQ8 ? kTK * 4 : 0);
     static constexpr int kStageBytes = round_up(kKBytes + kVBytes + kSBytes, 1024);
     static constexpr int kTxBytes = kKBytes + kVBytes + kSBytes;
     static constexpr int kPrefixBytes = round_up((kMaxSliceBatch + 1) * 4, 16);
@@ -100,8 +117,9 @@ struct Shape {
     // bytes so the 8 rows a warp reads at once fall in distinct banks
     static constexpr int kFragRow = D * 4 + 32;
     static constexpr int kFragBytes = kHC * kFragRow;
-    // a new key row (bf16) and value row (bf16, or int8 codes + fp32 scale)
-    static constexpr int kNewRowBytes = round_up(2 * D + (VQ8 ? D + 4 : 2 * D), 16);
+    // a new key row (bf16, or int8 codes) at 0, value row (bf16, or int8 codes) at
+    // 2 D, then for int8 values the value scale at 3 D and the key scale at 3 D + 4
+    static constexpr int kNewRowBytes = round_up(2 * D + (kVQ8 ? D + 8 : 2 * D), 16);
     // q-full and q-empty barriers, then the CTA's range slot, its weights, start, end, go flag
     static constexpr int kCtlBytes = 64;
     // fused append: theta'_p / pi (fp64) and the (cos, sin) of the current sequence, D / 2 each
@@ -148,7 +166,8 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
     lo = pack_bf16(x0 - h0, x1 - h1);
 }
 
-// The same split into fp16 hi + lo parts (values in [0, 1]).
+// The same split into fp16 hi + lo parts (|x| below the fp16 range: the P
+// weights in [0, 1], or q' rows for int8 keys).
 __device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint32_t& lo)
 {
     __half2 h = __floats2half2_rn(x0, x1);
@@ -175,6 +194,16 @@ __device__ __forceinline__ void widen_code_pairs(uint32_t r, uint32_t& d_even, u
     d_odd = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
 }
 
+// A register from ldmatrix (not transposed) on int8 key rows holds codes
+// (key k, dims d .. d+3) in bytes 0-3. Returns the fp16 pairs [(k, d), (k, d+1)]
+// and [(k, d+2), (k, d+3)], exactly, by the same mantissa construction.
+__device__ __forceinline__ void widen_code_quad(uint32_t r, uint32_t& d01, uint32_t& d23)
+{
+    const uint32_t u = r ^ 0x80808080u;
+    d01 = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4140), 0x64806480u);
+    d23 = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u);
+}
+
 __device__ __forceinline__ bool key_ok(int k, int lo, int hi) { return k >= lo && k < hi; }
 
 // Once per CTA the prep warp, having issued the reads of its first q rows, lets
@@ -186,6 +215,16 @@ __device__ __forceinline__ bool key_ok(int k, int lo, int hi) { return k >= lo &
 __device__ __forceinline__ void release_producer(uint32_t go, int lane)
 {
     if (lane == 0) ptx::flag_set(go, 1u);  // no __syncwarp: it too would wait for the reads
+}
+
+// fp16 hi + lo parts of x into element e of a q' fragment row (the operands of
+// a q8 cache's int8 keys, which widen to fp16).
+__device__ __forceinline__ void store_frag_f16(uint8_t* row, int e, float x)
+{
+    const __half h = __float2half_rn(x);
+    const __half l = __float2half_rn(x - __half2float(h));
+    *reinterpret_cast<__half*>(row + (e >> 1) * 8 + (e & 1) * 2) = h;
+    *reinterpret_cast<__half*>(row + (e >> 1) * 8 + 4 + (e & 1) * 2) = l;
 }
 
 // bf16 hi + lo parts of x into element e of a q' fragment row.
@@ -206,8 +245,8 @@ __device__ __forceinline__ void store_frag(uint8_t* row, int e, float x)
 // fragment rows (element e as fp32 at byte 4 e, the bytes its hi / lo pair
 // takes later) and each head is then finished in a rolled loop: at a launch's
 // start this code runs cold, and an unrolled body cost microseconds of
-// instruction fetch.
-template <int D, int HC, typename T>
+// instruction fetch. F16: fp16 hi / lo parts (for int8 keys), else bf16.
+template <int D, int HC, typename T, bool F16>
 __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool write_rot, bool new_seq, int pos,
                              const double* freq, float2* cs, uint8_t* frag, int row_bytes, uint32_t go, int lane)
 {
@@ -278,16 +317,22 @@ __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool
                     p.q_rot_out[qoff + ia[j]] = ya[j];
                     p.q_rot_out[qoff + ib[j]] = yb[j];
                 }
-                store_frag(row, ia[j], ya[j] * p.qscale);
-                store_frag(row, ib[j], yb[j] * p.qscale);
+                if (F16) {
+                    store_frag_f16(row, ia[j], ya[j] * p.qscale);
+                    store_frag_f16(row, ib[j], yb[j] * p.qscale);
+                } else {
+                    store_frag(row, ia[j], ya[j] * p.qscale);
+                    store_frag(row, ib[j], yb[j] * p.qscale);
+                }
             }
         }
     }
 }
 
 // Prep warp, separate append: the workspace's q' rows (already rotated and
-// prescaled, fp32) into the fragment slot, eight rows' loads at a time.
-template <int D, int HC>
+// prescaled, fp32) into the fragment slot, eight rows' loads at a time (fp16
+// parts for int8 keys when F16).
+template <int D, int HC, bool F16>
 __device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int h0, int nh, uint8_t* frag,
                                               int row_bytes, uint32_t go, int lane)
 {
@@ -308,7 +353,10 @@ __device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int
 #pragma unroll
             for (int j = 0; j < D / 64; ++j) {
                 uint32_t h, l;
-                split_bf16(x[i][j].x, x[i][j].y, h, l);
+                if (F16)
+                    split_f16(x[i][j].x, x[i][j].y, h, l);
+                else
+                    split_bf16(x[i][j].x, x[i][j].y, h, l);
                 *reinterpret_cast<uint2*>(frag + (hc0 + i) * row_bytes + (lane + 32 * j) * 8) = make_uint2(h, l);
             }
     }
@@ -328,13 +376,15 @@ __device__ __forceinline__ void prefetch_new_rows(const PartialParams& p, int b,
     }
 }
 
-// Prep warp, fused append: the new key row (RMSNorm, rotation, bf16) and value
-// row (bf16, or vq8 codes and scale) of (b, kvh) into a staging slot (key at 0,
-// value at 2 D, vq8 scale at 3 D), and into the cache at slot L when `store`.
-template <int D, bool VQ8, typename T>
+// Prep warp, fused append: the new key row (RMSNorm, rotation, then bf16, or
+// int8 codes and scale for q8) and value row (bf16, or int8 codes and scale) of
+// (b, kvh) into a staging slot (key at 0, value at 2 D, value scale at 3 D, key
+// scale at 3 D + 4), and into the cache at slot L when `store`.
+template <int D, int KV, typename T>
 __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, const float2* cs, uint8_t* staging,
                               bool store, int lane)
 {
+    constexpr bool VQ8 = KV != kKvBf16, KQ8 = KV == kKvQ8;
     constexpr int NP = D / 64;   // rotation pairs per lane
     constexpr int EPL = D / 32;  // values per lane
     const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D;
@@ -361,17 +411,41 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
             kb[j] = kb[j] * inv * (p.k_norm_w[ib[j]] + p.norm_offset);
         }
     }
-    __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(staging);
-    __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.k_cache) + slot * D;
 #pragma unroll
-    for (int j = 0; j < NP; ++j) {
-        rope_rotate(ka[j], kb[j], cs[lane + 32 * j]);
-        const __nv_bfloat16 ha = __float2bfloat16_rn(ka[j]), hb = __float2bfloat16_rn(kb[j]);
-        ks[ia[j]] = ha;
-        ks[ib[j]] = hb;
-        if (store) {
-            kc[ia[j]] = ha;
-            kc[ib[j]] = hb;
+    for (int j = 0; j < NP; ++j) rope_rotate(ka[j], kb[j], cs[lane + 32 * j]);
+    if (KQ8) {  // the rotated row's codes, by the vq8 rule over the whole row
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) amax = fmaxf(amax, fmaxf(fabsf(ka[j]), fabsf(kb[j])));
+        const float sc = vq8_scale(warp_max(amax));
+        int8_t* ks = reinterpret_cast<int8_t*>(staging);
+        int8_t* kc = static_cast<int8_t*>(p.k_cache) + slot * D;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int8_t ca = vq8_code(ka[j], sc), cb = vq8_code(kb[j], sc);
+            ks[ia[j]] = ca;
+            ks[ib[j]] = cb;
+            if (store) {
+                kc[ia[j]] = ca;
+                kc[ib[j]] = cb;
+            }
+        }
+        if (lane == 0) {
+            *reinterpret_cast<float*>(staging + 3 * D + 4) = sc;
+            if (store) p.k_scale[slot] = sc;
+        }
+    } else {
+        __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(staging);
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.k_cache) + slot * D;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const __nv_bfloat16 ha = __float2bfloat16_rn(ka[j]), hb = __float2bfloat16_rn(kb[j]);
+            ks[ia[j]] = ha;
+            ks[ib[j]] = hb;
+            if (store) {
+                kc[ia[j]] = ha;
+                kc[ib[j]] = hb;
+            }
         }
     }
     if (VQ8) {
@@ -417,40 +491,53 @@ __device__ __noinline__ void count_in_and_advance(const PartialParams& p, const 
 }
 
 // Owner warp of the new key: the staged rows over row r of the loaded stage.
-template <int D, bool VQ8, int TK>
-__device__ __forceinline__ void patch_stage_row(const uint8_t* staging, uint8_t* stage, int r, int k_bytes,
-                                                int v_bytes, int lane)
+template <class SH>
+__device__ __forceinline__ void patch_stage_row(const uint8_t* staging, uint8_t* stage, int r, int lane)
 {
-    for (int c = lane; c < D / 8; c += 32)
-        *reinterpret_cast<uint4*>(stage + tile_off<TK>(r, c)) = *reinterpret_cast<const uint4*>(staging + 16 * c);
-    if (VQ8) {
+    constexpr int D = SH::kD;
+    constexpr int TK = SH::kTK;
+    if (SH::kKQ8) {
         for (int c = lane; c < D / 16; c += 32)
-            *reinterpret_cast<uint4*>(stage + k_bytes + code_off<D, TK>(r, c)) =
-                *reinterpret_cast<const uint4*>(staging + 2 * D + 16 * c);
+            *reinterpret_cast<uint4*>(stage + code_off<D, TK>(r, c)) = *reinterpret_cast<const uint4*>(staging + 16 * c);
         if (lane == 0)
-            *reinterpret_cast<float*>(stage + k_bytes + v_bytes + 4 * r) =
-                *reinterpret_cast<const float*>(staging + 3 * D);
+            *reinterpret_cast<float*>(stage + SH::kKScaleOff + 4 * r) = *reinterpret_cast<const float*>(staging + 3 * D + 4);
     } else {
         for (int c = lane; c < D / 8; c += 32)
-            *reinterpret_cast<uint4*>(stage + k_bytes + tile_off<TK>(r, c)) =
+            *reinterpret_cast<uint4*>(stage + tile_off<TK>(r, c)) = *reinterpret_cast<const uint4*>(staging + 16 * c);
+    }
+    if (SH::kVQ8) {
+        for (int c = lane; c < D / 16; c += 32)
+            *reinterpret_cast<uint4*>(stage + SH::kKBytes + code_off<D, TK>(r, c)) =
+                *reinterpret_cast<const uint4*>(staging + 2 * D + 16 * c);
+        if (lane == 0)
+            *reinterpret_cast<float*>(stage + SH::kVScaleOff + 4 * r) = *reinterpret_cast<const float*>(staging + 3 * D);
+    } else {
+        for (int c = lane; c < D / 8; c += 32)
+            *reinterpret_cast<uint4*>(stage + SH::kKBytes + tile_off<TK>(r, c)) =
                 *reinterpret_cast<const uint4*>(staging + 2 * D + 16 * c);
     }
     __syncwarp();
 }
 
-template <int D, bool VQ8, int NHT>
+template <int D, int KV, int NHT>
 __global__ void __launch_bounds__(kThreads, (D == 256 ? 1 : 2))
 partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_s, const PartialParams p)
+                  const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_ks,
+                  const PartialParams p)
 {
-    using SH = Shape<D, VQ8, NHT>;
+    using SH = Shape<D, KV, NHT>;
+    constexpr bool VQ8 = SH::kVQ8;  // int8 value codes
+    constexpr bool KQ8 = SH::kKQ8;  // int8 key codes
     constexpr int MG = SH::kMG;     // 16-key groups per warp per stage
     constexpr int TK = SH::kTK;     // keys per stage
     constexpr int KS = D / 16;      // k-steps of QK, m-tiles of PV
     constexpr int HC = 8 * NHT;     // head columns of a unit
-    // merge scratch (inside one stage): all of D at once if it fits, else halves
-    constexpr int RC = (kConsumerWarps * HC * (D + 4) + 2 * kConsumerWarps * HC) * 4 <= SH::kStageBytes ? D : D / 2;
-    static_assert((kConsumerWarps * HC * (RC + 4) + 2 * kConsumerWarps * HC) * 4 <= SH::kStageBytes,
+    // merge scratch (inside one stage): all of D at once if it fits, else halves or quarters
+    constexpr int kScratchRow = 2 * kConsumerWarps * HC * 4;
+    constexpr int RC = kConsumerWarps * HC * (D + 4) * 4 + kScratchRow <= SH::kStageBytes       ? D
+                       : kConsumerWarps * HC * (D / 2 + 4) * 4 + kScratchRow <= SH::kStageBytes ? D / 2
+                                                                                               : D / 4;
+    static_assert(kConsumerWarps * HC * (RC + 4) * 4 + kScratchRow <= SH::kStageBytes,
                   "merge scratch must fit in one stage");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -489,6 +576,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
         if (VQ8) ptx::prefetch_tensormap(&tm_s);
+        if (KQ8) ptx::prefetch_tensormap(&tm_ks);
     }
     grid_dependency_wait();  // the step's inputs (and a separate append's rows) are complete
     if (p.fused && threadIdx.x >= 32 && threadIdx.x < 32 + D / 2)  // the rotation table, while warp 0 scans
@@ -566,14 +654,16 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     const int y = row0 + key;
 #pragma unroll
                     for (int c = 0; c < SH::kKBoxes; ++c)
-                        ptx::tma_load_2d_hint(st + c * SH::kBoxBytes, &tm_k, c * 64, y, bar, stream_policy);
+                        ptx::tma_load_2d_hint(st + c * SH::kBoxBytes, &tm_k, c * (KQ8 ? 128 : 64), y, bar,
+                                              stream_policy);
+                    if (KQ8)
+                        ptx::tma_load_2d_hint(st + SH::kKScaleOff, &tm_ks, key, head_row, bar, stream_policy);
                     if (VQ8) {
 #pragma unroll
                         for (int c = 0; c < SH::kVBoxes; ++c)
                             ptx::tma_load_2d_hint(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 128, y, bar,
                                                   stream_policy);
-                        ptx::tma_load_2d_hint(st + SH::kKBytes + SH::kVBytes, &tm_s, key, head_row, bar,
-                                              stream_policy);
+                        ptx::tma_load_2d_hint(st + SH::kVScaleOff, &tm_s, key, head_row, bar, stream_policy);
                     } else {
 #pragma unroll
                         for (int c = 0; c < SH::kVBoxes; ++c)
@@ -622,11 +712,11 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const bool rot = p.q_rot_out != nullptr && sg.st0 == 0;
                 uint8_t* st_row = staging + (seg & 1) * SH::kNewRowBytes;
                 if (p.io_dtype == UAA_DTYPE_F32)
-                    prep_fused_q<D, HC, float>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s, frag,
-                                               SH::kFragRow, seg == 0 ? go : 0u, lane);
+                    prep_fused_q<D, HC, float, KQ8>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s,
+                                                    frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
                 else
-                    prep_fused_q<D, HC, __nv_bfloat16>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s, cs_s,
-                                                       frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
+                    prep_fused_q<D, HC, __nv_bfloat16, KQ8>(p, sg.b, h0, nh, rot, sg.b != cs_b, fits ? L : 0, freq_s,
+                                                            cs_s, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
                 cs_b = sg.b;
                 // the q' fragments go to the consumers first; the new rows are needed only at
                 // the segment's last stage (rows_ready)
@@ -634,9 +724,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0) ptx::mbar_arrive(bar_qfull);
                 if (ends) {
                     if (p.io_dtype == UAA_DTYPE_F32)
-                        prep_new_rows<D, VQ8, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
+                        prep_new_rows<D, KV, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
                     else
-                        prep_new_rows<D, VQ8, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
+                        prep_new_rows<D, KV, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
                     __syncwarp();
                     if (lane == 0) {
                         __threadfence_block();
@@ -646,7 +736,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 pos += sg.n_st;
                 continue;
             } else {
-                prep_loaded_q<D, HC>(p, sg.b, h0, nh, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
+                prep_loaded_q<D, HC, KQ8>(p, sg.b, h0, nh, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_qfull);
@@ -681,8 +771,10 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             fits && sg.st0 + sg.n_st == sg.stages ? L - (t0 + MG * (sg.stages - 1)) * kTileKeys : -1;
         const int new_w = new_r >= 0 ? new_r / (16 * MG) : -1;
 
-        // this segment's q' fragments from the prep warp: head nt * 8 + g, dims
-        // 16 kk + 2t (+1) and 16 kk + 2t + 8 (+9), as (hi, lo) bf16 pairs
+        // this segment's q' fragments from the prep warp: head nt * 8 + g, as (hi, lo)
+        // pairs; k-step kk takes dims 16 kk + 2t (+1) and 16 kk + 2t + 8 (+9) against
+        // bf16 keys, and dims 16 kk + 4t .. 16 kk + 4t + 3 against int8 keys (the
+        // order in which ldmatrix hands out a code row; the contraction does not care)
         if (!failed && !ptx::mbar_wait(bar_qfull, seg & 1, kWaitLimitCycles)) {
             failed = true;
             if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
@@ -693,12 +785,20 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const uint8_t* row = frag + (nt * 8 + g) * SH::kFragRow;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-                const uint2 a = *reinterpret_cast<const uint2*>(row + (8 * kk + t) * 8);
-                const uint2 c = *reinterpret_cast<const uint2*>(row + (8 * kk + t + 4) * 8);
-                qhi[nt][kk][0] = a.x;
-                qlo[nt][kk][0] = a.y;
-                qhi[nt][kk][1] = c.x;
-                qlo[nt][kk][1] = c.y;
+                if (KQ8) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(row + (8 * kk + 2 * t) * 8);
+                    qhi[nt][kk][0] = a.x;
+                    qlo[nt][kk][0] = a.y;
+                    qhi[nt][kk][1] = a.z;
+                    qlo[nt][kk][1] = a.w;
+                } else {
+                    const uint2 a = *reinterpret_cast<const uint2*>(row + (8 * kk + t) * 8);
+                    const uint2 c = *reinterpret_cast<const uint2*>(row + (8 * kk + t + 4) * 8);
+                    qhi[nt][kk][0] = a.x;
+                    qlo[nt][kk][0] = a.y;
+                    qhi[nt][kk][1] = c.x;
+                    qlo[nt][kk][1] = c.y;
+                }
             }
         }
         __syncwarp();
@@ -730,8 +830,8 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     __threadfence_block();
                 }
                 if (__shfl_sync(0xffffffffu, ready, 0))
-                    patch_stage_row<D, VQ8, TK>(staging + (seg & 1) * SH::kNewRowBytes,
-                                                base_ptr + s * SH::kStageBytes, new_r, SH::kKBytes, SH::kVBytes, lane);
+                    patch_stage_row<SH>(staging + (seg & 1) * SH::kNewRowBytes, base_ptr + s * SH::kStageBytes, new_r,
+                                        lane);
                 else
                     failed = true;
             }
@@ -746,16 +846,54 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int nt = 0; nt < NHT; ++nt)
                         sacc[mg][nt][0] = sacc[mg][nt][1] = sacc[mg][nt][2] = sacc[mg][nt][3] = 0.f;
+                if (KQ8) {
+                    // int8 keys: one ldmatrix.x4 covers 16 keys x 32 dims (k-steps 2 kc and
+                    // 2 kc + 1); register j holds key g (+8 for odd j), dims 4t .. 4t + 3 of
+                    // 16-byte chunk 2 kc + j / 2, widened exactly to fp16 pairs
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
+                    for (int kc = 0; kc < KS / 2; ++kc) {
+#pragma unroll
+                        for (int mg = 0; mg < MG; ++mg) {
+                            uint32_t r[4], a0[4], a1[4];
+                            ptx::ldsm_x4(r, st + code_off<D, TK>(key_w + 16 * mg + lr + 8 * (lq & 1), 2 * kc + (lq >> 1)));
+                            widen_code_quad(r[0], a0[0], a0[2]);
+                            widen_code_quad(r[1], a0[1], a0[3]);
+                            widen_code_quad(r[2], a1[0], a1[2]);
+                            widen_code_quad(r[3], a1[1], a1[3]);
+#pragma unroll
+                            for (int nt = 0; nt < NHT; ++nt) {
+                                ptx::mma_f16(sacc[mg][nt], a0, qhi[nt][2 * kc][0], qhi[nt][2 * kc][1]);
+                                ptx::mma_f16(sacc[mg][nt], a0, qlo[nt][2 * kc][0], qlo[nt][2 * kc][1]);
+                                ptx::mma_f16(sacc[mg][nt], a1, qhi[nt][2 * kc + 1][0], qhi[nt][2 * kc + 1][1]);
+                                ptx::mma_f16(sacc[mg][nt], a1, qlo[nt][2 * kc + 1][0], qlo[nt][2 * kc + 1][1]);
+                            }
+                        }
+                    }
+                    // the logit of a code row is its scale times q' . codes
+                    const float* ksc = reinterpret_cast<const float*>(base_ptr + s * SH::kStageBytes + SH::kKScaleOff);
 #pragma unroll
                     for (int mg = 0; mg < MG; ++mg) {
-                        uint32_t a[4];
-                        ptx::ldsm_x4(a, st + tile_off<TK>(key_w + 16 * mg + lr + 8 * (lq & 1), 2 * kk + (lq >> 1)));
+                        const float k0 = ksc[key_w + 16 * mg + g], k8 = ksc[key_w + 16 * mg + g + 8];
 #pragma unroll
                         for (int nt = 0; nt < NHT; ++nt) {
-                            ptx::mma_bf16(sacc[mg][nt], a, qhi[nt][kk][0], qhi[nt][kk][1]);
-                            ptx::mma_bf16(sacc[mg][nt], a, qlo[nt][kk][0], qlo[nt][kk][1]);
+                            sacc[mg][nt][0] *= k0;
+                            sacc[mg][nt][1] *= k0;
+                            sacc[mg][nt][2] *= k8;
+                            sacc[mg][nt][3] *= k8;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+                        for (int mg = 0; mg < MG; ++mg) {
+                            uint32_t a[4];
+                            ptx::ldsm_x4(a, st + tile_off<TK>(key_w + 16 * mg + lr + 8 * (lq & 1), 2 * kk + (lq >> 1)));
+#pragma unroll
+                            for (int nt = 0; nt < NHT; ++nt) {
+                                ptx::mma_bf16(sacc[mg][nt], a, qhi[nt][kk][0], qhi[nt][kk][1]);
+                                ptx::mma_bf16(sacc[mg][nt], a, qlo[nt][kk][0], qlo[nt][kk][1]);
+                            }
                         }
                     }
                 }
@@ -769,8 +907,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 float w_g[MG], w_g8[MG], r_ratio = 1.f;
                 if (VQ8) {  // per-key scale relative to the running maximum; masked keys get 0
-                    const float* scl = reinterpret_cast<const float*>(base_ptr + s * SH::kStageBytes + SH::kKBytes +
-                                                                      SH::kVBytes);
+                    const float* scl = reinterpret_cast<const float*>(base_ptr + s * SH::kStageBytes + SH::kVScaleOff);
                     float smax = 0.f;
 #pragma unroll
                     for (int mg = 0; mg < MG; ++mg) {
@@ -1004,12 +1141,12 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
 }
 
-template <int D, bool VQ8, int NHT>
-cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& ts, int n_ctas, cudaStream_t s)
+template <int D, int KV, int NHT>
+cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ts,
+                       const CUtensorMap& tks, int n_ctas, cudaStream_t s)
 {
-    using SH = Shape<D, VQ8, NHT>;
-    auto kern = partial_tc_kernel<D, VQ8, NHT>;
+    using SH = Shape<D, KV, NHT>;
+    auto kern = partial_tc_kernel<D, KV, NHT>;
     static int configured_device_mask = 0;  // bit per device that has the smem attribute set
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1019,51 +1156,89 @@ cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUte
         if (e != cudaSuccess) return e;
         if (dev < 31) configured_device_mask |= 1 << dev;
     }
-    return launch_dependent(kern, dim3(n_ctas), dim3(kThreads), SH::kSmemBytes, s, tk, tv, ts, p);
+    return launch_dependent(kern, dim3(n_ctas), dim3(kThreads), SH::kSmemBytes, s, tk, tv, ts, tks, p);
+}
+
+template <int KV>
+size_t smem_bytes_kv(int D, int n_head_tiles)
+{
+    if (n_head_tiles == 2) {
+        switch (D) {
+        case 64: return Shape<64, KV, 2>::kSmemBytes;
+        case 128: return Shape<128, KV, 2>::kSmemBytes;
+        default: return 0;
+        }
+    }
+    switch (D) {
+    case 64: return Shape<64, KV, 1>::kSmemBytes;
+    case 128: return Shape<128, KV, 1>::kSmemBytes;
+    case 256: return Shape<256, KV, 1>::kSmemBytes;
+    default: return 0;
+    }
+}
+
+template <int KV>
+cudaError_t launch_kv(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ts,
+                      const CUtensorMap& tks, int n_head_tiles, int n_ctas, cudaStream_t s)
+{
+    if (n_head_tiles == 2) {
+        switch (p.D) {
+        case 64: return launch_one<64, KV, 2>(p, tk, tv, ts, tks, n_ctas, s);
+        case 128: return launch_one<128, KV, 2>(p, tk, tv, ts, tks, n_ctas, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (p.D) {
+    case 64: return launch_one<64, KV, 1>(p, tk, tv, ts, tks, n_ctas, s);
+    case 128: return launch_one<128, KV, 1>(p, tk, tv, ts, tks, n_ctas, s);
+    case 256: return launch_one<256, KV, 1>(p, tk, tv, ts, tks, n_ctas, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int kv_kind(int kv_dtype)
+{
+    return kv_dtype == UAA_DTYPE_Q8 ? kKvQ8 : (kv_dtype == UAA_DTYPE_VQ8 ? kKvVq8 : kKvBf16);
+}
+
+template <int KV>
+int keys_per_stage_kv(int D)
+{
+    switch (D) {
+    case 64: return KeyGroups<64, KV>::kMG * kTileKeys;
+    case 128: return KeyGroups<128, KV>::kMG * kTileKeys;
+    default: return KeyGroups<256, KV>::kMG * kTileKeys;
+    }
 }
 
 }  // namespace
 
 int partial_tc_keys_per_stage(int D, int kv_dtype)
 {
-    if (D != 64) return kTileKeys;
-    return (kv_dtype == UAA_DTYPE_VQ8 ? KeyGroups<64, true>::kMG : KeyGroups<64, false>::kMG) * kTileKeys;
+    switch (kv_kind(kv_dtype)) {
+    case kKvQ8: return keys_per_stage_kv<kKvQ8>(D);
+    case kKvVq8: return keys_per_stage_kv<kKvVq8>(D);
+    default: return keys_per_stage_kv<kKvBf16>(D);
+    }
 }
 
 size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles)
 {
-    const bool vq8 = kv_dtype == UAA_DTYPE_VQ8;
-    if (n_head_tiles == 2) {
-        switch (D) {
-        case 64: return vq8 ? Shape<64, true, 2>::kSmemBytes : Shape<64, false, 2>::kSmemBytes;
-        case 128: return vq8 ? Shape<128, true, 2>::kSmemBytes : Shape<128, false, 2>::kSmemBytes;
-        default: return 0;
-        }
-    }
-    switch (D) {
-    case 64: return vq8 ? Shape<64, true, 1>::kSmemBytes : Shape<64, false, 1>::kSmemBytes;
-    case 128: return vq8 ? Shape<128, true, 1>::kSmemBytes : Shape<128, false, 1>::kSmemBytes;
-    case 256: return vq8 ? Shape<256, true, 1>::kSmemBytes : Shape<256, false, 1>::kSmemBytes;
-    default: return 0;
+    switch (kv_kind(kv_dtype)) {
+    case kKvQ8: return smem_bytes_kv<kKvQ8>(D, n_head_tiles);
+    case kKvVq8: return smem_bytes_kv<kKvVq8>(D, n_head_tiles);
+    default: return smem_bytes_kv<kKvBf16>(D, n_head_tiles);
     }
 }
 
 cudaError_t launch_partial_tc(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& ts, int kv_dtype, int n_head_tiles, int n_ctas, cudaStream_t s)
+                              const CUtensorMap& ts, const CUtensorMap& tks, int kv_dtype, int n_head_tiles,
+                              int n_ctas, cudaStream_t s)
 {
-    const bool vq8 = kv_dtype == UAA_DTYPE_VQ8;
-    if (n_head_tiles == 2) {
-        switch (p.D) {
-        case 64: return vq8 ? launch_one<64, true, 2>(p, tk, tv, ts, n_ctas, s) : launch_one<64, false, 2>(p, tk, tv, ts, n_ctas, s);
-        case 128: return vq8 ? launch_one<128, true, 2>(p, tk, tv, ts, n_ctas, s) : launch_one<128, false, 2>(p, tk, tv, ts, n_ctas, s);
-        default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (p.D) {
-    case 64: return vq8 ? launch_one<64, true, 1>(p, tk, tv, ts, n_ctas, s) : launch_one<64, false, 1>(p, tk, tv, ts, n_ctas, s);
-    case 128: return vq8 ? launch_one<128, true, 1>(p, tk, tv, ts, n_ctas, s) : launch_one<128, false, 1>(p, tk, tv, ts, n_ctas, s);
-    case 256: return vq8 ? launch_one<256, true, 1>(p, tk, tv, ts, n_ctas, s) : launch_one<256, false, 1>(p, tk, tv, ts, n_ctas, s);
-    default: return cudaErrorInvalidValue;
+    switch (kv_kind(kv_dtype)) {
+    case kKvQ8: return launch_kv<kKvQ8>(p, tk, tv, ts, tks, n_head_tiles, n_ctas, s);
+    case kKvVq8: return launch_kv<kKvVq8>(p, tk, tv, ts, tks, n_head_tiles, n_ctas, s);
+    default: return launch_kv<kKvBf16>(p, tk, tv, ts, tks, n_head_tiles, n_ctas, s);
     }
 }
 

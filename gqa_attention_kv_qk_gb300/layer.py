@@ -30,8 +30,13 @@ class DecodeLayer:
         kv = cfg.get("kv_dtype", "bf16")
         dev = self.device
         kdt = torch.float32 if kv == "f32" else torch.bfloat16
-        self.k_cache = torch.zeros((batch, Hkv, capacity, D), dtype=kdt, device=dev)
-        if kv == "vq8":
+        if kv == "q8":
+            self.k_cache = torch.zeros((batch, Hkv, capacity, D), dtype=torch.int8, device=dev)
+            self.k_scale = torch.zeros((batch, Hkv, capacity), dtype=torch.float32, device=dev)
+        else:
+            self.k_cache = torch.zeros((batch, Hkv, capacity, D), dtype=kdt, device=dev)
+            self.k_scale = None
+        if kv in ("vq8", "q8"):
             self.v_cache = torch.zeros((batch, Hkv, capacity, D), dtype=torch.int8, device=dev)
             self.v_scale = torch.zeros((batch, Hkv, capacity), dtype=torch.float32, device=dev)
         else:
@@ -53,15 +58,23 @@ class DecodeLayer:
         to = lambda t: None if t is None else t.to(device=self.device, dtype=torch.float32).contiguous()
         self.q_norm_w, self.k_norm_w, self.sink = to(q_norm_w), to(k_norm_w), to(sink)
 
-    def load_cache(self, k_cache, v, lens):
-        """Copy host caches in. For a vq8 layer `v` holds fp32 values, quantised on
-        the device by uaa_vq8_quantize (the append's own rule)."""
-        self.k_cache.copy_(k_cache)
+    def load_cache(self, k, v, lens):
+        """Copy host caches in. For a vq8 layer `v` holds fp32 values, and for a q8
+        layer `k` too, quantised on the device by uaa_vq8_quantize (the append's
+        own rule)."""
+        D = self.cfg["head_dim"]
+
+        def quantize(vals, codes, scales):
+            vals = vals.to(device=self.device, dtype=torch.float32).contiguous()
+            B.uaa_vq8_quantize(vals.data_ptr(), B.DTYPE["f32"], vals.numel() // D, D, codes.data_ptr(),
+                               scales.data_ptr(), torch.cuda.current_stream(self.device))
+
+        if self.k_scale is not None:
+            quantize(k, self.k_cache, self.k_scale)
+        else:
+            self.k_cache.copy_(k)
         if self.v_scale is not None:
-            vals = v.to(device=self.device, dtype=torch.float32).contiguous()
-            D = self.cfg["head_dim"]
-            B.uaa_vq8_quantize(vals.data_ptr(), B.DTYPE["f32"], vals.numel() // D, D, self.v_cache.data_ptr(),
-                               self.v_scale.data_ptr(), torch.cuda.current_stream(self.device))
+            quantize(v, self.v_cache, self.v_scale)
         else:
             self.v_cache.copy_(v)
         lens = torch.as_tensor(lens, dtype=torch.int32)
@@ -97,6 +110,7 @@ class DecodeLayer:
         a.max_seq_len = max_seq_len
         a.out = B.ptr(self.out if out is None else out)
         a.q_rot = B.ptr(q_rot)
+        a.k_scale = B.ptr(self.k_scale)
         return a
 
     def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True, q_rot=None, out=None):

@@ -56,6 +56,13 @@ CONFIGS: dict[str, dict] = {
         kv_dtype="vq8", io_dtype="bf16", out_dtype="f32",
         rope_style="neox", rope_theta=150000.0, rope_scaling="yarn", factor=32.0,
         original_max_pos=4096, beta_fast=32.0, beta_slow=1.0, has_sink=True),
+    # The Llama-3.1-8B-like decode over a q8 cache (int8 keys and values, one fp32
+    # scale per token and kv head for each).
+    "llama31_8b_q8": dict(
+        batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, seq_len=8192, steps=64, seed=6,
+        kv_dtype="q8", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
+        low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
     # Gemma-3-12B-like decode: QK RMSNorm whose weights are stored as deltas from
     # one (applied as 1 + w), scale 1/sqrt(256), no softcap; one layer of each
     # kind per step (the model runs five local layers per global one): a local

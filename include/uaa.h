@@ -18,7 +18,7 @@
  *      log-sum-exp) per range it touches in the workspace.
  *   3. uaa_decode_attn_combine: log-sum-exp merge of those records, the sink
  *      logit added to the denominator, the remaining output rows written.
- *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16 and vq8 caches in one
+ *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16, vq8 and q8 caches in one
  *   kernel that forms q', k and v of the new token itself and attends the new
  *   key from shared memory); uaa_decode_attn runs 1-3 on one stream.
 
@@ -35,7 +35,8 @@
  *       llamay "Models and formats", "Architectures";
  *   - per-head attention sink in the softmax denominator, YaRN for gpt-oss:
  *       llamay "Models and formats", "Architectures" (gpt-oss row);
- *   - the vq8 cache (int8 values, per-token per-head fp32 scale, keys exact):
+ *   - the vq8 cache (int8 values, per-token per-head fp32 scale, keys exact)
+ *     and the q8 cache (keys stored the same way as values):
  *       llamay "Models and formats", "The KV cache, in three precisions".
  *
  * Conventions for every entry point:
@@ -44,9 +45,10 @@
  *     never synchronises (except uaa_device_status) and launches only on the
  *     given stream.
  *   - Layouts: q [B][Hq][D]; k_new, v_new [B][Hkv][D] (io_dtype);
- *     k_cache [B][Hkv][cap][D] (fp32, or bf16 for BF16 and VQ8 caches);
- *     v_cache [B][Hkv][cap][D] (fp32, bf16, or int8 codes for VQ8);
- *     v_scale [B][Hkv][cap] fp32 (VQ8 only); seq_lens [B] int32;
+ *     k_cache [B][Hkv][cap][D] (fp32, bf16 for BF16 and VQ8 caches, int8
+ *     codes for Q8); v_cache [B][Hkv][cap][D] (fp32, bf16, or int8 codes for
+ *     VQ8 and Q8); v_scale [B][Hkv][cap] fp32 (VQ8 and Q8); k_scale
+ *     [B][Hkv][cap] fp32 (Q8 only); seq_lens [B] int32;
  *     out [B][Hq][D] (out_dtype). Query head h reads kv head h / (Hq / Hkv).
  *   - Facts outside the supported ranges are refused with a status and a
  *     message naming the fact (uaa_last_error), never approximated.
@@ -67,7 +69,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 6
+#define UAA_ABI_VERSION 7
 
 typedef enum {
     UAA_OK = 0,
@@ -85,7 +87,12 @@ typedef enum {
     UAA_ROPE_SCALING_YARN = 2,
     UAA_ROPE_SCALING_LINEAR = 3
 } uaa_rope_scaling;
-typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2 } uaa_dtype;
+/* Cache storage: F32, BF16, VQ8 (bf16 keys, int8 value codes + one fp32 scale
+ * per token and kv head) or Q8 (keys stored like VQ8 values: the rotated key row
+ * as int8 codes + its own scale). Codes follow the rule of uaa_vq8_quantize.
+ * With Q8 the key codes meet q' (the normed, rotated q times the logit
+ * prescale) as fp16 tensor-core operands: |q'| must stay below 65504. */
+typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2, UAA_DTYPE_Q8 = 3 } uaa_dtype;
 
 /* Device-side status flags (sticky, in the workspace; read by uaa_device_status). */
 #define UAA_DEVFLAG_CAPACITY 0x1u   /* seq_lens[b] >= cache_capacity: that sequence was not appended */
@@ -136,7 +143,7 @@ typedef struct {
     int32_t window;           /* 0: none; W > 0: keys j with pos - W < j <= pos */
     float softcap;            /* 0: none; c > 0: s -> c tanh(s / c), after the scale */
     int32_t has_sink;         /* 1: sink[h] joins the softmax denominator of head h */
-    int32_t kv_dtype;         /* UAA_DTYPE_F32, _BF16 or _VQ8 */
+    int32_t kv_dtype;         /* UAA_DTYPE_F32, _BF16, _VQ8 or _Q8 */
     int32_t io_dtype;         /* q, k_new, v_new: UAA_DTYPE_F32 or _BF16 */
     int32_t out_dtype;        /* out: UAA_DTYPE_F32 or _BF16 */
     int32_t rotary_dim;       /* rotated dims per head: 0 (all D), or even, 2 <= R <= D */
@@ -154,12 +161,13 @@ typedef struct {
     const float* sink;        /* [Hq], required when has_sink */
     void* k_cache;            /* [B][Hkv][cap][D] */
     void* v_cache;            /* [B][Hkv][cap][D] */
-    float* v_scale;           /* [B][Hkv][cap], VQ8 only */
+    float* v_scale;           /* [B][Hkv][cap], VQ8 and Q8 */
     int32_t cache_capacity;   /* cap: slots per (sequence, kv head), a multiple of 4 */
     int32_t* seq_lens;        /* [B]: tokens cached before the step; the append adds 1 */
     int32_t max_seq_len;      /* host bound on seq_lens[b] before the step (+1 must fit cap) */
     void* out;                /* [B][Hq][D] out_dtype */
     float* q_rot;             /* optional [B][Hq][D] fp32: the normed, rotated q rows */
+    float* k_scale;           /* [B][Hkv][cap], Q8 only: the key rows' scales */
 } uaa_step_args;
 
 /* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed
@@ -177,7 +185,8 @@ typedef struct {
 /* Where each array lives in the workspace, and the split geometry. */
 typedef struct {
     int32_t n_ctas;           /* P: persistent CTAs of the partial step (stream-K ranges) */
-    int32_t stage_keys;       /* keys per ring stage: 64; at head_dim 64 128 (bf16), 256 (vq8) */
+    int32_t stage_keys;       /* keys per ring stage: 64; 128 for q8 at head_dim 128 / 256;
+                                 at head_dim 64 128 (bf16), 256 (vq8, q8) */
     int32_t heads_per_cta;    /* query heads of one unit (sequence, kv head, head group) */
     int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
     int32_t n_slices;         /* partial + combine launches (batch slices) */
@@ -217,14 +226,15 @@ uaa_status uaa_decode_attn_partial(const uaa_attn_desc* desc, const uaa_step_arg
 uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
-/* Steps 1 and 2 on one stream. For bf16 and vq8 caches this is one kernel: each
+/* Steps 1 and 2 on one stream. For bf16, vq8 and q8 caches this is one kernel: each
  * unit normalises and rotates its q rows in registers (the workspace's q rows
  * are not written), the warp that owns slot seq_lens[b] of a unit's last key
  * stage forms the new k and v rows and writes them over that slot of the
  * loaded stage (and, once per kv head, into the cache), and the last CTA to
  * have read the lengths advances seq_lens. Results, cache rows and seq_lens are
  * those of uaa_rope_qk_norm_append followed by uaa_decode_attn_partial, up to
- * fp32 rounding order (appended key rows within one bf16 ulp). For fp32 caches
+ * fp32 rounding order (appended key rows within one bf16 ulp, or one q8 code
+ * where the rotated key lies within fp32 rounding of a rounding tie). For fp32 caches
  * it is those two launches. Follow it with uaa_decode_attn_combine. */
 uaa_status uaa_decode_attn_append_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
                                           const uaa_workspace* ws, cudaStream_t stream);
@@ -252,7 +262,7 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch,
 
 /* Quantise n_rows rows of head_dim values (fp32 or bf16, v_dtype) to the vq8
  * storage: codes = rint(v / s) with s = max|v| / 127 in fp32 (the append's rule).
- * Used to fill a vq8 cache from existing values. */
+ * Used to fill a vq8 cache from existing values, and the keys of a q8 cache. */
 uaa_status uaa_vq8_quantize(const void* v, int32_t v_dtype, int64_t n_rows, int32_t head_dim,
                             int8_t* codes, float* scales, cudaStream_t stream);
 

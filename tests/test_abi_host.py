@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 6
+    assert B.uaa_abi_version() == 7
 
 
 def good_desc(**kw):
@@ -141,7 +141,9 @@ def test_workspace_layout_is_consistent(L, name):
             per_sm = 4 if kernel == 0 else (1 if layer["head_dim"] == 256 else 2)
             assert lay.kernel == kernel and lay.n_ctas == n_sm * per_sm
             d64 = kernel == 1 and layer["head_dim"] == 64
-            assert lay.stage_keys == ((256 if layer["kv_dtype"] == "vq8" else 128) if d64 else 64)
+            int8 = layer["kv_dtype"] in ("vq8", "q8")
+            want = (256 if int8 else 128) if d64 else (128 if layer["kv_dtype"] == "q8" else 64)
+            assert lay.stage_keys == want
             assert lay.n_slices == -(-batch // lay.slice_batch) and lay.slice_batch <= 1024
             Hq, D, HC, P = layer["n_q_heads"], layer["head_dim"], lay.heads_per_cta, lay.n_ctas
             assert lay.prefix_offset >= lay.q_rot_offset + batch * Hq * D * 4

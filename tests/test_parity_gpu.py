@@ -61,9 +61,12 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
     a = oracle_arrays(case, oracle_mod)
     layer = gpu_layer(case)
     kv = cfg.get("kv_dtype", "bf16")
-    if kv == "vq8":  # both quantisers on the same fp32 values
+    if kv in ("vq8", "q8"):  # both quantisers on the same fp32 values
         assert np.array_equal(layer.v_cache.cpu().numpy(), a["v_cache"])
         assert np.array_equal(layer.v_scale.cpu().numpy().view(np.uint32), a["v_scale"].view(np.uint32))
+    if kv == "q8":
+        assert np.array_equal(layer.k_cache.cpu().numpy(), a["k_cache"])
+        assert np.array_equal(layer.k_scale.cpu().numpy().view(np.uint32), a["k_scale"].view(np.uint32))
     B_, Hq, D = cfg["batch"], cfg["n_q_heads"], cfg["head_dim"]
     worst = (0.0, 0.0)
     for step in range(steps):
@@ -87,8 +90,9 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
             assert hdr[0] == 0x42414c31 and hdr[1] == lay.n_ctas and hdr[2] >= 1
         qr = oracle_mod.append(cfg, W.bits(inp["q"]).copy(), W.bits(inp["k_new"]).copy(),
                                W.bits(inp["v_new"]).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
-                               a["v_cache"], a["v_scale"], a["seq_lens"])
-        want = oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"])
+                               a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
+        want = oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"],
+                                 k_scale=a["k_scale"])
         # positions / slots: bit-exact
         assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
         assert layer.device_status() == 0
@@ -98,7 +102,19 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         for b in range(B_):
             slot = int(pre[b])
             kg = f64(layer.k_cache[b, :, slot].float())
-            if kv == "f32":
+            if kv == "q8":
+                # codes of the rotated key: the GPU rotates in fp32, the oracle in fp64, so a
+                # code may differ by one where k / s lies within rounding of a tie; the scale
+                # (max |k| / 127) by the fp32 rotation's relative error
+                kcg, kco = kg.astype(np.int64), a["k_cache"][b, :, slot].astype(np.int64)
+                ksg, kso = f64(layer.k_scale[b, :, slot]), a["k_scale"][b, :, slot].astype(np.float64)
+                assert np.abs(kcg - kco).max() <= 1, "q8 key code off by more than one"
+                assert (kcg != kco).sum() <= max(2, kco.size // 100), "q8 key codes differ beyond rounding ties"
+                assert np.allclose(ksg, kso, rtol=2e-6, atol=0), "q8 key scale beyond fp32 rounding"
+                assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
+                assert np.array_equal(layer.v_scale[b, :, slot].cpu().numpy().view(np.uint32),
+                                      a["v_scale"][b, :, slot].view(np.uint32))
+            elif kv == "f32":
                 ko = a["k_cache"][b, :, slot].astype(np.float64)
                 assert np.allclose(kg, ko, rtol=1e-5, atol=1e-6)
                 assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
@@ -130,6 +146,7 @@ SMALL = {
     "gemma2_9b_swa": dict(overrides=dict(batch=2, seq_len=5000), lens=[3000, 4999]),
     "gptoss_vq8_sink": dict(overrides=dict(batch=3, seq_len=4096), lens=[100, 1000, 4095]),
     "gemma3_12b_local_global": dict(overrides=dict(batch=3, seq_len=(1, 3000)), lens=[2999, 1023, 5]),
+    "llama31_8b_q8": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
 }
 
 
@@ -176,6 +193,19 @@ EDGE = [
                                                          norm_offset=True, norm_w_range=(-0.5, 0.5)), [299, 5]),
     ("d256-rotary64-linear", "gemma3_12b_local_global", dict(batch=2, seq_len=600, rotary_dim=64, layers=None),
      [599, 10]),
+    # q8 cache (int8 keys and values) at every head_dim and both head tilings
+    ("q8-first-token", "llama31_8b_q8", dict(batch=3, seq_len=200), [0, 1, 63]),
+    ("q8-d64-sink-yarn", "gptoss_vq8_sink", dict(batch=2, kv_dtype="q8", seq_len=500), [499, 64]),
+    ("q8-d64-g16", "gptoss_vq8_sink", dict(batch=2, kv_dtype="q8", n_q_heads=32, n_kv_heads=2, seq_len=300),
+     [299, 5]),
+    ("q8-d128-g16-qknorm", "qwen3_8b_ragged", dict(batch=3, kv_dtype="q8", n_q_heads=32, n_kv_heads=2,
+                                                   seq_len=(1, 700)), [1, 129, 700]),
+    ("q8-d256-window-softcap", "gemma2_9b_swa", dict(batch=2, kv_dtype="q8", seq_len=600,
+                                                     layers=[dict(window=100)]), [599, 40]),
+    ("q8-f32-io-interleaved", "llama31_8b_q8", dict(batch=2, io_dtype="f32", rope_style="interleaved",
+                                                    seq_len=300), [299, 0]),
+    ("q8-rotary96-norm-offset", "qwen3_8b_ragged", dict(batch=2, kv_dtype="q8", rotary_dim=96, norm_offset=True,
+                                                        norm_w_range=(-0.5, 0.5), seq_len=300), [299, 77]),
     ("d64-vq8-norm-offset-local", "gemma3_12b_local_global",
      dict(batch=2, seq_len=600, head_dim=64, kv_dtype="vq8", layers=[dict(window=100, rope_theta=10000.0,
                                                                           rope_scaling="none")]), [599, 40]),
@@ -398,7 +428,7 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry
 # ------------------------------------------------------------------ full size, sampled
 
 FULL = ["llama32_1b_tiny", "llama31_8b_decode", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink",
-        "gemma3_12b_local_global"]
+        "gemma3_12b_local_global", "llama31_8b_q8"]
 
 
 @pytest.mark.slow
@@ -416,16 +446,16 @@ def test_full_size_sampled(oracle_mod, name):
         out = layer.out.cpu().numpy()
         a = oracle_arrays(case, oracle_mod)
         qr = oracle_mod.append(layer_cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"],
-                               a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"])
+                               a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
         assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
         assert layer.device_status() == 0
         Bn, Hq = layer_cfg["batch"], layer_cfg["n_q_heads"]
         units = sorted({(int(rng.integers(Bn)), int(rng.integers(Hq))) for _ in range(24)} | {(0, 0), (Bn - 1, Hq - 1)})
         want = oracle_mod.attend(layer_cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"],
-                                 a["seq_lens"], units=units)
+                                 a["seq_lens"], units=units, k_scale=a["k_scale"])
         got = np.stack([out[b, h] for b, h in units])
         assert_out_close(got, want, name)
-        if layer_cfg["kv_dtype"] == "vq8":
+        if layer_cfg["kv_dtype"] in ("vq8", "q8"):
             pre = case["lens"].numpy()
             for b in range(Bn):
                 assert np.array_equal(layer.v_cache[b, :, pre[b]].cpu().numpy(), a["v_cache"][b, :, pre[b]])
