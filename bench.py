@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 from gqa_attention_kv_qk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (% of GB300 peak) and decode steps/sec at 1 GPU"
-DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64}
+DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_paged": 64}
 
 
 def measured_peaks() -> dict:

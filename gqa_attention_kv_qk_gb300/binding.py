@@ -21,6 +21,7 @@ UAA_ERR_DEVICE = 5
 UAA_DEVFLAG_CAPACITY = 0x1
 UAA_DEVFLAG_LEN_HINT = 0x2
 UAA_DEVFLAG_TIMEOUT = 0x4
+UAA_DEVFLAG_PAGE = 0x8
 
 ROPE_STYLE = {"neox": 0, "interleaved": 1}
 ROPE_SCALING = {"none": 0, "llama3": 1, "yarn": 2, "linear": 3}
@@ -52,7 +53,9 @@ class UaaStepArgs(ctypes.Structure):
                 ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("cache_capacity", ctypes.c_int32),
                 ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
-                ("out", ctypes.c_void_p), ("q_rot", ctypes.c_void_p), ("k_scale", ctypes.c_void_p)]
+                ("out", ctypes.c_void_p), ("q_rot", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
+                ("pages_per_seq", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
 
 
 class UaaWorkspace(ctypes.Structure):

@@ -215,9 +215,27 @@ uaa_status check_args(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     if ((long long)a->max_seq_len + 1 > a->cache_capacity)
         return fail(UAA_ERR_CAPACITY, "max_seq_len=%d + 1 new token does not fit cache_capacity=%d",
                     a->max_seq_len, a->cache_capacity);
-    if ((long long)a->batch * d->n_kv_heads * a->cache_capacity > 2147483647LL - 2 * uaa::kTileKeys)
+    if (a->block_table) {
+        const int ps = a->page_size;
+        if (ps < 16 || ps > 4096 || (ps & (ps - 1)) != 0)
+            return fail(UAA_ERR_UNSUPPORTED, "page_size=%d is not a power of two in [16, 4096]", ps);
+        // a page's scales are one TMA box of a stage; its shared-memory destination
+        // (4 bytes per key) must start on 128 bytes
+        if (ps < 32 && (d->kv_dtype == UAA_DTYPE_VQ8 || d->kv_dtype == UAA_DTYPE_Q8))
+            return fail(UAA_ERR_UNSUPPORTED, "page_size=%d is below 32, the smallest page of a vq8 / q8 cache", ps);
+        if (a->pages_per_seq <= 0 || (long long)a->pages_per_seq * ps != a->cache_capacity)
+            return fail(UAA_ERR_INVALID_ARGUMENT,
+                        "cache_capacity=%d is not pages_per_seq=%d x page_size=%d", a->cache_capacity,
+                        a->pages_per_seq, ps);
+        if (a->n_pages <= 0) return fail(UAA_ERR_INVALID_ARGUMENT, "n_pages=%d is not positive", a->n_pages);
+        if ((long long)a->n_pages * d->n_kv_heads * ps > 2147483647LL - 2 * uaa::kTileKeys)
+            return fail(UAA_ERR_UNSUPPORTED, "n_pages*n_kv_heads*page_size=%lld exceeds 2^31 cache rows",
+                        (long long)a->n_pages * d->n_kv_heads * ps);
+        if (!aligned16(a->block_table)) return fail(UAA_ERR_INVALID_ARGUMENT, "block_table is not 16-byte aligned");
+    } else if ((long long)a->batch * d->n_kv_heads * a->cache_capacity > 2147483647LL - 2 * uaa::kTileKeys) {
         return fail(UAA_ERR_UNSUPPORTED, "batch*n_kv_heads*cache_capacity=%lld exceeds 2^31 cache rows",
                     (long long)a->batch * d->n_kv_heads * a->cache_capacity);
+    }
     struct {
         const void* p;
         const char* name;
@@ -268,6 +286,21 @@ float softmax_scale(const uaa_attn_desc* d)
 
 // The prescale of the rotated q rows: logits come out in the log2 domain
 // (scale log2 e), or as s / c when a softcap c applies tanh to them first.
+// The paging of a step's caches (KvPages in internal.cuh).
+uaa::KvPages pages_of(const uaa_step_args* a)
+{
+    uaa::KvPages pg{};
+    if (a->block_table) {
+        pg.table = a->block_table;
+        int shift = 0;
+        while ((1 << shift) < a->page_size) ++shift;
+        pg.shift = shift;
+        pg.per_seq = a->pages_per_seq;
+        pg.n_pages = a->n_pages;
+    }
+    return pg;
+}
+
 float qscale(const uaa_attn_desc* d)
 {
     const float scale = softmax_scale(d);
@@ -389,6 +422,7 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.v_cache = a->v_cache;
     p.v_scale = a->v_scale;
     p.k_scale = a->k_scale;
+    p.pages = pages_of(a);
     p.seq_lens = a->seq_lens;
     char* w = static_cast<char*>(ws->ptr);
     p.q_prime = reinterpret_cast<float*>(w + pl.off_qrot);
@@ -409,9 +443,16 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
     CUtensorMap tk, tv, ts, tks;
     if (pl.kernel == 1) {
-        const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
-        const uint32_t tk_rows = (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype);  // box height
-        const uint64_t heads = (uint64_t)a->batch * d->n_kv_heads;
+        // contiguous caches: one box of a whole stage per row kind; paged caches: the
+        // pools, and one box per page-aligned sub-tile of min(64, page_size) keys
+        const bool paged = a->block_table != nullptr;
+        const uint64_t rows = paged ? (uint64_t)a->n_pages * d->n_kv_heads * a->page_size
+                                    : (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
+        const uint32_t tk_rows =
+            paged ? (uint32_t)(a->page_size < uaa::kTileKeys ? a->page_size : uaa::kTileKeys)
+                  : (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype);  // box height
+        const uint64_t heads = paged ? (uint64_t)a->n_pages * d->n_kv_heads : (uint64_t)a->batch * d->n_kv_heads;
+        const uint64_t scale_inner = paged ? (uint64_t)a->page_size : (uint64_t)a->cache_capacity;
         // int8 codes: boxes of tk_rows x min(D, 128) bytes, swizzled like the bf16 boxes so
         // the kernel's ldmatrix reads on them are free of bank conflicts; scales: one
         // tk_rows-float box per stage
@@ -420,8 +461,8 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         if (d->kv_dtype == UAA_DTYPE_Q8) {
             UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->k_cache, D, rows, D, code_box, tk_rows, code_sw,
                               "k_cache codes"));
-            UAA_TRY(encode_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->k_scale, a->cache_capacity, heads,
-                              (uint64_t)a->cache_capacity * 4, tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "k_scale"));
+            UAA_TRY(encode_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->k_scale, scale_inner, heads, scale_inner * 4,
+                              tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "k_scale"));
         } else {
             UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
                               CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
@@ -429,8 +470,8 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         if (d->kv_dtype == UAA_DTYPE_VQ8 || d->kv_dtype == UAA_DTYPE_Q8) {
             UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, code_box, tk_rows, code_sw,
                               "v_cache codes"));
-            UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, a->cache_capacity, heads,
-                              (uint64_t)a->cache_capacity * 4, tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
+            UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, scale_inner, heads, scale_inner * 4,
+                              tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
         } else {
             UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, tk_rows,
                               CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
@@ -459,6 +500,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.v_cache = a->v_cache;
         p.v_scale = a->v_scale;
         p.k_scale = a->k_scale;
+        p.pages = pages_of(a);
         p.seq_lens = a->seq_lens + b0;
         p.prefix = reinterpret_cast<int*>(w + pl.off_prefix + sl * pl.prefix_stride);
         p.ranges = reinterpret_cast<long long*>(w + pl.off_ranges + sl * pl.ranges_stride);

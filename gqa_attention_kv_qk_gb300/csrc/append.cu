@@ -101,12 +101,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
         const int head = is_q ? r : (is_k ? r - p.Hq : r - p.Hq - p.Hkv);
         const size_t in_row = (static_cast<size_t>(b) * (is_q ? p.Hq : p.Hkv) + head) * D;
 
-        const size_t slot = ((static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos) * D;
+        // the new token's cache row (k and v rows; -1: a paged table entry out of range)
+        const long long crow = is_q || !fits ? 0 : cache_row(p.pages, p.Hkv, p.cap, b, head, pos);
+        const bool stores = fits && crow >= 0;
+        if (!is_q && fits && crow < 0 && lane == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
+        const size_t slot = static_cast<size_t>(crow) * D;
         if (!is_q && !is_k) {  // value row: stored as given (or quantised)
-            if (!fits) continue;
+            if (!stores) continue;
             if (p.kv_dtype == UAA_DTYPE_VQ8 || p.kv_dtype == UAA_DTYPE_Q8) {
-                quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot,
-                                  p.v_scale + (static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos);
+                quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot, p.v_scale + crow);
             } else {
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) store_kv(p.v_cache, p.kv_dtype, slot + lane + 32 * i, x[i]);
@@ -141,10 +144,10 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                     p.q_rot_out[in_row + ia] = ya;
                     p.q_rot_out[in_row + ib] = yb;
                 }
-            } else if (fits && p.kv_dtype == UAA_DTYPE_Q8) {  // the whole rotated row first: its scale
-                rowbuf[warp][ia] = ya;                          // needs max |k| (pairs are disjoint)
+            } else if (stores && p.kv_dtype == UAA_DTYPE_Q8) {  // the whole rotated row first: its scale
+                rowbuf[warp][ia] = ya;                            // needs max |k| (pairs are disjoint)
                 rowbuf[warp][ib] = yb;
-            } else if (fits) {
+            } else if (stores) {
                 store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
                          slot + ia, ya);
                 store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
@@ -152,12 +155,11 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
             }
         }
         __syncwarp();
-        if (is_k && fits && p.kv_dtype == UAA_DTYPE_Q8) {  // q8 key: codes and scale of the rotated row
+        if (is_k && stores && p.kv_dtype == UAA_DTYPE_Q8) {  // q8 key: codes and scale of the rotated row
             float y[EPL];
 #pragma unroll
             for (int i = 0; i < EPL; ++i) y[i] = rowbuf[warp][lane + 32 * i];
-            quantize_row<EPL>(y, lane, static_cast<int8_t*>(p.k_cache) + slot,
-                              p.k_scale + (static_cast<size_t>(b) * p.Hkv + head) * p.cap + pos);
+            quantize_row<EPL>(y, lane, static_cast<int8_t*>(p.k_cache) + slot, p.k_scale + crow);
             __syncwarp();  // the row is read before the next one overwrites it
         }
     }

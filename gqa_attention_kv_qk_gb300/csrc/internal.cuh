@@ -18,6 +18,18 @@ constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at the top SM cloc
 
 // ---------------------------------------------------------------- parameters
 
+// Where the cache rows of a step live. Contiguous caches (table null): row
+// (b Hkv + g) cap + j holds position j of sequence b, kv head g. Paged caches:
+// position j is slot j mod ps of the sequence's logical page j / ps, which
+// table[b][j / ps] maps to a physical page of the pool [n_pages][Hkv][ps]:
+// row (page Hkv + g) ps + j mod ps (scales: the same row of [n_pages Hkv][ps]).
+struct KvPages {
+    const int* table;   // [B][per_seq] physical page per logical page, or null
+    int shift;          // log2(ps)
+    int per_seq;        // row length of the table
+    int n_pages;        // pages in the pool
+};
+
 struct AppendParams {
     int B, Hq, Hkv, D;
     int cap, max_len;
@@ -38,6 +50,7 @@ struct AppendParams {
     void* v_cache;
     float* v_scale;
     float* k_scale;         // q8 caches: the key rows' scales
+    KvPages pages;
     int* seq_lens;
     float* q_prime;         // workspace [B][Hq][D]
     float* q_rot_out;       // optional [B][Hq][D]
@@ -108,6 +121,7 @@ struct PartialParams {
     void* v_cache;
     float* v_scale;
     float* k_scale;         // q8 caches: the key rows' scales
+    KvPages pages;          // table rows are indexed with b_off + b
     int* seq_lens;          // slice-relative (advanced by the fused kernel only)
     int* prefix;            // [B + 1] stage prefix over sequences, written for the combine
     long long* ranges;      // [P' + 1] range starts, written for the combine
@@ -445,6 +459,17 @@ __device__ __forceinline__ int2 rope_pair(int pp, int half_rot, int D, bool neox
 {
     if (!neox) return make_int2(2 * pp, 2 * pp + 1);
     return pp < half_rot ? make_int2(pp, pp + half_rot) : make_int2(pp + half_rot, pp + D / 2);
+}
+
+// Cache row of (sequence b, kv head g, position j) under KvPages, or -1 where
+// a paged table entry lies outside [0, n_pages) (the caller flags
+// UAA_DEVFLAG_PAGE and neither reads nor writes that row).
+__device__ __forceinline__ long long cache_row(const KvPages& pg, int Hkv, int cap, int b, int g, int j)
+{
+    if (!pg.table) return (static_cast<long long>(b) * Hkv + g) * cap + j;
+    const int page = __ldg(pg.table + static_cast<size_t>(b) * pg.per_seq + (j >> pg.shift));
+    if (page < 0 || page >= pg.n_pages) return -1;
+    return ((static_cast<long long>(page) * Hkv + g) << pg.shift) | (j & ((1 << pg.shift) - 1));
 }
 
 // Rotation of pair (a, b) by the angle whose (cos, sin) is cs.

@@ -75,21 +75,24 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
             for (int i = 0; i < EPL; ++i) o[h][i] = 0.f;
         }
 
-        const size_t rows0 = (static_cast<size_t>(p.b_off + sg.b) * p.Hkv + sg.kvh) * p.cap;
-        const float* K = static_cast<const float*>(p.k_cache) + rows0 * D;
-        const float* V = static_cast<const float*>(p.v_cache) + rows0 * D;
+        const float* K = static_cast<const float*>(p.k_cache);
+        const float* V = static_cast<const float*>(p.v_cache);
         // warp w takes blocks of KB consecutive keys round-robin; a block's rows are
         // all loaded before the first is used (one memory round trip per block)
         for (int jb = j_beg + warp * KB; jb < j_end; jb += kSimtWarps * KB) {
             float kx[KB][EPL], vx[KB][EPL];
 #pragma unroll
-            for (int u = 0; u < KB; ++u)
+            for (int u = 0; u < KB; ++u) {
+                // the key's cache row (paged: through the block table; -1 reads as zeros)
+                const long long row =
+                    jb + u < j_end ? cache_row(p.pages, p.Hkv, p.cap, p.b_off + sg.b, sg.kvh, jb + u) : -1;
+                if (jb + u < j_end && row < 0 && lane == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
-                    const bool ok = jb + u < j_end;
-                    kx[u][i] = ok ? K[static_cast<size_t>(jb + u) * D + lane + 32 * i] : 0.f;
-                    vx[u][i] = ok ? V[static_cast<size_t>(jb + u) * D + lane + 32 * i] : 0.f;
+                    kx[u][i] = row >= 0 ? K[static_cast<size_t>(row) * D + lane + 32 * i] : 0.f;
+                    vx[u][i] = row >= 0 ? V[static_cast<size_t>(row) * D + lane + 32 * i] : 0.f;
                 }
+            }
 #pragma unroll
             for (int u = 0; u < KB; ++u) {
                 if (jb + u >= j_end) break;

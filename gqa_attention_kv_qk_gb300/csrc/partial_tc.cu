@@ -105,6 +105,9 @@ struct Shape {
     static constexpr int kVBoxes = kVQ8 ? kCodeBoxes : D / 64;
     static constexpr int kKBytes = kKQ8 ? kTK * D : kTK * D * 2;
     static constexpr int kVBytes = kVQ8 ? kTK * D : kTK * D * 2;
+    // bytes per row inside one box: 64 for int8 code rows at head_dim 64, else 128
+    static constexpr int kKRow = kKQ8 && D == 64 ? 64 : 128;
+    static constexpr int kVRow = kVQ8 && D == 64 ? 64 : 128;
     // a stage: keys | values | value scales (int8 values) | key scales (int8 keys)
     static constexpr int kVScaleOff = kKBytes + kVBytes;
     static constexpr int kKScaleOff = kVScaleOff + (kVQ8 ? kTK * 4 : 0);
@@ -388,7 +391,12 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
     constexpr int NP = D / 64;   // rotation pairs per lane
     constexpr int EPL = D / 32;  // values per lane
     const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D;
-    const size_t slot = (static_cast<size_t>(p.b_off + b) * p.Hkv + kvh) * p.cap + L;
+    const long long crow = cache_row(p.pages, p.Hkv, p.cap, p.b_off + b, kvh, L);
+    if (crow < 0) {  // a paged table entry out of range: the rows are staged, not stored
+        if (store && lane == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
+        store = false;
+    }
+    const size_t slot = crow < 0 ? 0 : static_cast<size_t>(crow);
     float ka[NP], kb[NP], v[EPL];
     int ia[NP], ib[NP];
     float ss = 0.f;
@@ -488,6 +496,25 @@ __device__ __noinline__ void count_in_and_advance(const PartialParams& p, const 
     __threadfence();
     for (int b = 0; b < p.B; ++b)
         if (lens[b] >= 0 && lens[b] < p.cap) p.seq_lens[b] = lens[b] + 1;
+}
+
+// Producer: the TMA loads of `n` consecutive cache rows starting at row y (key
+// and value rows, their scales at (sx, sy) of the scale tensors) into rows r0 ..
+// r0 + n - 1 of a stage; n is the tensor maps' box height.
+template <class SH>
+__device__ __forceinline__ void issue_rows(uint32_t st, int r0, const CUtensorMap* tk, const CUtensorMap* tv,
+                                           const CUtensorMap* ts, const CUtensorMap* tks, int y, int sx, int sy,
+                                           uint32_t bar, uint64_t policy)
+{
+#pragma unroll
+    for (int c = 0; c < SH::kKBoxes; ++c)
+        ptx::tma_load_2d_hint(st + c * SH::kBoxBytes + r0 * SH::kKRow, tk, c * (SH::kKQ8 ? 128 : 64), y, bar, policy);
+    if (SH::kKQ8) ptx::tma_load_2d_hint(st + SH::kKScaleOff + 4 * r0, tks, sx, sy, bar, policy);
+#pragma unroll
+    for (int c = 0; c < SH::kVBoxes; ++c)
+        ptx::tma_load_2d_hint(st + SH::kKBytes + c * SH::kBoxBytes + r0 * SH::kVRow, tv, c * (SH::kVQ8 ? 128 : 64),
+                              y, bar, policy);
+    if (SH::kVQ8) ptx::tma_load_2d_hint(st + SH::kVScaleOff + 4 * r0, ts, sx, sy, bar, policy);
 }
 
 // Owner warp of the new key: the staged rows over row r of the loaded stage.
@@ -626,7 +653,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c,
                                               p.fused != 0);
                 const int head_row = (p.b_off + sg.b) * p.Hkv + sg.kvh;
-                const int row0 = head_row * p.cap;
+                const int row0 = p.pages.table ? 0 : head_row * p.cap;  // contiguous caches
                 const int t0 = sg.lo / kTileKeys;
                 for (int k = 0; k < sg.n_st; ++k, ++it) {
                     const int s = it % SH::kStages;
@@ -651,24 +678,26 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     const uint32_t bar = bar_full + 8 * s;
                     ptx::mbar_arrive_expect_tx(bar, SH::kTxBytes);
                     const int key = (t0 + MG * (sg.st0 + k)) * kTileKeys;
-                    const int y = row0 + key;
-#pragma unroll
-                    for (int c = 0; c < SH::kKBoxes; ++c)
-                        ptx::tma_load_2d_hint(st + c * SH::kBoxBytes, &tm_k, c * (KQ8 ? 128 : 64), y, bar,
-                                              stream_policy);
-                    if (KQ8)
-                        ptx::tma_load_2d_hint(st + SH::kKScaleOff, &tm_ks, key, head_row, bar, stream_policy);
-                    if (VQ8) {
-#pragma unroll
-                        for (int c = 0; c < SH::kVBoxes; ++c)
-                            ptx::tma_load_2d_hint(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 128, y, bar,
-                                                  stream_policy);
-                        ptx::tma_load_2d_hint(st + SH::kVScaleOff, &tm_s, key, head_row, bar, stream_policy);
+                    if (!p.pages.table) {
+                        issue_rows<SH>(st, 0, &tm_k, &tm_v, &tm_s, &tm_ks, row0 + key, key, head_row, bar,
+                                       stream_policy);
                     } else {
-#pragma unroll
-                        for (int c = 0; c < SH::kVBoxes; ++c)
-                            ptx::tma_load_2d_hint(st + SH::kKBytes + c * SH::kBoxBytes, &tm_v, c * 64, y, bar,
-                                                  stream_policy);
+                        // paged: one load per page-aligned sub-tile; a sub-tile with no visible key
+                        // (beyond the unit's end or before its window) is not looked up and reads
+                        // as zeros from a negative row (masked by the consumers)
+                        const int sub = min(1 << p.pages.shift, kTileKeys);
+                        for (int r0 = 0; r0 < TK; r0 += sub) {
+                            const int ku = key + r0;
+                            long long row = -1;
+                            if (ku < sg.hi && ku + sub > sg.lo) {
+                                row = cache_row(p.pages, p.Hkv, p.cap, p.b_off + sg.b, sg.kvh, ku);
+                                if (row < 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
+                            }
+                            const int ps_mask = (1 << p.pages.shift) - 1;
+                            issue_rows<SH>(st, r0, &tm_k, &tm_v, &tm_s, &tm_ks, row < 0 ? -sub : static_cast<int>(row),
+                                           row < 0 ? 0 : static_cast<int>(row & ps_mask),
+                                           row < 0 ? -1 : static_cast<int>(row >> p.pages.shift), bar, stream_policy);
+                        }
                     }
                 }
                 pos += sg.n_st;

@@ -20,7 +20,13 @@ def _require_cuda(device):
 
 
 class DecodeLayer:
-    def __init__(self, cfg: dict, batch: int, capacity: int, device="cuda"):
+    """page_size: store the caches as pools of pages of that many positions;
+    block_table ([batch][capacity / page_size] int32, default: sequence b takes
+    pages b P .. b P + P - 1) maps each sequence's logical pages to pool pages, of
+    which there are n_pages (default: just enough)."""
+
+    def __init__(self, cfg: dict, batch: int, capacity: int, device="cuda", page_size=None, block_table=None,
+                 n_pages=None):
         self.cfg = dict(cfg)
         self.device = _require_cuda(device)
         self.batch = int(batch)
@@ -29,18 +35,33 @@ class DecodeLayer:
         Hq, Hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
         kv = cfg.get("kv_dtype", "bf16")
         dev = self.device
+        self.page_size = int(page_size or 0)
+        if self.page_size:
+            if capacity % self.page_size:
+                raise ValueError(f"capacity {capacity} is not a multiple of page_size {self.page_size}")
+            self.pages_per_seq = capacity // self.page_size
+            if block_table is None:
+                block_table = torch.arange(batch * self.pages_per_seq, dtype=torch.int32).reshape(batch, -1)
+            self.block_table = torch.as_tensor(block_table, dtype=torch.int32).to(dev).contiguous()
+            assert self.block_table.shape == (batch, self.pages_per_seq)
+            self.n_pages = int(n_pages or batch * self.pages_per_seq)
+            rows = (self.n_pages, Hkv, self.page_size)  # pools of pages
+        else:
+            self.pages_per_seq = self.n_pages = 0
+            self.block_table = None
+            rows = (batch, Hkv, capacity)
         kdt = torch.float32 if kv == "f32" else torch.bfloat16
         if kv == "q8":
-            self.k_cache = torch.zeros((batch, Hkv, capacity, D), dtype=torch.int8, device=dev)
-            self.k_scale = torch.zeros((batch, Hkv, capacity), dtype=torch.float32, device=dev)
+            self.k_cache = torch.zeros((*rows, D), dtype=torch.int8, device=dev)
+            self.k_scale = torch.zeros(rows, dtype=torch.float32, device=dev)
         else:
-            self.k_cache = torch.zeros((batch, Hkv, capacity, D), dtype=kdt, device=dev)
+            self.k_cache = torch.zeros((*rows, D), dtype=kdt, device=dev)
             self.k_scale = None
         if kv in ("vq8", "q8"):
-            self.v_cache = torch.zeros((batch, Hkv, capacity, D), dtype=torch.int8, device=dev)
-            self.v_scale = torch.zeros((batch, Hkv, capacity), dtype=torch.float32, device=dev)
+            self.v_cache = torch.zeros((*rows, D), dtype=torch.int8, device=dev)
+            self.v_scale = torch.zeros(rows, dtype=torch.float32, device=dev)
         else:
-            self.v_cache = torch.zeros((batch, Hkv, capacity, D), dtype=kdt, device=dev)
+            self.v_cache = torch.zeros((*rows, D), dtype=kdt, device=dev)
             self.v_scale = None
         self.seq_lens = torch.zeros((batch,), dtype=torch.int32, device=dev)
         self.max_len_hint = 0
@@ -58,25 +79,49 @@ class DecodeLayer:
         to = lambda t: None if t is None else t.to(device=self.device, dtype=torch.float32).contiguous()
         self.q_norm_w, self.k_norm_w, self.sink = to(q_norm_w), to(k_norm_w), to(sink)
 
+    def _to_pool(self, logical, pool):
+        """Logical rows [B][Hkv][cap][...] into a pool [n_pages][Hkv][page_size][...]."""
+        Bn, Hkv, ps, P = self.batch, logical.shape[1], self.page_size, self.pages_per_seq
+        rest = tuple(logical.shape[3:])
+        x = logical.reshape(Bn, Hkv, P, ps, *rest).transpose(1, 2).reshape(Bn * P, Hkv, ps, *rest)
+        pool.index_copy_(0, self.block_table.reshape(-1).long(), x.to(device=pool.device, dtype=pool.dtype))
+
+    def logical(self, name: str):
+        """A cache tensor ("k_cache", "v_cache", "k_scale", "v_scale") as logical
+        rows [B][Hkv][cap][...] (a gathered copy for a paged layer)."""
+        t = getattr(self, name)
+        if t is None or not self.page_size:
+            return t
+        Bn, P, ps = self.batch, self.pages_per_seq, self.page_size
+        x = t.index_select(0, self.block_table.reshape(-1).long())
+        Hkv, rest = x.shape[1], tuple(x.shape[3:])
+        return x.reshape(Bn, P, Hkv, ps, *rest).transpose(1, 2).reshape(Bn, Hkv, P * ps, *rest)
+
     def load_cache(self, k, v, lens):
-        """Copy host caches in. For a vq8 layer `v` holds fp32 values, and for a q8
-        layer `k` too, quantised on the device by uaa_vq8_quantize (the append's
-        own rule)."""
+        """Copy host caches (logical rows [B][Hkv][cap][D]) in. For a vq8 layer `v`
+        holds fp32 values, and for a q8 layer `k` too, quantised on the device by
+        uaa_vq8_quantize (the append's own rule)."""
         D = self.cfg["head_dim"]
+        s = torch.cuda.current_stream(self.device)
 
-        def quantize(vals, codes, scales):
-            vals = vals.to(device=self.device, dtype=torch.float32).contiguous()
-            B.uaa_vq8_quantize(vals.data_ptr(), B.DTYPE["f32"], vals.numel() // D, D, codes.data_ptr(),
-                               scales.data_ptr(), torch.cuda.current_stream(self.device))
+        def put(vals, cache, scales):
+            if scales is not None:  # codes and scales of the logical rows, then into place
+                vals = vals.to(device=self.device, dtype=torch.float32).contiguous()
+                codes = torch.empty(vals.shape, dtype=torch.int8, device=self.device)
+                sc = torch.empty(vals.shape[:-1], dtype=torch.float32, device=self.device)
+                B.uaa_vq8_quantize(vals.data_ptr(), B.DTYPE["f32"], vals.numel() // D, D, codes.data_ptr(),
+                                   sc.data_ptr(), s)
+                pairs = ((codes, cache), (sc, scales))
+            else:
+                pairs = ((vals, cache),)
+            for src, dst in pairs:
+                if self.page_size:
+                    self._to_pool(src.to(self.device), dst)
+                else:
+                    dst.copy_(src)
 
-        if self.k_scale is not None:
-            quantize(k, self.k_cache, self.k_scale)
-        else:
-            self.k_cache.copy_(k)
-        if self.v_scale is not None:
-            quantize(v, self.v_cache, self.v_scale)
-        else:
-            self.v_cache.copy_(v)
+        put(k, self.k_cache, self.k_scale)
+        put(v, self.v_cache, self.v_scale)
         lens = torch.as_tensor(lens, dtype=torch.int32)
         self.seq_lens.copy_(lens)
         self.max_len_hint = int(lens.max()) if lens.numel() else 0
@@ -111,6 +156,9 @@ class DecodeLayer:
         a.out = B.ptr(self.out if out is None else out)
         a.q_rot = B.ptr(q_rot)
         a.k_scale = B.ptr(self.k_scale)
+        if self.page_size:
+            a.block_table = B.ptr(self.block_table)
+            a.page_size, a.pages_per_seq, a.n_pages = self.page_size, self.pages_per_seq, self.n_pages
         return a
 
     def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True, q_rot=None, out=None):

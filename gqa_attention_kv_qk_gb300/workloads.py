@@ -23,7 +23,8 @@ TILE = 64  # cache capacities are rounded up to a multiple of this many slots
 
 # The workloads. Method keys follow the oracle / library vocabulary;
 # workload keys: batch, seq_len (int, or (lo, hi) inclusive for ragged lengths),
-# steps, seed, layers (per-layer overrides; one cache per layer).
+# steps, seed, layers (per-layer overrides; one cache per layer), page_size (a
+# paged cache: pages of that many positions, assigned by block_table below).
 CONFIGS: dict[str, dict] = {
     # Tiny Llama-3.2-1B-like step: fp32 everything, seed 0.
     "llama32_1b_tiny": dict(
@@ -63,6 +64,13 @@ CONFIGS: dict[str, dict] = {
         kv_dtype="q8", io_dtype="bf16", out_dtype="f32",
         rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
         low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
+    # The Llama-3.1-8B-like decode over a paged bf16 cache: pages of 16 positions,
+    # in seeded random order over a pool with spare pages.
+    "llama31_8b_paged": dict(
+        batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, seq_len=8192, steps=64, seed=7,
+        kv_dtype="bf16", io_dtype="bf16", out_dtype="f32", page_size=16,
+        rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
+        low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
     # Gemma-3-12B-like decode: QK RMSNorm whose weights are stored as deltas from
     # one (applied as 1 + w), scale 1/sqrt(256), no softcap; one layer of each
     # kind per step (the model runs five local layers per global one): a local
@@ -77,7 +85,7 @@ CONFIGS: dict[str, dict] = {
 }
 
 _TAGS = {"q": 1, "k_new": 2, "v_new": 3, "k_cache": 4, "v_cache": 5, "q_norm_w": 6,
-         "k_norm_w": 7, "sink": 8, "seq_lens": 9}
+         "k_norm_w": 7, "sink": 8, "seq_lens": 9, "block_table": 10}
 
 
 def config(name: str, **overrides) -> dict:
@@ -116,11 +124,22 @@ def _cast(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def capacity(cfg: dict, extra: int = 0) -> int:
-    """Slots per (sequence, kv head): the longest cached length + extra, rounded up."""
+    """Slots per (sequence, kv head): the longest cached length + extra, rounded up
+    to a multiple of 64 and of the page size of a paged workload."""
     sl = cfg["seq_len"]
     longest = sl[1] if isinstance(sl, (tuple, list)) else sl
     need = longest + max(extra, 1)
-    return (need + TILE - 1) // TILE * TILE
+    unit = max(TILE, int(cfg.get("page_size", 0) or 0))
+    return (need + unit - 1) // unit * unit
+
+
+def block_table(cfg: dict, pages_per_seq: int, n_pages: int) -> torch.Tensor:
+    """A paged workload's block table [B][pages_per_seq] int32: distinct pages of a
+    pool of n_pages, in seeded random order (the pool's other pages stay unused)."""
+    B = cfg["batch"]
+    assert n_pages >= B * pages_per_seq
+    perm = torch.randperm(n_pages, generator=_gen(cfg["seed"], "block_table", 0, cfg.get("layer", 0)))
+    return perm[: B * pages_per_seq].reshape(B, pages_per_seq).to(torch.int32)
 
 
 def seq_lens(cfg: dict) -> torch.Tensor:

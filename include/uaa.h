@@ -69,7 +69,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 7
+#define UAA_ABI_VERSION 8
 
 typedef enum {
     UAA_OK = 0,
@@ -100,6 +100,8 @@ typedef enum { UAA_DTYPE_F32 = 0, UAA_DTYPE_BF16 = 1, UAA_DTYPE_VQ8 = 2, UAA_DTY
 #define UAA_DEVFLAG_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up, or the workspace's
                                        scheduling state was left by such a launch; outputs are
                                        invalid until the workspace is zeroed again */
+#define UAA_DEVFLAG_PAGE 0x8u       /* a block_table entry outside [0, n_pages): that row was
+                                       neither written nor read (outputs of the sequence invalid) */
 
 /* Rotary embedding of the first R = rotary_dim dims of each head row (R = D when
  * the descriptor's rotary_dim is 0; the other D - R dims pass unchanged: the
@@ -168,6 +170,18 @@ typedef struct {
     void* out;                /* [B][Hq][D] out_dtype */
     float* q_rot;             /* optional [B][Hq][D] fp32: the normed, rotated q rows */
     float* k_scale;           /* [B][Hkv][cap], Q8 only: the key rows' scales */
+    /* Paged caches (a key and a value per head per position, in pages: llamay
+     * "What is refused" on what a KV page holds). block_table NULL: the caches
+     * are contiguous, [B][Hkv][cap][...]. Otherwise k_cache / v_cache are pools
+     * [n_pages][Hkv][page_size][D], v_scale / k_scale [n_pages][Hkv][page_size],
+     * position j of sequence b lives in slot j % page_size of physical page
+     * block_table[b][j / page_size], and cap = pages_per_seq * page_size. The
+     * table is read, never written; pages may be shared between sequences for
+     * reading (a step writes slot seq_lens[b] of its own page only). */
+    const int32_t* block_table; /* [B][pages_per_seq] int32, or NULL */
+    int32_t page_size;        /* keys per page: a power of two in [16, 4096]; >= 32 for VQ8 / Q8 */
+    int32_t pages_per_seq;    /* row length of block_table */
+    int32_t n_pages;          /* pages in each pool */
 } uaa_step_args;
 
 /* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed

@@ -59,7 +59,14 @@ def gpu_layer(case: dict, device="cuda"):
     """A DecodeLayer holding the case's cache (a vq8 / q8 cache is quantised on the device)."""
     from gqa_attention_kv_qk_gb300.layer import DecodeLayer
     cfg = case["cfg"]
-    layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device)
+    ps = int(cfg.get("page_size", 0) or 0)
+    if ps:  # a pool with spare pages, assigned in seeded random order
+        P = case["cap"] // ps
+        n_pages = cfg["batch"] * P + max(2, cfg["batch"])
+        layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device, page_size=ps,
+                            block_table=W.block_table(cfg, P, n_pages), n_pages=n_pages)
+    else:
+        layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device)
     k = case["k_values"] if cfg.get("kv_dtype") == "q8" else case["k_cache"]
     v = case["v_values"] if cfg.get("kv_dtype") in ("vq8", "q8") else case["v_cache"]
     layer.load_cache(k, v, case["lens"])

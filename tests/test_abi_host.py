@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 7
+    assert B.uaa_abi_version() == 8
 
 
 def good_desc(**kw):
@@ -113,6 +113,31 @@ def test_argument_refusals(L, kw, status, fact):
     st = B.uaa_decode_attn(good_desc(), fake_args(**kw), WS, None, check=False)
     assert st == status
     assert fact in B.last_error()
+
+
+@pytest.mark.parametrize("kw,status,fact", [
+    (dict(block_table=0x10000, page_size=24, pages_per_seq=8, n_pages=16), B.UAA_ERR_UNSUPPORTED, "page_size=24"),
+    (dict(block_table=0x10000, page_size=8, pages_per_seq=16, n_pages=16), B.UAA_ERR_UNSUPPORTED, "page_size=8"),
+    (dict(block_table=0x10000, page_size=16, pages_per_seq=3, n_pages=16), B.UAA_ERR_INVALID_ARGUMENT,
+     "pages_per_seq=3"),
+    (dict(block_table=0x10000, page_size=16, pages_per_seq=8, n_pages=0), B.UAA_ERR_INVALID_ARGUMENT, "n_pages=0"),
+    (dict(block_table=0x10008, page_size=16, pages_per_seq=8, n_pages=16), B.UAA_ERR_INVALID_ARGUMENT,
+     "block_table is not 16-byte aligned"),
+])
+def test_paging_refusals(L, kw, status, fact):
+    """A paged cache needs a power-of-two page size in [16, 4096] and a capacity of
+    whole pages (cache_capacity 128 here)."""
+    a = fake_args(cache_capacity=128, max_seq_len=64, **kw)
+    assert B.uaa_decode_attn(good_desc(), a, WS, None, check=False) == status
+    assert fact in B.last_error()
+
+
+@pytest.mark.parametrize("kv", ["vq8", "q8"])
+def test_int8_caches_refuse_16_key_pages(L, kv):
+    a = fake_args(cache_capacity=128, max_seq_len=64, block_table=0x10000, page_size=16, pages_per_seq=8,
+                  n_pages=16, k_scale=0x10000)
+    assert B.uaa_decode_attn(good_desc(kv_dtype=kv), a, WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert "page_size=16 is below 32" in B.last_error()
 
 
 def test_sink_flag_without_pointer_is_refused(L):

@@ -61,12 +61,13 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
     a = oracle_arrays(case, oracle_mod)
     layer = gpu_layer(case)
     kv = cfg.get("kv_dtype", "bf16")
+    C = lambda name: layer.logical(name)  # logical rows [B][Hkv][cap][...], paged or not
     if kv in ("vq8", "q8"):  # both quantisers on the same fp32 values
-        assert np.array_equal(layer.v_cache.cpu().numpy(), a["v_cache"])
-        assert np.array_equal(layer.v_scale.cpu().numpy().view(np.uint32), a["v_scale"].view(np.uint32))
+        assert np.array_equal(C("v_cache").cpu().numpy(), a["v_cache"])
+        assert np.array_equal(C("v_scale").cpu().numpy().view(np.uint32), a["v_scale"].view(np.uint32))
     if kv == "q8":
-        assert np.array_equal(layer.k_cache.cpu().numpy(), a["k_cache"])
-        assert np.array_equal(layer.k_scale.cpu().numpy().view(np.uint32), a["k_scale"].view(np.uint32))
+        assert np.array_equal(C("k_cache").cpu().numpy(), a["k_cache"])
+        assert np.array_equal(C("k_scale").cpu().numpy().view(np.uint32), a["k_scale"].view(np.uint32))
     B_, Hq, D = cfg["batch"], cfg["n_q_heads"], cfg["head_dim"]
     worst = (0.0, 0.0)
     for step in range(steps):
@@ -99,25 +100,27 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         if check_qrot:
             assert np.allclose(q_rot.cpu().numpy(), qr, rtol=2e-5, atol=2e-5)
         # the appended rows
+        kc_g, vc_g = C("k_cache"), C("v_cache")
+        ks_g, vs_g = C("k_scale"), C("v_scale")
         for b in range(B_):
             slot = int(pre[b])
-            kg = f64(layer.k_cache[b, :, slot].float())
+            kg = f64(kc_g[b, :, slot].float())
             if kv == "q8":
                 # codes of the rotated key: the GPU rotates in fp32, the oracle in fp64, so a
                 # code may differ by one where k / s lies within rounding of a tie; the scale
                 # (max |k| / 127) by the fp32 rotation's relative error
                 kcg, kco = kg.astype(np.int64), a["k_cache"][b, :, slot].astype(np.int64)
-                ksg, kso = f64(layer.k_scale[b, :, slot]), a["k_scale"][b, :, slot].astype(np.float64)
+                ksg, kso = f64(ks_g[b, :, slot]), a["k_scale"][b, :, slot].astype(np.float64)
                 assert np.abs(kcg - kco).max() <= 1, "q8 key code off by more than one"
                 assert (kcg != kco).sum() <= max(2, kco.size // 100), "q8 key codes differ beyond rounding ties"
                 assert np.allclose(ksg, kso, rtol=2e-6, atol=0), "q8 key scale beyond fp32 rounding"
-                assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
-                assert np.array_equal(layer.v_scale[b, :, slot].cpu().numpy().view(np.uint32),
+                assert np.array_equal(vc_g[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
+                assert np.array_equal(vs_g[b, :, slot].cpu().numpy().view(np.uint32),
                                       a["v_scale"][b, :, slot].view(np.uint32))
             elif kv == "f32":
                 ko = a["k_cache"][b, :, slot].astype(np.float64)
                 assert np.allclose(kg, ko, rtol=1e-5, atol=1e-6)
-                assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
+                assert np.array_equal(vc_g[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
             else:
                 ko = bf16_bits_to_f64(a["k_cache"][b, :, slot])
                 # one bf16 ulp, plus the fp32 rotation's absolute error where the
@@ -126,12 +129,17 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
                 assert np.all(np.abs(kg - ko) <= np.abs(ko) * 2.0 ** -7 + row_max * 2.0 ** -18), \
                     "k row beyond one bf16 ulp + the fp32 rotation error"
                 if kv == "bf16":
-                    vg = layer.v_cache[b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
+                    vg = vc_g[b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
                     assert np.array_equal(vg, a["v_cache"][b, :, slot])
                 else:
-                    assert np.array_equal(layer.v_cache[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
-                    assert np.array_equal(layer.v_scale[b, :, slot].cpu().numpy().view(np.uint32),
+                    assert np.array_equal(vc_g[b, :, slot].cpu().numpy(), a["v_cache"][b, :, slot])
+                    assert np.array_equal(vs_g[b, :, slot].cpu().numpy().view(np.uint32),
                                           a["v_scale"][b, :, slot].view(np.uint32))
+        if layer.page_size:  # pages outside every table row are never written
+            used = torch.zeros(layer.n_pages, dtype=torch.bool)
+            used[layer.block_table.reshape(-1).long().cpu()] = True
+            assert not layer.k_cache[~used.cuda()].float().abs().sum().item()
+            assert not layer.v_cache[~used.cuda()].float().abs().sum().item()
         mx, mean = assert_out_close(out, want, f"step {step}")
         worst = (max(worst[0], mx), max(worst[1], mean))
     return worst
@@ -147,6 +155,7 @@ SMALL = {
     "gptoss_vq8_sink": dict(overrides=dict(batch=3, seq_len=4096), lens=[100, 1000, 4095]),
     "gemma3_12b_local_global": dict(overrides=dict(batch=3, seq_len=(1, 3000)), lens=[2999, 1023, 5]),
     "llama31_8b_q8": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
+    "llama31_8b_paged": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
 }
 
 
@@ -206,6 +215,18 @@ EDGE = [
                                                     seq_len=300), [299, 0]),
     ("q8-rotary96-norm-offset", "qwen3_8b_ragged", dict(batch=2, kv_dtype="q8", rotary_dim=96, norm_offset=True,
                                                         norm_w_range=(-0.5, 0.5), seq_len=300), [299, 77]),
+    # paged caches: page sizes 16 .. 4096, every cache kind, windows that start mid-page
+    ("paged-16-bf16", "llama31_8b_decode", dict(batch=3, seq_len=1000, page_size=16), [999, 64, 0]),
+    ("paged-64-vq8-window", "gptoss_vq8_sink", dict(batch=2, seq_len=500, page_size=64, window=100), [499, 64]),
+    ("paged-32-vq8-window-37", "gptoss_vq8_sink", dict(batch=2, seq_len=500, page_size=32, window=37), [499, 20]),
+    ("paged-16-f32-window-37", "llama32_1b_tiny", dict(batch=2, seq_len=300, page_size=16, window=37), [299, 20]),
+    ("paged-16-bf16-window-37", "qwen3_8b_ragged", dict(batch=2, seq_len=(1, 500), page_size=16, window=37),
+     [499, 20]),
+    ("paged-256-q8", "llama31_8b_q8", dict(batch=2, seq_len=700, page_size=256), [699, 300]),
+    ("paged-32-f32", "llama32_1b_tiny", dict(batch=2, seq_len=300, page_size=32), [299, 40]),
+    ("paged-128-d256", "gemma2_9b_swa", dict(batch=2, seq_len=600, page_size=128, layers=None), [599, 10]),
+    ("paged-4096-d256-window", "gemma2_9b_swa", dict(batch=2, seq_len=5000, page_size=4096,
+                                                     layers=[dict(window=4096)]), [4999, 4100]),
     ("d64-vq8-norm-offset-local", "gemma3_12b_local_global",
      dict(batch=2, seq_len=600, head_dim=64, kv_dtype="vq8", layers=[dict(window=100, rope_theta=10000.0,
                                                                           rope_scaling="none")]), [599, 40]),
@@ -428,7 +449,7 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry
 # ------------------------------------------------------------------ full size, sampled
 
 FULL = ["llama32_1b_tiny", "llama31_8b_decode", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink",
-        "gemma3_12b_local_global", "llama31_8b_q8"]
+        "gemma3_12b_local_global", "llama31_8b_q8", "llama31_8b_paged"]
 
 
 @pytest.mark.slow
