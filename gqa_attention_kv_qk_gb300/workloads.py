@@ -24,7 +24,8 @@ TILE = 64  # cache capacities are rounded up to a multiple of this many slots
 # The workloads. Method keys follow the oracle / library vocabulary;
 # workload keys: batch, seq_len (int, or (lo, hi) inclusive for ragged lengths),
 # steps, seed, layers (per-layer overrides; one cache per layer), page_size (a
-# paged cache: pages of that many positions, assigned by block_table below).
+# paged cache: pages of that many positions, assigned by block_table below), q_len
+# (tokens per sequence in each step: a prefill chunk or draft tokens to verify).
 CONFIGS: dict[str, dict] = {
     # Tiny Llama-3.2-1B-like step: fp32 everything, seed 0.
     "llama32_1b_tiny": dict(
@@ -124,11 +125,12 @@ def _cast(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def capacity(cfg: dict, extra: int = 0) -> int:
-    """Slots per (sequence, kv head): the longest cached length + extra, rounded up
-    to a multiple of 64 and of the page size of a paged workload."""
+    """Slots per (sequence, kv head): the longest cached length + extra (tokens the
+    steps append), rounded up to a multiple of 64 and of the page size of a paged
+    workload."""
     sl = cfg["seq_len"]
     longest = sl[1] if isinstance(sl, (tuple, list)) else sl
-    need = longest + max(extra, 1)
+    need = longest + max(extra, int(cfg.get("q_len", 1) or 1))
     unit = max(TILE, int(cfg.get("page_size", 0) or 0))
     return (need + unit - 1) // unit * unit
 
@@ -153,12 +155,15 @@ def seq_lens(cfg: dict) -> torch.Tensor:
 
 
 def step_inputs(cfg: dict, step: int = 0) -> dict:
-    """q [B][Hq][D], k_new and v_new [B][Hkv][D] in the io dtype, fresh for each step."""
+    """q [B][Hq][D], k_new and v_new [B][Hkv][D] in the io dtype, fresh for each step;
+    with cfg q_len = T > 1 a chunk of T tokens per sequence, [B][T][H][D]."""
     B, Hq, Hkv, D = cfg["batch"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
     layer = cfg.get("layer", 0)
     io = cfg.get("io_dtype", "bf16")
+    T = int(cfg.get("q_len", 1) or 1)
+    tok = (T,) if T > 1 else ()
     out = {}
-    for tag, shape in (("q", (B, Hq, D)), ("k_new", (B, Hkv, D)), ("v_new", (B, Hkv, D))):
+    for tag, shape in (("q", (B, *tok, Hq, D)), ("k_new", (B, *tok, Hkv, D)), ("v_new", (B, *tok, Hkv, D))):
         x = torch.randn(shape, generator=_gen(cfg["seed"], tag, step, layer), dtype=torch.float32)
         out[tag] = _cast(x, io)
     return out

@@ -253,6 +253,22 @@ def attend_range(cfg: dict, q_row, k_rows, v_rows, scale_rows, j_lo, j_hi, sink=
     return o, lse.value
 
 
+def chunk_step(cfg: dict, q, k_new, v_new, q_norm_w, k_norm_w, sink, k_cache, v_cache,
+               v_scale, seq_lens, n_threads=None, k_scale=None) -> np.ndarray:
+    """T tokens per sequence (q [B][T][Hq][D], k_new / v_new [B][T][Hkv][D]): token t
+    takes position seq_len + t and attends every key up to its own and no later one
+    (causal within the chunk), so the chunk is T decode steps, taken in order. The
+    decoder page's absolute-KV-index position (P1.3) fixes where each token sits.
+    Returns out [B][T][Hq][D]; caches and seq_lens mutate (seq_lens += T)."""
+    T = q.shape[1]
+    outs = []
+    for t in range(T):
+        outs.append(decode_step(cfg, np.ascontiguousarray(q[:, t]), np.ascontiguousarray(k_new[:, t]),
+                                np.ascontiguousarray(v_new[:, t]), q_norm_w, k_norm_w, sink, k_cache, v_cache,
+                                v_scale, seq_lens, n_threads, k_scale))
+    return np.stack(outs, axis=1)
+
+
 def decode_step(cfg: dict, q, k_new, v_new, q_norm_w, k_norm_w, sink, k_cache, v_cache,
                 v_scale, seq_lens, n_threads=None, k_scale=None) -> np.ndarray:
     """append + attend over the whole batch; caches and seq_lens mutate in place."""

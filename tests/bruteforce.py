@@ -57,6 +57,63 @@ def vq8_numpy(v: np.ndarray):
     return q.astype(np.int8), s
 
 
+def chunk_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, seq_lens, q_norm_w=None, k_norm_w=None, sink=None,
+               inv_freq=None, mscale=1.0, causal=True):
+    """T tokens per sequence in one matrix expression (bf16 and f32 caches): all T
+    keys appended at positions L .. L + T - 1 first, then one logit matrix of the
+    T Hq query rows against every key, masked by token t's causal (j <= L + t) and
+    window (j > L + t - W) limits, softmax per row with the sink as an extra
+    column. q [B][T][Hq][D], k_new / v_new [B][T][Hkv][D] fp64; caches mutate.
+    Returns out [B][T][Hq][D]."""
+    B, T, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    G = Hq // Hkv
+    style = cfg.get("rope_style", "neox")
+    rd = cfg.get("rotary_dim", 0) or D
+    off = 1.0 if cfg.get("norm_offset") else 0.0
+    if inv_freq is None:
+        inv_freq = plain_inv_freq(rd, cfg.get("rope_theta", 10000.0))
+    scale = cfg.get("scale", 0.0) or 1.0 / np.sqrt(D)
+    kv = cfg.get("kv_dtype", "bf16")
+    W = cfg.get("window", 0) or 0
+    cap_ = cfg.get("softcap", 0.0) or 0.0
+    eps = cfg.get("norm_eps", 1e-6)
+    out = np.zeros((B, T, Hq, D))
+    for b in range(B):
+        L = int(seq_lens[b])
+        Qr = np.zeros((T, Hq, D))
+        for t in range(T):
+            R = rotation_matrix(D, style, inv_freq, mscale, L + t, rd)
+            qb, kb = q[b, t].astype(np.float64), k_new[b, t].astype(np.float64)
+            if cfg.get("qk_norm"):
+                qb, kb = rmsnorm_rows(qb, q_norm_w, eps, off), rmsnorm_rows(kb, k_norm_w, eps, off)
+            Qr[t] = qb @ R.T
+            kr = kb @ R.T
+            if kv == "bf16":
+                k_cache[b, :, L + t], v_cache[b, :, L + t] = bf16_round(kr), bf16_round(v_new[b, t])
+            else:
+                k_cache[b, :, L + t] = kr.astype(np.float32).astype(np.float64)
+                v_cache[b, :, L + t] = v_new[b, t].astype(np.float32).astype(np.float64)
+        n = L + T
+        seq_lens[b] = n
+        K = np.repeat(k_cache[b, :, :n], G, axis=0)                      # [Hq][n][D]
+        V = np.repeat(v_cache[b, :, :n], G, axis=0)
+        S = scale * np.einsum("thd,hjd->thj", Qr, K)                     # [T][Hq][n]
+        if cap_ > 0:
+            S = cap_ * np.tanh(S / cap_)
+        j = np.arange(n)[None, :]
+        pos = (L + np.arange(T))[:, None]
+        visible = ((j <= pos) if causal else (j < n)) & ((j > pos - W) if W > 0 else True)  # [T][n]
+        S = np.where(visible[:, None, :], S, -np.inf)
+        if sink is not None:
+            z = np.broadcast_to(np.asarray(sink, dtype=np.float64)[None, :, None], (T, Hq, 1))
+            S = np.concatenate([S, z], axis=2)
+        P = np.exp(S - S.max(axis=2, keepdims=True))
+        P = P / P.sum(axis=2, keepdims=True)
+        out[b] = np.einsum("thj,hjd->thd", P[:, :, :n], V)
+    return out
+
+
 def decode_step(cfg: dict, q, k_new, v_new, k_cache, v_cache, v_scale, seq_lens,
                 q_norm_w=None, k_norm_w=None, sink=None, inv_freq=None, mscale=1.0, k_scale=None):
     """All arrays fp64 (values, codes as float, scales as float). Caches mutate.

@@ -12,7 +12,7 @@ from gqa_attention_kv_qk_gb300 import workloads as W
 
 def host_case(cfg: dict, lens=None, cap=None, step: int = 0, fill_unused: str = "zero") -> dict:
     lens = W.seq_lens(cfg) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
-    cap = cap or W.capacity(cfg, extra=cfg.get("steps", 1))
+    cap = cap or W.capacity(cfg, extra=cfg.get("steps", 1) * int(cfg.get("q_len", 1) or 1))
     case = dict(cfg=cfg, lens=lens.clone(), cap=cap)
     case.update(W.cache(cfg, cap, lens, fill_unused=fill_unused))
     case.update(W.step_inputs(cfg, step))
@@ -47,7 +47,8 @@ def oracle_arrays(case: dict, oracle_mod) -> dict:
 
 def run_oracle_step(case: dict, oracle_mod, n_threads=None):
     a = oracle_arrays(case, oracle_mod)
-    out = oracle_mod.decode_step(case["cfg"], a["q"], a["k_new"], a["v_new"], a["q_norm_w"],
+    step = oracle_mod.chunk_step if int(case["cfg"].get("q_len", 1) or 1) > 1 else oracle_mod.decode_step
+    out = step(case["cfg"], a["q"], a["k_new"], a["v_new"], a["q_norm_w"],
                                  a["k_norm_w"], a["sink"], a["k_cache"], a["v_cache"],
                                  a["v_scale"], a["seq_lens"], n_threads=n_threads, k_scale=a["k_scale"])
     return out, a

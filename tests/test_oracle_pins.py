@@ -529,6 +529,62 @@ def test_whole_step_matches_bruteforce(oracle_mod, spec):
         assert np.array_equal(a["k_scale"], ks.astype(np.float32))
 
 
+CHUNKS = [
+    dict(name="llama31_8b_decode", n_q_heads=8, n_kv_heads=2, head_dim=64, q_len=4),
+    dict(name="qwen3_8b_ragged", n_q_heads=4, n_kv_heads=4, head_dim=64, q_len=3, window=2),
+    dict(name="gemma2_9b_swa", n_q_heads=8, n_kv_heads=1, head_dim=64, q_len=5, softcap=3.0, layers=None,
+         window=9, has_sink=True),
+    dict(name="llama32_1b_tiny", n_q_heads=8, n_kv_heads=2, head_dim=64, q_len=7, rotary_dim=32),
+]
+
+
+@pytest.mark.parametrize("spec", CHUNKS, ids=lambda s: "-".join(f"{k}={v}" for k, v in s.items()))
+def test_chunk_matches_masked_matrix_bruteforce(oracle_mod, spec):
+    """Several tokens per sequence: the oracle takes them as decode steps in order;
+    the brute force appends all of them first and masks one logit matrix by each
+    token's causal and window limits. The two agree."""
+    spec = dict(spec)
+    name = spec.pop("name")
+    cfg = W.layer_configs(W.config(name, batch=3, seq_len=(0, 40), steps=1, **spec))[0]
+    case = host_case(cfg, lens=[0, 17, 40])
+    out, a = run_oracle_step(case, oracle_mod)
+    T = cfg["q_len"]
+    assert out.shape == (3, T, cfg["n_q_heads"], cfg["head_dim"])
+    f64 = lambda t: t.to(torch.float64).numpy().copy()
+    inv, ms = (None, 1.0)
+    if cfg.get("rope_scaling", "none") != "none":
+        inv, ms = oracle_mod.rope_inv_freq(cfg)
+    lens = case["lens"].numpy().copy()
+    ref = BF.chunk_step(cfg, f64(case["q"]), f64(case["k_new"]), f64(case["v_new"]), f64(case["k_cache"]),
+                        f64(case["v_cache"]), lens, None if case["q_norm_w"] is None else case["q_norm_w"].numpy(),
+                        None if case["k_norm_w"] is None else case["k_norm_w"].numpy(),
+                        None if case["sink"] is None else case["sink"].numpy(), inv, ms)
+    assert np.array_equal(lens, a["seq_lens"]) and np.array_equal(lens, case["lens"].numpy() + T)
+    assert np.allclose(out, ref, rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("mistake", ["not_causal", "window_shortened_by_the_chunk"])
+def test_chunk_mask_mistakes_break_the_tolerance(oracle_mod, mistake):
+    """Negative controls for the chunk's mask: every token seeing all T new keys
+    (no causal limit), or every token's window shortened by T - 1 (the widened
+    window of the chunk's key range taken the wrong way), fails the parity bar."""
+    cfg = W.layer_configs(W.config("llama31_8b_decode", batch=2, seq_len=(0, 90), n_q_heads=8, n_kv_heads=2,
+                                   head_dim=64, q_len=6, window=(12 if mistake != "not_causal" else 0)))[0]
+    case = host_case(cfg, lens=[30, 90])
+    case["q"] = (case["q"].to(torch.float32) * 3).to(case["q"].dtype)
+    good, _ = run_oracle_step(case, oracle_mod)
+    f64 = lambda t: t.to(torch.float64).numpy().copy()
+    inv, ms = oracle_mod.rope_inv_freq(cfg)
+    args = lambda: (f64(case["q"]), f64(case["k_new"]), f64(case["v_new"]), f64(case["k_cache"]),
+                    f64(case["v_cache"]), case["lens"].numpy().copy(), None, None, None, inv, ms)
+    if mistake == "not_causal":
+        wrong = BF.chunk_step(cfg, *args(), causal=False)
+    else:
+        wrong = BF.chunk_step(dict(cfg, window=12 - (cfg["q_len"] - 1)), *args())
+    d = np.abs(good - wrong)
+    assert d.max() > TOL_MAX or d.mean() > TOL_MEAN, (mistake, d.max(), d.mean())
+
+
 def test_interleaved_step_equals_permuted_neox_step(oracle_mod):
     D = 64
     perm = np.concatenate([2 * np.arange(D // 2), 2 * np.arange(D // 2) + 1])  # neox p -> row
