@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 from gqa_attention_kv_qk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (% of GB300 peak) and decode steps/sec at 1 GPU"
-DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_paged": 64}
+DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_paged": 64, "llama31_8b_verify": 16}
 
 
 def measured_peaks() -> dict:
@@ -97,14 +97,15 @@ def partial_bytes(cfg: dict, lens_after: list[int]) -> int:
 
 
 def decode_step_bytes(cfg: dict, lens_before: list[int]) -> int:
-    """One decode step: the partial's KV reads plus the q/k/v reads, the appended
-    rows and the output."""
+    """One step (T = q_len tokens per sequence): the partial's KV reads (each key
+    once, whatever T) plus the q/k/v reads, the appended rows and the output."""
     B, Hq, Hkv, D = cfg["batch"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    T = int(cfg.get("q_len", 1) or 1)
     io = 4 if cfg.get("io_dtype") == "f32" else 2
     ob = 4 if cfg.get("out_dtype", "f32") == "f32" else 2
     kb, vb = _kv_row_bytes(cfg)
-    small = B * (Hq + 2 * Hkv) * D * io + B * Hkv * (kb + vb) + B * Hq * D * ob
-    return partial_bytes(cfg, [n + 1 for n in lens_before]) + small
+    small = T * (B * (Hq + 2 * Hkv) * D * io + B * Hkv * (kb + vb) + B * Hq * D * ob)
+    return partial_bytes(cfg, [n + T for n in lens_before]) + small
 
 
 # ---------------------------------------------------------------- clocks
@@ -220,10 +221,12 @@ def oracle_sample(cfg: dict, case: dict, budget_s: float, n_threads: int) -> dic
     B = cfg["batch"]
     lens0 = a["seq_lens"].copy()
 
+    step = O.chunk_step if int(cfg.get("q_len", 1) or 1) > 1 else O.decode_step
+
     def run(nb: int) -> float:
         sl = lens0[:nb].copy()
         t = time.perf_counter()
-        O.decode_step(cfg, a["q"][:nb].copy(), a["k_new"][:nb].copy(), a["v_new"][:nb].copy(), a["q_norm_w"],
+        step(cfg, a["q"][:nb].copy(), a["k_new"][:nb].copy(), a["v_new"][:nb].copy(), a["q_norm_w"],
                       a["k_norm_w"], a["sink"], a["k_cache"][:nb], a["v_cache"][:nb],
                       None if a["v_scale"] is None else a["v_scale"][:nb], sl, n_threads=n_threads,
                       k_scale=None if a["k_scale"] is None else a["k_scale"][:nb])
@@ -235,7 +238,8 @@ def oracle_sample(cfg: dict, case: dict, budget_s: float, n_threads: int) -> dic
     lens = [int(x) for x in lens0[:nb]]
     sub = dict(cfg, batch=nb)
     return {"bytes": decode_step_bytes(sub, lens), "seconds": secs,
-            "sample": f"one decode step of {nb} of {B} sequences (all {cfg['n_q_heads']} q heads), "
+            "sample": f"one step ({int(cfg.get('q_len', 1) or 1)} token(s) per sequence) of {nb} of {B} "
+                      f"sequences (all {cfg['n_q_heads']} q heads), "
                       f"{n_threads} threads"}
 
 
@@ -260,10 +264,11 @@ def run_uaa(args, world, rank, local) -> dict | None:
     name = args.workload
     cfg = W.config(name, seed=W.CONFIGS[name]["seed"] + 1000 * rank)
     n_dec = DECODES_PER_STEP.get(name, 1)
-    layers, cases = build_layers(cfg, cap_extra=n_dec + 1, device=device)
+    T = int(cfg.get("q_len", 1) or 1)  # tokens per sequence and call
+    layers, cases = build_layers(cfg, cap_extra=n_dec * T + 1, device=device)
     lens0 = [case["lens"].clone() for case in cases]
     lens0_dev = [l.to(device) for l in lens0]
-    hint = [int(l.max()) + n_dec - 1 for l in lens0]
+    hint = [int(l.max()) + (n_dec - 1) * T for l in lens0]
     stream = torch.cuda.Stream(device)
     inputs = [{k: case[k].to(device) for k in ("q", "k_new", "v_new")} for case in cases]
 
@@ -284,12 +289,12 @@ def run_uaa(args, world, rank, local) -> dict | None:
     for lc, l0 in zip(W.layer_configs(cfg), lens0):
         base = [int(x) for x in l0]
         for t in range(n_dec):
-            cur = [x + t for x in base]
+            cur = [x + t * T for x in base]
             step_bytes += decode_step_bytes(lc, cur)
-            part_bytes += partial_bytes(lc, [x + 1 for x in cur])
-    # kernels of one decode step of a layer: the fused append+partial and the
-    # combine (bf16 / vq8 caches), or append, partial and combine (fp32 caches)
-    fused = [layer.layout().kernel == 1 for layer in layers]
+            part_bytes += partial_bytes(lc, [x + T for x in cur])
+    # kernels of one call of a layer: the fused append+partial and the combine
+    # (bf16 / vq8 / q8 caches, one token), or append, partial and combine
+    fused = [layer.layout().kernel == 1 and T == 1 for layer in layers]
     launches_per_step = n_dec * sum(2 if f else 3 for f in fused)
 
     with torch.cuda.stream(stream):
@@ -379,11 +384,11 @@ def run_uaa(args, world, rank, local) -> dict | None:
                     off += n
                 vs.append(v)
             views.append(vs)
-        host_out = [[torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory() for _ in range(2)]
-                    for layer in layers]
+        outs = [layer.out_for(T) for layer in layers]
+        host_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)] for o in outs]
         h2d = sum(hi.numel() for hi in host_in) * n_dec
         d2h = sum(ho[0].numel() * ho[0].element_size() for ho in host_out) * n_dec
-        dev_out = [[torch.empty_like(layer.out) for _ in range(2)] for layer in layers]
+        dev_out = [[torch.empty_like(o) for _ in range(2)] for o in outs]
         copy = torch.cuda.Stream(device)
         ev = [[{n: torch.cuda.Event() for n in ("in", "done", "read")} for _ in range(2)] for _ in layers]
         # every call of the timed region: (benchmark step, decode step, layer); buffer
@@ -449,7 +454,7 @@ def run_uaa(args, world, rank, local) -> dict | None:
         "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "config": {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"], "n_q_heads": cfg["n_q_heads"],
                    "n_kv_heads": cfg["n_kv_heads"], "head_dim": cfg["head_dim"], "kv_dtype": cfg["kv_dtype"],
-                   "decode_steps_per_step": n_dec, "parallelism": f"replicas x{world}",
+                   "decode_steps_per_step": n_dec, "q_len": T, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV cache %.0f MB)" % (part_bytes / n_dec / 1e6),
                    "timing": "CUDA graph of one benchmark step, replayed K times; CUDA events"},
         "roofline": {"bound": "hbm", "achieved": round(part_gbs, 2) if part_gbs else None,

@@ -55,7 +55,7 @@ class UaaStepArgs(ctypes.Structure):
                 ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
                 ("out", ctypes.c_void_p), ("q_rot", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
-                ("pages_per_seq", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
+                ("pages_per_seq", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("q_len", ctypes.c_int32)]
 
 
 class UaaWorkspace(ctypes.Structure):
@@ -93,10 +93,11 @@ _SIGS = [
     ("uaa_decode_attn_append_partial", ctypes.c_int,
      [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
     ("uaa_decode_attn", ctypes.c_int, [_P(UaaAttnDesc), _P(UaaStepArgs), _P(UaaWorkspace), ctypes.c_void_p]),
-    ("uaa_workspace_size", ctypes.c_size_t, [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
-    ("uaa_num_splits", ctypes.c_int32, [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("uaa_workspace_size", ctypes.c_size_t,
+     [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("uaa_num_splits", ctypes.c_int32, [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("uaa_get_workspace_layout", ctypes.c_int,
-     [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P(UaaWorkspaceLayout)]),
+     [_P(UaaAttnDesc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P(UaaWorkspaceLayout)]),
     ("uaa_vq8_quantize", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
       ctypes.c_void_p]),
@@ -179,18 +180,18 @@ def uaa_decode_attn(desc, args, ws, stream=None, check=True) -> int:
                                         _stream(stream)), check)
 
 
-def uaa_workspace_size(desc, batch: int, max_seq_len: int, n_sm: int = 0) -> int:
-    return int(lib().uaa_workspace_size(ctypes.byref(desc), batch, max_seq_len, n_sm))
+def uaa_workspace_size(desc, batch: int, max_seq_len: int, n_sm: int = 0, q_len: int = 1) -> int:
+    return int(lib().uaa_workspace_size(ctypes.byref(desc), batch, max_seq_len, n_sm, q_len))
 
 
-def uaa_num_splits(desc, batch: int, max_seq_len: int, n_sm: int = 0) -> int:
-    return int(lib().uaa_num_splits(ctypes.byref(desc), batch, max_seq_len, n_sm))
+def uaa_num_splits(desc, batch: int, max_seq_len: int, n_sm: int = 0, q_len: int = 1) -> int:
+    return int(lib().uaa_num_splits(ctypes.byref(desc), batch, max_seq_len, n_sm, q_len))
 
 
-def uaa_get_workspace_layout(desc, batch: int, max_seq_len: int, n_sm: int = 0) -> UaaWorkspaceLayout:
+def uaa_get_workspace_layout(desc, batch: int, max_seq_len: int, n_sm: int = 0, q_len: int = 1) -> UaaWorkspaceLayout:
     out = UaaWorkspaceLayout()
-    _check(lib().uaa_get_workspace_layout(ctypes.byref(desc), batch, max_seq_len, n_sm, ctypes.byref(out)),
-           True)
+    _check(lib().uaa_get_workspace_layout(ctypes.byref(desc), batch, max_seq_len, n_sm, q_len,
+                                          ctypes.byref(out)), True)
     return out
 
 

@@ -104,8 +104,12 @@ uaa_status check_desc(const uaa_attn_desc* d)
 
 // ---------------------------------------------------------------- split geometry
 
+// Tokens per sequence one step takes at most (a prefill chunk).
+constexpr int kMaxQLen = 1024;
+
 struct Plan {
     int G;
+    int q_len;           // tokens per sequence (1: decode)
     int kernel;          // 0 CUDA-core, 1 tensor-core
     int heads_per_cta;   // query heads of one unit
     int head_groups;     // units per kv head
@@ -159,23 +163,28 @@ uaa::BalanceState balance_of(void* ws, const Plan& pl)
 // partition in internal.cuh), so the split needs no length bound. Batches above
 // kMaxSliceBatch sequences are cut into slices (one partial + combine launch each)
 // because a CTA keeps the slice's stage prefix in shared memory.
-uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, Plan* pl)
+uaa_status make_plan(const uaa_attn_desc* d, int batch, int q_len, int max_len, int n_sm, Plan* pl)
 {
     UAA_TRY(check_desc(d));
     if (batch < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "batch=%d is negative", batch);
     if (max_len < 0) return fail(UAA_ERR_INVALID_ARGUMENT, "max_seq_len=%d is negative", max_len);
     if (n_sm <= 0) return fail(UAA_ERR_INVALID_ARGUMENT, "SM count %d is not positive", n_sm);
+    if (q_len < 0 || q_len > kMaxQLen)
+        return fail(UAA_ERR_UNSUPPORTED, "q_len=%d is not in [0, %d]", q_len, kMaxQLen);
     Plan p{};
     p.G = d->n_q_heads / d->n_kv_heads;
+    p.q_len = q_len > 1 ? q_len : 1;
     p.kernel = d->kv_dtype == UAA_DTYPE_F32 ? 0 : 1;
-    if (p.kernel == 0 || d->head_dim == 256 || p.G <= 8) {
+    // a unit's query rows are the (token, head) pairs of one kv head: q_len G of them
+    const int rows = p.q_len * p.G;
+    if (p.kernel == 0 || d->head_dim == 256 || rows <= 8) {
         p.heads_per_cta = 8;
         p.n_head_tiles = 1;
     } else {
         p.heads_per_cta = 16;
         p.n_head_tiles = 2;
     }
-    p.head_groups = (p.G + p.heads_per_cta - 1) / p.heads_per_cta;
+    p.head_groups = (rows + p.heads_per_cta - 1) / p.heads_per_cta;
     p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype) / uaa::kTileKeys : 1;
     p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
     p.n_ctas = n_sm * p.per_sm;
@@ -192,7 +201,7 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int max_len, int n_sm, P
     p.off_status = 0;
     p.off_balance = 256;
     p.off_qrot = p.off_balance + balance_bytes(p.n_ctas);
-    p.off_prefix = p.off_qrot + align256(B * Hq * D * 4);
+    p.off_prefix = p.off_qrot + align256(B * p.q_len * Hq * D * 4);
     p.off_rec_lse = p.off_prefix + p.n_slices * p.prefix_stride;
     p.off_rec_o = p.off_rec_lse + p.n_slices * p.rec_lse_stride;
     p.off_ranges = p.off_rec_o + p.n_slices * p.rec_o_stride;
@@ -212,9 +221,10 @@ uaa_status check_args(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     if (a->cache_capacity <= 0 || a->cache_capacity % 4 != 0)
         return fail(UAA_ERR_INVALID_ARGUMENT, "cache_capacity=%d is not a positive multiple of 4",
                     a->cache_capacity);
-    if ((long long)a->max_seq_len + 1 > a->cache_capacity)
-        return fail(UAA_ERR_CAPACITY, "max_seq_len=%d + 1 new token does not fit cache_capacity=%d",
-                    a->max_seq_len, a->cache_capacity);
+    const int q_len = a->q_len > 1 ? a->q_len : 1;
+    if ((long long)a->max_seq_len + q_len > a->cache_capacity)
+        return fail(UAA_ERR_CAPACITY, "max_seq_len=%d + %d new token(s) does not fit cache_capacity=%d",
+                    a->max_seq_len, q_len, a->cache_capacity);
     if (a->block_table) {
         const int ps = a->page_size;
         if (ps < 16 || ps > 4096 || (ps & (ps - 1)) != 0)
@@ -272,7 +282,7 @@ uaa_status prepare(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_wor
     UAA_TRY(check_args(d, a, ws, need_io));
     const int n_sm = device_sm_count();
     if (n_sm <= 0) return fail(UAA_ERR_CUDA, "no CUDA device: the SM count query failed");
-    UAA_TRY(make_plan(d, a->batch, a->max_seq_len, n_sm, pl));
+    UAA_TRY(make_plan(d, a->batch, a->q_len, a->max_seq_len, n_sm, pl));
     if (ws->bytes < pl->total)
         return fail(UAA_ERR_INVALID_ARGUMENT, "workspace has %zu bytes, the step needs %zu", ws->bytes,
                     pl->total);
@@ -403,6 +413,7 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.Hq = d->n_q_heads;
     p.Hkv = d->n_kv_heads;
     p.D = d->head_dim;
+    p.q_len = pl.q_len;
     p.cap = a->cache_capacity;
     p.max_len = a->max_seq_len;
     p.style = d->rope.style;
@@ -492,10 +503,14 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.heads_per_cta = pl.heads_per_cta;
         p.head_groups = pl.head_groups;
         p.cap = a->cache_capacity;
-        p.window = d->window;
+        p.q_len = pl.q_len;
+        p.attn_window = d->window;
+        // the partition covers the union of the rows' windows: the first token's
+        // window starts q_len - 1 keys before the last one's
+        p.window = d->window > 0 ? d->window + pl.q_len - 1 : 0;
         p.mg = pl.mg;
         p.softcap_log2e = d->softcap > 0.f ? d->softcap * uaa::kLog2e : 0.f;
-        p.q_prime = reinterpret_cast<const float*>(w + pl.off_qrot) + (size_t)b0 * Hq * D;
+        p.q_prime = reinterpret_cast<const float*>(w + pl.off_qrot) + (size_t)b0 * pl.q_len * Hq * D;
         p.k_cache = a->k_cache;
         p.v_cache = a->v_cache;
         p.v_scale = a->v_scale;
@@ -564,7 +579,8 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.G = pl.G;
         p.heads_per_cta = pl.heads_per_cta;
         p.head_groups = pl.head_groups;
-        p.window = d->window;
+        p.q_len = pl.q_len;
+        p.window = d->window > 0 ? d->window + pl.q_len - 1 : 0;
         p.mg = pl.mg;
         p.P = pl.n_ctas;
         p.out_dtype = d->out_dtype;
@@ -576,7 +592,7 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         if (pl.kernel == 1) p.bal = balance_of(w, pl);
         p.rec_lse = reinterpret_cast<const float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
         p.rec_o = reinterpret_cast<const float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
-        p.out = static_cast<char*>(a->out) + (size_t)b0 * Hq * D * out_elem;
+        p.out = static_cast<char*>(a->out) + (size_t)b0 * pl.q_len * Hq * D * out_elem;
         p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
         const cudaError_t e = uaa::launch_combine(p, s);
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
@@ -589,7 +605,7 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
 uaa_status run_append_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws,
                               const Plan& pl, cudaStream_t s)
 {
-    if (pl.kernel == 1) return run_partial(d, a, ws, pl, s, true);
+    if (pl.kernel == 1 && pl.q_len == 1) return run_partial(d, a, ws, pl, s, true);
     UAA_TRY(run_append(d, a, ws, pl, s));
     return run_partial(d, a, ws, pl, s);
 }
@@ -641,29 +657,30 @@ uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
     return run_combine(desc, args, ws, pl, stream);
 }
 
-size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm)
+size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm,
+                          int32_t q_len)
 {
     Plan pl{};
     if (n_sm <= 0) n_sm = device_sm_count();
-    if (make_plan(desc, batch, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
+    if (make_plan(desc, batch, q_len, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
     return pl.total;
 }
 
-int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm)
+int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm, int32_t q_len)
 {
     Plan pl{};
     if (n_sm <= 0) n_sm = device_sm_count();
-    if (make_plan(desc, batch, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
+    if (make_plan(desc, batch, q_len, max_seq_len, n_sm, &pl) != UAA_OK) return 0;
     return pl.n_ctas;
 }
 
 uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm,
-                                    uaa_workspace_layout* layout)
+                                    int32_t q_len, uaa_workspace_layout* layout)
 {
     if (!layout) return fail(UAA_ERR_INVALID_ARGUMENT, "layout is NULL");
     Plan pl{};
     if (n_sm <= 0) n_sm = device_sm_count();
-    UAA_TRY(make_plan(desc, batch, max_seq_len, n_sm, &pl));
+    UAA_TRY(make_plan(desc, batch, q_len, max_seq_len, n_sm, &pl));
     layout->n_ctas = pl.n_ctas;
     layout->stage_keys = pl.mg * uaa::kTileKeys;
     layout->heads_per_cta = pl.heads_per_cta;
@@ -778,7 +795,7 @@ extern "C" uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const ua
     const int n_sm = device_sm_count();
     if (n_sm <= 0) return fail(UAA_ERR_CUDA, "no CUDA device: the SM count query failed");
     Plan pl{};
-    UAA_TRY(make_plan(desc, args->batch, args->max_seq_len, n_sm, &pl));
+    UAA_TRY(make_plan(desc, args->batch, args->q_len, args->max_seq_len, n_sm, &pl));
     if (pl.total > (size_t)UAA_STATIC_SCRATCH_BYTES)
         return fail(UAA_ERR_INVALID_ARGUMENT,
                     "this step needs %zu bytes of scratch; the built-in scratch of uaa_decode_attn_static "

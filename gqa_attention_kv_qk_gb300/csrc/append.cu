@@ -38,15 +38,16 @@ __device__ __forceinline__ void quantize_row(const float (&x)[EPL], int lane, in
     if (lane == 0) *scale = s;
 }
 
-// Row r of sequence b: the q rows (r < Hq), then the k rows, then the v rows.
-__device__ __forceinline__ const void* row_source(const AppendParams& p, int b, int r, size_t& at)
+// Row r of token t of sequence b: the q rows (r < Hq), then the k rows, then the v rows.
+__device__ __forceinline__ const void* row_source(const AppendParams& p, int b, int t, int r, size_t& at)
 {
+    const size_t bt = static_cast<size_t>(b) * p.q_len + t;
     if (r < p.Hq) {
-        at = (static_cast<size_t>(b) * p.Hq + r) * p.D;
+        at = (bt * p.Hq + r) * p.D;
         return p.q;
     }
     const int kv = r < p.Hq + p.Hkv ? r - p.Hq : r - p.Hq - p.Hkv;
-    at = (static_cast<size_t>(b) * p.Hkv + kv) * p.D;
+    at = (bt * p.Hkv + kv) * p.D;
     return r < p.Hq + p.Hkv ? p.k_new : p.v_new;
 }
 
@@ -68,103 +69,116 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     float x[EPL], nxt[EPL];
     if (warp < n_rows) {
         size_t at;
-        const void* src = row_source(p, b, warp, at);
+        const void* src = row_source(p, b, 0, warp, at);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
     }
 
+    // the step's tokens take positions L .. L + q_len - 1; a sequence whose tokens do
+    // not all fit the cache is not appended (and not advanced)
     const int L = p.seq_lens[b];
-    const bool fits = L >= 0 && L < p.cap;
+    const bool fits = L >= 0 && L + p.q_len <= p.cap;
     if (threadIdx.x == 0) {
         if (!fits) atomicOr(p.status, UAA_DEVFLAG_CAPACITY);
         else if (L > p.max_len) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
     }
-    const int pos = fits ? L : 0;
 
+    for (int tok = 0; tok < p.q_len; ++tok) {  // one token of the sequence at a time
+        const int pos = fits ? L + tok : 0;
+        if (tok > 0) {
+            __syncthreads();  // the previous token's rows no longer read the table
+            if (warp < n_rows) {
+                size_t at;
+                const void* src = row_source(p, b, tok, warp, at);
 #pragma unroll
-    for (int i0 = 0; i0 < HALF; i0 += 32)  // warp w takes pairs 32 w .. 32 w + 31
-        if (warp == i0 / 32)
-            cs[i0 + lane] = rope_pair_cos_sin(i0 + lane, p.half_rot, pos, param_at_lane(p.inv_freq_over_pi + i0, lane),
-                                              p.mscale);
-    __syncthreads();  // the cos / sin table is complete
-    for (int r = warp; r < n_rows; r += kAppendWarps) {
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) x[i] = nxt[i];
-        if (r + kAppendWarps < n_rows) {
-            size_t at;
-            const void* src = row_source(p, b, r + kAppendWarps, at);
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
-        }
-        const bool is_q = r < p.Hq;
-        const bool is_k = !is_q && r < p.Hq + p.Hkv;
-        const int head = is_q ? r : (is_k ? r - p.Hq : r - p.Hq - p.Hkv);
-        const size_t in_row = (static_cast<size_t>(b) * (is_q ? p.Hq : p.Hkv) + head) * D;
-
-        // the new token's cache row (k and v rows; -1: a paged table entry out of range)
-        const long long crow = is_q || !fits ? 0 : cache_row(p.pages, p.Hkv, p.cap, b, head, pos);
-        const bool stores = fits && crow >= 0;
-        if (!is_q && fits && crow < 0 && lane == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
-        const size_t slot = static_cast<size_t>(crow) * D;
-        if (!is_q && !is_k) {  // value row: stored as given (or quantised)
-            if (!stores) continue;
-            if (p.kv_dtype == UAA_DTYPE_VQ8 || p.kv_dtype == UAA_DTYPE_Q8) {
-                quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot, p.v_scale + crow);
-            } else {
-#pragma unroll
-                for (int i = 0; i < EPL; ++i) store_kv(p.v_cache, p.kv_dtype, slot + lane + 32 * i, x[i]);
+                for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
             }
-            continue;
-        }
-
-        if (p.qk_norm) {  // RMSNorm over the head row, before the rotation
-            float ss = 0.f;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) ss += x[i] * x[i];
-            ss = warp_sum(ss);
-            const float inv = rms_inv(ss, D, p.eps);
-            const float* w = is_q ? p.q_norm_w : p.k_norm_w;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) x[i] = x[i] * inv * (w[lane + 32 * i] + p.norm_offset);
         }
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) rowbuf[warp][lane + 32 * i] = x[i];
-        __syncwarp();
+        for (int i0 = 0; i0 < HALF; i0 += 32)  // warp w takes pairs 32 w .. 32 w + 31
+            if (warp == i0 / 32)
+                cs[i0 + lane] = rope_pair_cos_sin(i0 + lane, p.half_rot, pos, param_at_lane(p.inv_freq_over_pi + i0, lane),
+                                                  p.mscale);
+        __syncthreads();  // the cos / sin table is complete
+        for (int r = warp; r < n_rows; r += kAppendWarps) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) x[i] = nxt[i];
+            if (r + kAppendWarps < n_rows) {
+                size_t at;
+                const void* src = row_source(p, b, tok, r + kAppendWarps, at);
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
+            }
+            const bool is_q = r < p.Hq;
+            const bool is_k = !is_q && r < p.Hq + p.Hkv;
+            const int head = is_q ? r : (is_k ? r - p.Hq : r - p.Hq - p.Hkv);
+            const size_t in_row = ((static_cast<size_t>(b) * p.q_len + tok) * (is_q ? p.Hq : p.Hkv) + head) * D;
 
-        for (int pp = lane; pp < HALF; pp += 32) {
-            const int2 e = rope_pair(pp, p.half_rot, D, p.style == UAA_ROPE_NEOX);
-            const int ia = e.x, ib = e.y;
-            float ya = rowbuf[warp][ia], yb = rowbuf[warp][ib];
-            rope_rotate(ya, yb, cs[pp]);
-            if (is_q) {
-                float* qp = p.q_prime + in_row;
-                qp[ia] = ya * p.qscale;
-                qp[ib] = yb * p.qscale;
-                if (p.q_rot_out) {
-                    p.q_rot_out[in_row + ia] = ya;
-                    p.q_rot_out[in_row + ib] = yb;
+            // the new token's cache row (k and v rows; -1: a paged table entry out of range)
+            const long long crow = is_q || !fits ? 0 : cache_row(p.pages, p.Hkv, p.cap, b, head, pos);
+            const bool stores = fits && crow >= 0;
+            if (!is_q && fits && crow < 0 && lane == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
+            const size_t slot = static_cast<size_t>(crow) * D;
+            if (!is_q && !is_k) {  // value row: stored as given (or quantised)
+                if (!stores) continue;
+                if (p.kv_dtype == UAA_DTYPE_VQ8 || p.kv_dtype == UAA_DTYPE_Q8) {
+                    quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot, p.v_scale + crow);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < EPL; ++i) store_kv(p.v_cache, p.kv_dtype, slot + lane + 32 * i, x[i]);
                 }
-            } else if (stores && p.kv_dtype == UAA_DTYPE_Q8) {  // the whole rotated row first: its scale
-                rowbuf[warp][ia] = ya;                            // needs max |k| (pairs are disjoint)
-                rowbuf[warp][ib] = yb;
-            } else if (stores) {
-                store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
-                         slot + ia, ya);
-                store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
-                         slot + ib, yb);
+                continue;
+            }
+
+            if (p.qk_norm) {  // RMSNorm over the head row, before the rotation
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) ss += x[i] * x[i];
+                ss = warp_sum(ss);
+                const float inv = rms_inv(ss, D, p.eps);
+                const float* w = is_q ? p.q_norm_w : p.k_norm_w;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) x[i] = x[i] * inv * (w[lane + 32 * i] + p.norm_offset);
+            }
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) rowbuf[warp][lane + 32 * i] = x[i];
+            __syncwarp();
+
+            for (int pp = lane; pp < HALF; pp += 32) {
+                const int2 e = rope_pair(pp, p.half_rot, D, p.style == UAA_ROPE_NEOX);
+                const int ia = e.x, ib = e.y;
+                float ya = rowbuf[warp][ia], yb = rowbuf[warp][ib];
+                rope_rotate(ya, yb, cs[pp]);
+                if (is_q) {
+                    float* qp = p.q_prime + in_row;
+                    qp[ia] = ya * p.qscale;
+                    qp[ib] = yb * p.qscale;
+                    if (p.q_rot_out) {
+                        p.q_rot_out[in_row + ia] = ya;
+                        p.q_rot_out[in_row + ib] = yb;
+                    }
+                } else if (stores && p.kv_dtype == UAA_DTYPE_Q8) {  // the whole rotated row first: its scale
+                    rowbuf[warp][ia] = ya;                            // needs max |k| (pairs are disjoint)
+                    rowbuf[warp][ib] = yb;
+                } else if (stores) {
+                    store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
+                             slot + ia, ya);
+                    store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
+                             slot + ib, yb);
+                }
+            }
+            __syncwarp();
+            if (is_k && stores && p.kv_dtype == UAA_DTYPE_Q8) {  // q8 key: codes and scale of the rotated row
+                float y[EPL];
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) y[i] = rowbuf[warp][lane + 32 * i];
+                quantize_row<EPL>(y, lane, static_cast<int8_t*>(p.k_cache) + slot, p.k_scale + crow);
+                __syncwarp();  // the row is read before the next one overwrites it
             }
         }
-        __syncwarp();
-        if (is_k && stores && p.kv_dtype == UAA_DTYPE_Q8) {  // q8 key: codes and scale of the rotated row
-            float y[EPL];
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) y[i] = rowbuf[warp][lane + 32 * i];
-            quantize_row<EPL>(y, lane, static_cast<int8_t*>(p.k_cache) + slot, p.k_scale + crow);
-            __syncwarp();  // the row is read before the next one overwrites it
-        }
-    }
+    }  // tokens
     __syncthreads();
-    if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + 1;
+    if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + p.q_len;
 }
 
 template <int D>

@@ -40,11 +40,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int b = blockIdx.x / units, u = blockIdx.x - b * units;
     const int kvh = u / p.head_groups, hg = u - kvh * p.head_groups;
     const int HC = p.heads_per_cta;
-    const int h0 = kvh * p.G + hg * HC;
-    const int nh = min(HC, p.G - hg * HC);
+    const int r0 = hg * HC;                      // the unit's first query row (query_row)
+    const int nh = min(HC, p.q_len * p.G - r0);  // its query rows
     const int D = p.D;
     const int tid = threadIdx.x;
-    const size_t out0 = (static_cast<size_t>(b) * p.Hq + h0) * D;
+    // output element idx (row idx / D, column idx % D) of the unit
+    auto out_at = [&](int idx) {
+        const int hc = idx / D;
+        return query_row(b, r0 + hc, kvh, p.G, p.Hq, p.q_len) * D + (idx - hc * D);
+    };
     // the unit's first and last owner, left by the partial kernel (cleared for the next launch)
     unsigned* own = p.owners + 2 * static_cast<size_t>(blockIdx.x);
     const unsigned first = own[0], last = own[1];
@@ -54,11 +58,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         own[1] = 0u;
     }
     if (first == 0u || last == 0u) {  // no visible key: zeros
-        for (int idx = tid; idx < nh * D; idx += kCombineThreads) store_out(p.out, p.out_dtype, out0 + idx, 0.f);
+        for (int idx = tid; idx < nh * D; idx += kCombineThreads) store_out(p.out, p.out_dtype, out_at(idx), 0.f);
         return;
     }
     const int cA = static_cast<int>(first & 0x7fffffffu) - 1, cB = static_cast<int>(last) - 1;
     if (cA == cB) return;  // a whole unit: the partial kernel wrote it
+    if (cA < 0 || cB < cA || cB >= p.P) {  // owner words no range of this launch wrote: not read further
+        if (tid == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+        return;
+    }
     const bool first_is_slot0 = (first & 0x80000000u) != 0u;
     const int R = cB - cA + 1;  // the unit's records: owners cA .. cB
 
@@ -66,7 +74,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         wts[i] = p.rec_lse[static_cast<size_t>(record_of(cA + i / nh, cA, first_is_slot0)) * HC + (i % nh)];
     __syncthreads();
     for (int hc = tid; hc < nh; hc += kCombineThreads) {
-        const float z = p.sink ? p.sink[h0 + hc] * kLog2e : -INFINITY;
+        const float z = p.sink ? p.sink[kvh * p.G + (r0 + hc) % p.G] * kLog2e : -INFINITY;
         float M = z;
         for (int r = 0; r < R; ++r) M = fmaxf(M, wts[r * nh + hc]);
         float den = 0.f;
@@ -110,7 +118,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int idx = base + k * kCombineThreads;
-            if (idx < nh * D) store_out(p.out, p.out_dtype, out0 + idx, acc[k]);
+            if (idx < nh * D) store_out(p.out, p.out_dtype, out_at(idx), acc[k]);
         }
     }
 }

@@ -32,6 +32,7 @@ struct KvPages {
 
 struct AppendParams {
     int B, Hq, Hkv, D;
+    int q_len;              // tokens per sequence (rows [B][q_len][H][D] of q, k_new, v_new, q_prime)
     int cap, max_len;
     int style;              // UAA_ROPE_NEOX / _INTERLEAVED
     int half_rot;           // rotated pairs per head row (rotary_dim / 2)
@@ -111,9 +112,11 @@ constexpr unsigned kBalanceMagic = 0x42414c31u;
 struct PartialParams {
     int B, Hq, Hkv, D, G;
     int b_off;              // first sequence of this launch (batches are cut into slices)
-    int heads_per_cta;      // query heads per unit (8 * NHT for the tensor-core kernel)
-    int head_groups;        // ceil(G / heads_per_cta)
-    int cap, window;
+    int heads_per_cta;      // query rows per unit (8 * NHT for the tensor-core kernel)
+    int head_groups;        // row groups per kv head: ceil(q_len G / heads_per_cta)
+    int q_len;              // tokens per sequence: a unit's rows are (token, head) pairs (query_row)
+    int attn_window;        // the descriptor's window (0: none), per query row
+    int cap, window;        // window: of the partition, attn_window + q_len - 1 (0: none)
     int mg;                 // 64-key tiles per stage
     float softcap_log2e;    // 0: no softcap; else softcap * log2(e)
     const float* q_prime;   // [B][Hq][D] (slice-relative: already offset by b_off)
@@ -159,6 +162,7 @@ struct PartialParams {
 struct CombineParams {
     int B, Hq, Hkv, D, G;
     int heads_per_cta, head_groups;
+    int q_len;
     int window, mg, P;
     int out_dtype;
     const float* sink;      // [Hq] or null
@@ -293,9 +297,12 @@ __device__ __forceinline__ void sequence_keys(int L, int window, int cap, bool f
 // the lengths themselves into lens[0..B) (warp 0 scans, every thread returns
 // after the barrier; nothing reads seq_lens afterwards). Writes the prefix to
 // `global_copy` too when it is not null; flags go to `status` when it is not null.
+// With `owners` (one CTA of the launch passes it) the owner words of the units
+// of a sequence without stages are zeroed: no range writes them, and the
+// workspace region may hold other data from a step of another geometry.
 __device__ inline void build_stage_prefix(const int* seq_lens, int B, int window, int cap, int mg, int units,
                                           int* prefix, int* lens, int* global_copy, unsigned* status,
-                                          bool fused = false, int max_len = 0)
+                                          bool fused = false, int max_len = 0, unsigned* owners = nullptr)
 {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
@@ -315,6 +322,8 @@ __device__ inline void build_stage_prefix(const int* seq_lens, int B, int window
                 int lo, hi;
                 sequence_keys(n, window, cap, fused, lo, hi);
                 v = units * stages_of(lo, hi, mg);
+                if (owners && v == 0)
+                    for (int u = 0; u < 2 * units; ++u) owners[2 * static_cast<size_t>(b) * units + u] = 0u;
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -459,6 +468,16 @@ __device__ __forceinline__ int2 rope_pair(int pp, int half_rot, int D, bool neox
 {
     if (!neox) return make_int2(2 * pp, 2 * pp + 1);
     return pp < half_rot ? make_int2(pp, pp + half_rot) : make_int2(pp + half_rot, pp + D / 2);
+}
+
+// Query row r of a unit of kv head kvh: the rows of a kv head are the (token,
+// head) pairs of the step, token-major, so row r is token r / G at query head
+// kvh G + r % G. Returns its index in the [B][q_len][Hq] rows of q, q_prime and
+// out (with q_len = 1: b Hq + kvh G + r).
+__device__ __forceinline__ size_t query_row(int b, int r, int kvh, int G, int Hq, int q_len)
+{
+    const int t = r / G;
+    return (static_cast<size_t>(b) * q_len + t) * Hq + kvh * G + (r - t * G);
 }
 
 // Cache row of (sequence b, kv head g, position j) under KvPages, or -1 where

@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
     const int units = p.Hkv * p.head_groups;
     grid_dependency_wait();  // the append's lengths, q rows and cache rows are complete
     build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, 1, units, prefix, lens,
-                       blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr);
+                       blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr, false, 0,
+                       blockIdx.x == 0 ? p.owners : nullptr);
     const long long T = prefix[p.B];
     const int P = T < gridDim.x ? static_cast<int>(T) : static_cast<int>(gridDim.x);  // every range non-empty
     const long long s_c = static_cast<int>(blockIdx.x) < P ? range_start(blockIdx.x, T, P) : 0;
@@ -48,8 +49,16 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
 
     for (long long pos = s_c; pos < e_c;) {
         const Segment sg = segment_at(prefix, lens, p.B, p.window, p.cap, p.head_groups, units, pos, e_c);
-        const int h0 = sg.kvh * p.G + sg.hg * kSimtHeads;
-        const int nh = min(kSimtHeads, p.G - sg.hg * kSimtHeads);
+        const int r0 = sg.hg * kSimtHeads;                   // the unit's first query row (query_row)
+        const int nh = min(kSimtHeads, p.q_len * p.G - r0);  // its query rows
+        // several tokens per sequence: row r (token r / G) sees keys up to its own
+        // position, lens[b] - q_len + r / G, and with a window the last attn_window
+        int kmax[kSimtHeads], kmin[kSimtHeads];
+#pragma unroll
+        for (int h = 0; h < kSimtHeads; ++h) {
+            kmax[h] = lens[sg.b] - p.q_len + min(r0 + h, p.q_len * p.G - 1) / p.G;
+            kmin[h] = p.attn_window > 0 ? kmax[h] - p.attn_window + 1 : 0;
+        }
         if (threadIdx.x == 0) {  // this range's part in the unit's owners, for the combine
             unsigned* own = p.owners + 2 * (static_cast<size_t>(sg.b) * units + sg.kvh * p.head_groups + sg.hg);
             if (sg.st0 == 0) own[0] = (blockIdx.x + 1u) | (pos == s_c ? 0x80000000u : 0u);
@@ -64,7 +73,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
         for (int h = 0; h < kSimtHeads; ++h)
 #pragma unroll
             for (int i = 0; i < EPL; ++i)
-                q[h][i] = h < nh ? p.q_prime[(static_cast<size_t>(sg.b) * p.Hq + h0 + h) * D + lane + 32 * i] : 0.f;
+                q[h][i] = h < nh ? p.q_prime[query_row(sg.b, r0 + h, sg.kvh, p.G, p.Hq, p.q_len) * D + lane + 32 * i]
+                                 : 0.f;
 
         float m[kSimtHeads], l[kSimtHeads], o[kSimtHeads][EPL];
 #pragma unroll
@@ -99,6 +109,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
 #pragma unroll
                 for (int h = 0; h < kSimtHeads; ++h) {
                     if (h >= nh) break;
+                    if (jb + u > kmax[h] || jb + u < kmin[h]) continue;  // beyond the row's own token
                     float dot = 0.f;
 #pragma unroll
                     for (int i = 0; i < EPL; ++i) dot = fmaf(q[h][i], kx[u][i], dot);
@@ -133,7 +144,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kSimtWarps; ++w) M = fmaxf(M, red_m[w][h]);
-            const float zs = (sg.whole && p.sink) ? p.sink[h0 + h] * kLog2e : -INFINITY;
+            const int hq = sg.kvh * p.G + (r0 + h) % p.G;  // the row's query head
+            const float zs = (sg.whole && p.sink) ? p.sink[hq] * kLog2e : -INFINITY;
             if (sg.whole) M = fmaxf(M, zs);
             float L = 0.f, acc = 0.f;
             if (M != -INFINITY) {
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) partial_simt_kernel(const Par
             if (sg.whole) {
                 const float den = L + (zs == -INFINITY ? 0.f : exp2f(zs - M));
                 const float v = den > 0.f ? acc / den : 0.f;
-                const size_t oi = (static_cast<size_t>(sg.b) * p.Hq + h0 + h) * D + d;
+                const size_t oi = query_row(sg.b, r0 + h, sg.kvh, p.G, p.Hq, p.q_len) * D + d;
                 if (p.out_dtype == UAA_DTYPE_F32)
                     static_cast<float*>(p.out)[oi] = v;
                 else

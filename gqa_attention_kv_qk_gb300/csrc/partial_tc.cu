@@ -336,7 +336,7 @@ __device__ void prep_fused_q(const PartialParams& p, int b, int h0, int nh, bool
 // prescaled, fp32) into the fragment slot, eight rows' loads at a time (fp16
 // parts for int8 keys when F16).
 template <int D, int HC, bool F16>
-__device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int h0, int nh, uint8_t* frag,
+__device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int kvh, int r0, int nh, uint8_t* frag,
                                               int row_bytes, uint32_t go, int lane)
 {
 #pragma unroll 1
@@ -344,7 +344,8 @@ __device__ __forceinline__ void prep_loaded_q(const PartialParams& p, int b, int
         float2 x[8][D / 64];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float* qrow = p.q_prime + (static_cast<size_t>(b) * p.Hq + h0 + hc0 + i) * D;
+            const float* qrow =
+                p.q_prime + (hc0 + i < nh ? query_row(b, r0 + hc0 + i, kvh, p.G, p.Hq, p.q_len) : 0) * D;
 #pragma unroll
             for (int j = 0; j < D / 64; ++j)
                 x[i][j] = hc0 + i < nh ? *reinterpret_cast<const float2*>(qrow + 2 * lane + 64 * j)
@@ -619,7 +620,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     build_stage_prefix(p.seq_lens, p.B, p.window, p.cap, MG, units, prefix, lens,
                        blockIdx.x == 0 ? p.prefix : nullptr, blockIdx.x == 0 ? p.status : nullptr, p.fused != 0,
-                       p.max_len);  // ends with __syncthreads; seq_lens is not read again
+                       p.max_len, blockIdx.x == 0 ? p.owners : nullptr);  // ends with __syncthreads
     unsigned long long t_begin = 0;
     if (threadIdx.x == 0) {
         long long rs, re;
@@ -726,8 +727,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
                 break;
             }
-            const int h0 = sg.kvh * p.G + sg.hg * HC;
-            const int nh = min(HC, p.G - sg.hg * HC);
+            const int r0 = sg.hg * HC;                     // the unit's first query row
+            const int h0 = sg.kvh * p.G + r0;              // its query head (one token per sequence)
+            const int nh = min(HC, p.q_len * p.G - r0);    // its query rows
             if (lane == 0) {  // this range's part in the unit's owners, for the combine
                 unsigned* own = p.owners + 2 * (static_cast<size_t>(sg.b) * units + sg.kvh * p.head_groups + sg.hg);
                 if (sg.st0 == 0) own[0] = (static_cast<unsigned>(slot) + 1u) | (pos == s_c ? 0x80000000u : 0u);
@@ -765,7 +767,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 pos += sg.n_st;
                 continue;
             } else {
-                prep_loaded_q<D, HC, KQ8>(p, sg.b, h0, nh, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
+                prep_loaded_q<D, HC, KQ8>(p, sg.b, sg.kvh, r0, nh, frag, SH::kFragRow, seg == 0 ? go : 0u, lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_qfull);
@@ -789,8 +791,21 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                                       p.fused != 0);
         const int lo = sg.lo, hi = sg.hi;
         const int t0 = lo / kTileKeys;
-        const int h0 = sg.kvh * p.G + sg.hg * HC;
-        const int nh = min(HC, p.G - sg.hg * HC);
+        const int r0 = sg.hg * HC;                   // the unit's first query row (query_row)
+        const int nh = min(HC, p.q_len * p.G - r0);  // its query rows
+        // several tokens per sequence: row r (token r / G) sees keys up to its own
+        // position, lens[b] - q_len + r / G, and with a window the last attn_window
+        // of them; this thread's columns 2t, 2t + 1 of each 8-row tile
+        const bool causal = p.q_len > 1;
+        int kmax[NHT][2], kmin[NHT][2];
+#pragma unroll
+        for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int tok = min(r0 + nt * 8 + 2 * t + j, p.q_len * p.G - 1) / p.G;
+                kmax[nt][j] = lens[sg.b] - p.q_len + tok;
+                kmin[nt][j] = p.attn_window > 0 ? kmax[nt][j] - p.attn_window + 1 : INT_MIN;
+            }
 
         // fused append: the new key (slot L) is row new_r of the unit's last stage,
         // which consumer warp new_w owns; -1 when this segment does not end the unit
@@ -969,6 +984,10 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             float v = sacc[mg][nt][e];
                             if (cap2 > 0.f) v = tanhf(v) * cap2;
                             if (!((e < 2) ? vg[mg] : vg8[mg])) v = -INFINITY;
+                            if (causal) {
+                                const int key = kbase + 16 * mg + g + 8 * (e >> 1);
+                                if (key > kmax[nt][e & 1] || key < kmin[nt][e & 1]) v = -INFINITY;
+                            }
                             x[mg][nt][e] = v;
                         }
                         mx0 = fmaxf(mx0, fmaxf(x[mg][nt][0], x[mg][nt][2]));
@@ -1130,7 +1149,8 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * HC + hc]);
-                const float zs = (sg.whole && p.sink) ? p.sink[h0 + hc] * kLog2e : -INFINITY;
+                const int hq = sg.kvh * p.G + (r0 + hc) % p.G;  // the row's query head
+                const float zs = (sg.whole && p.sink) ? p.sink[hq] * kLog2e : -INFINITY;
                 if (sg.whole) M = fmaxf(M, zs);  // the sink joins the denominator of a whole unit
                 float L = 0.f, acc = 0.f;
                 if (M != -INFINITY) {
@@ -1145,7 +1165,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (sg.whole) {
                     const float den = L + (zs == -INFINITY ? 0.f : exp2f(zs - M));
                     const float v = den > 0.f ? acc / den : 0.f;
-                    const size_t oi = (static_cast<size_t>(sg.b) * p.Hq + h0 + hc) * D + c0 + dc;
+                    const size_t oi = query_row(sg.b, r0 + hc, sg.kvh, p.G, p.Hq, p.q_len) * D + c0 + dc;
                     if (p.out_dtype == UAA_DTYPE_F32)
                         static_cast<float*>(p.out)[oi] = v;
                     else

@@ -23,10 +23,12 @@ class DecodeLayer:
     """page_size: store the caches as pools of pages of that many positions;
     block_table ([batch][capacity / page_size] int32, default: sequence b takes
     pages b P .. b P + P - 1) maps each sequence's logical pages to pool pages, of
-    which there are n_pages (default: just enough)."""
+    which there are n_pages (default: just enough). max_q_len: the most tokens per
+    sequence one step takes (q, k_new, v_new of shape [B][T][H][D]); the
+    workspace is sized for it."""
 
     def __init__(self, cfg: dict, batch: int, capacity: int, device="cuda", page_size=None, block_table=None,
-                 n_pages=None):
+                 n_pages=None, max_q_len=1):
         self.cfg = dict(cfg)
         self.device = _require_cuda(device)
         self.batch = int(batch)
@@ -66,9 +68,12 @@ class DecodeLayer:
         self.seq_lens = torch.zeros((batch,), dtype=torch.int32, device=dev)
         self.max_len_hint = 0
         self.out = torch.empty((batch, Hq, D), dtype=_TORCH_DTYPE[cfg.get("out_dtype", "f32")], device=dev)
+        self._outs = {1: self.out}  # per tokens-per-step count: [B][Hq][D], or [B][T][Hq][D]
+        self.q_len = 1              # tokens per sequence of the current step
+        self.max_q_len = int(max_q_len)
         self.q_norm_w = self.k_norm_w = self.sink = None
         # workspace sized for the longest allowed sequence; zeroed once (status word)
-        nbytes = B.uaa_workspace_size(self.desc, batch, capacity - 1, 0)
+        nbytes = B.uaa_workspace_size(self.desc, batch, capacity - 1, 0, self.max_q_len)
         if nbytes == 0:
             raise B.UaaError(B.UAA_ERR_UNSUPPORTED, B.last_error())
         self.ws_tensor = torch.zeros((nbytes,), dtype=torch.uint8, device=dev)
@@ -132,10 +137,28 @@ class DecodeLayer:
         self.max_len_hint = int(lens.max()) if lens.numel() else 0
 
     # ------------------------------------------------------------ calls
+    def out_for(self, q_len: int):
+        """The layer's output rows for steps of q_len tokens per sequence."""
+        o = self._outs.get(q_len)
+        if o is None:
+            o = self._outs[q_len] = torch.empty((self.batch, q_len, *self.out.shape[1:]), dtype=self.out.dtype,
+                                                device=self.device)
+        return o
+
+    def _begin(self, q):
+        """Tokens per sequence of a step's q ([B][Hq][D] or [B][T][Hq][D])."""
+        T = int(q.shape[1]) if q.dim() == 4 else 1
+        if T > self.max_q_len:
+            raise ValueError(f"{T} tokens per sequence, the layer was built for max_q_len={self.max_q_len}")
+        self.q_len = T
+        return T
+
     def args(self, q, k_new, v_new, max_seq_len=None, q_rot=None, out=None) -> B.UaaStepArgs:
         """The step's argument struct (a copy of one built once per distinct set of pointers)."""
         msl = self.max_len_hint if max_seq_len is None else int(max_seq_len)
-        key = (B.ptr(q), B.ptr(k_new), B.ptr(v_new), msl, B.ptr(q_rot), B.ptr(self.out if out is None else out))
+        if out is None:
+            out = self.out_for(self.q_len)
+        key = (B.ptr(q), B.ptr(k_new), B.ptr(v_new), msl, B.ptr(q_rot), B.ptr(out), self.q_len)
         cache = self.__dict__.setdefault("_args_cache", {})
         a = cache.get(key)
         if a is None:
@@ -156,29 +179,36 @@ class DecodeLayer:
         a.out = B.ptr(self.out if out is None else out)
         a.q_rot = B.ptr(q_rot)
         a.k_scale = B.ptr(self.k_scale)
+        a.q_len = self.q_len
         if self.page_size:
             a.block_table = B.ptr(self.block_table)
             a.page_size, a.pages_per_seq, a.n_pages = self.page_size, self.pages_per_seq, self.n_pages
         return a
 
     def step(self, q, k_new, v_new, stream=None, max_seq_len=None, advance_hint=True, q_rot=None, out=None):
-        """One decode step (append, split-K partials, combine) on `stream`; the output
-        rows go to `out` (a [B][Hq][D] tensor of the layer's output dtype) if given."""
+        """One step (append, split-K partials, combine) on `stream` for q of one token
+        per sequence ([B][Hq][D]) or T tokens ([B][T][Hq][D], causal within the
+        chunk); the output rows ([B][Hq][D] or [B][T][Hq][D]) go to `out` if given."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        T = self._begin(q)
+        want = self.out_for(T)
         if out is not None:
-            assert out.shape == self.out.shape and out.dtype == self.out.dtype and out.is_contiguous()
+            assert out.shape == want.shape and out.dtype == want.dtype and out.is_contiguous()
         B.uaa_decode_attn(self.desc, self.args(q, k_new, v_new, max_seq_len, q_rot=q_rot, out=out), self.ws, s)
         if advance_hint and max_seq_len is None:
-            self.max_len_hint += 1
-        return self.out if out is None else out
+            self.max_len_hint += T
+        return want if out is None else out
 
     def append(self, q, k_new, v_new, stream=None, q_rot=None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self._begin(q)
         B.uaa_rope_qk_norm_append(self.desc, self.args(q, k_new, v_new, q_rot=q_rot), self.ws, s)
 
     def append_partial(self, q, k_new, v_new, stream=None, q_rot=None):
-        """Steps 1 and 2 (one fused kernel for bf16 / vq8 caches); follow with combine()."""
+        """Steps 1 and 2 (one fused kernel for bf16 / vq8 / q8 caches and one token);
+        follow with combine()."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self._begin(q)
         B.uaa_decode_attn_append_partial(self.desc, self.args(q, k_new, v_new, q_rot=q_rot), self.ws, s)
 
     def partial(self, stream=None):
@@ -188,12 +218,12 @@ class DecodeLayer:
     def combine(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         B.uaa_decode_attn_combine(self.desc, self.args(None, None, None), self.ws, s)
-        self.max_len_hint += 1
-        return self.out
+        self.max_len_hint += self.q_len
+        return self.out_for(self.q_len)
 
     def layout(self, max_seq_len=None) -> B.UaaWorkspaceLayout:
         return B.uaa_get_workspace_layout(self.desc, self.batch,
-                                          self.max_len_hint if max_seq_len is None else max_seq_len, 0)
+                                          self.max_len_hint if max_seq_len is None else max_seq_len, 0, self.q_len)
 
     def device_status(self, stream=None) -> int:
         s = stream if stream is not None else torch.cuda.current_stream(self.device)

@@ -72,6 +72,13 @@ CONFIGS: dict[str, dict] = {
         kv_dtype="bf16", io_dtype="bf16", out_dtype="f32", page_size=16,
         rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
         low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
+    # The Llama-3.1-8B-like cache with 4 tokens per sequence and step (draft tokens
+    # to verify), each attending the cache and the chunk's earlier tokens.
+    "llama31_8b_verify": dict(
+        batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, seq_len=8192, steps=16, seed=8, q_len=4,
+        kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
+        low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
     # Gemma-3-12B-like decode: QK RMSNorm whose weights are stored as deltas from
     # one (applied as 1 + w), scale 1/sqrt(256), no softcap; one layer of each
     # kind per step (the model runs five local layers per global one): a local

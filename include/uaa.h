@@ -18,7 +18,8 @@
  *      log-sum-exp) per range it touches in the workspace.
  *   3. uaa_decode_attn_combine: log-sum-exp merge of those records, the sink
  *      logit added to the denominator, the remaining output rows written.
- *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16, vq8 and q8 caches in one
+ *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16, vq8 and q8 caches and
+ *   one token per sequence in one
  *   kernel that forms q', k and v of the new token itself and attends the new
  *   key from shared memory); uaa_decode_attn runs 1-3 on one stream.
 
@@ -69,7 +70,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 8
+#define UAA_ABI_VERSION 9
 
 typedef enum {
     UAA_OK = 0,
@@ -182,6 +183,14 @@ typedef struct {
     int32_t page_size;        /* keys per page: a power of two in [16, 4096]; >= 32 for VQ8 / Q8 */
     int32_t pages_per_seq;    /* row length of block_table */
     int32_t n_pages;          /* pages in each pool */
+    /* Tokens per sequence in this step, T (0 counts as 1: a decode step). With
+     * T > 1 (a prefill chunk, or draft tokens to verify) q, k_new, v_new, out and
+     * q_rot hold T rows per sequence, [B][T][H][D]; token t sits at position
+     * seq_lens[b] + t, is appended there, and attends the keys up to and
+     * including its own (causal within the chunk, and within the window);
+     * seq_lens[b] grows by T, and max_seq_len + T must fit cache_capacity. The
+     * (token, head) rows of a kv head share every K/V tile the step reads. */
+    int32_t q_len;
 } uaa_step_args;
 
 /* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed
@@ -201,7 +210,7 @@ typedef struct {
     int32_t n_ctas;           /* P: persistent CTAs of the partial step (stream-K ranges) */
     int32_t stage_keys;       /* keys per ring stage: 64; 128 for q8 at head_dim 128 / 256;
                                  at head_dim 64 128 (bf16), 256 (vq8, q8) */
-    int32_t heads_per_cta;    /* query heads of one unit (sequence, kv head, head group) */
+    int32_t heads_per_cta;    /* query rows (token, head) of one unit (sequence, kv head, row group) */
     int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
     int32_t n_slices;         /* partial + combine launches (batch slices) */
     int32_t slice_batch;      /* sequences per slice (the last may hold fewer) */
@@ -248,8 +257,9 @@ uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_arg
  * have read the lengths advances seq_lens. Results, cache rows and seq_lens are
  * those of uaa_rope_qk_norm_append followed by uaa_decode_attn_partial, up to
  * fp32 rounding order (appended key rows within one bf16 ulp, or one q8 code
- * where the rotated key lies within fp32 rounding of a rounding tie). For fp32 caches
- * it is those two launches. Follow it with uaa_decode_attn_combine. */
+ * where the rotated key lies within fp32 rounding of a rounding tie). For fp32 caches,
+ * and for steps of q_len > 1, it is those two launches. Follow it with
+ * uaa_decode_attn_combine. */
 uaa_status uaa_decode_attn_append_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
                                           const uaa_workspace* ws, cudaStream_t stream);
 
@@ -258,20 +268,22 @@ uaa_status uaa_decode_attn_append_partial(const uaa_attn_desc* desc, const uaa_s
 uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
                            const uaa_workspace* ws, cudaStream_t stream);
 
-/* Workspace bytes for a step of `batch` sequences whose lengths before the step
- * are at most max_seq_len. n_sm <= 0 queries the current device's SM count; the
- * launches always use the current device's count. Returns 0 on a refused desc. */
+/* Workspace bytes for a step of `batch` sequences of q_len tokens each (0 or 1:
+ * decode) whose lengths before the step are at most max_seq_len; a workspace
+ * sized for q_len serves every step of at most q_len tokens. n_sm <= 0 queries
+ * the current device's SM count; the launches always use the current device's
+ * count. Returns 0 on a refused desc. */
 size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len,
-                          int32_t n_sm);
+                          int32_t n_sm, int32_t q_len);
 
 /* Number of CTAs P the split-K step runs (each attends one contiguous range of
  * the key stages of all units); 0 on a refused desc. */
 int32_t uaa_num_splits(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len,
-                       int32_t n_sm);
+                       int32_t n_sm, int32_t q_len);
 
 /* The workspace layout and split geometry (host only; n_sm as above). */
 uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch,
-                                    int32_t max_seq_len, int32_t n_sm,
+                                    int32_t max_seq_len, int32_t n_sm, int32_t q_len,
                                     uaa_workspace_layout* layout);
 
 /* Quantise n_rows rows of head_dim values (fp32 or bf16, v_dtype) to the vq8

@@ -65,9 +65,10 @@ def gpu_layer(case: dict, device="cuda"):
         P = case["cap"] // ps
         n_pages = cfg["batch"] * P + max(2, cfg["batch"])
         layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device, page_size=ps,
-                            block_table=W.block_table(cfg, P, n_pages), n_pages=n_pages)
+                            block_table=W.block_table(cfg, P, n_pages), n_pages=n_pages,
+                            max_q_len=int(cfg.get("q_len", 1) or 1))
     else:
-        layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device)
+        layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device, max_q_len=int(cfg.get("q_len", 1) or 1))
     k = case["k_values"] if cfg.get("kv_dtype") == "q8" else case["k_cache"]
     v = case["v_values"] if cfg.get("kv_dtype") in ("vq8", "q8") else case["v_cache"]
     layer.load_cache(k, v, case["lens"])

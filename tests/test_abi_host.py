@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 8
+    assert B.uaa_abi_version() == 9
 
 
 def good_desc(**kw):

@@ -69,11 +69,13 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         assert np.array_equal(C("k_cache").cpu().numpy(), a["k_cache"])
         assert np.array_equal(C("k_scale").cpu().numpy().view(np.uint32), a["k_scale"].view(np.uint32))
     B_, Hq, D = cfg["batch"], cfg["n_q_heads"], cfg["head_dim"]
+    T = int(cfg.get("q_len", 1) or 1)  # tokens per sequence and step
+    tok = (T,) if T > 1 else ()
     worst = (0.0, 0.0)
     for step in range(steps):
         inp = W.step_inputs(cfg, step)
         pre = a["seq_lens"].copy()
-        q_rot = torch.empty((B_, Hq, D), dtype=torch.float32, device="cuda")
+        q_rot = torch.empty((B_, *tok, Hq, D), dtype=torch.float32, device="cuda")
         dev = {k: v.cuda() for k, v in inp.items()}
         if entry == "split":
             layer.append(dev["q"], dev["k_new"], dev["v_new"], q_rot=q_rot)
@@ -89,11 +91,17 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         if lay.kernel == 1:
             hdr = layer.ws_tensor[lay.balance_offset: lay.balance_offset + 12].view(torch.int32).cpu().tolist()
             assert hdr[0] == 0x42414c31 and hdr[1] == lay.n_ctas and hdr[2] >= 1
-        qr = oracle_mod.append(cfg, W.bits(inp["q"]).copy(), W.bits(inp["k_new"]).copy(),
-                               W.bits(inp["v_new"]).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
-                               a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
-        want = oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"],
-                                 k_scale=a["k_scale"])
+        qrs, wants = [], []
+        for t in range(T):  # a chunk is its tokens' decode steps, in order
+            pick = (lambda x: x) if T == 1 else (lambda x: x[:, t])
+            qr = oracle_mod.append(cfg, W.bits(pick(inp["q"])).copy(), W.bits(pick(inp["k_new"])).copy(),
+                                   W.bits(pick(inp["v_new"])).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
+                                   a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
+            qrs.append(qr)
+            wants.append(oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"],
+                                           a["seq_lens"], k_scale=a["k_scale"]))
+        qr = qrs[0] if T == 1 else np.stack(qrs, axis=1)
+        want = wants[0] if T == 1 else np.stack(wants, axis=1)
         # positions / slots: bit-exact
         assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
         assert layer.device_status() == 0
@@ -102,8 +110,7 @@ def run_and_compare(oracle_mod, cfg, lens, cap=None, steps=1, fill_unused="zero"
         # the appended rows
         kc_g, vc_g = C("k_cache"), C("v_cache")
         ks_g, vs_g = C("k_scale"), C("v_scale")
-        for b in range(B_):
-            slot = int(pre[b])
+        for b, slot in ((b, int(pre[b]) + t) for b in range(B_) for t in range(T)):
             kg = f64(kc_g[b, :, slot].float())
             if kv == "q8":
                 # codes of the rotated key: the GPU rotates in fp32, the oracle in fp64, so a
@@ -156,6 +163,7 @@ SMALL = {
     "gemma3_12b_local_global": dict(overrides=dict(batch=3, seq_len=(1, 3000)), lens=[2999, 1023, 5]),
     "llama31_8b_q8": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
     "llama31_8b_paged": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
+    "llama31_8b_verify": dict(overrides=dict(batch=3, seq_len=1400, steps=3), lens=[700, 1000, 1337]),
 }
 
 
@@ -227,6 +235,20 @@ EDGE = [
     ("paged-128-d256", "gemma2_9b_swa", dict(batch=2, seq_len=600, page_size=128, layers=None), [599, 10]),
     ("paged-4096-d256-window", "gemma2_9b_swa", dict(batch=2, seq_len=5000, page_size=4096,
                                                      layers=[dict(window=4096)]), [4999, 4100]),
+    # several tokens per sequence (causal chunks): G x T rows from 2 to 64 per kv head,
+    # windows shorter than the chunk, every cache kind, paged, first tokens
+    ("chunk2-first-token", "llama31_8b_decode", dict(batch=3, seq_len=200, q_len=2), [0, 1, 63]),
+    ("chunk4-g4-d128", "llama31_8b_decode", dict(batch=2, seq_len=500, q_len=4), [499, 60]),
+    ("chunk3-mha-window2", "qwen3_8b_ragged", dict(batch=2, n_q_heads=8, n_kv_heads=8, seq_len=(1, 300), q_len=3,
+                                                   window=2), [299, 1]),
+    ("chunk8-g8-d64-vq8-sink", "gptoss_vq8_sink", dict(batch=2, n_q_heads=16, n_kv_heads=2, seq_len=400, q_len=8),
+     [399, 100]),
+    ("chunk5-d256-window-softcap", "gemma2_9b_swa", dict(batch=2, seq_len=600, q_len=5, layers=[dict(window=7)]),
+     [599, 3]),
+    ("chunk6-f32-paged16", "llama32_1b_tiny", dict(batch=2, seq_len=300, q_len=6, page_size=16), [290, 40]),
+    ("chunk16-q8-paged64", "llama31_8b_q8", dict(batch=2, seq_len=700, q_len=16, page_size=64), [680, 100]),
+    ("chunk64-prefill-g2", "llama31_8b_decode", dict(batch=2, n_q_heads=16, n_kv_heads=8, seq_len=300, q_len=64),
+     [200, 0]),
     ("d64-vq8-norm-offset-local", "gemma3_12b_local_global",
      dict(batch=2, seq_len=600, head_dim=64, kv_dtype="vq8", layers=[dict(window=100, rope_theta=10000.0,
                                                                           rope_scaling="none")]), [599, 40]),
@@ -449,7 +471,7 @@ def test_partial_records_match_oracle_ranges(oracle_mod, name, over, lens, entry
 # ------------------------------------------------------------------ full size, sampled
 
 FULL = ["llama32_1b_tiny", "llama31_8b_decode", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink",
-        "gemma3_12b_local_global", "llama31_8b_q8", "llama31_8b_paged"]
+        "gemma3_12b_local_global", "llama31_8b_q8", "llama31_8b_paged", "llama31_8b_verify"]
 
 
 @pytest.mark.slow
@@ -463,20 +485,23 @@ def test_full_size_sampled(oracle_mod, name):
     for layer_cfg in W.layer_configs(cfg):
         case = host_case(layer_cfg)
         layer = gpu_layer(case)
-        layer.step(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda())
-        out = layer.out.cpu().numpy()
+        out = layer.step(case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda()).cpu().numpy()
         a = oracle_arrays(case, oracle_mod)
-        qr = oracle_mod.append(layer_cfg, a["q"], a["k_new"], a["v_new"], a["q_norm_w"], a["k_norm_w"],
-                               a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
-        assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
-        assert layer.device_status() == 0
+        T = int(layer_cfg.get("q_len", 1) or 1)
         Bn, Hq = layer_cfg["batch"], layer_cfg["n_q_heads"]
         units = sorted({(int(rng.integers(Bn)), int(rng.integers(Hq))) for _ in range(24)} | {(0, 0), (Bn - 1, Hq - 1)})
-        want = oracle_mod.attend(layer_cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"],
-                                 a["seq_lens"], units=units, k_scale=a["k_scale"])
-        got = np.stack([out[b, h] for b, h in units])
-        assert_out_close(got, want, name)
+        for t in range(T):  # token t: appended, then attended, before token t + 1
+            pick = (lambda x: x) if T == 1 else (lambda x: np.ascontiguousarray(x[:, t]))
+            qr = oracle_mod.append(layer_cfg, pick(a["q"]), pick(a["k_new"]), pick(a["v_new"]), a["q_norm_w"],
+                                   a["k_norm_w"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
+            want = oracle_mod.attend(layer_cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"],
+                                     a["seq_lens"], units=units, k_scale=a["k_scale"])
+            got = np.stack([(out[b, h] if T == 1 else out[b, t, h]) for b, h in units])
+            assert_out_close(got, want, f"{name} token {t}")
+        assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
+        assert layer.device_status() == 0
         if layer_cfg["kv_dtype"] in ("vq8", "q8"):
             pre = case["lens"].numpy()
+            vc = layer.logical("v_cache")
             for b in range(Bn):
-                assert np.array_equal(layer.v_cache[b, :, pre[b]].cpu().numpy(), a["v_cache"][b, :, pre[b]])
+                assert np.array_equal(vc[b, :, pre[b]].cpu().numpy(), a["v_cache"][b, :, pre[b]])
