@@ -16,7 +16,7 @@ import torch
 
 from gqa_attention_kv_qk_gb300 import binding as B
 from gqa_attention_kv_qk_gb300 import workloads as W
-from tests.cases import gpu_layer, host_case, oracle_arrays
+from tests.cases import gpu_layer, host_case, oracle_arrays, run_oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -353,6 +353,43 @@ def test_capacity_flag_and_no_write(oracle_mod):
     assert layer.seq_lens.cpu().tolist() == [64, 11]
     assert torch.equal(layer.k_cache[0], before[0])
     assert layer.device_status() == 0  # cleared by the read
+
+
+@pytest.mark.parametrize("name", ["llama31_8b_decode", "llama32_1b_tiny"])
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_bad_page_entry_is_flagged_and_nothing_else_changes(oracle_mod, name, entry):
+    """Failure detection on the host side of a paged cache: a block-table entry
+    outside the pool (one under a visible page, one under the new token's page)
+    is read as zeros and never written through; the step sets UAA_DEVFLAG_PAGE,
+    the other sequence's output stays exact and no page of the pool changes but
+    the other sequence's new slot. Both the tensor-core (bf16) and the CUDA-core
+    (fp32) kernels."""
+    cfg = W.config(name, batch=2, seq_len=300, page_size=32)
+    case = host_case(cfg, lens=[299, 200])
+    want, _ = run_oracle_step(case, oracle_mod)
+    layer = gpu_layer(case)
+    orig = layer.block_table.clone()
+    k_before, v_before = layer.k_cache.clone(), layer.v_cache.clone()
+    layer.block_table[0, 3] = layer.n_pages + 5   # keys 96 .. 127 of sequence 0
+    layer.block_table[0, 299 // 32] = -1          # the page of sequence 0's new token
+    q, k, v = case["q"].cuda(), case["k_new"].cuda(), case["v_new"].cuda()
+    if entry == "split":
+        layer.append(q, k, v)
+        layer.partial()
+        out = layer.combine()
+    else:
+        out = layer.step(q, k, v)
+    torch.cuda.synchronize()
+    assert layer.device_status() & B.UAA_DEVFLAG_PAGE
+    assert_out_close(out[1].cpu().numpy(), want[1], "the other sequence")
+    # only sequence 1's new slot was written
+    slot1 = (int(orig[1, 200 // 32]), 200 % 32)
+    for pool, before in ((layer.k_cache, k_before), (layer.v_cache, v_before)):
+        diff = (pool.float() != before.float()).flatten(2).any(-1).nonzero().tolist()  # [page, head]
+        rows = {(pg, h) for pg, h in diff}
+        assert rows <= {(slot1[0], h) for h in range(cfg["n_kv_heads"])}, rows
+        changed = (pool[slot1[0]].float() != before[slot1[0]].float()).any(-1).nonzero().tolist()
+        assert all(r == slot1[1] for _, r in changed), changed
 
 
 def test_length_hint_violation_is_flagged_and_results_stay_exact(oracle_mod):
