@@ -186,7 +186,9 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int q_len, int max_len, 
     }
     p.head_groups = (rows + p.heads_per_cta - 1) / p.heads_per_cta;
     p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype) / uaa::kTileKeys : 1;
-    p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 ? 1 : 2);
+    // tensor-core kernel: two CTAs per SM, one at head_dim 256 and with two column
+    // tiles (its eight consumer warps take the registers of two CTAs)
+    p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 || p.n_head_tiles == 2 ? 1 : 2);
     p.n_ctas = n_sm * p.per_sm;
     p.slice = batch < uaa::kMaxSliceBatch ? (batch > 0 ? batch : 1) : uaa::kMaxSliceBatch;
     p.n_slices = batch > 0 ? (batch + p.slice - 1) / p.slice : 0;

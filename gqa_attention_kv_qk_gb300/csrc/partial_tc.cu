@@ -66,10 +66,13 @@
 namespace uaa {
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarp = kConsumerWarps;  // warp 4
-constexpr int kPrepWarp = kConsumerWarps + 1;  // warp 5
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+// Consumer warps come in key groups of four: warp w takes the keys of group w % 4
+// of every stage. With one 8-column tile there are four consumer warps; with two
+// there are eight, warp w serving tile w / 4, so no warp holds both tiles'
+// state. The producer and the prep warp follow the consumers.
+constexpr int kKeyGroups = 4;
+__host__ __device__ constexpr int consumer_warps(int nht) { return nht == 2 ? 8 : 4; }
+__host__ __device__ constexpr int cta_threads(int nht) { return (consumer_warps(nht) + 2) * 32; }
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -129,7 +132,8 @@ struct Shape {
     static constexpr int kTabBytes = 8 * D;
     static constexpr int kFixedBytes =
         1024 + kCtlBytes + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes + kTabBytes;
-    static constexpr int kCtaBudget = D == 256 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
+    // one CTA per SM at head_dim 256 and with two column tiles (eight consumer warps)
+    static constexpr int kCtaBudget = D == 256 || NHT == 2 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
     static constexpr int kStagesRaw = (kCtaBudget - kFixedBytes) / (kStageBytes + 16);
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static_assert(kStages >= 2, "a ring of at least two stages");
@@ -548,7 +552,7 @@ __device__ __forceinline__ void patch_stage_row(const uint8_t* staging, uint8_t*
 }
 
 template <int D, int KV, int NHT>
-__global__ void __launch_bounds__(kThreads, (D == 256 ? 1 : 2))
+__global__ void __launch_bounds__(cta_threads(NHT), (D == 256 || NHT == 2 ? 1 : 2))
 partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_ks,
                   const PartialParams p)
@@ -560,12 +564,15 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     constexpr int TK = SH::kTK;     // keys per stage
     constexpr int KS = D / 16;      // k-steps of QK, m-tiles of PV
     constexpr int HC = 8 * NHT;     // head columns of a unit
+    constexpr int CW = consumer_warps(NHT);          // consumer warps
+    constexpr int NTW = NHT * kKeyGroups / CW;       // 8-column tiles per consumer warp
+    constexpr int kProducerWarp = CW, kPrepWarp = CW + 1;
     // merge scratch (inside one stage): all of D at once if it fits, else halves or quarters
-    constexpr int kScratchRow = 2 * kConsumerWarps * HC * 4;
-    constexpr int RC = kConsumerWarps * HC * (D + 4) * 4 + kScratchRow <= SH::kStageBytes       ? D
-                       : kConsumerWarps * HC * (D / 2 + 4) * 4 + kScratchRow <= SH::kStageBytes ? D / 2
-                                                                                               : D / 4;
-    static_assert(kConsumerWarps * HC * (RC + 4) * 4 + kScratchRow <= SH::kStageBytes,
+    constexpr int kScratchRow = 2 * kKeyGroups * HC * 4;
+    constexpr int RC = kKeyGroups * HC * (D + 4) * 4 + kScratchRow <= SH::kStageBytes       ? D
+                       : kKeyGroups * HC * (D / 2 + 4) * 4 + kScratchRow <= SH::kStageBytes ? D / 2
+                                                                                           : D / 4;
+    static_assert(kKeyGroups * HC * (RC + 4) * 4 + kScratchRow <= SH::kStageBytes,
                   "merge scratch must fit in one stage");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -592,10 +599,10 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (threadIdx.x == 0) {  // shared-memory set-up overlaps the previous kernel's tail
         for (int s = 0; s < SH::kStages; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, kConsumerWarps);
+            ptx::mbar_init(bar_empty + 8 * s, CW);
         }
         ptx::mbar_init(bar_qfull, 1);
-        ptx::mbar_init(bar_qempty, kConsumerWarps);
+        ptx::mbar_init(bar_qempty, CW);
         ptx::flag_set(go, 0u);
         ptx::flag_set(rows_ready, 0u);
         ptx::flag_set(rows_ready + 4, 0u);
@@ -778,7 +785,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
-    const int key_w = 16 * MG * warp;  // this warp's first key in a stage
+    const int kgrp = CW == kKeyGroups ? warp : warp % kKeyGroups;         // this warp's key group
+    const int nt0 = CW == kKeyGroups ? 0 : (warp / kKeyGroups) * NTW;    // and its first 8-column tile
+    const int key_w = 16 * MG * kgrp;             // its first key in a stage
     const float cap2 = p.softcap_log2e;
     // ldmatrix lane roles: matrix q = lane / 8, row r = lane % 8 of that matrix.
     const int lq = lane >> 3, lr = lane & 7;
@@ -797,12 +806,12 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // position, lens[b] - q_len + r / G, and with a window the last attn_window
         // of them; this thread's columns 2t, 2t + 1 of each 8-row tile
         const bool causal = p.q_len > 1;
-        int kmax[NHT][2], kmin[NHT][2];
+        int kmax[NTW][2], kmin[NTW][2];
 #pragma unroll
-        for (int nt = 0; nt < NHT; ++nt)
+        for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int tok = min(r0 + nt * 8 + 2 * t + j, p.q_len * p.G - 1) / p.G;
+                const int tok = min(r0 + (nt0 + nt) * 8 + 2 * t + j, p.q_len * p.G - 1) / p.G;
                 kmax[nt][j] = lens[sg.b] - p.q_len + tok;
                 kmin[nt][j] = p.attn_window > 0 ? kmax[nt][j] - p.attn_window + 1 : INT_MIN;
             }
@@ -815,7 +824,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             fits && sg.st0 + sg.n_st == sg.stages ? L - (t0 + MG * (sg.stages - 1)) * kTileKeys : -1;
         const int new_w = new_r >= 0 ? new_r / (16 * MG) : -1;
 
-        // this segment's q' fragments from the prep warp: head nt * 8 + g, as (hi, lo)
+        // this segment's q' fragments from the prep warp: row (nt0 + nt) * 8 + g, as (hi, lo)
         // pairs; k-step kk takes dims 16 kk + 2t (+1) and 16 kk + 2t + 8 (+9) against
         // bf16 keys, and dims 16 kk + 4t .. 16 kk + 4t + 3 against int8 keys (the
         // order in which ldmatrix hands out a code row; the contraction does not care)
@@ -823,10 +832,10 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             failed = true;
             if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
         }
-        uint32_t qhi[NHT][KS][2], qlo[NHT][KS][2];
+        uint32_t qhi[NTW][KS][2], qlo[NTW][KS][2];
 #pragma unroll
-        for (int nt = 0; nt < NHT; ++nt) {
-            const uint8_t* row = frag + (nt * 8 + g) * SH::kFragRow;
+        for (int nt = 0; nt < NTW; ++nt) {
+            const uint8_t* row = frag + ((nt0 + nt) * 8 + g) * SH::kFragRow;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 if (KQ8) {
@@ -848,9 +857,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_qempty);  // the slot may be refilled
 
-        float m[NHT][2], l[NHT][2], o[NHT][KS][4];
+        float m[NTW][2], l[NTW][2], o[NTW][KS][4];
 #pragma unroll
-        for (int nt = 0; nt < NHT; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
             m[nt][0] = m[nt][1] = -INFINITY;
             l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
@@ -865,7 +874,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             }
             const int kbase = (t0 + MG * (sg.st0 + k)) * kTileKeys + key_w;  // this warp's first key
-            if (!failed && warp == new_w && k + 1 == sg.n_st) {  // the new key's row, over what the load brought
+            if (!failed && kgrp == new_w && k + 1 == sg.n_st) {  // the new key's row, over what the load brought
                 bool ready = true;
                 if (lane == 0) {
                     ready = ptx::flag_wait_eq(rows_ready + 4 * (seg & 1), static_cast<unsigned>(seg) + 1u,
@@ -884,11 +893,11 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint32_t st = base + s * SH::kStageBytes;
 
                 // S^T = K . Q'^T (keys x heads), one accumulator per 16-key group
-                float sacc[MG][NHT][4];
+                float sacc[MG][NTW][4];
 #pragma unroll
                 for (int mg = 0; mg < MG; ++mg)
 #pragma unroll
-                    for (int nt = 0; nt < NHT; ++nt)
+                    for (int nt = 0; nt < NTW; ++nt)
                         sacc[mg][nt][0] = sacc[mg][nt][1] = sacc[mg][nt][2] = sacc[mg][nt][3] = 0.f;
                 if (KQ8) {
                     // int8 keys: one ldmatrix.x4 covers 16 keys x 32 dims (k-steps 2 kc and
@@ -905,7 +914,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             widen_code_quad(r[2], a1[0], a1[2]);
                             widen_code_quad(r[3], a1[1], a1[3]);
 #pragma unroll
-                            for (int nt = 0; nt < NHT; ++nt) {
+                            for (int nt = 0; nt < NTW; ++nt) {
                                 ptx::mma_f16(sacc[mg][nt], a0, qhi[nt][2 * kc][0], qhi[nt][2 * kc][1]);
                                 ptx::mma_f16(sacc[mg][nt], a0, qlo[nt][2 * kc][0], qlo[nt][2 * kc][1]);
                                 ptx::mma_f16(sacc[mg][nt], a1, qhi[nt][2 * kc + 1][0], qhi[nt][2 * kc + 1][1]);
@@ -919,7 +928,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     for (int mg = 0; mg < MG; ++mg) {
                         const float k0 = ksc[key_w + 16 * mg + g], k8 = ksc[key_w + 16 * mg + g + 8];
 #pragma unroll
-                        for (int nt = 0; nt < NHT; ++nt) {
+                        for (int nt = 0; nt < NTW; ++nt) {
                             sacc[mg][nt][0] *= k0;
                             sacc[mg][nt][1] *= k0;
                             sacc[mg][nt][2] *= k8;
@@ -934,7 +943,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             uint32_t a[4];
                             ptx::ldsm_x4(a, st + tile_off<TK>(key_w + 16 * mg + lr + 8 * (lq & 1), 2 * kk + (lq >> 1)));
 #pragma unroll
-                            for (int nt = 0; nt < NHT; ++nt) {
+                            for (int nt = 0; nt < NTW; ++nt) {
                                 ptx::mma_bf16(sacc[mg][nt], a, qhi[nt][kk][0], qhi[nt][kk][1]);
                                 ptx::mma_bf16(sacc[mg][nt], a, qlo[nt][kk][0], qlo[nt][kk][1]);
                             }
@@ -972,10 +981,10 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     r_scale = r_new;
                 }
 
-                float x[MG][NHT][4], f[NHT][2];
+                float x[MG][NTW][4], f[NTW][2];
                 bool rescale = false;
 #pragma unroll
-                for (int nt = 0; nt < NHT; ++nt) {
+                for (int nt = 0; nt < NTW; ++nt) {
                     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                     for (int mg = 0; mg < MG; ++mg) {
@@ -1022,7 +1031,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                    for (int nt = 0; nt < NHT; ++nt)
+                    for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
                         for (int mi = 0; mi < KS; ++mi) {
                             o[nt][mi][0] *= f[nt][0];
@@ -1034,9 +1043,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
 #pragma unroll
                 for (int mg = 0; mg < MG; ++mg) {
-                    uint32_t bph[NHT][2], bpl[NHT][2];
+                    uint32_t bph[NTW][2], bpl[NTW][2];
 #pragma unroll
-                    for (int nt = 0; nt < NHT; ++nt) {
+                    for (int nt = 0; nt < NTW; ++nt) {
                         uint32_t h01, l01, h23, l23;
                         if (VQ8) {
                             split_f16(x[mg][nt][0] * w_g[mg], x[mg][nt][1] * w_g[mg], h01, l01);     // key g
@@ -1066,7 +1075,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             widen_code_pairs(r[1], c[0], c[1]);  // values 32j + 16 + 2g, +1
                             widen_code_pairs(r[3], c[2], c[3]);
 #pragma unroll
-                            for (int nt = 0; nt < NHT; ++nt) {
+                            for (int nt = 0; nt < NTW; ++nt) {
                                 ptx::mma_f16(o[nt][2 * j], a, bph[nt][0], bph[nt][1]);
                                 ptx::mma_f16(o[nt][2 * j], a, bpl[nt][0], bpl[nt][1]);
                                 ptx::mma_f16(o[nt][2 * j + 1], c, bph[nt][0], bph[nt][1]);
@@ -1093,7 +1102,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             a[2] &= m89;
                             a[3] &= m89;
 #pragma unroll
-                            for (int nt = 0; nt < NHT; ++nt) {
+                            for (int nt = 0; nt < NTW; ++nt) {
                                 ptx::mma_bf16(o[nt][mi], a, bph[nt][0], bph[nt][1]);
                                 ptx::mma_bf16(o[nt][mi], a, bpl[nt][0], bpl[nt][1]);
                             }
@@ -1109,7 +1118,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
         // ------------------------------------------------------------ merge
 #pragma unroll
-        for (int nt = 0; nt < NHT; ++nt)
+        for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -1117,45 +1126,45 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
         const int s_last = (it - 1) % SH::kStages;
         float* red_m = reinterpret_cast<float*>(base_ptr + s_last * SH::kStageBytes);
-        float* red_l = red_m + kConsumerWarps * HC;
-        float* red_o = red_l + kConsumerWarps * HC;
+        float* red_l = red_m + kKeyGroups * HC;
+        float* red_o = red_l + kKeyGroups * HC;
         const float o_unit = VQ8 ? r_scale : 1.f;
         const size_t rec = 2 * static_cast<size_t>(slot) + (pos == s_c ? 0 : 1);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += RC) {
-            ptx::named_barrier_sync(1, kConsumerWarps * 32);  // stage (or previous round) no longer read
+            ptx::named_barrier_sync(1, CW * 32);  // stage (or previous round) no longer read
             if (g == 0 && c0 == 0) {
 #pragma unroll
-                for (int nt = 0; nt < NHT; ++nt)
+                for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        red_m[warp * HC + nt * 8 + 2 * t + j] = m[nt][j];
-                        red_l[warp * HC + nt * 8 + 2 * t + j] = l[nt][j];
+                        red_m[kgrp * HC + (nt0 + nt) * 8 + 2 * t + j] = m[nt][j];
+                        red_l[kgrp * HC + (nt0 + nt) * 8 + 2 * t + j] = l[nt][j];
                     }
             }
 #pragma unroll
-            for (int nt = 0; nt < NHT; ++nt)
+            for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
                 for (int mi = 0; mi < KS; ++mi)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int hc = nt * 8 + 2 * t + (e & 1);
+                        const int hc = (nt0 + nt) * 8 + 2 * t + (e & 1);
                         const int d = VQ8 ? 16 * mi + 2 * g + (e >> 1) : 16 * mi + g + 8 * (e >> 1);
-                        if (d >= c0 && d < c0 + RC) red_o[(warp * HC + hc) * (RC + 4) + d - c0] = o[nt][mi][e] * o_unit;
+                        if (d >= c0 && d < c0 + RC) red_o[(kgrp * HC + hc) * (RC + 4) + d - c0] = o[nt][mi][e] * o_unit;
                     }
-            ptx::named_barrier_sync(1, kConsumerWarps * 32);
-            for (int idx = threadIdx.x; idx < nh * RC; idx += kConsumerWarps * 32) {
+            ptx::named_barrier_sync(1, CW * 32);
+            for (int idx = threadIdx.x; idx < nh * RC; idx += CW * 32) {
                 const int hc = idx / RC, dc = idx - hc * RC;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * HC + hc]);
+                for (int w = 0; w < kKeyGroups; ++w) M = fmaxf(M, red_m[w * HC + hc]);
                 const int hq = sg.kvh * p.G + (r0 + hc) % p.G;  // the row's query head
                 const float zs = (sg.whole && p.sink) ? p.sink[hq] * kLog2e : -INFINITY;
                 if (sg.whole) M = fmaxf(M, zs);  // the sink joins the denominator of a whole unit
                 float L = 0.f, acc = 0.f;
                 if (M != -INFINITY) {
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
+                    for (int w = 0; w < kKeyGroups; ++w) {
                         const float mw = red_m[w * HC + hc];
                         const float fw = mw == -INFINITY ? 0.f : exp2f(mw - M);
                         L += red_l[w * HC + hc] * fw;
@@ -1178,7 +1187,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         // the stage held for the scratch goes back to the producer (after the generic
         // accesses are ordered before the TMA writes that will refill it)
-        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+        ptx::named_barrier_sync(1, CW * 32);
         ptx::fence_proxy_async();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s_last);
@@ -1205,7 +1214,7 @@ cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUte
         if (e != cudaSuccess) return e;
         if (dev < 31) configured_device_mask |= 1 << dev;
     }
-    return launch_dependent(kern, dim3(n_ctas), dim3(kThreads), SH::kSmemBytes, s, tk, tv, ts, tks, p);
+    return launch_dependent(kern, dim3(n_ctas), dim3(cta_threads(NHT)), SH::kSmemBytes, s, tk, tv, ts, tks, p);
 }
 
 template <int KV>
