@@ -158,7 +158,8 @@ uaa::BalanceState balance_of(void* ws, const Plan& pl)
 }
 
 // Geometry of a step. The partial kernels are persistent: P = SMs x resident CTAs
-// (4 for the CUDA-core kernel, 2 for the tensor-core kernel, 1 at head_dim 256),
+// (4 for the CUDA-core kernel, 2 for the tensor-core kernel, 1 at head_dim 256 or
+// with two column tiles),
 // each attending one contiguous range of all units' key stages (the stream-K
 // partition in internal.cuh), so the split needs no length bound. Batches above
 // kMaxSliceBatch sequences are cut into slices (one partial + combine launch each)
