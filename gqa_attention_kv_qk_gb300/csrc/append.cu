@@ -1,12 +1,12 @@
 // append.cu -- step 1 of the decode step: per-head QK RMSNorm, rotary embedding at
 // the absolute KV index, and the append of the new k / v rows to the cache.
 //
-// One CTA of 16 warps per sequence. The CTA first builds the cos / sin table of
-// the sequence's position (rope_cos_sin) while each warp loads its first head
-// row; then each warp takes whole rows, loading the next while it processes the
-// current one: q rows go to the workspace pre-multiplied by the partial
-// kernel's logit prescale, k rows and v rows go to slot seq_lens[b] of the
-// cache. vq8 values (and q8 keys, after the rotation) are quantised in fp32
+// One CTA of 16 warps per token of each sequence. The CTA first builds the cos /
+// sin table of the token's position (rope_cos_sin) while each warp loads its
+// first head row; then each warp takes whole rows, loading the next while it
+// processes the current one: q rows go to the workspace pre-multiplied by the
+// partial kernel's logit prescale, k rows and v rows go to slot seq_lens[b] + t
+// of the cache for token t. vq8 values (and q8 keys, after the rotation) are quantised in fp32
 // with IEEE division and round-half-even, the storage rule of the vq8 cache
 // (llamay "Models and formats", "The KV cache, in three precisions").
 #include "internal.cuh"
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     __shared__ float rowbuf[kAppendWarps][D];
 
     grid_dependency_wait();  // the step's inputs and the previous step's reads are complete
-    const int b = blockIdx.x;
+    const int b = blockIdx.x / p.q_len, tok = blockIdx.x - b * p.q_len;  // one CTA per token
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // each warp takes rows warp, warp + W, ...; the next row is loaded while the
@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     float x[EPL], nxt[EPL];
     if (warp < n_rows) {
         size_t at;
-        const void* src = row_source(p, b, 0, warp, at);
+        const void* src = row_source(p, b, tok, warp, at);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
     }
@@ -78,22 +78,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     // not all fit the cache is not appended (and not advanced)
     const int L = p.seq_lens[b];
     const bool fits = L >= 0 && L + p.q_len <= p.cap;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && tok == 0) {
         if (!fits) atomicOr(p.status, UAA_DEVFLAG_CAPACITY);
         else if (L > p.max_len) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
     }
 
-    for (int tok = 0; tok < p.q_len; ++tok) {  // one token of the sequence at a time
+    {
         const int pos = fits ? L + tok : 0;
-        if (tok > 0) {
-            __syncthreads();  // the previous token's rows no longer read the table
-            if (warp < n_rows) {
-                size_t at;
-                const void* src = row_source(p, b, tok, warp, at);
-#pragma unroll
-                for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
-            }
-        }
 #pragma unroll
         for (int i0 = 0; i0 < HALF; i0 += 32)  // warp w takes pairs 32 w .. 32 w + 31
             if (warp == i0 / 32)
@@ -176,9 +167,27 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                 __syncwarp();  // the row is read before the next one overwrites it
             }
         }
-    }  // tokens
+    }
     __syncthreads();
-    if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + p.q_len;
+    if (p.q_len == 1) {  // the sequence's only CTA
+        if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + 1;
+        return;
+    }
+    // several tokens: every CTA of the grid counts in once it has read its length;
+    // the last one advances them all (the counter, the workspace word after the
+    // status word, wraps to zero for the next launch)
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicInc(p.status + 1, gridDim.x - 1) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+        const int n = p.seq_lens[i];
+        if (n >= 0 && n + p.q_len <= p.cap) p.seq_lens[i] = n + p.q_len;
+    }
 }
 
 template <int D>
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
-    const dim3 grid(p.B), block(kAppendWarps * 32);
+    const dim3 grid(p.B * p.q_len), block(kAppendWarps * 32);  // one CTA per token
     const bool f32 = p.io_dtype == UAA_DTYPE_F32;
     switch (p.D) {
     case 64:
