@@ -198,6 +198,38 @@ def test_large_batches_are_sliced(L):
     assert (lay.slice_batch, lay.n_slices) == (1024, 3)
 
 
+@pytest.mark.parametrize("name,kv", [("llama31_8b_decode", "bf16"), ("gptoss_vq8_sink", "vq8"),
+                                     ("llama31_8b_decode", "q8"), ("gemma2_9b_swa", "bf16"),
+                                     ("llama32_1b_tiny", "f32")])
+def test_chunk_geometry(L, name, kv):
+    """Steps of q_len tokens: a unit's rows are the q_len G (token, head) pairs of
+    a kv head, 8 or 16 to a unit (8 at head_dim 256 and on the CUDA-core kernel);
+    two 8-row tiles run one CTA per SM; the q' region holds q_len rows per
+    sequence; a workspace sized for q_len serves every smaller q_len."""
+    cfg = W.layer_configs(W.config(name, kv_dtype=kv, io_dtype="f32" if kv == "f32" else "bf16"))[0]
+    d = B.make_desc(cfg)
+    G = cfg["n_q_heads"] // cfg["n_kv_heads"]
+    sizes = []
+    for T in (1, 2, 4, 16, 64):
+        lay = B.uaa_get_workspace_layout(d, 8, 1000, 152, q_len=T)
+        rows = T * G
+        wide = lay.kernel == 1 and cfg["head_dim"] != 256 and rows > 8
+        assert lay.heads_per_cta == (16 if wide else 8)
+        assert lay.n_ctas == 152 * (4 if lay.kernel == 0 else (1 if cfg["head_dim"] == 256 or wide else 2))
+        assert lay.prefix_offset - lay.q_rot_offset >= 8 * T * cfg["n_q_heads"] * cfg["head_dim"] * 4
+        sizes.append(B.uaa_workspace_size(d, 8, 1000, 152, q_len=T))
+        assert sizes[-1] == lay.total_bytes
+    assert B.uaa_workspace_size(d, 8, 1000, 152, q_len=2000) == 0  # beyond the largest chunk
+    # a larger chunk never needs less workspace, so one sized for q_len serves the smaller ones
+    assert sizes == sorted(sizes)
+
+
+def test_chunk_capacity_refusal(L):
+    a = fake_args(cache_capacity=128, max_seq_len=120, q_len=16)
+    assert B.uaa_decode_attn(good_desc(), a, WS, None, check=False) == B.UAA_ERR_CAPACITY
+    assert "16 new token(s) does not fit cache_capacity=128" in B.last_error()
+
+
 def test_geometry_query_refuses_bad_desc(L):
     assert B.uaa_workspace_size(good_desc(head_dim=48), 4, 100, 152) == 0
     assert B.uaa_num_splits(good_desc(n_q_heads=9), 4, 100, 152) == 0
