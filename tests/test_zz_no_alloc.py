@@ -34,6 +34,8 @@ def _built():
 @pytest.mark.parametrize("name,over,lens", [
     ("llama31_8b_decode", dict(batch=3, seq_len=700), [699, 300, 5]),
     ("gptoss_vq8_sink", dict(batch=2, seq_len=500), [499, 77]),
+    ("llama31_8b_q8", dict(batch=2, seq_len=300), [299, 30]),
+    ("llama31_8b_verify", dict(batch=2, seq_len=400, page_size=64), [390, 77]),
 ])
 def test_static_scratch_matches_workspace_entry(name, over, lens):
     cfg = W.config(name, **over)
@@ -43,13 +45,15 @@ def test_static_scratch_matches_workspace_entry(name, over, lens):
     stream = torch.cuda.current_stream()
     for step in range(2):  # two calls in a row: the shared scratch keeps the previous contents
         inp = {k: v.cuda() for k, v in W.step_inputs(cfg, step).items()}
+        T = with_ws._begin(inp["q"])
+        no_alloc._begin(inp["q"])
         B.uaa_decode_attn(with_ws.desc, with_ws.args(inp["q"], inp["k_new"], inp["v_new"]), with_ws.ws, stream)
         B.uaa_decode_attn_static(no_alloc.desc, no_alloc.args(inp["q"], inp["k_new"], inp["v_new"]), stream)
-        with_ws.max_len_hint += 1
-        no_alloc.max_len_hint += 1
+        with_ws.max_len_hint += T
+        no_alloc.max_len_hint += T
         torch.cuda.synchronize()
-        want = with_ws.out.double().cpu().numpy()
-        got = no_alloc.out.double().cpu().numpy()
+        want = with_ws.out_for(T).double().cpu().numpy()
+        got = no_alloc.out_for(T).double().cpu().numpy()
         d = np.abs(got - want)
         assert np.all(np.isfinite(got))
         assert d.max() <= TOL_MAX and d.mean() <= TOL_MEAN, (step, d.max(), d.mean())
