@@ -2,14 +2,17 @@
  * uaa.h -- C ABI of the GB300 (sm_103a) grouped-query-attention decode step.
  *
  * One decode step of one attention layer, for a batch of sequences that each
- * hold a KV cache:
+ * hold a KV cache, with one new token per sequence or a causal chunk of q_len
+ * tokens (uaa_step_args.q_len):
  *
  *   1. uaa_rope_qk_norm_append: optional per-head RMSNorm of the new q and k
- *      rows, rotary position embedding at the sequence's absolute KV index, and
- *      the append of k and v at slot seq_lens[b] (seq_lens[b] then grows by 1).
+ *      rows, rotary position embedding at each token's absolute KV index, and
+ *      the append of k and v at slots seq_lens[b] .. seq_lens[b] + q_len - 1
+ *      (seq_lens[b] then grows by q_len).
  *   2. uaa_decode_attn_partial: split-K flash decoding. A persistent grid of P
- *      CTAs splits the key stages of all units (sequence, kv head, head group)
- *      into P contiguous ranges (a stream-K partition). The tensor-core kernel
+ *      CTAs splits the key stages of all units (sequence, kv head, group of
+ *      (token, head) query rows) into P contiguous ranges (a stream-K
+ *      partition). The tensor-core kernel
  *      sizes the ranges by the speed each CTA slot measured in the previous
  *      launches on the same workspace (the SMs of a GB300 do not all stream
  *      equally fast), so results may differ in rounding from launch to launch.
@@ -19,18 +22,19 @@
  *   3. uaa_decode_attn_combine: log-sum-exp merge of those records, the sink
  *      logit added to the denominator, the remaining output rows written.
  *   uaa_decode_attn_append_partial runs 1 and 2 (for bf16, vq8 and q8 caches and
- *   one token per sequence in one
- *   kernel that forms q', k and v of the new token itself and attends the new
- *   key from shared memory); uaa_decode_attn runs 1-3 on one stream.
+ *   one token per sequence in one kernel that forms q', k and v of the new
+ *   token itself and attends the new key from shared memory); uaa_decode_attn
+ *   runs 1-3 on one stream.
 
  * Where the method is defined (page title, then section):
  *   - integral GQA ratio, head_dim set, 1/sqrt(head_dim) scale, the split-K
  *     decode and KV-producer paths (prior art):
  *       Model support matrix, "Structural fact requirements", "Kernel path
  *       capabilities"; the typed-refusal convention: "Conformance CLI";
- *   - RoPE scaling (llama3, YaRN), QK-norm before RoPE, RMSNorm, positions at
- *     the absolute KV index, sliding window, attention-logit softcap:
- *       huggingface_decoder_completeness.md, P0.2, P1.1, P1.2, P1.3, P1.4;
+ *   - RoPE scaling (llama3, YaRN), QK-norm before RoPE, RMSNorm (and Gemma's
+ *     (1 + w) weight), positions at the absolute KV index, sliding window,
+ *     attention-logit softcap, partial rotary:
+ *       huggingface_decoder_completeness.md, P0.2, P1.1, P1.2, P1.3, P1.4, P1.5;
  *   - NeoX vs interleaved pairing and the llama3 parameters:
  *       FreeToken PR #722 "serve Llama and Mistral llama-arch GGUF", "Changes";
  *       llamay "Models and formats", "Architectures";
@@ -45,7 +49,9 @@
  *     aligned, row-major and dense. The library never allocates device memory,
  *     never synchronises (except uaa_device_status) and launches only on the
  *     given stream.
- *   - Layouts: q [B][Hq][D]; k_new, v_new [B][Hkv][D] (io_dtype);
+ *   - Layouts (with q_len = T > 1 every q, k_new, v_new, out and q_rot row set
+ *     has a token axis after B, [B][T][H][D]; paged caches: see block_table):
+ *     q [B][Hq][D]; k_new, v_new [B][Hkv][D] (io_dtype);
  *     k_cache [B][Hkv][cap][D] (fp32, bf16 for BF16 and VQ8 caches, int8
  *     codes for Q8); v_cache [B][Hkv][cap][D] (fp32, bf16, or int8 codes for
  *     VQ8 and Q8); v_scale [B][Hkv][cap] fp32 (VQ8 and Q8); k_scale
