@@ -111,7 +111,7 @@ struct Plan {
     int G;
     int q_len;           // tokens per sequence (1: decode)
     int kernel;          // 0 CUDA-core, 1 tensor-core
-    int heads_per_cta;   // query heads of one unit
+    int heads_per_cta;   // query rows of one unit ((token, head) pairs; heads for a decode step)
     int head_groups;     // units per kv head
     int n_head_tiles;    // 8-head column tiles of the tensor-core kernel
     int mg;              // 64-key tiles per ring stage

@@ -1,7 +1,8 @@
 // combine.cu -- step 3 of the decode step: log-sum-exp merge of the records of
 // units that the stream-K partition cut between CTAs, with the per-head sink.
 //
-// One CTA per unit (sequence, kv head, head group). A unit that lies inside one
+// One CTA per unit (sequence, kv head, group of (token, head) query rows: the
+// query heads of the kv head for a decode step). A unit that lies inside one
 // CTA's range was written by the partial kernel already and is skipped. For a
 // cut unit with records (o_c normalised, e_c the log2-sum-exp of the final
 // logits) from its owner CTAs, and the sink logit z_h of each head (llamay
