@@ -186,7 +186,7 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int q_len, int max_len, 
         p.n_head_tiles = 2;
     }
     p.head_groups = (rows + p.heads_per_cta - 1) / p.heads_per_cta;
-    p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype) / uaa::kTileKeys : 1;
+    p.mg = p.kernel == 1 ? uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype, p.n_head_tiles) / uaa::kTileKeys : 1;
     // tensor-core kernel: two CTAs per SM, one at head_dim 256 and with two column
     // tiles (its eight consumer warps take the registers of two CTAs)
     p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 || p.n_head_tiles == 2 ? 1 : 2);
@@ -464,7 +464,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
                                     : (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
         const uint32_t tk_rows =
             paged ? (uint32_t)(a->page_size < uaa::kTileKeys ? a->page_size : uaa::kTileKeys)
-                  : (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype);  // box height
+                  : (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype, pl.n_head_tiles);  // box height
         const uint64_t heads = paged ? (uint64_t)a->n_pages * d->n_kv_heads : (uint64_t)a->batch * d->n_kv_heads;
         const uint64_t scale_inner = paged ? (uint64_t)a->page_size : (uint64_t)a->cache_capacity;
         // int8 codes: boxes of tk_rows x min(D, 128) bytes, swizzled like the bf16 boxes so

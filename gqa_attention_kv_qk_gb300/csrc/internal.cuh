@@ -191,8 +191,9 @@ cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int 
 
 // Dynamic shared memory the tensor-core partial kernel needs.
 size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles);
-// Keys per ring stage of the tensor-core partial kernel (the TMA box height).
-int partial_tc_keys_per_stage(int D, int kv_dtype);
+// Keys per ring stage of the tensor-core partial kernel (the TMA box height) for
+// n_head_tiles 8-row column tiles per unit.
+int partial_tc_keys_per_stage(int D, int kv_dtype, int nht);
 // Largest batch slice one partial launch takes (its stage prefix lives in shared memory).
 constexpr int kMaxSliceBatch = 1024;
 

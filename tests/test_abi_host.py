@@ -215,6 +215,11 @@ def test_chunk_geometry(L, name, kv):
         rows = T * G
         wide = lay.kernel == 1 and cfg["head_dim"] != 256 and rows > 8
         assert lay.heads_per_cta == (16 if wide else 8)
+        if lay.kernel == 1:  # keys per ring stage: two 16-key groups per warp where keys are cheap or rows many
+            D = cfg["head_dim"]
+            want = (256 if kv in ("vq8", "q8") else 128) if D == 64 else (128 if kv == "q8" or (wide and D == 128)
+                                                                         else 64)
+            assert lay.stage_keys == want, (T, lay.stage_keys, want)
         assert lay.n_ctas == 152 * (4 if lay.kernel == 0 else (1 if cfg["head_dim"] == 256 or wide else 2))
         assert lay.prefix_offset - lay.q_rot_offset >= 8 * T * cfg["n_q_heads"] * cfg["head_dim"] * 4
         sizes.append(B.uaa_workspace_size(d, 8, 1000, 152, q_len=T))
