@@ -451,6 +451,7 @@ def run_uaa(args, world, rank, local) -> dict | None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"f32": "f32", "q8": "f16"}.get(cfg["kv_dtype"], "bf16"),
         "data": "synthetic (seeded N(0,1) cache and inputs)",
         "decode_steps_per_s": round(decodes / dev_s / world, 2),
+        "tokens_per_s_per_seq": round(decodes * T / dev_s / world, 2),  # q_len new tokens per sequence and step
         "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "config": {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"], "n_q_heads": cfg["n_q_heads"],
                    "n_kv_heads": cfg["n_kv_heads"], "head_dim": cfg["head_dim"], "kv_dtype": cfg["kv_dtype"],
