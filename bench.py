@@ -90,9 +90,13 @@ def visible(n: int, window: int) -> int:
 
 
 def partial_bytes(cfg: dict, lens_after: list[int]) -> int:
-    """Visible K and V rows the split-K partial must read (one read per kv head)."""
+    """Visible K and V rows the split-K partial must read (one read per kv head):
+    with T = q_len tokens per sequence and a window W, the union of the rows'
+    windows, W + T - 1 keys."""
     kb, vb = _kv_row_bytes(cfg)
+    T = int(cfg.get("q_len", 1) or 1)
     w = cfg.get("window", 0) or 0
+    w = w + T - 1 if w else 0
     return sum(visible(n, w) for n in lens_after) * cfg["n_kv_heads"] * (kb + vb)
 
 

@@ -67,3 +67,20 @@ def test_byte_accounting_counts_visible_keys_once_per_kv_head():
     assert bench.partial_bytes(cfg_q, [5]) == 5 * 2 * (128 + 64 + 4)
     small = 2 * (8 + 4) * 64 * 2 + 2 * 2 * 256 + 2 * 8 * 64 * 4
     assert bench.decode_step_bytes(cfg, [9, 19]) == bench.partial_bytes(cfg, [10, 20]) + small
+
+
+def test_byte_accounting_for_q8_and_chunks():
+    """q8 rows are D codes plus a 4-byte scale for keys and values alike; a step of
+    T tokens reads each visible key once (lengths grow by T) and moves T times
+    the small rows (q, k, v in; appended rows; outputs)."""
+    import bench
+    cfg = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, kv_dtype="q8", io_dtype="bf16",
+               out_dtype="f32", window=0)
+    assert bench.partial_bytes(cfg, [10, 20]) == (10 + 20) * 2 * (2 * (128 + 4))
+    chunk = dict(cfg, kv_dtype="bf16", q_len=4)
+    small = 4 * (2 * (8 + 4) * 128 * 2 + 2 * 2 * (256 + 256) + 2 * 8 * 128 * 4)
+    assert bench.decode_step_bytes(chunk, [9, 19]) == bench.partial_bytes(chunk, [13, 23]) + small
+    # with a window each token sees its own last W keys: the step reads the union of
+    # the rows' windows, W + T - 1 keys, once
+    win = dict(chunk, window=5)
+    assert bench.partial_bytes(win, [13, 23]) == (8 + 8) * 2 * 512
