@@ -531,7 +531,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         p.rec_lse = reinterpret_cast<float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
         p.rec_o = reinterpret_cast<float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
         p.sink = d->has_sink ? a->sink : nullptr;
-        p.out = static_cast<char*>(a->out) + (size_t)b0 * Hq * D * out_elem;
+        p.out = static_cast<char*>(a->out) + (size_t)b0 * pl.q_len * Hq * D * out_elem;
         p.out_dtype = d->out_dtype;
         p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
         if (fused) {
@@ -540,7 +540,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
             p.fused = 1;
             p.max_len = a->max_seq_len;
             p.arrivals = reinterpret_cast<unsigned*>(w + pl.off_status) + 1;
-            p.q = static_cast<const char*>(a->q) + (size_t)b0 * Hq * D * io_elem;
+            p.q = static_cast<const char*>(a->q) + (size_t)b0 * Hq * D * io_elem;  // one token per sequence
             p.k_new = static_cast<const char*>(a->k_new) + (size_t)b0 * Hkv * D * io_elem;
             p.v_new = static_cast<const char*>(a->v_new) + (size_t)b0 * Hkv * D * io_elem;
             p.io_dtype = d->io_dtype;
@@ -608,6 +608,9 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
 uaa_status run_append_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws,
                               const Plan& pl, cudaStream_t s)
 {
+    // one token per sequence; a chunk's append runs first, one CTA per token (a fused
+    // kernel that staged a chunk's rows itself measured slower: its prep warp's
+    // start-of-segment work is not hidden at one CTA per SM)
     if (pl.kernel == 1 && pl.q_len == 1) return run_partial(d, a, ws, pl, s, true);
     UAA_TRY(run_append(d, a, ws, pl, s));
     return run_partial(d, a, ws, pl, s);

@@ -249,6 +249,15 @@ EDGE = [
     ("chunk16-q8-paged64", "llama31_8b_q8", dict(batch=2, seq_len=700, q_len=16, page_size=64), [680, 100]),
     ("chunk64-prefill-g2", "llama31_8b_decode", dict(batch=2, n_q_heads=16, n_kv_heads=8, seq_len=300, q_len=64),
      [200, 0]),
+    # short chunks with two column tiles: new rows that cross a stage or page boundary,
+    # two head groups, windows shorter than the chunk; head_dim 256 with one column tile
+    ("chunk4-g4-stage-crossing", "llama31_8b_decode", dict(batch=4, seq_len=600, q_len=4), [126, 254, 1, 509]),
+    ("chunk3-g8-vq8-two-groups", "llama31_8b_decode", dict(batch=2, n_q_heads=32, n_kv_heads=4, kv_dtype="vq8",
+                                                           seq_len=400, q_len=3), [127, 30]),
+    ("chunk4-q8-window3", "llama31_8b_q8", dict(batch=2, seq_len=500, q_len=4, window=3), [254, 2]),
+    ("chunk2-g8-d64-paged32-vq8", "gptoss_vq8_sink", dict(batch=2, seq_len=500, q_len=2, page_size=32), [31, 400]),
+    ("chunk4-d256-g4-window", "gemma2_9b_swa", dict(batch=2, n_q_heads=16, n_kv_heads=4, seq_len=600, q_len=4,
+                                                    layers=[dict(window=50)]), [126, 590]),
     ("d64-vq8-norm-offset-local", "gemma3_12b_local_global",
      dict(batch=2, seq_len=600, head_dim=64, kv_dtype="vq8", layers=[dict(window=100, rope_theta=10000.0,
                                                                           rope_scaling="none")]), [599, 40]),
@@ -314,6 +323,18 @@ def test_batch_slices(oracle_mod, entry):
     lay_batch = B.uaa_get_workspace_layout(B.make_desc(cfg), 1100, 130, 152)
     assert lay_batch.n_slices == 2
     rng = np.random.default_rng(5)
+    run_and_compare(oracle_mod, cfg, [int(x) for x in rng.integers(0, 130, size=1100)], cap=256, entry=entry,
+                    check_qrot=True)
+
+
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_batch_slices_chunk(oracle_mod, entry):
+    """Slices with four tokens per sequence: a slice's queries, new rows, q' rows
+    and outputs start q_len rows per sequence further on."""
+    cfg = W.config("qwen3_8b_ragged", batch=1100, n_q_heads=8, n_kv_heads=2, seq_len=(1, 130), q_len=4)
+    lay_batch = B.uaa_get_workspace_layout(B.make_desc(cfg), 1100, 130, 152, 4)
+    assert lay_batch.n_slices == 2
+    rng = np.random.default_rng(6)
     run_and_compare(oracle_mod, cfg, [int(x) for x in rng.integers(0, 130, size=1100)], cap=256, entry=entry,
                     check_qrot=True)
 
