@@ -17,17 +17,21 @@
 // ranges cA .. cB, which the partial kernel leaves per unit (UnitOwners in
 // internal.cuh). The record weights are formed per
 // head from one parallel round of loads; every thread then loads all records'
-// rows for four output elements before it adds any of them.
+// rows for four output elements before it adds any of them. The CTA has a
+// thread per four output elements of a unit (128 to 512 threads), so a unit of
+// up to 16 rows of 128 dims is merged in one round of loads: the merge is a
+// chain of dependent loads, not a stream of bytes.
 #include "internal.cuh"
 
 namespace uaa {
 namespace {
 
-constexpr int kCombineThreads = 128;
+constexpr int kCombineMinThreads = 128;
+constexpr int kCombineMaxThreads = 512;
 constexpr int kMaxHeads = 16;    // heads of one unit
 constexpr int kRecBatch = 4;     // records loaded together per output element
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
+__global__ void __launch_bounds__(kCombineMaxThreads) combine_kernel(const CombineParams p)
 {
     extern __shared__ float wts[];  // [R][nh]: record log2-sum-exp, then weights
     grid_dependency_wait();         // the partial kernel's records are complete
@@ -44,7 +48,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int r0 = hg * HC;                      // the unit's first query row (query_row)
     const int nh = min(HC, p.q_len * p.G - r0);  // its query rows
     const int D = p.D;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, nthr = blockDim.x;
     // output element idx (row idx / D, column idx % D) of the unit
     auto out_at = [&](int idx) {
         const int hc = idx / D;
@@ -59,7 +63,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         own[1] = 0u;
     }
     if (first == 0u || last == 0u) {  // no visible key: zeros
-        for (int idx = tid; idx < nh * D; idx += kCombineThreads) store_out(p.out, p.out_dtype, out_at(idx), 0.f);
+        for (int idx = tid; idx < nh * D; idx += nthr) store_out(p.out, p.out_dtype, out_at(idx), 0.f);
         return;
     }
     const int cA = static_cast<int>(first & 0x7fffffffu) - 1, cB = static_cast<int>(last) - 1;
@@ -71,10 +75,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const bool first_is_slot0 = (first & 0x80000000u) != 0u;
     const int R = cB - cA + 1;  // the unit's records: owners cA .. cB
 
-    for (int i = tid; i < R * nh; i += kCombineThreads)
+    for (int i = tid; i < R * nh; i += nthr)
         wts[i] = p.rec_lse[static_cast<size_t>(record_of(cA + i / nh, cA, first_is_slot0)) * HC + (i % nh)];
     __syncthreads();
-    for (int hc = tid; hc < nh; hc += kCombineThreads) {
+    for (int hc = tid; hc < nh; hc += nthr) {
         const float z = p.sink ? p.sink[kvh * p.G + (r0 + hc) % p.G] * kLog2e : -INFINITY;
         float M = z;
         for (int r = 0; r < R; ++r) M = fmaxf(M, wts[r * nh + hc]);
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         for (int r = 0; r < R; ++r) wts[r * nh + hc] = M == -INFINITY ? 0.f : wts[r * nh + hc] * inv;
     }
     __syncthreads();
-    for (int base = tid; base < nh * D; base += 4 * kCombineThreads) {
+    for (int base = tid; base < nh * D; base += 4 * nthr) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int r0 = 0; r0 < R; r0 += kRecBatch) {
             float v[kRecBatch][4];
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
             for (int r = 0; r < kRecBatch; ++r)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int idx = base + k * kCombineThreads;
+                    const int idx = base + k * nthr;
                     v[r][k] = 0.f;
                     if (r0 + r < R && idx < nh * D) {
                         const int hc = idx / D, d = idx - hc * D;
@@ -112,13 +116,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
             for (int r = 0; r < kRecBatch; ++r)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int idx = base + k * kCombineThreads;
+                    const int idx = base + k * nthr;
                     if (r0 + r < R && idx < nh * D) acc[k] = fmaf(wts[(r0 + r) * nh + idx / D], v[r][k], acc[k]);
                 }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int idx = base + k * kCombineThreads;
+            const int idx = base + k * nthr;
             if (idx < nh * D) store_out(p.out, p.out_dtype, out_at(idx), acc[k]);
         }
     }
@@ -128,9 +132,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s)
 {
-    // one CTA per unit, and one that rebalances the partial kernel's ranges
+    // one CTA per unit, and one that rebalances the partial kernel's ranges; a
+    // thread per four output elements of a unit's rows, in whole warps
     const long long blocks = static_cast<long long>(p.B) * p.Hkv * p.head_groups + 1;
     if (blocks == 1) return cudaSuccess;
+    const int rows = p.heads_per_cta < p.q_len * p.G ? p.heads_per_cta : p.q_len * p.G;
+    int threads = (rows * p.D / 4 + 31) / 32 * 32;
+    threads = threads < kCombineMinThreads ? kCombineMinThreads : (threads > kCombineMaxThreads ? kCombineMaxThreads : threads);
     // weights for up to every range's record of a unit
     const size_t smem = static_cast<size_t>(p.P) * (p.heads_per_cta < kMaxHeads ? p.heads_per_cta : kMaxHeads) * 4;
     if (smem > 48 * 1024) {
@@ -138,7 +146,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s)
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    return launch_dependent(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads), smem, s, p);
+    return launch_dependent(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), smem, s, p);
 }
 
 }  // namespace uaa
