@@ -608,7 +608,7 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
 uaa_status run_append_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws,
                               const Plan& pl, cudaStream_t s)
 {
-    // one token per sequence; a chunk's append runs first, one CTA per token (a fused
+    // one token per sequence; a chunk's append runs first, a warp per head row (a fused
     // kernel that staged a chunk's rows itself measured slower: its prep warp's
     // start-of-segment work is not hidden at one CTA per SM)
     if (pl.kernel == 1 && pl.q_len == 1) return run_partial(d, a, ws, pl, s, true);

@@ -1,12 +1,13 @@
 // append.cu -- step 1 of the decode step: per-head QK RMSNorm, rotary embedding at
 // the absolute KV index, and the append of the new k / v rows to the cache.
 //
-// One CTA of 16 warps per token of each sequence. The CTA first builds the cos /
-// sin table of the token's position (rope_cos_sin) while each warp loads its
-// first head row; then each warp takes whole rows, loading the next while it
-// processes the current one: q rows go to the workspace pre-multiplied by the
-// partial kernel's logit prescale, k rows and v rows go to slot seq_lens[b] + t
-// of the cache for token t. vq8 values (and q8 keys, after the rotation) are quantised in fp32
+// CTAs of 16 warps per token of each sequence, as many as give every warp one of
+// the token's Hq + 2 Hkv head rows (a warp walking several rows is a chain of
+// dependent loads). Each CTA first builds the cos / sin table of the token's
+// position (rope_cos_sin) while each warp loads its first head row; then each
+// warp takes whole rows, loading the next while it processes the current one: q
+// rows go to the workspace pre-multiplied by the partial kernel's logit
+// prescale, k rows and v rows go to slot seq_lens[b] + t of the cache for token t. vq8 values (and q8 keys, after the rotation) are quantised in fp32
 // with IEEE division and round-half-even, the storage rule of the vq8 cache
 // (llamay "Models and formats", "The KV cache, in three precisions").
 #include "internal.cuh"
@@ -60,16 +61,20 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     __shared__ float rowbuf[kAppendWarps][D];
 
     grid_dependency_wait();  // the step's inputs and the previous step's reads are complete
-    const int b = blockIdx.x / p.q_len, tok = blockIdx.x - b * p.q_len;  // one CTA per token
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // each warp takes rows warp, warp + W, ...; the next row is loaded while the
-    // current one is processed (the first load goes out before the length's)
     const int n_rows = p.Hq + 2 * p.Hkv;
+    const int parts = (n_rows + kAppendWarps - 1) / kAppendWarps;  // CTAs per token
+    const int bt = blockIdx.x / parts, part = blockIdx.x - bt * parts;
+    const int b = bt / p.q_len, tok = bt - b * p.q_len;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = part * kAppendWarps + warp;  // this warp's first row
+    const int row_step = parts * kAppendWarps;
+
+    // each warp takes rows row0, row0 + row_step, ...; the next row is loaded while
+    // the current one is processed (the first load goes out before the length's)
     float x[EPL], nxt[EPL];
-    if (warp < n_rows) {
+    if (row0 < n_rows) {
         size_t at;
-        const void* src = row_source(p, b, tok, warp, at);
+        const void* src = row_source(p, b, tok, row0, at);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
     }
@@ -78,7 +83,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     // not all fit the cache is not appended (and not advanced)
     const int L = p.seq_lens[b];
     const bool fits = L >= 0 && L + p.q_len <= p.cap;
-    if (threadIdx.x == 0 && tok == 0) {
+    if (threadIdx.x == 0 && tok == 0 && part == 0) {
         if (!fits) atomicOr(p.status, UAA_DEVFLAG_CAPACITY);
         else if (L > p.max_len) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
     }
@@ -91,12 +96,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                 cs[i0 + lane] = rope_pair_cos_sin(i0 + lane, p.half_rot, pos, param_at_lane(p.inv_freq_over_pi + i0, lane),
                                                   p.mscale);
         __syncthreads();  // the cos / sin table is complete
-        for (int r = warp; r < n_rows; r += kAppendWarps) {
+        for (int r = row0; r < n_rows; r += row_step) {
 #pragma unroll
             for (int i = 0; i < EPL; ++i) x[i] = nxt[i];
-            if (r + kAppendWarps < n_rows) {
+            if (r + row_step < n_rows) {
                 size_t at;
-                const void* src = row_source(p, b, tok, r + kAppendWarps, at);
+                const void* src = row_source(p, b, tok, r + row_step, at);
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
             }
@@ -169,13 +174,9 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
         }
     }
     __syncthreads();
-    if (p.q_len == 1) {  // the sequence's only CTA
-        if (threadIdx.x == 0 && fits) p.seq_lens[b] = L + 1;
-        return;
-    }
-    // several tokens: every CTA of the grid counts in once it has read its length;
-    // the last one advances them all (the counter, the workspace word after the
-    // status word, wraps to zero for the next launch)
+    // every CTA of the grid counts in once it has read its length; the last one
+    // advances them all (the counter, the workspace word after the status word,
+    // wraps to zero for the next launch)
     __shared__ bool last;
     if (threadIdx.x == 0) {
         __threadfence();
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
-    const dim3 grid(p.B * p.q_len), block(kAppendWarps * 32);  // one CTA per token
+    const int parts = (p.Hq + 2 * p.Hkv + kAppendWarps - 1) / kAppendWarps;  // a warp per head row
+    const dim3 grid(p.B * p.q_len * parts), block(kAppendWarps * 32);
     const bool f32 = p.io_dtype == UAA_DTYPE_F32;
     switch (p.D) {
     case 64:
