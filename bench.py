@@ -448,6 +448,9 @@ def run_uaa(args, world, rank, local) -> dict | None:
         smp = oracle_sample(W.layer_configs(cfg)[0], cases[0], args.cpu_budget, n_thr)
         cpu = {"value": smp["bytes"] / smp["seconds"] / 1e9, "unit": "GB/s", "cores": n_thr, "kind": "oracle",
                "sample": smp["sample"]}
+        if n_thr > 1:  # and on one core, on a smaller sample of the same workload
+            one = oracle_sample(W.layer_configs(cfg)[0], cases[0], min(5.0, args.cpu_budget / 3), 1)
+            cpu["one_core"] = {"value": one["bytes"] / one["seconds"] / 1e9, "sample": one["sample"]}
     decodes = n_dec * args.steps * world
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
