@@ -198,6 +198,18 @@ def test_large_batches_are_sliced(L):
     assert (lay.slice_batch, lay.n_slices) == (1024, 3)
 
 
+def test_large_chunked_batches_are_sliced(L):
+    """Slices with several tokens per sequence: the same 1024-sequence slices, and
+    the q' region holds every slice's q_len rows per sequence (slice s starts
+    1024 q_len Hq rows in)."""
+    cfg = W.config("llama31_8b_decode")
+    d = B.make_desc(cfg)
+    for T in (2, 4):
+        lay = B.uaa_get_workspace_layout(d, 2500, 100, 152, q_len=T)
+        assert (lay.slice_batch, lay.n_slices) == (1024, 3)
+        assert lay.prefix_offset - lay.q_rot_offset >= 2500 * T * cfg["n_q_heads"] * cfg["head_dim"] * 4
+
+
 @pytest.mark.parametrize("name,kv", [("llama31_8b_decode", "bf16"), ("gptoss_vq8_sink", "vq8"),
                                      ("llama31_8b_decode", "q8"), ("gemma2_9b_swa", "bf16"),
                                      ("llama32_1b_tiny", "f32")])
