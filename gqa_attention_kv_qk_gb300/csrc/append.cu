@@ -213,7 +213,9 @@ __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
     const int parts = (p.Hq + 2 * p.Hkv + kAppendWarps - 1) / kAppendWarps;  // a warp per head row
-    const dim3 grid(p.B * p.q_len * parts), block(kAppendWarps * 32);
+    const long long ctas = static_cast<long long>(p.B) * p.q_len * parts;
+    if (ctas > 2147483647LL) return cudaErrorInvalidConfiguration;  // beyond one grid's x extent
+    const dim3 grid(static_cast<unsigned>(ctas)), block(kAppendWarps * 32);
     const bool f32 = p.io_dtype == UAA_DTYPE_F32;
     switch (p.D) {
     case 64:
