@@ -201,7 +201,8 @@ typedef struct {
 
 /* Scratch memory owned by the caller, at least uaa_workspace_size bytes, zeroed
  * once after allocation. It holds the rotated q rows, the split partials, the
- * device status word, the arrival counter of the fused kernel and the range
+ * device status word, the arrival counter of the append and fused kernels (the
+ * last CTA to arrive advances seq_lens) and the range
  * balance state (counters that every completed launch leaves at zero, and the
  * measured slot speeds that carry over to the next launch); it must not be
  * shared by steps that run concurrently. After UAA_DEVFLAG_TIMEOUT zero it
