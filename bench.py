@@ -313,19 +313,21 @@ def run_uaa(args, world, rank, local) -> dict | None:
             graph.replay()
         stream.synchronize()
 
-        # ---- timed region: exactly K benchmark steps
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # ---- timed region: exactly K benchmark steps (an event between steps, for
+        # the per-step spread)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         barrier(world)
         torch.cuda.synchronize()
         with ClockSampler(local) as clocks:
-            ev0.record(stream)
-            for _ in range(args.steps):
+            evs[0].record(stream)
+            for i in range(args.steps):
                 graph.replay()
-            ev1.record(stream)
-            ev1.synchronize()
+                evs[i + 1].record(stream)
+            evs[-1].synchronize()
         torch.cuda.synchronize()
         barrier(world)
-        dev_s = ev0.elapsed_time(ev1) / 1e3
+        dev_s = evs[0].elapsed_time(evs[-1]) / 1e3
+        per_step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
         for layer in layers:
             st = layer.device_status(stream)
             if st:
@@ -455,6 +457,9 @@ def run_uaa(args, world, rank, local) -> dict | None:
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 4),
+        # this rank's steps one by one (ms): the spread behind the mean above
+        "step_ms": {"median": round(per_step_ms[len(per_step_ms) // 2], 4), "best": round(per_step_ms[0], 4),
+                    "worst": round(per_step_ms[-1], 4)} if per_step_ms else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"f32": "f32", "q8": "f16"}.get(cfg["kv_dtype"], "bf16"),
         "data": "synthetic (seeded N(0,1) cache and inputs)",
         "decode_steps_per_s": round(decodes / dev_s / world, 2),
