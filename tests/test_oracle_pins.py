@@ -489,13 +489,36 @@ GRID = [
 ]
 
 
-@pytest.mark.parametrize("spec", GRID, ids=lambda s: "-".join(f"{k}={v}" for k, v in s.items()))
-def test_whole_step_matches_bruteforce(oracle_mod, spec):
+def _random_grid(n: int, seed: int) -> list:
+    """n feature mixes drawn independently: GQA ratio, head_dim, cache and input
+    dtypes, pairing, window, softcap, sink, partial rotary, QK norm (with or
+    without the stored-delta offset), each on a workload's own rope scaling."""
+    rng = np.random.default_rng(seed)
+    names = ["llama31_8b_decode", "qwen3_8b_ragged", "gptoss_vq8_sink", "llama32_1b_tiny", "gemma2_9b_swa",
+             "gemma3_12b_local_global"]
+    grid = []
+    for i in range(n):
+        D, Hkv, G = int(rng.choice([64, 128])), int(rng.choice([1, 2, 4])), int(rng.choice([1, 2, 4, 8]))
+        spec = dict(name=names[i % len(names)], n_q_heads=G * Hkv, n_kv_heads=Hkv, head_dim=D,
+                    kv_dtype=str(rng.choice(["f32", "bf16", "vq8", "q8"])), io_dtype=str(rng.choice(["f32", "bf16"])),
+                    rope_style=str(rng.choice(["neox", "interleaved"])), layers=None,
+                    window=int(rng.integers(1, 30)) if rng.random() < 0.5 else 0,
+                    softcap=float(rng.choice([1.0, 5.0, 30.0])) if rng.random() < 0.4 else 0.0,
+                    has_sink=bool(rng.random() < 0.4))
+        if rng.random() < 0.4:
+            spec["rotary_dim"] = int(rng.choice([D // 4, D // 2]))
+        if rng.random() < 0.4:
+            spec.update(qk_norm=True, norm_offset=bool(rng.random() < 0.5), norm_w_range=(-0.5, 1.5))
+        grid.append(spec)
+    return grid
+
+
+def _step_vs_bruteforce(oracle_mod, spec, lens):
     spec = dict(spec)
     name = spec.pop("name")
-    cfg = W.config(name, batch=3, seq_len=(0, 40), steps=1, **spec)
+    cfg = W.config(name, batch=len(lens), seq_len=(0, 40), steps=1, **spec)
     cfg = W.layer_configs(cfg)[0]
-    case = host_case(cfg, lens=[0, 17, 40])
+    case = host_case(cfg, lens=lens)
     out, a = run_oracle_step(case, oracle_mod)
     # brute force on fp64 copies of the same stored inputs
     f64 = lambda t: t.to(torch.float64).numpy().copy()
@@ -527,6 +550,18 @@ def test_whole_step_matches_bruteforce(oracle_mod, spec):
     if kv == "q8":  # the appended keys' codes and scales: the vq8 rule on the rotated key
         assert np.array_equal(a["k_cache"], kc.astype(np.int8))
         assert np.array_equal(a["k_scale"], ks.astype(np.float32))
+
+
+@pytest.mark.parametrize("spec", GRID, ids=lambda s: "-".join(f"{k}={v}" for k, v in s.items()))
+def test_whole_step_matches_bruteforce(oracle_mod, spec):
+    _step_vs_bruteforce(oracle_mod, spec, [0, 17, 40])
+
+
+@pytest.mark.parametrize("i,spec", list(enumerate(_random_grid(24, seed=11))), ids=[f"mix{i}" for i in range(24)])
+def test_random_feature_mixes_match_bruteforce(oracle_mod, i, spec):
+    """Seeded random mixes of every feature the step has, at random lengths."""
+    lens = [int(x) for x in np.random.default_rng(100 + i).integers(0, 41, size=3)]
+    _step_vs_bruteforce(oracle_mod, spec, lens)
 
 
 CHUNKS = [
