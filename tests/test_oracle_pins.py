@@ -573,7 +573,31 @@ CHUNKS = [
 ]
 
 
-@pytest.mark.parametrize("spec", CHUNKS, ids=lambda s: "-".join(f"{k}={v}" for k, v in s.items()))
+def _random_chunks(n: int, seed: int) -> list:
+    """Chunk mixes for the matrix brute force (bf16 and fp32 caches): 2 to 8
+    tokens, windows shorter and longer than the chunk, softcap, sink, partial
+    rotary, QK norm."""
+    rng = np.random.default_rng(seed)
+    names = ["llama31_8b_decode", "qwen3_8b_ragged", "gptoss_vq8_sink", "gemma2_9b_swa"]
+    grid = []
+    for i in range(n):
+        D, Hkv, G = int(rng.choice([64, 128])), int(rng.choice([1, 2])), int(rng.choice([1, 2, 4, 8]))
+        spec = dict(name=names[i % len(names)], n_q_heads=G * Hkv, n_kv_heads=Hkv, head_dim=D,
+                    kv_dtype=str(rng.choice(["f32", "bf16"])), io_dtype=str(rng.choice(["f32", "bf16"])),
+                    rope_style=str(rng.choice(["neox", "interleaved"])), layers=None, q_len=int(rng.integers(2, 9)),
+                    window=int(rng.integers(1, 12)) if rng.random() < 0.6 else 0,
+                    softcap=float(rng.choice([2.0, 20.0])) if rng.random() < 0.4 else 0.0,
+                    has_sink=bool(rng.random() < 0.4))
+        if rng.random() < 0.4:
+            spec["rotary_dim"] = D // 2
+        if rng.random() < 0.4:
+            spec.update(qk_norm=True, norm_offset=bool(rng.random() < 0.5), norm_w_range=(-0.5, 1.5))
+        grid.append(spec)
+    return grid
+
+
+@pytest.mark.parametrize("spec", CHUNKS + _random_chunks(10, seed=12),
+                         ids=[f"fixed{i}" for i in range(len(CHUNKS))] + [f"mix{i}" for i in range(10)])
 def test_chunk_matches_masked_matrix_bruteforce(oracle_mod, spec):
     """Several tokens per sequence: the oracle takes them as decode steps in order;
     the brute force appends all of them first and masks one logit matrix by each
