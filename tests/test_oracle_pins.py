@@ -709,3 +709,21 @@ def test_planted_mistakes_break_the_tolerance(oracle_mod, mistake):
         kg, kw = BF.bf16_round(oracle_mod.bf16_to_f64(kg)), oracle_mod.bf16_to_f64(kw)
     k_ulps = np.abs(kg - kw) / (np.abs(kg) * 2.0 ** -8 + 1e-30)
     assert mx > TOL_MAX or mean > TOL_MEAN or k_ulps.max() > 1.0, (mistake, mx, mean, k_ulps.max())
+
+
+@pytest.mark.parametrize("name", ["llama31_8b_decode", "gptoss_vq8_sink", "llama31_8b_q8", "llama31_8b_verify"])
+def test_oracle_is_independent_of_its_thread_count(oracle_mod, name):
+    """The oracle splits a step over threads by (sequence, head) unit only: one
+    thread and eight give the same bits, caches and lengths included."""
+    cfg = W.layer_configs(W.config(name, batch=4, seq_len=(1, 300), steps=1))[0]
+    lens = [1, 77, 150, 300]
+    outs = []
+    for n in (1, 8):
+        case = host_case(cfg, lens=lens)
+        out, a = run_oracle_step(case, oracle_mod, n_threads=n)
+        outs.append((out, a))
+    (o1, a1), (o8, a8) = outs
+    assert np.array_equal(o1, o8)
+    for k in ("k_cache", "v_cache", "v_scale", "k_scale", "seq_lens"):
+        if a1[k] is not None:
+            assert np.array_equal(a1[k], a8[k]), k
