@@ -148,6 +148,86 @@ def test_yarn_ramp_endpoints_and_mscale(oracle_mod):
     assert ms == pytest.approx(1.0 + 0.1 * math.log(32.0), rel=1e-15)
 
 
+def rotations_in_original_context(D, base, orig, p):
+    """How many turns pair p (a real number here) makes over the original context:
+    orig / wavelength = orig * base^(-2p/D) / (2 pi)."""
+    return orig * np.power(base, -2.0 * np.asarray(p, dtype=np.float64) / D) / (2 * math.pi)
+
+
+def yarn_ramp_violations(inv, plain, D, base, factor, orig, beta_fast, beta_slow):
+    """Checks a YaRN frequency table against the reading of the gpt-oss YaRN ramp
+    (llamay "Architectures": gpt-oss uses YaRN; the pages give no formula): the
+    kept share u_p = (theta'_p / theta_p - 1/factor) / (1 - 1/factor) of every pair
+    is 1 where the pair turns more than beta_fast times over the original context,
+    0 where it turns fewer than beta_slow times, and in between lies on ONE straight
+    line in the pair index whose ends, extended to u = 1 and u = 0, fall on the
+    (real-valued) pair indices that turn exactly beta_fast and beta_slow times.
+    Returns the list of violated conditions (empty when the table passes)."""
+    bad = []
+    u = (inv / plain - 1.0 / factor) / (1.0 - 1.0 / factor)
+    p = np.arange(D // 2, dtype=np.float64)
+    r = rotations_in_original_context(D, base, orig, p)
+    keep, squash = r > beta_fast, r < beta_slow
+    mid = ~keep & ~squash
+    if not np.allclose(u[keep], 1.0, rtol=0, atol=1e-13):
+        bad.append("pairs above beta_fast turns are changed")
+    if not np.allclose(u[squash], 0.0, rtol=0, atol=1e-13):
+        bad.append("pairs below beta_slow turns are not divided by the factor")
+    pm, um = p[mid], u[mid]
+    if pm.size < 3:
+        bad.append("fewer than three pairs inside the ramp")
+        return bad
+    if np.any(um <= 0.0) or np.any(um >= 1.0):
+        bad.append("a ramp pair is at an end value")
+    if np.abs(np.diff(um, 2)).max() > 1e-12:
+        bad.append("the ramp is not a straight line in the pair index")
+    slope, icpt = np.polyfit(pm, um, 1)
+    p_one, p_zero = (1.0 - icpt) / slope, -icpt / slope
+    if abs(rotations_in_original_context(D, base, orig, p_one) / beta_fast - 1) > 1e-9:
+        bad.append("the ramp does not leave 1 where a pair turns beta_fast times")
+    if abs(rotations_in_original_context(D, base, orig, p_zero) / beta_slow - 1) > 1e-9:
+        bad.append("the ramp does not reach 0 where a pair turns beta_slow times")
+    return bad
+
+
+YARN_RAMP_CASES = [(64, 150000.0, 32.0, 4096), (128, 150000.0, 32.0, 4096),
+                   (64, 10000.0, 16.0, 4096), (128, 10000.0, 32.0, 4096), (128, 1e6, 4.0, 32768)]
+
+
+@pytest.mark.parametrize("D,base,factor,orig", YARN_RAMP_CASES)
+def test_yarn_ramp_interior(oracle_mod, D, base, factor, orig):
+    """Every pair of the oracle's YaRN table, the interior of the ramp included,
+    against the turn counts over the original context (no rounding of the ends)."""
+    cfg = rope_cfg(head_dim=D, rope_theta=base, rope_scaling="yarn", factor=factor,
+                   original_max_pos=orig, beta_fast=32.0, beta_slow=1.0)
+    inv, _ = oracle_mod.rope_inv_freq(cfg)
+    plain = BF.plain_inv_freq(D, base)
+    assert yarn_ramp_violations(inv, plain, D, base, factor, orig, 32.0, 1.0) == []
+
+
+@pytest.mark.parametrize("variant", ["rounded_ends", "linear_in_divisor", "linear_in_turns"])
+@pytest.mark.parametrize("D,base,factor,orig", YARN_RAMP_CASES[:4])
+def test_yarn_ramp_pin_rejects_other_ramps(D, base, factor, orig, variant):
+    """Negative controls for the interior pin: the other common readings of the YaRN
+    ramp (ends rounded down / up to whole pairs; a ramp on the divisor instead of
+    the frequency; a ramp linear in the turn count) are tables the pin must refuse."""
+    plain = BF.plain_inv_freq(D, base)
+    p = np.arange(D // 2, dtype=np.float64)
+    lo = D * math.log(orig / (2 * math.pi * 32.0)) / (2 * math.log(base))
+    hi = D * math.log(orig / (2 * math.pi * 1.0)) / (2 * math.log(base))
+    if variant == "rounded_ends":
+        ramp = np.clip((p - math.floor(lo)) / (math.ceil(hi) - math.floor(lo)), 0, 1)
+        inv = plain / factor * ramp + plain * (1 - ramp)
+    elif variant == "linear_in_divisor":
+        ramp = np.clip((p - lo) / (hi - lo), 0, 1)
+        inv = plain / (1 + ramp * (factor - 1))
+    else:
+        r = rotations_in_original_context(D, base, orig, p)
+        keep = np.clip((r - 1.0) / (32.0 - 1.0), 0, 1)
+        inv = plain * keep + plain / factor * (1 - keep)
+    assert yarn_ramp_violations(inv, plain, D, base, factor, orig, 32.0, 1.0) != []
+
+
 # ------------------------------------------------------------------ RoPE rotation
 
 @pytest.mark.parametrize("style", ["neox", "interleaved"])
