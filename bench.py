@@ -2,13 +2,19 @@
 """Benchmark of the GQA decode step on GB300: decode-attention HBM GB/s and decode
 steps/sec at 1 GPU (N replicas under torchrun).
 
-Workload (default): the Llama-3.1-8B-like decode, 16 sequences at 8192 cached
+Headline workload: the Llama-3.1-8B-like decode, 16 sequences at 8192 cached
 tokens, 32 q / 8 kv heads, head_dim 128, bf16 cache, NeoX RoPE with llama3
 factor 8. One benchmark step = 64 consecutive decode steps from 8192 cached
 tokens (each: RoPE/append + split-K partials in one kernel, combine), after which the lengths
 return to 8192 (a 64-byte device copy) so every step times the same work. The
 64 decode steps are captured once in a CUDA graph and replayed. The KV cache
 (~545 MB) is larger than L2 (129 MB), so no flush is needed between steps.
+
+The same JSON line carries `per_config`: the other four workloads of the
+suite (tiny Llama-3.2-1B-like fp32 step, warm and with L2 flushed between steps;
+Qwen3-8B-like ragged; Gemma-2-9B-like windowed + global; gpt-oss-like vq8 with
+sinks), each measured the same way at the same --steps / --warmup, with its own
+roofline, end-to-end figure, clocks and oracle baseline.
 
 value       = algorithmic bytes of all timed steps / device time (CUDA events)
 e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each with
@@ -17,6 +23,7 @@ e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each wi
 roofline    = the split-K partial kernel alone (for bf16 / vq8 / q8 caches the kernel
               that also performs the append): its algorithmic bytes (visible KV
               rows) / its mean launch duration, against the measured HBM copy peak
+              (frac) and the 8 TB/s nominal HBM3e figure (frac_of_nominal)
 cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample
 """
 from __future__ import annotations
@@ -40,6 +47,11 @@ from gqa_attention_kv_qk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (% of GB300 peak) and decode steps/sec at 1 GPU"
 DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_paged": 64, "llama31_8b_verify": 16}
+HEADLINE = "llama31_8b_decode"
+# the suite's other workloads, reported beside the headline in the same line
+PER_CONFIG = ("llama32_1b_tiny", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink")
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+L2_BYTES = 129 * 2**20
 
 
 def measured_peaks() -> dict:
@@ -51,24 +63,22 @@ def measured_peaks() -> dict:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per launch of the partial kernel from the committed ncu summary
-    (profiles/partial_tc_<workload>.md), or None when there is none or when the
-    kernel's sources changed since the counters were taken."""
+    """DRAM bytes per launch of the partial kernel from one ncu capture
+    (profiles/traffic.json, written beside the capture's summary), or None when
+    there is none or when the kernel's sources changed since the counters were
+    taken."""
     import hashlib
-    import re
-    prof = os.path.join(ROOT, "profiles", f"partial_tc_{workload}.md")
-    if not os.path.exists(prof):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
         return None
-    text = open(prof).read()
-    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    m_h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
-    if not (m_t and m_h):
+    ent = json.load(open(path)).get(workload)
+    if not ent:
         return None
     csrc = os.path.join(ROOT, "gqa_attention_kv_qk_gb300", "csrc")
-    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("partial_tc.cu", "ptx.cuh", "internal.cuh"))
-    if hashlib.sha256(blob).hexdigest()[:16] != m_h.group(1):
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ent["sources"])
+    if hashlib.sha256(blob).hexdigest()[:16] != ent["sources_sha256_16"]:
         return None
-    return int(m_t.group(1))
+    return int(ent["traffic_bytes_per_launch"])
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -216,10 +226,12 @@ def sum_over_ranks(x: float, world: int) -> float:
 
 def oracle_sample(cfg: dict, case: dict, budget_s: float, n_threads: int) -> dict:
     """Time the fp64 CPU oracle on whole decode steps of a prefix of the batch
-    (all heads of each sequence), growing the prefix up to the time budget.
+    (all heads of each sequence), growing the prefix up to the time budget; a
+    whole batch that takes well under the budget is stepped several times (the
+    lengths put back each time, so every repetition is the same work).
     Returns bytes processed, seconds, and a description of the sample."""
     from oracle import oracle as O
-    from tests.cases import oracle_arrays  # the same storage arrays the parity tests use
+    from tests.cases import oracle_arrays  # the storage arrays the parity tests give the oracle
 
     a = oracle_arrays(case, O)
     B = cfg["batch"]
@@ -239,42 +251,106 @@ def oracle_sample(cfg: dict, case: dict, budget_s: float, n_threads: int) -> dic
     t1 = run(1)
     nb = int(max(1, min(B, budget_s / max(t1, 1e-6))))
     secs = run(nb) if nb > 1 else t1
+    reps = 1
+    if nb == B and secs < budget_s / 4:
+        reps = int(min(1000, max(1, budget_s / 2 / max(secs, 1e-6))))
+        secs = sum(run(nb) for _ in range(reps))
     lens = [int(x) for x in lens0[:nb]]
     sub = dict(cfg, batch=nb)
-    return {"bytes": decode_step_bytes(sub, lens), "seconds": secs,
-            "sample": f"one step ({int(cfg.get('q_len', 1) or 1)} token(s) per sequence) of {nb} of {B} "
-                      f"sequences (all {cfg['n_q_heads']} q heads), "
-                      f"{n_threads} threads"}
+    T = int(cfg.get("q_len", 1) or 1)
+    return {"bytes": decode_step_bytes(sub, lens) * reps, "seconds": secs, "steps": reps,
+            "sample": (f"{reps} x " if reps > 1 else "") + f"one step ({T} token(s) per sequence) of {nb} of {B} "
+                      f"sequences (all {cfg['n_q_heads']} q heads), {n_threads} threads"}
+
+
+def cpu_baseline(name: str, cases: list, budget: float) -> dict:
+    """The oracle on the host's cores (one thread per core), and on one core on a
+    smaller sample of the same workload; first layer of a multi-layer workload."""
+    lc = W.layer_configs(W.config(name))[0]
+    n_thr = len(os.sched_getaffinity(0))
+    smp = oracle_sample(lc, cases[0], budget, n_thr)
+    cpu = {"value": smp["bytes"] / smp["seconds"] / 1e9, "unit": "GB/s", "cores": n_thr, "kind": "oracle",
+           "sample": smp["sample"], "ms_per_decode_step": round(smp["seconds"] / smp["steps"] * 1e3, 3)}
+    if n_thr > 1:
+        one = oracle_sample(lc, cases[0], min(5.0, budget / 3), 1)
+        cpu["one_core"] = {"value": one["bytes"] / one["seconds"] / 1e9, "sample": one["sample"]}
+    return cpu
+
+
+# ---------------------------------------------------------------- the workload
+
+def workload_bytes(name: str, T_override=None):
+    """(bytes of one benchmark step, partial-kernel bytes of one benchmark step,
+    decode steps per benchmark step) from the seeded lengths alone (no device)."""
+    cfg = W.config(name)
+    n_dec = DECODES_PER_STEP.get(name, 1)
+    T = int(cfg.get("q_len", 1) or 1)
+    step_bytes = part_bytes = 0
+    for lc in W.layer_configs(cfg):
+        base = [int(x) for x in W.seq_lens(lc)]
+        for t in range(n_dec):
+            cur = [x + t * T for x in base]
+            step_bytes += decode_step_bytes(lc, cur)
+            part_bytes += partial_bytes(lc, [x + T for x in cur])
+    return step_bytes, part_bytes, n_dec
+
+
+def config_block(name: str, world: int) -> dict:
+    """The workload as the JSON line's `config` (the same dict on both arms)."""
+    cfg = W.config(name)
+    lcs = W.layer_configs(cfg)
+    step_bytes, part_bytes, n_dec = workload_bytes(name)
+    kv_mb = part_bytes / n_dec / 1e6
+    out = {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"], "n_q_heads": cfg["n_q_heads"],
+           "n_kv_heads": cfg["n_kv_heads"], "head_dim": cfg["head_dim"], "kv_dtype": cfg["kv_dtype"],
+           "layers": len(lcs), "decode_steps_per_step": n_dec, "q_len": int(cfg.get("q_len", 1) or 1),
+           "parallelism": f"replicas x{world}"}
+    if part_bytes / n_dec > 2 * L2_BYTES:
+        out["l2"] = "inputs larger than L2 (KV cache %.0f MB read per decode step)" % kv_mb
+    else:
+        out["l2"] = ("KV cache of %.2f MB per decode step fits in L2: warm (graph replayed back to back) "
+                     "and cold (L2 flushed by a %d MB write before each step) both reported" %
+                     (kv_mb, 3 * L2_BYTES // 2**20))
+    return out
 
 
 # ---------------------------------------------------------------- the GPU arm
 
 def build_layers(cfg: dict, cap_extra: int, device: str):
-    from tests.cases import gpu_layer, host_case
+    from gqa_attention_kv_qk_gb300.layer import DecodeLayer
     layers, cases = [], []
     for lc in W.layer_configs(cfg):
-        case = host_case(lc, cap=W.capacity(lc, extra=cap_extra))
-        layers.append(gpu_layer(case, device))
+        case = W.host_case(lc, cap=W.capacity(lc, extra=cap_extra))
+        layers.append(DecodeLayer.for_case(case, device))
         cases.append(case)
     return layers, cases
 
 
-def run_uaa(args, world, rank, local) -> dict | None:
+def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, cpu_budget: float) -> dict | None:
+    """One workload on this rank's GPU: device-timed steps (and, for a workload
+    whose cache fits in L2, the same steps with L2 flushed before each), the
+    partial kernel alone, the end-to-end leg with host buffers, and on rank 0 the
+    oracle baseline. Returns the record on rank 0."""
     from gqa_attention_kv_qk_gb300 import binding as Bd
-    from gqa_attention_kv_qk_gb300 import build as ext
-    ext.build()
     device = f"cuda:{local}"
-    torch.cuda.set_device(local)
-    name = args.workload
     cfg = W.config(name, seed=W.CONFIGS[name]["seed"] + 1000 * rank)
-    n_dec = DECODES_PER_STEP.get(name, 1)
+    step_bytes, part_bytes, n_dec = workload_bytes(name)
     T = int(cfg.get("q_len", 1) or 1)  # tokens per sequence and call
     layers, cases = build_layers(cfg, cap_extra=n_dec * T + 1, device=device)
+    if rank != 0:  # the seeded lengths of another rank's replica: its own bytes
+        step_bytes = part_bytes = 0
+        for lc, case in zip(W.layer_configs(cfg), cases):
+            base = [int(x) for x in case["lens"]]
+            for t in range(n_dec):
+                cur = [x + t * T for x in base]
+                step_bytes += decode_step_bytes(lc, cur)
+                part_bytes += partial_bytes(lc, [x + T for x in cur])
     lens0 = [case["lens"].clone() for case in cases]
     lens0_dev = [l.to(device) for l in lens0]
     hint = [int(l.max()) + (n_dec - 1) * T for l in lens0]
     stream = torch.cuda.Stream(device)
     inputs = [{k: case[k].to(device) for k in ("q", "k_new", "v_new")} for case in cases]
+    fits_l2 = part_bytes / n_dec <= 2 * L2_BYTES
 
     def reset():
         for layer, l0 in zip(layers, lens0_dev):
@@ -287,15 +363,6 @@ def run_uaa(args, world, rank, local) -> dict | None:
                 layer.step(inp["q"], inp["k_new"], inp["v_new"], stream=stream, max_seq_len=hint[li])
         reset()
 
-    # bytes of one benchmark step (lengths grow by one per decode step)
-    step_bytes = 0
-    part_bytes = 0
-    for lc, l0 in zip(W.layer_configs(cfg), lens0):
-        base = [int(x) for x in l0]
-        for t in range(n_dec):
-            cur = [x + t * T for x in base]
-            step_bytes += decode_step_bytes(lc, cur)
-            part_bytes += partial_bytes(lc, [x + T for x in cur])
     # kernels of one call of a layer: the fused append+partial and the combine
     # (bf16 / vq8 / q8 caches, one token), or append, partial and combine
     fused = [layer.layout().kernel == 1 and T == 1 for layer in layers]
@@ -332,6 +399,25 @@ def run_uaa(args, world, rank, local) -> dict | None:
             st = layer.device_status(stream)
             if st:
                 raise RuntimeError(f"device flags 0x{st:x} after the timed region")
+
+        # ---- cold: the same K steps, each after a write of 1.5x L2 (untimed), so
+        # the step finds none of its cache in L2
+        cold_s = None
+        if fits_l2:
+            flush = torch.empty(3 * L2_BYTES // 2, dtype=torch.uint8, device=device)
+            ce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            barrier(world)
+            torch.cuda.synchronize()
+            for e0, e1 in ce:
+                flush.fill_(1)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            stream.synchronize()
+            barrier(world)
+            cold_s = sum(e0.elapsed_time(e1) for e0, e1 in ce) / 1e3
+            del flush
 
         # ---- the partial kernel alone (events on the launching stream): the fused
         # append+partial kernel of the step for bf16 / vq8 caches, the partial
@@ -437,64 +523,95 @@ def run_uaa(args, world, rank, local) -> dict | None:
     dev_s = max_over_ranks(dev_s, world)
     e2e_s = max_over_ranks(e2e_s, world)
     total_bytes = sum_over_ranks(step_bytes * args.steps, world)
+    if cold_s is not None:
+        cold_s = max_over_ranks(cold_s, world)
+    del graph, layers, inputs, dev_in, dev_out, outs
+    torch.cuda.empty_cache()
     if rank != 0:
         return None
     peaks = measured_peaks()
     value = total_bytes / dev_s / 1e9
-    # part_bytes covers one round (n_dec launches per layer); the timing covers all rounds
-    part_gbs = (part_bytes / (n_dec * len(layers))) / (part_s / n_part) / 1e9 if n_part else None
-    clk = clocks.summary()
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        n_thr = len(os.sched_getaffinity(0))
-        smp = oracle_sample(W.layer_configs(cfg)[0], cases[0], args.cpu_budget, n_thr)
-        cpu = {"value": smp["bytes"] / smp["seconds"] / 1e9, "unit": "GB/s", "cores": n_thr, "kind": "oracle",
-               "sample": smp["sample"]}
-        if n_thr > 1:  # and on one core, on a smaller sample of the same workload
-            one = oracle_sample(W.layer_configs(cfg)[0], cases[0], min(5.0, args.cpu_budget / 3), 1)
-            cpu["one_core"] = {"value": one["bytes"] / one["seconds"] / 1e9, "sample": one["sample"]}
+    # part_bytes covers one benchmark step (n_dec launches per layer); the timing covers all rounds
+    n_layers = len(cases)
+    part_gbs = (part_bytes / (n_dec * n_layers)) / (part_s / n_part) / 1e9 if n_part else None
     decodes = n_dec * args.steps * world
-    return {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 4),
+    rec = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(dev_s / args.steps * 1e3, 4),
         # this rank's steps one by one (ms): the spread behind the mean above
         "step_ms": {"median": round(per_step_ms[len(per_step_ms) // 2], 4), "best": round(per_step_ms[0], 4),
                     "worst": round(per_step_ms[-1], 4)} if per_step_ms else None,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"f32": "f32", "q8": "f16"}.get(cfg["kv_dtype"], "bf16"),
-        "data": "synthetic (seeded N(0,1) cache and inputs)",
         "decode_steps_per_s": round(decodes / dev_s / world, 2),
         "tokens_per_s_per_seq": round(decodes * T / dev_s / world, 2),  # q_len new tokens per sequence and step
-        "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
-        "config": {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"], "n_q_heads": cfg["n_q_heads"],
-                   "n_kv_heads": cfg["n_kv_heads"], "head_dim": cfg["head_dim"], "kv_dtype": cfg["kv_dtype"],
-                   "decode_steps_per_step": n_dec, "q_len": T, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (KV cache %.0f MB)" % (part_bytes / n_dec / 1e6),
-                   "timing": "CUDA graph of one benchmark step, replayed K times; CUDA events"},
+        "pct_of_measured_copy_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "pct_of_nominal_hbm_peak": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "dtype": {"f32": "f32", "q8": "f16"}.get(cfg["kv_dtype"], "bf16"),
+        "config": config_block(name, world),
         "roofline": {"bound": "hbm", "achieved": round(part_gbs, 2) if part_gbs else None,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(part_gbs / peaks["hbm_gbs"], 4) if part_gbs else None,
                      "traffic": measured_traffic(name),
+                     "frac_of_nominal": round(part_gbs / NOMINAL_HBM_GBS, 4) if part_gbs else None,
                      "kernel": "fused append + split-K partial" if all(fused) else "split-K partial",
                      "peak_source": peaks["source"],
-                     "bytes_per_launch": part_bytes // max(1, n_dec * len(layers)),
+                     "bytes_per_launch": part_bytes // max(1, n_dec * n_layers),
                      "mean_launch_us": round(part_s / n_part * 1e6, 2) if n_part else None},
         "e2e": {"value": round(total_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
-        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu_baseline(name, cases, cpu_budget) if with_cpu else None,
     }
+    if cold_s is not None:
+        rec["cold"] = {"value": round(total_bytes / cold_s / 1e9, 2), "unit": "GB/s",
+                       "ms_per_step": round(cold_s / args.steps * 1e3, 4),
+                       "decode_steps_per_s": round(decodes / cold_s / world, 2),
+                       "l2": "flushed before each step by a %d MB write (not timed)" % (3 * L2_BYTES // 2**20)}
+        rec["warm_note"] = "steps replayed back to back: the cache stays in L2 between steps"
+    return rec
+
+
+def run_uaa(args, world, rank, local) -> dict | None:
+    from gqa_attention_kv_qk_gb300 import build as ext
+    ext.build()
+    torch.cuda.set_device(local)
+    name = args.workload
+    with_cpu = world == 1 and not args.no_cpu_baseline
+    head = measure(name, args, world, rank, local, with_cpu, args.cpu_budget)
+    per = {}
+    if name == HEADLINE and not args.no_per_config:
+        for other in PER_CONFIG:
+            r = measure(other, args, world, rank, local, with_cpu, args.cpu_budget / 3)
+            if r is not None:
+                r.pop("dtype", None)
+                per[other] = r
+    if rank != 0:
+        return None
+    res = {"metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "step_ms": head["step_ms"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+           "data": "synthetic (seeded N(0,1) cache and inputs)",
+           "decode_steps_per_s": head["decode_steps_per_s"], "tokens_per_s_per_seq": head["tokens_per_s_per_seq"],
+           "pct_of_measured_copy_peak": head["pct_of_measured_copy_peak"],
+           "pct_of_nominal_hbm_peak": head["pct_of_nominal_hbm_peak"],
+           "config": head["config"],
+           "timing": "CUDA graph of one benchmark step, replayed K times; CUDA events on the launching stream",
+           "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+           "clocks": head["clocks"], "cpu_baseline": head["cpu_baseline"]}
+    if "cold" in head:
+        res["cold"] = head["cold"]
+    if per:
+        res["per_config"] = per
+    return res
 
 
 def run_reference(args, world, rank) -> dict | None:
     """The oracle as the reference arm, on the host cores (rank 0 only)."""
     if rank != 0:
         return None
-    from tests.cases import host_case
     name = args.workload
     cfg = W.config(name)
     lc = W.layer_configs(cfg)[0]
-    case = host_case(lc, cap=W.capacity(lc, extra=2))
+    case = W.host_case(lc, cap=W.capacity(lc, extra=2))
     n_thr = len(os.sched_getaffinity(0))
     budget = max(0.5, args.cpu_budget / max(1, args.steps))
     for _ in range(args.warmup):
@@ -511,7 +628,8 @@ def run_reference(args, world, rank) -> dict | None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) cache and inputs)",
-            "config": {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"]},
+            "config": config_block(name, world),
+            "timing": "wall clock of each sample (time.perf_counter)",
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": n_thr, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -526,6 +644,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama31_8b_decode", choices=list(W.CONFIGS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the headline workload only (not the suite's other four)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "uaa":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -773,6 +773,9 @@ namespace {
 
 std::mutex g_static_scratch_mu;
 void* g_static_scratch_addr[64] = {};
+// per device: a call launched the partial kernel but not the combine that frees
+// its range slots, so the next call starts the scheduling state over
+bool g_static_scratch_dirty[64] = {};
 
 uaa_status static_scratch_address(void** out)
 {
@@ -812,9 +815,19 @@ extern "C" uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const ua
     const uaa_workspace ws{scratch, (size_t)UAA_STATIC_SCRATCH_BYTES};
     UAA_TRY(check_args(desc, args, &ws, true));
     if (args->batch == 0) return UAA_OK;
-    // the status word is the only scratch that must start at zero
-    const cudaError_t e = cudaMemsetAsync(static_cast<char*>(scratch) + pl.off_status, 0, sizeof(uint32_t), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch status word");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    // Every call starts from a clear status word and arrival counter (the first 8
+    // bytes: a launch whose bounded wait gave up may leave the counter short of
+    // its wrap). After a call that launched the partial kernel without its
+    // combine, the range slots stay claimed: clear the balance state too.
+    const size_t clear = g_static_scratch_dirty[dev] ? pl.off_qrot : 2 * sizeof(uint32_t);
+    e = cudaMemsetAsync(static_cast<char*>(scratch) + pl.off_status, 0, clear, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch state");
+    g_static_scratch_dirty[dev] = true;
     UAA_TRY(run_append_partial(desc, args, &ws, pl, stream));
-    return run_combine(desc, args, &ws, pl, stream);
+    UAA_TRY(run_combine(desc, args, &ws, pl, stream));
+    g_static_scratch_dirty[dev] = false;
+    return UAA_OK;
 }

@@ -611,7 +611,7 @@ __device__ inline void rebalance(const BalanceState& b, int P, int lane)
         for (int i = 0; i < kPerLane; ++i) {
             const int v = v0 + lane + 32 * i;
             if (v >= P) continue;
-            const bool ok = r[i] > 0.f && r[i] < 1e30f;  // a rate this launch measured
+            const bool ok = r[i] > 0.f && r[i] < 1e30f;  // a rate this launch measured (every claimed slot writes one)
             const float nw = ok ? (w[i] > 0.f ? 0.75f * w[i] + 0.25f * r[i] : r[i]) : w[i];
             b.weight[v] = nw;
             b.rate[v] = 0.f;

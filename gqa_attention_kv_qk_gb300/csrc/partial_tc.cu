@@ -648,6 +648,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // producer does so after its first ring fill, off the consumers' path); the
     // last to count in advances seq_lens once its own work is issued.
     if (e_c <= s_c) {  // uniform over the CTA: no stages
+        // a claimed slot always leaves a rate (0: nothing measured), so the combine
+        // never reads bytes of another launch geometry as one
+        if (threadIdx.x == 0 && slot >= 0) p.bal.rate[slot] = 0.f;
         if (threadIdx.x == 0 && p.fused) count_in_and_advance(p, lens);
         return;
     }

@@ -9,6 +9,7 @@ from __future__ import annotations
 import torch
 
 from . import binding as B
+from . import workloads as W
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -78,6 +79,27 @@ class DecodeLayer:
             raise B.UaaError(B.UAA_ERR_UNSUPPORTED, B.last_error())
         self.ws_tensor = torch.zeros((nbytes,), dtype=torch.uint8, device=dev)
         self.ws = B.UaaWorkspace(self.ws_tensor.data_ptr(), nbytes)
+
+    @classmethod
+    def for_case(cls, case: dict, device="cuda") -> "DecodeLayer":
+        """A layer holding a host case of workloads.host_case (a vq8 / q8 cache is
+        quantised on the device); a paged workload gets a pool with spare pages,
+        assigned in seeded random order."""
+        cfg = case["cfg"]
+        ps = int(cfg.get("page_size", 0) or 0)
+        T = int(cfg.get("q_len", 1) or 1)
+        if ps:
+            P = case["cap"] // ps
+            n_pages = cfg["batch"] * P + max(2, cfg["batch"])
+            layer = cls(cfg, cfg["batch"], case["cap"], device, page_size=ps,
+                        block_table=W.block_table(cfg, P, n_pages), n_pages=n_pages, max_q_len=T)
+        else:
+            layer = cls(cfg, cfg["batch"], case["cap"], device, max_q_len=T)
+        k = case["k_values"] if cfg.get("kv_dtype") == "q8" else case["k_cache"]
+        v = case["v_values"] if cfg.get("kv_dtype") in ("vq8", "q8") else case["v_cache"]
+        layer.load_cache(k, v, case["lens"])
+        layer.set_params(case["q_norm_w"], case["k_norm_w"], case["sink"])
+        return layer
 
     # ------------------------------------------------------------ state
     def set_params(self, q_norm_w=None, k_norm_w=None, sink=None):

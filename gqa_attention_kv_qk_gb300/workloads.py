@@ -236,6 +236,21 @@ def cache(cfg: dict, cap: int, lens: torch.Tensor, fill_unused: str = "zero") ->
     return {kkey: k, vkey: v}
 
 
+def host_case(cfg: dict, lens=None, cap=None, step: int = 0, fill_unused: str = "zero") -> dict:
+    """One step's seeded inputs and cache on the host: cfg, lens [B] int32, cap,
+    the cache tensors of cache(), the step inputs of step_inputs(), the norm
+    weights and the sinks. cap defaults to the workload's longest length plus
+    every token its steps append."""
+    lens = seq_lens(cfg) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
+    cap = cap or capacity(cfg, extra=cfg.get("steps", 1) * int(cfg.get("q_len", 1) or 1))
+    case = dict(cfg=cfg, lens=lens.clone(), cap=cap)
+    case.update(cache(cfg, cap, lens, fill_unused=fill_unused))
+    case.update(step_inputs(cfg, step))
+    case.update(norm_weights(cfg))
+    case["sink"] = sinks(cfg)
+    return case
+
+
 # ---------------------------------------------------------------- numpy views
 
 def bits(t: torch.Tensor) -> np.ndarray:

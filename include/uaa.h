@@ -206,7 +206,9 @@ typedef struct {
  * balance state (counters that every completed launch leaves at zero, and the
  * measured slot speeds that carry over to the next launch); it must not be
  * shared by steps that run concurrently. After UAA_DEVFLAG_TIMEOUT zero it
- * again. */
+ * again. A workspace may serve descs of different geometry in turn (different
+ * P = uaa_workspace_layout.n_ctas); the measured slot speeds then start over
+ * at each change of P (uniform ranges for one launch). */
 typedef struct {
     void* ptr;
     size_t bytes;
@@ -333,10 +335,16 @@ int32_t uaa_abi_version(void);
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
  *     first call on a device before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's
- *     contents. Each call clears the status word it starts from; device-side
- *     flags are therefore not reported (a sequence without a free slot is
- *     silently not appended). Calls whose kernels overlap on the GPU (two
- *     streams, or two threads) race on the array: serialise them.
+ *     contents. Each call clears the status word and the arrival counter it
+ *     starts from (and, after a call that returned an error between its
+ *     partial and combine launches, the range-balance state), so one failed
+ *     call leaves nothing that changes the next call's results. Device-side
+ *     flags are therefore neither reported nor clearable by the caller: a
+ *     sequence without a free slot is silently not appended, and a step whose
+ *     bounded wait gave up (UAA_DEVFLAG_TIMEOUT on the workspace entry) goes
+ *     unnoticed. Callers that need the flags use uaa_decode_attn with a
+ *     workspace and uaa_device_status. Calls whose kernels overlap on the GPU
+ *     (two streams, or two threads) race on the array: serialise them.
  * It runs the same kernels as uaa_decode_attn: results equal uaa_decode_attn's
  * for the same desc and args. */
 uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const uaa_step_args* args,

@@ -10,15 +10,7 @@ import torch
 from gqa_attention_kv_qk_gb300 import workloads as W
 
 
-def host_case(cfg: dict, lens=None, cap=None, step: int = 0, fill_unused: str = "zero") -> dict:
-    lens = W.seq_lens(cfg) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
-    cap = cap or W.capacity(cfg, extra=cfg.get("steps", 1) * int(cfg.get("q_len", 1) or 1))
-    case = dict(cfg=cfg, lens=lens.clone(), cap=cap)
-    case.update(W.cache(cfg, cap, lens, fill_unused=fill_unused))
-    case.update(W.step_inputs(cfg, step))
-    case.update(W.norm_weights(cfg))
-    case["sink"] = W.sinks(cfg)
-    return case
+host_case = W.host_case  # seeded inputs and cache (gqa_attention_kv_qk_gb300.workloads)
 
 
 def oracle_arrays(case: dict, oracle_mod) -> dict:
@@ -59,18 +51,4 @@ def run_oracle_step(case: dict, oracle_mod, n_threads=None):
 def gpu_layer(case: dict, device="cuda"):
     """A DecodeLayer holding the case's cache (a vq8 / q8 cache is quantised on the device)."""
     from gqa_attention_kv_qk_gb300.layer import DecodeLayer
-    cfg = case["cfg"]
-    ps = int(cfg.get("page_size", 0) or 0)
-    if ps:  # a pool with spare pages, assigned in seeded random order
-        P = case["cap"] // ps
-        n_pages = cfg["batch"] * P + max(2, cfg["batch"])
-        layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device, page_size=ps,
-                            block_table=W.block_table(cfg, P, n_pages), n_pages=n_pages,
-                            max_q_len=int(cfg.get("q_len", 1) or 1))
-    else:
-        layer = DecodeLayer(cfg, cfg["batch"], case["cap"], device, max_q_len=int(cfg.get("q_len", 1) or 1))
-    k = case["k_values"] if cfg.get("kv_dtype") == "q8" else case["k_cache"]
-    v = case["v_values"] if cfg.get("kv_dtype") in ("vq8", "q8") else case["v_cache"]
-    layer.load_cache(k, v, case["lens"])
-    layer.set_params(case["q_norm_w"], case["k_norm_w"], case["sink"])
-    return layer
+    return DecodeLayer.for_case(case, device)

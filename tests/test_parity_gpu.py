@@ -429,6 +429,71 @@ def test_length_hint_violation_is_flagged_and_results_stay_exact(oracle_mod):
     assert_out_close(layer.out.cpu(), want)
 
 
+def test_partial_repeated_without_combine_sets_timeout(oracle_mod):
+    """The range slots a tensor-core partial launch claims are freed by its
+    combine. A second partial launch before that combine finds every slot taken:
+    each of its CTAs returns at once (no wait runs out, nothing hangs) and
+    UAA_DEVFLAG_TIMEOUT is raised; once the caller zeroes the workspace, the next
+    step matches the oracle again."""
+    cfg = W.config("llama31_8b_decode", batch=3, seq_len=1400, steps=1)
+    case = host_case(cfg, lens=[1000, 1399, 5])
+    layer = gpu_layer(case)
+    assert layer.layout().kernel == 1
+    dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
+    layer.append(dev["q"], dev["k_new"], dev["v_new"])
+    layer.partial()
+    layer.partial()  # the combine of the first launch never ran
+    torch.cuda.synchronize()
+    assert layer.device_status() & B.UAA_DEVFLAG_TIMEOUT
+    layer.ws_tensor.zero_()
+    layer.set_lengths(case["lens"])
+    out = layer.step(dev["q"], dev["k_new"], dev["v_new"]).cpu()
+    want, a = run_oracle_step(case, oracle_mod)
+    assert_out_close(out, want)
+    assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
+    assert layer.device_status() == 0
+
+
+def test_workspace_shared_by_two_geometries(oracle_mod):
+    """One workspace serving two descs of different P in turn (head_dim 128 at two
+    CTAs per SM, then head_dim 256 at one): the second geometry's balance arrays
+    lie over the first's claim words. A launch of the second desc with fewer
+    stages than CTAs leaves the slots without work at weight 0 (nothing
+    measured, so the next launch splits uniformly) instead of reading stale
+    words as rates; both descs match the oracle throughout."""
+    c1 = W.config("llama31_8b_decode", batch=4, seq_len=4000, steps=1)
+    c2 = W.layer_configs(W.config("gemma2_9b_swa", batch=2, seq_len=300, steps=1, layers=[dict(window=0)]))[0]
+    case1, case2 = host_case(c1), host_case(c2, lens=[299, 40])
+    L1, L2 = gpu_layer(case1), gpu_layer(case2)
+    P1, P2 = L1.layout().n_ctas, L2.layout().n_ctas
+    assert P1 != P2 and L1.layout().kernel == 1 and L2.layout().kernel == 1
+    nbytes = max(L1.ws_tensor.numel(), L2.ws_tensor.numel())
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for L in (L1, L2):
+        L.ws_tensor, L.ws = ws, B.UaaWorkspace(ws.data_ptr(), nbytes)
+    d1 = {k: case1[k].cuda() for k in ("q", "k_new", "v_new")}
+    d2 = {k: case2[k].cuda() for k in ("q", "k_new", "v_new")}
+    want1, _ = run_oracle_step(case1, oracle_mod)
+    want2, _ = run_oracle_step(case2, oracle_mod)
+    al = lambda x: -(-x // 256) * 256
+    for rep in range(2):
+        for _ in range(3):
+            L1.set_lengths(case1["lens"])
+            assert_out_close(L1.step(d1["q"], d1["k_new"], d1["v_new"]).cpu(), want1, "head_dim 128")
+        L2.set_lengths(case2["lens"])
+        assert_out_close(L2.step(d2["q"], d2["k_new"], d2["v_new"]).cpu(), want2, "head_dim 256")
+        torch.cuda.synchronize()
+        lay = L2.layout()
+        T2 = int(ws[lay.prefix_offset: lay.prefix_offset + 3 * 4].view(torch.int32)[-1].item())
+        assert 0 < T2 < P2
+        w0 = lay.balance_offset + 256 + al(8 * P2) + al(4 * P2)
+        weight = ws[w0: w0 + 4 * P2].view(torch.float32).cpu().numpy()
+        cumw = ws[w0 + al(4 * P2): w0 + al(4 * P2) + 4 * (P2 + 1)].view(torch.int32).cpu().numpy()
+        assert np.all(weight[T2:] == 0.0), "a slot without work kept a weight"
+        assert np.all(cumw == 0), "a launch with unmeasured slots must split uniformly next"
+        assert L1.device_status() == 0
+
+
 # ------------------------------------------------------------------ split partials
 
 def stream_k_segments(prefix, starts, units, head_groups):
@@ -563,3 +628,63 @@ def test_full_size_sampled(oracle_mod, name):
             vc = layer.logical("v_cache")
             for b in range(Bn):
                 assert np.array_equal(vc[b, :, pre[b]].cpu().numpy(), a["v_cache"][b, :, pre[b]])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama31_8b_decode", "llama31_8b_q8"])
+def test_full_size_64_chained_steps(oracle_mod, name):
+    """The Llama-3.1-8B-like workload as the benchmark runs it: 16 sequences from
+    8192 cached tokens, 64 consecutive decode steps through the whole-step call
+    (fresh q / k / v for every step). Every step's full output against the
+    oracle's; after the last step the lengths, all 64 appended key and value rows
+    of every (sequence, kv head), and the untouched rows below them."""
+    cfg = W.config(name)
+    n = cfg["steps"]
+    assert n == 64
+    case = host_case(cfg)
+    a = oracle_arrays(case, oracle_mod)
+    kv = cfg["kv_dtype"]
+    orig = {k: a[k].copy() for k in ("k_cache", "v_cache")}
+    layer = gpu_layer(case)
+    L0 = case["lens"].numpy().astype(np.int64)
+    assert np.all(L0 == L0[0])
+    L = int(L0[0])
+    hint = L + n - 1
+    for step in range(n):
+        inp = W.step_inputs(cfg, step)
+        out = layer.step(inp["q"].cuda(), inp["k_new"].cuda(), inp["v_new"].cuda(), max_seq_len=hint).cpu()
+        qr = oracle_mod.append(cfg, W.bits(inp["q"]).copy(), W.bits(inp["k_new"]).copy(),
+                               W.bits(inp["v_new"]).copy(), a["q_norm_w"], a["k_norm_w"], a["k_cache"],
+                               a["v_cache"], a["v_scale"], a["seq_lens"], a["k_scale"])
+        want = oracle_mod.attend(cfg, qr, a["sink"], a["k_cache"], a["v_cache"], a["v_scale"], a["seq_lens"],
+                                 k_scale=a["k_scale"])
+        assert_out_close(out, want, f"{name} step {step}")
+        assert np.array_equal(layer.seq_lens.cpu().numpy(), a["seq_lens"])
+    assert layer.device_status() == 0
+    assert np.all(a["seq_lens"] == L + n)
+    new = slice(L, L + n)
+    kg = layer.k_cache[:, :, new].cpu()
+    if kv == "q8":
+        vg = layer.v_cache[:, :, new].cpu().numpy()
+        kcg, kco = kg.numpy().astype(np.int64), a["k_cache"][:, :, new].astype(np.int64)
+        assert np.abs(kcg - kco).max() <= 1, "q8 key code off by more than one"
+        per_row = (kcg != kco).sum(axis=-1)
+        assert per_row.max() <= 2 and (kcg != kco).sum() <= kco.size // 100
+        ksg = layer.k_scale[:, :, new].cpu().numpy().astype(np.float64)
+        assert np.allclose(ksg, a["k_scale"][:, :, new], rtol=2e-6, atol=0)
+        assert np.array_equal(vg, a["v_cache"][:, :, new])
+        assert np.array_equal(layer.v_scale[:, :, new].cpu().numpy().view(np.uint32),
+                              a["v_scale"][:, :, new].view(np.uint32))
+        below = (layer.k_cache[:, :, :L].cpu().numpy(), layer.v_cache[:, :, :L].cpu().numpy())
+    else:
+        kgf = kg.to(torch.float64).numpy()
+        ko = bf16_bits_to_f64(a["k_cache"][:, :, new])
+        row_max = np.abs(ko).max(axis=-1, keepdims=True)
+        assert np.all(np.abs(kgf - ko) <= np.abs(ko) * 2.0 ** -7 + row_max * 2.0 ** -18), \
+            "k rows beyond one bf16 ulp + the fp32 rotation error"
+        assert np.array_equal(layer.v_cache[:, :, new].view(torch.int16).cpu().numpy().view(np.uint16),
+                              a["v_cache"][:, :, new]), "an appended value row differs"
+        below = (layer.k_cache[:, :, :L].view(torch.int16).cpu().numpy().view(np.uint16),
+                 layer.v_cache[:, :, :L].view(torch.int16).cpu().numpy().view(np.uint16))
+    assert np.array_equal(below[0], orig["k_cache"][:, :, :L]), "a cached key row changed"
+    assert np.array_equal(below[1], orig["v_cache"][:, :, :L]), "a cached value row changed"
