@@ -46,7 +46,8 @@ sys.path.insert(0, ROOT)
 from gqa_attention_kv_qk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (% of GB300 peak) and decode steps/sec at 1 GPU"
-DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_paged": 64, "llama31_8b_verify": 16}
+DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_paged": 64, "llama31_8b_verify": 16,
+                    "llama32_1b_tiny": 64}
 HEADLINE = "llama31_8b_decode"
 # the suite's other workloads, reported beside the headline in the same line
 PER_CONFIG = ("llama32_1b_tiny", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink")
@@ -334,6 +335,8 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
     from gqa_attention_kv_qk_gb300 import binding as Bd
     device = f"cuda:{local}"
     cfg = W.config(name, seed=W.CONFIGS[name]["seed"] + 1000 * rank)
+    if args.reproducible:
+        cfg["reproducible"] = True
     step_bytes, part_bytes, n_dec = workload_bytes(name)
     T = int(cfg.get("q_len", 1) or 1)  # tokens per sequence and call
     layers, cases = build_layers(cfg, cap_extra=n_dec * T + 1, device=device)
@@ -356,17 +359,20 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
         for layer, l0 in zip(layers, lens0_dev):
             layer.seq_lens.copy_(l0, non_blocking=True)
 
-    def one_step():  # one benchmark step: n_dec decode steps of every layer, then lengths reset
-        for _ in range(n_dec):
+    def one_step(n=n_dec):  # one benchmark step: n decode steps of every layer, then lengths reset
+        for _ in range(n):
             for li, layer in enumerate(layers):
                 inp = inputs[li]
                 layer.step(inp["q"], inp["k_new"], inp["v_new"], stream=stream, max_seq_len=hint[li])
         reset()
 
     # kernels of one call of a layer: the fused append+partial and the combine
-    # (bf16 / vq8 / q8 caches, one token), or append, partial and combine
-    fused = [layer.layout().kernel == 1 and T == 1 for layer in layers]
-    launches_per_step = n_dec * sum(2 if f else 3 for f in fused)
+    # (bf16 / vq8 / q8 caches, one token), one kernel for a small fp32 step, or
+    # append, partial and combine
+    lays = [layer.layout(max_seq_len=h) for layer, h in zip(layers, hint)]
+    fused = [lay.kernel == 1 and T == 1 for lay in lays]
+    one_launch = [lay.step_splits > 0 for lay in lays]
+    launches_per_step = n_dec * sum(lay.step_kernels for lay in lays)
 
     with torch.cuda.stream(stream):
         # warm-up, then capture one benchmark step in a graph
@@ -400,10 +406,15 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
             if st:
                 raise RuntimeError(f"device flags 0x{st:x} after the timed region")
 
-        # ---- cold: the same K steps, each after a write of 1.5x L2 (untimed), so
-        # the step finds none of its cache in L2
+        # ---- cold: K single decode steps (a graph of one step and the length reset),
+        # each after a write of 1.5x L2 (untimed, and long enough that the host has
+        # queued the step before the GPU reaches it), so the step finds none of its
+        # cache in L2
         cold_s = None
         if fits_l2:
+            graph1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph1, stream=stream):
+                one_step(1)
             flush = torch.empty(3 * L2_BYTES // 2, dtype=torch.uint8, device=device)
             ce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
@@ -412,18 +423,20 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
             for e0, e1 in ce:
                 flush.fill_(1)
                 e0.record(stream)
-                graph.replay()
+                graph1.replay()
                 e1.record(stream)
             stream.synchronize()
             barrier(world)
             cold_s = sum(e0.elapsed_time(e1) for e0, e1 in ce) / 1e3
-            del flush
+            del flush, graph1
 
         # ---- the partial kernel alone (events on the launching stream): the fused
         # append+partial kernel of the step for bf16 / vq8 caches, the partial
-        # kernel after its separate append for fp32 caches
+        # kernel after its separate append for fp32 caches; a step that is one
+        # kernel takes the timed region's per-step time (events around single
+        # launches of a few microseconds would time the host's launch instead)
         pe = []
-        rounds = -(-20 // n_dec)  # at least 20 launches per layer
+        rounds = 0 if all(one_launch) else -(-20 // n_dec)  # at least 20 launches per layer
         for _ in range(rounds):
             reset()
             for _ in range(n_dec):
@@ -431,6 +444,12 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
                     inp = inputs[li]
                     args_ = layer.args(inp["q"], inp["k_new"], inp["v_new"], max_seq_len=hint[li])
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    if one_launch[li]:  # the whole step is the one kernel
+                        e0.record(stream)
+                        Bd.uaa_decode_attn(layer.desc, args_, layer.ws, stream)
+                        e1.record(stream)
+                        pe.append((e0, e1))
+                        continue
                     if fused[li]:
                         e0.record(stream)
                         Bd.uaa_decode_attn_append_partial(layer.desc, args_, layer.ws, stream)
@@ -533,6 +552,8 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
     value = total_bytes / dev_s / 1e9
     # part_bytes covers one benchmark step (n_dec launches per layer); the timing covers all rounds
     n_layers = len(cases)
+    if all(one_launch):  # the timed region: one kernel per layer and decode step (and a length reset per 64)
+        part_s, n_part = dev_s, args.steps * n_dec * n_layers
     part_gbs = (part_bytes / (n_dec * n_layers)) / (part_s / n_part) / 1e9 if n_part else None
     decodes = n_dec * args.steps * world
     rec = {
@@ -551,7 +572,9 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
                      "frac": round(part_gbs / peaks["hbm_gbs"], 4) if part_gbs else None,
                      "traffic": measured_traffic(name),
                      "frac_of_nominal": round(part_gbs / NOMINAL_HBM_GBS, 4) if part_gbs else None,
-                     "kernel": "fused append + split-K partial" if all(fused) else "split-K partial",
+                     "kernel": ("fused append + split-K partial" if all(fused) else
+                                "fp32 one-launch step (append, attention, merge)" if all(one_launch) else
+                                "split-K partial"),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": part_bytes // max(1, n_dec * n_layers),
                      "mean_launch_us": round(part_s / n_part * 1e6, 2) if n_part else None},
@@ -562,11 +585,15 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
         "cpu_baseline": cpu_baseline(name, cases, cpu_budget) if with_cpu else None,
     }
     if cold_s is not None:
-        rec["cold"] = {"value": round(total_bytes / cold_s / 1e9, 2), "unit": "GB/s",
-                       "ms_per_step": round(cold_s / args.steps * 1e3, 4),
-                       "decode_steps_per_s": round(decodes / cold_s / world, 2),
-                       "l2": "flushed before each step by a %d MB write (not timed)" % (3 * L2_BYTES // 2**20)}
-        rec["warm_note"] = "steps replayed back to back: the cache stays in L2 between steps"
+        first = sum(decode_step_bytes(lc, [int(x) for x in l0]) for lc, l0 in zip(W.layer_configs(cfg), lens0))
+        rec["cold"] = {"value": round(first * args.steps / cold_s / 1e9, 2), "unit": "GB/s",
+                       "us_per_decode_step": round(cold_s / args.steps * 1e6, 3),
+                       "decode_steps_per_s": round(args.steps / cold_s, 2),
+                       "l2": "one decode step per graph replay, L2 flushed before each by a %d MB write (not timed)"
+                             % (3 * L2_BYTES // 2**20)}
+        rec["warm_note"] = ("%d decode steps per graph replay, back to back: the cache stays in L2 between steps"
+                            % n_dec)
+        rec["us_per_decode_step"] = round(dev_s / (args.steps * n_dec) * 1e6, 3)
     return rec
 
 
@@ -646,6 +673,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure the headline workload only (not the suite's other four)")
+    ap.add_argument("--reproducible", action="store_true",
+                    help="uniform stream-K ranges (equal bits on every launch) instead of speed-weighted ones")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "uaa":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

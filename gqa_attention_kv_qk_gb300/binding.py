@@ -43,7 +43,7 @@ class UaaAttnDesc(ctypes.Structure):
                 ("softcap", ctypes.c_float), ("has_sink", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
-                ("norm_offset", ctypes.c_int32)]
+                ("norm_offset", ctypes.c_int32), ("reproducible", ctypes.c_int32)]
 
 
 class UaaStepArgs(ctypes.Structure):
@@ -66,6 +66,7 @@ class UaaWorkspaceLayout(ctypes.Structure):
     _fields_ = [("n_ctas", ctypes.c_int32), ("stage_keys", ctypes.c_int32),
                 ("heads_per_cta", ctypes.c_int32), ("kernel", ctypes.c_int32),
                 ("n_slices", ctypes.c_int32), ("slice_batch", ctypes.c_int32),
+                ("step_kernels", ctypes.c_int32), ("step_splits", ctypes.c_int32),
                 ("status_offset", ctypes.c_size_t), ("q_rot_offset", ctypes.c_size_t),
                 ("prefix_offset", ctypes.c_size_t), ("rec_lse_offset", ctypes.c_size_t),
                 ("rec_o_offset", ctypes.c_size_t), ("prefix_stride", ctypes.c_size_t),
@@ -254,6 +255,7 @@ def make_desc(cfg: dict) -> UaaAttnDesc:
     d.out_dtype = DTYPE[cfg.get("out_dtype", "f32")]
     d.rotary_dim = int(cfg.get("rotary_dim", 0) or 0)
     d.norm_offset = int(bool(cfg.get("norm_offset", False)))
+    d.reproducible = int(bool(cfg.get("reproducible", False)))
     return d
 
 

@@ -83,6 +83,8 @@ uaa_status check_desc(const uaa_attn_desc* d)
                     d->rotary_dim, d->head_dim);
     if (d->norm_offset != 0 && d->norm_offset != 1)
         return fail(UAA_ERR_UNSUPPORTED, "norm_offset=%d is not 0 or 1", d->norm_offset);
+    if (d->reproducible != 0 && d->reproducible != 1)
+        return fail(UAA_ERR_UNSUPPORTED, "reproducible=%d is not 0 or 1", d->reproducible);
     if (d->qk_norm != 0 && d->qk_norm != 1)
         return fail(UAA_ERR_UNSUPPORTED, "qk_norm=%d is not 0 or 1", d->qk_norm);
     if (d->qk_norm && (!(d->norm_eps >= 0.f) || !isfinite(d->norm_eps)))
@@ -527,6 +529,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
             p.bal = balance_of(w, pl);
             p.slice = sl;
             p.per_sm = pl.per_sm;
+            p.uniform = d->reproducible;
         }
         p.rec_lse = reinterpret_cast<float*>(w + pl.off_rec_lse + sl * pl.rec_lse_stride);
         p.rec_o = reinterpret_cast<float*>(w + pl.off_rec_o + sl * pl.rec_o_stride);
@@ -603,6 +606,74 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     return UAA_OK;
 }
 
+// The whole step: the fp32 one-launch kernel where it applies, else steps 1 and
+// 2 (fused for the tensor-core kernel) and the combine.
+uaa_status run_step(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                    cudaStream_t s);
+
+// Keys per split of the fp32 one-launch step.
+constexpr int kF32SplitKeys = 512;
+
+// Splits per unit of the fp32 one-launch step (step_f32.cu), or 0 when the step
+// takes the three-kernel path: it serves fp32 caches with one token per
+// sequence in a single batch slice whose split records fit the slice's 2P.
+int f32_step_splits(const uaa_attn_desc* d, const uaa_step_args* a, const Plan& pl)
+{
+    if (pl.kernel != 0 || pl.q_len != 1 || pl.n_slices != 1) return 0;
+    const long long S = ((long long)a->max_seq_len + kF32SplitKeys) / kF32SplitKeys;  // keys: max_seq_len + 1
+    const long long recs = (long long)a->batch * d->n_kv_heads * pl.head_groups * S;
+    if (S > 1 && recs > 2LL * pl.n_ctas) return 0;
+    return (int)S;
+}
+
+uaa_status run_step_f32(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                        int splits, cudaStream_t s)
+{
+    if (a->batch == 0) return UAA_OK;
+    char* w = static_cast<char*>(ws->ptr);
+    uaa::StepF32Params p{};
+    p.B = a->batch;
+    p.Hq = d->n_q_heads;
+    p.Hkv = d->n_kv_heads;
+    p.D = d->head_dim;
+    p.G = pl.G;
+    p.head_groups = pl.head_groups;
+    p.cap = a->cache_capacity;
+    p.max_len = a->max_seq_len;
+    p.window = d->window;
+    p.splits = splits;
+    p.split_keys = kF32SplitKeys;
+    p.style = d->rope.style;
+    p.half_rot = rotary_dims(d) / 2;
+    p.qk_norm = d->qk_norm;
+    p.eps = d->norm_eps;
+    p.norm_offset = d->norm_offset ? 1.f : 0.f;
+    p.qscale = qscale(d);
+    p.softcap_log2e = d->softcap > 0.f ? d->softcap * uaa::kLog2e : 0.f;
+    p.io_dtype = d->io_dtype;
+    p.out_dtype = d->out_dtype;
+    p.q = a->q;
+    p.k_new = a->k_new;
+    p.v_new = a->v_new;
+    p.q_norm_w = a->q_norm_w;
+    p.k_norm_w = a->k_norm_w;
+    p.sink = d->has_sink ? a->sink : nullptr;
+    p.k_cache = static_cast<float*>(a->k_cache);
+    p.v_cache = static_cast<float*>(a->v_cache);
+    p.pages = pages_of(a);
+    p.seq_lens = a->seq_lens;
+    p.out = a->out;
+    p.q_rot_out = a->q_rot;
+    p.rec_o = reinterpret_cast<float*>(w + pl.off_rec_o);
+    p.rec_lse = reinterpret_cast<float*>(w + pl.off_rec_lse);
+    p.unit_count = reinterpret_cast<unsigned*>(w + pl.off_owners);
+    p.arrivals = reinterpret_cast<unsigned*>(w + pl.off_status) + 1;
+    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+    rope_table(d, p.inv_freq_over_pi, &p.mscale);
+    const cudaError_t e = uaa::launch_step_f32(p, s);
+    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "fp32 step kernel launch");
+}
+
 // Steps 1 and 2: one fused launch for the tensor-core kernel, append then
 // partial for the fp32 kernel.
 uaa_status run_append_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws,
@@ -614,6 +685,15 @@ uaa_status run_append_partial(const uaa_attn_desc* d, const uaa_step_args* a, co
     if (pl.kernel == 1 && pl.q_len == 1) return run_partial(d, a, ws, pl, s, true);
     UAA_TRY(run_append(d, a, ws, pl, s));
     return run_partial(d, a, ws, pl, s);
+}
+
+uaa_status run_step(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                    cudaStream_t s)
+{
+    const int splits = f32_step_splits(d, a, pl);
+    if (splits > 0) return run_step_f32(d, a, ws, pl, splits, s);
+    UAA_TRY(run_append_partial(d, a, ws, pl, s));
+    return run_combine(d, a, ws, pl, s);
 }
 
 }  // namespace
@@ -659,8 +739,7 @@ uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
 {
     Plan pl{};
     UAA_TRY(prepare(desc, args, ws, true, &pl));
-    UAA_TRY(run_append_partial(desc, args, ws, pl, stream));
-    return run_combine(desc, args, ws, pl, stream);
+    return run_step(desc, args, ws, pl, stream);
 }
 
 size_t uaa_workspace_size(const uaa_attn_desc* desc, int32_t batch, int32_t max_seq_len, int32_t n_sm,
@@ -693,6 +772,16 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, in
     layout->kernel = pl.kernel;
     layout->n_slices = pl.n_slices;
     layout->slice_batch = pl.slice;
+    {
+        uaa_step_args a{};
+        a.batch = batch;
+        a.max_seq_len = max_seq_len;
+        layout->step_splits = f32_step_splits(desc, &a, pl);
+        layout->step_kernels = batch == 0 ? 0
+                               : layout->step_splits > 0 ? 1
+                               : (pl.kernel == 1 && pl.q_len == 1) ? 2 * pl.n_slices
+                                                                   : 1 + 2 * pl.n_slices;
+    }
     layout->status_offset = pl.off_status;
     layout->q_rot_offset = pl.off_qrot;
     layout->prefix_offset = pl.off_prefix;
@@ -826,8 +915,7 @@ extern "C" uaa_status uaa_decode_attn_static(const uaa_attn_desc* desc, const ua
     e = cudaMemsetAsync(static_cast<char*>(scratch) + pl.off_status, 0, clear, stream);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch state");
     g_static_scratch_dirty[dev] = true;
-    UAA_TRY(run_append_partial(desc, args, &ws, pl, stream));
-    UAA_TRY(run_combine(desc, args, &ws, pl, stream));
+    UAA_TRY(run_step(desc, args, &ws, pl, stream));
     g_static_scratch_dirty[dev] = false;
     return UAA_OK;
 }

@@ -132,6 +132,7 @@ struct PartialParams {
     // balance state (tensor-core kernel; null: uniform ranges)
     BalanceState bal;
     int slice;              // index of this launch's batch slice (part of the claim tag)
+    int uniform;            // uniform ranges whatever the slot weights (reproducible results)
     int per_sm;             // CTAs per SM of the launch
     float* rec_o;           // [2P][heads_per_cta][D]
     float* rec_lse;         // [2P][heads_per_cta]
@@ -177,6 +178,40 @@ struct CombineParams {
     unsigned* status;
 };
 
+// The whole decode step in one launch for fp32 caches and one token per
+// sequence (step_f32.cu): a CTA per (sequence, kv head, group of up to 8 query
+// heads, key split).
+struct StepF32Params {
+    int B, Hq, Hkv, D, G;
+    int head_groups;        // ceil(G / 8)
+    int cap, max_len;
+    int window;             // the descriptor's window (0: none)
+    int splits;             // key splits per unit: each split_keys keys, the last takes the rest
+    int split_keys;
+    int style, half_rot, qk_norm;
+    float eps, norm_offset, qscale, mscale;
+    float softcap_log2e;    // 0: no softcap
+    int io_dtype, out_dtype;
+    const void* q;          // [B][Hq][D] io_dtype
+    const void* k_new;      // [B][Hkv][D]
+    const void* v_new;
+    const float* q_norm_w;
+    const float* k_norm_w;
+    const float* sink;      // [Hq] or null
+    float* k_cache;
+    float* v_cache;
+    KvPages pages;
+    int* seq_lens;
+    void* out;              // [B][Hq][D]
+    float* q_rot_out;       // optional [B][Hq][D]
+    float* rec_o;           // [B][units][splits][8][D] (splits > 1)
+    float* rec_lse;         // [B][units][splits][8]
+    unsigned* unit_count;   // [B][units][2]: word 0 counts a unit's finished splits (zero between launches)
+    unsigned* arrivals;     // grid arrival counter (zero between launches)
+    unsigned* status;
+    double inv_freq_over_pi[kMaxHeadDim / 2];
+};
+
 // ---------------------------------------------------------------- launches
 // Each returns the launch error (cudaGetLastError) of its kernel.
 
@@ -186,6 +221,7 @@ cudaError_t launch_partial_tc(const PartialParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_s, const CUtensorMap& tm_ks,
                               int kv_dtype, int n_head_tiles, int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_step_f32(const StepF32Params& p, cudaStream_t s);
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
                                 float* scales, cudaStream_t s);
 
@@ -230,8 +266,9 @@ __device__ __forceinline__ void grid_dependency_wait()
 // Lets the next kernel on the stream (launched with launch_dependent) be
 // scheduled before this one completes: its CTAs take SMs as this grid's tail
 // frees them and do their set-up; its grid_dependency_wait still waits for this
-// grid to complete. Only the combine uses it: triggered from the partial kernel
-// it cost 3 % (combine CTAs parked on SMs the partial kernel's tail still used).
+// grid to complete. The combine and the fp32 one-launch step (a few CTAs) use
+// it: triggered from the partial kernel it cost 3 % (combine CTAs parked on SMs
+// the partial kernel's tail still used).
 __device__ __forceinline__ void allow_dependent_launch()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -566,9 +603,9 @@ __device__ inline int claim_slot(const PartialParams& p, unsigned& w0, unsigned&
 
 // The range [s, e) of slot v when the launch holds T stages (empty: no work),
 // writing start[v] (and start[P'] = T from the last range) for the combine.
-// Weighted when every slot has a weight (wP > 0) and T >= P: one stage each,
-// the other T - P shared in proportion to the weights; otherwise uniform over
-// P' = min(P, T).
+// Weighted when every slot has a weight (wP > 0), T >= P and the launch does
+// not ask for reproducible results: one stage each, the other T - P shared in
+// proportion to the weights; otherwise uniform over P' = min(P, T).
 __device__ inline void slot_range(const PartialParams& p, int v, unsigned w0, unsigned w1, unsigned wP, long long T,
                                   long long& s, long long& e)
 {
@@ -576,7 +613,7 @@ __device__ inline void slot_range(const PartialParams& p, int v, unsigned w0, un
     const int Pp = T < P ? static_cast<int>(T) : P;
     s = e = 0;
     if (v < 0 || v >= Pp) return;
-    if (T >= P && wP > 0) {
+    if (T >= P && wP > 0 && !p.uniform) {
         const long long extra = T - P;
         s = v + extra * w0 / wP;
         e = v + 1 + extra * w1 / wP;

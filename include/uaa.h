@@ -15,7 +15,8 @@
  *      partition). The tensor-core kernel
  *      sizes the ranges by the speed each CTA slot measured in the previous
  *      launches on the same workspace (the SMs of a GB300 do not all stream
- *      equally fast), so results may differ in rounding from launch to launch.
+ *      equally fast), so results may differ in rounding from launch to launch;
+ *      a desc with reproducible = 1 keeps the ranges uniform instead.
  *      A unit that lies inside one range is finished there and its output rows
  *      written; every other unit leaves one record (normalised output rows and
  *      log-sum-exp) per range it touches in the workspace.
@@ -76,7 +77,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 9
+#define UAA_ABI_VERSION 10
 
 typedef enum {
     UAA_OK = 0,
@@ -158,6 +159,9 @@ typedef struct {
     int32_t rotary_dim;       /* rotated dims per head: 0 (all D), or even, 2 <= R <= D */
     int32_t norm_offset;      /* 1: the QK RMSNorm weight applies as (1 + w) (Gemma's
                                  stored delta, decoder-completeness page P1.1); else 0 */
+    int32_t reproducible;     /* 1: the tensor-core partial step splits its ranges uniformly
+                                 instead of by the slot speeds measured in earlier launches,
+                                 so equal inputs give equal bits on every launch; else 0 */
 } uaa_attn_desc;
 
 typedef struct {
@@ -223,6 +227,10 @@ typedef struct {
     int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
     int32_t n_slices;         /* partial + combine launches (batch slices) */
     int32_t slice_batch;      /* sequences per slice (the last may hold fewer) */
+    int32_t step_kernels;     /* kernels one uaa_decode_attn call launches */
+    int32_t step_splits;      /* key splits per unit of the fp32 one-launch step, 0 when the
+                                 step does not take it (tensor-core caches, chunks, records
+                                 beyond 2P, several slices) */
     size_t status_offset;     /* uint32 device flags */
     size_t q_rot_offset;      /* fp32 [B][Hq][D]: rotated q times the kernel's logit prescale */
     size_t prefix_offset;     /* int32 [n_slices][slice_batch + 1]: units x stages, prefix over
@@ -273,7 +281,13 @@ uaa_status uaa_decode_attn_append_partial(const uaa_attn_desc* desc, const uaa_s
                                           const uaa_workspace* ws, cudaStream_t stream);
 
 /* Steps 1-3 on one stream: the whole decode step of one layer
- * (uaa_decode_attn_append_partial, then uaa_decode_attn_combine). */
+ * (uaa_decode_attn_append_partial, then uaa_decode_attn_combine). An fp32 cache
+ * with one token per sequence, a batch of one slice and at most 2P split
+ * records (uaa_workspace_layout.step_splits > 0) takes one kernel instead: a
+ * CTA per (sequence, kv head, group of up to 8 query heads, split of 512 keys)
+ * appends, attends its keys and writes a record, and the last split of each
+ * unit to finish merges them (sink included) into the output rows; the results
+ * equal those of the three steps up to fp32 rounding order. */
 uaa_status uaa_decode_attn(const uaa_attn_desc* desc, const uaa_step_args* args,
                            const uaa_workspace* ws, cudaStream_t stream);
 

@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 9
+    assert B.uaa_abi_version() == 10
 
 
 def good_desc(**kw):
@@ -92,6 +92,10 @@ def test_enum_refusals(L):
     d.norm_offset = 2
     assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
     assert "norm_offset=2" in B.last_error()
+    d = good_desc()
+    d.reproducible = 3
+    assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
+    assert "reproducible=3" in B.last_error()
     d = good_desc()
     d.rope.scaling = 9
     assert B.uaa_decode_attn(d, fake_args(), WS, None, check=False) == B.UAA_ERR_UNSUPPORTED
@@ -268,7 +272,8 @@ def test_struct_sizes_match_the_header(L, tmp_path):
         'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(uaa_attn_desc), sizeof(uaa_step_args),'
         ' sizeof(uaa_workspace), sizeof(uaa_workspace_layout), offsetof(uaa_attn_desc, out_dtype),'
         ' offsetof(uaa_attn_desc, norm_offset),'
-        ' offsetof(uaa_step_args, q_rot), offsetof(uaa_workspace_layout, total_bytes)); return 0;}\n')
+        ' offsetof(uaa_step_args, q_rot), offsetof(uaa_workspace_layout, total_bytes));'
+        ' printf("%zu\\n", offsetof(uaa_attn_desc, reproducible)); return 0;}\n')
     exe = tmp_path / "probe"
     r = subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src),
                         "-o", str(exe)], capture_output=True, text=True)
@@ -278,5 +283,5 @@ def test_struct_sizes_match_the_header(L, tmp_path):
     want = [ctypes.sizeof(B.UaaAttnDesc), ctypes.sizeof(B.UaaStepArgs), ctypes.sizeof(B.UaaWorkspace),
             ctypes.sizeof(B.UaaWorkspaceLayout), B.UaaAttnDesc.out_dtype.offset, B.UaaAttnDesc.norm_offset.offset,
             B.UaaStepArgs.q_rot.offset,
-            B.UaaWorkspaceLayout.total_bytes.offset]
+            B.UaaWorkspaceLayout.total_bytes.offset, B.UaaAttnDesc.reproducible.offset]
     assert got == want

@@ -494,6 +494,53 @@ def test_workspace_shared_by_two_geometries(oracle_mod):
         assert L1.device_status() == 0
 
 
+@pytest.mark.parametrize("name,over", [("llama31_8b_decode", dict(batch=4, seq_len=4000)),
+                                       ("gptoss_vq8_sink", dict(batch=4, seq_len=3000)),
+                                       ("llama31_8b_q8", dict(batch=3, seq_len=3000))])
+def test_reproducible_desc_gives_equal_bits(oracle_mod, name, over):
+    """With reproducible = 1 the tensor-core kernel keeps its ranges uniform
+    whatever the slot speeds measured before: the same step repeated on the same
+    inputs gives the same bits on every launch, and matches the oracle."""
+    cfg = W.config(name, reproducible=True, steps=1, **over)
+    case = host_case(cfg)
+    layer = gpu_layer(case)
+    assert layer.layout().kernel == 1
+    dev = {k: case[k].cuda() for k in ("q", "k_new", "v_new")}
+    outs = []
+    for _ in range(5):
+        layer.set_lengths(case["lens"])
+        outs.append(layer.step(dev["q"], dev["k_new"], dev["v_new"], advance_hint=False).clone())
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    want, a = run_oracle_step(case, oracle_mod)
+    assert_out_close(outs[0].cpu(), want)
+    lay = layer.layout()
+    ws = layer.ws_tensor
+    Bn, P = cfg["batch"], lay.n_ctas
+    T = int(ws[lay.prefix_offset: lay.prefix_offset + (Bn + 1) * 4].view(torch.int32)[-1].item())
+    n = min(P, T)
+    starts = ws[lay.ranges_offset: lay.ranges_offset + (n + 1) * 8].view(torch.int64).cpu().numpy()
+    assert np.array_equal(starts, [c * T // n for c in range(n + 1)])
+    assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("over,lens", [
+    (dict(batch=3, seq_len=1500), [1499, 600, 0]),
+    (dict(batch=2, seq_len=1100, window=700, softcap=30.0, has_sink=True, qk_norm=True,
+          norm_w_range=(0.5, 1.5)), [1099, 1]),
+    (dict(batch=2, seq_len=1100, n_q_heads=40, n_kv_heads=4, page_size=64), [1099, 513]),
+])
+def test_fp32_step_in_one_kernel(oracle_mod, over, lens):
+    """The fp32 decode step in one launch with several key splits per unit, merged
+    by the split that finishes last (with window, softcap, sink and QK norm; ten
+    query heads per kv head, two head groups; paged), over two chained steps."""
+    cfg = W.config("llama32_1b_tiny", steps=2, **over)
+    lay = B.uaa_get_workspace_layout(B.make_desc(cfg), cfg["batch"], max(lens) + 1, 0)
+    assert lay.step_kernels == 1 and lay.step_splits >= 2
+    run_and_compare(oracle_mod, cfg, lens, steps=2, entry="fused")
+
+
 # ------------------------------------------------------------------ split partials
 
 def stream_k_segments(prefix, starts, units, head_groups):
