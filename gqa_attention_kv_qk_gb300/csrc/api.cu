@@ -457,10 +457,11 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     char* w = static_cast<char*>(ws->ptr);
     const size_t D = d->head_dim, Hq = d->n_q_heads;
     const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
-    CUtensorMap tk, tv, ts, tks;
+    uaa::PartialMaps maps{};
     if (pl.kernel == 1) {
-        // contiguous caches: one box of a whole stage per row kind; paged caches: the
-        // pools, and one box per page-aligned sub-tile of min(64, page_size) keys
+        // contiguous caches: one box of a whole stage per row kind (and a second set of
+        // 64-key boxes for units' partial last stages); paged caches: the pools, and one
+        // box per page-aligned sub-tile of min(64, page_size) keys
         const bool paged = a->block_table != nullptr;
         const uint64_t rows = paged ? (uint64_t)a->n_pages * d->n_kv_heads * a->page_size
                                     : (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
@@ -469,31 +470,44 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
                   : (uint32_t)uaa::partial_tc_keys_per_stage(d->head_dim, d->kv_dtype, pl.n_head_tiles);  // box height
         const uint64_t heads = paged ? (uint64_t)a->n_pages * d->n_kv_heads : (uint64_t)a->batch * d->n_kv_heads;
         const uint64_t scale_inner = paged ? (uint64_t)a->page_size : (uint64_t)a->cache_capacity;
-        // int8 codes: boxes of tk_rows x min(D, 128) bytes, swizzled like the bf16 boxes so
+        // int8 codes: boxes of box_rows x min(D, 128) bytes, swizzled like the bf16 boxes so
         // the kernel's ldmatrix reads on them are free of bank conflicts; scales: one
-        // tk_rows-float box per stage
+        // box_rows-float box per stage
         const uint32_t code_box = D > 128 ? 128u : (uint32_t)D;
         const CUtensorMapSwizzle code_sw = D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-        if (d->kv_dtype == UAA_DTYPE_Q8) {
-            UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->k_cache, D, rows, D, code_box, tk_rows, code_sw,
-                              "k_cache codes"));
-            UAA_TRY(encode_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->k_scale, scale_inner, heads, scale_inner * 4,
-                              tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "k_scale"));
-        } else {
-            UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, tk_rows,
-                              CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
+        auto encode_set = [&](uint32_t box_rows, CUtensorMap& tk, CUtensorMap& tv, CUtensorMap& ts,
+                              CUtensorMap& tks) -> uaa_status {
+            if (d->kv_dtype == UAA_DTYPE_Q8) {
+                UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->k_cache, D, rows, D, code_box, box_rows,
+                                  code_sw, "k_cache codes"));
+                UAA_TRY(encode_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->k_scale, scale_inner, heads,
+                                  scale_inner * 4, box_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "k_scale"));
+            } else {
+                UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64, box_rows,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
+            }
+            if (d->kv_dtype == UAA_DTYPE_VQ8 || d->kv_dtype == UAA_DTYPE_Q8) {
+                UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, code_box, box_rows,
+                                  code_sw, "v_cache codes"));
+                UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, scale_inner, heads,
+                                  scale_inner * 4, box_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
+            } else {
+                UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, box_rows,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
+                ts = tv;  // unused by the bf16 kernel
+            }
+            if (d->kv_dtype != UAA_DTYPE_Q8) tks = ts;  // unused without key codes
+            return UAA_OK;
+        };
+        UAA_TRY(encode_set(tk_rows, maps.k, maps.v, maps.s, maps.ks));
+        if (!paged && tk_rows > (uint32_t)uaa::kTileKeys) {
+            UAA_TRY(encode_set((uint32_t)uaa::kTileKeys, maps.kt, maps.vt, maps.st, maps.kst));
+        } else {  // never used: every stage is one 64-key tile, or the pool boxes are sub-tiles already
+            maps.kt = maps.k;
+            maps.vt = maps.v;
+            maps.st = maps.s;
+            maps.kst = maps.ks;
         }
-        if (d->kv_dtype == UAA_DTYPE_VQ8 || d->kv_dtype == UAA_DTYPE_Q8) {
-            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->v_cache, D, rows, D, code_box, tk_rows, code_sw,
-                              "v_cache codes"));
-            UAA_TRY(encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->v_scale, scale_inner, heads, scale_inner * 4,
-                              tk_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE, "v_scale"));
-        } else {
-            UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64, tk_rows,
-                              CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
-            ts = tv;  // unused by the bf16 kernel
-        }
-        if (d->kv_dtype != UAA_DTYPE_Q8) tks = ts;  // unused without key codes
     }
     for (int sl = 0; sl < pl.n_slices; ++sl) {
         const int b0 = sl * pl.slice;
@@ -561,7 +575,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
         }
         const cudaError_t e = pl.kernel == 0
                                   ? uaa::launch_partial_simt(p, pl.n_ctas, s)
-                                  : uaa::launch_partial_tc(p, tk, tv, ts, tks, d->kv_dtype, pl.n_head_tiles, pl.n_ctas, s);
+                                  : uaa::launch_partial_tc(p, maps, d->kv_dtype, pl.n_head_tiles, pl.n_ctas, s);
         if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
     }
     return UAA_OK;

@@ -217,9 +217,16 @@ struct StepF32Params {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_partial_simt(const PartialParams& p, int n_ctas, cudaStream_t s);
-cudaError_t launch_partial_tc(const PartialParams& p, const CUtensorMap& tm_k,
-                              const CUtensorMap& tm_v, const CUtensorMap& tm_s, const CUtensorMap& tm_ks,
-                              int kv_dtype, int n_head_tiles, int n_ctas, cudaStream_t s);
+// Tensor maps of the tensor-core partial kernel: keys, values, value scales and
+// key scales with boxes of a whole ring stage (or, for paged pools, of a page
+// sub-tile), and the same with boxes of one 64-key tile (contiguous caches,
+// for units' last stages that need fewer tiles than a stage holds).
+struct PartialMaps {
+    CUtensorMap k, v, s, ks;
+    CUtensorMap kt, vt, st, kst;
+};
+cudaError_t launch_partial_tc(const PartialParams& p, const PartialMaps& m, int kv_dtype, int n_head_tiles,
+                              int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_step_f32(const StepF32Params& p, cudaStream_t s);
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,

@@ -557,6 +557,8 @@ template <int D, int KV, int NHT>
 __global__ void __launch_bounds__(cta_threads(NHT), (D == 256 || NHT == 2 ? 1 : 2))
 partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_ks,
+                  const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+                  const __grid_constant__ CUtensorMap tm_st, const __grid_constant__ CUtensorMap tm_kst,
                   const PartialParams p)
 {
     using SH = Shape<D, KV, NHT>;
@@ -614,6 +616,12 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         ptx::prefetch_tensormap(&tm_v);
         if (VQ8) ptx::prefetch_tensormap(&tm_s);
         if (KQ8) ptx::prefetch_tensormap(&tm_ks);
+        if (MG > 1 && !p.pages.table) {  // the 64-key maps of units' partial last stages
+            ptx::prefetch_tensormap(&tm_kt);
+            ptx::prefetch_tensormap(&tm_vt);
+            if (VQ8) ptx::prefetch_tensormap(&tm_st);
+            if (KQ8) ptx::prefetch_tensormap(&tm_kst);
+        }
     }
     grid_dependency_wait();  // the step's inputs (and a separate append's rows) are complete
     if (p.fused && threadIdx.x >= 32 && threadIdx.x < 32 + D / 2)  // the rotation table, while warp 0 scans
@@ -689,12 +697,21 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     }
                     const uint32_t st = base + s * SH::kStageBytes;
                     const uint32_t bar = bar_full + 8 * s;
-                    ptx::mbar_arrive_expect_tx(bar, SH::kTxBytes);
                     const int key = (t0 + MG * (sg.st0 + k)) * kTileKeys;
-                    if (!p.pages.table) {
+                    // 64-key tiles of this stage up to the unit's last visible key: a unit's
+                    // last stage may need fewer than MG (its other rows are masked)
+                    const int nt = MG > 1 ? min(MG, (sg.hi - key + kTileKeys - 1) / kTileKeys) : MG;
+                    if (!p.pages.table && nt < MG) {
+                        ptx::mbar_arrive_expect_tx(bar, nt * (SH::kTxBytes / MG));
+                        for (int r0 = 0; r0 < nt * kTileKeys; r0 += kTileKeys)
+                            issue_rows<SH>(st, r0, &tm_kt, &tm_vt, &tm_st, &tm_kst, row0 + key + r0, key + r0,
+                                           head_row, bar, stream_policy);
+                    } else if (!p.pages.table) {
+                        ptx::mbar_arrive_expect_tx(bar, SH::kTxBytes);
                         issue_rows<SH>(st, 0, &tm_k, &tm_v, &tm_s, &tm_ks, row0 + key, key, head_row, bar,
                                        stream_policy);
                     } else {
+                        ptx::mbar_arrive_expect_tx(bar, SH::kTxBytes);
                         // paged: one load per page-aligned sub-tile; a sub-tile with no visible key
                         // (beyond the unit's end or before its window) is not looked up and reads
                         // as zeros from a negative row (masked by the consumers)
@@ -1205,8 +1222,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 }
 
 template <int D, int KV, int NHT>
-cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ts,
-                       const CUtensorMap& tks, int n_ctas, cudaStream_t s)
+cudaError_t launch_one(const PartialParams& p, const PartialMaps& m, int n_ctas, cudaStream_t s)
 {
     using SH = Shape<D, KV, NHT>;
     auto kern = partial_tc_kernel<D, KV, NHT>;
@@ -1219,7 +1235,8 @@ cudaError_t launch_one(const PartialParams& p, const CUtensorMap& tk, const CUte
         if (e != cudaSuccess) return e;
         if (dev < 31) configured_device_mask |= 1 << dev;
     }
-    return launch_dependent(kern, dim3(n_ctas), dim3(cta_threads(NHT)), SH::kSmemBytes, s, tk, tv, ts, tks, p);
+    return launch_dependent(kern, dim3(n_ctas), dim3(cta_threads(NHT)), SH::kSmemBytes, s, m.k, m.v, m.s, m.ks, m.kt,
+                            m.vt, m.st, m.kst, p);
 }
 
 template <int KV>
@@ -1241,20 +1258,19 @@ size_t smem_bytes_kv(int D, int n_head_tiles)
 }
 
 template <int KV>
-cudaError_t launch_kv(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ts,
-                      const CUtensorMap& tks, int n_head_tiles, int n_ctas, cudaStream_t s)
+cudaError_t launch_kv(const PartialParams& p, const PartialMaps& m, int n_head_tiles, int n_ctas, cudaStream_t s)
 {
     if (n_head_tiles == 2) {
         switch (p.D) {
-        case 64: return launch_one<64, KV, 2>(p, tk, tv, ts, tks, n_ctas, s);
-        case 128: return launch_one<128, KV, 2>(p, tk, tv, ts, tks, n_ctas, s);
+        case 64: return launch_one<64, KV, 2>(p, m, n_ctas, s);
+        case 128: return launch_one<128, KV, 2>(p, m, n_ctas, s);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (p.D) {
-    case 64: return launch_one<64, KV, 1>(p, tk, tv, ts, tks, n_ctas, s);
-    case 128: return launch_one<128, KV, 1>(p, tk, tv, ts, tks, n_ctas, s);
-    case 256: return launch_one<256, KV, 1>(p, tk, tv, ts, tks, n_ctas, s);
+    case 64: return launch_one<64, KV, 1>(p, m, n_ctas, s);
+    case 128: return launch_one<128, KV, 1>(p, m, n_ctas, s);
+    case 256: return launch_one<256, KV, 1>(p, m, n_ctas, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1294,14 +1310,13 @@ size_t partial_tc_smem_bytes(int D, int kv_dtype, int n_head_tiles)
     }
 }
 
-cudaError_t launch_partial_tc(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& ts, const CUtensorMap& tks, int kv_dtype, int n_head_tiles,
+cudaError_t launch_partial_tc(const PartialParams& p, const PartialMaps& m, int kv_dtype, int n_head_tiles,
                               int n_ctas, cudaStream_t s)
 {
     switch (kv_kind(kv_dtype)) {
-    case kKvQ8: return launch_kv<kKvQ8>(p, tk, tv, ts, tks, n_head_tiles, n_ctas, s);
-    case kKvVq8: return launch_kv<kKvVq8>(p, tk, tv, ts, tks, n_head_tiles, n_ctas, s);
-    default: return launch_kv<kKvBf16>(p, tk, tv, ts, tks, n_head_tiles, n_ctas, s);
+    case kKvQ8: return launch_kv<kKvQ8>(p, m, n_head_tiles, n_ctas, s);
+    case kKvVq8: return launch_kv<kKvVq8>(p, m, n_head_tiles, n_ctas, s);
+    default: return launch_kv<kKvBf16>(p, m, n_head_tiles, n_ctas, s);
     }
 }
 
