@@ -280,11 +280,10 @@ def cpu_baseline(name: str, cases: list, budget: float) -> dict:
 
 # ---------------------------------------------------------------- the workload
 
-def workload_bytes(name: str, T_override=None):
+def workload_bytes(cfg: dict):
     """(bytes of one benchmark step, partial-kernel bytes of one benchmark step,
     decode steps per benchmark step) from the seeded lengths alone (no device)."""
-    cfg = W.config(name)
-    n_dec = DECODES_PER_STEP.get(name, 1)
+    n_dec = DECODES_PER_STEP.get(cfg["name"], 1)
     T = int(cfg.get("q_len", 1) or 1)
     step_bytes = part_bytes = 0
     for lc in W.layer_configs(cfg):
@@ -296,11 +295,11 @@ def workload_bytes(name: str, T_override=None):
     return step_bytes, part_bytes, n_dec
 
 
-def config_block(name: str, world: int) -> dict:
+def config_block(cfg: dict, world: int) -> dict:
     """The workload as the JSON line's `config` (the same dict on both arms)."""
-    cfg = W.config(name)
+    name = cfg["name"]
     lcs = W.layer_configs(cfg)
-    step_bytes, part_bytes, n_dec = workload_bytes(name)
+    step_bytes, part_bytes, n_dec = workload_bytes(cfg)
     kv_mb = part_bytes / n_dec / 1e6
     out = {"workload": name, "batch": cfg["batch"], "seq_len": cfg["seq_len"], "n_q_heads": cfg["n_q_heads"],
            "n_kv_heads": cfg["n_kv_heads"], "head_dim": cfg["head_dim"], "kv_dtype": cfg["kv_dtype"],
@@ -335,9 +334,11 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
     from gqa_attention_kv_qk_gb300 import binding as Bd
     device = f"cuda:{local}"
     cfg = W.config(name, seed=W.CONFIGS[name]["seed"] + 1000 * rank)
+    if args.batch:
+        cfg["batch"] = args.batch
     if args.reproducible:
         cfg["reproducible"] = True
-    step_bytes, part_bytes, n_dec = workload_bytes(name)
+    step_bytes, part_bytes, n_dec = workload_bytes(cfg)
     T = int(cfg.get("q_len", 1) or 1)  # tokens per sequence and call
     layers, cases = build_layers(cfg, cap_extra=n_dec * T + 1, device=device)
     if rank != 0:  # the seeded lengths of another rank's replica: its own bytes
@@ -566,7 +567,7 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
         "pct_of_measured_copy_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "pct_of_nominal_hbm_peak": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "dtype": {"f32": "f32", "q8": "f16"}.get(cfg["kv_dtype"], "bf16"),
-        "config": config_block(name, world),
+        "config": config_block(cfg, world),
         "roofline": {"bound": "hbm", "achieved": round(part_gbs, 2) if part_gbs else None,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(part_gbs / peaks["hbm_gbs"], 4) if part_gbs else None,
@@ -655,7 +656,7 @@ def run_reference(args, world, rank) -> dict | None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) cache and inputs)",
-            "config": config_block(name, world),
+            "config": config_block(cfg, world),
             "timing": "wall clock of each sample (time.perf_counter)",
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": n_thr, "kind": "oracle",
                              "sample": sample},
@@ -673,6 +674,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure the headline workload only (not the suite's other four)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (a smaller case for profiling; not a benchmark config)")
     ap.add_argument("--reproducible", action="store_true",
                     help="uniform stream-K ranges (equal bits on every launch) instead of speed-weighted ones")
     args = ap.parse_args(argv)
