@@ -733,10 +733,17 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 pos += sg.n_st;
             }
             if (p.fused && !counted) count_in_and_advance(p, lens);
-            // Copies in flight land before the CTA may exit (bounded).
+            // Every copy this thread issued lands before the CTA may exit, also after a
+            // failed wait (then the consumers no longer wait for them): the last kStages
+            // issued stages are the only ones not yet consumed, and once the producer
+            // stops no barrier starts a new phase, so a phase that completed earlier
+            // reads as complete. Bounded: a copy that never lands ends the wait.
             const int first = it > SH::kStages ? it - SH::kStages : 0;
-            for (int i = first; i < it && ok; ++i)
-                ok = ptx::mbar_wait(bar_full + 8 * (i % SH::kStages), (i / SH::kStages) & 1, kWaitLimitCycles);
+            for (int i = first; i < it; ++i)
+                if (!ptx::mbar_wait(bar_full + 8 * (i % SH::kStages), (i / SH::kStages) & 1, kWaitLimitCycles)) {
+                    atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                    break;
+                }
         }
         return;
     }
