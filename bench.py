@@ -59,8 +59,9 @@ def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def measured_traffic(workload: str):
@@ -109,6 +110,20 @@ def partial_bytes(cfg: dict, lens_after: list[int]) -> int:
     w = cfg.get("window", 0) or 0
     w = w + T - 1 if w else 0
     return sum(visible(n, w) for n in lens_after) * cfg["n_kv_heads"] * (kb + vb)
+
+
+def attention_flops(cfg: dict, lens_before: list[int]) -> int:
+    """Tensor work of one step (q_len = T tokens per sequence): every (token, query
+    head) row against each key it sees (the cache and the chunk's tokens up to its
+    own, within the window), 2 D flops for QK and 2 D for P.V per (row, key)."""
+    T = int(cfg.get("q_len", 1) or 1)
+    G = cfg["n_q_heads"] // cfg["n_kv_heads"]
+    w = cfg.get("window", 0) or 0
+    keys = 0
+    for n in lens_before:
+        for t in range(T):
+            keys += visible(n + t + 1, w)
+    return keys * cfg["n_kv_heads"] * G * 4 * cfg["head_dim"]
 
 
 def decode_step_bytes(cfg: dict, lens_before: list[int]) -> int:
@@ -555,6 +570,12 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
     n_layers = len(cases)
     if all(one_launch):  # the timed region: one kernel per layer and decode step (and a length reset per 64)
         part_s, n_part = dev_s, args.steps * n_dec * n_layers
+    # tensor work of one benchmark step (a prefill chunk is bound by it, not by the cache bytes)
+    step_flops = 0
+    for lc, l0 in zip(W.layer_configs(cfg), lens0):
+        base = [int(x) for x in l0]
+        for t in range(n_dec):
+            step_flops += attention_flops(lc, [x + t * T for x in base])
     part_gbs = (part_bytes / (n_dec * n_layers)) / (part_s / n_part) / 1e9 if n_part else None
     decodes = n_dec * args.steps * world
     rec = {
@@ -582,9 +603,18 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
         "e2e": {"value": round(total_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "tflops": round(step_flops * args.steps / dev_s / 1e12, 2),
         "clocks": clocks.summary(),
         "cpu_baseline": cpu_baseline(name, cases, cpu_budget) if with_cpu else None,
     }
+    if T >= 64 and n_part:  # a prefill chunk: the partial kernel against the bf16 tensor peak
+        kern_tf = (step_flops / (n_dec * n_layers)) / (part_s / n_part) / 1e12
+        hbm = rec["roofline"]
+        rec["roofline"] = {"bound": "tensor", "achieved": round(kern_tf, 2), "peak": peaks["bf16_tflops"],
+                           "unit": "TFLOP/s", "frac": round(kern_tf / peaks["bf16_tflops"], 4),
+                           "traffic": hbm["traffic"], "kernel": hbm["kernel"], "peak_source": peaks["source"],
+                           "flops_per_launch": step_flops // max(1, n_dec * n_layers),
+                           "mean_launch_us": hbm["mean_launch_us"], "hbm_gbs": hbm["achieved"]}
     if cold_s is not None:
         first = sum(decode_step_bytes(lc, [int(x) for x in l0]) for lc, l0 in zip(W.layer_configs(cfg), lens0))
         rec["cold"] = {"value": round(first * args.steps / cold_s / 1e9, 2), "unit": "GB/s",

@@ -79,6 +79,13 @@ CONFIGS: dict[str, dict] = {
         kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
         rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
         low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
+    # The Llama-3.1-8B-like cache with a 512-token prefill chunk per sequence and step
+    # (each token attends the cache and the chunk's earlier tokens).
+    "llama31_8b_prefill": dict(
+        batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, seq_len=8192, steps=1, seed=9, q_len=512,
+        kv_dtype="bf16", io_dtype="bf16", out_dtype="f32",
+        rope_style="neox", rope_theta=500000.0, rope_scaling="llama3", factor=8.0,
+        low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192),
     # Gemma-3-12B-like decode: QK RMSNorm whose weights are stored as deltas from
     # one (applied as 1 + w), scale 1/sqrt(256), no softcap; one layer of each
     # kind per step (the model runs five local layers per global one): a local

@@ -249,6 +249,11 @@ EDGE = [
     ("chunk16-q8-paged64", "llama31_8b_q8", dict(batch=2, seq_len=700, q_len=16, page_size=64), [680, 100]),
     ("chunk64-prefill-g2", "llama31_8b_decode", dict(batch=2, n_q_heads=16, n_kv_heads=8, seq_len=300, q_len=64),
      [200, 0]),
+    # prefill chunks: 256 and 1,024 tokens (many 16-row groups per kv head), one from an empty cache
+    ("chunk256-prefill-g4", "llama31_8b_decode", dict(batch=2, n_q_heads=8, n_kv_heads=2, seq_len=1400, q_len=256,
+                                                     steps=1), [1000, 0]),
+    ("chunk1024-prefill-g4", "llama31_8b_decode", dict(batch=1, n_q_heads=8, n_kv_heads=2, seq_len=1100, q_len=1024,
+                                                      steps=1), [60]),
     # short chunks with two column tiles: new rows that cross a stage or page boundary,
     # two head groups, windows shorter than the chunk; head_dim 256 with one column tile
     ("chunk4-g4-stage-crossing", "llama31_8b_decode", dict(batch=4, seq_len=600, q_len=4), [126, 254, 1, 509]),
