@@ -385,7 +385,7 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
     # kernels of one call of a layer: the fused append+partial and the combine
     # (bf16 / vq8 / q8 caches, one token), one kernel for a small fp32 step, or
     # append, partial and combine
-    lays = [layer.layout(max_seq_len=h) for layer, h in zip(layers, hint)]
+    lays = [Bd.uaa_get_workspace_layout(layer.desc, layer.batch, h, 0, T) for layer, h in zip(layers, hint)]
     fused = [lay.kernel == 1 and T == 1 for lay in lays]
     one_launch = [lay.step_splits > 0 for lay in lays]
     launches_per_step = n_dec * sum(lay.step_kernels for lay in lays)
@@ -596,6 +596,7 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
                      "frac_of_nominal": round(part_gbs / NOMINAL_HBM_GBS, 4) if part_gbs else None,
                      "kernel": ("fused append + split-K partial" if all(fused) else
                                 "fp32 one-launch step (append, attention, merge)" if all(one_launch) else
+                                "query-tiled prefill" if all(lay.kernel == 2 for lay in lays) else
                                 "split-K partial"),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": part_bytes // max(1, n_dec * n_layers),

@@ -121,6 +121,7 @@ struct Plan {
     int slice;           // sequences per partial launch
     int n_slices;
     int per_sm;          // resident CTAs per SM
+    int prefill;         // a contiguous cache takes the query-tiled prefill kernel (no combine)
     size_t off_status, off_qrot, off_prefix, off_rec_lse, off_rec_o, off_ranges, off_owners, off_balance, total;
     size_t prefix_stride, rec_lse_stride, rec_o_stride, ranges_stride, owners_stride;  // bytes per slice
 };
@@ -193,6 +194,10 @@ uaa_status make_plan(const uaa_attn_desc* d, int batch, int q_len, int max_len, 
     // tiles (its eight consumer warps take the registers of two CTAs)
     p.per_sm = p.kernel == 0 ? 4 : (d->head_dim == 256 || p.n_head_tiles == 2 ? 1 : 2);
     p.n_ctas = n_sm * p.per_sm;
+    // long chunks on contiguous bf16 caches: whole 64-row blocks of (token, head) rows
+    // per CTA, each streaming its keys once (the partial kernel's units hold 16 rows)
+    p.prefill = p.kernel == 1 && d->kv_dtype == UAA_DTYPE_BF16 && (d->head_dim == 64 || d->head_dim == 128) &&
+                rows >= uaa::kPrefillRows;
     p.slice = batch < uaa::kMaxSliceBatch ? (batch > 0 ? batch : 1) : uaa::kMaxSliceBatch;
     p.n_slices = batch > 0 ? (batch + p.slice - 1) / p.slice : 0;
 
@@ -449,11 +454,46 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     return e == cudaSuccess ? UAA_OK : cuda_fail(e, "append kernel launch");
 }
 
+// The query-tiled prefill kernel takes step 2 of this call (and step 3 has nothing to do).
+bool takes_prefill(const uaa_step_args* a, const Plan& pl) { return pl.prefill && !a->block_table; }
+
+uaa_status run_prefill(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
+                       cudaStream_t s)
+{
+    char* w = static_cast<char*>(ws->ptr);
+    const uint64_t D = d->head_dim;
+    const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
+    CUtensorMap tk, tv;
+    UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64,
+                      (uint32_t)uaa::kTileKeys, CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
+    UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64,
+                      (uint32_t)uaa::kTileKeys, CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
+    uaa::PrefillParams p{};
+    p.B = a->batch;
+    p.Hq = d->n_q_heads;
+    p.Hkv = d->n_kv_heads;
+    p.D = d->head_dim;
+    p.G = pl.G;
+    p.q_len = pl.q_len;
+    p.cap = a->cache_capacity;
+    p.window = d->window;
+    p.softcap_log2e = d->softcap > 0.f ? d->softcap * uaa::kLog2e : 0.f;
+    p.q_prime = reinterpret_cast<const float*>(w + pl.off_qrot);
+    p.seq_lens = a->seq_lens;
+    p.sink = d->has_sink ? a->sink : nullptr;
+    p.out = a->out;
+    p.out_dtype = d->out_dtype;
+    p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+    const cudaError_t e = uaa::launch_prefill_tc(p, tk, tv, s);
+    return e == cudaSuccess ? UAA_OK : cuda_fail(e, "prefill kernel launch");
+}
+
 // fused: the tensor-core kernel also performs the append (steps 1 and 2 in one launch).
 uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_workspace* ws, const Plan& pl,
                        cudaStream_t s, bool fused = false)
 {
     if (a->batch == 0) return UAA_OK;
+    if (takes_prefill(a, pl)) return run_prefill(d, a, ws, pl, s);
     char* w = static_cast<char*>(ws->ptr);
     const size_t D = d->head_dim, Hq = d->n_q_heads;
     const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
@@ -585,6 +625,7 @@ uaa_status run_combine(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
                        cudaStream_t s)
 {
     if (a->batch == 0) return UAA_OK;
+    if (takes_prefill(a, pl)) return UAA_OK;  // the prefill kernel wrote the output rows
     char* w = static_cast<char*>(ws->ptr);
     const size_t D = d->head_dim, Hq = d->n_q_heads;
     const size_t out_elem = d->out_dtype == UAA_DTYPE_F32 ? 4 : 2;
@@ -783,7 +824,7 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, in
     layout->n_ctas = pl.n_ctas;
     layout->stage_keys = pl.mg * uaa::kTileKeys;
     layout->heads_per_cta = pl.heads_per_cta;
-    layout->kernel = pl.kernel;
+    layout->kernel = pl.prefill ? 2 : pl.kernel;
     layout->n_slices = pl.n_slices;
     layout->slice_batch = pl.slice;
     {
@@ -793,6 +834,7 @@ uaa_status uaa_get_workspace_layout(const uaa_attn_desc* desc, int32_t batch, in
         layout->step_splits = f32_step_splits(desc, &a, pl);
         layout->step_kernels = batch == 0 ? 0
                                : layout->step_splits > 0 ? 1
+                               : pl.prefill ? 2
                                : (pl.kernel == 1 && pl.q_len == 1) ? 2 * pl.n_slices
                                                                    : 1 + 2 * pl.n_slices;
     }

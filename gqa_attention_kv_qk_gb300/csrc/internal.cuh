@@ -212,6 +212,24 @@ struct StepF32Params {
     double inv_freq_over_pi[kMaxHeadDim / 2];
 };
 
+// Attention of a long chunk (prefill_tc.cu), after the append: a CTA per
+// (sequence, kv head, block of 128 (token, head) rows) streams the keys its rows
+// see once and writes their output rows; contiguous bf16 caches, head_dim 64 or
+// 128.
+struct PrefillParams {
+    int B, Hq, Hkv, D, G;
+    int q_len;              // tokens per sequence
+    int cap;
+    int window;             // the descriptor's window per query row (0: none)
+    float softcap_log2e;    // 0: no softcap; else softcap * log2(e)
+    const float* q_prime;   // [B][q_len][Hq][D], written by the append
+    const int* seq_lens;    // lengths after the append
+    const float* sink;      // [Hq] or null
+    void* out;              // [B][q_len][Hq][D]
+    int out_dtype;
+    unsigned* status;
+};
+
 // ---------------------------------------------------------------- launches
 // Each returns the launch error (cudaGetLastError) of its kernel.
 
@@ -228,6 +246,10 @@ struct PartialMaps {
 cudaError_t launch_partial_tc(const PartialParams& p, const PartialMaps& m, int kv_dtype, int n_head_tiles,
                               int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+// tk, tv: tensor maps of the key and value caches with boxes of 64 rows x 64 columns.
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
+// Query rows per CTA of the prefill kernel.
+constexpr int kPrefillRows = 128;
 cudaError_t launch_step_f32(const StepF32Params& p, cudaStream_t s);
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
                                 float* scales, cudaStream_t s);

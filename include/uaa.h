@@ -77,7 +77,7 @@
 extern "C" {
 #endif
 
-#define UAA_ABI_VERSION 10
+#define UAA_ABI_VERSION 11
 
 typedef enum {
     UAA_OK = 0,
@@ -224,10 +224,14 @@ typedef struct {
     int32_t stage_keys;       /* keys per ring stage: 64; 128 for q8 at head_dim 128 / 256;
                                  at head_dim 64 128 (bf16), 256 (vq8, q8) */
     int32_t heads_per_cta;    /* query rows (token, head) of one unit (sequence, kv head, row group) */
-    int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial */
+    int32_t kernel;           /* 0: fp32 CUDA-core partial, 1: TMA + tensor-core partial,
+                                 2: query-tiled prefill on a contiguous cache (bf16 cache,
+                                 head_dim 64 / 128, q_len x G >= 128 rows per kv head;
+                                 a paged cache of this geometry takes kernel 1, whose
+                                 fields the others still describe) */
     int32_t n_slices;         /* partial + combine launches (batch slices) */
     int32_t slice_batch;      /* sequences per slice (the last may hold fewer) */
-    int32_t step_kernels;     /* kernels one uaa_decode_attn call launches */
+    int32_t step_kernels;     /* kernels one uaa_decode_attn call launches (contiguous cache) */
     int32_t step_splits;      /* key splits per unit of the fp32 one-launch step, 0 when the
                                  step does not take it (tensor-core caches, chunks, records
                                  beyond 2P, several slices) */
@@ -258,11 +262,18 @@ uaa_status uaa_rope_qk_norm_append(const uaa_attn_desc* desc, const uaa_step_arg
                                    const uaa_workspace* ws, cudaStream_t stream);
 
 /* Step 2 (split-K partials) over the visible keys of every sequence; writes the
- * output rows of units finished inside one CTA and records for the others. */
+ * output rows of units finished inside one CTA and records for the others.
+ * A long chunk on a contiguous bf16 cache (head_dim 64 or 128, q_len x G >= 128
+ * (token, head) rows per kv head; uaa_workspace_layout.kernel == 2) takes the
+ * query-tiled prefill kernel instead: a CTA per (sequence, kv head, block of
+ * 128 rows) reads each key and value tile its rows see once, and writes the
+ * block's output rows itself (sink included); rows of a sequence the append
+ * could not take are zero. Step 3 then has nothing to do. */
 uaa_status uaa_decode_attn_partial(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
-/* Step 3 (log-sum-exp combine + sink) of the recorded units into args->out. */
+/* Step 3 (log-sum-exp combine + sink) of the recorded units into args->out;
+ * launches nothing after the query-tiled prefill kernel. */
 uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 

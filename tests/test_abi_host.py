@@ -36,7 +36,7 @@ def test_every_declared_entry_point_is_exported(L):
         assert hasattr(L, n), f"{n} declared in uaa.h but not exported"
     bound = {s[0] for s in B._SIGS}
     assert bound == set(names), "binding and header disagree"
-    assert B.uaa_abi_version() == 10
+    assert B.uaa_abi_version() == 11
 
 
 def good_desc(**kw):
@@ -229,9 +229,16 @@ def test_chunk_geometry(L, name, kv):
     for T in (1, 2, 4, 16, 64):
         lay = B.uaa_get_workspace_layout(d, 8, 1000, 152, q_len=T)
         rows = T * G
-        wide = lay.kernel == 1 and cfg["head_dim"] != 256 and rows > 8
+        # 128 rows or more per kv head on a bf16 cache at head_dim 64 / 128: the
+        # query-tiled prefill kernel (append + prefill, no combine; a paged cache of
+        # the same geometry takes the partial kernel, whose geometry is still reported)
+        prefill = kv == "bf16" and cfg["head_dim"] in (64, 128) and rows >= 128
+        assert lay.kernel == (2 if prefill else (0 if kv == "f32" else 1))
+        assert lay.step_kernels == (2 if prefill or (kv != "f32" and T == 1) else (1 if lay.step_splits else 3))
+        tc = lay.kernel in (1, 2)
+        wide = tc and cfg["head_dim"] != 256 and rows > 8
         assert lay.heads_per_cta == (16 if wide else 8)
-        if lay.kernel == 1:  # keys per ring stage: two 16-key groups per warp where keys are cheap or rows many
+        if tc:  # keys per ring stage: two 16-key groups per warp where keys are cheap or rows many
             D = cfg["head_dim"]
             want = (256 if kv in ("vq8", "q8") else 128) if D == 64 else (128 if kv == "q8" or (wide and D == 128)
                                                                          else 64)
