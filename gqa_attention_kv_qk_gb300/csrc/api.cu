@@ -335,7 +335,7 @@ float qscale(const uaa_attn_desc* d)
 // Entries of pairs beyond R/2 stay 0 (those pairs are not rotated).
 int rotary_dims(const uaa_attn_desc* d) { return d->rotary_dim > 0 ? d->rotary_dim : d->head_dim; }
 
-void rope_table(const uaa_attn_desc* d, double* inv_freq_over_pi, float* mscale)
+void rope_table(const uaa_attn_desc* d, double* inv_freq_over_pi, float* mscale, double* mscale64 = nullptr)
 {
     const int D = rotary_dims(d);
     for (int i = 0; i < d->head_dim / 2; ++i) inv_freq_over_pi[i] = 0.0;
@@ -373,6 +373,7 @@ void rope_table(const uaa_attn_desc* d, double* inv_freq_over_pi, float* mscale)
         inv_freq_over_pi[i] = g / pi;
     }
     *mscale = (float)ms;
+    if (mscale64) *mscale64 = ms;
 }
 
 // ---------------------------------------------------------------- TMA descriptors
@@ -449,7 +450,7 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.q_prime = reinterpret_cast<float*>(w + pl.off_qrot);
     p.q_rot_out = a->q_rot;
     p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
-    rope_table(d, p.inv_freq_over_pi, &p.mscale);
+    rope_table(d, p.inv_freq_over_pi, &p.mscale, &p.mscale64);
     const cudaError_t e = uaa::launch_append(p, s);
     return e == cudaSuccess ? UAA_OK : cuda_fail(e, "append kernel launch");
 }
@@ -484,7 +485,7 @@ uaa_status run_prefill(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     p.out = a->out;
     p.out_dtype = d->out_dtype;
     p.status = reinterpret_cast<unsigned*>(w + pl.off_status);
-    const cudaError_t e = uaa::launch_prefill_tc(p, tk, tv, s);
+    const cudaError_t e = uaa::launch_prefill_umma(p, tk, tv, s);
     return e == cudaSuccess ? UAA_OK : cuda_fail(e, "prefill kernel launch");
 }
 
@@ -611,7 +612,7 @@ uaa_status run_partial(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
             p.q_norm_w = a->q_norm_w;
             p.k_norm_w = a->k_norm_w;
             p.q_rot_out = a->q_rot ? a->q_rot + (size_t)b0 * Hq * D : nullptr;
-            rope_table(d, p.inv_freq_over_pi, &p.mscale);
+            rope_table(d, p.inv_freq_over_pi, &p.mscale, &p.mscale64);
         }
         const cudaError_t e = pl.kernel == 0
                                   ? uaa::launch_partial_simt(p, pl.n_ctas, s)

@@ -140,10 +140,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
             for (int i = 0; i < EPL; ++i) rowbuf[warp][lane + 32 * i] = x[i];
             __syncwarp();
 
+            // keys of a bf16 (or vq8) cache: rounded as their exact values (bf16_near_boundary)
+            const bool kbf16 = is_k && stores && p.kv_dtype != UAA_DTYPE_F32 && p.kv_dtype != UAA_DTYPE_Q8;
             for (int pp = lane; pp < HALF; pp += 32) {
                 const int2 e = rope_pair(pp, p.half_rot, D, p.style == UAA_ROPE_NEOX);
                 const int ia = e.x, ib = e.y;
                 float ya = rowbuf[warp][ia], yb = rowbuf[warp][ib];
+                const float a0 = ya, b0 = yb;
                 rope_rotate(ya, yb, cs[pp]);
                 if (is_q) {
                     float* qp = p.q_prime + in_row;
@@ -156,11 +159,33 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                 } else if (stores && p.kv_dtype == UAA_DTYPE_Q8) {  // the whole rotated row first: its scale
                     rowbuf[warp][ia] = ya;                            // needs max |k| (pairs are disjoint)
                     rowbuf[warp][ib] = yb;
+                } else if (kbf16) {
+                    __nv_bfloat16 ha = __float2bfloat16_rn(ya), hb = __float2bfloat16_rn(yb);
+                    const float eb = key_error_bound(a0, b0, cs[pp]);
+                    const bool near = bf16_near_boundary(ya, eb) || bf16_near_boundary(yb, eb);
+                    if (__any_sync(0xffffffffu, near)) {  // the pair again in fp64 (the whole warp for the norm)
+                        size_t at;
+                        const void* src = row_source(p, b, tok, r, at);
+                        double inv64 = 0.0;
+                        if (p.qk_norm) {
+                            double raw[EPL];
+#pragma unroll
+                            for (int i = 0; i < EPL; ++i) raw[i] = load_as_float<T>(src, at + lane + 32 * i);
+                            inv64 = rms_inv64<EPL>(raw, D, p.eps);
+                        }
+                        if (near) {
+                            const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[ia]) + p.norm_offset : 1.0;
+                            const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[ib]) + p.norm_offset : 1.0;
+                            key_pair_exact(load_as_float<T>(src, at + ia), load_as_float<T>(src, at + ib), wa, wb,
+                                           inv64, rope_cos_sin64(pp, p.half_rot, pos, p.inv_freq_over_pi[pp], p.mscale64),
+                                           ha, hb);
+                        }
+                    }
+                    static_cast<__nv_bfloat16*>(p.k_cache)[slot + ia] = ha;
+                    static_cast<__nv_bfloat16*>(p.k_cache)[slot + ib] = hb;
                 } else if (stores) {
-                    store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
-                             slot + ia, ya);
-                    store_kv(p.k_cache, p.kv_dtype == UAA_DTYPE_F32 ? UAA_DTYPE_F32 : UAA_DTYPE_BF16,
-                             slot + ib, yb);
+                    store_kv(p.k_cache, UAA_DTYPE_F32, slot + ia, ya);
+                    store_kv(p.k_cache, UAA_DTYPE_F32, slot + ib, yb);
                 }
             }
             __syncwarp();

@@ -41,6 +41,7 @@ struct AppendParams {
     float norm_offset;      // added to each RMSNorm weight (0, or 1 for Gemma's stored delta)
     float qscale;           // q_prime = rotated q * qscale (the partial kernel's logit prescale)
     float mscale;           // cos / sin multiplier (YaRN attention factor, else 1)
+    double mscale64;        // the same in fp64 (keys recomputed near a bf16 rounding boundary)
     int io_dtype, kv_dtype;
     const void* q;
     const void* k_new;
@@ -153,6 +154,7 @@ struct PartialParams {
     int style, qk_norm;
     int half_rot;           // rotated pairs per head row (rotary_dim / 2)
     float eps, qscale, mscale;
+    double mscale64;        // mscale in fp64 (keys recomputed near a bf16 rounding boundary)
     float norm_offset;      // added to each RMSNorm weight
     const float* q_norm_w;
     const float* k_norm_w;
@@ -212,7 +214,7 @@ struct StepF32Params {
     double inv_freq_over_pi[kMaxHeadDim / 2];
 };
 
-// Attention of a long chunk (prefill_tc.cu), after the append: a CTA per
+// Attention of a long chunk (prefill_umma.cu), after the append: a CTA per
 // (sequence, kv head, block of 128 (token, head) rows) streams the keys its rows
 // see once and writes their output rows; contiguous bf16 caches, head_dim 64 or
 // 128.
@@ -247,7 +249,7 @@ cudaError_t launch_partial_tc(const PartialParams& p, const PartialMaps& m, int 
                               int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 // tk, tv: tensor maps of the key and value caches with boxes of 64 rows x 64 columns.
-cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
+cudaError_t launch_prefill_umma(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
 // Query rows per CTA of the prefill kernel.
 constexpr int kPrefillRows = 128;
 cudaError_t launch_step_f32(const StepF32Params& p, cudaStream_t s);
@@ -535,6 +537,87 @@ __device__ __forceinline__ int2 rope_pair(int pp, int half_rot, int D, bool neox
 {
     if (!neox) return make_int2(2 * pp, 2 * pp + 1);
     return pp < half_rot ? make_int2(pp, pp + half_rot) : make_int2(pp + half_rot, pp + D / 2);
+}
+
+// ---------------------------------------------------------------- bf16 keys, rounded as their exact values
+// A rotated key element goes to a bf16 cache rounded to nearest-even from its
+// exact value (the method's storage precision). The fp32 result y of the
+// normalisation and rotation lies within key_error_bound of the exact value;
+// where that interval holds no bf16 rounding boundary, RN(y) is the exact
+// value's rounding. Otherwise (about one element in 500) the element is
+// recomputed in fp64 (rope_cos_sin64, rms_inv64) and rounded from there
+// (bf16_from_double).
+
+// Bound on |y - exact| for y = a c - b s computed in fp32 from a, b (after an
+// fp32 RMSNorm, if any) and c, s (sincospif of the exactly reduced angle times
+// the multiplier): about 18 fp32 ulps of |a c| + |b s| in the worst case, taken
+// eight times over.
+__device__ __forceinline__ float key_error_bound(float a, float b, float2 cs)
+{
+    return 0x1p-17f * (fabsf(a * cs.x) + fabsf(b * cs.y)) + 0x1p-120f;
+}
+
+// Whether bf16 rounding of the exact value may differ from RN(y), |y - exact| <= e:
+// a rounding boundary (midpoint between neighbouring bf16 values) lies within e
+// of y. Values below 2^-118 always count as near (never met by real keys); inf
+// and NaN never.
+__device__ __forceinline__ bool bf16_near_boundary(float y, float e)
+{
+    const uint32_t ab = __float_as_uint(y) & 0x7fffffffu;
+    if (ab >= 0x7f800000u) return false;
+    const uint32_t rb = (ab + 0x7fffu + ((ab >> 16) & 1u)) & 0xffff0000u;  // RN-even to bf16, as bits of |y|
+    const uint32_t E = rb >> 23;                                             // its biased exponent
+    if (E < 9) return true;
+    const float u = __uint_as_float((E - 7u) << 23);              // bf16 spacing in that binade
+    const float h_lo = (rb & 0x007f0000u) ? 0.5f * u : 0.25f * u;  // below a power of two the spacing halves
+    const float d = __uint_as_float(ab) - __uint_as_float(rb);     // exact
+    return !(e < fminf(0.5f * u - d, h_lo + d));
+}
+
+// x rounded to nearest-even bf16 (overflow to infinity): toward zero to fp32 with
+// a sticky last bit (round to odd), then to nearest-even.
+__device__ __forceinline__ __nv_bfloat16 bf16_from_double(double x)
+{
+    float f = __double2float_rz(x);
+    if (static_cast<double>(f) != x) f = __uint_as_float(__float_as_uint(f) | 1u);
+    return __float2bfloat16_rn(f);
+}
+
+// (cos, sin) of the angle pos * theta'_p in fp64, times the multiplier; (1, 0) for a pair that is not rotated.
+__device__ __forceinline__ double2 rope_cos_sin64(int pp, int half_rot, int pos, double inv_freq_over_pi,
+                                                  double mscale)
+{
+    if (pp >= half_rot) return make_double2(1.0, 0.0);
+    const double t = static_cast<double>(pos) * inv_freq_over_pi;
+    const double r = fma(-2.0, rint(0.5 * t), t);
+    double sn, cn;
+    sincospi(r, &sn, &cn);
+    return make_double2(cn * mscale, sn * mscale);
+}
+
+// fp64 RMSNorm factor of a head row held EPL elements per lane (every lane of the warp calls it).
+template <int EPL>
+__device__ __forceinline__ double rms_inv64(const double (&x)[EPL], int D, float eps)
+{
+    double ss = 0.0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) ss = fma(x[i], x[i], ss);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    return 1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps));
+}
+
+// The rotated pair (ra, rb: raw key elements; wa, wb: their norm weights plus
+// offset, used when inv64 > 0) in fp64, rounded to bf16.
+__device__ __forceinline__ void key_pair_exact(double ra, double rb, double wa, double wb, double inv64, double2 cs,
+                                               __nv_bfloat16& ha, __nv_bfloat16& hb)
+{
+    if (inv64 > 0.0) {
+        ra = ra * inv64 * wa;
+        rb = rb * inv64 * wb;
+    }
+    ha = bf16_from_double(ra * cs.x - rb * cs.y);
+    hb = bf16_from_double(ra * cs.y + rb * cs.x);
 }
 
 // Query row r of a unit of kv head kvh: the rows of a kv head are the (token,

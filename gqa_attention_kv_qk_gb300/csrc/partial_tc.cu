@@ -426,8 +426,13 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
             kb[j] = kb[j] * inv * (p.k_norm_w[ib[j]] + p.norm_offset);
         }
     }
+    float ka0[NP], kb0[NP];  // before the rotation
 #pragma unroll
-    for (int j = 0; j < NP; ++j) rope_rotate(ka[j], kb[j], cs[lane + 32 * j]);
+    for (int j = 0; j < NP; ++j) {
+        ka0[j] = ka[j];
+        kb0[j] = kb[j];
+        rope_rotate(ka[j], kb[j], cs[lane + 32 * j]);
+    }
     if (KQ8) {  // the rotated row's codes, by the vq8 rule over the whole row
         float amax = 0.f;
 #pragma unroll
@@ -450,11 +455,43 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
             if (store) p.k_scale[slot] = sc;
         }
     } else {
+        // rounded as the exact values (bf16_near_boundary): the rare pair near a
+        // rounding boundary again in fp64
         __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(staging);
         __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.k_cache) + slot * D;
+        __nv_bfloat16 hka[NP], hkb[NP];
+        bool near[NP], any = false;
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
-            const __nv_bfloat16 ha = __float2bfloat16_rn(ka[j]), hb = __float2bfloat16_rn(kb[j]);
+            hka[j] = __float2bfloat16_rn(ka[j]);
+            hkb[j] = __float2bfloat16_rn(kb[j]);
+            const float eb = key_error_bound(ka0[j], kb0[j], cs[lane + 32 * j]);
+            near[j] = bf16_near_boundary(ka[j], eb) || bf16_near_boundary(kb[j], eb);
+            any |= near[j];
+        }
+        if (__any_sync(0xffffffffu, any)) {
+            double inv64 = 0.0;
+            if (p.qk_norm) {
+                double raw[EPL];
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) raw[i] = load_as_float<T>(p.k_new, src + lane + 32 * i);
+                inv64 = rms_inv64<EPL>(raw, D, p.eps);
+            }
+#pragma unroll
+            for (int j = 0; j < NP; ++j)
+                if (near[j]) {
+                    const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[ia[j]]) + p.norm_offset : 1.0;
+                    const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[ib[j]]) + p.norm_offset : 1.0;
+                    key_pair_exact(load_as_float<T>(p.k_new, src + ia[j]), load_as_float<T>(p.k_new, src + ib[j]), wa,
+                                   wb, inv64,
+                                   rope_cos_sin64(lane + 32 * j, p.half_rot, L, p.inv_freq_over_pi[lane + 32 * j],
+                                                  p.mscale64),
+                                   hka[j], hkb[j]);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const __nv_bfloat16 ha = hka[j], hb = hkb[j];
             ks[ia[j]] = ha;
             ks[ib[j]] = hb;
             if (store) {

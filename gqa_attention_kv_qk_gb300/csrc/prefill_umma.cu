@@ -1,0 +1,460 @@
+// prefill_umma.cu -- attention of a long chunk of tokens (a prefill chunk) over
+// a contiguous bf16 cache on the 5th-generation tensor cores (tcgen05): step 2
+// for steps of many tokens per sequence, after the separate append has written
+// the chunk's rows and q'.
+//
+// The (token, head) rows of one kv head (token-major: row r is token r / G,
+// query head r % G of the group, as in query_row) are cut into blocks of 128.
+// One CTA per (sequence, kv head, row block) streams the keys its rows see (the
+// cache and the chunk's tokens up to the block's last one, within the window)
+// once, 64 keys per block, and writes the block's output rows itself: no
+// records, no combine. The row blocks of one kv head are neighbours in the
+// grid, so they read the same tiles at about the same time and HBM delivers
+// each tile about once.
+//
+// Per 64-key block j, with M = 128 rows on the tensor core:
+//   S_j (128 x 64, fp32 in TMEM) = Q' . K_j^T, Q' = the q' rows (fp32, rotated
+//     and prescaled by the append) as bf16 hi + lo parts (two MMAs per
+//     k-step), K_j as it sits in the TMA ring (keys x dims, 128-byte swizzle);
+//   softmax: thread r of the four softmax warps owns row r (TMEM lane r): it
+//     reads S_j, applies softcap and the causal / window masks, and keeps a
+//     running maximum m that it raises only when a logit exceeds it by more
+//     than 2^8 (exp2(s - m) <= 256 otherwise; the final division cancels m),
+//     rescaling its O row in TMEM then; P_j = exp2(S_j - m) goes to shared
+//     memory as bf16 hi + lo parts;
+//   O (128 x D, fp32 in TMEM) += P_j . V_j, V_j straight from the ring (keys x
+//     dims: N-contiguous).
+// S is double-buffered in TMEM and P in shared memory, so the softmax of block
+// j + 1 runs while the tensor core computes P_j . V_j and S_{j+2}.
+//
+// Warps (192 threads, one CTA per SM): warp 0 lane 0 issues the TMA loads of
+// the key and value tiles into a ring of stages (full / empty mbarriers; the
+// MMA's commit frees a stage); warp 1 allocates TMEM and its lane 0 issues every
+// MMA; warps 2-5 stage the q' rows and run the softmax and the epilogue. Every
+// wait is bounded: a wait that gives up sets UAA_DEVFLAG_TIMEOUT, the thread
+// stops waiting from then on, and the CTA still drains its copies and MMAs and
+// frees its TMEM before it exits.
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace uaa {
+namespace {
+
+constexpr int kUmRows = kPrefillRows;  // query rows per CTA (M of the MMAs)
+constexpr int kUmKeys = 64;            // keys per block (N of S, K of P . V)
+constexpr int kUmThreads = 192;
+constexpr uint32_t kUmTmemCols = 256;  // S[2] (64 columns each) + O (D columns)
+
+template <int D>
+struct UmShape {
+    static constexpr int kBoxes = D / 64;                 // 64-dim boxes of a row
+    static constexpr int kQBox = kUmRows * 128;           // 128 rows of one box: 16 KB
+    static constexpr int kQBytes = kBoxes * kQBox;        // Q' hi (or lo)
+    static constexpr int kKV = kUmKeys * D * 2;           // the keys (or values) of a stage
+    static constexpr int kStageBytes = 2 * kKV;
+    static constexpr int kStages = D == 128 ? 3 : 4;
+    static constexpr int kPBytes = kUmRows * kUmKeys * 2; // P hi (or lo) of one block: 16 KB
+    static constexpr int kOffQlo = kQBytes;
+    static constexpr int kOffRing = 2 * kQBytes;
+    static constexpr int kOffP = kOffRing + kStages * kStageBytes;  // P[2]: hi, lo
+    static constexpr int kOffBar = kOffP + 4 * kPBytes;
+    static constexpr int kSmemBytes = 1024 + kOffBar + 256;
+};
+
+__device__ __forceinline__ uint32_t um_pack(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// (x0, x1) ~= hi + lo: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void um_split(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    hi = um_pack(x0, x1);
+    lo = um_pack(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+
+// Byte offset of 16-byte chunk c (< 8) of row r in a 1024-byte-aligned tile of
+// 128-byte rows with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t um_swz(int r, int c)
+{
+    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kUmThreads, 1)
+prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const PrefillParams p)
+{
+    using SH = UmShape<D>;
+    constexpr int NS = SH::kStages;
+    constexpr int KS = D / 16;  // k-steps of Q'.K^T
+    constexpr uint32_t kIdS = ptx::umma_idesc_bf16(kUmRows, kUmKeys, false, false);
+    constexpr uint32_t kIdO = ptx::umma_idesc_bf16(kUmRows, D, false, true);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t q_hi = base, q_lo = base + SH::kOffQlo, ring = base + SH::kOffRing, pbuf = base + SH::kOffP;
+    const uint32_t bars = base + SH::kOffBar;
+    const uint32_t bar_full = bars, bar_empty = bars + 8 * NS;
+    const uint32_t bar_q = bars + 16 * NS;        // q' rows staged (128 arrivals)
+    const uint32_t bar_s = bar_q + 8;             // [2] S_j in TMEM (MMA commit)
+    const uint32_t bar_sfree = bar_s + 16;        // [2] S_j read (128 arrivals)
+    const uint32_t bar_p = bar_sfree + 16;        // [2] P_j in shared memory (128 arrivals)
+    const uint32_t bar_pv = bar_p + 16;           // [2] P_j . V_j done (MMA commit)
+    const uint32_t bar_drain = bar_pv + 16;       // every MMA done (MMA commit)
+    const uint32_t tmem_slot = bar_drain + 8;
+    uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (tmem_slot - ptx::smem_u32(smem_raw)));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rows = p.q_len * p.G;  // query rows of the kv head
+    const int n_rb = (rows + kUmRows - 1) / kUmRows;
+    const int rb = blockIdx.x % n_rb;
+    const int bk = blockIdx.x / n_rb;  // b * Hkv + kvh
+    const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        ptx::mbar_init(bar_q, 128);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar_s + 8 * i, 1);
+            ptx::mbar_init(bar_sfree + 8 * i, 128);
+            ptx::mbar_init(bar_p + 8 * i, 128);
+            ptx::mbar_init(bar_pv + 8 * i, 1);
+        }
+        ptx::mbar_init(bar_drain, 1);
+        ptx::fence_barrier_init();
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, kUmTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    grid_dependency_wait();  // the append's rows, q' and lengths are complete
+    __syncthreads();         // barriers initialised, TMEM allocated
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot_ptr;
+    const uint32_t t_o = tmem + 2 * kUmKeys;  // O: columns 128 ..
+
+    // The chunk's tokens sit at L .. L + q_len - 1 (the append advanced the length
+    // past them); a sequence the append could not take keeps its length and gets zero rows.
+    const int L_after = p.seq_lens[b];
+    const int L = L_after - p.q_len;
+    const bool valid = L >= 0 && L_after <= p.cap;
+    const int r_first = rb * kUmRows, r_last = min(rows, r_first + kUmRows) - 1;
+    const int hi = valid ? L + r_last / p.G + 1 : 0;  // keys the block sees: [lo, hi)
+    const int lo = valid && p.window > 0 ? max(0, L + r_first / p.G + 1 - p.window) : 0;
+    const int kb0 = lo / kUmKeys;
+    const int n_st = (hi + kUmKeys - 1) / kUmKeys - kb0;  // key blocks
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0 && n_st > 0) {
+            const int row0 = (b * p.Hkv + kvh) * p.cap + kb0 * kUmKeys;
+            int issued = 0;
+            for (int i = 0; i < n_st; ++i) {
+                const int s = i % NS;
+                if (i >= NS && !ptx::mbar_wait(bar_empty + 8 * s, ((i / NS) - 1) & 1, kWaitLimitCycles)) {
+                    atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                    break;
+                }
+                const uint32_t st = ring + s * SH::kStageBytes, bar = bar_full + 8 * s;
+                ptx::mbar_arrive_expect_tx(bar, SH::kStageBytes);
+#pragma unroll
+                for (int c = 0; c < SH::kBoxes; ++c) {
+                    // plain loads: the other row blocks of this kv head read the same tiles from L2
+                    ptx::tma_load_2d(st + c * (kUmKeys * 128), &tm_k, c * 64, row0 + i * kUmKeys, bar);
+                    ptx::tma_load_2d(st + SH::kKV + c * (kUmKeys * 128), &tm_v, c * 64, row0 + i * kUmKeys, bar);
+                }
+                issued = i + 1;
+            }
+            // every issued copy lands before the CTA may exit
+            for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
+                if (!ptx::mbar_wait(bar_full + 8 * (i % NS), (i / NS) & 1, kWaitLimitCycles)) {
+                    atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+                    break;
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issue
+        if (lane == 0 && n_st > 0) {
+            bool ok = ptx::mbar_wait(bar_q, 0, kWaitLimitCycles);
+            ptx::tc_fence_after();
+            // S_j = Q'hi . K_j^T + Q'lo . K_j^T into S buffer j % 2
+            auto issue_s = [&](int j) {
+                const int s = j % NS;
+                ok = ok && ptx::mbar_wait(bar_full + 8 * s, (j / NS) & 1, kWaitLimitCycles);
+                if (!ok) return;
+                ptx::tc_fence_after();
+                const uint32_t kt = ring + s * SH::kStageBytes;
+                const uint32_t d = tmem + (j & 1) * kUmKeys;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint32_t off = (kk >> 2) * SH::kQBox + (kk & 3) * 32;
+                        const uint32_t koff = (kk >> 2) * (kUmKeys * 128) + (kk & 3) * 32;
+                        ptx::umma_bf16(d, ptx::umma_desc((part ? q_lo : q_hi) + off, 16, 1024),
+                                       ptx::umma_desc(kt + koff, 16, 1024), kIdS, part | kk);
+                    }
+                ptx::umma_commit(bar_s + 8 * (j & 1));
+            };
+            issue_s(0);
+            if (n_st > 1) issue_s(1);
+            for (int j = 0; j < n_st && ok; ++j) {
+                ok = ptx::mbar_wait(bar_p + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                // O += P_j hi . V_j + P_j lo . V_j; V_j: keys x dims, dims contiguous
+                const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
+                const uint32_t ph = pbuf + (j & 1) * 2 * SH::kPBytes;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int k2 = 0; k2 < kUmKeys / 16; ++k2)
+                        ptx::umma_bf16(t_o, ptx::umma_desc(ph + part * SH::kPBytes + k2 * 32, 16, 1024),
+                                       ptx::umma_desc(vt + k2 * 2048, kUmKeys * 128, 1024), kIdO,
+                                       (j > 0 || part > 0 || k2 > 0) ? 1u : 0u);
+                ptx::umma_commit(bar_pv + 8 * (j & 1));
+                ptx::umma_commit(bar_empty + 8 * (j % NS));  // the stage may be refilled
+                if (j + 2 < n_st) {
+                    ok = ptx::mbar_wait(bar_sfree + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_s(j + 2);
+                }
+            }
+            if (!ok) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+            // every MMA issued has completed before TMEM is freed
+            ptx::umma_commit(bar_drain);
+            if (!ptx::mbar_wait(bar_drain, 0, kWaitLimitCycles)) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax + epilogue
+        const int r = 32 * (warp & 3) + lane;  // this thread's row and TMEM lane
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const int R = r_first + r;
+        const bool row_ok = valid && R < rows;
+        const int kmax = L + R / p.G;  // the last key the row sees
+        const int kmin = p.window > 0 ? kmax - p.window + 1 : INT_MIN;
+        {
+            // q' row as bf16 hi / lo in the swizzled K-major tiles (zeros for a missing row)
+            const float* q = p.q_prime + (row_ok ? query_row(b, R, kvh, p.G, p.Hq, p.q_len) : 0) * D;
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) {
+                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                if (row_ok) {
+                    x0 = *reinterpret_cast<const float4*>(q + 8 * c);
+                    x1 = *reinterpret_cast<const float4*>(q + 8 * c + 4);
+                }
+                uint32_t h[4], l[4];
+                um_split(x0.x, x0.y, h[0], l[0]);
+                um_split(x0.z, x0.w, h[1], l[1]);
+                um_split(x1.x, x1.y, h[2], l[2]);
+                um_split(x1.z, x1.w, h[3], l[3]);
+                const uint32_t off = (c >> 3) * SH::kQBox + um_swz(r, c & 7);
+                ptx::st_shared_v4(q_hi + off, h[0], h[1], h[2], h[3]);
+                ptx::st_shared_v4(q_lo + off, l[0], l[1], l[2], l[3]);
+            }
+            ptx::fence_proxy_async();  // visible to the tensor core
+            ptx::mbar_arrive(bar_q);
+        }
+        const float cap2 = p.softcap_log2e;
+        float m = -INFINITY;  // the running maximum the P values are taken against
+        float l = 0.f;        // sum of P (relative to m)
+        bool ok = true;
+        // (tcgen05.ld / st are warp-wide: the branches around them are warp-uniform)
+        for (int j = 0; j < n_st; ++j) {
+            ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles));
+            ptx::tc_fence_after();
+            float x[kUmKeys];
+            {
+                uint32_t u[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (ok) {
+                        ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + 32 * h, u);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) u[i] = 0u;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[32 * h + i] = __uint_as_float(u[i]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_sfree + 8 * (j & 1));  // S buffer j % 2 may be overwritten
+
+            const int key0 = (kb0 + j) * kUmKeys;
+            const bool whole = row_ok && key0 + kUmKeys - 1 <= kmax && key0 >= kmin;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kUmKeys; ++i) {
+                float v = x[i];
+                if (cap2 > 0.f) v = tanhf(v) * cap2;
+                if (!whole && !(row_ok && key0 + i <= kmax && key0 + i >= kmin)) v = -INFINITY;
+                x[i] = v;
+                mx = fmaxf(mx, v);
+            }
+            // raise the reference maximum where a logit exceeds it by more than 2^8,
+            // rescaling what the row's O already holds
+            const bool raise = mx > m + 8.f;
+            const float f = raise ? ptx::ex2(m - mx) : 1.f;  // 0 while m = -inf
+            if (j > 0 && __any_sync(0xffffffffu, raise && m != -INFINITY)) {
+                ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
+                                                                  kWaitLimitCycles));
+                ptx::tc_fence_after();
+                if (ok) {
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t u[32];
+                            ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+                        ptx::tmem_st32(t_o + lane_addr + 32 * c, u);
+                    }
+                    ptx::tmem_wait_st();
+                }
+            }
+            if (raise) {
+                l *= f;
+                m = mx;
+            }
+            const float mu = m == -INFINITY ? 0.f : m;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < kUmKeys; ++i) {
+                x[i] = ptx::ex2(x[i] - mu);
+                sum += x[i];
+            }
+            l += sum;
+            // value rows of keys at or past the sequence's end (unused slots, or another
+            // head's rows) may hold anything, NaN included: zero them, as P is 0 there
+            const int v_keep = L_after - key0;
+            if (ok && v_keep < kUmKeys) {
+                const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
+                const int first = max(v_keep, 0), n_chunks = (kUmKeys - first) * SH::kBoxes * 8;
+                for (int i = r; i < n_chunks; i += 128) {
+                    const int row = first + i / (SH::kBoxes * 8), rem = i % (SH::kBoxes * 8);
+                    ptx::st_shared_v4(vt + (rem >> 3) * (kUmKeys * 128) + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
+                }
+            }
+            // P buffer j % 2 is free once P_{j-2} . V_{j-2} has completed
+            if (j >= 2)
+                ok = __all_sync(0xffffffffu,
+                                ok && ptx::mbar_wait(bar_pv + 8 * (j & 1), ((j - 2) >> 1) & 1, kWaitLimitCycles));
+            const uint32_t ph = pbuf + (j & 1) * 2 * SH::kPBytes;
+#pragma unroll
+            for (int c = 0; c < kUmKeys / 8; ++c) {
+                uint32_t h[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) um_split(x[8 * c + 2 * e], x[8 * c + 2 * e + 1], h[e], lw[e]);
+                ptx::st_shared_v4(ph + um_swz(r, c), h[0], h[1], h[2], h[3]);
+                ptx::st_shared_v4(ph + SH::kPBytes + um_swz(r, c), lw[0], lw[1], lw[2], lw[3]);
+            }
+            ptx::fence_proxy_async();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_p + 8 * (j & 1));
+        }
+        if (!ok && lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+
+        // ------------------------------------------------------------ the rows
+        // O is complete once the last P . V has (commits complete in order)
+        if (n_st > 0) {
+            ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv + 8 * ((n_st - 1) & 1), ((n_st - 1) >> 1) & 1,
+                                                              kWaitLimitCycles));
+            ptx::tc_fence_after();
+        }
+        {
+            const int hq = kvh * p.G + R % p.G;
+            const float z = p.sink ? p.sink[hq] * kLog2e : -INFINITY;
+            const float M = fmaxf(m, z);
+            float scale = 0.f;
+            if (M != -INFINITY) {
+                const float fm = m == -INFINITY ? 0.f : ptx::ex2(m - M);
+                const float den = l * fm + (z == -INFINITY ? 0.f : ptx::ex2(z - M));
+                scale = den > 0.f ? fm / den : 0.f;
+            }
+            if (!ok || n_st == 0) scale = 0.f;
+            const size_t row = query_row(b, R, kvh, p.G, p.Hq, p.q_len) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t u[32];
+                if (ok && n_st > 0) {
+                    ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u[i] = 0u;
+                }
+                if (R >= rows) continue;
+                if (p.out_dtype == UAA_DTYPE_F32) {
+                    float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        o[i] = make_float4(__uint_as_float(u[4 * i]) * scale, __uint_as_float(u[4 * i + 1]) * scale,
+                                           __uint_as_float(u[4 * i + 2]) * scale,
+                                           __uint_as_float(u[4 * i + 3]) * scale);
+                } else {
+                    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[i] = make_uint4(um_pack(__uint_as_float(u[8 * i]) * scale, __uint_as_float(u[8 * i + 1]) * scale),
+                                          um_pack(__uint_as_float(u[8 * i + 2]) * scale, __uint_as_float(u[8 * i + 3]) * scale),
+                                          um_pack(__uint_as_float(u[8 * i + 4]) * scale, __uint_as_float(u[8 * i + 5]) * scale),
+                                          um_pack(__uint_as_float(u[8 * i + 6]) * scale, __uint_as_float(u[8 * i + 7]) * scale));
+                }
+            }
+        }
+    }
+
+    // TMEM is freed by the warp that allocated it, after every reader and the MMAs are done
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kUmTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_um(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s)
+{
+    using SH = UmShape<D>;
+    static_assert(SH::kSmemBytes <= 232448, "shared memory of the prefill kernel");
+    auto kern = prefill_umma_kernel<D>;
+    static int configured_device_mask = 0;  // bit per device that has the smem attribute set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 31 || !(configured_device_mask & (1 << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev < 31) configured_device_mask |= 1 << dev;
+    }
+    const long long n_rb = (static_cast<long long>(p.q_len) * p.G + kUmRows - 1) / kUmRows;
+    const long long ctas = static_cast<long long>(p.B) * p.Hkv * n_rb;
+    if (ctas == 0) return cudaSuccess;
+    if (ctas > 2147483647LL) return cudaErrorInvalidConfiguration;
+    return launch_dependent(kern, dim3(static_cast<unsigned>(ctas)), dim3(kUmThreads), SH::kSmemBytes, s, tk, tv, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_umma(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s)
+{
+    switch (p.D) {
+    case 64: return launch_um<64>(p, tk, tv, s);
+    case 128: return launch_um<128>(p, tk, tv, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace uaa
