@@ -16,22 +16,25 @@
 //   S_j (128 x 64, fp32 in TMEM) = Q' . K_j^T, Q' = the q' rows (fp32, rotated
 //     and prescaled by the append) as bf16 hi + lo parts (two MMAs per
 //     k-step), K_j as it sits in the TMA ring (keys x dims, 128-byte swizzle);
-//   softmax: thread r of the four softmax warps owns row r (TMEM lane r): it
-//     reads S_j, applies softcap and the causal / window masks, and keeps a
-//     running maximum m that it raises only when a logit exceeds it by more
+//   softmax: two threads own row r (TMEM lane r), one per 32-key half: they
+//     read S_j, apply softcap and the causal / window masks, and keep a
+//     running maximum m that they raise only when a logit exceeds it by more
 //     than 2^8 (exp2(s - m) <= 256 otherwise; the final division cancels m),
-//     rescaling its O row in TMEM then; P_j = exp2(S_j - m) goes to shared
-//     memory as bf16 hi + lo parts;
-//   O (128 x D, fp32 in TMEM) += P_j . V_j, V_j straight from the ring (keys x
-//     dims: N-contiguous).
-// S is double-buffered in TMEM and P in shared memory, so the softmax of block
-// j + 1 runs while the tensor core computes P_j . V_j and S_{j+2}.
+//     rescaling the O row in TMEM then; P_j = exp2(S_j - m) goes back to TMEM
+//     as bf16 hi + lo parts;
+//   O (128 x D, fp32 in TMEM) += P_j . V_j, P_j the MMA's A operand in TMEM,
+//     V_j straight from the ring (keys x dims: N-contiguous).
+// S and P are double-buffered in TMEM: the MMA warp issues S_{j+2} as soon as
+// the softmax has read S_j, and P_j . V_j once P_j is written, so the tensor
+// core works on S_{j+2} and P_j . V_j while the softmax takes block j + 1.
+// Shared memory holds q' and a ring of five 64-key stages (eight at head_dim 64).
 //
-// Warps (192 threads, one CTA per SM): warp 0 lane 0 issues the TMA loads of
-// the key and value tiles into a ring of stages (full / empty mbarriers; the
-// MMA's commit frees a stage); warp 1 allocates TMEM and its lane 0 issues every
-// MMA; warps 2-5 stage the q' rows and run the softmax and the epilogue. Every
-// wait is bounded: a wait that gives up sets UAA_DEVFLAG_TIMEOUT, the thread
+// Warps (320 threads, one CTA per SM): warp 0 lane 0 issues the TMA loads of
+// the key and value tiles into the ring (full / empty mbarriers; the MMA's
+// commit frees a stage); warp 1 allocates TMEM and its lane 0 issues every MMA;
+// warps 2-9 stage the q' rows and run the softmax and the epilogue, two warps
+// per row (one per key half of a block and per half of O's columns), which
+// exchange row maxima and sums through shared memory. Every wait is bounded: a wait that gives up sets UAA_DEVFLAG_TIMEOUT, the thread
 // stops waiting from then on, and the CTA still drains its copies and MMAs and
 // frees its TMEM before it exits.
 #include "internal.cuh"
@@ -42,8 +45,10 @@ namespace {
 
 constexpr int kUmRows = kPrefillRows;  // query rows per CTA (M of the MMAs)
 constexpr int kUmKeys = 64;            // keys per block (N of S, K of P . V)
-constexpr int kUmThreads = 192;
-constexpr uint32_t kUmTmemCols = 256;  // S[2] (64 columns each) + O (D columns)
+constexpr int kUmThreads = 320;       // TMA warp, MMA warp, 8 softmax warps
+constexpr uint32_t kUmTmemCols = 512;  // S[2] (64 columns each), O (D columns), P[2] (hi + lo: 64 columns each)
+constexpr uint32_t kUmOCol = 2 * kUmKeys;  // O's first column
+constexpr uint32_t kUmPCol = 256;          // P[b] at 256 + 64 b: hi in the first 32 columns, lo in the next
 
 template <int D>
 struct UmShape {
@@ -52,13 +57,11 @@ struct UmShape {
     static constexpr int kQBytes = kBoxes * kQBox;        // Q' hi (or lo)
     static constexpr int kKV = kUmKeys * D * 2;           // the keys (or values) of a stage
     static constexpr int kStageBytes = 2 * kKV;
-    static constexpr int kStages = D == 128 ? 3 : 4;
-    static constexpr int kPBytes = kUmRows * kUmKeys * 2; // P hi (or lo) of one block: 16 KB
+    static constexpr int kStages = D == 128 ? 5 : 8;
     static constexpr int kOffQlo = kQBytes;
     static constexpr int kOffRing = 2 * kQBytes;
-    static constexpr int kOffP = kOffRing + kStages * kStageBytes;  // P[2]: hi, lo
-    static constexpr int kOffBar = kOffP + 4 * kPBytes;
-    static constexpr int kSmemBytes = 1024 + kOffBar + 256;
+    static constexpr int kOffBar = kOffRing + kStages * kStageBytes;  // barriers, TMEM address, row exchange
+    static constexpr int kSmemBytes = 1024 + kOffBar + 256 + 2 * 4 * kUmRows;
 };
 
 __device__ __forceinline__ uint32_t um_pack(float lo, float hi)
@@ -88,22 +91,25 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 {
     using SH = UmShape<D>;
     constexpr int NS = SH::kStages;
-    constexpr int KS = D / 16;  // k-steps of Q'.K^T
+    constexpr int KS = D / 16;       // k-steps of Q'.K^T
+    constexpr int KH = kUmKeys / 2;  // keys per softmax thread and block
     constexpr uint32_t kIdS = ptx::umma_idesc_bf16(kUmRows, kUmKeys, false, false);
     constexpr uint32_t kIdO = ptx::umma_idesc_bf16(kUmRows, D, false, true);
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t q_hi = base, q_lo = base + SH::kOffQlo, ring = base + SH::kOffRing, pbuf = base + SH::kOffP;
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t q_hi = base, q_lo = base + SH::kOffQlo, ring = base + SH::kOffRing;
     const uint32_t bars = base + SH::kOffBar;
     const uint32_t bar_full = bars, bar_empty = bars + 8 * NS;
-    const uint32_t bar_q = bars + 16 * NS;        // q' rows staged (128 arrivals)
+    const uint32_t bar_q = bars + 16 * NS;        // q' rows staged (256 arrivals)
     const uint32_t bar_s = bar_q + 8;             // [2] S_j in TMEM (MMA commit)
-    const uint32_t bar_sfree = bar_s + 16;        // [2] S_j read (128 arrivals)
-    const uint32_t bar_p = bar_sfree + 16;        // [2] P_j in shared memory (128 arrivals)
+    const uint32_t bar_sfree = bar_s + 16;        // [2] S_j read (256 arrivals)
+    const uint32_t bar_p = bar_sfree + 16;        // [2] P_j in TMEM (256 arrivals)
     const uint32_t bar_pv = bar_p + 16;           // [2] P_j . V_j done (MMA commit)
     const uint32_t bar_drain = bar_pv + 16;       // every MMA done (MMA commit)
     const uint32_t tmem_slot = bar_drain + 8;
-    uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (tmem_slot - ptx::smem_u32(smem_raw)));
+    uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (tmem_slot - raw));
+    float* xch = reinterpret_cast<float*>(smem_raw + (bars + 256 - raw));  // [2][128]: the warp pairs' row maxima / sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows = p.q_len * p.G;  // query rows of the kv head
@@ -117,11 +123,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             ptx::mbar_init(bar_full + 8 * s, 1);
             ptx::mbar_init(bar_empty + 8 * s, 1);
         }
-        ptx::mbar_init(bar_q, 128);
+        ptx::mbar_init(bar_q, 256);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_s + 8 * i, 1);
-            ptx::mbar_init(bar_sfree + 8 * i, 128);
-            ptx::mbar_init(bar_p + 8 * i, 128);
+            ptx::mbar_init(bar_sfree + 8 * i, 256);
+            ptx::mbar_init(bar_p + 8 * i, 256);
             ptx::mbar_init(bar_pv + 8 * i, 1);
         }
         ptx::mbar_init(bar_drain, 1);
@@ -138,7 +144,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     __syncthreads();         // barriers initialised, TMEM allocated
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot_ptr;
-    const uint32_t t_o = tmem + 2 * kUmKeys;  // O: columns 128 ..
+    const uint32_t t_o = tmem + kUmOCol;
 
     // The chunk's tokens sit at L .. L + q_len - 1 (the append advanced the length
     // past them); a sequence the append could not take keeps its length and gets zero rows.
@@ -206,27 +212,29 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             issue_s(0);
             if (n_st > 1) issue_s(1);
             for (int j = 0; j < n_st && ok; ++j) {
-                ok = ptx::mbar_wait(bar_p + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                // O += P_j hi . V_j + P_j lo . V_j; V_j: keys x dims, dims contiguous
-                const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
-                const uint32_t ph = pbuf + (j & 1) * 2 * SH::kPBytes;
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int k2 = 0; k2 < kUmKeys / 16; ++k2)
-                        ptx::umma_bf16(t_o, ptx::umma_desc(ph + part * SH::kPBytes + k2 * 32, 16, 1024),
-                                       ptx::umma_desc(vt + k2 * 2048, kUmKeys * 128, 1024), kIdO,
-                                       (j > 0 || part > 0 || k2 > 0) ? 1u : 0u);
-                ptx::umma_commit(bar_pv + 8 * (j & 1));
-                ptx::umma_commit(bar_empty + 8 * (j % NS));  // the stage may be refilled
-                if (j + 2 < n_st) {
+                if (j + 2 < n_st) {  // S buffer j % 2 is free once the softmax has read S_j
                     ok = ptx::mbar_wait(bar_sfree + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
                     if (!ok) break;
                     ptx::tc_fence_after();
                     issue_s(j + 2);
+                    if (!ok) break;
                 }
+                ok = ptx::mbar_wait(bar_p + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                // O += P_j hi . V_j + P_j lo . V_j; P_j from TMEM (8 columns per 16 keys),
+                // V_j: keys x dims, dims contiguous
+                const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
+                const uint32_t tp = tmem + kUmPCol + (j & 1) * kUmKeys;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int k2 = 0; k2 < kUmKeys / 16; ++k2)
+                        ptx::umma_bf16_ts(t_o, tp + part * (kUmKeys / 2) + k2 * 8,
+                                          ptx::umma_desc(vt + k2 * 2048, kUmKeys * 128, 1024), kIdO,
+                                          (j > 0 || part > 0 || k2 > 0) ? 1u : 0u);
+                ptx::umma_commit(bar_pv + 8 * (j & 1));
+                ptx::umma_commit(bar_empty + 8 * (j % NS));  // the stage may be refilled
             }
             if (!ok) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             // every MMA issued has completed before TMEM is freed
@@ -235,74 +243,96 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
-        const int r = 32 * (warp & 3) + lane;  // this thread's row and TMEM lane
-        const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        // Warp w (2 <= w < 10) takes rows 32 (w % 4) .. + 31 (its TMEM lanes) and key
+        // half h = (w - 2) / 4 of each block (32 columns of S), so two warps share
+        // every SM sub-partition's softmax work. The pair exchanges row maxima
+        // through shared memory and a named barrier, and its partial sums at the end.
+        const int h = (warp - 2) >> 2;           // key half of a block, and half of O's columns
+        const int quad = warp & 3;
+        const int r = 32 * quad + lane;          // this thread's row and TMEM lane
+        const int tid = 32 * (warp - 2) + lane;  // 0 .. 255
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
+        const int pair_bar = 1 + quad;           // named barrier of the warp pair (64 threads)
         const int R = r_first + r;
         const bool row_ok = valid && R < rows;
         const int kmax = L + R / p.G;  // the last key the row sees
         const int kmin = p.window > 0 ? kmax - p.window + 1 : INT_MIN;
         {
-            // q' row as bf16 hi / lo in the swizzled K-major tiles (zeros for a missing row)
+            // q' row (this thread: half of its dims) as bf16 hi / lo in the swizzled
+            // K-major tiles (zeros for a missing row)
             const float* q = p.q_prime + (row_ok ? query_row(b, R, kvh, p.G, p.Hq, p.q_len) : 0) * D;
 #pragma unroll 4
-            for (int c = 0; c < D / 8; ++c) {
+            for (int c = h * (D / 16); c < (h + 1) * (D / 16); ++c) {
                 float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
                 if (row_ok) {
                     x0 = *reinterpret_cast<const float4*>(q + 8 * c);
                     x1 = *reinterpret_cast<const float4*>(q + 8 * c + 4);
                 }
-                uint32_t h[4], l[4];
-                um_split(x0.x, x0.y, h[0], l[0]);
-                um_split(x0.z, x0.w, h[1], l[1]);
-                um_split(x1.x, x1.y, h[2], l[2]);
-                um_split(x1.z, x1.w, h[3], l[3]);
+                uint32_t hh[4], ll[4];
+                um_split(x0.x, x0.y, hh[0], ll[0]);
+                um_split(x0.z, x0.w, hh[1], ll[1]);
+                um_split(x1.x, x1.y, hh[2], ll[2]);
+                um_split(x1.z, x1.w, hh[3], ll[3]);
                 const uint32_t off = (c >> 3) * SH::kQBox + um_swz(r, c & 7);
-                ptx::st_shared_v4(q_hi + off, h[0], h[1], h[2], h[3]);
-                ptx::st_shared_v4(q_lo + off, l[0], l[1], l[2], l[3]);
+                ptx::st_shared_v4(q_hi + off, hh[0], hh[1], hh[2], hh[3]);
+                ptx::st_shared_v4(q_lo + off, ll[0], ll[1], ll[2], ll[3]);
             }
             ptx::fence_proxy_async();  // visible to the tensor core
             ptx::mbar_arrive(bar_q);
         }
         const float cap2 = p.softcap_log2e;
-        float m = -INFINITY;  // the running maximum the P values are taken against
-        float l = 0.f;        // sum of P (relative to m)
+        float m = -INFINITY;  // the running maximum the P values are taken against (the same in both warps)
+        float l = 0.f;        // this half's sum of P (relative to m)
         bool ok = true;
         // (tcgen05.ld / st are warp-wide: the branches around them are warp-uniform)
         for (int j = 0; j < n_st; ++j) {
             ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles));
             ptx::tc_fence_after();
-            float x[kUmKeys];
+            float x[KH];
             {
                 uint32_t u[32];
+                if (ok) {
+                    ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + KH * h, u);
+                    ptx::tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (ok) {
-                        ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + 32 * h, u);
-                        ptx::tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) u[i] = 0u;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[32 * h + i] = __uint_as_float(u[i]);
+                    for (int i = 0; i < 32; ++i) u[i] = 0u;
                 }
+#pragma unroll
+                for (int i = 0; i < KH; ++i) x[i] = __uint_as_float(u[i]);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_sfree + 8 * (j & 1));  // S buffer j % 2 may be overwritten
 
-            const int key0 = (kb0 + j) * kUmKeys;
-            const bool whole = row_ok && key0 + kUmKeys - 1 <= kmax && key0 >= kmin;
-            float mx = -INFINITY;
+            const int key0 = (kb0 + j) * kUmKeys + KH * h;  // this thread's first key
+            if (cap2 > 0.f) {
 #pragma unroll
-            for (int i = 0; i < kUmKeys; ++i) {
-                float v = x[i];
-                if (cap2 > 0.f) v = tanhf(v) * cap2;
-                if (!whole && !(row_ok && key0 + i <= kmax && key0 + i >= kmin)) v = -INFINITY;
-                x[i] = v;
-                mx = fmaxf(mx, v);
+                for (int i = 0; i < KH; ++i) x[i] = tanhf(x[i]) * cap2;
             }
+            if (!(row_ok && key0 + KH - 1 <= kmax && key0 >= kmin)) {  // some keys masked
+                const int i_lo = !row_ok ? KH : (p.window > 0 ? kmin - key0 : 0), i_hi = row_ok ? kmax - key0 : -1;
+#pragma unroll
+                for (int i = 0; i < KH; ++i)
+                    if (i < i_lo || i > i_hi) x[i] = -INFINITY;
+            }
+            float mh;
+            {
+                float t8[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) t8[a] = fmaxf(fmaxf(x[a], x[a + 8]), fmaxf(x[a + 16], x[a + 24]));
+#pragma unroll
+                for (int a = 0; a < 4; ++a) t8[a] = fmaxf(t8[a], t8[a + 4]);
+                mh = fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]));
+            }
+            // the row's maximum over both halves (the second barrier: both have read
+            // before either writes again)
+            xch[h * kUmRows + r] = mh;
+            ptx::named_barrier_sync(pair_bar, 64);
+            const float mx = fmaxf(mh, xch[(h ^ 1) * kUmRows + r]);
+            ptx::named_barrier_sync(pair_bar, 64);
+
             // raise the reference maximum where a logit exceeds it by more than 2^8,
-            // rescaling what the row's O already holds
+            // rescaling what the row's O already holds (this warp: its half of the columns)
             const bool raise = mx > m + 8.f;
             const float f = raise ? ptx::ex2(m - mx) : 1.f;  // 0 while m = -inf
             if (j > 0 && __any_sync(0xffffffffu, raise && m != -INFINITY)) {
@@ -311,12 +341,12 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 ptx::tc_fence_after();
                 if (ok) {
 #pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t u[32];
-                            ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
-                            ptx::tmem_wait_ld();
+                    for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
+                        uint32_t u[32];
+                        ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+                        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
                         ptx::tmem_st32(t_o + lane_addr + 32 * c, u);
                     }
                     ptx::tmem_wait_st();
@@ -327,44 +357,51 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 m = mx;
             }
             const float mu = m == -INFINITY ? 0.f : m;
-            float sum = 0.f;
+            {
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < kUmKeys; ++i) {
-                x[i] = ptx::ex2(x[i] - mu);
-                sum += x[i];
+                for (int i = 0; i < KH; ++i) {
+                    x[i] = ptx::ex2(x[i] - mu);
+                    s4[i & 3] += x[i];
+                }
+                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
-            l += sum;
             // value rows of keys at or past the sequence's end (unused slots, or another
             // head's rows) may hold anything, NaN included: zero them, as P is 0 there
-            const int v_keep = L_after - key0;
-            if (ok && v_keep < kUmKeys) {
+            const int v_keep = L_after - (kb0 + j) * kUmKeys;
+            if (v_keep < kUmKeys) {
                 const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
                 const int first = max(v_keep, 0), n_chunks = (kUmKeys - first) * SH::kBoxes * 8;
-                for (int i = r; i < n_chunks; i += 128) {
+                for (int i = tid; i < n_chunks; i += 256) {
                     const int row = first + i / (SH::kBoxes * 8), rem = i % (SH::kBoxes * 8);
                     ptx::st_shared_v4(vt + (rem >> 3) * (kUmKeys * 128) + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
                 }
+                ptx::fence_proxy_async();  // visible to the tensor core
             }
-            // P buffer j % 2 is free once P_{j-2} . V_{j-2} has completed
+            // P buffer j % 2 (TMEM) is free once P_{j-2} . V_{j-2} has completed
             if (j >= 2)
                 ok = __all_sync(0xffffffffu,
                                 ok && ptx::mbar_wait(bar_pv + 8 * (j & 1), ((j - 2) >> 1) & 1, kWaitLimitCycles));
-            const uint32_t ph = pbuf + (j & 1) * 2 * SH::kPBytes;
+            // P_j (this thread: keys 32 h .. + 31 of its row) as bf16 hi / lo pairs into TMEM
+            if (ok) {
+                uint32_t hh[KH / 2], lw[KH / 2];
 #pragma unroll
-            for (int c = 0; c < kUmKeys / 8; ++c) {
-                uint32_t h[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) um_split(x[8 * c + 2 * e], x[8 * c + 2 * e + 1], h[e], lw[e]);
-                ptx::st_shared_v4(ph + um_swz(r, c), h[0], h[1], h[2], h[3]);
-                ptx::st_shared_v4(ph + SH::kPBytes + um_swz(r, c), lw[0], lw[1], lw[2], lw[3]);
+                for (int e = 0; e < KH / 2; ++e) um_split(x[2 * e], x[2 * e + 1], hh[e], lw[e]);
+                const uint32_t tp = tmem + lane_addr + kUmPCol + (j & 1) * kUmKeys + (KH / 2) * h;
+                ptx::tmem_st16(tp, hh);
+                ptx::tmem_st16(tp + kUmKeys / 2, lw);
+                ptx::tmem_wait_st();
             }
-            ptx::fence_proxy_async();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_p + 8 * (j & 1));
         }
         if (!ok && lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
 
         // ------------------------------------------------------------ the rows
+        // the row's sum over both halves
+        xch[h * kUmRows + r] = l;
+        ptx::named_barrier_sync(pair_bar, 64);
+        l += xch[(h ^ 1) * kUmRows + r];
         // O is complete once the last P . V has (commits complete in order)
         if (n_st > 0) {
             ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv + 8 * ((n_st - 1) & 1), ((n_st - 1) >> 1) & 1,
@@ -384,7 +421,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             if (!ok || n_st == 0) scale = 0.f;
             const size_t row = query_row(b, R, kvh, p.G, p.Hq, p.q_len) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
                 uint32_t u[32];
                 if (ok && n_st > 0) {
                     ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
