@@ -466,9 +466,9 @@ uaa_status run_prefill(const uaa_attn_desc* d, const uaa_step_args* a, const uaa
     const uint64_t rows = (uint64_t)a->batch * d->n_kv_heads * a->cache_capacity;
     CUtensorMap tk, tv;
     UAA_TRY(encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->k_cache, D, rows, D * 2, 64,
-                      (uint32_t)uaa::kTileKeys, CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
+                      (uint32_t)uaa::kPrefillKeys, CU_TENSOR_MAP_SWIZZLE_128B, "k_cache"));
     UAA_TRY(encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->v_cache, D, rows, D * 2, 64,
-                      (uint32_t)uaa::kTileKeys, CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
+                      (uint32_t)uaa::kPrefillKeys, CU_TENSOR_MAP_SWIZZLE_128B, "v_cache"));
     uaa::PrefillParams p{};
     p.B = a->batch;
     p.Hq = d->n_q_heads;

@@ -248,10 +248,11 @@ struct PartialMaps {
 cudaError_t launch_partial_tc(const PartialParams& p, const PartialMaps& m, int kv_dtype, int n_head_tiles,
                               int n_ctas, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
-// tk, tv: tensor maps of the key and value caches with boxes of 64 rows x 64 columns.
+// tk, tv: tensor maps of the key and value caches with boxes of kPrefillKeys rows x 64 columns.
 cudaError_t launch_prefill_umma(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-// Query rows per CTA of the prefill kernel.
+// Query rows per CTA of the prefill kernel, and keys per block (the height of its TMA boxes).
 constexpr int kPrefillRows = 128;
+constexpr int kPrefillKeys = 128;
 cudaError_t launch_step_f32(const StepF32Params& p, cudaStream_t s);
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
                                 float* scales, cudaStream_t s);

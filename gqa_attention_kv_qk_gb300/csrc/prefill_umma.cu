@@ -7,36 +7,39 @@
 // query head r % G of the group, as in query_row) are cut into blocks of 128.
 // One CTA per (sequence, kv head, row block) streams the keys its rows see (the
 // cache and the chunk's tokens up to the block's last one, within the window)
-// once, 64 keys per block, and writes the block's output rows itself: no
+// once, 128 keys per block, and writes the block's output rows itself: no
 // records, no combine. The row blocks of one kv head are neighbours in the
 // grid, so they read the same tiles at about the same time and HBM delivers
 // each tile about once.
 //
-// Per 64-key block j, with M = 128 rows on the tensor core:
-//   S_j (128 x 64, fp32 in TMEM) = Q' . K_j^T, Q' = the q' rows (fp32, rotated
-//     and prescaled by the append) as bf16 hi + lo parts (two MMAs per
-//     k-step), K_j as it sits in the TMA ring (keys x dims, 128-byte swizzle);
-//   softmax: two threads own row r (TMEM lane r), one per 32-key half: they
+// Per 128-key block j, with M = 128 rows and N = 128 on the tensor core (the
+// shape it runs at full rate; N = 64 takes half again as long per flop):
+//   S_j (128 x 128, fp32 in TMEM) = Q' . K_j^T, Q' = the q' rows (fp32, rotated
+//     and prescaled by the append) as bf16 hi + lo parts in shared memory (two
+//     MMAs per k-step, back to back on the same K chunk), K_j as the TMA
+//     wrote it (keys x dims, 128-byte swizzle);
+//   softmax: two threads own row r (TMEM lane r), one per 64-key half: they
 //     read S_j, apply softcap and the causal / window masks, and keep a
 //     running maximum m that they raise only when a logit exceeds it by more
 //     than 2^8 (exp2(s - m) <= 256 otherwise; the final division cancels m),
 //     rescaling the O row in TMEM then; P_j = exp2(S_j - m) goes back to TMEM
 //     as bf16 hi + lo parts;
 //   O (128 x D, fp32 in TMEM) += P_j . V_j, P_j the MMA's A operand in TMEM,
-//     V_j straight from the ring (keys x dims: N-contiguous).
-// S and P are double-buffered in TMEM: the MMA warp issues S_{j+2} as soon as
-// the softmax has read S_j, and P_j . V_j once P_j is written, so the tensor
-// core works on S_{j+2} and P_j . V_j while the softmax takes block j + 1.
-// Shared memory holds q' and a ring of five 64-key stages (eight at head_dim 64).
+//     V_j as the TMA wrote it (keys x dims: N-contiguous).
+// S is double-buffered in TMEM: the MMA warp issues S_{j+2} as soon as the
+// softmax has read S_j, so the tensor core computes it while the softmax
+// works; P (one buffer) is written once P_{j-1} . V_{j-1} has completed. Keys
+// and values have rings of their own (a key tile is free once its S is done, a
+// value tile once its P . V is).
 //
-// Warps (320 threads, one CTA per SM): warp 0 lane 0 issues the TMA loads of
-// the key and value tiles into the ring (full / empty mbarriers; the MMA's
-// commit frees a stage); warp 1 allocates TMEM and its lane 0 issues every MMA;
-// warps 2-9 stage the q' rows and run the softmax and the epilogue, two warps
-// per row (one per key half of a block and per half of O's columns), which
-// exchange row maxima and sums through shared memory. Every wait is bounded: a wait that gives up sets UAA_DEVFLAG_TIMEOUT, the thread
-// stops waiting from then on, and the CTA still drains its copies and MMAs and
-// frees its TMEM before it exits.
+// Warps (320 threads, one CTA per SM): warp 0 issues the TMA loads (lane 0 the
+// keys, lane 1 the values; full / empty mbarriers, the MMA's commits free the
+// slots); warp 1 allocates TMEM and its lane 0 issues every MMA; warps 2-9
+// stage the q' rows and run the softmax and the epilogue, two warps per row
+// (one per key half of a block and per half of O's columns), which exchange row
+// maxima and sums through shared memory. Every wait is bounded: a wait that
+// gives up sets UAA_DEVFLAG_TIMEOUT, the thread stops waiting from then on, and
+// the CTA still drains its copies and MMAs and frees its TMEM before it exits.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -44,24 +47,29 @@ namespace uaa {
 namespace {
 
 constexpr int kUmRows = kPrefillRows;  // query rows per CTA (M of the MMAs)
-constexpr int kUmKeys = 64;            // keys per block (N of S, K of P . V)
-constexpr int kUmThreads = 320;       // TMA warp, MMA warp, 8 softmax warps
-constexpr uint32_t kUmTmemCols = 512;  // S[2] (64 columns each), O (D columns), P[2] (hi + lo: 64 columns each)
-constexpr uint32_t kUmOCol = 2 * kUmKeys;  // O's first column
-constexpr uint32_t kUmPCol = 256;          // P[b] at 256 + 64 b: hi in the first 32 columns, lo in the next
+constexpr int kUmKeys = kPrefillKeys;  // keys per block (N of S, K of P . V)
+constexpr int kUmThreads = 320;        // TMA warp, MMA warp, 8 softmax warps
+// TMEM columns: S[b] at 128 b; P at 256 (bf16 hi in the first 64 columns, lo
+// in the next 64); O at 384 (D columns)
+constexpr uint32_t kUmTmemCols = 512;
+constexpr uint32_t kUmPCol = 256;
+constexpr uint32_t kUmOCol = 384;
 
 template <int D>
 struct UmShape {
-    static constexpr int kBoxes = D / 64;                 // 64-dim boxes of a row
-    static constexpr int kQBox = kUmRows * 128;           // 128 rows of one box: 16 KB
-    static constexpr int kQBytes = kBoxes * kQBox;        // Q' hi (or lo)
-    static constexpr int kKV = kUmKeys * D * 2;           // the keys (or values) of a stage
-    static constexpr int kStageBytes = 2 * kKV;
-    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kBoxes = D / 64;                  // 64-dim boxes of a row
+    static constexpr int kQBox = kUmRows * 128;            // 128 rows of one box: 16 KB
+    static constexpr int kQBytes = kBoxes * kQBox;         // Q' hi (or lo)
+    static constexpr int kTile = kUmKeys * D * 2;          // the keys (or values) of a block
+    static constexpr int kKSlots = D == 128 ? 3 : 5;
+    static constexpr int kVSlots = D == 128 ? 2 : 5;
     static constexpr int kOffQlo = kQBytes;
-    static constexpr int kOffRing = 2 * kQBytes;
-    static constexpr int kOffBar = kOffRing + kStages * kStageBytes;  // barriers, TMEM address, row exchange
-    static constexpr int kSmemBytes = 1024 + kOffBar + 256 + 2 * 4 * kUmRows;
+    static constexpr int kOffK = 2 * kQBytes;
+    static constexpr int kOffV = kOffK + kKSlots * kTile;
+    static constexpr int kOffBar = kOffV + kVSlots * kTile;  // barriers and the TMEM address: 256 bytes
+    static constexpr int kOffXch = kOffBar + 256;             // the warp pairs' row exchange: [2][128] floats
+    static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 4 * kUmRows;
+    static_assert(16 * (kKSlots + kVSlots) + 80 <= 256, "barrier area");
 };
 
 __device__ __forceinline__ uint32_t um_pack(float lo, float hi)
@@ -90,7 +98,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const PrefillParams p)
 {
     using SH = UmShape<D>;
-    constexpr int NS = SH::kStages;
+    constexpr int NK = SH::kKSlots, NV = SH::kVSlots;
     constexpr int KS = D / 16;       // k-steps of Q'.K^T
     constexpr int KH = kUmKeys / 2;  // keys per softmax thread and block
     constexpr uint32_t kIdS = ptx::umma_idesc_bf16(kUmRows, kUmKeys, false, false);
@@ -98,18 +106,19 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t q_hi = base, q_lo = base + SH::kOffQlo, ring = base + SH::kOffRing;
+    const uint32_t q_hi = base, q_lo = base + SH::kOffQlo, kring = base + SH::kOffK, vring = base + SH::kOffV;
     const uint32_t bars = base + SH::kOffBar;
-    const uint32_t bar_full = bars, bar_empty = bars + 8 * NS;
-    const uint32_t bar_q = bars + 16 * NS;        // q' rows staged (256 arrivals)
-    const uint32_t bar_s = bar_q + 8;             // [2] S_j in TMEM (MMA commit)
-    const uint32_t bar_sfree = bar_s + 16;        // [2] S_j read (256 arrivals)
-    const uint32_t bar_p = bar_sfree + 16;        // [2] P_j in TMEM (256 arrivals)
-    const uint32_t bar_pv = bar_p + 16;           // [2] P_j . V_j done (MMA commit)
-    const uint32_t bar_drain = bar_pv + 16;       // every MMA done (MMA commit)
+    const uint32_t bar_kfull = bars, bar_kempty = bars + 8 * NK;
+    const uint32_t bar_vfull = bars + 16 * NK, bar_vempty = bar_vfull + 8 * NV;
+    const uint32_t bar_q = bar_vempty + 8 * NV;  // q' rows staged (256 arrivals)
+    const uint32_t bar_s = bar_q + 8;            // [2] S_j in TMEM (MMA commit)
+    const uint32_t bar_sfree = bar_s + 16;       // [2] S_j read (256 arrivals)
+    const uint32_t bar_p = bar_sfree + 16;       // P_j in TMEM (256 arrivals)
+    const uint32_t bar_pv = bar_p + 8;           // P_j . V_j done (MMA commit)
+    const uint32_t bar_drain = bar_pv + 8;       // every MMA done (MMA commit)
     const uint32_t tmem_slot = bar_drain + 8;
     uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (tmem_slot - raw));
-    float* xch = reinterpret_cast<float*>(smem_raw + (bars + 256 - raw));  // [2][128]: the warp pairs' row maxima / sums
+    float* xch = reinterpret_cast<float*>(smem_raw + (base + SH::kOffXch - raw));  // [2][128]: row maxima / sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows = p.q_len * p.G;  // query rows of the kv head
@@ -119,17 +128,21 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, 1);
+        for (int s = 0; s < NK; ++s) {
+            ptx::mbar_init(bar_kfull + 8 * s, 1);
+            ptx::mbar_init(bar_kempty + 8 * s, 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            ptx::mbar_init(bar_vfull + 8 * s, 1);
+            ptx::mbar_init(bar_vempty + 8 * s, 1);
         }
         ptx::mbar_init(bar_q, 256);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_s + 8 * i, 1);
             ptx::mbar_init(bar_sfree + 8 * i, 256);
-            ptx::mbar_init(bar_p + 8 * i, 256);
-            ptx::mbar_init(bar_pv + 8 * i, 1);
         }
+        ptx::mbar_init(bar_p, 256);
+        ptx::mbar_init(bar_pv, 1);
         ptx::mbar_init(bar_drain, 1);
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_k);
@@ -158,29 +171,32 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int n_st = (hi + kUmKeys - 1) / kUmKeys - kb0;  // key blocks
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0 && n_st > 0) {
+        // ---------------------------------------------------------------- TMA producers
+        // lane 0: key tiles into the key ring; lane 1: value tiles into the value ring
+        if (lane < 2 && n_st > 0) {
+            const bool is_v = lane == 1;
+            const int NSL = is_v ? NV : NK;
+            const uint32_t ring = is_v ? vring : kring;
+            const uint32_t full = is_v ? bar_vfull : bar_kfull, empty = is_v ? bar_vempty : bar_kempty;
+            const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
             const int row0 = (b * p.Hkv + kvh) * p.cap + kb0 * kUmKeys;
             int issued = 0;
             for (int i = 0; i < n_st; ++i) {
-                const int s = i % NS;
-                if (i >= NS && !ptx::mbar_wait(bar_empty + 8 * s, ((i / NS) - 1) & 1, kWaitLimitCycles)) {
+                const int s = i % NSL;
+                if (i >= NSL && !ptx::mbar_wait(empty + 8 * s, ((i / NSL) - 1) & 1, kWaitLimitCycles)) {
                     atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
                     break;
                 }
-                const uint32_t st = ring + s * SH::kStageBytes, bar = bar_full + 8 * s;
-                ptx::mbar_arrive_expect_tx(bar, SH::kStageBytes);
+                const uint32_t st = ring + s * SH::kTile, bar = full + 8 * s;
+                ptx::mbar_arrive_expect_tx(bar, SH::kTile);
 #pragma unroll
-                for (int c = 0; c < SH::kBoxes; ++c) {
-                    // plain loads: the other row blocks of this kv head read the same tiles from L2
-                    ptx::tma_load_2d(st + c * (kUmKeys * 128), &tm_k, c * 64, row0 + i * kUmKeys, bar);
-                    ptx::tma_load_2d(st + SH::kKV + c * (kUmKeys * 128), &tm_v, c * 64, row0 + i * kUmKeys, bar);
-                }
+                for (int c = 0; c < SH::kBoxes; ++c)  // plain loads: the other row blocks read the same tiles from L2
+                    ptx::tma_load_2d(st + c * (kUmKeys * 128), tm, c * 64, row0 + i * kUmKeys, bar);
                 issued = i + 1;
             }
             // every issued copy lands before the CTA may exit
-            for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
-                if (!ptx::mbar_wait(bar_full + 8 * (i % NS), (i / NS) & 1, kWaitLimitCycles)) {
+            for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
+                if (!ptx::mbar_wait(full + 8 * (i % NSL), (i / NSL) & 1, kWaitLimitCycles)) {
                     atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
                     break;
                 }
@@ -189,25 +205,29 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0 && n_st > 0) {
             bool ok = ptx::mbar_wait(bar_q, 0, kWaitLimitCycles);
+            ptx::fence_proxy_async();
             ptx::tc_fence_after();
-            // S_j = Q'hi . K_j^T + Q'lo . K_j^T into S buffer j % 2
+            // S_j = Q'hi . K_j^T + Q'lo . K_j^T into S buffer j % 2 (hi and lo of one
+            // k-step back to back: the tensor core takes a B chunk twice in a row
+            // faster than two different ones)
             auto issue_s = [&](int j) {
-                const int s = j % NS;
-                ok = ok && ptx::mbar_wait(bar_full + 8 * s, (j / NS) & 1, kWaitLimitCycles);
+                const int s = j % NK;
+                ok = ok && ptx::mbar_wait(bar_kfull + 8 * s, (j / NK) & 1, kWaitLimitCycles);
                 if (!ok) return;
                 ptx::tc_fence_after();
-                const uint32_t kt = ring + s * SH::kStageBytes;
+                const uint32_t kt = kring + s * SH::kTile;
                 const uint32_t d = tmem + (j & 1) * kUmKeys;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
-                    for (int kk = 0; kk < KS; ++kk) {
+                    for (int part = 0; part < 2; ++part) {
                         const uint32_t off = (kk >> 2) * SH::kQBox + (kk & 3) * 32;
                         const uint32_t koff = (kk >> 2) * (kUmKeys * 128) + (kk & 3) * 32;
                         ptx::umma_bf16(d, ptx::umma_desc((part ? q_lo : q_hi) + off, 16, 1024),
                                        ptx::umma_desc(kt + koff, 16, 1024), kIdS, part | kk);
                     }
                 ptx::umma_commit(bar_s + 8 * (j & 1));
+                ptx::umma_commit(bar_kempty + 8 * s);  // the key tile may be refilled
             };
             issue_s(0);
             if (n_st > 1) issue_s(1);
@@ -219,22 +239,23 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     issue_s(j + 2);
                     if (!ok) break;
                 }
-                ok = ptx::mbar_wait(bar_p + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
+                const int sv = j % NV;
+                ok = ptx::mbar_wait(bar_p, j & 1, kWaitLimitCycles) &&
+                     ptx::mbar_wait(bar_vfull + 8 * sv, (j / NV) & 1, kWaitLimitCycles);
                 if (!ok) break;
                 ptx::tc_fence_after();
                 // O += P_j hi . V_j + P_j lo . V_j; P_j from TMEM (8 columns per 16 keys),
                 // V_j: keys x dims, dims contiguous
-                const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
-                const uint32_t tp = tmem + kUmPCol + (j & 1) * kUmKeys;
+                const uint32_t vt = vring + sv * SH::kTile;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                for (int k2 = 0; k2 < kUmKeys / 16; ++k2)
 #pragma unroll
-                    for (int k2 = 0; k2 < kUmKeys / 16; ++k2)
-                        ptx::umma_bf16_ts(t_o, tp + part * (kUmKeys / 2) + k2 * 8,
+                    for (int part = 0; part < 2; ++part)
+                        ptx::umma_bf16_ts(t_o, tmem + kUmPCol + part * (kUmKeys / 2) + k2 * 8,
                                           ptx::umma_desc(vt + k2 * 2048, kUmKeys * 128, 1024), kIdO,
                                           (j > 0 || part > 0 || k2 > 0) ? 1u : 0u);
-                ptx::umma_commit(bar_pv + 8 * (j & 1));
-                ptx::umma_commit(bar_empty + 8 * (j % NS));  // the stage may be refilled
+                ptx::umma_commit(bar_pv);
+                ptx::umma_commit(bar_vempty + 8 * sv);  // the value tile may be refilled
             }
             if (!ok) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             // every MMA issued has completed before TMEM is freed
@@ -244,7 +265,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
         // Warp w (2 <= w < 10) takes rows 32 (w % 4) .. + 31 (its TMEM lanes) and key
-        // half h = (w - 2) / 4 of each block (32 columns of S), so two warps share
+        // half h = (w - 2) / 4 of each block (64 columns of S), so two warps share
         // every SM sub-partition's softmax work. The pair exchanges row maxima
         // through shared memory and a named barrier, and its partial sums at the end.
         const int h = (warp - 2) >> 2;           // key half of a block, and half of O's columns
@@ -289,17 +310,18 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles));
             ptx::tc_fence_after();
             float x[KH];
-            {
+#pragma unroll
+            for (int c = 0; c < KH / 32; ++c) {
                 uint32_t u[32];
                 if (ok) {
-                    ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + KH * h, u);
+                    ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + KH * h + 32 * c, u);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) u[i] = 0u;
                 }
 #pragma unroll
-                for (int i = 0; i < KH; ++i) x[i] = __uint_as_float(u[i]);
+                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(u[i]);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_sfree + 8 * (j & 1));  // S buffer j % 2 may be overwritten
@@ -319,7 +341,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             {
                 float t8[8];
 #pragma unroll
-                for (int a = 0; a < 8; ++a) t8[a] = fmaxf(fmaxf(x[a], x[a + 8]), fmaxf(x[a + 16], x[a + 24]));
+                for (int a = 0; a < 8; ++a) {
+                    t8[a] = x[a];
+#pragma unroll
+                    for (int i = a + 8; i < KH; i += 8) t8[a] = fmaxf(t8[a], x[i]);
+                }
 #pragma unroll
                 for (int a = 0; a < 4; ++a) t8[a] = fmaxf(t8[a], t8[a + 4]);
                 mh = fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]));
@@ -331,27 +357,10 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             const float mx = fmaxf(mh, xch[(h ^ 1) * kUmRows + r]);
             ptx::named_barrier_sync(pair_bar, 64);
 
-            // raise the reference maximum where a logit exceeds it by more than 2^8,
-            // rescaling what the row's O already holds (this warp: its half of the columns)
+            // raise the reference maximum where a logit exceeds it by more than 2^8
             const bool raise = mx > m + 8.f;
             const float f = raise ? ptx::ex2(m - mx) : 1.f;  // 0 while m = -inf
-            if (j > 0 && __any_sync(0xffffffffu, raise && m != -INFINITY)) {
-                ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
-                                                                  kWaitLimitCycles));
-                ptx::tc_fence_after();
-                if (ok) {
-#pragma unroll 1
-                    for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
-                        uint32_t u[32];
-                        ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
-                        ptx::tmem_st32(t_o + lane_addr + 32 * c, u);
-                    }
-                    ptx::tmem_wait_st();
-                }
-            }
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, raise && m != -INFINITY);
             if (raise) {
                 l *= f;
                 m = mx;
@@ -367,33 +376,52 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
             // value rows of keys at or past the sequence's end (unused slots, or another
-            // head's rows) may hold anything, NaN included: zero them, as P is 0 there
+            // head's rows) may hold anything, NaN included: zero them once they have
+            // landed, as P is 0 there
             const int v_keep = L_after - (kb0 + j) * kUmKeys;
             if (v_keep < kUmKeys) {
-                const uint32_t vt = ring + (j % NS) * SH::kStageBytes + SH::kKV;
+                const int sv = j % NV;
+                ok = __all_sync(0xffffffffu,
+                                ok && ptx::mbar_wait(bar_vfull + 8 * sv, (j / NV) & 1, kWaitLimitCycles));
+                const uint32_t vt = vring + sv * SH::kTile;
                 const int first = max(v_keep, 0), n_chunks = (kUmKeys - first) * SH::kBoxes * 8;
-                for (int i = tid; i < n_chunks; i += 256) {
+                for (int i = tid; i < n_chunks && ok; i += 256) {
                     const int row = first + i / (SH::kBoxes * 8), rem = i % (SH::kBoxes * 8);
                     ptx::st_shared_v4(vt + (rem >> 3) * (kUmKeys * 128) + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
                 }
                 ptx::fence_proxy_async();  // visible to the tensor core
             }
-            // P buffer j % 2 (TMEM) is free once P_{j-2} . V_{j-2} has completed
-            if (j >= 2)
-                ok = __all_sync(0xffffffffu,
-                                ok && ptx::mbar_wait(bar_pv + 8 * (j & 1), ((j - 2) >> 1) & 1, kWaitLimitCycles));
-            // P_j (this thread: keys 32 h .. + 31 of its row) as bf16 hi / lo pairs into TMEM
-            if (ok) {
-                uint32_t hh[KH / 2], lw[KH / 2];
+            // P and O are free once P_{j-1} . V_{j-1} has completed: then the rows' O
+            // halves are rescaled (where the maximum rose) and P_j is written
+            if (j >= 1)
+                ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv, (j - 1) & 1, kWaitLimitCycles));
+            ptx::tc_fence_after();
+            if (ok && rescale) {
+#pragma unroll 1
+                for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
+                    uint32_t u[32];
+                    ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < KH / 2; ++e) um_split(x[2 * e], x[2 * e + 1], hh[e], lw[e]);
-                const uint32_t tp = tmem + lane_addr + kUmPCol + (j & 1) * kUmKeys + (KH / 2) * h;
-                ptx::tmem_st16(tp, hh);
-                ptx::tmem_st16(tp + kUmKeys / 2, lw);
+                    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+                    ptx::tmem_st32(t_o + lane_addr + 32 * c, u);
+                }
+            }
+            // P_j (this thread: keys 64 h .. + 63 of its row) as bf16 hi / lo pairs
+            if (ok) {
+#pragma unroll
+                for (int c = 0; c < KH / 32; ++c) {
+                    uint32_t hh[16], lw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) um_split(x[32 * c + 2 * e], x[32 * c + 2 * e + 1], hh[e], lw[e]);
+                    const uint32_t tp = tmem + lane_addr + kUmPCol + (KH / 2) * h + 16 * c;
+                    ptx::tmem_st16(tp, hh);
+                    ptx::tmem_st16(tp + kUmKeys / 2, lw);
+                }
                 ptx::tmem_wait_st();
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_p + 8 * (j & 1));
+            ptx::mbar_arrive(bar_p);
         }
         if (!ok && lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
 
@@ -404,8 +432,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         l += xch[(h ^ 1) * kUmRows + r];
         // O is complete once the last P . V has (commits complete in order)
         if (n_st > 0) {
-            ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv + 8 * ((n_st - 1) & 1), ((n_st - 1) >> 1) & 1,
-                                                              kWaitLimitCycles));
+            ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv, (n_st - 1) & 1, kWaitLimitCycles));
             ptx::tc_fence_after();
         }
         {
