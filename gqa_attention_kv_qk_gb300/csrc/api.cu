@@ -425,6 +425,7 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.Hkv = d->n_kv_heads;
     p.D = d->head_dim;
     p.q_len = pl.q_len;
+    p.tokens_per_cta = pl.q_len < 16 ? pl.q_len : 16;  // fewer, longer CTAs for a long chunk (at most 16)
     p.cap = a->cache_capacity;
     p.max_len = a->max_seq_len;
     p.style = d->rope.style;

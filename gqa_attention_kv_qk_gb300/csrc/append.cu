@@ -1,11 +1,12 @@
 // append.cu -- step 1 of the decode step: per-head QK RMSNorm, rotary embedding at
 // the absolute KV index, and the append of the new k / v rows to the cache.
 //
-// CTAs of 16 warps per token of each sequence, as many as give every warp one of
-// the token's Hq + 2 Hkv head rows (a warp walking several rows is a chain of
-// dependent loads). Each CTA first builds the cos / sin table of the token's
-// position (rope_cos_sin) while each warp loads its first head row; then each
-// warp takes whole rows, loading the next while it processes the current one: q
+// CTAs of 16 warps per group of tokens of each sequence (one token for a decode
+// step, up to 16 of a long chunk), as many as give every warp one of a token's
+// Hq + 2 Hkv head rows (a warp walking several rows is a chain of dependent
+// loads). A CTA first builds the cos / sin tables of its tokens' positions
+// (rope_cos_sin) while each warp loads its first head row; then each warp takes
+// whole rows, token after token, loading the next while it processes the current one: q
 // rows go to the workspace pre-multiplied by the partial kernel's logit
 // prescale, k rows and v rows go to slot seq_lens[b] + t of the cache for token t. vq8 values (and q8 keys, after the rotation) are quantised in fp32
 // with IEEE division and round-half-even, the storage rule of the vq8 cache
@@ -16,6 +17,7 @@ namespace uaa {
 namespace {
 
 constexpr int kAppendWarps = 16;
+constexpr int kAppendMaxTokens = 16;  // tokens of one sequence per CTA at most
 
 __device__ __forceinline__ void store_kv(void* cache, int dtype, size_t i, float v)
 {
@@ -57,24 +59,28 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
 {
     constexpr int EPL = D / 32;  // row elements per lane
     constexpr int HALF = D / 2;
-    __shared__ float2 cs[HALF];
+    __shared__ float2 cs_all[kAppendMaxTokens][HALF];  // the group's cos / sin tables, one per token
+    __shared__ double freq_s[HALF];
     __shared__ float rowbuf[kAppendWarps][D];
 
     grid_dependency_wait();  // the step's inputs and the previous step's reads are complete
     const int n_rows = p.Hq + 2 * p.Hkv;
-    const int parts = (n_rows + kAppendWarps - 1) / kAppendWarps;  // CTAs per token
-    const int bt = blockIdx.x / parts, part = blockIdx.x - bt * parts;
-    const int b = bt / p.q_len, tok = bt - b * p.q_len;
+    const int parts = (n_rows + kAppendWarps - 1) / kAppendWarps;  // CTAs per token group
+    const int groups = (p.q_len + p.tokens_per_cta - 1) / p.tokens_per_cta;
+    const int bg = blockIdx.x / parts, part = blockIdx.x - bg * parts;
+    const int b = bg / groups, grp = bg - b * groups;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = part * kAppendWarps + warp;  // this warp's first row
     const int row_step = parts * kAppendWarps;
+    const int tok0 = grp * p.tokens_per_cta, tok1 = min(p.q_len, tok0 + p.tokens_per_cta);
 
-    // each warp takes rows row0, row0 + row_step, ...; the next row is loaded while
-    // the current one is processed (the first load goes out before the length's)
+    // each warp takes rows row0, row0 + row_step, ... of every token of the group;
+    // the next row is loaded while the current one is processed (the first load
+    // goes out before the length's)
     float x[EPL], nxt[EPL];
     if (row0 < n_rows) {
         size_t at;
-        const void* src = row_source(p, b, tok, row0, at);
+        const void* src = row_source(p, b, tok0, row0, at);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
     }
@@ -83,27 +89,34 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     // not all fit the cache is not appended (and not advanced)
     const int L = p.seq_lens[b];
     const bool fits = L >= 0 && L + p.q_len <= p.cap;
-    if (threadIdx.x == 0 && tok == 0 && part == 0) {
+    if (threadIdx.x == 0 && grp == 0 && part == 0) {
         if (!fits) atomicOr(p.status, UAA_DEVFLAG_CAPACITY);
         else if (L > p.max_len) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
     }
 
-    {
+    // the cos / sin tables of every token of the group, built by all warps at once
+    for (int i = threadIdx.x; i < HALF; i += blockDim.x) freq_s[i] = p.inv_freq_over_pi[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < (tok1 - tok0) * HALF; i += blockDim.x) {
+        const int t = i / HALF, pp = i - t * HALF;
+        cs_all[t][pp] = rope_pair_cos_sin(pp, p.half_rot, fits ? L + tok0 + t : 0, freq_s[pp], p.mscale);
+    }
+    __syncthreads();  // the tables are complete
+
+    for (int tok = tok0; tok < tok1; ++tok) {
         const int pos = fits ? L + tok : 0;
-#pragma unroll
-        for (int i0 = 0; i0 < HALF; i0 += 32)  // warp w takes pairs 32 w .. 32 w + 31
-            if (warp == i0 / 32)
-                cs[i0 + lane] = rope_pair_cos_sin(i0 + lane, p.half_rot, pos, param_at_lane(p.inv_freq_over_pi + i0, lane),
-                                                  p.mscale);
-        __syncthreads();  // the cos / sin table is complete
+        const float2* cs = cs_all[tok - tok0];
         for (int r = row0; r < n_rows; r += row_step) {
 #pragma unroll
             for (int i = 0; i < EPL; ++i) x[i] = nxt[i];
-            if (r + row_step < n_rows) {
-                size_t at;
-                const void* src = row_source(p, b, tok, r + row_step, at);
+            {  // the next row of this token, or the first of the next token
+                const bool more = r + row_step < n_rows;
+                if (more || tok + 1 < tok1) {
+                    size_t at;
+                    const void* src = row_source(p, b, more ? tok : tok + 1, more ? r + row_step : row0, at);
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
+                    for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
+                }
             }
             const bool is_q = r < p.Hq;
             const bool is_k = !is_q && r < p.Hq + p.Hkv;
@@ -161,7 +174,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                     rowbuf[warp][ib] = yb;
                 } else if (kbf16) {
                     __nv_bfloat16 ha = __float2bfloat16_rn(ya), hb = __float2bfloat16_rn(yb);
-                    const float eb = key_error_bound(a0, b0, cs[pp]);
+                    const float eb = key_error_bound(a0, b0, cs[pp], p.qk_norm != 0);
                     const bool near = bf16_near_boundary(ya, eb) || bf16_near_boundary(yb, eb);
                     if (__any_sync(0xffffffffu, near)) {  // the pair again in fp64 (the whole warp for the norm)
                         size_t at;
@@ -177,8 +190,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                             const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[ia]) + p.norm_offset : 1.0;
                             const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[ib]) + p.norm_offset : 1.0;
                             key_pair_exact(load_as_float<T>(src, at + ia), load_as_float<T>(src, at + ib), wa, wb,
-                                           inv64, rope_cos_sin64(pp, p.half_rot, pos, p.inv_freq_over_pi[pp], p.mscale64),
-                                           ha, hb);
+                                           inv64, rope_cos_sin64(pp, p.half_rot, pos, freq_s[pp], p.mscale64), ha, hb);
                         }
                     }
                     static_cast<__nv_bfloat16*>(p.k_cache)[slot + ia] = ha;
@@ -238,7 +250,8 @@ __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
     const int parts = (p.Hq + 2 * p.Hkv + kAppendWarps - 1) / kAppendWarps;  // a warp per head row
-    const long long ctas = static_cast<long long>(p.B) * p.q_len * parts;
+    const int groups = (p.q_len + p.tokens_per_cta - 1) / p.tokens_per_cta;
+    const long long ctas = static_cast<long long>(p.B) * groups * parts;
     if (ctas > 2147483647LL) return cudaErrorInvalidConfiguration;  // beyond one grid's x extent
     const dim3 grid(static_cast<unsigned>(ctas)), block(kAppendWarps * 32);
     const bool f32 = p.io_dtype == UAA_DTYPE_F32;

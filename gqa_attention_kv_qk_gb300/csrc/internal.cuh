@@ -33,6 +33,7 @@ struct KvPages {
 struct AppendParams {
     int B, Hq, Hkv, D;
     int q_len;              // tokens per sequence (rows [B][q_len][H][D] of q, k_new, v_new, q_prime)
+    int tokens_per_cta;     // consecutive tokens of one sequence a CTA takes
     int cap, max_len;
     int style;              // UAA_ROPE_NEOX / _INTERLEAVED
     int half_rot;           // rotated pairs per head row (rotary_dim / 2)
@@ -549,13 +550,17 @@ __device__ __forceinline__ int2 rope_pair(int pp, int half_rot, int D, bool neox
 // recomputed in fp64 (rope_cos_sin64, rms_inv64) and rounded from there
 // (bf16_from_double).
 
-// Bound on |y - exact| for y = a c - b s computed in fp32 from a, b (after an
-// fp32 RMSNorm, if any) and c, s (sincospif of the exactly reduced angle times
-// the multiplier): about 18 fp32 ulps of |a c| + |b s| in the worst case, taken
-// eight times over.
-__device__ __forceinline__ float key_error_bound(float a, float b, float2 cs)
+// Bound on |y - exact| for y = a c - b s computed in fp32 from a, b and c, s
+// (sincospif of the exactly reduced angle, cast to fp32, times the multiplier
+// mu; |c| + |s| >= mu). The cos / sin error (half an ulp of the angle, one of
+// sincospif, the multiplier's rounding: below 2^-21.8 mu) and the rounding of
+// the rotation (2^-23 mu) scale with |a| + |b|, not with |y| (they do not
+// cancel where the rotation does); an fp32 RMSNorm adds about 12 ulps to a and
+// b (2^-20.4). The bound takes 2^-19 (2^-18 after a norm) times (|a| + |b|)
+// (|c| + |s|): three to five times the worst case.
+__device__ __forceinline__ float key_error_bound(float a, float b, float2 cs, bool normed)
 {
-    return 0x1p-17f * (fabsf(a * cs.x) + fabsf(b * cs.y)) + 0x1p-120f;
+    return (normed ? 0x1p-18f : 0x1p-19f) * (fabsf(a) + fabsf(b)) * (fabsf(cs.x) + fabsf(cs.y)) + 0x1p-120f;
 }
 
 // Whether bf16 rounding of the exact value may differ from RN(y), |y - exact| <= e:

@@ -465,7 +465,7 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
         for (int j = 0; j < NP; ++j) {
             hka[j] = __float2bfloat16_rn(ka[j]);
             hkb[j] = __float2bfloat16_rn(kb[j]);
-            const float eb = key_error_bound(ka0[j], kb0[j], cs[lane + 32 * j]);
+            const float eb = key_error_bound(ka0[j], kb0[j], cs[lane + 32 * j], p.qk_norm != 0);
             near[j] = bf16_near_boundary(ka[j], eb) || bf16_near_boundary(kb[j], eb);
             any |= near[j];
         }
