@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kAppendWarps = 16;
 constexpr int kAppendMaxTokens = 16;  // tokens of one sequence per CTA at most
+constexpr int kAppendAhead = 4;       // head rows in flight per warp
 
 __device__ __forceinline__ void store_kv(void* cache, int dtype, size_t i, float v)
 {
@@ -54,14 +55,27 @@ __device__ __forceinline__ const void* row_source(const AppendParams& p, int b, 
     return r < p.Hq + p.Hkv ? p.k_new : p.v_new;
 }
 
+// A key pair whose fp32 rotation lies near a bf16 rounding boundary, queued for
+// its fp64 recomputation (key_pair_exact): the pair's cache row (element index),
+// position and rotation pair, its raw elements and the row's fp64 norm factor.
+struct NearKey {
+    size_t slot;
+    double inv64;
+    int pos;
+    short ia, ib, pp;
+    float ra, rb;
+};
+constexpr int kNearCap = 16;  // queued pairs per warp; a full queue is flushed
+
 template <int D, typename T>  // T: the io element type (float or __nv_bfloat16)
-__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p)
+__global__ void __launch_bounds__(kAppendWarps * 32, 2) append_kernel(const AppendParams p)
 {
     constexpr int EPL = D / 32;  // row elements per lane
     constexpr int HALF = D / 2;
     __shared__ float2 cs_all[kAppendMaxTokens][HALF];  // the group's cos / sin tables, one per token
     __shared__ double freq_s[HALF];
     __shared__ float rowbuf[kAppendWarps][D];
+    __shared__ NearKey near_q[kAppendWarps][kNearCap];
 
     grid_dependency_wait();  // the step's inputs and the previous step's reads are complete
     const int n_rows = p.Hq + 2 * p.Hkv;
@@ -74,16 +88,23 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     const int row_step = parts * kAppendWarps;
     const int tok0 = grp * p.tokens_per_cta, tok1 = min(p.q_len, tok0 + p.tokens_per_cta);
 
-    // each warp takes rows row0, row0 + row_step, ... of every token of the group;
-    // the next row is loaded while the current one is processed (the first load
-    // goes out before the length's)
-    float x[EPL], nxt[EPL];
-    if (row0 < n_rows) {
+    // each warp takes rows row0, row0 + row_step, ... of every token of the group
+    // (items k = 0 .. n_items - 1, token-major); the rows of the next kAppendAhead
+    // items are in flight while one is processed (the first loads go out before the
+    // length's): a row is a few hundred bytes, and one in flight per warp leaves
+    // HBM mostly idle
+    const int rpw = row0 < n_rows ? (n_rows - 1 - row0) / row_step + 1 : 0;  // rows per token
+    const int n_items = rpw * (tok1 - tok0);
+    auto load_item = [&](int k, float (&dst)[EPL]) {
         size_t at;
-        const void* src = row_source(p, b, tok0, row0, at);
+        const void* src = row_source(p, b, tok0 + k / rpw, row0 + (k % rpw) * row_step, at);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
-    }
+        for (int i = 0; i < EPL; ++i) dst[i] = load_as_float<T>(src, at + lane + 32 * i);
+    };
+    float buf[kAppendAhead][EPL];
+#pragma unroll
+    for (int u = 0; u < kAppendAhead; ++u)
+        if (u < n_items) load_item(u, buf[u]);
 
     // the step's tokens take positions L .. L + q_len - 1; a sequence whose tokens do
     // not all fit the cache is not appended (and not advanced)
@@ -94,6 +115,25 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
         else if (L > p.max_len) atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
     }
 
+    // near-boundary key pairs of this warp: one lane per queued pair recomputes it in
+    // fp64 and overwrites the two elements (the fp64 pipe runs whole warps: a queue
+    // shares its cost among up to kNearCap pairs)
+    int n_near = 0;  // warp-uniform
+    auto flush_near = [&]() {
+        __syncwarp();
+        if (lane < n_near) {
+            const NearKey q = near_q[warp][lane];
+            const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[q.ia]) + p.norm_offset : 1.0;
+            const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[q.ib]) + p.norm_offset : 1.0;
+            __nv_bfloat16 ha, hb;
+            key_pair_exact(q.ra, q.rb, wa, wb, q.inv64, rope_cos_sin64(q.pp, p.half_rot, q.pos, freq_s[q.pp], p.mscale64),
+                           ha, hb);
+            static_cast<__nv_bfloat16*>(p.k_cache)[q.slot + q.ia] = ha;
+            static_cast<__nv_bfloat16*>(p.k_cache)[q.slot + q.ib] = hb;
+        }
+        __syncwarp();
+    };
+
     // the cos / sin tables of every token of the group, built by all warps at once
     for (int i = threadIdx.x; i < HALF; i += blockDim.x) freq_s[i] = p.inv_freq_over_pi[i];
     __syncthreads();
@@ -103,21 +143,10 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     }
     __syncthreads();  // the tables are complete
 
-    for (int tok = tok0; tok < tok1; ++tok) {
-        const int pos = fits ? L + tok : 0;
-        const float2* cs = cs_all[tok - tok0];
-        for (int r = row0; r < n_rows; r += row_step) {
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) x[i] = nxt[i];
-            {  // the next row of this token, or the first of the next token
-                const bool more = r + row_step < n_rows;
-                if (more || tok + 1 < tok1) {
-                    size_t at;
-                    const void* src = row_source(p, b, more ? tok : tok + 1, more ? r + row_step : row0, at);
-#pragma unroll
-                    for (int i = 0; i < EPL; ++i) nxt[i] = load_as_float<T>(src, at + lane + 32 * i);
-                }
-            }
+    // one head row r of token tok, held in x
+    auto row_body = [&](int tok, int r, float (&x)[EPL]) {
+            const int pos = fits ? L + tok : 0;
+            const float2* cs = cs_all[tok - tok0];
             const bool is_q = r < p.Hq;
             const bool is_k = !is_q && r < p.Hq + p.Hkv;
             const int head = is_q ? r : (is_k ? r - p.Hq : r - p.Hq - p.Hkv);
@@ -129,14 +158,14 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
             if (!is_q && fits && crow < 0 && lane == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
             const size_t slot = static_cast<size_t>(crow) * D;
             if (!is_q && !is_k) {  // value row: stored as given (or quantised)
-                if (!stores) continue;
+                if (!stores) return;
                 if (p.kv_dtype == UAA_DTYPE_VQ8 || p.kv_dtype == UAA_DTYPE_Q8) {
                     quantize_row<EPL>(x, lane, static_cast<int8_t*>(p.v_cache) + slot, p.v_scale + crow);
                 } else {
 #pragma unroll
                     for (int i = 0; i < EPL; ++i) store_kv(p.v_cache, p.kv_dtype, slot + lane + 32 * i, x[i]);
                 }
-                continue;
+                return;
             }
 
             if (p.qk_norm) {  // RMSNorm over the head row, before the rotation
@@ -155,6 +184,8 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
 
             // keys of a bf16 (or vq8) cache: rounded as their exact values (bf16_near_boundary)
             const bool kbf16 = is_k && stores && p.kv_dtype != UAA_DTYPE_F32 && p.kv_dtype != UAA_DTYPE_Q8;
+            bool row_inv_done = false;
+            double row_inv64 = 0.0;
             for (int pp = lane; pp < HALF; pp += 32) {
                 const int2 e = rope_pair(pp, p.half_rot, D, p.style == UAA_ROPE_NEOX);
                 const int ia = e.x, ib = e.y;
@@ -173,28 +204,40 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                     rowbuf[warp][ia] = ya;                            // needs max |k| (pairs are disjoint)
                     rowbuf[warp][ib] = yb;
                 } else if (kbf16) {
-                    __nv_bfloat16 ha = __float2bfloat16_rn(ya), hb = __float2bfloat16_rn(yb);
+                    // the fp32 rounding now; a pair near a rounding boundary is queued and
+                    // overwritten by its fp64 recomputation when the warp's queue is flushed
+                    static_cast<__nv_bfloat16*>(p.k_cache)[slot + ia] = __float2bfloat16_rn(ya);
+                    static_cast<__nv_bfloat16*>(p.k_cache)[slot + ib] = __float2bfloat16_rn(yb);
                     const float eb = key_error_bound(a0, b0, cs[pp], p.qk_norm != 0);
                     const bool near = bf16_near_boundary(ya, eb) || bf16_near_boundary(yb, eb);
-                    if (__any_sync(0xffffffffu, near)) {  // the pair again in fp64 (the whole warp for the norm)
+                    const unsigned mask = __ballot_sync(0xffffffffu, near);
+                    if (mask) {
                         size_t at;
                         const void* src = row_source(p, b, tok, r, at);
-                        double inv64 = 0.0;
-                        if (p.qk_norm) {
+                        if (p.qk_norm && !row_inv_done) {  // the row's fp64 norm factor, once
                             double raw[EPL];
 #pragma unroll
                             for (int i = 0; i < EPL; ++i) raw[i] = load_as_float<T>(src, at + lane + 32 * i);
-                            inv64 = rms_inv64<EPL>(raw, D, p.eps);
+                            row_inv64 = rms_inv64<EPL>(raw, D, p.eps);
+                            row_inv_done = true;
+                        }
+                        if (n_near + __popc(mask) > kNearCap) {
+                            flush_near();
+                            n_near = 0;
                         }
                         if (near) {
-                            const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[ia]) + p.norm_offset : 1.0;
-                            const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[ib]) + p.norm_offset : 1.0;
-                            key_pair_exact(load_as_float<T>(src, at + ia), load_as_float<T>(src, at + ib), wa, wb,
-                                           inv64, rope_cos_sin64(pp, p.half_rot, pos, freq_s[pp], p.mscale64), ha, hb);
+                            NearKey& q = near_q[warp][n_near + __popc(mask & ((1u << lane) - 1u))];
+                            q.slot = slot;
+                            q.pos = pos;
+                            q.ia = static_cast<short>(ia);
+                            q.ib = static_cast<short>(ib);
+                            q.pp = static_cast<short>(pp);
+                            q.ra = load_as_float<T>(src, at + ia);
+                            q.rb = load_as_float<T>(src, at + ib);
+                            q.inv64 = p.qk_norm ? row_inv64 : 0.0;
                         }
+                        n_near += __popc(mask);
                     }
-                    static_cast<__nv_bfloat16*>(p.k_cache)[slot + ia] = ha;
-                    static_cast<__nv_bfloat16*>(p.k_cache)[slot + ib] = hb;
                 } else if (stores) {
                     store_kv(p.k_cache, UAA_DTYPE_F32, slot + ia, ya);
                     store_kv(p.k_cache, UAA_DTYPE_F32, slot + ib, yb);
@@ -208,8 +251,21 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
                 quantize_row<EPL>(y, lane, static_cast<int8_t*>(p.k_cache) + slot, p.k_scale + crow);
                 __syncwarp();  // the row is read before the next one overwrites it
             }
+    };
+    for (int k0 = 0; k0 < n_items; k0 += kAppendAhead) {
+#pragma unroll
+        for (int u = 0; u < kAppendAhead; ++u) {
+            const int k = k0 + u;
+            if (k < n_items) {
+                float x[EPL];
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) x[i] = buf[u][i];
+                if (k + kAppendAhead < n_items) load_item(k + kAppendAhead, buf[u]);
+                row_body(tok0 + k / rpw, row0 + (k % rpw) * row_step, x);
+            }
         }
     }
+    if (n_near) flush_near();
     __syncthreads();
     // every CTA of the grid counts in once it has read its length; the last one
     // advances them all (the counter, the workspace word after the status word,
