@@ -18,26 +18,28 @@
 //     and prescaled by the append) as bf16 hi + lo parts in shared memory (two
 //     MMAs per k-step, back to back on the same K chunk), K_j as the TMA
 //     wrote it (keys x dims, 128-byte swizzle);
-//   softmax: two threads own row r (TMEM lane r), one per 64-key half: they
+//   softmax: four threads own row r (TMEM lane r), one per 32-key quarter: they
 //     read S_j, apply softcap and the causal / window masks, and keep a
 //     running maximum m that they raise only when a logit exceeds it by more
 //     than 2^8 (exp2(s - m) <= 256 otherwise; the final division cancels m),
 //     rescaling the O row in TMEM then; P_j = exp2(S_j - m) goes back to TMEM
-//     as bf16 hi + lo parts;
+//     as bf16 hi + lo parts (by truncation: 2^-14 relative);
 //   O (128 x D, fp32 in TMEM) += P_j . V_j, P_j the MMA's A operand in TMEM,
 //     V_j as the TMA wrote it (keys x dims: N-contiguous).
-// S is double-buffered in TMEM: the MMA warp issues S_{j+2} as soon as the
-// softmax has read S_j, so the tensor core computes it while the softmax
-// works; P (one buffer) is written once P_{j-1} . V_{j-1} has completed. Keys
-// and values have rings of their own (a key tile is free once its S is done, a
-// value tile once its P . V is).
+// S is double-buffered in TMEM: the MMA warp issues P_j . V_j as soon as P_j is
+// written and then S_{j+2} (into the buffer the softmax has read S_j from), so
+// the tensor core works while the softmax takes block j + 1; P (one buffer) is
+// written once P_{j-1} . V_{j-1} has completed. Keys and values have rings of
+// their own (a key tile is free once its S is done, a value tile once its
+// P . V is).
 //
-// Warps (320 threads, one CTA per SM): warp 0 issues the TMA loads (lane 0 the
+// Warps (576 threads, one CTA per SM): warp 0 issues the TMA loads (lane 0 the
 // keys, lane 1 the values; full / empty mbarriers, the MMA's commits free the
-// slots); warp 1 allocates TMEM and its lane 0 issues every MMA; warps 2-9
-// stage the q' rows and run the softmax and the epilogue, two warps per row
-// (one per key half of a block and per half of O's columns), which exchange row
-// maxima and sums through shared memory. Every wait is bounded: a wait that
+// slots); warp 1 allocates TMEM and its lane 0 issues every MMA; warps 2-17
+// stage the q' rows and run the softmax and the epilogue, four warps per row
+// (one per quarter of a block's keys and of O's columns), which exchange row
+// maxima and sums through shared memory: the softmax is latency-bound, and
+// four warps per SM sub-partition hide what two did not. Every wait is bounded: a wait that
 // gives up sets UAA_DEVFLAG_TIMEOUT, the thread stops waiting from then on, and
 // the CTA still drains its copies and MMAs and frees its TMEM before it exits.
 #include "internal.cuh"
@@ -48,7 +50,9 @@ namespace {
 
 constexpr int kUmRows = kPrefillRows;  // query rows per CTA (M of the MMAs)
 constexpr int kUmKeys = kPrefillKeys;  // keys per block (N of S, K of P . V)
-constexpr int kUmThreads = 320;        // TMA warp, MMA warp, 8 softmax warps
+constexpr int kUmSplit = 4;            // softmax warps per 32-row quarter (threads per row)
+constexpr int kUmSoftmax = 4 * 32 * kUmSplit;  // softmax threads
+constexpr int kUmThreads = 64 + kUmSoftmax;    // TMA warp, MMA warp, softmax warps
 // TMEM columns: S[b] at 128 b; P at 256 (bf16 hi in the first 64 columns, lo
 // in the next 64); O at 384 (D columns)
 constexpr uint32_t kUmTmemCols = 512;
@@ -61,14 +65,14 @@ struct UmShape {
     static constexpr int kQBox = kUmRows * 128;            // 128 rows of one box: 16 KB
     static constexpr int kQBytes = kBoxes * kQBox;         // Q' hi (or lo)
     static constexpr int kTile = kUmKeys * D * 2;          // the keys (or values) of a block
-    static constexpr int kKSlots = D == 128 ? 3 : 5;
-    static constexpr int kVSlots = D == 128 ? 2 : 5;
+    static constexpr int kKSlots = D == 128 ? 2 : 4;
+    static constexpr int kVSlots = D == 128 ? 2 : 4;
     static constexpr int kOffQlo = kQBytes;
     static constexpr int kOffK = 2 * kQBytes;
     static constexpr int kOffV = kOffK + kKSlots * kTile;
     static constexpr int kOffBar = kOffV + kVSlots * kTile;  // barriers and the TMEM address: 256 bytes
-    static constexpr int kOffXch = kOffBar + 256;             // the warp pairs' row exchange: [2][128] floats
-    static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 4 * kUmRows;
+    static constexpr int kOffXch = kOffBar + 256;             // the row exchange: [kUmSplit][128] floats
+    static constexpr int kSmemBytes = 1024 + kOffXch + kUmSplit * 4 * kUmRows;
     static_assert(16 * (kKSlots + kVSlots) + 80 <= 256, "barrier area");
 };
 
@@ -83,6 +87,17 @@ __device__ __forceinline__ void um_split(float x0, float x1, uint32_t& hi, uint3
 {
     hi = um_pack(x0, x1);
     lo = um_pack(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+
+// (x0, x1) ~= hi + lo by truncation: hi = the upper 16 bits of x (a bf16), lo =
+// the upper 16 bits of x - hi (exact in fp32); |x - hi - lo| < 2^-14 |x|. Integer
+// and fp32-add work only, where um_split's conversions share the pipe that
+// computes the exponentials.
+__device__ __forceinline__ void um_split_trunc(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    const uint32_t h0 = __float_as_uint(x0) & 0xffff0000u, h1 = __float_as_uint(x1) & 0xffff0000u;
+    hi = __byte_perm(h0, h1, 0x7632);
+    lo = __byte_perm(__float_as_uint(x0 - __uint_as_float(h0)), __float_as_uint(x1 - __uint_as_float(h1)), 0x7632);
 }
 
 // Byte offset of 16-byte chunk c (< 8) of row r in a 1024-byte-aligned tile of
@@ -100,7 +115,8 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     using SH = UmShape<D>;
     constexpr int NK = SH::kKSlots, NV = SH::kVSlots;
     constexpr int KS = D / 16;       // k-steps of Q'.K^T
-    constexpr int KH = kUmKeys / 2;  // keys per softmax thread and block
+    constexpr int KH = kUmKeys / kUmSplit;  // keys per softmax thread and block
+    constexpr int CW = D / kUmSplit;        // O columns per softmax thread
     constexpr uint32_t kIdS = ptx::umma_idesc_bf16(kUmRows, kUmKeys, false, false);
     constexpr uint32_t kIdO = ptx::umma_idesc_bf16(kUmRows, D, false, true);
     extern __shared__ uint8_t smem_raw[];
@@ -110,15 +126,15 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t bars = base + SH::kOffBar;
     const uint32_t bar_kfull = bars, bar_kempty = bars + 8 * NK;
     const uint32_t bar_vfull = bars + 16 * NK, bar_vempty = bar_vfull + 8 * NV;
-    const uint32_t bar_q = bar_vempty + 8 * NV;  // q' rows staged (256 arrivals)
+    const uint32_t bar_q = bar_vempty + 8 * NV;  // q' rows staged (one arrival per softmax thread)
     const uint32_t bar_s = bar_q + 8;            // [2] S_j in TMEM (MMA commit)
-    const uint32_t bar_sfree = bar_s + 16;       // [2] S_j read (256 arrivals)
-    const uint32_t bar_p = bar_sfree + 16;       // P_j in TMEM (256 arrivals)
+    const uint32_t bar_sfree = bar_s + 16;       // [2] S_j read (one arrival per softmax thread)
+    const uint32_t bar_p = bar_sfree + 16;       // P_j in TMEM (one arrival per softmax thread)
     const uint32_t bar_pv = bar_p + 8;           // P_j . V_j done (MMA commit)
     const uint32_t bar_drain = bar_pv + 8;       // every MMA done (MMA commit)
     const uint32_t tmem_slot = bar_drain + 8;
     uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (tmem_slot - raw));
-    float* xch = reinterpret_cast<float*>(smem_raw + (base + SH::kOffXch - raw));  // [2][128]: row maxima / sums
+    float* xch = reinterpret_cast<float*>(smem_raw + (base + SH::kOffXch - raw));  // [kUmSplit][128]: row maxima / sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows = p.q_len * p.G;  // query rows of the kv head
@@ -136,12 +152,12 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             ptx::mbar_init(bar_vfull + 8 * s, 1);
             ptx::mbar_init(bar_vempty + 8 * s, 1);
         }
-        ptx::mbar_init(bar_q, 256);
+        ptx::mbar_init(bar_q, kUmSoftmax);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_s + 8 * i, 1);
-            ptx::mbar_init(bar_sfree + 8 * i, 256);
+            ptx::mbar_init(bar_sfree + 8 * i, kUmSoftmax);
         }
-        ptx::mbar_init(bar_p, 256);
+        ptx::mbar_init(bar_p, kUmSoftmax);
         ptx::mbar_init(bar_pv, 1);
         ptx::mbar_init(bar_drain, 1);
         ptx::fence_barrier_init();
@@ -232,13 +248,6 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             issue_s(0);
             if (n_st > 1) issue_s(1);
             for (int j = 0; j < n_st && ok; ++j) {
-                if (j + 2 < n_st) {  // S buffer j % 2 is free once the softmax has read S_j
-                    ok = ptx::mbar_wait(bar_sfree + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_s(j + 2);
-                    if (!ok) break;
-                }
                 const int sv = j % NV;
                 ok = ptx::mbar_wait(bar_p, j & 1, kWaitLimitCycles) &&
                      ptx::mbar_wait(bar_vfull + 8 * sv, (j / NV) & 1, kWaitLimitCycles);
@@ -256,6 +265,12 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                                           (j > 0 || part > 0 || k2 > 0) ? 1u : 0u);
                 ptx::umma_commit(bar_pv);
                 ptx::umma_commit(bar_vempty + 8 * sv);  // the value tile may be refilled
+                if (j + 2 < n_st) {  // S buffer j % 2 is free once the softmax has read S_j
+                    ok = ptx::mbar_wait(bar_sfree + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_s(j + 2);
+                }
             }
             if (!ok) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             // every MMA issued has completed before TMEM is freed
@@ -264,16 +279,17 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
-        // Warp w (2 <= w < 10) takes rows 32 (w % 4) .. + 31 (its TMEM lanes) and key
-        // half h = (w - 2) / 4 of each block (64 columns of S), so two warps share
-        // every SM sub-partition's softmax work. The pair exchanges row maxima
-        // through shared memory and a named barrier, and its partial sums at the end.
-        const int h = (warp - 2) >> 2;           // key half of a block, and half of O's columns
+        // Warp w (2 <= w < 2 + 4 kUmSplit) takes rows 32 (w % 4) .. + 31 (its TMEM
+        // lanes) and key quarter h = (w - 2) / 4 of each block (32 columns of S),
+        // so kUmSplit warps share every SM sub-partition's softmax work. The warps
+        // of a row quarter exchange row maxima through shared memory and a named
+        // barrier, and their partial sums at the end.
+        const int h = (warp - 2) >> 2;           // key quarter of a block, and quarter of O's columns
         const int quad = warp & 3;
         const int r = 32 * quad + lane;          // this thread's row and TMEM lane
-        const int tid = 32 * (warp - 2) + lane;  // 0 .. 255
+        const int tid = 32 * (warp - 2) + lane;  // 0 .. kUmSoftmax - 1
         const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
-        const int pair_bar = 1 + quad;           // named barrier of the warp pair (64 threads)
+        const int quad_bar = 1 + quad;           // named barrier of the row quarter's warps
         const int R = r_first + r;
         const bool row_ok = valid && R < rows;
         const int kmax = L + R / p.G;  // the last key the row sees
@@ -283,7 +299,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             // K-major tiles (zeros for a missing row)
             const float* q = p.q_prime + (row_ok ? query_row(b, R, kvh, p.G, p.Hq, p.q_len) : 0) * D;
 #pragma unroll 4
-            for (int c = h * (D / 16); c < (h + 1) * (D / 16); ++c) {
+            for (int c = h * (D / 8 / kUmSplit); c < (h + 1) * (D / 8 / kUmSplit); ++c) {
                 float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
                 if (row_ok) {
                     x0 = *reinterpret_cast<const float4*>(q + 8 * c);
@@ -309,19 +325,19 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int j = 0; j < n_st; ++j) {
             ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles));
             ptx::tc_fence_after();
+            static_assert(KH == 32, "one 32-column TMEM load per thread and block");
             float x[KH];
-#pragma unroll
-            for (int c = 0; c < KH / 32; ++c) {
+            {
                 uint32_t u[32];
                 if (ok) {
-                    ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + KH * h + 32 * c, u);
+                    ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + KH * h, u);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) u[i] = 0u;
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(u[i]);
+                for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(u[i]);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_sfree + 8 * (j & 1));  // S buffer j % 2 may be overwritten
@@ -350,12 +366,14 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 for (int a = 0; a < 4; ++a) t8[a] = fmaxf(t8[a], t8[a + 4]);
                 mh = fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]));
             }
-            // the row's maximum over both halves (the second barrier: both have read
-            // before either writes again)
+            // the row's maximum over its quarters (the second barrier: all have read
+            // before any writes again)
             xch[h * kUmRows + r] = mh;
-            ptx::named_barrier_sync(pair_bar, 64);
-            const float mx = fmaxf(mh, xch[(h ^ 1) * kUmRows + r]);
-            ptx::named_barrier_sync(pair_bar, 64);
+            ptx::named_barrier_sync(quad_bar, 32 * kUmSplit);
+            float mx = mh;
+#pragma unroll
+            for (int o = 1; o < kUmSplit; ++o) mx = fmaxf(mx, xch[((h + o) % kUmSplit) * kUmRows + r]);
+            ptx::named_barrier_sync(quad_bar, 32 * kUmSplit);
 
             // raise the reference maximum where a logit exceeds it by more than 2^8
             const bool raise = mx > m + 8.f;
@@ -385,7 +403,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                                 ok && ptx::mbar_wait(bar_vfull + 8 * sv, (j / NV) & 1, kWaitLimitCycles));
                 const uint32_t vt = vring + sv * SH::kTile;
                 const int first = max(v_keep, 0), n_chunks = (kUmKeys - first) * SH::kBoxes * 8;
-                for (int i = tid; i < n_chunks && ok; i += 256) {
+                for (int i = tid; i < n_chunks && ok; i += kUmSoftmax) {
                     const int row = first + i / (SH::kBoxes * 8), rem = i % (SH::kBoxes * 8);
                     ptx::st_shared_v4(vt + (rem >> 3) * (kUmKeys * 128) + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
                 }
@@ -396,28 +414,25 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             if (j >= 1)
                 ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv, (j - 1) & 1, kWaitLimitCycles));
             ptx::tc_fence_after();
-            if (ok && rescale) {
+            if (ok && rescale) {  // this thread's CW columns of the O row
 #pragma unroll 1
-                for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
-                    uint32_t u[32];
-                    ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
+                for (int c = 0; c < CW / 16; ++c) {
+                    uint32_t u[16];
+                    ptx::tmem_ld16(t_o + lane_addr + CW * h + 16 * c, u);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
-                    ptx::tmem_st32(t_o + lane_addr + 32 * c, u);
+                    for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+                    ptx::tmem_st16(t_o + lane_addr + CW * h + 16 * c, u);
                 }
             }
-            // P_j (this thread: keys 64 h .. + 63 of its row) as bf16 hi / lo pairs
+            // P_j (this thread: keys 32 h .. + 31 of its row) as bf16 hi / lo pairs
             if (ok) {
+                uint32_t hh[16], lw[16];
 #pragma unroll
-                for (int c = 0; c < KH / 32; ++c) {
-                    uint32_t hh[16], lw[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) um_split(x[32 * c + 2 * e], x[32 * c + 2 * e + 1], hh[e], lw[e]);
-                    const uint32_t tp = tmem + lane_addr + kUmPCol + (KH / 2) * h + 16 * c;
-                    ptx::tmem_st16(tp, hh);
-                    ptx::tmem_st16(tp + kUmKeys / 2, lw);
-                }
+                for (int e = 0; e < 16; ++e) um_split_trunc(x[2 * e], x[2 * e + 1], hh[e], lw[e]);
+                const uint32_t tp = tmem + lane_addr + kUmPCol + (KH / 2) * h;
+                ptx::tmem_st16(tp, hh);
+                ptx::tmem_st16(tp + kUmKeys / 2, lw);
                 ptx::tmem_wait_st();
             }
             ptx::tc_fence_before();
@@ -426,10 +441,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (!ok && lane == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
 
         // ------------------------------------------------------------ the rows
-        // the row's sum over both halves
+        // the row's sum over its quarters
         xch[h * kUmRows + r] = l;
-        ptx::named_barrier_sync(pair_bar, 64);
-        l += xch[(h ^ 1) * kUmRows + r];
+        ptx::named_barrier_sync(quad_bar, 32 * kUmSplit);
+#pragma unroll
+        for (int o = 1; o < kUmSplit; ++o) l += xch[((h + o) % kUmSplit) * kUmRows + r];
         // O is complete once the last P . V has (commits complete in order)
         if (n_st > 0) {
             ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_pv, (n_st - 1) & 1, kWaitLimitCycles));
@@ -448,27 +464,28 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             if (!ok || n_st == 0) scale = 0.f;
             const size_t row = query_row(b, R, kvh, p.G, p.Hq, p.q_len) * D;
 #pragma unroll 1
-            for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
-                uint32_t u[32];
+            for (int c = 0; c < CW / 16; ++c) {  // this thread's CW columns, 16 at a time
+                const int col = CW * h + 16 * c;
+                uint32_t u[16];
                 if (ok && n_st > 0) {
-                    ptx::tmem_ld32(t_o + lane_addr + 32 * c, u);
+                    ptx::tmem_ld16(t_o + lane_addr + col, u);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = 0u;
+                    for (int i = 0; i < 16; ++i) u[i] = 0u;
                 }
                 if (R >= rows) continue;
                 if (p.out_dtype == UAA_DTYPE_F32) {
-                    float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row + 32 * c);
+                    float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row + col);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
+                    for (int i = 0; i < 4; ++i)
                         o[i] = make_float4(__uint_as_float(u[4 * i]) * scale, __uint_as_float(u[4 * i + 1]) * scale,
                                            __uint_as_float(u[4 * i + 2]) * scale,
                                            __uint_as_float(u[4 * i + 3]) * scale);
                 } else {
-                    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row + 32 * c);
+                    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row + col);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < 2; ++i)
                         o[i] = make_uint4(um_pack(__uint_as_float(u[8 * i]) * scale, __uint_as_float(u[8 * i + 1]) * scale),
                                           um_pack(__uint_as_float(u[8 * i + 2]) * scale, __uint_as_float(u[8 * i + 3]) * scale),
                                           um_pack(__uint_as_float(u[8 * i + 4]) * scale, __uint_as_float(u[8 * i + 5]) * scale),
