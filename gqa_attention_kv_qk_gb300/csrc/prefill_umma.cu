@@ -15,9 +15,10 @@
 // Per 128-key block j, with M = 128 rows and N = 128 on the tensor core (the
 // shape it runs at full rate; N = 64 takes half again as long per flop):
 //   S_j (128 x 128, fp32 in TMEM) = Q' . K_j^T, Q' = the q' rows (fp32, rotated
-//     and prescaled by the append) as bf16 hi + lo parts in shared memory (two
-//     MMAs per k-step, back to back on the same K chunk), K_j as the TMA
-//     wrote it (keys x dims, 128-byte swizzle);
+//     and prescaled by the append) as bf16 hi + lo parts in TMEM (the MMA's A
+//     operand; two MMAs per k-step, back to back on the same K chunk), K_j as
+//     the TMA wrote it (keys x dims, 128-byte swizzle), so an S MMA reads only
+//     K from shared memory;
 //   softmax: four threads own row r (TMEM lane r), one per 32-key quarter: they
 //     read S_j, apply softcap and the causal / window masks, and keep a
 //     running maximum m that they raise only when a logit exceeds it by more
@@ -26,12 +27,11 @@
 //     as bf16 hi + lo parts (by truncation: 2^-14 relative);
 //   O (128 x D, fp32 in TMEM) += P_j . V_j, P_j the MMA's A operand in TMEM,
 //     V_j as the TMA wrote it (keys x dims: N-contiguous).
-// S is double-buffered in TMEM: the MMA warp issues P_j . V_j as soon as P_j is
-// written and then S_{j+2} (into the buffer the softmax has read S_j from), so
-// the tensor core works while the softmax takes block j + 1; P (one buffer) is
-// written once P_{j-1} . V_{j-1} has completed. Keys and values have rings of
-// their own (a key tile is free once its S is done, a value tile once its
-// P . V is).
+// The MMA warp issues S_{j+1} as soon as the softmax has read S_j into
+// registers (one S buffer), and P_j . V_j once P_j is written, so the tensor
+// core works while the softmax takes block j; P (one buffer) is written once
+// P_{j-1} . V_{j-1} has completed. Keys and values have rings of their own (a
+// key tile is free once its S is done, a value tile once its P . V is).
 //
 // Warps (576 threads, one CTA per SM): warp 0 issues the TMA loads (lane 0 the
 // keys, lane 1 the values; full / empty mbarriers, the MMA's commits free the
@@ -53,27 +53,26 @@ constexpr int kUmKeys = kPrefillKeys;  // keys per block (N of S, K of P . V)
 constexpr int kUmSplit = 4;            // softmax warps per 32-row quarter (threads per row)
 constexpr int kUmSoftmax = 4 * 32 * kUmSplit;  // softmax threads
 constexpr int kUmThreads = 64 + kUmSoftmax;    // TMA warp, MMA warp, softmax warps
-// TMEM columns: S[b] at 128 b; P at 256 (bf16 hi in the first 64 columns, lo
-// in the next 64); O at 384 (D columns)
+// TMEM columns: S at 0; P at 128 (bf16 hi in the first 64 columns, lo in the
+// next 64); O at 256 (D columns); Q' at 384 (bf16 hi in D / 2 columns, lo in
+// the next D / 2)
 constexpr uint32_t kUmTmemCols = 512;
-constexpr uint32_t kUmPCol = 256;
-constexpr uint32_t kUmOCol = 384;
+constexpr uint32_t kUmPCol = 128;
+constexpr uint32_t kUmOCol = 256;
+constexpr uint32_t kUmQCol = 384;
 
 template <int D>
 struct UmShape {
     static constexpr int kBoxes = D / 64;                  // 64-dim boxes of a row
-    static constexpr int kQBox = kUmRows * 128;            // 128 rows of one box: 16 KB
-    static constexpr int kQBytes = kBoxes * kQBox;         // Q' hi (or lo)
     static constexpr int kTile = kUmKeys * D * 2;          // the keys (or values) of a block
-    static constexpr int kKSlots = D == 128 ? 2 : 4;
-    static constexpr int kVSlots = D == 128 ? 2 : 4;
-    static constexpr int kOffQlo = kQBytes;
-    static constexpr int kOffK = 2 * kQBytes;
+    static constexpr int kKSlots = D == 128 ? 3 : 6;
+    static constexpr int kVSlots = D == 128 ? 3 : 6;
+    static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kKSlots * kTile;
-    static constexpr int kOffBar = kOffV + kVSlots * kTile;  // barriers and the TMEM address: 256 bytes
-    static constexpr int kOffXch = kOffBar + 256;             // the row exchange: [kUmSplit][128] floats
+    static constexpr int kOffBar = kOffV + kVSlots * kTile;  // barriers and the TMEM address: 512 bytes
+    static constexpr int kOffXch = kOffBar + 512;             // the row exchange: [kUmSplit][128] floats
     static constexpr int kSmemBytes = 1024 + kOffXch + kUmSplit * 4 * kUmRows;
-    static_assert(16 * (kKSlots + kVSlots) + 80 <= 256, "barrier area");
+    static_assert(16 * (kKSlots + kVSlots) + 64 <= 512, "barrier area");
 };
 
 __device__ __forceinline__ uint32_t um_pack(float lo, float hi)
@@ -100,13 +99,6 @@ __device__ __forceinline__ void um_split_trunc(float x0, float x1, uint32_t& hi,
     lo = __byte_perm(__float_as_uint(x0 - __uint_as_float(h0)), __float_as_uint(x1 - __uint_as_float(h1)), 0x7632);
 }
 
-// Byte offset of 16-byte chunk c (< 8) of row r in a 1024-byte-aligned tile of
-// 128-byte rows with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t um_swz(int r, int c)
-{
-    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
 template <int D>
 __global__ void __launch_bounds__(kUmThreads, 1)
 prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -122,14 +114,14 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t q_hi = base, q_lo = base + SH::kOffQlo, kring = base + SH::kOffK, vring = base + SH::kOffV;
+    const uint32_t kring = base + SH::kOffK, vring = base + SH::kOffV;
     const uint32_t bars = base + SH::kOffBar;
     const uint32_t bar_kfull = bars, bar_kempty = bars + 8 * NK;
     const uint32_t bar_vfull = bars + 16 * NK, bar_vempty = bar_vfull + 8 * NV;
-    const uint32_t bar_q = bar_vempty + 8 * NV;  // q' rows staged (one arrival per softmax thread)
-    const uint32_t bar_s = bar_q + 8;            // [2] S_j in TMEM (MMA commit)
-    const uint32_t bar_sfree = bar_s + 16;       // [2] S_j read (one arrival per softmax thread)
-    const uint32_t bar_p = bar_sfree + 16;       // P_j in TMEM (one arrival per softmax thread)
+    const uint32_t bar_q = bar_vempty + 8 * NV;  // q' rows in TMEM (one arrival per softmax thread)
+    const uint32_t bar_s = bar_q + 8;            // S_j in TMEM (MMA commit)
+    const uint32_t bar_sfree = bar_s + 8;        // S_j read (one arrival per softmax thread)
+    const uint32_t bar_p = bar_sfree + 8;        // P_j in TMEM (one arrival per softmax thread)
     const uint32_t bar_pv = bar_p + 8;           // P_j . V_j done (MMA commit)
     const uint32_t bar_drain = bar_pv + 8;       // every MMA done (MMA commit)
     const uint32_t tmem_slot = bar_drain + 8;
@@ -153,10 +145,8 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             ptx::mbar_init(bar_vempty + 8 * s, 1);
         }
         ptx::mbar_init(bar_q, kUmSoftmax);
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(bar_s + 8 * i, 1);
-            ptx::mbar_init(bar_sfree + 8 * i, kUmSoftmax);
-        }
+        ptx::mbar_init(bar_s, 1);
+        ptx::mbar_init(bar_sfree, kUmSoftmax);
         ptx::mbar_init(bar_p, kUmSoftmax);
         ptx::mbar_init(bar_pv, 1);
         ptx::mbar_init(bar_drain, 1);
@@ -221,33 +211,36 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0 && n_st > 0) {
             bool ok = ptx::mbar_wait(bar_q, 0, kWaitLimitCycles);
-            ptx::fence_proxy_async();
             ptx::tc_fence_after();
-            // S_j = Q'hi . K_j^T + Q'lo . K_j^T into S buffer j % 2 (hi and lo of one
-            // k-step back to back: the tensor core takes a B chunk twice in a row
-            // faster than two different ones)
+            // S_j = Q'hi . K_j^T + Q'lo . K_j^T; Q' from TMEM (8 columns per 16 dims), K_j
+            // from the ring (hi and lo of one k-step back to back: the tensor core takes
+            // a B chunk twice in a row faster than two different ones)
             auto issue_s = [&](int j) {
                 const int s = j % NK;
                 ok = ok && ptx::mbar_wait(bar_kfull + 8 * s, (j / NK) & 1, kWaitLimitCycles);
                 if (!ok) return;
                 ptx::tc_fence_after();
                 const uint32_t kt = kring + s * SH::kTile;
-                const uint32_t d = tmem + (j & 1) * kUmKeys;
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t off = (kk >> 2) * SH::kQBox + (kk & 3) * 32;
                         const uint32_t koff = (kk >> 2) * (kUmKeys * 128) + (kk & 3) * 32;
-                        ptx::umma_bf16(d, ptx::umma_desc((part ? q_lo : q_hi) + off, 16, 1024),
-                                       ptx::umma_desc(kt + koff, 16, 1024), kIdS, part | kk);
+                        ptx::umma_bf16_ts(tmem, tmem + kUmQCol + part * (D / 2) + kk * 8,
+                                          ptx::umma_desc(kt + koff, 16, 1024), kIdS, part | kk);
                     }
-                ptx::umma_commit(bar_s + 8 * (j & 1));
+                ptx::umma_commit(bar_s);
                 ptx::umma_commit(bar_kempty + 8 * s);  // the key tile may be refilled
             };
             issue_s(0);
-            if (n_st > 1) issue_s(1);
             for (int j = 0; j < n_st && ok; ++j) {
+                if (j + 1 < n_st) {  // the S buffer is free once the softmax has read S_j
+                    ok = ptx::mbar_wait(bar_sfree, j & 1, kWaitLimitCycles);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_s(j + 1);
+                    if (!ok) break;
+                }
                 const int sv = j % NV;
                 ok = ptx::mbar_wait(bar_p, j & 1, kWaitLimitCycles) &&
                      ptx::mbar_wait(bar_vfull + 8 * sv, (j / NV) & 1, kWaitLimitCycles);
@@ -265,12 +258,6 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                                           (j > 0 || part > 0 || k2 > 0) ? 1u : 0u);
                 ptx::umma_commit(bar_pv);
                 ptx::umma_commit(bar_vempty + 8 * sv);  // the value tile may be refilled
-                if (j + 2 < n_st) {  // S buffer j % 2 is free once the softmax has read S_j
-                    ok = ptx::mbar_wait(bar_sfree + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_s(j + 2);
-                }
             }
             if (!ok) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
             // every MMA issued has completed before TMEM is freed
@@ -295,26 +282,25 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int kmax = L + R / p.G;  // the last key the row sees
         const int kmin = p.window > 0 ? kmax - p.window + 1 : INT_MIN;
         {
-            // q' row (this thread: half of its dims) as bf16 hi / lo in the swizzled
-            // K-major tiles (zeros for a missing row)
+            // q' row (this thread: dims CW h .. CW h + CW - 1) as bf16 hi / lo pairs into
+            // TMEM, 8 columns (16 dims) at a time (zeros for a missing row)
             const float* q = p.q_prime + (row_ok ? query_row(b, R, kvh, p.G, p.Hq, p.q_len) : 0) * D;
-#pragma unroll 4
-            for (int c = h * (D / 8 / kUmSplit); c < (h + 1) * (D / 8 / kUmSplit); ++c) {
-                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                if (row_ok) {
-                    x0 = *reinterpret_cast<const float4*>(q + 8 * c);
-                    x1 = *reinterpret_cast<const float4*>(q + 8 * c + 4);
+#pragma unroll 1
+            for (int c = 0; c < CW / 16; ++c) {
+                const int d0 = CW * h + 16 * c;
+                uint32_t hh[8], ll[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row_ok) v = *reinterpret_cast<const float4*>(q + d0 + 4 * e);
+                    um_split(v.x, v.y, hh[2 * e], ll[2 * e]);
+                    um_split(v.z, v.w, hh[2 * e + 1], ll[2 * e + 1]);
                 }
-                uint32_t hh[4], ll[4];
-                um_split(x0.x, x0.y, hh[0], ll[0]);
-                um_split(x0.z, x0.w, hh[1], ll[1]);
-                um_split(x1.x, x1.y, hh[2], ll[2]);
-                um_split(x1.z, x1.w, hh[3], ll[3]);
-                const uint32_t off = (c >> 3) * SH::kQBox + um_swz(r, c & 7);
-                ptx::st_shared_v4(q_hi + off, hh[0], hh[1], hh[2], hh[3]);
-                ptx::st_shared_v4(q_lo + off, ll[0], ll[1], ll[2], ll[3]);
+                ptx::tmem_st8(tmem + lane_addr + kUmQCol + d0 / 2, hh);
+                ptx::tmem_st8(tmem + lane_addr + kUmQCol + D / 2 + d0 / 2, ll);
             }
-            ptx::fence_proxy_async();  // visible to the tensor core
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
             ptx::mbar_arrive(bar_q);
         }
         const float cap2 = p.softcap_log2e;
@@ -323,14 +309,14 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         bool ok = true;
         // (tcgen05.ld / st are warp-wide: the branches around them are warp-uniform)
         for (int j = 0; j < n_st; ++j) {
-            ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, kWaitLimitCycles));
+            ok = __all_sync(0xffffffffu, ok && ptx::mbar_wait(bar_s, j & 1, kWaitLimitCycles));
             ptx::tc_fence_after();
             static_assert(KH == 32, "one 32-column TMEM load per thread and block");
             float x[KH];
             {
                 uint32_t u[32];
                 if (ok) {
-                    ptx::tmem_ld32(tmem + lane_addr + (j & 1) * kUmKeys + KH * h, u);
+                    ptx::tmem_ld32(tmem + lane_addr + KH * h, u);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -340,7 +326,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(u[i]);
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_sfree + 8 * (j & 1));  // S buffer j % 2 may be overwritten
+            ptx::mbar_arrive(bar_sfree);  // the S buffer may be overwritten
 
             const int key0 = (kb0 + j) * kUmKeys + KH * h;  // this thread's first key
             if (cap2 > 0.f) {
