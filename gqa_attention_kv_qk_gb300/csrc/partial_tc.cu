@@ -132,8 +132,10 @@ struct Shape {
     static constexpr int kCtlBytes = 64;
     // fused append: theta'_p / pi (fp64) and the (cos, sin) of the current sequence, D / 2 each
     static constexpr int kTabBytes = 8 * D;
+    // fused append: new key pairs whose fp64 recomputation is deferred (NearQueue)
+    static constexpr int kNearBytes = 512;
     static constexpr int kFixedBytes =
-        1024 + kCtlBytes + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes + kTabBytes;
+        1024 + kCtlBytes + kPrefixBytes + kLensBytes + kFragBytes + 2 * kNewRowBytes + kTabBytes + kNearBytes;
     // one CTA per SM at head_dim 256 and with two column tiles (eight consumer warps)
     static constexpr int kCtaBudget = D == 256 || NHT == 2 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
     static constexpr int kStagesRaw = (kCtaBudget - kFixedBytes) / (kStageBytes + 16);
@@ -390,9 +392,69 @@ __device__ __forceinline__ void prefetch_new_rows(const PartialParams& p, int b,
 // int8 codes and scale for q8) and value row (bf16, or int8 codes and scale) of
 // (b, kvh) into a staging slot (key at 0, value at 2 D, value scale at 3 D, key
 // scale at 3 D + 4), and into the cache at slot L when `store`.
+// New key pairs (fused append) whose fp32 rotation lies near a bf16 rounding
+// boundary: the staged row keeps the fp32 rounding (the step's own attention
+// uses it, an ulp at most away), and after its last segment the prep warp
+// recomputes each queued pair in fp64 and writes it over the cache's copy, so
+// that the cache holds the exact value's rounding. A full queue recomputes at once.
+struct NearEntry {
+    size_t slot;   // the cache row (element index of its first element)
+    int src;       // the raw row in k_new (element index), slice-relative
+    int pos;       // the token's position
+    short ia, ib, pp, pad;
+};
+struct NearQueue {
+    int n;
+    int pad[3];
+    NearEntry e[20];
+};
+static_assert(sizeof(NearQueue) <= 512, "the near-key queue's shared memory");
+
+template <int D, typename T>
+__device__ void fix_near_keys(const PartialParams& p, NearQueue* q, int lane)
+{
+    constexpr int EPL = D / 32;
+    constexpr int kCap = static_cast<int>(sizeof(q->e) / sizeof(q->e[0]));
+    static_assert(kCap <= 32, "one lane per queued pair");
+    const int n = q->n;
+    // the rows' fp64 norm factors (a whole-warp reduction per distinct row; lane i
+    // keeps entry i's), then every pair at once, one per lane
+    double inv64 = 0.0;
+    if (p.qk_norm) {
+        int last_src = -1;
+        double last_inv = 0.0;
+        for (int i = 0; i < n; ++i) {
+            const int src = q->e[i].src;
+            if (src != last_src) {
+                double raw[EPL];
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) raw[k] = load_as_float<T>(p.k_new, static_cast<size_t>(src) + lane + 32 * k);
+                last_inv = rms_inv64<EPL>(raw, D, p.eps);
+                last_src = src;
+            }
+            if (lane == i) inv64 = last_inv;
+        }
+    }
+    if (lane < n) {
+        const NearEntry e = q->e[lane];
+        const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[e.ia]) + p.norm_offset : 1.0;
+        const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[e.ib]) + p.norm_offset : 1.0;
+        __nv_bfloat16 ha, hb;
+        key_pair_exact(load_as_float<T>(p.k_new, static_cast<size_t>(e.src) + e.ia),
+                       load_as_float<T>(p.k_new, static_cast<size_t>(e.src) + e.ib), wa, wb, inv64,
+                       rope_cos_sin64(e.pp, p.half_rot, e.pos, p.inv_freq_over_pi[e.pp], p.mscale64), ha, hb);
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.k_cache) + e.slot;
+        kc[e.ia] = ha;
+        kc[e.ib] = hb;
+    }
+    __syncwarp();
+    if (lane == 0) q->n = 0;
+    __syncwarp();
+}
+
 template <int D, int KV, typename T>
 __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, const float2* cs, uint8_t* staging,
-                              bool store, int lane)
+                              bool store, int lane, NearQueue* nearq)
 {
     constexpr bool VQ8 = KV != kKvBf16, KQ8 = KV == kKvQ8;
     constexpr int NP = D / 64;   // rotation pairs per lane
@@ -469,25 +531,41 @@ __device__ void prep_new_rows(const PartialParams& p, int b, int kvh, int L, con
             near[j] = bf16_near_boundary(ka[j], eb) || bf16_near_boundary(kb[j], eb);
             any |= near[j];
         }
-        if (__any_sync(0xffffffffu, any)) {
-            double inv64 = 0.0;
-            if (p.qk_norm) {
-                double raw[EPL];
+        // the cache's copy of a near pair is recomputed later (NearQueue); a row that
+        // is only staged (not stored) needs nothing more
+        if (store && __any_sync(0xffffffffu, any)) {
+            int cnt = 0;
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) raw[i] = load_as_float<T>(p.k_new, src + lane + 32 * i);
-                inv64 = rms_inv64<EPL>(raw, D, p.eps);
+            for (int j = 0; j < NP; ++j) cnt += near[j] ? 1 : 0;
+            int incl = cnt;  // inclusive prefix over the lanes
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
             }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            int n0 = nearq->n;
+            if (n0 + total > static_cast<int>(sizeof(nearq->e) / sizeof(nearq->e[0]))) {
+                fix_near_keys<D, T>(p, nearq, lane);  // full: the queued pairs first
+                n0 = 0;
+            }
+            if (n0 + total <= static_cast<int>(sizeof(nearq->e) / sizeof(nearq->e[0]))) {
+                int at = n0 + incl - cnt;
 #pragma unroll
-            for (int j = 0; j < NP; ++j)
-                if (near[j]) {
-                    const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[ia[j]]) + p.norm_offset : 1.0;
-                    const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[ib[j]]) + p.norm_offset : 1.0;
-                    key_pair_exact(load_as_float<T>(p.k_new, src + ia[j]), load_as_float<T>(p.k_new, src + ib[j]), wa,
-                                   wb, inv64,
-                                   rope_cos_sin64(lane + 32 * j, p.half_rot, L, p.inv_freq_over_pi[lane + 32 * j],
-                                                  p.mscale64),
-                                   hka[j], hkb[j]);
-                }
+                for (int j = 0; j < NP; ++j)
+                    if (near[j]) {
+                        NearEntry& e = nearq->e[at++];
+                        e.slot = slot * D;
+                        e.src = static_cast<int>(src);
+                        e.pos = L;
+                        e.ia = static_cast<short>(ia[j]);
+                        e.ib = static_cast<short>(ib[j]);
+                        e.pp = static_cast<short>(lane + 32 * j);
+                    }
+                __syncwarp();
+                if (lane == 0) nearq->n = n0 + total;
+                __syncwarp();
+            }
         }
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
@@ -634,6 +712,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* staging = frag + SH::kFragBytes;  // two slots of kNewRowBytes, by segment parity
     double* freq_s = reinterpret_cast<double*>(staging + 2 * SH::kNewRowBytes);  // [D / 2] theta'_p / pi
     float2* cs_s = reinterpret_cast<float2*>(freq_s + D / 2);                    // [D / 2] (cos, sin)
+    NearQueue* nearq = reinterpret_cast<NearQueue*>(cs_s + D / 2);               // deferred key pairs
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.Hkv * p.head_groups;
@@ -647,6 +726,7 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         ptx::flag_set(go, 0u);
         ptx::flag_set(rows_ready, 0u);
         ptx::flag_set(rows_ready + 4, 0u);
+        nearq->n = 0;
         ptx::fence_barrier_init();
     } else if (threadIdx.x == 32 * kProducerWarp) {
         ptx::prefetch_tensormap(&tm_k);
@@ -828,9 +908,9 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0) ptx::mbar_arrive(bar_qfull);
                 if (ends) {
                     if (p.io_dtype == UAA_DTYPE_F32)
-                        prep_new_rows<D, KV, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
+                        prep_new_rows<D, KV, float>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane, nearq);
                     else
-                        prep_new_rows<D, KV, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane);
+                        prep_new_rows<D, KV, __nv_bfloat16>(p, sg.b, sg.kvh, L, cs_s, st_row, sg.hg == 0, lane, nearq);
                     __syncwarp();
                     if (lane == 0) {
                         __threadfence_block();
@@ -845,6 +925,15 @@ partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_qfull);
             pos += sg.n_st;
+        }
+        // the deferred key pairs, off the consumers' path: recomputed in fp64 and
+        // written over the cache's fp32 rounding
+        if (p.fused && KV != kKvQ8) {
+            __syncwarp();
+            if (p.io_dtype == UAA_DTYPE_F32)
+                fix_near_keys<D, float>(p, nearq, lane);
+            else
+                fix_near_keys<D, __nv_bfloat16>(p, nearq, lane);
         }
         return;
     }
