@@ -38,8 +38,7 @@
 // slots); warp 1 allocates TMEM and its lane 0 issues every MMA; warps 2-17
 // stage the q' rows and run the softmax and the epilogue, four warps per row
 // (one per quarter of a block's keys and of O's columns), which exchange row
-// maxima and sums through shared memory: the softmax is latency-bound, and
-// four warps per SM sub-partition hide what two did not. Every wait is bounded: a wait that
+// maxima and sums through shared memory. Every wait is bounded: a wait that
 // gives up sets UAA_DEVFLAG_TIMEOUT, the thread stops waiting from then on, and
 // the CTA still drains its copies and MMAs and frees its TMEM before it exits.
 #include "internal.cuh"
