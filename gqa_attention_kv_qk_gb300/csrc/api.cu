@@ -425,7 +425,12 @@ uaa_status run_append(const uaa_attn_desc* d, const uaa_step_args* a, const uaa_
     p.Hkv = d->n_kv_heads;
     p.D = d->head_dim;
     p.q_len = pl.q_len;
-    p.tokens_per_cta = pl.q_len < 16 ? pl.q_len : 16;  // fewer, longer CTAs for a long chunk (at most 16)
+    {  // tokens per CTA: one for short steps (parallelism), up to 16 once the grid has ~4 CTAs per SM anyway
+        const int n_sm = device_sm_count();
+        const long long tokens = (long long)a->batch * pl.q_len;
+        long long tpc = n_sm > 0 ? tokens / (4LL * n_sm) : 1;
+        p.tokens_per_cta = (int)(tpc < 1 ? 1 : (tpc > 16 ? 16 : tpc));
+    }
     p.cap = a->cache_capacity;
     p.max_len = a->max_seq_len;
     p.style = d->rope.style;

@@ -67,8 +67,11 @@ struct NearKey {
 };
 constexpr int kNearCap = 16;  // queued pairs per warp; a full queue is flushed
 
-template <int D, typename T>  // T: the io element type (float or __nv_bfloat16)
-__global__ void __launch_bounds__(kAppendWarps * 32, 2) append_kernel(const AppendParams p)
+// T: the io element type (float or __nv_bfloat16); MINB: CTAs per SM the
+// registers are capped for (2 for long chunks, where occupancy keeps HBM busy;
+// 1 for short steps, which are latency-bound and should not spill)
+template <int D, typename T, int MINB>
+__global__ void __launch_bounds__(kAppendWarps * 32, MINB) append_kernel(const AppendParams p)
 {
     constexpr int EPL = D / 32;  // row elements per lane
     constexpr int HALF = D / 2;
@@ -126,20 +129,31 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 2) append_kernel(const Appe
             const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[q.ia]) + p.norm_offset : 1.0;
             const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[q.ib]) + p.norm_offset : 1.0;
             __nv_bfloat16 ha, hb;
-            key_pair_exact(q.ra, q.rb, wa, wb, q.inv64, rope_cos_sin64(q.pp, p.half_rot, q.pos, freq_s[q.pp], p.mscale64),
-                           ha, hb);
+            key_pair_exact(q.ra, q.rb, wa, wb, q.inv64,
+                           rope_cos_sin64(q.pp, p.half_rot, q.pos, p.inv_freq_over_pi[q.pp], p.mscale64), ha, hb);
             static_cast<__nv_bfloat16*>(p.k_cache)[q.slot + q.ia] = ha;
             static_cast<__nv_bfloat16*>(p.k_cache)[q.slot + q.ib] = hb;
         }
         __syncwarp();
     };
 
-    // the cos / sin tables of every token of the group, built by all warps at once
-    for (int i = threadIdx.x; i < HALF; i += blockDim.x) freq_s[i] = p.inv_freq_over_pi[i];
-    __syncthreads();
-    for (int i = threadIdx.x; i < (tok1 - tok0) * HALF; i += blockDim.x) {
-        const int t = i / HALF, pp = i - t * HALF;
-        cs_all[t][pp] = rope_pair_cos_sin(pp, p.half_rot, fits ? L + tok0 + t : 0, freq_s[pp], p.mscale);
+    // the cos / sin tables of every token of the group: one token's by warps 0 ..
+    // HALF / 32 - 1 with fixed-offset parameter reads (param_at_lane; a short step
+    // is latency-bound), several tokens' by all warps from a shared copy of the
+    // frequencies
+    if (tok1 - tok0 == 1) {
+#pragma unroll
+        for (int i0 = 0; i0 < HALF; i0 += 32)
+            if (warp == i0 / 32)
+                cs_all[0][i0 + lane] = rope_pair_cos_sin(i0 + lane, p.half_rot, fits ? L + tok0 : 0,
+                                                         param_at_lane(p.inv_freq_over_pi + i0, lane), p.mscale);
+    } else {
+        for (int i = threadIdx.x; i < HALF; i += blockDim.x) freq_s[i] = p.inv_freq_over_pi[i];
+        __syncthreads();
+        for (int i = threadIdx.x; i < (tok1 - tok0) * HALF; i += blockDim.x) {
+            const int t = i / HALF, pp = i - t * HALF;
+            cs_all[t][pp] = rope_pair_cos_sin(pp, p.half_rot, fits ? L + tok0 + t : 0, freq_s[pp], p.mscale);
+        }
     }
     __syncthreads();  // the tables are complete
 
@@ -311,18 +325,19 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
     if (ctas > 2147483647LL) return cudaErrorInvalidConfiguration;  // beyond one grid's x extent
     const dim3 grid(static_cast<unsigned>(ctas)), block(kAppendWarps * 32);
     const bool f32 = p.io_dtype == UAA_DTYPE_F32;
+    const bool wide = p.tokens_per_cta > 1;
+#define UAA_APPEND_LAUNCH(DD)                                                                                     \
+    (f32 ? (wide ? launch_dependent(append_kernel<DD, float, 2>, grid, block, 0, s, p)                            \
+                 : launch_dependent(append_kernel<DD, float, 1>, grid, block, 0, s, p))                           \
+         : (wide ? launch_dependent(append_kernel<DD, __nv_bfloat16, 2>, grid, block, 0, s, p)                    \
+                 : launch_dependent(append_kernel<DD, __nv_bfloat16, 1>, grid, block, 0, s, p)))
     switch (p.D) {
-    case 64:
-        return f32 ? launch_dependent(append_kernel<64, float>, grid, block, 0, s, p)
-                   : launch_dependent(append_kernel<64, __nv_bfloat16>, grid, block, 0, s, p);
-    case 128:
-        return f32 ? launch_dependent(append_kernel<128, float>, grid, block, 0, s, p)
-                   : launch_dependent(append_kernel<128, __nv_bfloat16>, grid, block, 0, s, p);
-    case 256:
-        return f32 ? launch_dependent(append_kernel<256, float>, grid, block, 0, s, p)
-                   : launch_dependent(append_kernel<256, __nv_bfloat16>, grid, block, 0, s, p);
+    case 64: return UAA_APPEND_LAUNCH(64);
+    case 128: return UAA_APPEND_LAUNCH(128);
+    case 256: return UAA_APPEND_LAUNCH(256);
     default: return cudaErrorInvalidValue;
     }
+#undef UAA_APPEND_LAUNCH
 }
 
 cudaError_t launch_vq8_quantize(const void* v, int v_dtype, int64_t n_rows, int D, int8_t* codes,
