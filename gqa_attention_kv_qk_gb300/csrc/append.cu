@@ -67,11 +67,12 @@ struct NearKey {
 };
 constexpr int kNearCap = 16;  // queued pairs per warp; a full queue is flushed
 
-// T: the io element type (float or __nv_bfloat16); MINB: CTAs per SM the
-// registers are capped for (2 for long chunks, where occupancy keeps HBM busy;
-// 1 for short steps, which are latency-bound and should not spill)
-template <int D, typename T, int MINB>
-__global__ void __launch_bounds__(kAppendWarps * 32, MINB) append_kernel(const AppendParams p)
+// T: the io element type (float or __nv_bfloat16); AHEAD: head rows in flight
+// per warp (kAppendAhead for token groups, where a warp walks many rows; 1 for
+// one token per CTA, so that two CTAs per SM fit without spilling and a short
+// step's grid runs in one wave)
+template <int D, typename T, int AHEAD>
+__global__ void __launch_bounds__(kAppendWarps * 32, 2) append_kernel(const AppendParams p)
 {
     constexpr int EPL = D / 32;  // row elements per lane
     constexpr int HALF = D / 2;
@@ -104,9 +105,9 @@ __global__ void __launch_bounds__(kAppendWarps * 32, MINB) append_kernel(const A
 #pragma unroll
         for (int i = 0; i < EPL; ++i) dst[i] = load_as_float<T>(src, at + lane + 32 * i);
     };
-    float buf[kAppendAhead][EPL];
+    float buf[AHEAD][EPL];
 #pragma unroll
-    for (int u = 0; u < kAppendAhead; ++u)
+    for (int u = 0; u < AHEAD; ++u)
         if (u < n_items) load_item(u, buf[u]);
 
     // the step's tokens take positions L .. L + q_len - 1; a sequence whose tokens do
@@ -266,15 +267,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32, MINB) append_kernel(const A
                 __syncwarp();  // the row is read before the next one overwrites it
             }
     };
-    for (int k0 = 0; k0 < n_items; k0 += kAppendAhead) {
+    for (int k0 = 0; k0 < n_items; k0 += AHEAD) {
 #pragma unroll
-        for (int u = 0; u < kAppendAhead; ++u) {
+        for (int u = 0; u < AHEAD; ++u) {
             const int k = k0 + u;
             if (k < n_items) {
                 float x[EPL];
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) x[i] = buf[u][i];
-                if (k + kAppendAhead < n_items) load_item(k + kAppendAhead, buf[u]);
+                if (k + AHEAD < n_items) load_item(k + AHEAD, buf[u]);
                 row_body(tok0 + k / rpw, row0 + (k % rpw) * row_step, x);
             }
         }
@@ -327,9 +328,9 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
     const bool f32 = p.io_dtype == UAA_DTYPE_F32;
     const bool wide = p.tokens_per_cta > 1;
 #define UAA_APPEND_LAUNCH(DD)                                                                                     \
-    (f32 ? (wide ? launch_dependent(append_kernel<DD, float, 2>, grid, block, 0, s, p)                            \
+    (f32 ? (wide ? launch_dependent(append_kernel<DD, float, kAppendAhead>, grid, block, 0, s, p)                 \
                  : launch_dependent(append_kernel<DD, float, 1>, grid, block, 0, s, p))                           \
-         : (wide ? launch_dependent(append_kernel<DD, __nv_bfloat16, 2>, grid, block, 0, s, p)                    \
+         : (wide ? launch_dependent(append_kernel<DD, __nv_bfloat16, kAppendAhead>, grid, block, 0, s, p)         \
                  : launch_dependent(append_kernel<DD, __nv_bfloat16, 1>, grid, block, 0, s, p)))
     switch (p.D) {
     case 64: return UAA_APPEND_LAUNCH(64);
