@@ -14,7 +14,10 @@ The same JSON line carries `per_config`: the other four workloads of the
 suite (tiny Llama-3.2-1B-like fp32 step, warm and with L2 flushed between steps;
 Qwen3-8B-like ragged; Gemma-2-9B-like windowed + global; gpt-oss-like vq8 with
 sinks), each measured the same way at the same --steps / --warmup, with its own
-roofline, end-to-end figure, clocks and oracle baseline.
+roofline, end-to-end figure, clocks and oracle baseline, and the 512-token
+prefill chunk per sequence on the headline's cache (query-tiled tcgen05
+kernel; roofline in TFLOP/s against the measured bf16 tensor peak; no oracle
+baseline).
 
 value       = algorithmic bytes of all timed steps / device time (CUDA events)
 e2e         = the same bytes / time of K x 64 calls of DecodeLayer.step, each with
@@ -50,7 +53,9 @@ DECODES_PER_STEP = {"llama31_8b_decode": 64, "llama31_8b_q8": 64, "llama31_8b_pa
                     "llama32_1b_tiny": 64}
 HEADLINE = "llama31_8b_decode"
 # the suite's other workloads, reported beside the headline in the same line
-PER_CONFIG = ("llama32_1b_tiny", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink")
+PER_CONFIG = ("llama32_1b_tiny", "qwen3_8b_ragged", "gemma2_9b_swa", "gptoss_vq8_sink", "llama31_8b_prefill")
+# the oracle takes tens of seconds per sequence of a 512-token chunk: no CPU baseline in per_config
+NO_CPU_IN_PER_CONFIG = ("llama31_8b_prefill",)
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 L2_BYTES = 129 * 2**20
 
@@ -639,7 +644,8 @@ def run_uaa(args, world, rank, local) -> dict | None:
     per = {}
     if name == HEADLINE and not args.no_per_config:
         for other in PER_CONFIG:
-            r = measure(other, args, world, rank, local, with_cpu, args.cpu_budget / 3)
+            r = measure(other, args, world, rank, local, with_cpu and other not in NO_CPU_IN_PER_CONFIG,
+                        args.cpu_budget / 3)
             if r is not None:
                 r.pop("dtype", None)
                 per[other] = r
