@@ -257,7 +257,10 @@ typedef struct {
 } uaa_workspace_layout;
 
 /* Step 1 (append). Writes the k/v rows at slot seq_lens[b], increments seq_lens,
- * and stores the rotated q rows in the workspace (and in args->q_rot if set). */
+ * and stores the rotated q rows in the workspace (and in args->q_rot if set).
+ * A bf16 key element is the exact normalised, rotated value rounded to nearest
+ * even: computed in fp32, and recomputed in fp64 where the fp32 result lies
+ * within its error bound of a bf16 rounding boundary. */
 uaa_status uaa_rope_qk_norm_append(const uaa_attn_desc* desc, const uaa_step_args* args,
                                    const uaa_workspace* ws, cudaStream_t stream);
 
@@ -284,7 +287,9 @@ uaa_status uaa_decode_attn_combine(const uaa_attn_desc* desc, const uaa_step_arg
  * loaded stage (and, once per kv head, into the cache), and the last CTA to
  * have read the lengths advances seq_lens. Results, cache rows and seq_lens are
  * those of uaa_rope_qk_norm_append followed by uaa_decode_attn_partial, up to
- * fp32 rounding order (appended key rows within one bf16 ulp, or one q8 code
+ * fp32 rounding order (bf16 key rows in the cache are the same bits; the step's
+ * own attention may use a new key element one bf16 ulp away where its exact
+ * rounding is recomputed after the attention; a q8 key code may differ by one
  * where the rotated key lies within fp32 rounding of a rounding tie). For fp32 caches,
  * and for steps of q_len > 1, it is those two launches. Follow it with
  * uaa_decode_attn_combine. */
