@@ -1,17 +1,25 @@
 // append.cu -- step 1 of the decode step: per-head QK RMSNorm, rotary embedding at
 // the absolute KV index, and the append of the new k / v rows to the cache.
+// q rows go to the workspace pre-multiplied by the partial kernel's logit
+// prescale, k rows and v rows go to slot seq_lens[b] + t of the cache for token
+// t. vq8 values (and q8 keys, after the rotation) are quantised in fp32 with IEEE
+// division and round-half-even, the storage rule of the vq8 cache (llamay "Models
+// and formats", "The KV cache, in three precisions"); bf16 keys are rounded as
+// their exact values (near a rounding boundary, recomputed in fp64).
 //
-// CTAs of 16 warps per group of tokens of each sequence (one token for a decode
-// step, up to 16 of a long chunk), as many as give every warp one of a token's
-// Hq + 2 Hkv head rows (a warp walking several rows is a chain of dependent
-// loads). A CTA first builds the cos / sin tables of its tokens' positions
-// (rope_cos_sin) while each warp loads its first head row; then each warp takes
-// whole rows, token after token, loading the next while it processes the current one: q
-// rows go to the workspace pre-multiplied by the partial kernel's logit
-// prescale, k rows and v rows go to slot seq_lens[b] + t of the cache for token t. vq8 values (and q8 keys, after the rotation) are quantised in fp32
-// with IEEE division and round-half-even, the storage rule of the vq8 cache
-// (llamay "Models and formats", "The KV cache, in three precisions").
+// Two kernels. One token per sequence (the separate append of fp32 caches, and
+// any step whose layout the other does not take): append_kernel, CTAs of 16
+// warps per group of tokens of a sequence, as many as give every warp one of a
+// token's Hq + 2 Hkv head rows (a warp walking several rows is a chain of
+// dependent loads); a CTA first builds the cos / sin tables of its tokens'
+// positions (rope_cos_sin) while each warp loads its first head row, then each
+// warp takes whole rows, loading the next while it processes the current one.
+// Several tokens per sequence (verify steps, prefill chunks): append_staged_kernel
+// (below), which streams each stage of tokens through shared memory.
+#include <algorithm>
+
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace uaa {
 namespace {
@@ -299,6 +307,533 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 2) append_kernel(const Appe
     }
 }
 
+// ---------------------------------------------------------------- chunks: staged rows
+// Several tokens per sequence (a verify step or a prefill chunk). The q, k and v
+// rows of consecutive tokens of one sequence are three contiguous blocks, so a
+// stage of tokens arrives in shared memory as three bulk async copies
+// (cp.async.bulk, two stages in flight per CTA), and every thread takes 16
+// elements of a head row at a time with 16-byte accesses: a pair-wise rotation
+// needs the row's two halves (NeoX) or adjacent elements (interleaved), which a
+// row in shared memory gives without shuffles. The rotation angles are reduced
+// in 64-bit integer arithmetic (rope_cos_sin_fx: the same remainder, rounded once
+// to fp32, as rope_cos_sin, with no fp64 instruction). Near-boundary key pairs go
+// to one queue per CTA and are recomputed in fp64 a pair per thread (the fp64
+// pipe runs a whole warp per instruction, so a queue per CTA makes far fewer
+// passes than a queue per warp). Measured on the 512-token prefill of the
+// Llama-3.1-like cache (ncu): 240 us for the row-per-warp kernel (about 32 KB of
+// loads in flight per SM, and a warp-wide fp64 pass per warp with a near pair),
+// 74 us staged.
+
+constexpr int kStagedThreads = 512;
+constexpr int kStagedNearCap = 128;            // queued pairs per CTA (flushed when half full)
+constexpr int kStagedInputBytes = 48 * 1024;   // input bytes of one stage, at most (one token at least)
+
+// A queued near-boundary key pair (key_pair_exact): the element index of its cache
+// row, its position and rotation pair, the two elements' indices in the row, their
+// raw values, and the row's fp64 norm factor (0: no norm).
+struct StagedNear {
+    size_t slot;
+    double inv64;
+    int pos;
+    short ia, ib, pp, pad;
+    float ra, rb;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Elements e .. e + 7 of a head row in shared memory, as fp32 (e a multiple of 8).
+template <typename T>
+__device__ __forceinline__ void load8(const uint8_t* row, int e, float (&x)[8])
+{
+    if constexpr (sizeof(T) == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(row + 4 * e);
+        const float4 c = *reinterpret_cast<const float4*>(row + 4 * e + 16);
+        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = c.x, x[5] = c.y, x[6] = c.z, x[7] = c.w;
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 2 * e);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float elem_at(const uint8_t* row, int e)
+{
+    if constexpr (sizeof(T) == 4)
+        return reinterpret_cast<const float*>(row)[e];
+    else
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(row)[e]) << 16);
+}
+
+__device__ __forceinline__ void store8_f32(float* dst, const float (&y)[8], float scale)
+{
+    reinterpret_cast<float4*>(dst)[0] = make_float4(y[0] * scale, y[1] * scale, y[2] * scale, y[3] * scale);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(y[4] * scale, y[5] * scale, y[6] * scale, y[7] * scale);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+
+__device__ __forceinline__ void store8_bf16(void* dst, const float (&y)[8])
+{
+    *reinterpret_cast<uint4*>(dst) =
+        make_uint4(bf16x2_bits(y[0], y[1]), bf16x2_bits(y[2], y[3]), bf16x2_bits(y[4], y[5]), bf16x2_bits(y[6], y[7]));
+}
+
+__device__ __forceinline__ void store8_codes(int8_t* dst, const float (&y)[8], float s)
+{
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(vq8_code(y[i], s))) << (8 * (i & 3));
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+}
+
+// Sum / maximum over the U lanes that hold one head row (aligned groups of U lanes).
+template <int U>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = U / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int U>
+__device__ __forceinline__ double group_sum64(double v)
+{
+#pragma unroll
+    for (int o = U / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int U>
+__device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int o = U / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// A queued pair recomputed in fp64 and written over the cache's fp32 rounding.
+__device__ __forceinline__ void fix_staged_pair(const AppendParams& p, const StagedNear& q, const double* freq)
+{
+    const double wa = p.qk_norm ? static_cast<double>(p.k_norm_w[q.ia]) + p.norm_offset : 1.0;
+    const double wb = p.qk_norm ? static_cast<double>(p.k_norm_w[q.ib]) + p.norm_offset : 1.0;
+    __nv_bfloat16 ha, hb;
+    key_pair_exact(q.ra, q.rb, wa, wb, q.inv64, rope_cos_sin64(q.pp, p.half_rot, q.pos, freq[q.pp], p.mscale64), ha,
+                   hb);
+    static_cast<__nv_bfloat16*>(p.k_cache)[q.slot + q.ia] = ha;
+    static_cast<__nv_bfloat16*>(p.k_cache)[q.slot + q.ib] = hb;
+}
+
+// A 4-byte asynchronous copy into shared memory (its completion: cp_async_wait_all
+// by the issuing thread, then a barrier for the others).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// theta'_p / pi modulo 2 (exact) as a multiple of 2^-63, rounded to nearest: the
+// angle pos * theta'_p / pi modulo 2 is then the low 64 bits of pos * g, read as a
+// signed multiple of 2^-63 (an error below pos * 2^-64).
+__device__ __forceinline__ unsigned long long angle_step(double inv_freq_over_pi)
+{
+    return __double2ull_rn(ldexp(fmod(inv_freq_over_pi, 2.0), 63));
+}
+
+// cos and sin of pos * theta'_p times mscale, as rope_cos_sin computes them: the
+// angle in units of pi reduced to [-1, 1) and rounded once to fp32 for sincospif.
+// Here the reduction is exact integer arithmetic (no fp64 instruction): the
+// product's low 64 bits are the angle modulo 2, and the conversion rounds it to
+// nearest.
+__device__ __forceinline__ float2 rope_cos_sin_fx(int pos, unsigned long long g, float mscale)
+{
+    const long long t = static_cast<long long>(static_cast<unsigned long long>(pos) * g);
+    float sn, cn;
+    sincospif(__ll2float_rn(t) * 0x1p-63f, &sn, &cn);
+    return make_float2(cn * mscale, sn * mscale);
+}
+
+// Shared memory of the staged kernel with tps tokens per stage.
+__host__ __device__ inline size_t staged_stage_bytes(int tps, int Hq, int Hkv, int D, int esz)
+{
+    return static_cast<size_t>(tps) * (Hq + 2 * Hkv) * D * esz;
+}
+
+__host__ __device__ inline size_t staged_smem_bytes(int tps, int Hq, int Hkv, int D, int esz)
+{
+    return 2 * staged_stage_bytes(tps, Hq, Hkv, D, esz) + static_cast<size_t>(tps) * (D / 2) * sizeof(float2) +
+           (D / 2) * (sizeof(double) + sizeof(unsigned long long)) + 2 * D * sizeof(float) +
+           kStagedNearCap * sizeof(StagedNear) + 2 * sizeof(uint64_t) + 8 * sizeof(int);
+}
+
+// Stages of tokens_per_cta tokens (the last of a sequence may hold fewer); CTA c
+// takes stages c, c + gridDim.x, ... Inputs 16-byte aligned; NeoX rotation with
+// half_rot a multiple of 8.
+template <int D, typename T>
+__global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const AppendParams p)
+{
+    constexpr int HALF = D / 2;
+    constexpr int U = D / 16;  // threads per head row, 16 elements each
+    constexpr int ESZ = sizeof(T);
+    extern __shared__ __align__(16) uint8_t sm[];
+    const int tid = threadIdx.x;
+    const int TPS = p.tokens_per_cta;
+    const int SPS = (p.q_len + TPS - 1) / TPS;  // stages per sequence
+    const int n_stages = p.B * SPS;
+    const uint32_t stage_bytes = static_cast<uint32_t>(staged_stage_bytes(TPS, p.Hq, p.Hkv, D, ESZ));
+    float2* cs = reinterpret_cast<float2*>(sm + 2 * stage_bytes);       // [TPS][HALF] the stage's (cos, sin)
+    double* freq = reinterpret_cast<double*>(cs + TPS * HALF);          // [HALF] theta'_p / pi
+    unsigned long long* fstep = reinterpret_cast<unsigned long long*>(freq + HALF);  // [HALF] angle_step
+    float* nw = reinterpret_cast<float*>(fstep + HALF);                 // [2][D] q / k norm weights + offset
+    StagedNear* nq = reinterpret_cast<StagedNear*>(nw + 2 * D);         // [kStagedNearCap]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(nq + kStagedNearCap);  // a full barrier per stage buffer
+    // [0] queued pairs, [1] last CTA, [2 + j] the length of the sequence of the stage in
+    // buffer j, [4] the next 32-item chunk of the stage to take
+    int* ctl = reinterpret_cast<int*>(bars + 2);
+    const uint32_t sm_u32 = ptx::smem_u32(sm);
+    const bool neox = p.style == UAA_ROPE_NEOX;
+
+    if (tid == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+        ctl[0] = 0;
+        ctl[4] = 0;
+        ptx::fence_barrier_init();
+    }
+    grid_dependency_wait();  // the step's inputs and the previous step's reads are complete
+    for (int i = tid; i < HALF; i += blockDim.x) {
+        const double f = p.inv_freq_over_pi[i];
+        freq[i] = f;
+        fstep[i] = angle_step(f);
+    }
+    if (p.qk_norm)
+        for (int i = tid; i < 2 * D; i += blockDim.x)
+            nw[i] = (i < D ? p.q_norm_w[i] : p.k_norm_w[i - D]) + p.norm_offset;
+
+    // thread 0 issues stage i of this CTA into buffer i & 1, and its sequence's length
+    // into ctl[2 + (i & 1)] (an async copy: the thread does not wait for it)
+    int issued = 0;
+    auto issue = [&](int i) {
+        const int st = blockIdx.x + i * gridDim.x;
+        if (st >= n_stages) return;
+        const int b = st / SPS, t0 = (st - b * SPS) * TPS, nt = min(TPS, p.q_len - t0);
+        const size_t tok = static_cast<size_t>(b) * p.q_len + t0;
+        const uint32_t qb = static_cast<uint32_t>(nt * p.Hq * D * ESZ), kb = static_cast<uint32_t>(nt * p.Hkv * D * ESZ);
+        const uint32_t dst = sm_u32 + (i & 1) * stage_bytes;
+        const uint32_t bar = ptx::smem_u32(&bars[i & 1]);
+        ptx::mbar_arrive_expect_tx(bar, qb + 2 * kb);
+        bulk_load(dst, static_cast<const T*>(p.q) + tok * p.Hq * D, qb, bar);
+        bulk_load(dst + qb, static_cast<const T*>(p.k_new) + tok * p.Hkv * D, kb, bar);
+        bulk_load(dst + qb + kb, static_cast<const T*>(p.v_new) + tok * p.Hkv * D, kb, bar);
+        cp_async_4(ptx::smem_u32(&ctl[2 + (i & 1)]), p.seq_lens + b);
+        ptx::cp_async_commit();
+        issued = i + 1;
+    };
+    if (tid == 0) {
+        issue(0);
+        issue(1);
+        ptx::cp_async_wait_all();  // the lengths of the first two stages
+    }
+    __syncthreads();
+
+    // r / H for head counts H > 1 as __umulhi(r, ceil(2^32 / H)): exact for r < 2^32 / H
+    // (here r < 16 H, so for H < 2^14)
+    const unsigned div_q = p.Hq > 1 ? 0xFFFFFFFFu / p.Hq + 1u : 0u;
+    const unsigned div_kv = p.Hkv > 1 ? 0xFFFFFFFFu / p.Hkv + 1u : 0u;
+    int failed_at = -1;
+    for (int i = 0;; ++i) {
+        const int st = blockIdx.x + i * gridDim.x;
+        if (st >= n_stages) break;
+        const int b = st / SPS, t0 = (st - b * SPS) * TPS, nt = min(TPS, p.q_len - t0);
+        // the stage's tokens take positions L + t0 .. ; a sequence whose tokens do not
+        // all fit the cache is not appended (its q rows rotate at position 0)
+        const int L = ctl[2 + (i & 1)];
+        const bool fits = L >= 0 && L + p.q_len <= p.cap;
+        if (tid == 0 && t0 == 0) {
+            if (!fits)
+                atomicOr(p.status, UAA_DEVFLAG_CAPACITY);
+            else if (L > p.max_len)
+                atomicOr(p.status, UAA_DEVFLAG_LEN_HINT);
+        }
+        for (int e = tid; e < nt * HALF; e += blockDim.x) {
+            const int t = e / HALF, pp = e - t * HALF;
+            cs[e] = pp < p.half_rot ? rope_cos_sin_fx(fits ? L + t0 + t : 0, fstep[pp], p.mscale) : make_float2(1.f, 0.f);
+        }
+        // one warp waits for the stage's copies; the others wait in the barrier
+        const bool landed =
+            tid >= 32 || ptx::mbar_wait(ptx::smem_u32(&bars[i & 1]), (i >> 1) & 1, kWaitLimitCycles);
+        if (!__syncthreads_and(landed)) {  // also: the table is complete
+            if (tid == 0) atomicOr(p.status, UAA_DEVFLAG_TIMEOUT);
+            failed_at = i;
+            break;
+        }
+
+        const uint8_t* sb = sm + (i & 1) * stage_bytes;
+        const int nq_rows = nt * p.Hq, nk_rows = nt * p.Hkv;
+        const int n_items = (nq_rows + 2 * nk_rows) * U;  // rows in buffer order: q, then k, then v
+        // warps take 32-item chunks from a counter: the chunks holding key items first
+        // (the near-boundary checks make them the longest), then the others in order
+        const int n_chunks = (n_items + 31) / 32;
+        const int kc0 = nq_rows * U / 32, kc1 = ((nq_rows + nk_rows) * U + 31) / 32;
+        for (;;) {
+            int wi = 0;
+            if ((tid & 31) == 0) wi = atomicAdd(&ctl[4], 1);
+            wi = __shfl_sync(0xffffffffu, wi, 0);
+            if (wi >= n_chunks) break;
+            const int chunk = wi < kc1 - kc0 ? kc0 + wi : (wi < kc1 ? wi - (kc1 - kc0) : wi);
+            const int it = 32 * chunk + (tid & 31);
+            const bool valid = it < n_items;
+            const int rr = valid ? it / U : 0, u = it & (U - 1);
+            const int kind = rr < nq_rows ? 0 : (rr < nq_rows + nk_rows ? 1 : 2);  // q, k, v
+            const int r = kind == 0 ? rr : (kind == 1 ? rr - nq_rows : rr - nq_rows - nk_rows);
+            const int H = kind == 0 ? p.Hq : p.Hkv;
+            const int tok = H == 1 ? r : static_cast<int>(__umulhi(static_cast<unsigned>(r), kind == 0 ? div_q : div_kv));
+            const int head = r - tok * H;
+            const int pos = fits ? L + t0 + tok : 0;
+            const uint8_t* row = sb + static_cast<size_t>(rr) * D * ESZ;
+
+            // this thread's 16 elements, as two runs of 8 at e0 and e1: a NeoX unit
+            // below half_rot pairs element e0 + j with e1 + j (rotation pair 8u + j);
+            // otherwise the 16 elements are contiguous (values, interleaved pairs
+            // (2pp, 2pp + 1), and NeoX pass-through elements past 2 half_rot)
+            const bool neox_rot = neox && kind < 2 && 8 * u < p.half_rot;
+            int e0, e1;
+            if (neox_rot) {
+                e0 = 8 * u;
+                e1 = e0 + p.half_rot;
+            } else if (neox && kind < 2) {
+                e0 = 2 * p.half_rot + 16 * (u - p.half_rot / 8);
+                e1 = e0 + 8;
+            } else {
+                e0 = 16 * u;
+                e1 = e0 + 8;
+            }
+            float x0[8], x1[8];
+            load8<T>(row, e0, x0);
+            load8<T>(row, e1, x1);
+
+            // RMSNorm over the head row (every lane takes part in the group sum)
+            const bool normed = p.qk_norm && kind < 2;
+            float inv = 1.f;
+            if (p.qk_norm) {
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss += x0[j] * x0[j];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss += x1[j] * x1[j];
+                ss = group_sum<U>(ss);
+                if (normed) {
+                    inv = rms_inv(ss, D, p.eps);
+                    const float* w = nw + kind * D;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        x0[j] = x0[j] * inv * w[e0 + j];
+                        x1[j] = x1[j] * inv * w[e1 + j];
+                    }
+                }
+            }
+
+            // rotation (pass-through elements stay exact)
+            const float2* cst = cs + tok * HALF;
+            if (kind < 2 && neox) {
+                if (neox_rot) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) rope_rotate(x0[j], x1[j], cst[8 * u + j]);
+                }
+            } else if (kind < 2) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (8 * u + j < p.half_rot) rope_rotate(x0[2 * j], x0[2 * j + 1], cst[8 * u + j]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (8 * u + 4 + j < p.half_rot) rope_rotate(x1[2 * j], x1[2 * j + 1], cst[8 * u + 4 + j]);
+            }
+
+            // the new token's cache row (k and v rows; -1: a paged table entry out of range)
+            long long crow = -1;
+            if (valid && kind > 0 && fits) {
+                crow = cache_row(p.pages, p.Hkv, p.cap, b, head, pos);
+                if (crow < 0 && u == 0) atomicOr(p.status, UAA_DEVFLAG_PAGE);
+            }
+            const bool stores = crow >= 0;
+
+            // row maximum for the int8 codes (q8 keys after the rotation, vq8 / q8 values)
+            const bool quant = kind == 1 ? p.kv_dtype == UAA_DTYPE_Q8
+                                         : kind == 2 && (p.kv_dtype == UAA_DTYPE_VQ8 || p.kv_dtype == UAA_DTYPE_Q8);
+            float amax = 0.f;
+            if (__any_sync(0xffffffffu, valid && quant)) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fmaxf(fabsf(x0[j]), fabsf(x1[j])));
+                amax = group_max<U>(amax);
+            }
+
+            if (valid && kind == 0) {
+                const size_t qrow = (static_cast<size_t>(b) * p.q_len + t0 + tok) * p.Hq + head;
+                float* qp = p.q_prime + qrow * D;
+                store8_f32(qp + e0, x0, p.qscale);
+                store8_f32(qp + e1, x1, p.qscale);
+                if (p.q_rot_out) {
+                    store8_f32(p.q_rot_out + qrow * D + e0, x0, 1.f);
+                    store8_f32(p.q_rot_out + qrow * D + e1, x1, 1.f);
+                }
+            } else if (stores) {
+                const size_t slot = static_cast<size_t>(crow) * D;
+                if (quant) {
+                    const float s = vq8_scale(amax);
+                    int8_t* codes = static_cast<int8_t*>(kind == 1 ? p.k_cache : p.v_cache) + slot;
+                    store8_codes(codes + e0, x0, s);
+                    store8_codes(codes + e1, x1, s);
+                    if (u == 0) (kind == 1 ? p.k_scale : p.v_scale)[crow] = s;
+                } else if (p.kv_dtype == UAA_DTYPE_F32) {
+                    float* c = static_cast<float*>(kind == 1 ? p.k_cache : p.v_cache) + slot;
+                    store8_f32(c + e0, x0, 1.f);
+                    store8_f32(c + e1, x1, 1.f);
+                } else {
+                    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(kind == 1 ? p.k_cache : p.v_cache) + slot;
+                    store8_bf16(c + e0, x0);
+                    store8_bf16(c + e1, x1);
+                }
+            }
+
+            // keys of a bf16 (or vq8) cache: rounded as their exact values. Pair j of the
+            // 8 this thread holds lies near a bf16 rounding boundary (bf16_near_boundary)
+            // when the error bound of its fp32 rotation (from the pre-rotation values,
+            // recomputed from the staged row) reaches one; an unrotated, unnormalised
+            // element is exact.
+            unsigned near = 0;
+            if (stores && kind == 1 && p.kv_dtype != UAA_DTYPE_F32 && p.kv_dtype != UAA_DTYPE_Q8) {
+                float a0[8], a1[8];
+                load8<T>(row, e0, a0);
+                load8<T>(row, e1, a1);
+                if (normed) {
+                    const float* w = nw + D;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        a0[j] = a0[j] * inv * w[e0 + j];
+                        a1[j] = a1[j] * inv * w[e1 + j];
+                    }
+                }
+                auto check = [&](float pa, float pc, float ya, float yc, int j, int pp, bool rot) {
+                    if (!rot && !normed) return;
+                    const float2 cj = rot ? cst[pp] : make_float2(1.f, 0.f);
+                    const float eb = key_error_bound(pa, pc, cj, normed);
+                    if (bf16_near_boundary(ya, eb) || bf16_near_boundary(yc, eb)) near |= 1u << j;
+                };
+                if (neox) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) check(a0[j], a1[j], x0[j], x1[j], j, 8 * u + j, neox_rot);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        check(a0[2 * j], a0[2 * j + 1], x0[2 * j], x0[2 * j + 1], j, 8 * u + j, 8 * u + j < p.half_rot);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        check(a1[2 * j], a1[2 * j + 1], x1[2 * j], x1[2 * j + 1], 4 + j, 8 * u + 4 + j,
+                              8 * u + 4 + j < p.half_rot);
+                }
+            }
+
+            // near pairs: the row's fp64 norm factor (a group sum), then one queue entry
+            // per pair (recomputed here when the queue is full)
+            double inv64 = 0.0;
+            if (p.qk_norm && __any_sync(0xffffffffu, near != 0u)) {
+                double ss = 0.0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const double ra = elem_at<T>(row, e0 + j), rb = elem_at<T>(row, e1 + j);
+                    ss = fma(ra, ra, ss);
+                    ss = fma(rb, rb, ss);
+                }
+                ss = group_sum64<U>(ss);
+                inv64 = 1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(p.eps));
+            }
+            if (near) {
+                const size_t slot = static_cast<size_t>(crow) * D;
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    if (!((near >> j) & 1u)) continue;
+                    StagedNear q;
+                    int ia, ib, pp;
+                    if (neox_rot) {
+                        ia = e0 + j, ib = e1 + j, pp = 8 * u + j;
+                    } else if (neox) {
+                        ia = e0 + j, ib = e1 + j, pp = HALF - 1;  // a pass-through pair (pp >= half_rot)
+                    } else {
+                        ia = (j < 4 ? e0 : e1) + 2 * (j & 3), ib = ia + 1, pp = 8 * u + j;
+                    }
+                    q.slot = slot;
+                    q.inv64 = inv64;
+                    q.pos = pos;
+                    q.ia = static_cast<short>(ia);
+                    q.ib = static_cast<short>(ib);
+                    q.pp = static_cast<short>(pp);
+                    q.pad = 0;
+                    q.ra = elem_at<T>(row, ia);
+                    q.rb = elem_at<T>(row, ib);
+                    const int at = atomicAdd(&ctl[0], 1);
+                    if (at < kStagedNearCap)
+                        nq[at] = q;
+                    else
+                        fix_staged_pair(p, q, freq);  // after this thread's own store of the row
+                }
+            }
+        }
+        if (tid == 0) ptx::cp_async_wait_all();  // the next stage's length, issued a stage ago
+        __syncthreads();  // the buffer and the table are consumed; queued pairs and the next length are visible
+        if (ctl[0] > kStagedNearCap / 2) {  // uniform: read after the barrier
+            const int n = min(ctl[0], kStagedNearCap);
+            for (int e = tid; e < n; e += blockDim.x) fix_staged_pair(p, nq[e], freq);
+            __syncthreads();
+            if (tid == 0) ctl[0] = 0;
+            __syncthreads();
+        }
+        if (tid == 0) {
+            ctl[4] = 0;  // no warp takes chunks until the next stage's barrier
+            issue(i + 2);
+        }
+    }
+    __syncthreads();
+    {
+        const int n = min(ctl[0], kStagedNearCap);
+        for (int e = tid; e < n; e += blockDim.x) fix_staged_pair(p, nq[e], freq);
+    }
+    if (tid == 0) {
+        // no copy into this CTA's shared memory may be in flight at its exit: the
+        // length copies, and (bounded) the stages issued after the last one consumed
+        ptx::cp_async_wait_all();
+        if (failed_at >= 0)
+            for (int j = failed_at; j < issued; ++j)
+                if (!ptx::mbar_wait(ptx::smem_u32(&bars[j & 1]), (j >> 1) & 1, kWaitLimitCycles)) break;
+    }
+    __syncthreads();
+    // every CTA counts in once its stages are done; the last one advances the lengths
+    if (tid == 0) {
+        __threadfence();
+        ctl[1] = atomicInc(p.status + 1, gridDim.x - 1) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!ctl[1]) return;
+    __threadfence();
+    for (int i = tid; i < p.B; i += blockDim.x) {
+        const int n = p.seq_lens[i];
+        if (n >= 0 && n + p.q_len <= p.cap) p.seq_lens[i] = n + p.q_len;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_dtype,
                                                            int64_t n_rows, int8_t* codes,
@@ -318,8 +853,65 @@ __global__ void __launch_bounds__(256) vq8_quantize_kernel(const void* v, int v_
 
 }  // namespace
 
+// The staged kernel for several tokens per sequence, when its layout conditions
+// hold; false: use the row-per-warp kernel.
+bool launch_staged(const AppendParams& p, cudaStream_t s, cudaError_t& err)
+{
+    auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    if (p.q_len < 2 || (p.style == UAA_ROPE_NEOX && p.half_rot % 8 != 0)) return false;
+    if (!a16(p.q) || !a16(p.k_new) || !a16(p.v_new) || !a16(p.k_cache) || !a16(p.v_cache) || !a16(p.q_prime) ||
+        !a16(p.q_rot_out))
+        return false;
+    int dev = 0, n_sm = 0, smem_optin = 0, smem_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+        return false;
+    const int esz = p.io_dtype == UAA_DTYPE_F32 ? 4 : 2;
+    const long long per_token = static_cast<long long>(p.Hq + 2 * p.Hkv) * p.D * esz;
+    // tokens per stage: a stage of at most kStagedInputBytes, and small steps spread
+    // over the SMs (about two stages per SM before a CTA takes several); among those,
+    // the largest whose items fill whole passes of the CTA's threads (a part-filled
+    // last pass leaves warps idle at the stage's barrier)
+    long long tps = kStagedInputBytes / per_token;
+    tps = std::min<long long>(tps, static_cast<long long>(p.B) * p.q_len / (2LL * std::max(n_sm, 1)));
+    tps = std::max<long long>(1, std::min<long long>({tps, 16, p.q_len}));
+    const long long items_per_token = static_cast<long long>(p.Hq + 2 * p.Hkv) * (p.D / 16);
+    for (long long t = tps; t >= 2; --t)
+        if (t * items_per_token % kStagedThreads == 0) {
+            tps = t;
+            break;
+        }
+    const size_t smem = staged_smem_bytes(static_cast<int>(tps), p.Hq, p.Hkv, p.D, esz);
+    if (smem > static_cast<size_t>(smem_optin)) return false;
+    AppendParams q = p;
+    q.tokens_per_cta = static_cast<int>(tps);
+    const long long n_stages = static_cast<long long>(p.B) * ((p.q_len + tps - 1) / tps);
+    const long long per_sm = std::max<long long>(1, std::min<long long>(2, smem_sm / static_cast<long long>(smem + 1024)));
+    const long long ctas = std::min<long long>(n_stages, per_sm * n_sm);
+    const dim3 grid(static_cast<unsigned>(ctas)), block(kStagedThreads);
+    const bool f32 = p.io_dtype == UAA_DTYPE_F32;
+#define UAA_STAGED_LAUNCH(DD)                                                                                          \
+    do {                                                                                                               \
+        auto* kern = f32 ? append_staged_kernel<DD, float> : append_staged_kernel<DD, __nv_bfloat16>;                 \
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));        \
+        if (err == cudaSuccess) err = launch_dependent(kern, grid, block, smem, s, q);                                 \
+    } while (0)
+    switch (p.D) {
+    case 64: UAA_STAGED_LAUNCH(64); break;
+    case 128: UAA_STAGED_LAUNCH(128); break;
+    case 256: UAA_STAGED_LAUNCH(256); break;
+    default: return false;
+    }
+#undef UAA_STAGED_LAUNCH
+    return true;
+}
+
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
+    cudaError_t staged_err = cudaSuccess;
+    if (launch_staged(p, s, staged_err)) return staged_err;
     const int parts = (p.Hq + 2 * p.Hkv + kAppendWarps - 1) / kAppendWarps;  // a warp per head row
     const int groups = (p.q_len + p.tokens_per_cta - 1) / p.tokens_per_cta;
     const long long ctas = static_cast<long long>(p.B) * groups * parts;
