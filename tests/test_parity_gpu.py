@@ -274,6 +274,16 @@ EDGE = [
     ("d64-vq8-norm-offset-local", "gemma3_12b_local_global",
      dict(batch=2, seq_len=600, head_dim=64, kv_dtype="vq8", layers=[dict(window=100, rope_theta=10000.0,
                                                                           rope_scaling="none")]), [599, 40]),
+    # chunks whose append takes the row-per-warp kernel (NeoX with rotary_dim / 2 not a
+    # multiple of 8): one token per CTA, and the token groups of a 1,280-token step;
+    # partial rotary in chunks on the staged append (NeoX with the QK norm, interleaved fp32)
+    ("chunk4-rotary36-row-append", "llama31_8b_decode", dict(batch=2, seq_len=500, q_len=4, rotary_dim=36),
+     [499, 60]),
+    ("chunk640-rotary36-grouped-append", "llama31_8b_decode", dict(batch=2, n_q_heads=8, n_kv_heads=2, seq_len=1400,
+                                                                   q_len=640, rotary_dim=36, steps=1), [700, 0]),
+    ("chunk4-rotary96-qknorm", "qwen3_8b_ragged", dict(batch=2, seq_len=300, q_len=4, rotary_dim=96), [296, 5]),
+    ("chunk3-rotary16-interleaved-f32", "llama32_1b_tiny", dict(batch=2, seq_len=300, q_len=3, rotary_dim=16),
+     [290, 5]),
 ]
 
 
@@ -294,10 +304,10 @@ def test_edge_cases(oracle_mod, spec, entry):
 def test_appended_keys_bit_exact_at_scale(oracle_mod, name, over, T):
     """The appended bf16 key rows equal the oracle's bits over ~1M key elements
     per case: about one element in 150 lies within the fp32 path's error bound of
-    a bf16 rounding boundary and is recomputed in fp64 (queued per warp in the
-    append kernel, after the last segment in the fused kernel), so the fp64 path
-    runs thousands of times here, with and without the QK norm and under YaRN's
-    cos / sin multiplier."""
+    a bf16 rounding boundary and is recomputed in fp64 (after the last segment in
+    the fused kernel, queued per CTA in the staged append of the 16-token step),
+    so the fp64 path runs thousands of times here, with and without the QK norm
+    and under YaRN's cos / sin multiplier."""
     cfg = W.layer_configs(W.config(name, steps=1, **over))[0]
     lens = [int(x) for x in np.random.default_rng(17).integers(0, 180, size=cfg["batch"])]
     case = host_case(cfg, lens=lens)
