@@ -32,6 +32,7 @@ cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import shutil
@@ -146,13 +147,18 @@ def decode_step_bytes(cfg: dict, lens_before: list[int]) -> int:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    """nvidia-smi samples (every 20 ms) of the SM clock and the throttle reasons,
+    each with its timestamp; mark_start / mark_end bracket the timed region, and
+    summary() reports the samples taken inside it (all samples when the region
+    was too short to hold one, with under_load = 0)."""
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, device_index: int):
         self.proc = None
         self.lines: list[str] = []
+        self.t0 = self.t1 = None
         exe = shutil.which("nvidia-smi")
         if not exe:
             return
@@ -164,13 +170,19 @@ class ClockSampler:
         except Exception:
             pass
         self.cmd = [exe, "-i", ident, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-                    "-lms", "50"]
+                    "-lms", "20"]
 
     def __enter__(self):
         if hasattr(self, "cmd"):
             self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             time.sleep(0.15)
         return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def __exit__(self, *exc):
         if self.proc:
@@ -184,24 +196,28 @@ class ClockSampler:
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []  # (time or None, sm MHz, max MHz, active reasons)
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < len(self.FIELDS):
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None
+            rows.append((ts, sm, mx, {nm for nm, val in zip(names, parts[5:9]) if val.lower().startswith("active")}))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "under_load": 0}
+        inside = [r for r in rows if self.t0 and self.t1 and r[0] and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": sorted(set().union(*(r[3] for r in use))), "samples": len(rows),
+                "under_load": len(inside)}
 
 
 # ---------------------------------------------------------------- distributed
@@ -413,11 +429,13 @@ def measure(name: str, args, world: int, rank: int, local: int, with_cpu: bool, 
         barrier(world)
         torch.cuda.synchronize()
         with ClockSampler(local) as clocks:
+            clocks.mark_start()
             evs[0].record(stream)
             for i in range(args.steps):
                 graph.replay()
                 evs[i + 1].record(stream)
             evs[-1].synchronize()
+            clocks.mark_end()
         torch.cuda.synchronize()
         barrier(world)
         dev_s = evs[0].elapsed_time(evs[-1]) / 1e3

@@ -84,3 +84,31 @@ def test_byte_accounting_for_q8_and_chunks():
     # the rows' windows, W + T - 1 keys, once
     win = dict(chunk, window=5)
     assert bench.partial_bytes(win, [13, 23]) == (8 + 8) * 2 * 512
+
+
+def test_clock_summary_uses_samples_inside_the_timed_region():
+    """The reported SM clock and throttle reasons come from the nvidia-smi
+    samples taken between mark_start and mark_end; without such a sample (a
+    region shorter than the sampling period) all samples count, and the line
+    says so with under_load = 0."""
+    import datetime
+
+    import bench
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    c.lines = []
+    for i in range(12):
+        t = base + datetime.timedelta(milliseconds=20 * i)
+        sm = 1980 if 3 <= i <= 8 else 2070                      # the loaded samples run slower
+        cap = "Active" if i == 5 else "Not Active"
+        c.lines.append(f"{t:%Y/%m/%d %H:%M:%S}.{t.microsecond // 1000:03d}, {sm}, 2070, 900.0, 0x4, "
+                       f"Not Active, Not Active, Not Active, {cap}")
+    c.lines.append("garbage line")
+    c.t0 = base + datetime.timedelta(milliseconds=55)
+    c.t1 = base + datetime.timedelta(milliseconds=170)
+    s = c.summary()
+    assert s == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 12,
+                 "under_load": 6}
+    c.t0 = c.t1 = None
+    s = c.summary()
+    assert s["under_load"] == 0 and s["samples"] == 12 and s["sm_mhz"] == 2025.0
